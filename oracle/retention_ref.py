@@ -1,0 +1,335 @@
+"""Float64 CPU oracle for RetNet multi-scale retention (MSR).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this module; only
+``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may use it.  It shares no code,
+constants or helpers with the CUDA path.
+
+Sources (web pages about RetNet; formulas partly garbled by extraction):
+
+* [P1] «从RoPE到Retention：一文拆解RetNet如何用'旋转'和'衰减'重塑序列建模»
+  (jsqmd.com news 854720): §2 (theta_shift / rotate_every_two, Q←Q⊙Θ,
+  K←K⊙Θ̄), §3 (decay D_nm), §4.1 parallel form, §4.2 recurrent form
+  S_n = γS_{n-1} + K_nᵀV_n, output Q_nS_n, §4.3 chunkwise form, §5 (GroupNorm,
+  division by √d, zero initial state of shape heads×d×d).
+* [P3] RetNet 保留网络 explainer (aiqz.cc article retnet-network):
+  "核心机制" (mask M_nj = γ^{n-j} for n ≥ j, 0 for n < j), "并行表征"
+  ((QKᵀ⊙M)V without softmax), "循环表征" (decay the state by γ, add the outer
+  product K_nᵀV_n, read with Q_n), "分块循环" (parallel inside a chunk, γ^b
+  carry between chunks, b=1 → recurrent, b=n → parallel), "Python 演示"
+  (parallel and recurrent agree to < 1e-8), "常见误区" (the factorisation
+  γ^{n-j} = γ^n·γ^{-j} turns the pairwise sum into a state recurrence).
+* [P5] «Transformer后繼有模！MSRA提出全新大模型基礎架構» (b99b.cn): GroupNorm
+  is used for its scale invariance; complex-valued position encoding.
+
+Readings taken where the pages are silent or garbled (each is listed again in
+the design doc):
+
+R1  rotate_every_two acts on interleaved pairs (2i, 2i+1) and maps
+    (a, b) → (−b, a); theta_shift(x) = x·cos + rotate_every_two(x)·sin with the
+    angle n·θ_i shared by both members of pair i.  So each pair is rotated
+    counter-clockwise by n·θ_i.
+R2  Q and K are both rotated by +n·θ at their own absolute position n.  The
+    real dot product then depends on the position difference only, which is
+    what the complex-conjugate pairing Θ / Θ̄ of [P1] §2 expresses.
+R3  Exactly one score scale d_k^{-1/2} is applied, folded into K′ ([P1] §5
+    "除以√d"; the `/ seq_len.sqrt()` of the [P1] §4.1 snippet is read as a
+    garbled √d).
+R4  state_in is the state *before* the first token (S_{-1}); its contribution
+    to token t decays by γ^{t+1}.
+R5  A decode step outputs q′·S_n with the *updated* state ([P1] §4.2
+    "Output = QₙSₙ"; [P3] "循环表征").
+R6  Masked entries (n < m) are exact zeros.
+R7  GroupNorm: one group per head over the d_v channels of one token,
+    biased variance, eps given by the caller (1e-5 default), optional affine.
+R8  A ragged last chunk of length r uses carry γ^r and ζ_j = γ^{r-1-j}.
+
+Conventions: q, k are [B, H, L, d_k]; v is [B, H, L, d_v]; gamma is [H];
+theta is [d_k/2]; states are [B, H, d_k, d_v]; absolute position of local
+index t is n = pos0 + t.  Every function computes in float64.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+__all__ = [
+    "rotate_every_two",
+    "theta_shift",
+    "rotation_tables",
+    "prologue",
+    "decay_mask",
+    "parallel_core",
+    "recurrent_core",
+    "chunkwise_core",
+    "state_closed_form",
+    "retention",
+    "decode_step",
+    "group_norm",
+    "brute_force",
+]
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Θ rotation prologue ([P1] §2; readings R1–R3)
+# --------------------------------------------------------------------------
+
+def rotate_every_two(x):
+    """(x_{2i}, x_{2i+1}) → (−x_{2i+1}, x_{2i}) on the last axis ([P1] §2, R1)."""
+    x = _f64(x)
+    out = np.empty_like(x)
+    out[..., 0::2] = -x[..., 1::2]
+    out[..., 1::2] = x[..., 0::2]
+    return out
+
+
+def rotation_tables(positions, theta):
+    """sin/cos of n·θ_i, each value repeated for both members of pair i.
+
+    positions: int array [L]; theta: [d/2].  Returns (sin, cos) of shape [L, d].
+    """
+    n = np.asarray(positions, dtype=np.float64)[:, None]
+    ang = n * _f64(theta)[None, :]
+    return np.repeat(np.sin(ang), 2, axis=-1), np.repeat(np.cos(ang), 2, axis=-1)
+
+
+def theta_shift(x, sin, cos):
+    """x·cos + rotate_every_two(x)·sin ([P1] §2)."""
+    x = _f64(x)
+    return x * cos + rotate_every_two(x) * sin
+
+
+def prologue(q, k, theta, pos0=0):
+    """q′ = Θ-rotated q; k′ = d_k^{-1/2}·Θ-rotated k (R2, R3)."""
+    q = _f64(q)
+    k = _f64(k)
+    L, d_k = q.shape[-2], q.shape[-1]
+    sin, cos = rotation_tables(np.arange(L) + int(pos0), theta)
+    qp = theta_shift(q, sin, cos)
+    kp = theta_shift(k, sin, cos) / math.sqrt(d_k)
+    return qp, kp
+
+
+# --------------------------------------------------------------------------
+# Core forms on already-rotated q′, k′ (per head; broadcast over B, H)
+# --------------------------------------------------------------------------
+
+def decay_mask(gamma, L):
+    """D_nm = γ^{n−m} for n ≥ m, exactly 0 otherwise ([P1] §3; [P3] 核心机制, R6)."""
+    n = np.arange(L)[:, None]
+    m = np.arange(L)[None, :]
+    diff = n - m
+    with np.errstate(divide="ignore", invalid="ignore"):
+        # γ^0 = 1 also for γ = 0; entries above the diagonal are set to 0.
+        d = np.where(diff >= 0, np.power(float(gamma), np.maximum(diff, 0).astype(np.float64)), 0.0)
+    return d
+
+
+def _heads(gamma, H):
+    g = _f64(gamma).reshape(-1)
+    if g.shape[0] != H:
+        raise ValueError("gamma must have one value per head")
+    return g
+
+
+def parallel_core(qp, kp, v, gamma, state_in=None):
+    """O = (Q′K′ᵀ ⊙ D)V + γ^{t+1} q′_t S_in, and S_out ([P1] §4.1; [P3] 并行表征, R4)."""
+    qp, kp, v = _f64(qp), _f64(kp), _f64(v)
+    B, H, L, _ = qp.shape
+    g = _heads(gamma, H)
+    out = np.zeros(v.shape[:-2] + (L, v.shape[-1]))
+    for h in range(H):
+        D = decay_mask(g[h], L)
+        scores = qp[:, h] @ np.swapaxes(kp[:, h], -1, -2)
+        out[:, h] = (scores * D) @ v[:, h]
+        if state_in is not None:
+            xi = np.power(g[h], np.arange(1, L + 1, dtype=np.float64))
+            out[:, h] += xi[None, :, None] * (qp[:, h] @ _f64(state_in)[:, h])
+    return out, state_closed_form(kp, v, gamma, state_in)
+
+
+def state_closed_form(kp, v, gamma, state_in=None):
+    """S_out = γ^L S_in + Σ_m γ^{L−1−m} k′_mᵀ v_m (the recurrence of [P1] §4.2 unrolled)."""
+    kp, v = _f64(kp), _f64(v)
+    B, H, L, d_k = kp.shape
+    g = _heads(gamma, H)
+    S = np.zeros((B, H, d_k, v.shape[-1]))
+    for h in range(H):
+        w = np.power(g[h], np.arange(L - 1, -1, -1, dtype=np.float64))
+        S[:, h] = np.swapaxes(kp[:, h] * w[None, :, None], -1, -2) @ v[:, h]
+        if state_in is not None:
+            S[:, h] += np.power(g[h], float(L)) * _f64(state_in)[:, h]
+    return S
+
+
+def recurrent_core(qp, kp, v, gamma, state_in=None):
+    """S_n = γS_{n−1} + k′_nᵀv_n ; o_n = q′_n S_n ([P1] §4.2; [P3] 循环表征, R5)."""
+    qp, kp, v = _f64(qp), _f64(kp), _f64(v)
+    B, H, L, d_k = qp.shape
+    d_v = v.shape[-1]
+    g = _heads(gamma, H)
+    S = np.zeros((B, H, d_k, d_v)) if state_in is None else _f64(state_in).copy()
+    out = np.zeros((B, H, L, d_v))
+    gb = g[None, :, None, None]
+    for t in range(L):
+        S = gb * S + kp[:, :, t, :, None] * v[:, :, t, None, :]
+        out[:, :, t] = np.einsum("bhk,bhkv->bhv", qp[:, :, t], S)
+    return out, S
+
+
+def chunkwise_core(qp, kp, v, gamma, state_in=None, chunk=None):
+    """Chunkwise recurrent form ([P1] §4.3; [P3] 分块循环; R8 for a ragged tail).
+
+    Within chunk i (local index j = 0..r−1, r ≤ chunk) and with S the state
+    at the end of chunk i−1:
+        o_j   = γ^{j+1} q′_j S + Σ_{m ≤ j} γ^{j−m} (q′_j·k′_m) v_m
+        S_new = γ^r S + Σ_j γ^{r−1−j} k′_jᵀ v_j
+    These follow from unrolling S_n = γS_{n−1} + k′_nᵀv_n over one chunk
+    (the γ^{n−j} = γ^n·γ^{−j} factorisation of [P3] 常见误区).
+    """
+    qp, kp, v = _f64(qp), _f64(kp), _f64(v)
+    B, H, L, d_k = qp.shape
+    d_v = v.shape[-1]
+    g = _heads(gamma, H)
+    if chunk is None:
+        chunk = L
+    if chunk < 1:
+        raise ValueError("chunk must be >= 1")
+    S = np.zeros((B, H, d_k, d_v)) if state_in is None else _f64(state_in).copy()
+    out = np.zeros((B, H, L, d_v))
+    for start in range(0, L, chunk):
+        r = min(chunk, L - start)
+        sl = slice(start, start + r)
+        for h in range(H):
+            gh = g[h]
+            xi = np.power(gh, np.arange(1, r + 1, dtype=np.float64))        # γ^{j+1}
+            zeta = np.power(gh, np.arange(r - 1, -1, -1, dtype=np.float64))  # γ^{r−1−j}
+            D = decay_mask(gh, r)
+            q_i, k_i, v_i = qp[:, h, sl], kp[:, h, sl], v[:, h, sl]
+            inner = ((q_i @ np.swapaxes(k_i, -1, -2)) * D) @ v_i
+            cross = xi[None, :, None] * (q_i @ S[:, h])
+            out[:, h, sl] = inner + cross
+            S[:, h] = np.power(gh, float(r)) * S[:, h] + np.swapaxes(k_i * zeta[None, :, None], -1, -2) @ v_i
+    return out, S
+
+
+# --------------------------------------------------------------------------
+# GroupNorm epilogue ([P1] §5; [P5]; reading R7)
+# --------------------------------------------------------------------------
+
+def group_norm(o, eps=1e-5, weight=None, bias=None):
+    """Normalise each (b, h, t) row over its d_v channels; optional affine of shape [H, d_v]."""
+    o = _f64(o)
+    mu = o.mean(axis=-1, keepdims=True)
+    var = ((o - mu) ** 2).mean(axis=-1, keepdims=True)
+    y = (o - mu) / np.sqrt(var + float(eps))
+    if weight is not None:
+        y = y * _f64(weight)[None, :, None, :]
+    if bias is not None:
+        y = y + _f64(bias)[None, :, None, :]
+    return y
+
+
+# --------------------------------------------------------------------------
+# Full operation and the decode step
+# --------------------------------------------------------------------------
+
+def retention(q, k, v, gamma, theta, pos0=0, state_in=None, form="chunkwise",
+              chunk=None, gn=None):
+    """Prologue + one of the three forms + optional GroupNorm.
+
+    Returns (out, state_out).  ``gn`` is None or a dict with keys eps, weight,
+    bias (weight/bias may be None).
+    """
+    qp, kp = prologue(q, k, theta, pos0)
+    if form == "parallel":
+        out, S = parallel_core(qp, kp, v, gamma, state_in)
+    elif form == "recurrent":
+        out, S = recurrent_core(qp, kp, v, gamma, state_in)
+    elif form == "chunkwise":
+        out, S = chunkwise_core(qp, kp, v, gamma, state_in, chunk)
+    else:
+        raise ValueError(form)
+    if gn is not None:
+        out = group_norm(out, gn.get("eps", 1e-5), gn.get("weight"), gn.get("bias"))
+    return out, S
+
+
+def decode_step(q, k, v, gamma, theta, pos, state, gn=None):
+    """One recurrent step at absolute position ``pos`` ([P1] §4.2, R5).
+
+    q, k: [B, H, d_k]; v: [B, H, d_v]; state: [B, H, d_k, d_v].
+    Returns (o [B, H, d_v], new_state).
+    """
+    q, k, v, state = _f64(q), _f64(k), _f64(v), _f64(state)
+    qp, kp = prologue(q[:, :, None, :], k[:, :, None, :], theta, pos)
+    qp, kp = qp[:, :, 0], kp[:, :, 0]
+    g = _heads(gamma, q.shape[1])[None, :, None, None]
+    S = g * state + kp[..., :, None] * v[..., None, :]
+    o = np.einsum("bhk,bhkv->bhv", qp, S)
+    if gn is not None:
+        o = group_norm(o[:, :, None, :], gn.get("eps", 1e-5), gn.get("weight"), gn.get("bias"))[:, :, 0]
+    return o, S
+
+
+# --------------------------------------------------------------------------
+# Brute force: the definition written out with scalar loops (tiny inputs)
+# --------------------------------------------------------------------------
+
+def brute_force(q, k, v, gamma, theta, pos0=0, state_in=None):
+    """Scalar-loop evaluation of out and state_out straight from the definitions.
+
+    Rotation uses math.cos / math.sin per pair; the output is the double sum
+    Σ_{m ≤ t} γ^{t−m} (q′_t·k′_m) v_m plus γ^{t+1} q′_t S_in, and the state is
+    γ^L S_in + Σ_m γ^{L−1−m} k′_mᵀ v_m.  Pure Python: tiny shapes only.
+    """
+    q = np.asarray(q, dtype=np.float64).tolist()
+    k = np.asarray(k, dtype=np.float64).tolist()
+    v = np.asarray(v, dtype=np.float64).tolist()
+    th = [float(t) for t in np.asarray(theta, dtype=np.float64)]
+    gam = [float(x) for x in np.asarray(gamma, dtype=np.float64)]
+    S_in = None if state_in is None else np.asarray(state_in, dtype=np.float64).tolist()
+    B, H, L, d_k = len(q), len(q[0]), len(q[0][0]), len(q[0][0][0])
+    d_v = len(v[0][0][0])
+    scale = 1.0 / math.sqrt(d_k)
+
+    def rot(x, n):
+        y = [0.0] * d_k
+        for i in range(d_k // 2):
+            c, s = math.cos(n * th[i]), math.sin(n * th[i])
+            a, b = x[2 * i], x[2 * i + 1]
+            y[2 * i] = a * c - b * s
+            y[2 * i + 1] = b * c + a * s
+        return y
+
+    out = [[[[0.0] * d_v for _ in range(L)] for _ in range(H)] for _ in range(B)]
+    st = [[[[0.0] * d_v for _ in range(d_k)] for _ in range(H)] for _ in range(B)]
+    for b in range(B):
+        for h in range(H):
+            g = gam[h]
+            qr = [rot(q[b][h][t], pos0 + t) for t in range(L)]
+            kr = [[scale * e for e in rot(k[b][h][t], pos0 + t)] for t in range(L)]
+            for t in range(L):
+                acc = [0.0] * d_v
+                for m in range(t + 1):
+                    w = (g ** (t - m)) * sum(qr[t][c] * kr[m][c] for c in range(d_k))
+                    for c in range(d_v):
+                        acc[c] += w * v[b][h][m][c]
+                if S_in is not None:
+                    gt = g ** (t + 1)
+                    for c in range(d_v):
+                        acc[c] += gt * sum(qr[t][kk] * S_in[b][h][kk][c] for kk in range(d_k))
+                out[b][h][t] = acc
+            for kk in range(d_k):
+                for c in range(d_v):
+                    s = 0.0 if S_in is None else (g ** L) * S_in[b][h][kk][c]
+                    for m in range(L):
+                        s += (g ** (L - 1 - m)) * kr[m][kk] * v[b][h][m][c]
+                    st[b][h][kk][c] = s
+    return np.array(out), np.array(st)

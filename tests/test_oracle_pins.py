@@ -1,0 +1,328 @@
+"""Pins of the float64 oracle against things other than itself.
+
+Each check ties the oracle to a passage of the RetNet pages, a closed form, a
+library routine or a brute-force evaluation; ``test_mutants_are_caught``
+plants plausible mistakes in the oracle's source and checks that at least
+one pin fails for every one of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import retention_ref as R
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(seed=0, B=2, H=2, L=7, d_k=4, d_v=3, state=True):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, H, L, d_k))
+    k = rng.standard_normal((B, H, L, d_k))
+    v = rng.standard_normal((B, H, L, d_v))
+    gamma = rng.uniform(0.3, 0.95, size=H)
+    theta = rng.uniform(0.1, 2.0, size=d_k // 2)
+    S = rng.standard_normal((B, H, d_k, d_v)) if state else None
+    return q, k, v, gamma, theta, S
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(a - b)) / max(1e-300, np.max(np.abs(b))))
+
+
+# ----------------------------------------------------------------------------
+# Pins, written as functions so that the mutation test can rerun them.
+# Each returns None on success and raises AssertionError on failure.
+# ----------------------------------------------------------------------------
+
+def pin_demo_parallel_equals_recurrent():
+    """RetNet 保留网络 explainer, 'Python 演示': parallel ≡ recurrent, err < 1e-8."""
+    cfg = json.load(open(os.path.join(GOLDEN, "demo_parallel_recurrent.json")))
+    rs = np.random.RandomState(cfg["seed"])
+    n, dim, g = cfg["n"], cfg["dim"], cfg["gamma"]
+    x = rs.randn(n, dim)
+    wq, wk, wv = rs.randn(dim, dim), rs.randn(dim, dim), rs.randn(dim, dim)
+    q, k, v = (x @ w for w in (wq, wk, wv))
+    op, _ = R.parallel_core(q[None, None], k[None, None], v[None, None], [g])
+    orr, _ = R.recurrent_core(q[None, None], k[None, None], v[None, None], [g])
+    assert np.abs(op - orr).max() < cfg["max_abs_err"]
+
+
+def pin_rotation_fixed_angles():
+    """«从RoPE到Retention…» §2 theta_shift at angles k·π/2, worked by hand."""
+    cases = json.load(open(os.path.join(GOLDEN, "rotation_cases.json")))["cases"]
+    for c in cases:
+        x = np.array(c["x"])[None, :]
+        sin, cos = R.rotation_tables([c["n"]], c["theta"])
+        y = R.theta_shift(x, sin, cos)[0]
+        assert np.allclose(y, c["expect"], atol=1e-12), (c, y)
+
+
+def pin_retention_hand_case():
+    """A two-token case worked by hand from the definitions (golden file)."""
+    c = json.load(open(os.path.join(GOLDEN, "rotation_cases.json")))["retention_cases"][0]
+    q = np.array(c["q"])[None, None]
+    k = np.array(c["k"])[None, None]
+    v = np.array(c["v"])[None, None]
+    for form, chunk in (("parallel", None), ("recurrent", None), ("chunkwise", 1), ("chunkwise", 2)):
+        o, S = R.retention(q, k, v, [c["gamma"]], c["theta"], c["pos0"], None, form, chunk)
+        assert np.allclose(o[0, 0], c["out"], atol=1e-12), (form, o)
+        assert np.allclose(S[0, 0], c["state"], atol=1e-12), (form, S)
+    o, S = R.brute_force(q, k, v, [c["gamma"]], c["theta"], c["pos0"])
+    assert np.allclose(o[0, 0], c["out"], atol=1e-12)
+    assert np.allclose(S[0, 0], c["state"], atol=1e-12)
+
+
+def pin_forms_match_brute_force():
+    """Parallel, recurrent and chunkwise (several b) equal the scalar double loop."""
+    for seed, pos0, state in ((0, 0, False), (1, 5, True), (2, 123, True)):
+        q, k, v, g, th, S = _rand_case(seed, state=state)
+        ob, Sb = R.brute_force(q, k, v, g, th, pos0, S)
+        for form, chunk in (("parallel", None), ("recurrent", None), ("chunkwise", 1),
+                            ("chunkwise", 2), ("chunkwise", 3), ("chunkwise", 7)):
+            o, Sx = R.retention(q, k, v, g, th, pos0, S, form, chunk)
+            assert _rel(o, ob) < 1e-12, (form, chunk, _rel(o, ob))
+            assert _rel(Sx, Sb) < 1e-12, (form, chunk, _rel(Sx, Sb))
+
+
+def pin_linear_attention_limit():
+    """γ = 1, θ = 0: causal linear attention, o_t = q_t·Σ_{m≤t} k_mᵀv_m/√d + q_t S_in (cumsum)."""
+    q, k, v, _, th, S = _rand_case(3, L=9)
+    H, d_k = q.shape[1], q.shape[-1]
+    kv = np.einsum("bhtk,bhtv->bhtkv", k, v) / math.sqrt(d_k)
+    cum = np.cumsum(kv, axis=2) + S[:, :, None]
+    expect = np.einsum("bhtk,bhtkv->bhtv", q, cum)
+    for form, chunk in (("parallel", None), ("recurrent", None), ("chunkwise", 4)):
+        o, Sx = R.retention(q, k, v, np.ones(H), np.zeros_like(th), 0, S, form, chunk)
+        assert _rel(o, expect) < 1e-12
+        assert _rel(Sx, cum[:, :, -1]) < 1e-12
+    o, _ = R.brute_force(q, k, v, np.ones(H), np.zeros_like(th), 0, S)
+    assert _rel(o, expect) < 1e-12
+
+
+def pin_gamma_zero():
+    """γ = 0: only the diagonal survives (0⁰ = 1): o_t = (q′_t·k′_t) v_t; S_out = k′_{L−1}ᵀ v_{L−1}."""
+    q, k, v, _, th, S = _rand_case(4, L=6)
+    H = q.shape[1]
+    qp, kp = R.prologue(q, k, th, 7)
+    expect = np.einsum("bhtk,bhtk->bht", qp, kp)[..., None] * v
+    exS = kp[:, :, -1, :, None] * v[:, :, -1, None, :]
+    for form, chunk in (("parallel", None), ("recurrent", None), ("chunkwise", 4)):
+        o, Sx = R.retention(q, k, v, np.zeros(H), th, 7, S, form, chunk)
+        assert _rel(o, expect) < 1e-12
+        assert _rel(Sx, exS) < 1e-12
+    o, Sb = R.brute_force(q, k, v, np.zeros(H), th, 7, S)
+    assert _rel(o, expect) < 1e-12 and _rel(Sb, exS) < 1e-12
+
+
+def pin_single_token():
+    """L = 1: o = (q′·k′)v + γ q′ S_in; S_out = γ S_in + k′ᵀv."""
+    q, k, v, g, th, S = _rand_case(5, L=1)
+    qp, kp = R.prologue(q, k, th, 11)
+    ex = (np.einsum("bhtk,bhtk->bht", qp, kp)[..., None] * v
+          + g[None, :, None, None] * np.einsum("bhtk,bhkv->bhtv", qp, S))
+    exS = g[None, :, None, None] * S + kp[:, :, 0, :, None] * v[:, :, 0, None, :]
+    for form in ("parallel", "recurrent", "chunkwise"):
+        o, Sx = R.retention(q, k, v, g, th, 11, S, form, 1)
+        assert _rel(o, ex) < 1e-12 and _rel(Sx, exS) < 1e-12
+
+
+def pin_theta_zero_is_identity():
+    q, k, *_ = _rand_case(6)
+    qp, kp = R.prologue(q, k, np.zeros(q.shape[-1] // 2), 99)
+    assert np.array_equal(qp, q)
+    assert np.allclose(kp, k / math.sqrt(q.shape[-1]), rtol=0, atol=1e-15)
+
+
+def pin_rotation_preserves_pair_norms():
+    q, _, _, _, th, _ = _rand_case(7)
+    sin, cos = R.rotation_tables(np.arange(q.shape[2]) + 1000, th)
+    y = R.theta_shift(q, sin, cos)
+    n0 = q[..., 0::2] ** 2 + q[..., 1::2] ** 2
+    n1 = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    assert np.allclose(n0, n1, rtol=1e-12, atol=0)
+
+
+def pin_position_shift_invariance():
+    """Only n − m matters (Θ on Q, Θ̄ on K ⇒ relative position): pos0 does not change O."""
+    q, k, v, g, th, _ = _rand_case(8)
+    o0, S0 = R.retention(q, k, v, g, th, 0, None, "chunkwise", 3)
+    o1, _ = R.retention(q, k, v, g, th, 41, None, "chunkwise", 3)
+    assert _rel(o1, o0) < 1e-11
+    ob, _ = R.brute_force(q, k, v, g, th, 41)
+    assert _rel(ob, o0) < 1e-11
+
+
+def pin_exact_causality():
+    """D_nm = 0 for n < m: outputs before m are bit-identical when later inputs change."""
+    q, k, v, g, th, S = _rand_case(9, L=12)
+    m = 5
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    rng = np.random.default_rng(99)
+    q2[:, :, m:] = rng.standard_normal(q2[:, :, m:].shape) * 100
+    k2[:, :, m:] = rng.standard_normal(k2[:, :, m:].shape) * 100
+    v2[:, :, m:] = rng.standard_normal(v2[:, :, m:].shape) * 100
+    for form, chunk in (("parallel", None), ("recurrent", None), ("chunkwise", 4), ("chunkwise", 5)):
+        o1, _ = R.retention(q, k, v, g, th, 3, S, form, chunk)
+        o2, _ = R.retention(q2, k2, v2, g, th, 3, S, form, chunk)
+        assert np.array_equal(o1[:, :, :m], o2[:, :, :m]), form
+        assert not np.array_equal(o1[:, :, m:], o2[:, :, m:])
+
+
+def pin_chunk_limits():
+    """b = 1 reduces to the recurrent form and b = L to the parallel form (分块循环)."""
+    q, k, v, g, th, S = _rand_case(10, L=10)
+    orec, Srec = R.retention(q, k, v, g, th, 2, S, "recurrent")
+    opar, Spar = R.retention(q, k, v, g, th, 2, S, "parallel")
+    o1, S1 = R.retention(q, k, v, g, th, 2, S, "chunkwise", 1)
+    oL, SL = R.retention(q, k, v, g, th, 2, S, "chunkwise", 10)
+    assert _rel(o1, orec) < 1e-12 and _rel(S1, Srec) < 1e-12
+    assert _rel(oL, opar) < 1e-12 and _rel(SL, Spar) < 1e-12
+
+
+def pin_split_call():
+    """One call over [0, L) equals two calls over halves with the state passed through."""
+    q, k, v, g, th, S = _rand_case(11, L=12)
+    o, Sx = R.retention(q, k, v, g, th, 4, S, "chunkwise", 3)
+    h = 6
+    oa, Sa = R.retention(q[:, :, :h], k[:, :, :h], v[:, :, :h], g, th, 4, S, "chunkwise", 3)
+    ob, Sb = R.retention(q[:, :, h:], k[:, :, h:], v[:, :, h:], g, th, 4 + h, Sa, "chunkwise", 3)
+    assert _rel(np.concatenate([oa, ob], axis=2), o) < 1e-12
+    assert _rel(Sb, Sx) < 1e-12
+
+
+def pin_ragged_tail():
+    q, k, v, g, th, S = _rand_case(12, L=11)
+    opar, Spar = R.retention(q, k, v, g, th, 0, S, "parallel")
+    for chunk in (2, 3, 4, 5, 6, 10):
+        o, Sx = R.retention(q, k, v, g, th, 0, S, "chunkwise", chunk)
+        assert _rel(o, opar) < 1e-12 and _rel(Sx, Spar) < 1e-12
+
+
+def pin_linearity():
+    q, k, v, g, th, S = _rand_case(13)
+    v2 = np.random.default_rng(1).standard_normal(v.shape)
+    S2 = np.random.default_rng(2).standard_normal(S.shape)
+    oa, Sa = R.retention(q, k, v, g, th, 0, S, "chunkwise", 3)
+    ob, Sb = R.retention(q, k, v2, g, th, 0, S2, "chunkwise", 3)
+    oc, Sc = R.retention(q, k, 2.0 * v - 3.0 * v2, g, th, 0, 2.0 * S - 3.0 * S2, "chunkwise", 3)
+    assert _rel(oc, 2.0 * oa - 3.0 * ob) < 1e-12
+    assert _rel(Sc, 2.0 * Sa - 3.0 * Sb) < 1e-12
+
+
+def pin_decode_steps_equal_recurrent():
+    q, k, v, g, th, S = _rand_case(14, L=8)
+    orec, Srec = R.retention(q, k, v, g, th, 20, S, "recurrent")
+    st = S.copy()
+    for t in range(q.shape[2]):
+        o, st = R.decode_step(q[:, :, t], k[:, :, t], v[:, :, t], g, th, 20 + t, st)
+        assert _rel(o, orec[:, :, t]) < 1e-12
+    assert _rel(st, Srec) < 1e-12
+
+
+def pin_groupnorm_matches_torch():
+    """Per-head GroupNorm equals torch.nn.functional.group_norm (float64, CPU)."""
+    rng = np.random.default_rng(15)
+    B, H, L, d_v = 2, 3, 5, 8
+    o = rng.standard_normal((B, H, L, d_v)) * 3 + 1
+    w = rng.standard_normal((H, d_v))
+    b = rng.standard_normal((H, d_v))
+    y = R.group_norm(o, 1e-5, w, b)
+    x = torch.from_numpy(o).permute(0, 2, 1, 3).reshape(B * L, H * d_v)
+    t = torch.nn.functional.group_norm(x, H, torch.from_numpy(w.reshape(-1)),
+                                       torch.from_numpy(b.reshape(-1)), eps=1e-5)
+    t = t.reshape(B, L, H, d_v).permute(0, 2, 1, 3).numpy()
+    assert _rel(y, t) < 1e-12
+    y0 = R.group_norm(o, 1e-5)
+    assert np.allclose(y0.mean(-1), 0, atol=1e-12)
+    assert np.allclose(y0.var(-1), 1, atol=1e-4)
+
+
+PINS = [
+    pin_demo_parallel_equals_recurrent, pin_rotation_fixed_angles, pin_retention_hand_case,
+    pin_forms_match_brute_force, pin_linear_attention_limit, pin_gamma_zero, pin_single_token,
+    pin_theta_zero_is_identity, pin_rotation_preserves_pair_norms, pin_position_shift_invariance,
+    pin_exact_causality, pin_chunk_limits, pin_split_call, pin_ragged_tail, pin_linearity,
+    pin_decode_steps_equal_recurrent, pin_groupnorm_matches_torch,
+]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin()
+
+
+# ----------------------------------------------------------------------------
+# Mutation test: every planted mistake must be caught by some pin.
+# (function, text in its source, replacement) — applied to a copy of the
+# oracle module's namespace, never to the file.
+# ----------------------------------------------------------------------------
+
+MUTANTS = {
+    "rotation_sign": ("rotate_every_two", "out[..., 0::2] = -x[..., 1::2]", "out[..., 0::2] = x[..., 1::2]"),
+    "rotation_halves": ("rotate_every_two",
+                        "out[..., 0::2] = -x[..., 1::2]\n    out[..., 1::2] = x[..., 0::2]",
+                        "h = x.shape[-1] // 2\n    out[..., :h] = -x[..., h:]\n    out[..., h:] = x[..., :h]"),
+    "k_conjugate_angle": ("prologue", "kp = theta_shift(k, sin, cos)", "kp = theta_shift(k, -sin, cos)"),
+    "no_scale": ("prologue", "/ math.sqrt(d_k)", ""),
+    "scale_seq_len": ("prologue", "/ math.sqrt(d_k)", "/ math.sqrt(L)"),
+    "mask_not_causal": ("decay_mask", "np.where(diff >= 0,", "np.where(diff >= -1,"),
+    "mask_exponent_off_by_one": ("decay_mask", "np.maximum(diff, 0)", "np.maximum(diff - 1, 0)"),
+    "parallel_state_decay": ("parallel_core", "np.arange(1, L + 1,", "np.arange(0, L,"),
+    "recurrent_old_state_output": ("recurrent_core",
+                                   "S = gb * S + kp[:, :, t, :, None] * v[:, :, t, None, :]\n        out[:, :, t] = np.einsum(\"bhk,bhkv->bhv\", qp[:, :, t], S)",
+                                   "out[:, :, t] = np.einsum(\"bhk,bhkv->bhv\", qp[:, :, t], S)\n        S = gb * S + kp[:, :, t, :, None] * v[:, :, t, None, :]"),
+    "chunk_xi": ("chunkwise_core", "np.arange(1, r + 1,", "np.arange(0, r,"),
+    "chunk_zeta_reversed": ("chunkwise_core", "np.arange(r - 1, -1, -1,", "np.arange(0, r,"),
+    "chunk_carry": ("chunkwise_core", "np.power(gh, float(r)) * S[:, h]", "np.power(gh, float(r - 1)) * S[:, h]"),
+    "chunk_transposed_kv": ("chunkwise_core", "np.swapaxes(k_i * zeta[None, :, None], -1, -2) @ v_i",
+                            "np.swapaxes(k_i[..., ::-1] * zeta[None, :, None], -1, -2) @ v_i"),
+    "state_closed_form_power": ("state_closed_form", "np.power(g[h], float(L))", "np.power(g[h], float(L - 1))"),
+    "gn_unbiased": ("group_norm", "((o - mu) ** 2).mean(axis=-1, keepdims=True)",
+                    "((o - mu) ** 2).sum(axis=-1, keepdims=True) / (o.shape[-1] - 1)"),
+    "gn_eps_outside": ("group_norm", "np.sqrt(var + float(eps))", "(np.sqrt(var) + float(eps))"),
+    "decode_no_decay": ("decode_step", "S = g * state +", "S = state +"),
+}
+
+
+def _make_mutant(name):
+    import inspect
+    import textwrap
+    import types
+
+    fn_name, old, new = MUTANTS[name]
+    src = textwrap.dedent(inspect.getsource(getattr(R, fn_name)))
+    assert old in src, f"mutant {name}: pattern not found in {fn_name}"
+    src = src.replace(old, new, 1)
+    mod = types.ModuleType("oracle_mutant")
+    mod.__dict__.update({k: v for k, v in R.__dict__.items() if not k.startswith("__")})
+    exec(compile(src, f"<mutant {name}>", "exec"), mod.__dict__)
+    # functions defined in the copy must see the mutated function
+    for k, v in list(mod.__dict__.items()):
+        if isinstance(v, types.FunctionType) and v.__module__ == R.__name__:
+            mod.__dict__[k] = types.FunctionType(v.__code__, mod.__dict__, v.__name__, v.__defaults__)
+    mod.__dict__[fn_name] = types.FunctionType(
+        mod.__dict__[fn_name].__code__, mod.__dict__, fn_name, mod.__dict__[fn_name].__defaults__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutants_are_caught(name, monkeypatch):
+    mod = _make_mutant(name)
+    global R
+    saved = R
+    R = mod
+    caught = []
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError, FloatingPointError, IndexError):
+                caught.append(pin.__name__)
+    finally:
+        R = saved
+    assert caught, f"mutant {name} was not caught by any pin"
