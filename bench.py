@@ -1,0 +1,390 @@
+#!/usr/bin/env python
+"""Benchmark of the retention hot path on B300; prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Timed step: one ret_chunkwise call on the 7B-shape workload (B2 H16 L8192
+d_k256 d_v512, chunk 128, bf16, fp32 state_in), inputs resident in HBM.
+The decode workload (batch 128, H16, d_k256, d_v512, fp32 state 1.07 GB) is
+timed the same way and reported under "decode".  N > 1 runs one independent
+replica per GPU (the path has no exchange step) and reports the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "chunkwise retention tokens/s & % bf16 tensor peak; decode state GB/s % HBM"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="msr7b")
+    ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------
+# Algorithmic work (per call), stated in the design doc
+# --------------------------------------------------------------------------
+def chunk_flops(w):
+    """2b·d_k + 2b·d_v + 4·d_k·d_v flop per token per head (QKᵀ, PV, Q·S, KᵀV)."""
+    b = w.chunk
+    return w.B * w.H * w.L * (2 * b * w.d_k + 2 * b * w.d_v + 4 * w.d_k * w.d_v)
+
+
+def chunk_bytes(w):
+    """Read Q, K, V once, write O once (bf16), read state_in and write state_out (fp32)."""
+    return w.B * w.H * w.L * (2 * w.d_k + 2 * w.d_v) * 2 + 2 * w.B * w.H * w.d_k * w.d_v * 4
+
+
+def decode_bytes(w):
+    """Read and write the fp32 state once, plus q, k, v in and o out (bf16)."""
+    return 2 * w.B * w.H * w.d_k * w.d_v * 4 + w.B * w.H * (2 * w.d_k + 2 * w.d_v) * 2
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in ("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "linear_recurrent_sequence_prologue_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_msr7b_traffic.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m1 = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    m2 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not m1 or not m2 or m1.group(1) != kernel_source_sha():
+        return None
+    return float(m2.group(1))
+
+
+# --------------------------------------------------------------------------
+# Clock sampling during the timed region (NVML reads only)
+# --------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev_index):
+        self.samples, self.reasons, self.ok = [], 0, False
+        self._stop = threading.Event()
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(dev_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            self.max_mhz = None
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                self.reasons |= int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
+            except Exception:
+                pass
+            time.sleep(0.005)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
+                "samples": len(self.samples)}
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the float64 oracle as it stands, on a bounded sample
+# --------------------------------------------------------------------------
+def cpu_baseline(w, inp, budget_s=12.0):
+    import numpy as np
+    from oracle import retention_ref as O
+    from linear_recurrent_sequence_prologue_b300.inputs import to_f64
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([d.get("num_threads", 1) for d in threadpool_info()] or [1])
+    except Exception:
+        cores = os.cpu_count()
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    done, t0 = 0, time.perf_counter()
+    for b, h in heads:
+        sl = lambda t: to_f64(t[b:b + 1, h:h + 1])
+        O.retention(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]),
+                    np.asarray(inp["gamma"], np.float64)[h:h + 1],
+                    np.asarray(inp["theta"], np.float64), 0,
+                    None if inp["state_in"] is None else sl(inp["state_in"]), "chunkwise", w.chunk)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    per_head = dt / done
+    value = (w.B * w.L) / (per_head * len(heads))
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {len(heads)} (b,h) heads of the {w.name} workload, float64 "
+                      f"chunkwise oracle, {dt:.1f} s; tokens/s scaled to all heads"}
+
+
+# --------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from linear_recurrent_sequence_prologue_b300.inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=0)
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w, inp, budget_s=2.0)
+        if i >= args.warmup:
+            vals.append(r["value"])
+    v = statistics.median(vals)
+    line = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "impl": "reference",
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d_k": w.d_k,
+                       "d_v": w.d_v, "chunk": w.chunk},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                             "sample": r["sample"] + " (per step)"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "vs_baseline": None}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from linear_recurrent_sequence_prologue_b300 import build
+    build.build()
+    import linear_recurrent_sequence_prologue_b300 as R
+    from linear_recurrent_sequence_prologue_b300 import _lib
+    from linear_recurrent_sequence_prologue_b300.inputs import (WORKLOADS, make_decode_inputs,
+                                                                make_inputs)
+    lib = R.load()
+    peaks, peak_kind = measured_peaks()
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=0)
+    q, k, v = inp["q"].to(dev), inp["k"].to(dev), inp["v"].to(dev)
+    s_in = inp["state_in"].to(dev) if inp["state_in"] is not None else None
+    out = torch.empty((w.B, w.H, w.L, w.d_v), dtype=torch.bfloat16, device=dev)
+    s_out = torch.empty((w.B, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
+    _, ws_bytes = R.plan("chunkwise", torch.bfloat16, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk,
+                         gamma=inp["gamma"])
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=w.chunk, state_in=s_in,
+                    out=out, gn=None, workspace=ws, return_state=False)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # per-launch events through the library's profiling hook
+    import ctypes as C
+    max_k = 8
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_k * args.steps)]
+    ev_handles = (C.c_void_p * len(evs))(*[C.c_void_p(e.cuda_event) if hasattr(e, "cuda_event") else None for e in evs])
+    # torch.cuda.Event creates the CUDA event lazily; record once to materialise
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    ev_handles = (C.c_void_p * len(evs))(*[C.c_void_p(e.cuda_event) for e in evs])
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    names = []
+    with sampler:
+        lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+        start.record(stream)
+        for _ in range(args.steps):
+            step()
+        end.record(stream)
+        n_k = lib.ret_profile_end()
+        torch.cuda.synchronize()
+    names = [lib.ret_profile_kernel(i).decode() for i in range(n_k)]
+    barrier()
+    ms = start.elapsed_time(end)
+    per_kernel = {}
+    for i, nm in enumerate(names):
+        per_kernel.setdefault(nm, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tok_per_step = w.B * w.L
+    value = world * tok_per_step * args.steps / (ms / 1e3)
+    flops = chunk_flops(w)
+    top = max(per_kernel, key=lambda n: sum(per_kernel[n]))
+    top_ms = statistics.mean(per_kernel[top])
+    achieved = flops / (top_ms / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = profiled_traffic(top)
+
+    # ---------------- decode workload ----------------
+    dw = WORKLOADS["decode"]
+    dsteps = max(args.decode_steps, 1)
+    pool = 16
+    dinp = make_decode_inputs(dw, seed=0, steps=pool, device=f"cuda:{local}")
+    dstate = dinp["state"]
+    dout = torch.empty((dw.B, dw.H, dw.d_v), dtype=torch.bfloat16, device=dev)
+
+    def dstep(t):
+        i = t % pool
+        R.step(dinp["q"][i], dinp["k"][i], dinp["v"][i], dinp["gamma"], dinp["theta"], t, dstate,
+               out=dout)
+
+    for t in range(max(3, args.warmup)):
+        dstep(t)
+    torch.cuda.synchronize()
+    ds, de = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dsampler = ClockSampler(local)
+    barrier()
+    with dsampler:
+        ds.record(stream)
+        for t in range(dsteps):
+            dstep(t)
+        de.record(stream)
+        torch.cuda.synchronize()
+    dms = ds.elapsed_time(de) / dsteps
+    dgbs = decode_bytes(dw) / (dms / 1e3) / 1e9
+    decode = {"metric": "decode state GB/s", "value": world * dgbs, "unit": "GB/s",
+              "ms_per_step": dms, "steps": dsteps,
+              "config": {"workload": "decode", "B": dw.B, "H": dw.H, "d_k": dw.d_k, "d_v": dw.d_v,
+                         "state_bytes": 4 * dw.B * dw.H * dw.d_k * dw.d_v,
+                         "l2": "state 1.07 GB > 126 MB L2 (no flush needed)"},
+              "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": dgbs / peaks["hbm_gbs"], "traffic": None,
+                           "peak_kind": peak_kind},
+              "clocks": dsampler.summary()}
+    del dinp, dstate
+
+    # ---------------- end to end through the API with host buffers ----------------
+    hq, hk, hv = inp["q"].pin_memory(), inp["k"].pin_memory(), inp["v"].pin_memory()
+    hs = inp["state_in"].pin_memory() if inp["state_in"] is not None else None
+    hout = torch.empty((w.B, w.H, w.L, w.d_v), dtype=torch.bfloat16).pin_memory()
+    hsout = torch.empty((w.B, w.H, w.d_k, w.d_v), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dq, dk, dv = hq.to(dev, non_blocking=True), hk.to(dev, non_blocking=True), hv.to(dev, non_blocking=True)
+        dsin = hs.to(dev, non_blocking=True) if hs is not None else None
+        o, so = R.chunkwise(dq, dk, dv, inp["gamma"], inp["theta"], chunk=w.chunk, state_in=dsin,
+                            workspace=ws)
+        hout.copy_(o, non_blocking=True)
+        hsout.copy_(so, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    es.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize()
+    ems = es.elapsed_time(ee) / args.e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hs,) if hs is not None else ()))
+    d2h = hout.numel() * hout.element_size() + hsout.numel() * hsout.element_size()
+    e2e = {"value": world * tok_per_step / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0, 1.28^2) q,k,v; state_in N(0, 1e-2))",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d_k": w.d_k,
+                       "d_v": w.d_v, "chunk": w.chunk, "state_in": True,
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs 537 MB > 126 MB L2 (no flush needed)"},
+            "roofline": {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                         "peak_kind": f"bf16_tflops burst ({peak_kind})",
+                         "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
+                         "algorithmic_flop_per_launch": flops,
+                         "algorithmic_bytes_per_launch": chunk_bytes(w),
+                         "launch_ms": top_ms},
+            "kernels_ms": {n: statistics.mean(t) for n, t in per_kernel.items()},
+            "gpu_launches": n_k + dsteps + 2 * 0,
+            "clocks": sampler.summary(),
+            "decode": decode,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

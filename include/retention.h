@@ -1,0 +1,198 @@
+/*
+ * retention.h — C ABI of libretention.so: RetNet multi-scale retention (MSR)
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The operation (per batch row b and head h, decay γ_h, rotation
+ * frequencies θ_i, absolute position n = pos0 + t of local index t):
+ *
+ *   q′_t = R(nθ) q_t,  k′_t = d_k^{-1/2} R(nθ) k_t          (Θ prologue)
+ *   o_t  = Σ_{m≤t} γ^{t−m} (q′_t·k′_m) v_m + γ^{t+1} q′_t S_in
+ *   S_out = γ^L S_in + Σ_m γ^{L−1−m} k′_mᵀ v_m
+ *   optional per-head GroupNorm of o_t over its d_v channels.
+ *
+ * R(φ) rotates every interleaved pair (x_{2i}, x_{2i+1}) counter-clockwise by
+ * φ_i = n·θ_i: theta_shift(x) = x·cos + rotate_every_two(x)·sin of
+ * «从RoPE到Retention：一文拆解RetNet如何用'旋转'和'衰减'重塑序列建模» §2
+ * (Q←Q⊙Θ, K←K⊙Θ̄; the real dot product of the two rotated vectors depends on
+ * n − m only).  The decay mask D_nm = γ^{n−m} (n ≥ m, else exactly 0) is §3 of
+ * that page; the parallel, recurrent and chunkwise-recurrent forms are its
+ * §4.1–§4.3 and the sections 并行表征 / 循环表征 / 分块循环 of the RetNet
+ * 保留网络 explainer (aiqz.cc); the 1/√d scale and GroupNorm are §5 of the
+ * first page.  The three forms compute the same result up to rounding.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Layout    q, k: [B, H, L, d_k]; v, out: [B, H, L, d_v]; states:
+ *           [B, H, d_k, d_v] fp32; all row-major and contiguous.
+ * Memory    q, k, v, out, state*, workspace, gn->weight, gn->bias are DEVICE
+ *           pointers owned by the caller.  gamma[H] and theta[d_k/2] are HOST
+ *           arrays, read during the call only.  The library allocates no
+ *           device memory in any call.
+ * Dtypes    RET_BF16 inputs run on the tensor cores (fp32 accumulate);
+ *           RET_F32 inputs run on fp32 FFMA kernels.  out may be bf16 or fp32.
+ * Sizes     1 ≤ H ≤ 128; d_k even, 2 ≤ d_k ≤ 512; 1 ≤ d_v ≤ 1024;
+ *           0 ≤ pos0 and pos0 + L ≤ 2^24 (positions are exact in fp32);
+ *           every pointer 16-byte aligned; 0 < γ_h ≤ 1; θ finite.
+ * Errors    Arguments are validated synchronously: RET_EINVAL (bad argument)
+ *           or RET_EUNSUPPORTED (valid but not implemented), no launch and no
+ *           side effect.  A CUDA launch error returns RET_ECUDA.  Kernels
+ *           never trap: a bounded wait that expires sets a device status word
+ *           that ret_sync_status() reports as RET_ETIMEOUT.
+ * Streams   Every call is asynchronous on `stream` (no host synchronisation).
+ * Aliasing  state_in == state_out is allowed; out must not alias the inputs.
+ */
+#ifndef RETENTION_H
+#define RETENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RET_ABI_VERSION 1
+
+typedef enum {
+  RET_OK = 0,
+  RET_EINVAL = 1,        /* an argument is out of range, NULL or misaligned   */
+  RET_EUNSUPPORTED = 2,  /* valid arguments outside the implemented domain     */
+  RET_ECUDA = 3,         /* a CUDA call or launch failed                       */
+  RET_ETIMEOUT = 4,      /* a kernel's bounded wait expired (see sync_status)  */
+  RET_EWORKSPACE = 5     /* workspace missing or smaller than required         */
+} ret_status;
+
+typedef enum { RET_F32 = 0, RET_BF16 = 1 } ret_dtype;
+
+/* Per-head GroupNorm epilogue («从RoPE到Retention…» §5; one group = one head's d_v
+ * channels of one token; biased variance).  weight/bias: DEVICE [H*d_v] fp32,
+ * NULL means 1 / 0.  Pass a NULL ret_gn* (or enabled = 0) to skip it. */
+typedef struct {
+  int enabled;
+  float eps;
+  const float* weight;
+  const float* bias;
+} ret_gn;
+
+/* Kernel path chosen for a call (reported by ret_*_plan). */
+typedef enum {
+  RET_PATH_TC = 1,     /* tcgen05 tensor-core kernels (bf16 inputs)       */
+  RET_PATH_SIMT = 2    /* fp32 FFMA kernels                               */
+} ret_path;
+
+/* ------------------------------------------------------------------------
+ * ret_chunkwise — chunkwise-recurrent form, carried-state layout.
+ * Chunks of `chunk` tokens are processed in order: inside a chunk the
+ * parallel form, across chunks the state S ← γ^b S + (ζ⊙K′)ᵀV with
+ * ζ_j = γ^{b−1−j}, and the cross-chunk output term γ^{j+1} q′_j S
+ * («从RoPE到Retention…» §4.3; RetNet 保留网络 explainer, 分块循环).
+ * state_in: NULL means S_in = 0.  state_out: NULL skips the final state.
+ * The per-chunk state is updated in fp32 as S_i = fmaf(γ^b, S_{i−1}, ΔS_i)
+ * with ΔS_i accumulated from zero; ret_chunkwise_scan uses the same order,
+ * so the two layouts return bit-identical state_out.
+ * workspace: DEVICE scratch of at least ret_chunkwise_plan(...)->bytes
+ * (NULL allowed when that is 0).  The required size depends on the path.
+ * ------------------------------------------------------------------------ */
+ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                         const float* gamma, const float* theta,
+                         int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                         const float* state_in, float* state_out,
+                         void* out, ret_dtype out_dt, const ret_gn* gn,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Path and workspace bytes ret_chunkwise would use for these arguments.
+ * gamma may be NULL (then the tensor-core path is assumed allowed). */
+ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                              int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
+                              int* path, size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * ret_chunkwise_scan — the same result as ret_chunkwise, computed in the
+ * parallel-then-scan layout: every chunk's ΔS_i from zero (all chunks in
+ * parallel), an fp32 scan S_i = fmaf(γ^b, S_{i−1}, ΔS_i) over chunks, then
+ * every chunk's outputs from its entering state (all chunks in parallel).
+ * Arguments as ret_chunkwise; the workspace holds one d_k×d_v fp32 state per
+ * (b, h, chunk).
+ * ------------------------------------------------------------------------ */
+ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                              const float* gamma, const float* theta,
+                              int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                              const float* state_in, float* state_out,
+                              void* out, ret_dtype out_dt, const ret_gn* gn,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                   int d_k, int d_v, int chunk, ret_dtype out_dt,
+                                   int gn_enabled, int* path, size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * ret_parallel — parallel form O = (Q′K′ᵀ ⊙ D) V + γ^{t+1} q′_t S_in
+ * («从RoPE到Retention…» §4.1; RetNet 保留网络 explainer, 并行表征).
+ * O(L²) work.  state_out (optional) is the closed-form final state.
+ * ------------------------------------------------------------------------ */
+ret_status ret_parallel(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                        const float* gamma, const float* theta,
+                        int B, int H, int L, int d_k, int d_v, int64_t pos0,
+                        const float* state_in, float* state_out,
+                        void* out, ret_dtype out_dt, const ret_gn* gn,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+ret_status ret_parallel_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                             int d_k, int d_v, ret_dtype out_dt, int gn_enabled,
+                             int state_out_wanted, int* path, size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * ret_step — one recurrent decode step at absolute position `pos`
+ * («从RoPE到Retention…» §4.2: S_n = γS_{n−1} + K_nᵀV_n, output Q_nS_n with
+ * the updated state).  q, k: [B, H, d_k]; v, out: [B, H, d_v];
+ * state: [B, H, d_k, d_v] fp32, updated in place.  No workspace.
+ * ------------------------------------------------------------------------ */
+ret_status ret_step(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                    const float* gamma, const float* theta,
+                    int B, int H, int d_k, int d_v, int64_t pos,
+                    float* state, void* out, ret_dtype out_dt, const ret_gn* gn,
+                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * ret_rotate — the Θ prologue alone: y_t = scale·R((pos0+t)θ) x_t for
+ * x, y: [B, H, L, d] («从RoPE到Retention…» §2 theta_shift).  Exposed for
+ * testing the prologue that the other calls fuse or run in front.
+ * ------------------------------------------------------------------------ */
+ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta,
+                      int B, int H, int L, int d, int64_t pos0, float scale,
+                      void* y, ret_dtype out_dt, cudaStream_t stream);
+
+/* Synchronise `stream`, then return and clear the device status word:
+ * RET_ETIMEOUT if a kernel's bounded wait expired since the last call,
+ * RET_ECUDA on a CUDA error, else RET_OK. */
+ret_status ret_sync_status(cudaStream_t stream);
+
+/* Launch a one-block kernel that waits on a barrier nothing will complete,
+ * with a wait budget of `budget_us` microseconds (1 … 2,000,000); it must
+ * give up, record RET_ETIMEOUT and exit.  Tests the failure path on a GPU
+ * without faulting it. */
+ret_status ret_selftest_timeout(int budget_us, cudaStream_t stream);
+
+/* Profiling hook.  ret_profile_begin arms it with `n_events` caller-created
+ * CUDA events; every later kernel launch of the library records events
+ * [2i] and [2i+1] on the call's stream just before and after its i-th
+ * launch (while 2i+1 < n_events).  ret_profile_end disarms it and returns the
+ * number of kernels recorded; ret_profile_kernel(i) names the i-th one.
+ * Process-wide and not thread-safe: for benchmarks. */
+ret_status ret_profile_begin(cudaEvent_t* events, int n_events);
+int ret_profile_end(void);
+const char* ret_profile_kernel(int i);
+
+/* Force every later call in this process onto one path (RET_PATH_SIMT) or
+ * back to automatic selection (0).  For cross-checks between paths. */
+ret_status ret_force_path(int path);
+
+const char* ret_status_string(ret_status s);
+int ret_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RETENTION_H */

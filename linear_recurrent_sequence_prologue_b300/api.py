@@ -1,0 +1,221 @@
+"""Python binding of libretention.so: torch tensors in, pointers out.
+
+Only argument marshalling happens here (dtype/shape checks, the per-call
+workspace from torch's caching allocator, the current CUDA stream).  Every
+step of the computation runs in the library's CUDA kernels.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import RET_BF16, RET_F32, RetGN, check, load
+
+_DT = {torch.float32: RET_F32, torch.bfloat16: RET_BF16}
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+    return _DT[t.dtype]
+
+
+def _host_f32(x, n: int, name: str):
+    a = np.ascontiguousarray(np.asarray(x.detach().cpu() if torch.is_tensor(x) else x,
+                                        dtype=np.float32).reshape(-1))
+    if a.shape[0] != n:
+        raise ValueError(f"{name} must have {n} values, got {a.shape[0]}")
+    return a, a.ctypes.data_as(C.POINTER(C.c_float))
+
+
+def _dev(t: Optional[torch.Tensor], name: str, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def _gn_struct(gn, H: int, d_v: int, device):
+    if not gn:
+        return None, []
+    keep = []
+    w = gn.get("weight") if isinstance(gn, dict) else None
+    b = gn.get("bias") if isinstance(gn, dict) else None
+    eps = float(gn.get("eps", 1e-5)) if isinstance(gn, dict) else 1e-5
+    for name, t in (("gn weight", w), ("gn bias", b)):
+        if t is not None:
+            _dev(t, name, torch.float32)
+            if t.numel() != H * d_v:
+                raise ValueError(f"{name} must have H*d_v values")
+            keep.append(t)
+    s = RetGN(1, eps, C.c_void_p(w.data_ptr()) if w is not None else None,
+              C.c_void_p(b.data_ptr()) if b is not None else None)
+    return C.byref(s), [s] + keep
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0, None
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace needs {nbytes} bytes")
+        return C.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size(), workspace
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return C.c_void_p(ws.data_ptr()), nbytes, ws
+
+
+def _check_seq(q, k, v):
+    if q.dim() != 4 or k.shape != q.shape or v.dim() != 4 or v.shape[:3] != q.shape[:3]:
+        raise ValueError("q, k: [B, H, L, d_k]; v: [B, H, L, d_v]")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    return q.shape[0], q.shape[1], q.shape[2], q.shape[3], v.shape[3]
+
+
+def plan(form: str, in_dtype, B, H, L, d_k, d_v, chunk=None, out_dtype=None, gn=False,
+         gamma=None, state_out=False):
+    """(path, workspace bytes) the library would use.  path: 1 = tcgen05, 2 = fp32."""
+    lib = load()
+    idt = _DT[in_dtype]
+    odt = _DT[out_dtype or in_dtype]
+    gp = None
+    if gamma is not None:
+        garr, gp = _host_f32(gamma, H, "gamma")
+    path, nbytes = C.c_int(0), C.c_size_t(0)
+    if form == "chunkwise":
+        st = lib.ret_chunkwise_plan(idt, gp, B, H, L, d_k, d_v, chunk, odt, int(bool(gn)),
+                                    C.byref(path), C.byref(nbytes))
+    elif form == "chunkwise_scan":
+        st = lib.ret_chunkwise_scan_plan(idt, gp, B, H, L, d_k, d_v, chunk, odt, int(bool(gn)),
+                                         C.byref(path), C.byref(nbytes))
+    elif form == "parallel":
+        st = lib.ret_parallel_plan(idt, gp, B, H, L, d_k, d_v, odt, int(bool(gn)),
+                                   int(bool(state_out)), C.byref(path), C.byref(nbytes))
+    else:
+        raise ValueError(form)
+    check(f"ret_{form}_plan", st)
+    return path.value, nbytes.value
+
+
+def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
+              return_state: bool = True, out=None, out_dtype=None, gn=None, workspace=None,
+              stream=None, layout: str = "carry"):
+    """Chunkwise retention.  Returns (out, state_out or None).
+
+    layout="carry" runs ret_chunkwise (state carried across chunks);
+    layout="scan" runs ret_chunkwise_scan (chunk-parallel then scan).
+    """
+    lib = load()
+    B, H, L, d_k, d_v = _check_seq(q, k, v)
+    idt = _dtype_code(q)
+    odtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, L, d_v), dtype=odtype, device=q.device)
+    odt = _dtype_code(out)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
+    st_in = _dev(state_in, "state_in", torch.float32, (B, H, d_k, d_v))
+    state_out = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device) if return_state else None
+    gns, keep = _gn_struct(gn, H, d_v, q.device)
+    _, nbytes = plan("chunkwise_scan" if layout == "scan" else "chunkwise", q.dtype, B, H, L, d_k,
+                     d_v, chunk, odtype, bool(gn), gamma=garr)
+    wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
+    fn = lib.ret_chunkwise_scan if layout == "scan" else lib.ret_chunkwise
+    st = fn(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, L, d_k, d_v, int(pos0),
+            int(chunk), st_in, _dev(state_out, "state_out"), _dev(out, "out"), odt, gns, wsp, wsn,
+            _stream(stream))
+    check(fn.__name__, st)
+    return out, state_out
+
+
+def parallel(q, k, v, gamma, theta, pos0: int = 0, state_in=None, return_state: bool = False,
+             out=None, out_dtype=None, gn=None, workspace=None, stream=None):
+    """Parallel-form retention.  Returns (out, state_out or None)."""
+    lib = load()
+    B, H, L, d_k, d_v = _check_seq(q, k, v)
+    idt = _dtype_code(q)
+    odtype = out_dtype or q.dtype
+    if out is None:
+        out = torch.empty((B, H, L, d_v), dtype=odtype, device=q.device)
+    odt = _dtype_code(out)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
+    st_in = _dev(state_in, "state_in", torch.float32, (B, H, d_k, d_v))
+    state_out = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device) if return_state else None
+    gns, keep = _gn_struct(gn, H, d_v, q.device)
+    _, nbytes = plan("parallel", q.dtype, B, H, L, d_k, d_v, None, odtype, bool(gn), gamma=garr,
+                     state_out=return_state)
+    wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
+    st = lib.ret_parallel(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, L, d_k, d_v,
+                          int(pos0), st_in, _dev(state_out, "state_out"), _dev(out, "out"), odt, gns,
+                          wsp, wsn, _stream(stream))
+    check("ret_parallel", st)
+    return out, state_out
+
+
+def step(q, k, v, gamma, theta, pos: int, state, out=None, out_dtype=None, gn=None, stream=None):
+    """One decode step; updates `state` [B, H, d_k, d_v] in place.  Returns out [B, H, d_v]."""
+    lib = load()
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[:2] != q.shape[:2]:
+        raise ValueError("q, k: [B, H, d_k]; v: [B, H, d_v]")
+    B, H, d_k = q.shape
+    d_v = v.shape[2]
+    idt = _dtype_code(q)
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=out_dtype or q.dtype, device=q.device)
+    odt = _dtype_code(out)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
+    gns, keep = _gn_struct(gn, H, d_v, q.device)
+    st = lib.ret_step(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, d_k, d_v, int(pos),
+                      _dev(state, "state", torch.float32, (B, H, d_k, d_v)), _dev(out, "out"), odt,
+                      gns, _stream(stream))
+    check("ret_step", st)
+    return out
+
+
+def rotate(x, theta, pos0: int = 0, scale: float = 1.0, out_dtype=None, stream=None):
+    """The Θ prologue alone: scale · R((pos0+t)θ) x for x [B, H, L, d]."""
+    lib = load()
+    B, H, L, d = x.shape
+    y = torch.empty_like(x, dtype=out_dtype or x.dtype)
+    tarr, tp = _host_f32(theta, d // 2, "theta")
+    st = lib.ret_rotate(_dev(x, "x"), _dtype_code(x), tp, B, H, L, d, int(pos0), float(scale),
+                        _dev(y, "y"), _dtype_code(y), _stream(stream))
+    check("ret_rotate", st)
+    return y
+
+
+def sync_status(stream=None) -> int:
+    """Synchronise and return (and clear) the device status word as a ret_status code."""
+    return load().ret_sync_status(_stream(stream))
+
+
+def selftest_timeout(budget_us: int, stream=None) -> None:
+    check("ret_selftest_timeout", load().ret_selftest_timeout(int(budget_us), _stream(stream)))
+
+
+def force_path(path: int) -> None:
+    """0 = automatic, 2 = fp32 kernels only (cross-checks)."""
+    check("ret_force_path", load().ret_force_path(int(path)))
+
+
+def status_string(code: int) -> str:
+    return load().ret_status_string(int(code)).decode()

@@ -1,0 +1,400 @@
+// Chunkwise retention on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Form («从RoPE到Retention…» §4.3; RetNet 保留网络 explainer 分块循环), per
+// (b, h) with chunk b = 128, local indices j, m in the chunk, S the fp32 state
+// entering the chunk, ζ_m = γ^{b−1−m}:
+//   o_j = γ^{j+1} q′_j S + Σ_{m≤j} γ^{j−m} (q′_j·k′_m) v_m
+//   S  ← fmaf(γ^b, S, ΔS),  ΔS = Σ_m (ζ_m k′_m)ᵀ v_m
+// Rewriting with K̂′_m = ζ_m k′_m (ζ folded into the prologue),
+// P̂ = Q′K̂′ᵀ masked to m ≤ j (plain causal mask, exact zeros), and
+// Ŝ = bf16(γ^b S):
+//   o_j = ω_j · (Q′Ŝ + P̂V)_j   with ω_j = γ^{j+1−b}
+// because ω_j·γ^b = γ^{j+1} and ω_j·ζ_m = γ^{j−m}.  So one fp32 accumulator
+// holds both output terms and the decay mask reduces to a per-row scale
+// applied at the store (γ^{b−1} ≥ 2^-60 keeps every factor in range; the host
+// routes other heads to the fp32 path).
+//
+// Each CTA owns one (b·h, 128-wide d_v tile) and walks the chunks in order.
+// Transposed products keep d_v on the 128 TMEM lanes:
+//   P̂   [j × m]      = Q′ · K̂′ᵀ          A = Q′ (smem, K-major), B = K̂′ (K-major)
+//   Õᵀ  [v × j]      = Ŝᵀ · Q′ᵀ          A = Ŝᵀ (TMEM, bf16),    B = Q′ (K-major)
+//   Õᵀ  [v × j]     += Vᵀ · P̂ᵀ           A = Vᵀ (MN-major),      B = P̂ (K-major)
+//   ΔSᵀ [v × k]      = Vᵀ · K̂′           A = Vᵀ (MN-major),      B = K̂′ (MN-major)
+// TMEM (512 columns): Õᵀ [0,128), P̂ [128,256), ΔSᵀ piece [256,384),
+// Ŝᵀ bf16 [384, 384 + d_k/2).  The fp32 master state Sᵀ lives in the
+// registers of the 16 drain warps (d_k/4 values per thread).
+#pragma once
+
+#include "common.cuh"
+#include "tc_primitives.cuh"
+
+namespace ret {
+namespace tcc {
+
+using namespace ret::tc;
+
+constexpr int CH = 128;               // chunk length = tile rows
+constexpr int VT = 128;               // d_v columns per CTA
+constexpr int NCW = 16;               // drain ("compute") warps
+constexpr int NWARPS = NCW + 2;       // + TMA producer + MMA issuer
+constexpr int NTHREADS = NWARPS * 32;
+
+enum Bar : int {
+  Q_FULL = 0, K_FULL_LO, K_FULL_HI, V_FULL,
+  Q_EMPTY, K_EMPTY_LO, K_EMPTY_HI, V_EMPTY,
+  P_FULL, P_FREE, DS_FULL, DS_FREE, O_FULL, O_FREE, S_INIT, MMA_DONE, NBAR_
+};
+
+template <int DK>
+struct Cfg {
+  static_assert(DK == 64 || DK == 128 || DK == 256, "d_k");
+  static constexpr int QBOX = DK / 64;            // 64-column boxes of Q′ / K̂′
+  static constexpr int NPIECE = DK > 128 ? 2 : 1; // ΔS pieces (N ≤ 128 each)
+  static constexpr int PN = DK / NPIECE;
+  static constexpr int LOBOX = PN / 64;           // K boxes of piece 0
+  static constexpr int SPT = DK / 4;              // state values per drain thread
+  static constexpr uint32_t BOX = CH * 64 * 2;    // 16 KB
+  static constexpr uint32_t Q_BYTES = CH * DK * 2;
+  static constexpr uint32_t V_BYTES = CH * VT * 2;
+  static constexpr uint32_t P_BYTES = CH * CH * 2;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + Q_BYTES;
+  static constexpr uint32_t OFF_P = OFF_V + V_BYTES;
+  static constexpr uint32_t OFF_OMEGA = OFF_P + P_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_OMEGA + CH * 4;
+  static constexpr uint32_t OFF_TPTR = OFF_BAR + NBAR_ * 8;
+  static constexpr uint32_t USED = OFF_TPTR + 16;
+  static constexpr uint32_t SMEM_BYTES = USED + 1024;   // slack for 1024-B alignment
+  static constexpr uint32_t T_O = 0, T_P = 128, T_DS = 256, T_SH = 384;
+};
+
+struct ChunkArgs {
+  const float* state_in;   // [BH][DK][d_v] or nullptr
+  float* state_out;        // or nullptr
+  void* out;               // [BH][L][d_v] bf16, or fp32 when out_f32
+  int out_f32;
+  int H, L, d_v, nchunks;
+};
+
+// ---------------------------------------------------------------------------
+// Front pass: Q′ = R(nθ)q and K̂′ = d_k^{-1/2}·ζ_{t mod b}·R(nθ)k in bf16.
+// Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by all
+// B·H heads of that row.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rotate_qk_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+    __nv_bfloat16* __restrict__ qo, __nv_bfloat16* __restrict__ ko, CallConsts cc, int BH,
+    int H, int L, int d, float pos0, int chunk) {
+  const int vecs = d / 8;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(L) * vecs) return;
+  const int t = static_cast<int>(idx / vecs), cidx = static_cast<int>(idx % vecs);
+  float c[4], s[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cidx + u], c[u], s[u]);
+  const float e = static_cast<float>(chunk - 1 - (t % chunk));
+  for (int bh = 0; bh < BH; ++bh) {
+    const int h = bh % H;
+    const float zk = cc.kscale * gpow(cc.lg2g[h], e);
+    const size_t off = (static_cast<size_t>(bh) * L + t) * d + 8 * cidx;
+    const uint4 qv = *reinterpret_cast<const uint4*>(q + off);
+    const uint4 kv = *reinterpret_cast<const uint4*>(k + off);
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
+    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
+    uint32_t qr[4], kr[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
+      qr[u] = pack_bf16x2(a * c[u] - b * s[u], fmaf(a, s[u], b * c[u]));
+      const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
+      const float cz = zk * c[u], sz = zk * s[u];
+      kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
+    }
+    *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
+    *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Main kernel.  grid = (d_v / 128, B·H); block = 576 threads; 1 CTA per SM.
+// ---------------------------------------------------------------------------
+template <int DK>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, ChunkArgs args, CallConsts cc) {
+  using C = Cfg<DK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
+  float* omega = reinterpret_cast<float*>(smem + C::OFF_OMEGA);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v0 = blockIdx.x * VT;
+  const int bh = blockIdx.y;
+  const int h = bh % args.H;
+  const int L = args.L, d_v = args.d_v, nch = args.nchunks;
+  const float gb = cc.gb[h];
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    const uint32_t counts[NBAR_] = {1, 1, 1, 1, 1, 1, 1, 1, 1, NCW, 1, NCW / C::NPIECE, 1, NCW, NCW, 1};
+    for (int i = 0; i < NBAR_; ++i) mbar_init(bar(i), counts[i]);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + C::OFF_TPTR, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x < CH) omega[threadIdx.x] = gpow(cc.lg2g[h], static_cast<float>(static_cast<int>(threadIdx.x) + 1 - CH));
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_TPTR);
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ---------------------------
+    if (lane == 0) {
+      int issued = -1;   // last chunk whose loads were all issued
+      for (int i = 0; i < nch; ++i) {
+        const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
+        const int y = bh * L + i * CH;
+        if (i > 0 && !mbar_wait(bar(K_EMPTY_LO), pp, 0x101)) break;
+        mbar_arrive_expect_tx(bar(K_FULL_LO), C::LOBOX * C::BOX);
+        for (int b = 0; b < C::LOBOX; ++b) tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL_LO));
+        if (i > 0 && !mbar_wait(bar(Q_EMPTY), pp, 0x102)) break;
+        mbar_arrive_expect_tx(bar(Q_FULL), C::Q_BYTES);
+        for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sQ + b * C::BOX, &tm_q, 64 * b, y, bar(Q_FULL));
+        if constexpr (C::NPIECE == 2) {
+          if (i > 0 && !mbar_wait(bar(K_EMPTY_HI), pp, 0x103)) break;
+          mbar_arrive_expect_tx(bar(K_FULL_HI), (C::QBOX - C::LOBOX) * C::BOX);
+          for (int b = C::LOBOX; b < C::QBOX; ++b)
+            tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL_HI));
+        }
+        if (i > 0 && !mbar_wait(bar(V_EMPTY), pp, 0x104)) break;
+        mbar_arrive_expect_tx(bar(V_FULL), C::V_BYTES);
+        for (int b = 0; b < 2; ++b) tma_load_2d(sV + b * C::BOX, &tm_v, v0 + 64 * b, y, bar(V_FULL));
+        issued = i;
+      }
+      // Never leave the CTA with bulk copies still landing in its shared
+      // memory: wait (bounded) until the last issued chunk has arrived.
+      if (issued >= 0 && status_aborted()) {
+        const uint32_t pl = static_cast<uint32_t>(issued) & 1u;
+        mbar_wait(bar(K_FULL_LO), pl, 0x1f1, kWaitBudgetCycles / 8);
+        mbar_wait(bar(Q_FULL), pl, 0x1f2, kWaitBudgetCycles / 8);
+        if (C::NPIECE == 2) mbar_wait(bar(K_FULL_HI), pl, 0x1f3, kWaitBudgetCycles / 8);
+        mbar_wait(bar(V_FULL), pl, 0x1f4, kWaitBudgetCycles / 8);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer -----------------------------
+    if (lane == 0) {
+      const uint32_t tO = tmem + C::T_O, tP = tmem + C::T_P, tDS = tmem + C::T_DS,
+                     tSH = tmem + C::T_SH;
+      constexpr uint32_t ID_P = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t ID_QS = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(128, 128, 1, 0);
+      constexpr uint32_t ID_KV = idesc_bf16_f32(128, C::PN, 1, 1);
+      auto kv_piece = [&](int p) {
+        for (int s = 0; s < CH / 16; ++s) {
+          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
+          const uint64_t b = sdesc_sw128(sK + (p * C::LOBOX) * C::BOX + s * 2048, C::BOX, 1024);
+          mma_ss(tDS, a, b, ID_KV, s > 0 ? 1u : 0u);
+        }
+      };
+      for (int i = 0; i < nch; ++i) {
+        const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+        // A: P̂ = Q′ K̂′ᵀ
+        if (!mbar_wait(bar(Q_FULL), pi, 0x201)) break;
+        if (!mbar_wait(bar(K_FULL_LO), pi, 0x202)) break;
+        tc_fence_after();
+        bool okhi = true;
+        for (int s = 0; s < DK / 16; ++s) {
+          if (C::NPIECE == 2 && s == (C::LOBOX * 4)) {
+            if (!mbar_wait(bar(K_FULL_HI), pi, 0x203)) { okhi = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
+          mma_ss(tP, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), ID_P,
+                 s > 0 ? 1u : 0u);
+        }
+        if (!okhi) break;
+        mma_commit(bar(P_FULL));
+        // C: Õᵀ = Ŝᵀ Q′ᵀ  (needs the previous chunk's state and a free Õ)
+        if (i == 0) {
+          if (!mbar_wait(bar(S_INIT), 0, 0x204)) break;
+        } else {
+          const uint32_t par = static_cast<uint32_t>(i * C::NPIECE - 1) & 1u;
+          if (!mbar_wait(bar(DS_FREE), par, 0x205)) break;
+          if (!mbar_wait(bar(O_FREE), static_cast<uint32_t>(i - 1) & 1u, 0x206)) break;
+        }
+        tc_fence_after();
+        for (int s = 0; s < DK / 16; ++s) {
+          const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
+          mma_ts(tO, tSH + s * 8, sdesc_sw128(sQ + off, 16, 1024), ID_QS, s > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(Q_EMPTY));
+        // B: ΔSᵀ piece 0 = Vᵀ K̂′[:, piece 0]
+        if (!mbar_wait(bar(V_FULL), pi, 0x207)) break;
+        tc_fence_after();
+        kv_piece(0);
+        mma_commit(bar(DS_FULL));
+        mma_commit(bar(K_EMPTY_LO));
+        // E: Õᵀ += Vᵀ P̂ᵀ  (needs the masked bf16 P̂ in shared memory)
+        if (!mbar_wait(bar(P_FREE), pi, 0x208)) break;
+        tc_fence_after();
+        for (int s = 0; s < CH / 16; ++s) {
+          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
+          const uint64_t b = sdesc_sw128(sP + (s >> 2) * C::BOX + (s & 3) * 32, 16, 1024);
+          mma_ss(tO, a, b, ID_PV, 1u);
+        }
+        mma_commit(bar(O_FULL));
+        // D: ΔSᵀ piece 1
+        if constexpr (C::NPIECE == 2) {
+          if (!mbar_wait(bar(DS_FREE), static_cast<uint32_t>(2 * i) & 1u, 0x209)) break;
+          tc_fence_after();
+          kv_piece(1);
+          mma_commit(bar(DS_FULL));
+          mma_commit(bar(K_EMPTY_HI));
+        }
+        mma_commit(bar(V_EMPTY));
+      }
+      // All issued MMAs must finish before TMEM is released.
+      mma_commit(bar(MMA_DONE));
+      mbar_wait(bar(MMA_DONE), 0, 0x2ff);
+    }
+  } else {
+    // ------------------------------ drain warps ----------------------------
+    const int w = warp - 2;                 // 0..15
+    const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+    const int cs = w >> 2;                  // 32-column slice for P̂ / Õ drains
+    const int kr = w >> 2;                  // state k range [kr*SPT, kr*SPT+SPT)
+    const int piece = (kr * C::SPT) / C::PN;
+    const int vl = 32 * quarter + lane;     // local v (TMEM lane) for Õ / ΔS / Ŝ
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+    const size_t sbase = static_cast<size_t>(bh) * DK * d_v + v0 + vl;
+
+    float S[C::SPT];
+#pragma unroll
+    for (int u = 0; u < C::SPT; ++u)
+      S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
+
+    auto write_shat = [&]() {
+#pragma unroll
+      for (int c = 0; c < C::SPT / 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pk[u] = pack_bf16x2(gb * S[c * 8 + 2 * u], gb * S[c * 8 + 2 * u + 1]);
+        tmem_st4(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 8) / 2, pk);
+      }
+      tmem_st_wait();
+    };
+    write_shat();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(S_INIT));
+
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+      const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+      // ---- P̂ drain: causal mask, bf16, into the K-major swizzled tile ----
+      if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const int j = vl;   // row of P̂ = TMEM lane
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t r[8];
+          tmem_ld8(tmem + C::T_P + lane_off + 32 * cs + 8 * g, r);
+          tmem_ld_wait();
+          uint32_t pk[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int m = 32 * cs + 8 * g + 2 * u;
+            const float a = (m <= j) ? __uint_as_float(r[2 * u]) : 0.f;
+            const float b = (m + 1 <= j) ? __uint_as_float(r[2 * u + 1]) : 0.f;
+            pk[u] = pack_bf16x2(a, b);
+          }
+          const int m0 = 32 * cs + 8 * g;
+          st_shared_v4(sP + (m0 >> 6) * C::BOX + sw128_offset(j, m0 & 63), pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FREE));
+
+      auto drain_ds = [&](int p) -> bool {
+        if (!mbar_wait(bar(DS_FULL), static_cast<uint32_t>(i * C::NPIECE + p) & 1u, 0x302)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < C::SPT / 8; ++c) {
+          uint32_t d[8];
+          tmem_ld8(tmem + C::T_DS + lane_off + (kr * C::SPT - p * C::PN) + c * 8, d);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) S[c * 8 + u] = fmaf(gb, S[c * 8 + u], __uint_as_float(d[u]));
+        }
+        write_shat();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(DS_FREE));
+        return true;
+      };
+      if (piece == 0 && !drain_ds(0)) { ok = false; break; }
+
+      // ---- Õ drain: ω_j scale, store ----
+      if (!mbar_wait(bar(O_FULL), pi, 0x303)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const size_t orow = static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          uint32_t r[8];
+          tmem_ld8(tmem + C::T_O + lane_off + 32 * cs + 8 * g, r);
+          tmem_ld_wait();
+          const size_t base = (orow + 8 * g) * d_v + v0 + vl;
+          if (args.out_f32) {
+            float* o = reinterpret_cast<float*>(args.out) + base;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 8 * g + c] * __uint_as_float(r[c]);
+          } else {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + base;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              o[static_cast<size_t>(c) * d_v] =
+                  __float2bfloat16_rn(omega[32 * cs + 8 * g + c] * __uint_as_float(r[c]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(O_FREE));
+
+      if (C::NPIECE == 2 && piece == 1 && !drain_ds(1)) { ok = false; break; }
+    }
+    if (ok && args.state_out) {
+#pragma unroll
+      for (int u = 0; u < C::SPT; ++u)
+        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] = S[u];
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace tcc
+}  // namespace ret

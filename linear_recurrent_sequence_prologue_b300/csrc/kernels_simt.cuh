@@ -1,0 +1,434 @@
+// fp32 FFMA kernels: the Θ prologue, the chunk-parallel layout of the
+// chunkwise form (per-chunk ΔS, state scan, per-chunk outputs), GroupNorm,
+// and the recurrent decode step.
+//
+// Chunkwise form («从RoPE到Retention…» §4.3; RetNet 保留网络 explainer 分块循环)
+// with S the state entering chunk i and j, m local indices in the chunk:
+//   o_j   = γ^{j+1} q′_j S + Σ_{m≤j} γ^{j−m} (q′_j·k′_m) v_m
+//   ΔS_i  = Σ_j γ^{r−1−j} k′_jᵀ v_j        (r = chunk length)
+//   S_i   = fmaf(γ^r, S_{i−1}, ΔS_i)
+// The parallel form (§4.1) is the same kernel with one chunk of length L.
+#pragma once
+
+#include "common.cuh"
+
+namespace ret {
+namespace simt {
+
+// ---------------------------------------------------------------------------
+// Θ prologue: y[bh, t, :] = scale · R((pos0 + t)θ) x[bh, t, :]   (§2 theta_shift)
+// Block (32, 8): x → pair index, y → row.  Angles depend on (t, i) only, so
+// each thread loops over all BH heads with one sincos.
+// ---------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
+                                                     Tout* __restrict__ y, CallConsts cc,
+                                                     int BH, int L, int d, float pos0,
+                                                     float scale) {
+  const int i = blockIdx.x * 32 + threadIdx.x;   // pair
+  const int t = blockIdx.y * 8 + threadIdx.y;    // row
+  if (i >= d / 2 || t >= L) return;
+  float c, s;
+  angle_cs(pos0 + static_cast<float>(t), cc.theta[i], c, s);
+  c *= scale;
+  s *= scale;
+  for (int bh = 0; bh < BH; ++bh) {
+    const size_t off = (static_cast<size_t>(bh) * L + t) * d + 2 * i;
+    const float a = to_f32(x[off]);
+    const float b = to_f32(x[off + 1]);
+    y[off] = from_f32<Tout>(a * c - b * s);
+    y[off + 1] = from_f32<Tout>(fmaf(a, s, b * c));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// ΔS_i[k][v] = Σ_j (γ^{r−1−j} k′_j[k]) v_j[v], accumulated in j order from 0.
+// Block 16×16 threads, 64 k × 64 v tile, 4×4 outputs per thread.
+// grid = (ceil(d_v/64), ceil(d_k/64), BH·nchunks); kp = rotated K′ (fp32).
+// out: ws[bh][chunk][k][v].
+// ---------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(256) chunk_dS_kernel(const float* __restrict__ kp,
+                                                       const Tin* __restrict__ v,
+                                                       float* __restrict__ ws, CallConsts cc,
+                                                       int H, int L, int d_k, int d_v, int chunk,
+                                                       int nchunks) {
+  __shared__ float sk[16][64];
+  __shared__ float sv[16][64];
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const int tid = ty * 16 + tx;
+  const int v0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
+  const int bh = blockIdx.z / nchunks, ci = blockIdx.z % nchunks;
+  const int h = bh % H;
+  const int start = ci * chunk;
+  const int r = min(chunk, L - start);
+  const float lg2 = cc.lg2g[h];
+  float acc[4][4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+
+  for (int j0 = 0; j0 < r; j0 += 16) {
+    for (int e = tid; e < 16 * 64; e += 256) {
+      const int jj = e / 64, cc2 = e % 64;
+      const int j = j0 + jj;
+      float kv = 0.f, vv = 0.f;
+      if (j < r) {
+        const size_t row = static_cast<size_t>(bh) * L + start + j;
+        if (k0 + cc2 < d_k) kv = gpow(lg2, static_cast<float>(r - 1 - j)) * kp[row * d_k + k0 + cc2];
+        if (v0 + cc2 < d_v) vv = to_f32(v[row * d_v + v0 + cc2]);
+      }
+      sk[jj][cc2] = kv;
+      sv[jj][cc2] = vv;
+    }
+    __syncthreads();
+    const int jn = min(16, r - j0);
+    for (int jj = 0; jj < jn; ++jj) {
+      float a[4], b[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        a[u] = sk[jj][ty + 16 * u];
+        b[u] = sv[jj][tx + 16 * u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[u][w] = fmaf(a[u], b[w], acc[u][w]);
+    }
+    __syncthreads();
+  }
+  float* dst = ws + (static_cast<size_t>(bh) * nchunks + ci) * d_k * d_v;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int kk = k0 + ty + 16 * u;
+    if (kk >= d_k) continue;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int vv = v0 + tx + 16 * w;
+      if (vv < d_v) dst[static_cast<size_t>(kk) * d_v + vv] = acc[u][w];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Inter-chunk scan over ws[bh][i][k][v] (holding ΔS_i on entry): writes the
+// state entering chunk i into slot i and the final state to state_out.
+// S_i = fmaf(g, S_{i−1}, ΔS_i) with g = γ^chunk (γ^tail for a ragged last
+// chunk), both rounded from double on the host.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) state_scan_kernel(float* __restrict__ ws,
+                                                         const float* __restrict__ state_in,
+                                                         float* __restrict__ state_out,
+                                                         CallConsts cc,
+                                                         int H, int d_k, int d_v, int nchunks,
+                                                         int BH) {
+  const size_t per = static_cast<size_t>(d_k) * d_v;
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= per * BH) return;
+  const size_t bh = idx / per, e = idx % per;
+  const int h = static_cast<int>(bh % H);
+  float S = state_in ? state_in[idx] : 0.f;
+  float* p = ws + bh * nchunks * per + e;
+  for (int i = 0; i < nchunks; ++i) {
+    const float d = p[static_cast<size_t>(i) * per];
+    p[static_cast<size_t>(i) * per] = S;
+    const float g = (i == nchunks - 1) ? cc.gtail[h] : cc.gb[h];
+    S = fmaf(g, S, d);
+  }
+  if (state_out) state_out[idx] = S;
+}
+
+// ---------------------------------------------------------------------------
+// Per-chunk outputs: o_j = γ^{j+1} q′_j S + Σ_{m≤j} γ^{j−m}(q′_j·k′_m) v_m.
+// Block 256 threads = 16 rows × 16 column-threads (4 v each); 64 v per block.
+// grid = (ceil(d_v/64), ceil(chunk/16), BH·nchunks).  S = ws slot of the
+// chunk (state entering it) or, when ws_states == nullptr, state_in / 0.
+// Writes o to out (Tout) or to an fp32 buffer when out_f32 != nullptr.
+// ---------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) chunk_out_kernel(
+    const float* __restrict__ qp, const float* __restrict__ kp, const Tin* __restrict__ v,
+    const float* __restrict__ ws_states, const float* __restrict__ state_in,
+    Tout* __restrict__ out, float* __restrict__ out_f32, CallConsts cc, int H, int L, int d_k,
+    int d_v, int chunk, int nchunks) {
+  extern __shared__ float smem[];
+  float* sq = smem;                 // [16][d_k]
+  float* sp = smem + 16 * d_k;      // [16][64] scores
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int v0 = blockIdx.x * 64;
+  const int bh = blockIdx.z / nchunks, ci = blockIdx.z % nchunks;
+  const int h = bh % H;
+  const int start = ci * chunk;
+  const int r = min(chunk, L - start);
+  const int j0 = blockIdx.y * 16;
+  if (j0 >= r) return;
+  const float lg2 = cc.lg2g[h];
+  const size_t rowbase = static_cast<size_t>(bh) * L + start;
+
+  for (int e = threadIdx.x; e < 16 * d_k; e += 256) {
+    const int jj = e / d_k, kk = e % d_k;
+    sq[e] = (j0 + jj < r) ? qp[(rowbase + j0 + jj) * d_k + kk] : 0.f;
+  }
+  __syncthreads();
+
+  const int j = j0 + ty;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+  // cross-chunk term q′_j S (ξ applied below)
+  const float* S = ws_states ? ws_states + (static_cast<size_t>(bh) * nchunks + ci) * d_k * d_v
+                             : (state_in ? state_in + static_cast<size_t>(bh) * d_k * d_v : nullptr);
+  if (S) {
+    for (int kk = 0; kk < d_k; ++kk) {
+      const float qv = sq[ty * d_k + kk];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int vv = v0 + tx + 16 * u;
+        if (vv < d_v) o[u] = fmaf(qv, S[static_cast<size_t>(kk) * d_v + vv], o[u]);
+      }
+    }
+    const float xi = gpow(lg2, static_cast<float>(j + 1));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) o[u] *= xi;
+  }
+  // intra-chunk term over key tiles of 64
+  const int mmax = min(r, j0 + 16);
+  for (int m0 = 0; m0 < mmax; m0 += 64) {
+    __syncthreads();
+    // scores for rows j0..j0+15, keys m0..m0+63: 4 per thread
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int mm = tx + 16 * u;
+      const int m = m0 + mm;
+      float sc = 0.f;
+      if (m < r && m <= j && j < r) {
+        const float* kr = kp + (rowbase + m) * d_k;
+        const float* qr = sq + ty * d_k;
+        float acc = 0.f;
+        for (int kk = 0; kk < d_k; ++kk) acc = fmaf(qr[kk], kr[kk], acc);
+        sc = acc * gpow(lg2, static_cast<float>(j - m));
+      }
+      sp[ty * 64 + mm] = sc;
+    }
+    __syncthreads();
+    const int mn = min(64, mmax - m0);
+    for (int mm = 0; mm < mn; ++mm) {
+      const float pv = sp[ty * 64 + mm];
+      const size_t vrow = (rowbase + m0 + mm) * d_v;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int vv = v0 + tx + 16 * u;
+        if (vv < d_v) o[u] = fmaf(pv, to_f32(v[vrow + vv]), o[u]);
+      }
+    }
+  }
+  if (j >= r) return;
+  const size_t orow = (rowbase + j) * d_v;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int vv = v0 + tx + 16 * u;
+    if (vv >= d_v) continue;
+    if (out_f32) out_f32[orow + vv] = o[u];
+    else out[orow + vv] = from_f32<Tout>(o[u]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// GroupNorm over d_v for each (b, h, t) row: one warp per row, fp32 input.
+// («从RoPE到Retention…» §5; one group per head, biased variance.)
+// ---------------------------------------------------------------------------
+template <typename Tout>
+__global__ void __launch_bounds__(256) groupnorm_kernel(const float* __restrict__ x,
+                                                        Tout* __restrict__ y,
+                                                        const float* __restrict__ w,
+                                                        const float* __restrict__ b, int H,
+                                                        int L, int d_v, size_t rows, float eps) {
+  const size_t row = static_cast<size_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const int h = static_cast<int>((row / L) % H);
+  const float* xr = x + row * d_v;
+  float s = 0.f;
+  for (int c = lane; c < d_v; c += 32) s += xr[c];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float mu = s / static_cast<float>(d_v);
+  float q = 0.f;
+  for (int c = lane; c < d_v; c += 32) {
+    const float dlt = xr[c] - mu;
+    q = fmaf(dlt, dlt, q);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+  const float rstd = rsqrtf(q / static_cast<float>(d_v) + eps);
+  Tout* yr = y + row * d_v;
+  for (int c = lane; c < d_v; c += 32) {
+    float val = (xr[c] - mu) * rstd;
+    if (w) val *= w[h * d_v + c];
+    if (b) val += b[h * d_v + c];
+    yr[c] = from_f32<Tout>(val);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Decode step («从RoPE到Retention…» §4.2):  S ← γ S + k′ᵀv ;  o = q′ S (new S).
+// One block per (b, h); thread t owns VEC consecutive v columns and walks all
+// d_k rows of S once (read, update, write, accumulate o).  S is streamed with
+// evict-first hints.  Optional GroupNorm over d_v (block reduction).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 ld_stream4(const float* p) {
+  float4 r;
+  asm volatile("ld.global.cs.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_stream4(float* p, float4 v) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
+
+template <typename Tin, typename Tout, int VEC>
+__global__ void __launch_bounds__(256) decode_step_kernel(
+    const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v,
+    float* __restrict__ S, Tout* __restrict__ out, CallConsts cc, int H, int d_k, int d_v,
+    float pos, int gn_on, float eps, const float* __restrict__ gw,
+    const float* __restrict__ gbias) {
+  extern __shared__ float sm[];
+  float* qs = sm;           // [d_k]
+  float* ks = sm + d_k;     // [d_k]
+  float* red = sm + 2 * d_k;  // [64]
+  const int bh = blockIdx.x;
+  const int h = bh % H;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < d_k / 2; i += blockDim.x) {
+    float c, s;
+    angle_cs(pos, cc.theta[i], c, s);
+    const size_t off = static_cast<size_t>(bh) * d_k + 2 * i;
+    const float q0 = to_f32(q[off]), q1 = to_f32(q[off + 1]);
+    const float k0 = to_f32(k[off]), k1 = to_f32(k[off + 1]);
+    qs[2 * i] = q0 * c - q1 * s;
+    qs[2 * i + 1] = fmaf(q0, s, q1 * c);
+    ks[2 * i] = cc.kscale * (k0 * c - k1 * s);
+    ks[2 * i + 1] = cc.kscale * fmaf(k0, s, k1 * c);
+  }
+  __syncthreads();
+  const float g = cc.gamma[h];
+  const int c0 = tid * VEC;
+  const bool active = c0 < d_v;
+  float vv[VEC], o[VEC];
+#pragma unroll
+  for (int u = 0; u < VEC; ++u) {
+    vv[u] = active ? to_f32(v[static_cast<size_t>(bh) * d_v + c0 + u]) : 0.f;
+    o[u] = 0.f;
+  }
+  float* Sp = S + static_cast<size_t>(bh) * d_k * d_v + c0;
+  if (active) {
+    if constexpr (VEC == 4) {
+      constexpr int U = 8;
+      int kk = 0;
+      for (; kk + U <= d_k; kk += U) {
+        float4 sv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) sv[u] = ld_stream4(Sp + static_cast<size_t>(kk + u) * d_v);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const float kv = ks[kk + u], qv = qs[kk + u];
+          sv[u].x = fmaf(g, sv[u].x, kv * vv[0]);
+          sv[u].y = fmaf(g, sv[u].y, kv * vv[1]);
+          sv[u].z = fmaf(g, sv[u].z, kv * vv[2]);
+          sv[u].w = fmaf(g, sv[u].w, kv * vv[3]);
+          st_stream4(Sp + static_cast<size_t>(kk + u) * d_v, sv[u]);
+          o[0] = fmaf(qv, sv[u].x, o[0]);
+          o[1] = fmaf(qv, sv[u].y, o[1]);
+          o[2] = fmaf(qv, sv[u].z, o[2]);
+          o[3] = fmaf(qv, sv[u].w, o[3]);
+        }
+      }
+      for (; kk < d_k; ++kk) {
+        float4 s4 = ld_stream4(Sp + static_cast<size_t>(kk) * d_v);
+        const float kv = ks[kk], qv = qs[kk];
+        s4.x = fmaf(g, s4.x, kv * vv[0]);
+        s4.y = fmaf(g, s4.y, kv * vv[1]);
+        s4.z = fmaf(g, s4.z, kv * vv[2]);
+        s4.w = fmaf(g, s4.w, kv * vv[3]);
+        st_stream4(Sp + static_cast<size_t>(kk) * d_v, s4);
+        o[0] = fmaf(qv, s4.x, o[0]);
+        o[1] = fmaf(qv, s4.y, o[1]);
+        o[2] = fmaf(qv, s4.z, o[2]);
+        o[3] = fmaf(qv, s4.w, o[3]);
+      }
+    } else {
+      for (int kk = 0; kk < d_k; ++kk) {
+        float* p = Sp + static_cast<size_t>(kk) * d_v;
+        const float sn = fmaf(g, *p, ks[kk] * vv[0]);
+        *p = sn;
+        o[0] = fmaf(qs[kk], sn, o[0]);
+      }
+    }
+  }
+  if (gn_on) {
+    // block mean / variance over the d_v outputs of this (b, h)
+    float s = 0.f;
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) s += active ? o[u] : 0.f;
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((tid & 31) == 0) red[tid >> 5] = s;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w2 = 0; w2 < (blockDim.x + 31) / 32; ++w2) tot += red[w2];
+    const float mu = tot / static_cast<float>(d_v);
+    __syncthreads();
+    float q2 = 0.f;
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) q2 += active ? (o[u] - mu) * (o[u] - mu) : 0.f;
+    for (int off = 16; off > 0; off >>= 1) q2 += __shfl_xor_sync(0xffffffffu, q2, off);
+    if ((tid & 31) == 0) red[32 + (tid >> 5)] = q2;
+    __syncthreads();
+    float totq = 0.f;
+    for (int w2 = 0; w2 < (blockDim.x + 31) / 32; ++w2) totq += red[32 + w2];
+    const float rstd = rsqrtf(totq / static_cast<float>(d_v) + eps);
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) {
+      float val = (o[u] - mu) * rstd;
+      if (gw) val *= active ? gw[h * d_v + c0 + u] : 1.f;
+      if (gbias) val += active ? gbias[h * d_v + c0 + u] : 0.f;
+      o[u] = val;
+    }
+  }
+  if (active) {
+#pragma unroll
+    for (int u = 0; u < VEC; ++u) out[static_cast<size_t>(bh) * d_v + c0 + u] = from_f32<Tout>(o[u]);
+  }
+}
+
+// Self-test of the bounded-wait failure path: wait on an mbarrier that no
+// one will ever arrive on; the wait must give up and record a timeout.
+__global__ void selftest_timeout_kernel(long long budget_cycles) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&bar));
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(1) : "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    for (;;) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(a), "r"(0)
+          : "memory");
+      if (ok) break;
+      if (clock64() - t0 > budget_cycles) {
+        report_timeout(0xdead0001u);
+        break;
+      }
+    }
+  }
+}
+
+}  // namespace simt
+}  // namespace ret

@@ -1,0 +1,573 @@
+// libretention.so — C ABI (include/retention.h): argument validation, path
+// selection, workspace layout and kernel launches.  One translation unit so
+// the device status word and the kernels share a module.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "retention.h"
+#include "common.cuh"
+#include "tc_primitives.cuh"
+#include "kernels_simt.cuh"
+#include "kernel_tc_chunk.cuh"
+
+using namespace ret;
+
+namespace {
+
+int g_force_path = 0;
+
+// Profiling hook state (see ret_profile_begin).
+struct ProfileHook {
+  cudaEvent_t* ev = nullptr;
+  int cap = 0;
+  int used = 0;              // kernels recorded
+  const char* names[64] = {};
+} g_prof;
+
+// Brackets one kernel launch with the hook's events when it is armed.
+struct Mark {
+  cudaStream_t st;
+  bool on;
+  Mark(const char* name, cudaStream_t s) : st(s), on(false) {
+    if (g_prof.ev && 2 * g_prof.used + 1 < g_prof.cap && g_prof.used < 64) {
+      g_prof.names[g_prof.used] = name;
+      cudaEventRecord(g_prof.ev[2 * g_prof.used], st);
+      on = true;
+    }
+  }
+  ~Mark() {
+    if (on) {
+      cudaEventRecord(g_prof.ev[2 * g_prof.used + 1], st);
+      ++g_prof.used;
+    }
+  }
+};
+
+constexpr int64_t kMaxPos = int64_t(1) << 24;
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ---------------------------------------------------------------------------
+// Per-call constants from the host arrays γ[H], θ[d_k/2]
+// ---------------------------------------------------------------------------
+ret_status make_consts(CallConsts& cc, const float* gamma, const float* theta, int H, int d_k,
+                       int chunk, int L) {
+  std::memset(&cc, 0, sizeof(cc));
+  if (!gamma || !theta) return RET_EINVAL;
+  for (int i = 0; i < d_k / 2; ++i) {
+    if (!std::isfinite(theta[i])) return RET_EINVAL;
+    cc.theta[i] = theta[i];
+  }
+  const int tail = (chunk > 0 && L > 0) ? (L - ((L - 1) / chunk) * chunk) : 0;
+  for (int h = 0; h < H; ++h) {
+    const double g = gamma[h];
+    if (!(g > 0.0) || !(g <= 1.0)) return RET_EINVAL;
+    const double lg = std::log2(g);
+    cc.gamma[h] = gamma[h];
+    cc.lg2g[h] = static_cast<float>(lg);
+    cc.gb[h] = static_cast<float>(std::pow(g, static_cast<double>(chunk > 0 ? chunk : 1)));
+    cc.gtail[h] = static_cast<float>(std::pow(g, static_cast<double>(tail > 0 ? tail : 1)));
+  }
+  cc.kscale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d_k)));
+  return RET_OK;
+}
+
+ret_status check_common(const void* q, const void* k, const void* v, ret_dtype in_dt, int B,
+                        int H, int L, int d_k, int d_v, int64_t pos0, const float* s_in,
+                        const float* s_out, const void* out, ret_dtype out_dt, const ret_gn* gn) {
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (!q || !k || !v || !out) return RET_EINVAL;
+  if (!al16(q) || !al16(k) || !al16(v) || !al16(out)) return RET_EINVAL;
+  if ((s_in && !al16(s_in)) || (s_out && !al16(s_out))) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1) return RET_EINVAL;
+  if (d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  if (pos0 < 0 || pos0 + L > kMaxPos) return RET_EINVAL;
+  if (static_cast<int64_t>(B) * H * L >= (int64_t(1) << 31)) return RET_EINVAL;
+  if (gn && gn->enabled) {
+    if (!(gn->eps > 0.f) || !std::isfinite(gn->eps)) return RET_EINVAL;
+    if ((gn->weight && !al16(gn->weight)) || (gn->bias && !al16(gn->bias))) return RET_EINVAL;
+  }
+  return RET_OK;
+}
+
+bool gn_on(const ret_gn* gn) { return gn && gn->enabled; }
+
+ret_status cuda_status(cudaError_t e) { return e == cudaSuccess ? RET_OK : RET_ECUDA; }
+
+ret_status last_launch() { return cuda_status(cudaGetLastError()); }
+
+// ---------------------------------------------------------------------------
+// TMA descriptors (driver entry point fetched through the runtime)
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult qres{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &qres) == cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box 64 × 128, 128-B swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------------------------
+// Path choice
+// ---------------------------------------------------------------------------
+bool tc_gamma_ok(const float* gamma, int H, int chunk) {
+  if (!gamma) return true;
+  for (int h = 0; h < H; ++h) {
+    const double g = gamma[h];
+    if (!(g > 0.0) || !(g <= 1.0)) return false;
+    // every factor γ^{±(b−1)} of the rewritten form stays within 2^±60
+    if (-(chunk - 1) * std::log2(g) > 60.0) return false;
+  }
+  return true;
+}
+
+bool tc_chunk_ok(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int d_v,
+                 int chunk) {
+  if (g_force_path == RET_PATH_SIMT) return false;
+  if (in_dt != RET_BF16) return false;
+  if (!(d_k == 64 || d_k == 128 || d_k == 256)) return false;
+  if (d_v % tcc::VT != 0 || chunk != tcc::CH || L % tcc::CH != 0) return false;
+  return tc_gamma_ok(gamma, H, chunk);
+}
+
+struct Plan {
+  int path = 0;
+  size_t bytes = 0;
+  // workspace offsets
+  size_t off_q = 0, off_k = 0, off_states = 0, off_ofp32 = 0;
+};
+
+Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k, int d_v,
+                    int chunk, bool gn) {
+  Plan p;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const int nch = (L + chunk - 1) / chunk;
+  size_t off = 0;
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk)) {
+    p.path = RET_PATH_TC;
+    p.off_q = off; off += up256(BH * L * d_k * 2);
+    p.off_k = off; off += up256(BH * L * d_k * 2);
+  } else {
+    p.path = RET_PATH_SIMT;
+    p.off_q = off; off += up256(BH * L * d_k * 4);
+    p.off_k = off; off += up256(BH * L * d_k * 4);
+    p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4);
+  }
+  if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
+  p.bytes = off;
+  return p;
+}
+
+Plan plan_parallel(int B, int H, int L, int d_k, int d_v, bool gn, bool want_state) {
+  Plan p;
+  const size_t BH = static_cast<size_t>(B) * H;
+  size_t off = 0;
+  p.path = RET_PATH_SIMT;
+  p.off_q = off; off += up256(BH * L * d_k * 4);
+  p.off_k = off; off += up256(BH * L * d_k * 4);
+  if (want_state) { p.off_states = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4); }
+  if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
+  p.bytes = off;
+  return p;
+}
+
+template <typename T> T* wsp(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ---------------------------------------------------------------------------
+// fp32 path: rotation into fp32 workspace, per-chunk ΔS, scan, outputs
+// ---------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const CallConsts& cc,
+                            int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                            const float* s_in, float* s_out, Tout* out, const ret_gn* gn,
+                            void* ws, const Plan& p, bool need_states, cudaStream_t st) {
+  const int BH = B * H;
+  const int nch = (L + chunk - 1) / chunk;
+  float* qp = wsp<float>(ws, p.off_q);
+  float* kp = wsp<float>(ws, p.off_k);
+  {
+    dim3 grid((d_k / 2 + 31) / 32, (L + 7) / 8);
+    {
+      Mark m("rotate_q_f32", st);
+      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(q, qp, cc, BH, L, d_k,
+                                                                    static_cast<float>(pos0), 1.f);
+    }
+    {
+      Mark m("rotate_k_f32", st);
+      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(k, kp, cc, BH, L, d_k,
+                                                                    static_cast<float>(pos0), cc.kscale);
+    }
+  }
+  float* states = need_states ? wsp<float>(ws, p.off_states) : nullptr;
+  if (states) {
+    dim3 g1((d_v + 63) / 64, (d_k + 63) / 64, BH * nch);
+    {
+      Mark m("chunk_dS_f32", st);
+      simt::chunk_dS_kernel<Tin><<<g1, dim3(16, 16), 0, st>>>(kp, v, states, cc, H, L, d_k, d_v,
+                                                              chunk, nch);
+    }
+    const size_t n = static_cast<size_t>(BH) * d_k * d_v;
+    Mark m("state_scan", st);
+    simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        states, s_in, s_out, cc, H, d_k, d_v, nch, BH);
+  }
+  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
+  {
+    dim3 g2((d_v + 63) / 64, (chunk + 15) / 16, BH * nch);
+    const size_t smem = (16 * static_cast<size_t>(d_k) + 16 * 64) * sizeof(float);
+    // ws_states == nullptr means "use state_in for the single chunk" (parallel form)
+    const float* wst = (nch > 1 || states) ? states : nullptr;
+    Mark m("chunk_out_f32", st);
+    simt::chunk_out_kernel<Tin, Tout><<<g2, 256, smem, st>>>(qp, kp, v, wst, s_in, out, ofp, cc,
+                                                             H, L, d_k, d_v, chunk, nch);
+  }
+  if (ofp) {
+    const size_t rows = static_cast<size_t>(BH) * L;
+    Mark m("groupnorm", st);
+    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        ofp, out, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
+  }
+  return last_launch();
+}
+
+template <typename Tout>
+ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                        const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
+                        int64_t pos0, const float* s_in, float* s_out, Tout* out,
+                        const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st) {
+  const int BH = B * H;
+  __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
+  __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
+  {
+    const size_t n = static_cast<size_t>(L) * (d_k / 8);
+    Mark m("rotate_qk_bf16", st);
+    tcc::rotate_qk_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        q, k, qr, kr, cc, BH, H, L, d_k, static_cast<float>(pos0), tcc::CH);
+  }
+  CUtensorMap mq, mk, mv;
+  const uint64_t rows = static_cast<uint64_t>(BH) * L;
+  if (!make_map(&mq, qr, rows, d_k) || !make_map(&mk, kr, rows, d_k) || !make_map(&mv, v, rows, d_v))
+    return RET_ECUDA;
+  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
+  tcc::ChunkArgs a;
+  a.state_in = s_in;
+  a.state_out = s_out;
+  a.out = ofp ? static_cast<void*>(ofp) : static_cast<void*>(out);
+  a.out_f32 = (ofp || sizeof(Tout) == 4) ? 1 : 0;
+  a.H = H;
+  a.L = L;
+  a.d_v = d_v;
+  a.nchunks = L / tcc::CH;
+  dim3 grid(d_v / tcc::VT, BH);
+  auto launch = [&](auto kern, uint32_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    Mark m("chunk_tc", st);
+    kern<<<grid, tcc::NTHREADS, smem, st>>>(mq, mk, mv, a, cc);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if (d_k == 256) e = launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES);
+  else if (d_k == 128) e = launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES);
+  else e = launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES);
+  if (e != cudaSuccess) return RET_ECUDA;
+  if (ofp) {
+    const size_t r = static_cast<size_t>(BH) * L;
+    Mark m("groupnorm", st);
+    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
+        ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+  }
+  return last_launch();
+}
+
+template <typename Tin>
+ret_status dispatch_simt_out(const void* q, const void* k, const void* v, const CallConsts& cc,
+                             int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                             const float* s_in, float* s_out, void* out, ret_dtype out_dt,
+                             const ret_gn* gn, void* ws, const Plan& p, bool need_states,
+                             cudaStream_t st) {
+  const Tin* qq = static_cast<const Tin*>(q);
+  const Tin* kk = static_cast<const Tin*>(k);
+  const Tin* vv = static_cast<const Tin*>(v);
+  if (out_dt == RET_F32)
+    return run_simt_chunked<Tin, float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, chunk, s_in,
+                                        s_out, static_cast<float*>(out), gn, ws, p, need_states, st);
+  return run_simt_chunked<Tin, __nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, chunk,
+                                               s_in, s_out, static_cast<__nv_bfloat16*>(out), gn,
+                                               ws, p, need_states, st);
+}
+
+}  // namespace
+
+// ===========================================================================
+// Exported entry points
+// ===========================================================================
+extern "C" {
+
+const char* ret_status_string(ret_status s) {
+  switch (s) {
+    case RET_OK: return "ok";
+    case RET_EINVAL: return "invalid argument";
+    case RET_EUNSUPPORTED: return "arguments outside the implemented domain";
+    case RET_ECUDA: return "CUDA error";
+    case RET_ETIMEOUT: return "a kernel's bounded wait expired";
+    case RET_EWORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int ret_abi_version(void) { return RET_ABI_VERSION; }
+
+ret_status ret_profile_begin(cudaEvent_t* events, int n_events) {
+  if (!events || n_events < 2) return RET_EINVAL;
+  g_prof.ev = events;
+  g_prof.cap = n_events;
+  g_prof.used = 0;
+  return RET_OK;
+}
+
+int ret_profile_end(void) {
+  const int n = g_prof.used;
+  g_prof.ev = nullptr;
+  g_prof.cap = 0;
+  return n;
+}
+
+const char* ret_profile_kernel(int i) {
+  return (i >= 0 && i < g_prof.used && i < 64) ? g_prof.names[i] : "";
+}
+
+ret_status ret_force_path(int path) {
+  if (path != 0 && path != RET_PATH_SIMT && path != RET_PATH_TC) return RET_EINVAL;
+  g_force_path = path;
+  return RET_OK;
+}
+
+ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,
+                              int d_v, int chunk, ret_dtype out_dt, int gn_enabled, int* path,
+                              size_t* workspace_bytes) {
+  if (!path || !workspace_bytes) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || chunk < 1)
+    return RET_EINVAL;
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_enabled != 0);
+  *path = p.path;
+  *workspace_bytes = p.bytes;
+  return RET_OK;
+}
+
+ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                         const float* gamma, const float* theta, int B, int H, int L, int d_k,
+                         int d_v, int64_t pos0, int chunk, const float* state_in,
+                         float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
+                              out_dt, gn);
+  if (s != RET_OK) return s;
+  if (chunk < 1) return RET_EINVAL;
+  CallConsts cc;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn));
+  if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes || !al16(workspace)))
+    return RET_EWORKSPACE;
+  if (p.path == RET_PATH_TC) {
+    const auto* qq = static_cast<const __nv_bfloat16*>(q);
+    const auto* kk = static_cast<const __nv_bfloat16*>(k);
+    const auto* vv = static_cast<const __nv_bfloat16*>(v);
+    if (out_dt == RET_F32)
+      return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
+                                 static_cast<float*>(out), gn, workspace, p, stream);
+    return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
+                                       state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
+                                       p, stream);
+  }
+  if (in_dt == RET_F32)
+    return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                                    state_out, out, out_dt, gn, workspace, p, true, stream);
+  return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                                          state_out, out, out_dt, gn, workspace, p, true, stream);
+}
+
+ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                   int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
+                                   int* path, size_t* workspace_bytes) {
+  if (in_dt == RET_BF16 && tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk))
+    return RET_EUNSUPPORTED;
+  return ret_chunkwise_plan(in_dt, gamma, B, H, L, d_k, d_v, chunk, out_dt, gn_enabled, path,
+                            workspace_bytes);
+}
+
+ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                              const float* gamma, const float* theta, int B, int H, int L,
+                              int d_k, int d_v, int64_t pos0, int chunk, const float* state_in,
+                              float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  // The fp32 path of ret_chunkwise already runs in the chunk-parallel layout.
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk)) return RET_EUNSUPPORTED;
+  return ret_chunkwise(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                       state_out, out, out_dt, gn, workspace, workspace_bytes, stream);
+}
+
+ret_status ret_parallel_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,
+                             int d_v, ret_dtype out_dt, int gn_enabled, int state_out_wanted,
+                             int* path, size_t* workspace_bytes) {
+  (void)gamma;
+  if (!path || !workspace_bytes) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024)
+    return RET_EINVAL;
+  const Plan p = plan_parallel(B, H, L, d_k, d_v, gn_enabled != 0, state_out_wanted != 0);
+  *path = p.path;
+  *workspace_bytes = p.bytes;
+  return RET_OK;
+}
+
+ret_status ret_parallel(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                        const float* gamma, const float* theta, int B, int H, int L, int d_k,
+                        int d_v, int64_t pos0, const float* state_in, float* state_out,
+                        void* out, ret_dtype out_dt, const ret_gn* gn, void* workspace,
+                        size_t workspace_bytes, cudaStream_t stream) {
+  ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
+                              out_dt, gn);
+  if (s != RET_OK) return s;
+  CallConsts cc;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, L, L)) != RET_OK) return s;
+  const Plan p = plan_parallel(B, H, L, d_k, d_v, gn_on(gn), state_out != nullptr);
+  if (!workspace || workspace_bytes < p.bytes || !al16(workspace)) return RET_EWORKSPACE;
+  // One chunk of length L: the chunk kernels evaluate the parallel form.
+  if (in_dt == RET_F32)
+    return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, L, state_in, state_out,
+                                    out, out_dt, gn, workspace, p, state_out != nullptr, stream);
+  return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, L, state_in,
+                                          state_out, out, out_dt, gn, workspace, p,
+                                          state_out != nullptr, stream);
+}
+
+ret_status ret_step(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                    const float* gamma, const float* theta, int B, int H, int d_k, int d_v,
+                    int64_t pos, float* state, void* out, ret_dtype out_dt, const ret_gn* gn,
+                    cudaStream_t stream) {
+  ret_status s = check_common(q, k, v, in_dt, B, H, 1, d_k, d_v, pos, state, state, out, out_dt, gn);
+  if (s != RET_OK) return s;
+  if (!state) return RET_EINVAL;
+  CallConsts cc;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, 1, 1)) != RET_OK) return s;
+  const int vec = (d_v % 4 == 0) ? 4 : 1;
+  const int threads = (d_v + vec - 1) / vec;
+  if (threads > 256) return RET_EUNSUPPORTED;
+  const int nthr = ((threads + 31) / 32) * 32;
+  const size_t smem = (2 * static_cast<size_t>(d_k) + 64) * sizeof(float);
+  const int BH = B * H;
+  const int g = gn_on(gn) ? 1 : 0;
+  const float eps = g ? gn->eps : 0.f;
+  const float* gw = g ? gn->weight : nullptr;
+  const float* gbb = g ? gn->bias : nullptr;
+  const float fpos = static_cast<float>(pos);
+  Mark mark("decode_step", stream);
+#define RET_DECODE(TIN, TOUT, VEC)                                                           \
+  simt::decode_step_kernel<TIN, TOUT, VEC><<<BH, nthr, smem, stream>>>(                      \
+      static_cast<const TIN*>(q), static_cast<const TIN*>(k), static_cast<const TIN*>(v),     \
+      state, static_cast<TOUT*>(out), cc, H, d_k, d_v, fpos, g, eps, gw, gbb)
+  if (in_dt == RET_BF16) {
+    if (out_dt == RET_BF16) { if (vec == 4) RET_DECODE(__nv_bfloat16, __nv_bfloat16, 4); else RET_DECODE(__nv_bfloat16, __nv_bfloat16, 1); }
+    else { if (vec == 4) RET_DECODE(__nv_bfloat16, float, 4); else RET_DECODE(__nv_bfloat16, float, 1); }
+  } else {
+    if (out_dt == RET_BF16) { if (vec == 4) RET_DECODE(float, __nv_bfloat16, 4); else RET_DECODE(float, __nv_bfloat16, 1); }
+    else { if (vec == 4) RET_DECODE(float, float, 4); else RET_DECODE(float, float, 1); }
+  }
+#undef RET_DECODE
+  return last_launch();
+}
+
+ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B, int H, int L,
+                      int d, int64_t pos0, float scale, void* y, ret_dtype out_dt,
+                      cudaStream_t stream) {
+  if (!x || !y || !theta || !al16(x) || !al16(y)) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || L < 1 || d < 2 || d > 2 * kMaxPairs || (d & 1)) return RET_EINVAL;
+  if (pos0 < 0 || pos0 + L > kMaxPos || !std::isfinite(scale)) return RET_EINVAL;
+  CallConsts cc;
+  std::memset(&cc, 0, sizeof(cc));
+  for (int i = 0; i < d / 2; ++i) {
+    if (!std::isfinite(theta[i])) return RET_EINVAL;
+    cc.theta[i] = theta[i];
+  }
+  const int BH = B * H;
+  dim3 grid((d / 2 + 31) / 32, (L + 7) / 8);
+  const float p0 = static_cast<float>(pos0);
+  if (in_dt == RET_BF16 && out_dt == RET_BF16)
+    simt::rotate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, L, d, p0, scale);
+  else if (in_dt == RET_BF16)
+    simt::rotate_kernel<__nv_bfloat16, float><<<grid, dim3(32, 8), 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), cc, BH, L, d, p0, scale);
+  else if (out_dt == RET_BF16)
+    simt::rotate_kernel<float, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
+        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, L, d, p0, scale);
+  else
+    simt::rotate_kernel<float, float><<<grid, dim3(32, 8), 0, stream>>>(
+        static_cast<const float*>(x), static_cast<float*>(y), cc, BH, L, d, p0, scale);
+  return last_launch();
+}
+
+ret_status ret_sync_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return RET_ECUDA;
+  unsigned int h[4] = {0, 0, 0, 0};
+  if (cudaMemcpyFromSymbol(h, g_ret_status, sizeof(h)) != cudaSuccess) return RET_ECUDA;
+  if (h[0] != 0u) {
+    const unsigned int z[4] = {0, 0, 0, 0};
+    if (cudaMemcpyToSymbol(g_ret_status, z, sizeof(z)) != cudaSuccess) return RET_ECUDA;
+    if (h[0] & kStatusTimeout) return RET_ETIMEOUT;
+  }
+  return RET_OK;
+}
+
+ret_status ret_selftest_timeout(int budget_us, cudaStream_t stream) {
+  if (budget_us < 1 || budget_us > 2000000) return RET_EINVAL;
+  int dev = 0, khz = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RET_ECUDA;
+  if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess) return RET_ECUDA;
+  if (khz <= 0) khz = 2000000;
+  const long long cycles = static_cast<long long>(budget_us) * (khz / 1000);
+  simt::selftest_timeout_kernel<<<1, 32, 0, stream>>>(cycles);
+  return last_launch();
+}
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+"""Host-side checks of the C ABI: build, symbol exports, validation, planning.
+
+None of these launch a kernel, so they run without a GPU.
+"""
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+from linear_recurrent_sequence_prologue_b300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "retention.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ret_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("ret_parallel", "ret_chunkwise", "ret_step", "ret_status_string"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ret_[a-z_0-9]+)\b", out))
+    missing = [n for n in header_functions() if n not in exported]
+    assert not missing, missing
+    for n in header_functions():
+        assert hasattr(lib, n)
+        assert n in _lib.SIGNATURES, f"binding lacks a signature for {n}"
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ret_abi_version() == 1
+    for code in range(6):
+        assert lib.ret_status_string(code)
+    assert b"unknown" in lib.ret_status_string(99)
+
+
+def _fp(a):
+    return a.ctypes.data_as(C.POINTER(C.c_float))
+
+
+def _chunkwise_args(**over):
+    g = np.full(2, 0.9, np.float32)
+    t = np.ones(8, np.float32)
+    a = dict(q=C.c_void_p(0x1000), k=C.c_void_p(0x2000), v=C.c_void_p(0x3000), in_dt=_lib.RET_F32,
+             gamma=_fp(g), theta=_fp(t), B=1, H=2, L=64, d_k=16, d_v=16, pos0=0, chunk=16,
+             s_in=None, s_out=None, out=C.c_void_p(0x4000), out_dt=_lib.RET_F32, gn=None,
+             ws=None, wsb=0, stream=None)
+    a.update(over)
+    return a, (g, t)
+
+
+def _call_chunkwise(lib, a):
+    return lib.ret_chunkwise(a["q"], a["k"], a["v"], a["in_dt"], a["gamma"], a["theta"], a["B"],
+                             a["H"], a["L"], a["d_k"], a["d_v"], a["pos0"], a["chunk"], a["s_in"],
+                             a["s_out"], a["out"], a["out_dt"], a["gn"], a["ws"], a["wsb"],
+                             a["stream"])
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), _lib.RET_EINVAL),
+    (dict(out=None), _lib.RET_EINVAL),
+    (dict(q=C.c_void_p(0x1004)), _lib.RET_EINVAL),          # misaligned
+    (dict(d_k=15), _lib.RET_EINVAL),                          # odd d_k
+    (dict(d_k=1024), _lib.RET_EINVAL),
+    (dict(H=0), _lib.RET_EINVAL),
+    (dict(H=129), _lib.RET_EINVAL),
+    (dict(L=0), _lib.RET_EINVAL),
+    (dict(chunk=0), _lib.RET_EINVAL),
+    (dict(pos0=-1), _lib.RET_EINVAL),
+    (dict(pos0=(1 << 24) - 10), _lib.RET_EINVAL),            # positions beyond 2^24
+    (dict(in_dt=7), _lib.RET_EINVAL),
+    (dict(gamma=None), _lib.RET_EINVAL),
+    (dict(ws=None, wsb=0), _lib.RET_EWORKSPACE),              # fp32 path needs scratch
+])
+def test_chunkwise_validation_is_synchronous(lib, over, expect):
+    a, keep = _chunkwise_args(**over)
+    assert _call_chunkwise(lib, a) == expect
+
+
+def test_gamma_out_of_range_rejected(lib):
+    for bad in (0.0, -0.5, 1.5, float("nan")):
+        g = np.array([0.9, bad], np.float32)
+        a, keep = _chunkwise_args(gamma=_fp(g))
+        assert _call_chunkwise(lib, a) == _lib.RET_EINVAL
+
+
+def test_step_and_rotate_validation(lib):
+    g = np.full(2, 0.9, np.float32)
+    t = np.ones(8, np.float32)
+    st = lib.ret_step(None, None, None, _lib.RET_BF16, _fp(g), _fp(t), 1, 2, 16, 16, 0,
+                      C.c_void_p(0x1000), C.c_void_p(0x2000), _lib.RET_BF16, None, None)
+    assert st == _lib.RET_EINVAL
+    st = lib.ret_rotate(C.c_void_p(0x1000), _lib.RET_BF16, _fp(t), 1, 1, 8, 15, 0, 1.0,
+                        C.c_void_p(0x2000), _lib.RET_BF16, None)
+    assert st == _lib.RET_EINVAL
+    assert lib.ret_selftest_timeout(0, None) == _lib.RET_EINVAL
+    assert lib.ret_force_path(5) == _lib.RET_EINVAL
+
+
+def _plan(lib, in_dt, B, H, L, d_k, d_v, chunk, gn=0, gamma=None):
+    path, nb = C.c_int(0), C.c_size_t(0)
+    gp = _fp(gamma) if gamma is not None else None
+    st = lib.ret_chunkwise_plan(in_dt, gp, B, H, L, d_k, d_v, chunk, in_dt, gn, C.byref(path), C.byref(nb))
+    assert st == _lib.RET_OK
+    return path.value, nb.value
+
+
+def test_path_selection(lib):
+    # 7B shape: tensor-core path, workspace = rotated Q′ and K̂′ in bf16
+    p, nb = _plan(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128)
+    assert p == _lib.RET_PATH_TC
+    assert nb == 2 * 2 * 16 * 8192 * 256 * 2
+    # fp32 inputs, chunk 64, d_v 64 → fp32 kernels
+    assert _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)[0] == _lib.RET_PATH_SIMT
+    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64)[0] == _lib.RET_PATH_SIMT
+    # a head whose γ^127 underflows the rewritten form goes to the fp32 kernels
+    g = np.array([0.5, 0.99], np.float32)
+    assert _plan(lib, _lib.RET_BF16, 1, 2, 256, 256, 128, 128, gamma=g)[0] == _lib.RET_PATH_SIMT
+    g = np.array([0.9, 0.99], np.float32)
+    assert _plan(lib, _lib.RET_BF16, 1, 2, 256, 256, 128, 128, gamma=g)[0] == _lib.RET_PATH_TC

@@ -1,0 +1,270 @@
+"""GPU parity: every ABI call against the float64 oracle on seeded inputs.
+
+Ordered from small to large.  Sizes the oracle finishes in seconds span
+several tiles and a ragged tail; the full workloads are checked on sampled
+(b, h) pairs, which the oracle computes head by head.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import linear_recurrent_sequence_prologue_b300 as R
+from linear_recurrent_sequence_prologue_b300.inputs import (WORKLOADS, Workload, gamma_schedule,
+                                                            make_decode_inputs, make_inputs,
+                                                            theta_schedule, to_f64)
+from oracle import retention_ref as O
+
+from helpers import BF16_TOL, assert_close, gpu_np, head_slice, max_rel_inf, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from linear_recurrent_sequence_prologue_b300 import build
+    build.build()
+    R.load()
+    R.force_path(0)
+    yield
+    R.force_path(0)
+
+
+def _cuda(inp):
+    d = dict(inp)
+    for key in ("q", "k", "v", "state_in"):
+        if d.get(key) is not None:
+            d[key] = d[key].cuda()
+    return d
+
+
+def _oracle_full(inp, w, form="chunkwise", chunk=None, pos0=0, gn=None):
+    return O.retention(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                       np.asarray(inp["gamma"], np.float64), np.asarray(inp["theta"], np.float64),
+                       pos0, to_f64(inp["state_in"]), form, chunk, gn)
+
+
+def _custom(B, H, L, d_k, d_v, dtype, chunk, std=1.0, state_std=0.0, seed=0):
+    w = Workload("custom", B, H, L, d_k, d_v, dtype, chunk, std, state_std=state_std)
+    return w, make_inputs(w, seed)
+
+
+# ---------------------------------------------------------------- prologue --
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_rotate_matches_oracle(dtype):
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(2, 3, 200, 64, generator=g).to(dtype)
+    th = theta_schedule(64)
+    for pos0, scale in ((0, 1.0), (12345, 0.125)):
+        y = R.rotate(x.cuda(), th, pos0=pos0, scale=scale, out_dtype=torch.float32)
+        sin, cos = O.rotation_tables(np.arange(200) + pos0, th.astype(np.float64))
+        ref = scale * O.theta_shift(to_f64(x), sin, cos)
+        assert max_rel_inf(gpu_np(y), ref) < 2e-6
+
+
+# ------------------------------------------------------------ fp32 (Tiny) --
+def test_tiny_all_forms_vs_brute_force():
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w, seed=0)
+    ref_o, ref_s = O.brute_force(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                                 inp["gamma"].astype(np.float64), inp["theta"].astype(np.float64))
+    d = _cuda(inp)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk)
+    assert_close(gpu_np(o), ref_o, torch.float32, "chunkwise")
+    assert_close(gpu_np(s), ref_s, torch.float32, "chunkwise state")
+    o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk, layout="scan")
+    assert torch.equal(s, s2) and torch.equal(o, o2)
+    o3, s3 = R.parallel(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], return_state=True)
+    assert_close(gpu_np(o3), ref_o, torch.float32, "parallel")
+    assert_close(gpu_np(s3), ref_s, torch.float32, "parallel state")
+    # recurrent form = 64 decode steps
+    st = torch.zeros(1, 2, 16, 16, device="cuda")
+    outs = [R.step(d["q"][:, :, t].contiguous(), d["k"][:, :, t].contiguous(),
+                   d["v"][:, :, t].contiguous(), inp["gamma"], inp["theta"], t, st)
+            for t in range(w.L)]
+    assert_close(gpu_np(torch.stack(outs, 2)), ref_o, torch.float32, "steps")
+    assert_close(gpu_np(st), ref_s, torch.float32, "steps state")
+
+
+@pytest.mark.parametrize("L,chunk,pos0", [(64, 16, 0), (61, 16, 7), (50, 1, 3), (33, 64, 1000), (1, 16, 5)])
+def test_fp32_edge_cases(L, chunk, pos0):
+    w, inp = _custom(2, 3, L, 16, 12, "f32", chunk, state_std=0.3, seed=L)
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", chunk, pos0)
+    d = _cuda(inp)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=chunk, pos0=pos0,
+                       state_in=d["state_in"])
+    assert_close(gpu_np(o), ref_o, torch.float32, "out")
+    assert_close(gpu_np(s), ref_s, torch.float32, "state")
+    o2, s2 = R.parallel(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], pos0=pos0,
+                        state_in=d["state_in"], return_state=True)
+    assert_close(gpu_np(o2), ref_o, torch.float32, "parallel out")
+    assert_close(gpu_np(s2), ref_s, torch.float32, "parallel state")
+
+
+def test_groupnorm_fp32_with_affine():
+    w, inp = _custom(2, 3, 48, 16, 24, "f32", 16, seed=9)
+    gw = torch.randn(3 * 24, generator=torch.Generator().manual_seed(1))
+    gbias = torch.randn(3 * 24, generator=torch.Generator().manual_seed(2))
+    gn = {"eps": 1e-5, "weight": gw.reshape(3, 24).numpy(), "bias": gbias.reshape(3, 24).numpy()}
+    ref_o, _ = _oracle_full(inp, w, "chunkwise", 16, 0, gn)
+    d = _cuda(inp)
+    o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=16,
+                       gn={"eps": 1e-5, "weight": gw.cuda(), "bias": gbias.cuda()})
+    assert_close(gpu_np(o), ref_o, torch.float32, "gn")
+
+
+# ------------------------------------------------------- bf16, small shapes --
+def test_small_workload_all_heads():
+    w = WORKLOADS["small"]
+    inp = make_inputs(w, seed=0)
+    ref_o, _ = _oracle_full(inp, w, "chunkwise", w.chunk)
+    d = _cuda(inp)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk)
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "small out")
+
+
+@pytest.mark.parametrize("d_k,d_v,L,H", [(64, 128, 128, 1), (128, 128, 384, 2), (256, 256, 512, 2),
+                                         (256, 512, 256, 3)])
+def test_tc_chunkwise_vs_oracle(d_k, d_v, L, H):
+    w, inp = _custom(2, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1, seed=d_k + L)
+    path, _ = R.plan("chunkwise", torch.bfloat16, 2, H, L, d_k, d_v, 128, gamma=inp["gamma"])
+    assert path == R.RET_PATH_TC
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", 128, pos0=17)
+    d = _cuda(inp)
+    for odt in (torch.bfloat16, torch.float32):
+        o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=17,
+                           state_in=d["state_in"], out_dtype=odt)
+        assert R.sync_status() == R.RET_OK
+        assert_close(gpu_np(o), ref_o, torch.bfloat16, f"tc out {odt}")
+        assert_close(gpu_np(s), ref_s, torch.bfloat16, "tc state")
+
+
+def test_tc_matches_fp32_kernels():
+    w, inp = _custom(1, 2, 256, 256, 256, "bf16", 128, state_std=0.1, seed=5)
+    d = _cuda(inp)
+    o_tc, s_tc = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128,
+                             state_in=d["state_in"], out_dtype=torch.float32)
+    R.force_path(R.RET_PATH_SIMT)
+    try:
+        o_f, s_f = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128,
+                               state_in=d["state_in"], out_dtype=torch.float32)
+    finally:
+        R.force_path(0)
+    assert rel_fro(gpu_np(o_tc), gpu_np(o_f)) < BF16_TOL
+    assert rel_fro(gpu_np(s_tc), gpu_np(s_f)) < BF16_TOL
+
+
+@pytest.mark.parametrize("path", [0, 2])
+def test_exact_causality_on_gpu(path):
+    """Outputs before position m are bit-identical when inputs at ≥ m change."""
+    w, inp = _custom(1, 2, 384, 128, 128, "bf16", 128, state_std=0.1, seed=11)
+    d = _cuda(inp)
+    m = 200
+    q2, k2, v2 = d["q"].clone(), d["k"].clone(), d["v"].clone()
+    gen = torch.Generator(device="cuda").manual_seed(4)
+    for t in (q2, k2, v2):
+        t[:, :, m:] = (torch.randn(t[:, :, m:].shape, generator=gen, device="cuda") * 3).to(t.dtype)
+    R.force_path(path)
+    try:
+        o1, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, state_in=d["state_in"])
+        o2, _ = R.chunkwise(q2, k2, v2, inp["gamma"], inp["theta"], chunk=128, state_in=d["state_in"])
+    finally:
+        R.force_path(0)
+    assert torch.equal(o1[:, :, :m], o2[:, :, :m])
+    assert not torch.equal(o1[:, :, m:], o2[:, :, m:])
+
+
+def test_split_call_consistency_tc():
+    w, inp = _custom(1, 2, 512, 256, 128, "bf16", 128, state_std=0.1, seed=12)
+    d = _cuda(inp)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=5,
+                       state_in=d["state_in"], out_dtype=torch.float32)
+    h = 256
+    sl = lambda t, a, b: t[:, :, a:b].contiguous()
+    oa, sa = R.chunkwise(sl(d["q"], 0, h), sl(d["k"], 0, h), sl(d["v"], 0, h), inp["gamma"],
+                         inp["theta"], chunk=128, pos0=5, state_in=d["state_in"], out_dtype=torch.float32)
+    ob, sb = R.chunkwise(sl(d["q"], h, 512), sl(d["k"], h, 512), sl(d["v"], h, 512), inp["gamma"],
+                         inp["theta"], chunk=128, pos0=5 + h, state_in=sa, out_dtype=torch.float32)
+    assert torch.equal(torch.cat([oa, ob], 2), o)
+    assert torch.equal(sb, s)
+
+
+# -------------------------------------------------------- full workloads --
+def test_msr1p3b_groupnorm_sampled_heads():
+    w = WORKLOADS["msr1p3b"]
+    inp = make_inputs(w, seed=0)
+    d = _cuda(inp)
+    o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
+                       gn={"eps": w.gn_eps}, return_state=False)
+    assert R.sync_status() == R.RET_OK
+    for b, h in ((0, 0), (3, 5), (7, 7)):
+        q, k, v, s, g, th = head_slice(inp, b, h)
+        ref, _ = O.retention(q, k, v, g, th, 0, s, "chunkwise", w.chunk, {"eps": w.gn_eps})
+        assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref, torch.bfloat16, f"1.3B (b={b},h={h})")
+
+
+def test_msr7b_sampled_heads():
+    w = WORKLOADS["msr7b"]
+    inp = make_inputs(w, seed=0)
+    d = _cuda(inp)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
+                       state_in=d["state_in"])
+    assert R.sync_status() == R.RET_OK
+    for b, h in ((0, 0), (1, 15)):
+        q, k, v, si, g, th = head_slice(inp, b, h)
+        ref_o, ref_s = O.retention(q, k, v, g, th, 0, si, "chunkwise", w.chunk)
+        assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref_o, torch.bfloat16, f"7B out (b={b},h={h})")
+        assert_close(gpu_np(s[b:b + 1, h:h + 1]), ref_s, torch.bfloat16, f"7B state (b={b},h={h})")
+
+
+def test_decode_1024_steps_vs_chunkwise_and_oracle():
+    w = WORKLOADS["decode"]
+    inp = make_decode_inputs(w, seed=0, device="cuda")
+    S0 = inp["state"]
+    st = S0.clone()
+    outs = torch.empty((w.steps, w.B, w.H, w.d_v), dtype=torch.bfloat16, device="cuda")
+    for t in range(w.steps):
+        R.step(inp["q"][t], inp["k"][t], inp["v"][t], inp["gamma"], inp["theta"], t, st, out=outs[t])
+    assert R.sync_status() == R.RET_OK
+    q = inp["q"].permute(1, 2, 0, 3).contiguous()
+    k = inp["k"].permute(1, 2, 0, 3).contiguous()
+    v = inp["v"].permute(1, 2, 0, 3).contiguous()
+    oc, sc = R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=128, state_in=S0)
+    od = outs.permute(1, 2, 0, 3)
+    assert rel_fro(gpu_np(od), gpu_np(oc)) <= BF16_TOL
+    assert rel_fro(gpu_np(st), gpu_np(sc)) <= BF16_TOL
+    # two sampled heads against the float64 recurrent form
+    for b, h in ((0, 0), (77, 9)):
+        ref_o, ref_s = O.retention(to_f64(q[b:b + 1, h:h + 1]), to_f64(k[b:b + 1, h:h + 1]),
+                                   to_f64(v[b:b + 1, h:h + 1]), inp["gamma"][h:h + 1].astype(np.float64),
+                                   inp["theta"].astype(np.float64), 0, to_f64(S0[b:b + 1, h:h + 1]),
+                                   "recurrent")
+        assert_close(gpu_np(od[b:b + 1, h:h + 1]), ref_o, torch.bfloat16, f"decode (b={b},h={h})")
+        assert_close(gpu_np(st[b:b + 1, h:h + 1]), ref_s, torch.bfloat16, f"decode state (b={b},h={h})")
+
+
+def test_decode_groupnorm_and_odd_width():
+    w, inp = _custom(3, 2, 1, 32, 30, "bf16", 1, state_std=0.1, seed=21)
+    d = _cuda(inp)
+    st = d["state_in"].clone()
+    o = R.step(d["q"][:, :, 0].contiguous(), d["k"][:, :, 0].contiguous(), d["v"][:, :, 0].contiguous(),
+               inp["gamma"], inp["theta"], 41, st, out_dtype=torch.float32, gn={"eps": 1e-5})
+    ref_o, ref_s = O.decode_step(to_f64(inp["q"][:, :, 0]), to_f64(inp["k"][:, :, 0]),
+                                 to_f64(inp["v"][:, :, 0]), inp["gamma"].astype(np.float64),
+                                 inp["theta"].astype(np.float64), 41, to_f64(inp["state_in"]),
+                                 {"eps": 1e-5})
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "decode gn")
+    assert max_rel_inf(gpu_np(st), ref_s) < 1e-5
+
+
+# -------------------------------------------------------- failure path --
+def test_bounded_wait_timeout_reports_and_recovers():
+    assert R.sync_status() == R.RET_OK
+    R.selftest_timeout(2000)
+    assert R.sync_status() == R.RET_ETIMEOUT
+    assert R.sync_status() == R.RET_OK
+    w, inp = _custom(1, 2, 64, 16, 16, "f32", 16, seed=1)
+    d = _cuda(inp)
+    o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=16)
+    ref_o, _ = _oracle_full(inp, w, "chunkwise", 16)
+    assert_close(gpu_np(o), ref_o, torch.float32, "after timeout")
