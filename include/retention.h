@@ -108,6 +108,35 @@ ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H,
                               int* path, size_t* workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * ret_chunkwise_noalloc — ret_chunkwise for callers that may not allocate
+ * device memory themselves, e.g. plugins whose host application owns the
+ * whole device memory budget, or latency-critical loops that cannot afford
+ * a cudaMalloc (or a caching allocator's growth) inside them.  The RetNet
+ * pages have no counterpart: this is a library convenience.
+ * Scratch: instead of a caller workspace it uses one array of
+ * RET_NOALLOC_SCRATCH_BYTES that lives in the library's own device image.
+ * Every GPU that loads the library holds that array until the process
+ * exits.  Arguments as ret_chunkwise (all data pointers still come from the
+ * caller).  A problem whose plan needs more scratch than the array holds
+ * (ret_chunkwise_plan's workspace_bytes) returns RET_EWORKSPACE with no
+ * launch.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current), so make that first call
+ * before any stream capture.  All calls share the one array and it keeps
+ * whatever the previous call left; every kernel that reads it writes it
+ * first, so nothing needs clearing, but calls that can overlap on the GPU
+ * (different streams, or different host threads) race on it: serialise them.
+ * The call itself allocates nothing.
+ * ------------------------------------------------------------------------ */
+#define RET_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                                 const float* gamma, const float* theta,
+                                 int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                                 const float* state_in, float* state_out,
+                                 void* out, ret_dtype out_dt, const ret_gn* gn,
+                                 cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
  * ret_chunkwise_scan — the same result as ret_chunkwise, computed in the
  * parallel-then-scan layout: every chunk's ΔS_i from zero (all chunks in
  * parallel), an fp32 scan S_i = fmaf(γ^b, S_{i−1}, ΔS_i) over chunks, then

@@ -15,6 +15,7 @@ LIB_PATH = os.path.join(HERE, "libretention.so")
 RET_OK, RET_EINVAL, RET_EUNSUPPORTED, RET_ECUDA, RET_ETIMEOUT, RET_EWORKSPACE = range(6)
 RET_F32, RET_BF16 = 0, 1
 RET_PATH_TC, RET_PATH_SIMT = 1, 2
+RET_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 STATUS_NAMES = {
     RET_OK: "RET_OK", RET_EINVAL: "RET_EINVAL", RET_EUNSUPPORTED: "RET_EUNSUPPORTED",
@@ -33,6 +34,7 @@ _FORWARD = [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i, _i64]
 SIGNATURES = {
     "ret_chunkwise": (_i, _FORWARD + [_i, _vp, _vp, _vp, _i, C.POINTER(RetGN), _vp, _sz, _vp]),
     "ret_chunkwise_scan": (_i, _FORWARD + [_i, _vp, _vp, _vp, _i, C.POINTER(RetGN), _vp, _sz, _vp]),
+    "ret_chunkwise_noalloc": (_i, _FORWARD + [_i, _vp, _vp, _vp, _i, C.POINTER(RetGN), _vp]),
     "ret_parallel": (_i, _FORWARD + [_vp, _vp, _vp, _i, C.POINTER(RetGN), _vp, _sz, _vp]),
     "ret_chunkwise_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
     "ret_chunkwise_scan_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),

@@ -329,6 +329,30 @@ ret_status dispatch_simt_out(const void* q, const void* k, const void* v, const 
                                                ws, p, need_states, st);
 }
 
+// Scratch of ret_chunkwise_noalloc: part of this module's device image, so
+// using it allocates nothing at call time.  Its device address is looked up
+// once per device (with that device current) and cached.
+__device__ __align__(256) unsigned char g_noalloc_scratch[RET_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+ret_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RET_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return RET_EUNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return RET_ECUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return RET_OK;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -420,6 +444,23 @@ ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype 
                                     state_out, out, out_dt, gn, workspace, p, true, stream);
   return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
                                           state_out, out, out_dt, gn, workspace, p, true, stream);
+}
+
+ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                                 const float* gamma, const float* theta, int B, int H, int L,
+                                 int d_k, int d_v, int64_t pos0, int chunk,
+                                 const float* state_in, float* state_out, void* out,
+                                 ret_dtype out_dt, const ret_gn* gn, cudaStream_t stream) {
+  ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
+                              out_dt, gn);
+  if (s != RET_OK) return s;
+  if (chunk < 1) return RET_EINVAL;
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn));
+  if (p.bytes > static_cast<size_t>(RET_NOALLOC_SCRATCH_BYTES)) return RET_EWORKSPACE;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != RET_OK) return s;
+  return ret_chunkwise(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                       state_out, out, out_dt, gn, scratch, RET_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
