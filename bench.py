@@ -78,7 +78,7 @@ def kernel_source_sha():
 
 def profiled_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_msr7b_traffic.md")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_msr7b.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
@@ -93,30 +93,40 @@ def profiled_traffic(kernel):
 # Clock sampling during the timed region (NVML reads only)
 # --------------------------------------------------------------------------
 class ClockSampler:
+    """Samples the SM clock and the clock-event reasons through NVML while
+    the timed region runs (reads only; no GPU setting is touched)."""
+
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, dev_index):
-        self.samples, self.reasons, self.ok = [], 0, False
+    def __init__(self, dev_index, period_s=0.002):
+        self.samples, self.reasons, self.ok, self.err = [], 0, False, None
+        self.period = period_s
         self._stop = threading.Event()
+        self.max_mhz = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(dev_index)
+            self._reasons_fn = (getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                                or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons"))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.ok = True
-        except Exception:
-            self.max_mhz = None
+        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.err = f"{type(e).__name__}: {e}"
+
+    def _sample(self):
+        self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+        self.reasons |= int(self._reasons_fn(self.h))
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                self.reasons |= int(self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h))
-            except Exception:
-                pass
-            time.sleep(0.005)
+                self._sample()
+            except Exception as e:  # noqa: BLE001
+                self.err = f"{type(e).__name__}: {e}"
+            time.sleep(self.period)
 
     def __enter__(self):
         if self.ok:
@@ -128,13 +138,20 @@ class ClockSampler:
         if self.ok:
             self._stop.set()
             self.t.join()
+            if not self.samples:       # a very short region: take one sample after it
+                try:
+                    self._sample()
+                except Exception:  # noqa: BLE001
+                    pass
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
-                "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz,
+               "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
+               "samples": len(self.samples), "source": "nvml"}
+        if self.err:
+            out["error"] = self.err
+        return out
 
 
 # --------------------------------------------------------------------------
@@ -320,7 +337,7 @@ def main():
               "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": dgbs / peaks["hbm_gbs"], "traffic": None,
                            "peak_kind": peak_kind},
-              "clocks": dsampler.summary()}
+              "gpu_launches": dsteps, "clocks": dsampler.summary()}
     del dinp, dstate
 
     # ---------------- end to end through the API with host buffers ----------------
@@ -374,7 +391,7 @@ def main():
                          "algorithmic_bytes_per_launch": chunk_bytes(w),
                          "launch_ms": top_ms},
             "kernels_ms": {n: statistics.mean(t) for n, t in per_kernel.items()},
-            "gpu_launches": n_k + dsteps + 2 * 0,
+            "gpu_launches": n_k,
             "clocks": sampler.summary(),
             "decode": decode,
             "e2e": e2e,
