@@ -32,11 +32,11 @@ UNIT = "tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="msr7b")
-    ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--decode-steps", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -69,22 +69,23 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(files=("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh")):
     h = hashlib.sha256()
-    for f in ("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh"):
+    for f in files:
         h.update(open(os.path.join(ROOT, "linear_recurrent_sequence_prologue_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel):
+def profiled_traffic(kernel, workload="msr7b",
+                     files=("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh")):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
-    p = os.path.join(ROOT, "profiles", f"{kernel}_msr7b.md")
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(p):
         return None
     txt = open(p).read()
     m1 = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
     m2 = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not m1 or not m2 or m1.group(1) != kernel_source_sha():
+    if not m1 or not m2 or m1.group(1) != kernel_source_sha(files):
         return None
     return float(m2.group(1))
 
@@ -93,17 +94,20 @@ def profiled_traffic(kernel):
 # Clock sampling during the timed region (NVML reads only)
 # --------------------------------------------------------------------------
 class ClockSampler:
-    """Samples the SM clock and the clock-event reasons through NVML while
-    the timed region runs (reads only; no GPU setting is touched)."""
+    """Samples the SM clock and the clock-event reasons while the timed region
+    runs: through NVML when pynvml is importable, else by polling nvidia-smi
+    (reads only; no GPU setting is touched)."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown",
+                  "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, dev_index, period_s=0.002):
-        self.samples, self.reasons, self.ok, self.err = [], 0, False, None
-        self.period = period_s
+        self.samples, self.reasons, self.err = [], set(), None
+        self.dev, self.period, self.max_mhz, self.source = dev_index, period_s, None, None
         self._stop = threading.Event()
-        self.max_mhz = None
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -112,13 +116,33 @@ class ClockSampler:
             self._reasons_fn = (getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
                                 or getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons"))
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # noqa: BLE001 - reported in the JSON line
+            self.source = "nvml"
+        except Exception as e:  # noqa: BLE001
             self.err = f"{type(e).__name__}: {e}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.source, self.err = "nvidia-smi", None
+
+    def _sample_nvml(self):
+        self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+        bits = int(self._reasons_fn(self.h))
+        self.reasons |= {n for b, n in self.REASONS.items() if bits & b}
+
+    def _sample_smi(self):
+        import subprocess
+        out = subprocess.run(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                             timeout=5).stdout.strip().split(",")
+        vals = [v.strip() for v in out]
+        self.samples.append(float(vals[0]))
+        self.max_mhz = float(vals[1])
+        for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                            "sw_power_cap"), vals[2:]):
+            if v.lower() == "active":
+                self.reasons.add(name)
 
     def _sample(self):
-        self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-        self.reasons |= int(self._reasons_fn(self.h))
+        (self._sample_nvml if self.source == "nvml" else self._sample_smi)()
 
     def _run(self):
         while not self._stop.is_set():
@@ -129,26 +153,20 @@ class ClockSampler:
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
+        if self.source:
             self.t = threading.Thread(target=self._run, daemon=True)
             self.t.start()
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.source:
             self._stop.set()
             self.t.join()
-            if not self.samples:       # a very short region: take one sample after it
-                try:
-                    self._sample()
-                except Exception:  # noqa: BLE001
-                    pass
 
     def summary(self):
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-               "sm_max_mhz": self.max_mhz,
-               "reasons": [n for b, n in self.REASONS.items() if self.reasons & b],
-               "samples": len(self.samples), "source": "nvml"}
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples), "source": self.source}
         if self.err:
             out["error"] = self.err
         return out
@@ -217,6 +235,7 @@ def main():
     if args.impl == "reference":
         return run_reference(args)
 
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -247,25 +266,35 @@ def main():
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=w.chunk, state_in=s_in,
-                    out=out, gn=None, workspace=ws, return_state=False)
-
     def barrier():
         if world > 1:
             dist.barrier()
 
+    # The timed loop calls the C ABI directly with arguments marshalled once,
+    # so host-side Python work cannot leave gaps between launches.
+    import ctypes as C
+    garr = np.ascontiguousarray(inp["gamma"], np.float32)
+    tarr = np.ascontiguousarray(inp["theta"], np.float32)
+    fptr = lambda a: a.ctypes.data_as(C.POINTER(C.c_float))
+    vp = lambda t: C.c_void_p(t.data_ptr()) if t is not None else None
+    cargs = (vp(q), vp(k), vp(v), _lib.RET_BF16, fptr(garr), fptr(tarr), w.B, w.H, w.L, w.d_k,
+             w.d_v, 0, w.chunk, vp(s_in), None, vp(out), _lib.RET_BF16, None, vp(ws), ws_bytes,
+             C.c_void_p(stream.cuda_stream))
+
+    def cstep():
+        st = lib.ret_chunkwise(*cargs)
+        if st != _lib.RET_OK:
+            raise RuntimeError(f"ret_chunkwise returned {st}")
+
     for _ in range(args.warmup):
-        step()
+        cstep()
     torch.cuda.synchronize()
 
-    # per-launch events through the library's profiling hook
-    import ctypes as C
-    max_k = 8
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * max_k * args.steps)]
-    ev_handles = (C.c_void_p * len(evs))(*[C.c_void_p(e.cuda_event) if hasattr(e, "cuda_event") else None for e in evs])
-    # torch.cuda.Event creates the CUDA event lazily; record once to materialise
-    for e in evs:
+    # Per-launch events through the library's profiling hook, armed for the
+    # first steps of the timed region (it records at most 64 launches).
+    hook_steps = min(args.steps, 16)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(128)]
+    for e in evs:   # torch creates CUDA events lazily; record once to materialise
         e.record(stream)
     torch.cuda.synchronize()
     ev_handles = (C.c_void_p * len(evs))(*[C.c_void_p(e.cuda_event) for e in evs])
@@ -274,14 +303,14 @@ def main():
     sampler = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
-    names = []
     with sampler:
-        lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
         start.record(stream)
-        for _ in range(args.steps):
-            step()
+        lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+        for it in range(args.steps):
+            cstep()
+            if it + 1 == hook_steps:
+                n_k = lib.ret_profile_end()
         end.record(stream)
-        n_k = lib.ret_profile_end()
         torch.cuda.synchronize()
     names = [lib.ret_profile_kernel(i).decode() for i in range(n_k)]
     barrier()
@@ -289,6 +318,7 @@ def main():
     per_kernel = {}
     for i, nm in enumerate(names):
         per_kernel.setdefault(nm, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+    launches_per_step = n_k / hook_steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -310,10 +340,17 @@ def main():
     dstate = dinp["state"]
     dout = torch.empty((dw.B, dw.H, dw.d_v), dtype=torch.bfloat16, device=dev)
 
+    dg = np.ascontiguousarray(dinp["gamma"], np.float32)
+    dth = np.ascontiguousarray(dinp["theta"], np.float32)
+    dptrs = [(vp(dinp["q"][i]), vp(dinp["k"][i]), vp(dinp["v"][i])) for i in range(pool)]
+    dstream = C.c_void_p(stream.cuda_stream)
+
     def dstep(t):
-        i = t % pool
-        R.step(dinp["q"][i], dinp["k"][i], dinp["v"][i], dinp["gamma"], dinp["theta"], t, dstate,
-               out=dout)
+        qp_, kp_, vp_ = dptrs[t % pool]
+        st = lib.ret_step(qp_, kp_, vp_, _lib.RET_BF16, fptr(dg), fptr(dth), dw.B, dw.H, dw.d_k,
+                          dw.d_v, t, vp(dstate), vp(dout), _lib.RET_BF16, None, dstream)
+        if st != _lib.RET_OK:
+            raise RuntimeError(f"ret_step returned {st}")
 
     for t in range(max(3, args.warmup)):
         dstep(t)
@@ -335,7 +372,9 @@ def main():
                          "state_bytes": 4 * dw.B * dw.H * dw.d_k * dw.d_v,
                          "l2": "state 1.07 GB > 126 MB L2 (no flush needed)"},
               "roofline": {"bound": "hbm", "achieved": dgbs, "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": dgbs / peaks["hbm_gbs"], "traffic": None,
+                           "unit": "GB/s", "frac": dgbs / peaks["hbm_gbs"],
+                           "traffic": profiled_traffic("decode_step", "decode",
+                                                       ("kernels_simt.cuh", "common.cuh")),
                            "peak_kind": peak_kind},
               "gpu_launches": dsteps, "clocks": dsampler.summary()}
     del dinp, dstate
@@ -391,7 +430,7 @@ def main():
                          "algorithmic_bytes_per_launch": chunk_bytes(w),
                          "launch_ms": top_ms},
             "kernels_ms": {n: statistics.mean(t) for n, t in per_kernel.items()},
-            "gpu_launches": n_k,
+            "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": sampler.summary(),
             "decode": decode,
             "e2e": e2e,

@@ -17,12 +17,17 @@
 // Each CTA owns one (b·h, 128-wide d_v tile) and walks the chunks in order.
 // Transposed products keep d_v on the 128 TMEM lanes:
 //   P̂   [j × m]      = Q′ · K̂′ᵀ          A = Q′ (smem, K-major), B = K̂′ (K-major)
+//   ΔSᵀ [v × k]      = Vᵀ · K̂′           A = Vᵀ (MN-major),      B = K̂′ (MN-major)
 //   Õᵀ  [v × j]      = Ŝᵀ · Q′ᵀ          A = Ŝᵀ (TMEM, bf16),    B = Q′ (K-major)
 //   Õᵀ  [v × j]     += Vᵀ · P̂ᵀ           A = Vᵀ (MN-major),      B = P̂ (K-major)
-//   ΔSᵀ [v × k]      = Vᵀ · K̂′           A = Vᵀ (MN-major),      B = K̂′ (MN-major)
-// TMEM (512 columns): Õᵀ [0,128), P̂ [128,256), ΔSᵀ piece [256,384),
-// Ŝᵀ bf16 [384, 384 + d_k/2).  The fp32 master state Sᵀ lives in the
-// registers of the 16 drain warps (d_k/4 values per thread).
+// issued in that order for every chunk.  TMEM columns: X = [0, 128) holds P̂
+// and then, once P̂ has been read out, Õᵀ; D = [128, 128 + d_k) holds the
+// whole ΔSᵀ; SH = [128 + d_k, 128 + 3d_k/2) holds Ŝᵀ in bf16 pairs.  The
+// fp32 master state Sᵀ lives in the registers of the 16 drain warps (d_k/4
+// values per thread).  Every drain releases its TMEM region as soon as its
+// tcgen05.ld has completed, before the arithmetic and the stores, and ΔSᵀ
+// takes one MMA per chunk, so K̂′ is free right after the second product
+// and the next chunk's K̂′ load overlaps the last two products.
 #pragma once
 
 #include "common.cuh"
@@ -40,18 +45,24 @@ constexpr int NWARPS = NCW + 2;       // + TMA producer + MMA issuer
 constexpr int NTHREADS = NWARPS * 32;
 
 enum Bar : int {
-  Q_FULL = 0, K_FULL_LO, K_FULL_HI, V_FULL,
-  Q_EMPTY, K_EMPTY_LO, K_EMPTY_HI, V_EMPTY,
-  P_FULL, P_FREE, DS_FULL, DS_FREE, O_FULL, O_FREE, S_INIT, MMA_DONE, NBAR_
+  Q_FULL = 0, K_FULL, V_FULL,         // TMA → MMA
+  Q_EMPTY, K_EMPTY, V_EMPTY,          // MMA → TMA
+  P_FULL,                             // QK done            (MMA → drain)
+  X_READ,                             // P̂ read out of X     (drain → MMA)
+  P_SMEM,                             // P̂ in shared memory  (drain → MMA)
+  DS_FULL,                            // ΔS done            (MMA → drain)
+  DS_FREE,                            // ΔS read out of D    (drain → MMA)
+  SH_FREE,                            // QS done, Ŝ may be rewritten (MMA → drain)
+  SH_READY,                           // Ŝ written          (drain → MMA)
+  O_FULL,                             // PV done            (MMA → drain)
+  X_FREE,                             // Õ read out of X     (drain → MMA)
+  MMA_DONE, NBAR_
 };
 
 template <int DK>
 struct Cfg {
   static_assert(DK == 64 || DK == 128 || DK == 256, "d_k");
   static constexpr int QBOX = DK / 64;            // 64-column boxes of Q′ / K̂′
-  static constexpr int NPIECE = DK > 128 ? 2 : 1; // ΔS pieces (N ≤ 128 each)
-  static constexpr int PN = DK / NPIECE;
-  static constexpr int LOBOX = PN / 64;           // K boxes of piece 0
   static constexpr int SPT = DK / 4;              // state values per drain thread
   static constexpr uint32_t BOX = CH * 64 * 2;    // 16 KB
   static constexpr uint32_t Q_BYTES = CH * DK * 2;
@@ -66,7 +77,8 @@ struct Cfg {
   static constexpr uint32_t OFF_TPTR = OFF_BAR + NBAR_ * 8;
   static constexpr uint32_t USED = OFF_TPTR + 16;
   static constexpr uint32_t SMEM_BYTES = USED + 1024;   // slack for 1024-B alignment
-  static constexpr uint32_t T_O = 0, T_P = 128, T_DS = 256, T_SH = 384;
+  static constexpr uint32_t T_X = 0, T_D = 128, T_SH = 128 + DK;
+  static constexpr uint32_t T_COLS = (128 + DK + DK / 2) <= 256 ? 256 : 512;
 };
 
 struct ChunkArgs {
@@ -118,6 +130,9 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
 
 // ---------------------------------------------------------------------------
 // Main kernel.  grid = (d_v / 128, B·H); block = 576 threads; 1 CTA per SM.
+// Warp 0: TMA producer.  Warp 1: MMA issuer.  Warps 2..17: drain warps; the
+// drain warp with hardware warp id w reads TMEM lanes 32·(w % 4) … +31
+// (v for Õᵀ/ΔSᵀ/Ŝᵀ, j for P̂) and handles column slice (w − 2) / 4.
 // ---------------------------------------------------------------------------
 template <int DK>
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -144,12 +159,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    const uint32_t counts[NBAR_] = {1, 1, 1, 1, 1, 1, 1, 1, 1, NCW, 1, NCW / C::NPIECE, 1, NCW, NCW, 1};
-    for (int i = 0; i < NBAR_; ++i) mbar_init(bar(i), counts[i]);
+    for (int i = 0; i < NBAR_; ++i) {
+      const bool from_drain = (i == X_READ || i == P_SMEM || i == DS_FREE || i == SH_READY ||
+                               i == X_FREE);
+      mbar_init(bar(i), from_drain ? NCW : 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(sb + C::OFF_TPTR, 512);
+    tmem_alloc(sb + C::OFF_TPTR, C::T_COLS);
     tmem_relinquish();
   }
   if (threadIdx.x < CH) omega[threadIdx.x] = gpow(cc.lg2g[h], static_cast<float>(static_cast<int>(threadIdx.x) + 1 - CH));
@@ -160,109 +178,82 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ---------------------------
+    // Buffers free up in the order K̂′ (after ΔS), Q′ (after QS), V (after PV).
     if (lane == 0) {
       int issued = -1;   // last chunk whose loads were all issued
       for (int i = 0; i < nch; ++i) {
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
         const int y = bh * L + i * CH;
-        if (i > 0 && !mbar_wait(bar(K_EMPTY_LO), pp, 0x101)) break;
-        mbar_arrive_expect_tx(bar(K_FULL_LO), C::LOBOX * C::BOX);
-        for (int b = 0; b < C::LOBOX; ++b) tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL_LO));
+        if (i > 0 && !mbar_wait(bar(K_EMPTY), pp, 0x101)) break;
+        mbar_arrive_expect_tx(bar(K_FULL), C::Q_BYTES);
+        for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL));
         if (i > 0 && !mbar_wait(bar(Q_EMPTY), pp, 0x102)) break;
         mbar_arrive_expect_tx(bar(Q_FULL), C::Q_BYTES);
         for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sQ + b * C::BOX, &tm_q, 64 * b, y, bar(Q_FULL));
-        if constexpr (C::NPIECE == 2) {
-          if (i > 0 && !mbar_wait(bar(K_EMPTY_HI), pp, 0x103)) break;
-          mbar_arrive_expect_tx(bar(K_FULL_HI), (C::QBOX - C::LOBOX) * C::BOX);
-          for (int b = C::LOBOX; b < C::QBOX; ++b)
-            tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL_HI));
-        }
-        if (i > 0 && !mbar_wait(bar(V_EMPTY), pp, 0x104)) break;
+        if (i > 0 && !mbar_wait(bar(V_EMPTY), pp, 0x103)) break;
         mbar_arrive_expect_tx(bar(V_FULL), C::V_BYTES);
         for (int b = 0; b < 2; ++b) tma_load_2d(sV + b * C::BOX, &tm_v, v0 + 64 * b, y, bar(V_FULL));
         issued = i;
       }
-      // Never leave the CTA with bulk copies still landing in its shared
-      // memory: wait (bounded) until the last issued chunk has arrived.
       if (issued >= 0 && status_aborted()) {
         const uint32_t pl = static_cast<uint32_t>(issued) & 1u;
-        mbar_wait(bar(K_FULL_LO), pl, 0x1f1, kWaitBudgetCycles / 8);
+        mbar_wait(bar(K_FULL), pl, 0x1f1, kWaitBudgetCycles / 8);
         mbar_wait(bar(Q_FULL), pl, 0x1f2, kWaitBudgetCycles / 8);
-        if (C::NPIECE == 2) mbar_wait(bar(K_FULL_HI), pl, 0x1f3, kWaitBudgetCycles / 8);
-        mbar_wait(bar(V_FULL), pl, 0x1f4, kWaitBudgetCycles / 8);
+        mbar_wait(bar(V_FULL), pl, 0x1f3, kWaitBudgetCycles / 8);
       }
     }
   } else if (warp == 1) {
     // ------------------------------ MMA issuer -----------------------------
     if (lane == 0) {
-      const uint32_t tO = tmem + C::T_O, tP = tmem + C::T_P, tDS = tmem + C::T_DS,
-                     tSH = tmem + C::T_SH;
+      const uint32_t tX = tmem + C::T_X, tD = tmem + C::T_D, tSH = tmem + C::T_SH;
       constexpr uint32_t ID_P = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t ID_QS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, 128, 1, 0);
-      constexpr uint32_t ID_KV = idesc_bf16_f32(128, C::PN, 1, 1);
-      auto kv_piece = [&](int p) {
-        for (int s = 0; s < CH / 16; ++s) {
-          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
-          const uint64_t b = sdesc_sw128(sK + (p * C::LOBOX) * C::BOX + s * 2048, C::BOX, 1024);
-          mma_ss(tDS, a, b, ID_KV, s > 0 ? 1u : 0u);
-        }
-      };
+      constexpr uint32_t ID_KV = idesc_bf16_f32(128, DK, 1, 1);
       for (int i = 0; i < nch; ++i) {
         const uint32_t pi = static_cast<uint32_t>(i) & 1u;
-        // A: P̂ = Q′ K̂′ᵀ
-        if (!mbar_wait(bar(Q_FULL), pi, 0x201)) break;
-        if (!mbar_wait(bar(K_FULL_LO), pi, 0x202)) break;
+        const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
+        // 1. P̂ = Q′ K̂′ᵀ into X (needs Õ of the previous chunk read out)
+        if (!mbar_wait(bar(K_FULL), pi, 0x201)) break;
+        if (!mbar_wait(bar(Q_FULL), pi, 0x202)) break;
+        if (i > 0 && !mbar_wait(bar(X_FREE), pp, 0x203)) break;
         tc_fence_after();
-        bool okhi = true;
         for (int s = 0; s < DK / 16; ++s) {
-          if (C::NPIECE == 2 && s == (C::LOBOX * 4)) {
-            if (!mbar_wait(bar(K_FULL_HI), pi, 0x203)) { okhi = false; break; }
-            tc_fence_after();
-          }
           const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
-          mma_ss(tP, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), ID_P,
+          mma_ss(tX, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), ID_P,
                  s > 0 ? 1u : 0u);
         }
-        if (!okhi) break;
         mma_commit(bar(P_FULL));
-        // C: Õᵀ = Ŝᵀ Q′ᵀ  (needs the previous chunk's state and a free Õ)
-        if (i == 0) {
-          if (!mbar_wait(bar(S_INIT), 0, 0x204)) break;
-        } else {
-          const uint32_t par = static_cast<uint32_t>(i * C::NPIECE - 1) & 1u;
-          if (!mbar_wait(bar(DS_FREE), par, 0x205)) break;
-          if (!mbar_wait(bar(O_FREE), static_cast<uint32_t>(i - 1) & 1u, 0x206)) break;
+        // 2. ΔSᵀ = Vᵀ K̂′ into D (needs the previous ΔS read out)
+        if (!mbar_wait(bar(V_FULL), pi, 0x204)) break;
+        if (i > 0 && !mbar_wait(bar(DS_FREE), pp, 0x205)) break;
+        tc_fence_after();
+        for (int s = 0; s < CH / 16; ++s) {
+          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
+          const uint64_t b = sdesc_sw128(sK + s * 2048, C::BOX, 1024);
+          mma_ss(tD, a, b, ID_KV, s > 0 ? 1u : 0u);
         }
+        mma_commit(bar(DS_FULL));
+        mma_commit(bar(K_EMPTY));
+        // 3. Õᵀ = Ŝᵀ Q′ᵀ into X (needs P̂ read out and Ŝ of the previous chunk)
+        if (!mbar_wait(bar(X_READ), pi, 0x206)) break;
+        if (!mbar_wait(bar(SH_READY), pi, 0x207)) break;
         tc_fence_after();
         for (int s = 0; s < DK / 16; ++s) {
           const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
-          mma_ts(tO, tSH + s * 8, sdesc_sw128(sQ + off, 16, 1024), ID_QS, s > 0 ? 1u : 0u);
+          mma_ts(tX, tSH + s * 8, sdesc_sw128(sQ + off, 16, 1024), ID_QS, s > 0 ? 1u : 0u);
         }
         mma_commit(bar(Q_EMPTY));
-        // B: ΔSᵀ piece 0 = Vᵀ K̂′[:, piece 0]
-        if (!mbar_wait(bar(V_FULL), pi, 0x207)) break;
-        tc_fence_after();
-        kv_piece(0);
-        mma_commit(bar(DS_FULL));
-        mma_commit(bar(K_EMPTY_LO));
-        // E: Õᵀ += Vᵀ P̂ᵀ  (needs the masked bf16 P̂ in shared memory)
-        if (!mbar_wait(bar(P_FREE), pi, 0x208)) break;
+        mma_commit(bar(SH_FREE));
+        // 4. Õᵀ += Vᵀ P̂ᵀ (needs the masked bf16 P̂ in shared memory)
+        if (!mbar_wait(bar(P_SMEM), pi, 0x208)) break;
         tc_fence_after();
         for (int s = 0; s < CH / 16; ++s) {
           const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
           const uint64_t b = sdesc_sw128(sP + (s >> 2) * C::BOX + (s & 3) * 32, 16, 1024);
-          mma_ss(tO, a, b, ID_PV, 1u);
+          mma_ss(tX, a, b, ID_PV, 1u);
         }
         mma_commit(bar(O_FULL));
-        // D: ΔSᵀ piece 1
-        if constexpr (C::NPIECE == 2) {
-          if (!mbar_wait(bar(DS_FREE), static_cast<uint32_t>(2 * i) & 1u, 0x209)) break;
-          tc_fence_after();
-          kv_piece(1);
-          mma_commit(bar(DS_FULL));
-          mma_commit(bar(K_EMPTY_HI));
-        }
         mma_commit(bar(V_EMPTY));
       }
       // All issued MMAs must finish before TMEM is released.
@@ -275,7 +266,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
     const int cs = w >> 2;                  // 32-column slice for P̂ / Õ drains
     const int kr = w >> 2;                  // state k range [kr*SPT, kr*SPT+SPT)
-    const int piece = (kr * C::SPT) / C::PN;
     const int vl = 32 * quarter + lane;     // local v (TMEM lane) for Õ / ΔS / Ŝ
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const size_t sbase = static_cast<size_t>(bh) * DK * d_v + v0 + vl;
@@ -285,35 +275,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int u = 0; u < C::SPT; ++u)
       S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
 
+    // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
     auto write_shat = [&]() {
 #pragma unroll
-      for (int c = 0; c < C::SPT / 8; ++c) {
-        uint32_t pk[4];
+      for (int c = 0; c < C::SPT / 16; ++c) {
+        uint32_t pk[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          pk[u] = pack_bf16x2(gb * S[c * 8 + 2 * u], gb * S[c * 8 + 2 * u + 1]);
-        tmem_st4(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 8) / 2, pk);
+        for (int u = 0; u < 8; ++u)
+          pk[u] = pack_bf16x2(gb * S[c * 16 + 2 * u], gb * S[c * 16 + 2 * u + 1]);
+        tmem_st8(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 16) / 2, pk);
       }
       tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(SH_READY));
     };
     write_shat();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(S_INIT));
 
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
       const uint32_t pi = static_cast<uint32_t>(i) & 1u;
-      // ---- P̂ drain: causal mask, bf16, into the K-major swizzled tile ----
+      // ---- (a) P̂ drain: causal mask, bf16, into the K-major swizzled tile ----
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
       {
+        // 8-column groups keep the register peak low (S stays live); X is
+        // released after the last group's tcgen05.ld.
         const int j = vl;   // row of P̂ = TMEM lane
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t r[8];
-          tmem_ld8(tmem + C::T_P + lane_off + 32 * cs + 8 * g, r);
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 8 * g, r);
           tmem_ld_wait();
+          if (g == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(X_READ));
+          }
           uint32_t pk[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -327,47 +325,52 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_SMEM));
+
+      // ---- (b) ΔS drain: S = fmaf(γ^b, S, ΔS) ----
+      if (!mbar_wait(bar(DS_FULL), pi, 0x302)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::SPT / 16; ++c) {
+        uint32_t d[16];
+        tmem_ld16(tmem + C::T_D + lane_off + kr * C::SPT + c * 16, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) S[16 * c + u] = fmaf(gb, S[16 * c + u], __uint_as_float(d[u]));
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(P_FREE));
+      if (lane == 0) mbar_arrive(bar(DS_FREE));
 
-      auto drain_ds = [&](int p) -> bool {
-        if (!mbar_wait(bar(DS_FULL), static_cast<uint32_t>(i * C::NPIECE + p) & 1u, 0x302)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < C::SPT / 8; ++c) {
-          uint32_t d[8];
-          tmem_ld8(tmem + C::T_DS + lane_off + (kr * C::SPT - p * C::PN) + c * 8, d);
-          tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 8; ++u) S[c * 8 + u] = fmaf(gb, S[c * 8 + u], __uint_as_float(d[u]));
-        }
-        write_shat();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(DS_FREE));
-        return true;
-      };
-      if (piece == 0 && !drain_ds(0)) { ok = false; break; }
+      // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
+      if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
+      tc_fence_after();
+      write_shat();
 
-      // ---- Õ drain: ω_j scale, store ----
-      if (!mbar_wait(bar(O_FULL), pi, 0x303)) { ok = false; break; }
+      // ---- (d) Õ drain: release X, then ω_j scale and store ----
+      if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
       tc_fence_after();
       {
-        const size_t orow = static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs;
+        const size_t base = (static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs) * d_v + v0 + vl;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint32_t r[8];
-          tmem_ld8(tmem + C::T_O + lane_off + 32 * cs + 8 * g, r);
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 8 * g, r);
           tmem_ld_wait();
-          const size_t base = (orow + 8 * g) * d_v + v0 + vl;
+          if (g == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(X_FREE));
+          }
+          const size_t gb0 = base + static_cast<size_t>(8 * g) * d_v;
           if (args.out_f32) {
-            float* o = reinterpret_cast<float*>(args.out) + base;
+            float* o = reinterpret_cast<float*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 8 * g + c] * __uint_as_float(r[c]);
           } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + base;
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 8; ++c)
               o[static_cast<size_t>(c) * d_v] =
@@ -375,11 +378,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(O_FREE));
-
-      if (C::NPIECE == 2 && piece == 1 && !drain_ds(1)) { ok = false; break; }
     }
     if (ok && args.state_out) {
 #pragma unroll
@@ -392,7 +390,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, C::T_COLS);
   }
 }
 
