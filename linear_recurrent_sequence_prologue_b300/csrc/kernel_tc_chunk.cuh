@@ -210,6 +210,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       constexpr uint32_t ID_QS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t ID_PV = idesc_bf16_f32(128, 128, 1, 0);
       constexpr uint32_t ID_KV = idesc_bf16_f32(128, DK, 1, 1);
+      // Shared-memory descriptors are built once; every k-step adds its byte
+      // offset / 16 to the start-address field (no carry: all operands sit
+      // below 256 KB), so the unrolled issue loops cost a few integer adds
+      // per MMA and the single issuing thread keeps ahead of the tensor core.
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);      // K-major Q′
+      const uint64_t dK = sdesc_sw128(sK, 16, 1024);      // K-major K̂′
+      const uint64_t dKm = sdesc_sw128(sK, C::BOX, 1024); // MN-major K̂′
+      const uint64_t dV = sdesc_sw128(sV, C::BOX, 1024);  // MN-major V
+      const uint64_t dP = sdesc_sw128(sP, 16, 1024);      // K-major P̂
+      auto kmaj = [](int s) -> uint64_t {                 // k-step s of a K-major tile
+        return static_cast<uint64_t>(((s >> 2) * C::BOX + (s & 3) * 32) >> 4);
+      };
       for (int i = 0; i < nch; ++i) {
         const uint32_t pi = static_cast<uint32_t>(i) & 1u;
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
@@ -218,41 +230,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(bar(Q_FULL), pi, 0x202)) break;
         if (i > 0 && !mbar_wait(bar(X_FREE), pp, 0x203)) break;
         tc_fence_after();
-        for (int s = 0; s < DK / 16; ++s) {
-          const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
-          mma_ss(tX, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), ID_P,
-                 s > 0 ? 1u : 0u);
-        }
+#pragma unroll
+        for (int s = 0; s < DK / 16; ++s) mma_ss(tX, dQ + kmaj(s), dK + kmaj(s), ID_P, s > 0 ? 1u : 0u);
         mma_commit(bar(P_FULL));
         // 2. ΔSᵀ = Vᵀ K̂′ into D (needs the previous ΔS read out)
         if (!mbar_wait(bar(V_FULL), pi, 0x204)) break;
         if (i > 0 && !mbar_wait(bar(DS_FREE), pp, 0x205)) break;
         tc_fence_after();
-        for (int s = 0; s < CH / 16; ++s) {
-          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
-          const uint64_t b = sdesc_sw128(sK + s * 2048, C::BOX, 1024);
-          mma_ss(tD, a, b, ID_KV, s > 0 ? 1u : 0u);
-        }
+#pragma unroll
+        for (int s = 0; s < CH / 16; ++s)
+          mma_ss(tD, dV + static_cast<uint64_t>(s * 128), dKm + static_cast<uint64_t>(s * 128), ID_KV,
+                 s > 0 ? 1u : 0u);   // +2048 bytes (16 rows) per step
         mma_commit(bar(DS_FULL));
         mma_commit(bar(K_EMPTY));
         // 3. Õᵀ = Ŝᵀ Q′ᵀ into X (needs P̂ read out and Ŝ of the previous chunk)
         if (!mbar_wait(bar(X_READ), pi, 0x206)) break;
         if (!mbar_wait(bar(SH_READY), pi, 0x207)) break;
         tc_fence_after();
-        for (int s = 0; s < DK / 16; ++s) {
-          const uint32_t off = (s >> 2) * C::BOX + (s & 3) * 32;
-          mma_ts(tX, tSH + s * 8, sdesc_sw128(sQ + off, 16, 1024), ID_QS, s > 0 ? 1u : 0u);
-        }
+#pragma unroll
+        for (int s = 0; s < DK / 16; ++s) mma_ts(tX, tSH + s * 8, dQ + kmaj(s), ID_QS, s > 0 ? 1u : 0u);
         mma_commit(bar(Q_EMPTY));
         mma_commit(bar(SH_FREE));
         // 4. Õᵀ += Vᵀ P̂ᵀ (needs the masked bf16 P̂ in shared memory)
         if (!mbar_wait(bar(P_SMEM), pi, 0x208)) break;
         tc_fence_after();
-        for (int s = 0; s < CH / 16; ++s) {
-          const uint64_t a = sdesc_sw128(sV + s * 2048, C::BOX, 1024);
-          const uint64_t b = sdesc_sw128(sP + (s >> 2) * C::BOX + (s & 3) * 32, 16, 1024);
-          mma_ss(tX, a, b, ID_PV, 1u);
-        }
+#pragma unroll
+        for (int s = 0; s < CH / 16; ++s)
+          mma_ss(tX, dV + static_cast<uint64_t>(s * 128), dP + kmaj(s), ID_PV, 1u);
         mma_commit(bar(O_FULL));
         mma_commit(bar(V_EMPTY));
       }
@@ -299,29 +303,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
       {
-        // 8-column groups keep the register peak low (S stays live); X is
-        // released after the last group's tcgen05.ld.
+        // Two rounds of two 8-column loads per wait keep the register peak low
+        // (S stays live) while halving the TMEM round trips; X is released
+        // after the last load.
         const int j = vl;   // row of P̂ = TMEM lane
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t r[8];
-          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 8 * g, r);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[16];
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&r[8]));
           tmem_ld_wait();
-          if (g == 3) {
+          if (hf == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(X_READ));
           }
-          uint32_t pk[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int m = 32 * cs + 8 * g + 2 * u;
-            const float a = (m <= j) ? __uint_as_float(r[2 * u]) : 0.f;
-            const float b = (m + 1 <= j) ? __uint_as_float(r[2 * u + 1]) : 0.f;
-            pk[u] = pack_bf16x2(a, b);
+          for (int g = 0; g < 2; ++g) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int m = 32 * cs + 16 * hf + 8 * g + 2 * u;
+              const float a = (m <= j) ? __uint_as_float(r[8 * g + 2 * u]) : 0.f;
+              const float b = (m + 1 <= j) ? __uint_as_float(r[8 * g + 2 * u + 1]) : 0.f;
+              pk[u] = pack_bf16x2(a, b);
+            }
+            const int m0 = 32 * cs + 16 * hf + 8 * g;
+            st_shared_v4(sP + (m0 >> 6) * C::BOX + sw128_offset(j, m0 & 63), pk[0], pk[1], pk[2], pk[3]);
           }
-          const int m0 = 32 * cs + 8 * g;
-          st_shared_v4(sP + (m0 >> 6) * C::BOX + sw128_offset(j, m0 & 63), pk[0], pk[1], pk[2], pk[3]);
         }
       }
       fence_proxy_async_smem();
@@ -354,27 +363,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       {
         const size_t base = (static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs) * d_v + v0 + vl;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint32_t r[8];
-          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 8 * g, r);
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[16];
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&r[8]));
           tmem_ld_wait();
-          if (g == 3) {
+          if (hf == 1) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(X_FREE));
           }
-          const size_t gb0 = base + static_cast<size_t>(8 * g) * d_v;
+          const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
           if (args.out_f32) {
             float* o = reinterpret_cast<float*>(args.out) + gb0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 8 * g + c] * __uint_as_float(r[c]);
+            for (int c = 0; c < 16; ++c)
+              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]);
           } else {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
+            for (int c = 0; c < 16; ++c)
               o[static_cast<size_t>(c) * d_v] =
-                  __float2bfloat16_rn(omega[32 * cs + 8 * g + c] * __uint_as_float(r[c]));
+                  __float2bfloat16_rn(omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]));
           }
         }
       }
