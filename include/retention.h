@@ -142,7 +142,9 @@ ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, re
  * parallel), an fp32 scan S_i = fmaf(γ^b, S_{i−1}, ΔS_i) over chunks, then
  * every chunk's outputs from its entering state (all chunks in parallel).
  * Arguments as ret_chunkwise; the workspace holds one d_k×d_v fp32 state per
- * (b, h, chunk).
+ * (b, h, chunk) (ret_chunkwise_scan_plan gives its size).  On both kernel
+ * paths the two layouts run the same tile arithmetic in the same order, so
+ * state_out and out are bit-identical to ret_chunkwise's.
  * ------------------------------------------------------------------------ */
 ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_dtype in_dt,
                               const float* gamma, const float* theta,

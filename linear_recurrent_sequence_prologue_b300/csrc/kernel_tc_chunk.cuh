@@ -84,9 +84,13 @@ struct Cfg {
 struct ChunkArgs {
   const float* state_in;   // [BH][DK][d_v] or nullptr
   float* state_out;        // or nullptr
-  void* out;               // [BH][L][d_v] bf16, or fp32 when out_f32
+  void* out;               // [BH][L][d_v] bf16, or fp32 when out_f32; nullptr: no output
   int out_f32;
   int H, L, d_v, nchunks;
+  // Chunk-parallel layout: the rows of grid.y are (sequence, chunk) pairs of
+  // one chunk each, head = (blockIdx.y / seq_div) % H.  raw_ds: state_out
+  // receives the chunk's ΔS itself instead of fmaf(γ^b, S, ΔS).
+  int seq_div, raw_ds;
 };
 
 // ---------------------------------------------------------------------------
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
   const int bh = blockIdx.y;
-  const int h = bh % args.H;
+  const int h = (bh / args.seq_div) % args.H;
   const int L = args.L, d_v = args.d_v, nch = args.nchunks;
   const float gb = cc.gb[h];
 
@@ -346,7 +350,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld16(tmem + C::T_D + lane_off + kr * C::SPT + c * 16, d);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) S[16 * c + u] = fmaf(gb, S[16 * c + u], __uint_as_float(d[u]));
+        for (int u = 0; u < 16; ++u)
+          S[16 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gb, S[16 * c + u], __uint_as_float(d[u]));
       }
       tc_fence_before();
       __syncwarp();
@@ -374,7 +379,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(bar(X_FREE));
           }
           const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
-          if (args.out_f32) {
+          if (!args.out) {
+          } else if (args.out_f32) {
             float* o = reinterpret_cast<float*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 16; ++c)

@@ -167,7 +167,7 @@ struct Plan {
 };
 
 Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k, int d_v,
-                    int chunk, bool gn) {
+                    int chunk, bool gn, bool scan = false) {
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   const int nch = (L + chunk - 1) / chunk;
@@ -176,6 +176,7 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
     p.path = RET_PATH_TC;
     p.off_q = off; off += up256(BH * L * d_k * 2);
     p.off_k = off; off += up256(BH * L * d_k * 2);
+    if (scan) { p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4); }
   } else {
     p.path = RET_PATH_SIMT;
     p.off_q = off; off += up256(BH * L * d_k * 4);
@@ -261,11 +262,17 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
   return last_launch();
 }
 
+// scan = false: one CTA walks all chunks of its (b, h), carrying the state.
+// scan = true: chunk-parallel layout — every chunk's ΔS from zero (one CTA
+// per chunk), the fp32 scan over chunks, then every chunk's outputs from its
+// entering state.  Both run the same kernel code, so state and outputs agree
+// bit for bit.
 template <typename Tout>
 ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                         const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
                         int64_t pos0, const float* s_in, float* s_out, Tout* out,
-                        const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st) {
+                        const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st,
+                        bool scan = false) {
   const int BH = B * H;
   __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
@@ -280,6 +287,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   if (!make_map(&mq, qr, rows, d_k) || !make_map(&mk, kr, rows, d_k) || !make_map(&mv, v, rows, d_v))
     return RET_ECUDA;
   float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
+  const int nch = L / tcc::CH;
   tcc::ChunkArgs a;
   a.state_in = s_in;
   a.state_out = s_out;
@@ -288,20 +296,55 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   a.H = H;
   a.L = L;
   a.d_v = d_v;
-  a.nchunks = L / tcc::CH;
-  dim3 grid(d_v / tcc::VT, BH);
-  auto launch = [&](auto kern, uint32_t smem) -> cudaError_t {
+  a.nchunks = nch;
+  a.seq_div = 1;
+  a.raw_ds = 0;
+  auto launch = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args, int rows,
+                    const char* name) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    Mark m("chunk_tc", st);
-    kern<<<grid, tcc::NTHREADS, smem, st>>>(mq, mk, mv, a, cc);
+    Mark m(name, st);
+    kern<<<dim3(d_v / tcc::VT, rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
     return cudaGetLastError();
   };
+  auto run = [&](const tcc::ChunkArgs& args, int rows, const char* name) -> cudaError_t {
+    if (d_k == 256) return launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name);
+    if (d_k == 128) return launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
+    return launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
+  };
   cudaError_t e;
-  if (d_k == 256) e = launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES);
-  else if (d_k == 128) e = launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES);
-  else e = launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES);
+  if (!scan) {
+    e = run(a, BH, "chunk_tc");
+  } else {
+    // The [BH, L, d] tensors viewed as [BH·nch, 128, d]: one chunk per row.
+    float* states = wsp<float>(ws, p.off_states);
+    tcc::ChunkArgs d = a;
+    d.L = tcc::CH;
+    d.nchunks = 1;
+    d.seq_div = nch;
+    d.raw_ds = 1;
+    d.state_in = nullptr;
+    d.state_out = states;   // ΔS of every chunk
+    d.out = nullptr;
+    e = run(d, BH * nch, "chunk_tc_dS");
+    if (e == cudaSuccess) {
+      const size_t n = static_cast<size_t>(BH) * d_k * d_v;
+      Mark m("state_scan", st);
+      simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+          states, s_in, s_out, cc, H, d_k, d_v, nch, BH);
+      e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) {
+      tcc::ChunkArgs o = a;
+      o.L = tcc::CH;
+      o.nchunks = 1;
+      o.seq_div = nch;
+      o.state_in = states;    // state entering every chunk
+      o.state_out = nullptr;
+      e = run(o, BH * nch, "chunk_tc_out");
+    }
+  }
   if (e != cudaSuccess) return RET_ECUDA;
   if (ofp) {
     const size_t r = static_cast<size_t>(BH) * L;
@@ -414,18 +457,23 @@ ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H,
   return RET_OK;
 }
 
-ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype in_dt,
-                         const float* gamma, const float* theta, int B, int H, int L, int d_k,
-                         int d_v, int64_t pos0, int chunk, const float* state_in,
-                         float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
-                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// Shared body of ret_chunkwise (scan = false) and ret_chunkwise_scan (true).
+ret_status chunkwise_impl(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                          const float* gamma, const float* theta, int B, int H, int L, int d_k,
+                          int d_v, int64_t pos0, int chunk, const float* state_in,
+                          float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                          bool scan) {
   ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
                               out_dt, gn);
   if (s != RET_OK) return s;
   if (chunk < 1) return RET_EINVAL;
   CallConsts cc;
   if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
-  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn));
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), scan);
   if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes || !al16(workspace)))
     return RET_EWORKSPACE;
   if (p.path == RET_PATH_TC) {
@@ -434,16 +482,29 @@ ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype 
     const auto* vv = static_cast<const __nv_bfloat16*>(v);
     if (out_dt == RET_F32)
       return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
-                                 static_cast<float*>(out), gn, workspace, p, stream);
+                                 static_cast<float*>(out), gn, workspace, p, stream, scan);
     return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
                                        state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
-                                       p, stream);
+                                       p, stream, scan);
   }
+  // The fp32 kernels always run in the chunk-parallel layout.
   if (in_dt == RET_F32)
     return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
                                     state_out, out, out_dt, gn, workspace, p, true, stream);
   return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
                                           state_out, out, out_dt, gn, workspace, p, true, stream);
+}
+}  // namespace
+
+extern "C" {
+
+ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                         const float* gamma, const float* theta, int B, int H, int L, int d_k,
+                         int d_v, int64_t pos0, int chunk, const float* state_in,
+                         float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                        state_out, out, out_dt, gn, workspace, workspace_bytes, stream, false);
 }
 
 ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, ret_dtype in_dt,
@@ -466,10 +527,16 @@ ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, re
 ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
                                    int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
                                    int* path, size_t* workspace_bytes) {
-  if (in_dt == RET_BF16 && tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk))
-    return RET_EUNSUPPORTED;
-  return ret_chunkwise_plan(in_dt, gamma, B, H, L, d_k, d_v, chunk, out_dt, gn_enabled, path,
-                            workspace_bytes);
+  if (!path || !workspace_bytes) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || chunk < 1)
+    return RET_EINVAL;
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_enabled != 0, true);
+  *path = p.path;
+  *workspace_bytes = p.bytes;
+  return RET_OK;
 }
 
 ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_dtype in_dt,
@@ -477,10 +544,8 @@ ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_d
                               int d_k, int d_v, int64_t pos0, int chunk, const float* state_in,
                               float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-  // The fp32 path of ret_chunkwise already runs in the chunk-parallel layout.
-  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk)) return RET_EUNSUPPORTED;
-  return ret_chunkwise(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
-                       state_out, out, out_dt, gn, workspace, workspace_bytes, stream);
+  return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                        state_out, out, out_dt, gn, workspace, workspace_bytes, stream, true);
 }
 
 ret_status ret_parallel_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,

@@ -129,6 +129,12 @@ def test_path_selection(lib):
     p, nb = _plan(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128)
     assert p == _lib.RET_PATH_TC
     assert nb == 2 * 2 * 16 * 8192 * 256 * 2
+    # the chunk-parallel layout adds one fp32 d_k×d_v state per (b, h, chunk)
+    path, nb2 = C.c_int(0), C.c_size_t(0)
+    assert lib.ret_chunkwise_scan_plan(_lib.RET_BF16, None, 2, 16, 8192, 256, 512, 128,
+                                       _lib.RET_BF16, 0, C.byref(path), C.byref(nb2)) == _lib.RET_OK
+    assert path.value == _lib.RET_PATH_TC
+    assert nb2.value == nb + 2 * 16 * 64 * 256 * 512 * 4
     # fp32 inputs, chunk 64, d_v 64 → fp32 kernels
     assert _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)[0] == _lib.RET_PATH_SIMT
     assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64)[0] == _lib.RET_PATH_SIMT

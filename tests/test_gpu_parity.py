@@ -189,6 +189,27 @@ def test_split_call_consistency_tc():
     assert torch.equal(sb, s)
 
 
+@pytest.mark.parametrize("d_k,d_v,L,H", [(64, 128, 384, 2), (256, 512, 512, 2)])
+def test_tc_scan_layout_is_bit_identical_to_carry(d_k, d_v, L, H):
+    """Chunk-parallel layout (ΔS per chunk, fp32 scan, outputs from entering
+    states) against the carried-state layout: same state and outputs, bit for bit."""
+    w, inp = _custom(2, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1, seed=d_k + 7)
+    path, _ = R.plan("chunkwise_scan", torch.bfloat16, 2, H, L, d_k, d_v, 128, gamma=inp["gamma"])
+    assert path == R.RET_PATH_TC
+    d = _cuda(inp)
+    for odt in (torch.bfloat16, torch.float32):
+        o1, s1 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=9,
+                             state_in=d["state_in"], out_dtype=odt)
+        o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=9,
+                             state_in=d["state_in"], out_dtype=odt, layout="scan")
+        assert R.sync_status() == R.RET_OK
+        assert torch.equal(s1, s2)
+        assert torch.equal(o1, o2)
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", 128, pos0=9)
+    assert_close(gpu_np(o2), ref_o, torch.bfloat16, "scan out")
+    assert_close(gpu_np(s2), ref_s, torch.bfloat16, "scan state")
+
+
 # -------------------------------------------------------- full workloads --
 def test_msr1p3b_groupnorm_sampled_heads():
     w = WORKLOADS["msr1p3b"]
@@ -210,6 +231,12 @@ def test_msr7b_sampled_heads():
     o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
                        state_in=d["state_in"])
     assert R.sync_status() == R.RET_OK
+    # full size: the chunk-parallel layout returns the same bits
+    o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
+                         state_in=d["state_in"], layout="scan")
+    assert R.sync_status() == R.RET_OK
+    assert torch.equal(s, s2) and torch.equal(o, o2)
+    del o2, s2
     for b, h in ((0, 0), (1, 15)):
         q, k, v, si, g, th = head_slice(inp, b, h)
         ref_o, ref_s = O.retention(q, k, v, g, th, 0, si, "chunkwise", w.chunk)
