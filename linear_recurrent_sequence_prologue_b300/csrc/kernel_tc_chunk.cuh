@@ -96,39 +96,57 @@ struct ChunkArgs {
 // ---------------------------------------------------------------------------
 // Front pass: Q′ = R(nθ)q and K̂′ = d_k^{-1/2}·ζ_{t mod b}·R(nθ)k in bf16.
 // Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by all
-// B·H heads of that row.
+// B·H heads of that row, eight heads' loads in flight at a time; raw q and
+// k are read with the evict-first hint.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rotate_qk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ qo, __nv_bfloat16* __restrict__ ko, CallConsts cc, int BH,
     int H, int L, int d, float pos0, int chunk) {
+  constexpr int U = 8;   // heads in flight per thread (the pass is HBM-bound)
   const int vecs = d / 8;
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (idx >= static_cast<size_t>(L) * vecs) return;
-  const int t = static_cast<int>(idx / vecs), cidx = static_cast<int>(idx % vecs);
+  // Positions are walked last to first, so the first chunks the main kernel
+  // reads are the last ones written and are still in L2.
+  const int tt = static_cast<int>(idx / vecs), cidx = static_cast<int>(idx % vecs);
+  const int t = L - 1 - tt;
   float c[4], s[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cidx + u], c[u], s[u]);
   const float e = static_cast<float>(chunk - 1 - (t % chunk));
-  for (int bh = 0; bh < BH; ++bh) {
-    const int h = bh % H;
-    const float zk = cc.kscale * gpow(cc.lg2g[h], e);
-    const size_t off = (static_cast<size_t>(bh) * L + t) * d + 8 * cidx;
-    const uint4 qv = *reinterpret_cast<const uint4*>(q + off);
-    const uint4 kv = *reinterpret_cast<const uint4*>(k + off);
-    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w};
-    const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
-    uint32_t qr[4], kr[4];
+  const size_t hstride = static_cast<size_t>(L) * d;   // elements between heads
+  const size_t off0 = static_cast<size_t>(t) * d + 8 * cidx;
+  for (int bh0 = 0; bh0 < BH; bh0 += U) {
+    uint4 qv[U], kv[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
-      qr[u] = pack_bf16x2(a * c[u] - b * s[u], fmaf(a, s[u], b * c[u]));
-      const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
-      const float cz = zk * c[u], sz = zk * s[u];
-      kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
+    for (int uu = 0; uu < U; ++uu) {
+      if (bh0 + uu < BH) {
+        const size_t off = off0 + static_cast<size_t>(bh0 + uu) * hstride;
+        qv[uu] = __ldcs(reinterpret_cast<const uint4*>(q + off));
+        kv[uu] = __ldcs(reinterpret_cast<const uint4*>(k + off));
+      }
     }
-    *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
-    *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
+#pragma unroll
+    for (int uu = 0; uu < U; ++uu) {
+      const int bh = bh0 + uu;
+      if (bh >= BH) break;
+      const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
+      const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
+      const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
+      uint32_t qr[4], kr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
+        qr[u] = pack_bf16x2(a * c[u] - b * s[u], fmaf(a, s[u], b * c[u]));
+        const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
+        const float cz = zk * c[u], sz = zk * s[u];
+        kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
+      }
+      const size_t off = off0 + static_cast<size_t>(bh) * hstride;
+      *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
+      *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
+    }
   }
 }
 
