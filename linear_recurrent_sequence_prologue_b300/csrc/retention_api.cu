@@ -15,6 +15,7 @@
 #include "tc_primitives.cuh"
 #include "kernels_simt.cuh"
 #include "kernel_tc_chunk.cuh"
+#include "kernel_tc_parallel.cuh"
 
 using namespace ret;
 
@@ -166,13 +167,18 @@ struct Plan {
   size_t off_q = 0, off_k = 0, off_states = 0, off_ofp32 = 0;
 };
 
+// Grid rows of the tensor-core launches: B·H (carry layout) or B·H·L/128
+// (one chunk per row) must fit gridDim.y.
+constexpr size_t kMaxGridRows = 65535;
+
 Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k, int d_v,
                     int chunk, bool gn, bool scan = false) {
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   const int nch = (L + chunk - 1) / chunk;
   size_t off = 0;
-  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk)) {
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk) &&
+      (scan ? BH * nch : BH) <= kMaxGridRows) {
     p.path = RET_PATH_TC;
     p.off_q = off; off += up256(BH * L * d_k * 2);
     p.off_k = off; off += up256(BH * L * d_k * 2);
@@ -188,10 +194,26 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
   return p;
 }
 
-Plan plan_parallel(int B, int H, int L, int d_k, int d_v, bool gn, bool want_state) {
+Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k, int d_v,
+                   bool gn, bool want_state) {
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   size_t off = 0;
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && BH <= kMaxGridRows &&
+      static_cast<size_t>(L / tcc::CH) <= kMaxGridRows &&
+      (!want_state || BH * (L / tcc::CH) <= kMaxGridRows)) {
+    // rotated Q′ / K̂′ in bf16; per-block ΔS states when state_out is wanted
+    p.path = RET_PATH_TC;
+    p.off_q = off; off += up256(BH * L * d_k * 2);
+    p.off_k = off; off += up256(BH * L * d_k * 2);
+    if (want_state) {
+      p.off_states = off;
+      off += up256(BH * (L / tcc::CH) * static_cast<size_t>(d_k) * d_v * 4);
+    }
+    if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
+    p.bytes = off;
+    return p;
+  }
   p.path = RET_PATH_SIMT;
   p.off_q = off; off += up256(BH * L * d_k * 4);
   p.off_k = off; off += up256(BH * L * d_k * 4);
@@ -267,12 +289,14 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
 // per chunk), the fp32 scan over chunks, then every chunk's outputs from its
 // entering state.  Both run the same kernel code, so state and outputs agree
 // bit for bit.
+// parallel = true (ret_parallel): the parallel-form kernel computes the
+// outputs, and state_out (if wanted) comes from the ΔS + scan steps.
 template <typename Tout>
 ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
                         const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
                         int64_t pos0, const float* s_in, float* s_out, Tout* out,
                         const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st,
-                        bool scan = false) {
+                        bool scan = false, bool parallel = false) {
   const int BH = B * H;
   __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
@@ -313,8 +337,46 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     if (d_k == 128) return launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
     return launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
   };
-  cudaError_t e;
-  if (!scan) {
+  cudaError_t e = cudaSuccess;
+  if (parallel) {
+    tcp::ParArgs pa;
+    pa.state_in = s_in;
+    pa.out = a.out;
+    pa.out_f32 = a.out_f32;
+    pa.H = H;
+    pa.L = L;
+    pa.d_v = d_v;
+    auto plaunch = [&](auto kern, uint32_t smem) -> cudaError_t {
+      cudaError_t e2 = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            static_cast<int>(smem));
+      if (e2 != cudaSuccess) return e2;
+      Mark m("parallel_tc", st);
+      kern<<<dim3(d_v / tcp::VT, BH, nch), tcp::NTHREADS, smem, st>>>(mq, mk, mv, pa, cc);
+      return cudaGetLastError();
+    };
+    if (d_k == 256) e = plaunch(tcp::parallel_tc_kernel<256>, tcp::Cfg<256>::SMEM_BYTES);
+    else if (d_k == 128) e = plaunch(tcp::parallel_tc_kernel<128>, tcp::Cfg<128>::SMEM_BYTES);
+    else e = plaunch(tcp::parallel_tc_kernel<64>, tcp::Cfg<64>::SMEM_BYTES);
+    if (e == cudaSuccess && s_out) {   // closed-form final state: ΔS per block, then the scan
+      float* states = wsp<float>(ws, p.off_states);
+      tcc::ChunkArgs d = a;
+      d.L = tcc::CH;
+      d.nchunks = 1;
+      d.seq_div = nch;
+      d.raw_ds = 1;
+      d.state_in = nullptr;
+      d.state_out = states;
+      d.out = nullptr;
+      e = run(d, BH * nch, "chunk_tc_dS");
+      if (e == cudaSuccess) {
+        const size_t n = static_cast<size_t>(BH) * d_k * d_v;
+        Mark m("state_scan", st);
+        simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+            states, s_in, s_out, cc, H, d_k, d_v, nch, BH);
+        e = cudaGetLastError();
+      }
+    }
+  } else if (!scan) {
     e = run(a, BH, "chunk_tc");
   } else {
     // The [BH, L, d] tensors viewed as [BH·nch, 128, d]: one chunk per row.
@@ -551,14 +613,13 @@ ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_d
 ret_status ret_parallel_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,
                              int d_v, ret_dtype out_dt, int gn_enabled, int state_out_wanted,
                              int* path, size_t* workspace_bytes) {
-  (void)gamma;
   if (!path || !workspace_bytes) return RET_EINVAL;
   if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
   if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
   if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
       d_v < 1 || d_v > 1024)
     return RET_EINVAL;
-  const Plan p = plan_parallel(B, H, L, d_k, d_v, gn_enabled != 0, state_out_wanted != 0);
+  const Plan p = plan_parallel(in_dt, gamma, B, H, L, d_k, d_v, gn_enabled != 0, state_out_wanted != 0);
   *path = p.path;
   *workspace_bytes = p.bytes;
   return RET_OK;
@@ -573,10 +634,23 @@ ret_status ret_parallel(const void* q, const void* k, const void* v, ret_dtype i
                               out_dt, gn);
   if (s != RET_OK) return s;
   CallConsts cc;
-  if ((s = make_consts(cc, gamma, theta, H, d_k, L, L)) != RET_OK) return s;
-  const Plan p = plan_parallel(B, H, L, d_k, d_v, gn_on(gn), state_out != nullptr);
+  const Plan p = plan_parallel(in_dt, gamma, B, H, L, d_k, d_v, gn_on(gn), state_out != nullptr);
   if (!workspace || workspace_bytes < p.bytes || !al16(workspace)) return RET_EWORKSPACE;
-  // One chunk of length L: the chunk kernels evaluate the parallel form.
+  if (p.path == RET_PATH_TC) {
+    // 128-row blocks (the front pass folds ζ over blocks of 128)
+    if ((s = make_consts(cc, gamma, theta, H, d_k, tcc::CH, L)) != RET_OK) return s;
+    const auto* qq = static_cast<const __nv_bfloat16*>(q);
+    const auto* kk = static_cast<const __nv_bfloat16*>(k);
+    const auto* vv = static_cast<const __nv_bfloat16*>(v);
+    if (out_dt == RET_F32)
+      return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
+                                 static_cast<float*>(out), gn, workspace, p, stream, false, true);
+    return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
+                                       state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
+                                       p, stream, false, true);
+  }
+  if ((s = make_consts(cc, gamma, theta, H, d_k, L, L)) != RET_OK) return s;
+  // One chunk of length L: the fp32 chunk kernels evaluate the parallel form.
   if (in_dt == RET_F32)
     return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, L, state_in, state_out,
                                     out, out_dt, gn, workspace, p, state_out != nullptr, stream);

@@ -135,6 +135,10 @@ def test_path_selection(lib):
                                        _lib.RET_BF16, 0, C.byref(path), C.byref(nb2)) == _lib.RET_OK
     assert path.value == _lib.RET_PATH_TC
     assert nb2.value == nb + 2 * 16 * 64 * 256 * 512 * 4
+    # the parallel form of the same shape runs on the tensor cores as well
+    assert lib.ret_parallel_plan(_lib.RET_BF16, None, 2, 16, 8192, 256, 512, _lib.RET_BF16, 0, 0,
+                                 C.byref(path), C.byref(nb2)) == _lib.RET_OK
+    assert path.value == _lib.RET_PATH_TC and nb2.value == nb   # rotated Q′ / K̂′ only
     # fp32 inputs, chunk 64, d_v 64 → fp32 kernels
     assert _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)[0] == _lib.RET_PATH_SIMT
     assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64)[0] == _lib.RET_PATH_SIMT

@@ -210,6 +210,46 @@ def test_tc_scan_layout_is_bit_identical_to_carry(d_k, d_v, L, H):
     assert_close(gpu_np(s2), ref_s, torch.bfloat16, "scan state")
 
 
+@pytest.mark.parametrize("d_k,d_v,L,H,state", [(64, 128, 256, 1, False), (128, 256, 384, 2, True),
+                                               (256, 512, 512, 2, True)])
+def test_tc_parallel_form_vs_oracle(d_k, d_v, L, H, state):
+    """ret_parallel on the tensor cores: block-tiled (Q′K′ᵀ ⊙ D)V, no recurrence."""
+    w, inp = _custom(2, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1 if state else 0.0,
+                     seed=d_k + L)
+    path, _ = R.plan("parallel", torch.bfloat16, 2, H, L, d_k, d_v, gamma=inp["gamma"],
+                     state_out=True)
+    assert path == R.RET_PATH_TC
+    ref_o, ref_s = _oracle_full(inp, w, "parallel", pos0=5)
+    d = _cuda(inp)
+    for odt in (torch.bfloat16, torch.float32):
+        o, s = R.parallel(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], pos0=5,
+                          state_in=d["state_in"], return_state=True, out_dtype=odt)
+        assert R.sync_status() == R.RET_OK
+        assert_close(gpu_np(o), ref_o, torch.bfloat16, f"parallel out {odt}")
+        assert_close(gpu_np(s), ref_s, torch.bfloat16, "parallel state")
+    # the parallel and chunkwise forms agree closely; the final state is the same bits
+    oc, sc = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=5,
+                         state_in=d["state_in"], out_dtype=torch.float32)
+    assert rel_fro(gpu_np(o), gpu_np(oc)) < 1e-2
+    assert torch.equal(s, sc)
+
+
+def test_tc_parallel_groupnorm_and_causality():
+    w, inp = _custom(1, 2, 384, 128, 128, "bf16", 128, std=1.0, seed=31)
+    gn = {"eps": 1e-5}
+    ref_o, _ = _oracle_full(inp, w, "parallel", gn=gn)
+    d = _cuda(inp)
+    o, _ = R.parallel(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], gn=gn)
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "parallel gn")
+    m = 200
+    q2, k2, v2 = d["q"].clone(), d["k"].clone(), d["v"].clone()
+    for t in (q2, k2, v2):
+        t[:, :, m:] = 3.0
+    o1, _ = R.parallel(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"])
+    o2, _ = R.parallel(q2, k2, v2, inp["gamma"], inp["theta"])
+    assert torch.equal(o1[:, :, :m], o2[:, :, :m])
+
+
 # -------------------------------------------------------- full workloads --
 def test_msr1p3b_groupnorm_sampled_heads():
     w = WORKLOADS["msr1p3b"]
