@@ -91,6 +91,27 @@ def profiled_traffic(kernel, workload="msr7b",
 
 
 # --------------------------------------------------------------------------
+# Multi-rank timing: one independent replica per rank (the path has no
+# exchange step); the job's time is the slowest rank's, its throughput the
+# units of all ranks over that time.
+# --------------------------------------------------------------------------
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """Largest value of `value` over the ranks of the default process group."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job units per second when every rank processes units_per_rank."""
+    return world * units_per_rank / seconds_max
+
+
+# --------------------------------------------------------------------------
 # Clock sampling during the timed region (NVML reads only)
 # --------------------------------------------------------------------------
 class ClockSampler:
@@ -319,12 +340,9 @@ def main():
     for i, nm in enumerate(names):
         per_kernel.setdefault(nm, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
     launches_per_step = n_k / hook_steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     tok_per_step = w.B * w.L
-    value = world * tok_per_step * args.steps / (ms / 1e3)
+    value = replica_throughput(tok_per_step * args.steps, ms / 1e3, world)
     flops = chunk_flops(w)
     top = max(per_kernel, key=lambda n: sum(per_kernel[n]))
     top_ms = statistics.mean(per_kernel[top])
@@ -364,9 +382,9 @@ def main():
             dstep(t)
         de.record(stream)
         torch.cuda.synchronize()
-    dms = ds.elapsed_time(de) / dsteps
+    dms = max_over_ranks(ds.elapsed_time(de) / dsteps, world, dev)
     dgbs = decode_bytes(dw) / (dms / 1e3) / 1e9
-    decode = {"metric": "decode state GB/s", "value": world * dgbs, "unit": "GB/s",
+    decode = {"metric": "decode state GB/s", "value": replica_throughput(dgbs, 1.0, world), "unit": "GB/s",
               "ms_per_step": dms, "steps": dsteps,
               "config": {"workload": "decode", "B": dw.B, "H": dw.H, "d_k": dw.d_k, "d_v": dw.d_v,
                          "state_bytes": 4 * dw.B * dw.H * dw.d_k * dw.d_v,
@@ -402,10 +420,10 @@ def main():
         e2e_step()
     ee.record(stream)
     torch.cuda.synchronize()
-    ems = es.elapsed_time(ee) / args.e2e_steps
+    ems = max_over_ranks(es.elapsed_time(ee) / args.e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hs,) if hs is not None else ()))
     d2h = hout.numel() * hout.element_size() + hsout.numel() * hsout.element_size()
-    e2e = {"value": world * tok_per_step / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": replica_throughput(tok_per_step, ems / 1e3, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": args.e2e_steps}
 
     cpu = None
