@@ -116,11 +116,12 @@ def plan(form: str, in_dtype, B, H, L, d_k, d_v, chunk=None, out_dtype=None, gn=
 
 def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
               return_state: bool = True, out=None, out_dtype=None, gn=None, workspace=None,
-              stream=None, layout: str = "carry"):
+              stream=None, layout: str = "carry", state_out=None):
     """Chunkwise retention.  Returns (out, state_out or None).
 
     layout="carry" runs ret_chunkwise (state carried across chunks);
     layout="scan" runs ret_chunkwise_scan (chunk-parallel then scan).
+    out / state_out / workspace may be given to avoid allocations.
     """
     lib = load()
     B, H, L, d_k, d_v = _check_seq(q, k, v)
@@ -132,7 +133,8 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
     garr, gp = _host_f32(gamma, H, "gamma")
     tarr, tp = _host_f32(theta, d_k // 2, "theta")
     st_in = _dev(state_in, "state_in", torch.float32, (B, H, d_k, d_v))
-    state_out = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device) if return_state else None
+    if state_out is None and return_state:
+        state_out = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device)
     gns, keep = _gn_struct(gn, H, d_v, q.device)
     _, nbytes = plan("chunkwise_scan" if layout == "scan" else "chunkwise", q.dtype, B, H, L, d_k,
                      d_v, chunk, odtype, bool(gn), gamma=garr)
