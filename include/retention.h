@@ -78,7 +78,9 @@ typedef struct {
 /* Kernel path chosen for a call (reported by ret_*_plan). */
 typedef enum {
   RET_PATH_TC = 1,     /* tcgen05 tensor-core kernels (bf16 inputs)       */
-  RET_PATH_SIMT = 2    /* fp32 FFMA kernels                               */
+  RET_PATH_SIMT = 2,   /* fp32 FFMA kernels                               */
+  RET_PATH_TC_SINGLE = 3  /* ret_force_path only: the tensor-core path with
+                             one CTA per d_v tile instead of CTA pairs    */
 } ret_path;
 
 /* ------------------------------------------------------------------------
@@ -215,8 +217,10 @@ ret_status ret_profile_begin(cudaEvent_t* events, int n_events);
 int ret_profile_end(void);
 const char* ret_profile_kernel(int i);
 
-/* Force every later call in this process onto one path (RET_PATH_SIMT) or
- * back to automatic selection (0).  For cross-checks between paths. */
+/* Force every later call in this process onto one path (RET_PATH_SIMT),
+ * onto the tensor-core path without CTA pairs (RET_PATH_TC_SINGLE), or back
+ * to automatic selection (0).  For cross-checks between paths.  Plans still
+ * report RET_PATH_TC for both tensor-core variants. */
 ret_status ret_force_path(int path);
 
 const char* ret_status_string(ret_status s);

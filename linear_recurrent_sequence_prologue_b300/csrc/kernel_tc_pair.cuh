@@ -1,0 +1,396 @@
+// Chunkwise retention on a CTA pair (tcgen05 cta_group::2).
+//
+// Same arithmetic as the single-CTA chunk kernel (kernel_tc_chunk.cuh: form
+// of «从RoPE到Retention…» §4.3 and the RetNet 保留网络 explainer 分块循环,
+// rewritten with K̂′_m = ζ_m k′_m, P̂ = causal(Q′K̂′ᵀ), Ŝ = bf16(γ^b S),
+// o_j = ω_j (Q′Ŝ + P̂V)_j, S ← fmaf(γ^b, S, ΔS)), but the two CTAs that own
+// the d_v tiles 2p and 2p+1 of one (b, h) form a cluster and run every
+// product as one pair MMA issued by the even CTA:
+//   P̂   [j × m]  = Q′ · K̂′ᵀ     M = 128: each CTA holds its 64 query rows of
+//                                Q′ and one half of the keys of K̂′
+//   ΔSᵀ [v × k]  = Vᵀ · K̂′      M = 256: each CTA its own V tile and one
+//                                half of the d_k columns of K̂′
+//   Õᵀ  [v × j]  = Ŝᵀ · Q′ᵀ     M = 256: Ŝᵀ from each CTA's TMEM, Q′ rows
+//                                split by query half
+//   Õᵀ  [v × j] += Vᵀ · P̂ᵀ      M = 256: P̂ rows split by query half
+// So each CTA stages half of Q′ and half of P̂ instead of all of them, and
+// the operand reads from shared memory per CTA drop by about 40%, which
+// leaves room to double-buffer Q′ and V.  The query half of P̂ each CTA
+// drains is exactly the half its own PV operand needs, so no P̂ crosses
+// between the CTAs; each CTA still drains its own Õᵀ, ΔSᵀ and keeps its
+// own fp32 state tile, as in the single-CTA kernel, and the results are
+// the same numbers in the same order.
+//
+// Synchronisation: TMA loads of both CTAs count their bytes on the even
+// CTA's FULL barriers; pair commits arrive on the barriers of both CTAs;
+// drain warps of both CTAs arrive on the even CTA's barriers with
+// cluster-scope release, and the issuing thread waits on them with
+// cluster-scope acquire.
+#pragma once
+
+#include "common.cuh"
+#include "tc_primitives.cuh"
+#include "kernel_tc_chunk.cuh"
+
+namespace ret {
+namespace tcq {
+
+using namespace ret::tc;
+using tcc::ChunkArgs;
+using tcc::CH;
+using tcc::NCW;
+using tcc::NTHREADS;
+using tcc::VT;
+
+enum Bar : int {
+  Q_FULL0 = 0, Q_FULL1, V_FULL0, V_FULL1, K_FULL,   // TMA → MMA (even CTA's copy counts)
+  Q_EMPTY0, Q_EMPTY1, V_EMPTY0, V_EMPTY1, K_EMPTY,  // MMA → TMA (both CTAs)
+  P_FULL,     // QK done                      (MMA → drains)
+  X_READ,     // P̂ read out of X              (drains → MMA)
+  P_SMEM,     // P̂ halves in shared memory    (drains → MMA)
+  DS_FULL,    // ΔS done                      (MMA → drains)
+  DS_FREE,    // ΔS read out of D             (drains → MMA)
+  SH_FREE,    // QS done, Ŝ may be rewritten  (MMA → drains)
+  SH_READY,   // Ŝ written                    (drains → MMA)
+  O_FULL,     // PV done                      (MMA → drains)
+  X_FREE,     // Õ read out of X              (drains → MMA)
+  MMA_DONE, NBAR_
+};
+
+template <int DK>
+struct Cfg {
+  static_assert(DK == 128 || DK == 256, "d_k");
+  static constexpr int QBOX = DK / 64;             // 64-column boxes across d_k
+  static constexpr int SPT = DK / 4;               // state values per drain thread
+  static constexpr uint32_t HBOX = 64 * 64 * 2;    // 64-row box, 8 KB
+  static constexpr uint32_t BOX = CH * 64 * 2;     // 128-row box, 16 KB
+  static constexpr uint32_t QH_BYTES = QBOX * HBOX;        // 64 query rows of Q′
+  static constexpr uint32_t KQ_BYTES = QBOX * HBOX;        // 64 keys of K̂′, all d_k
+  static constexpr uint32_t KV_BYTES = (QBOX / 2) * BOX;   // all keys, d_k / 2 columns
+  static constexpr uint32_t V_BYTES = 2 * BOX;             // 128 keys × 128 v
+  static constexpr uint32_t P_BYTES = 2 * HBOX;            // 64 query rows × 128 keys
+  static constexpr uint32_t OFF_Q = 0;                     // two slots
+  static constexpr uint32_t OFF_KQ = OFF_Q + 2 * QH_BYTES;
+  static constexpr uint32_t OFF_KV = OFF_KQ + KQ_BYTES;
+  static constexpr uint32_t OFF_V = OFF_KV + KV_BYTES;     // two slots
+  static constexpr uint32_t OFF_P = OFF_V + 2 * V_BYTES;
+  static constexpr uint32_t OFF_OMEGA = OFF_P + P_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_OMEGA + CH * 4;
+  static constexpr uint32_t OFF_TPTR = OFF_BAR + NBAR_ * 8;
+  static constexpr uint32_t USED = OFF_TPTR + 16;
+  static constexpr uint32_t SMEM_BYTES = USED + 1024;     // slack for 1024-B alignment
+  static constexpr uint32_t T_X = 0, T_D = 128, T_SH = 128 + DK;
+  static constexpr uint32_t T_COLS = 512;
+};
+
+// grid = (d_v / 128, rows), cluster = (2, 1, 1); block = 576 threads.
+// Warp 0: TMA producer (both CTAs).  Warp 1: pair MMA issuer (even CTA).
+// Warps 2..17: drain warps, as in the single-CTA kernel.
+template <int DK>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    pair_tc_kernel(const __grid_constant__ CUtensorMap tm_qh,   // Q′, 64-row boxes
+                   const __grid_constant__ CUtensorMap tm_kh,   // K̂′, 64-row boxes
+                   const __grid_constant__ CUtensorMap tm_k,    // K̂′, 128-row boxes
+                   const __grid_constant__ CUtensorMap tm_v,    // V, 128-row boxes
+                   ChunkArgs args, CallConsts cc) {
+  using C = Cfg<DK>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + C::OFF_Q, sKQ = sb + C::OFF_KQ, sKV = sb + C::OFF_KV;
+  const uint32_t sV = sb + C::OFF_V, sP = sb + C::OFF_P;
+  float* omega = reinterpret_cast<float*>(smem + C::OFF_OMEGA);
+  auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
+  // The even CTA's barriers in the cluster window (offsets are preserved).
+  const uint32_t lead_bar0 = mapa_shared(bar(0), 0);
+  auto lead_bar = [&](int i) -> uint32_t { return lead_bar0 + 8u * static_cast<uint32_t>(i); };
+
+  const uint32_t rank = cluster_ctarank();   // 0: issues the pair MMAs
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int v0 = blockIdx.x * VT;
+  const int bh = blockIdx.y;
+  const int h = (bh / args.seq_div) % args.H;
+  const int L = args.L, d_v = args.d_v, nch = args.nchunks;
+  const float gb = cc.gb[h];
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tm_qh);
+    tma_prefetch_desc(&tm_kh);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    for (int i = 0; i < NBAR_; ++i) {
+      const bool from_drain = (i == X_READ || i == P_SMEM || i == DS_FREE || i == SH_READY ||
+                               i == X_FREE);
+      mbar_init(bar(i), from_drain ? 2 * NCW : 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(sb + C::OFF_TPTR, C::T_COLS);
+    tmem_relinquish_pair();
+  }
+  if (threadIdx.x < CH) omega[threadIdx.x] = gpow(cc.lg2g[h], static_cast<float>(static_cast<int>(threadIdx.x) + 1 - CH));
+  // Both CTAs' barriers exist before any copy or arrival can target them.
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + C::OFF_TPTR);
+
+  if (warp == 0) {
+    // ------------------------------ TMA producer ---------------------------
+    // Per chunk: Q′ rows of this CTA's query half, V tile, then K̂′ (its
+    // key half with all d_k, and all keys with its d_k half).  Q′ and V
+    // slots were freed a chunk earlier, so they land well ahead; K̂′ waits
+    // for ΔS of the previous chunk.
+    if (lane == 0) {
+      int issued = -1;
+      const int yh = 64 * static_cast<int>(rank);
+      for (int i = 0; i < nch; ++i) {
+        const int y = bh * L + i * CH;
+        const int s = i & 1;
+        if (i > 1 && !mbar_wait(bar(Q_EMPTY0 + s), static_cast<uint32_t>((i >> 1) - 1) & 1u, 0x102)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + s), 2 * C::QH_BYTES);
+        for (int b = 0; b < C::QBOX; ++b)
+          tma_load_2d_pair(sQ + s * C::QH_BYTES + b * C::HBOX, &tm_qh, 64 * b, y + yh, lead_bar(Q_FULL0 + s));
+        if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), static_cast<uint32_t>((i >> 1) - 1) & 1u, 0x103)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(V_FULL0 + s), 2 * C::V_BYTES);
+        for (int b = 0; b < 2; ++b)
+          tma_load_2d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, y, lead_bar(V_FULL0 + s));
+        if (i > 0 && !mbar_wait(bar(K_EMPTY), static_cast<uint32_t>(i - 1) & 1u, 0x101)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(K_FULL), 2 * (C::KQ_BYTES + C::KV_BYTES));
+        for (int b = 0; b < C::QBOX; ++b)
+          tma_load_2d_pair(sKQ + b * C::HBOX, &tm_kh, 64 * b, y + yh, lead_bar(K_FULL));
+        for (int b = 0; b < C::QBOX / 2; ++b)
+          tma_load_2d_pair(sKV + b * C::BOX, &tm_k, 64 * (static_cast<int>(rank) * (C::QBOX / 2) + b), y,
+                           lead_bar(K_FULL));
+        issued = i;
+      }
+      // Never leave with copies still landing: the even CTA's FULL barriers
+      // count both CTAs' bytes, so it waits (bounded) for the last phases.
+      if (rank == 0 && issued >= 0 && status_aborted()) {
+        for (int c = issued > 0 ? issued - 1 : 0; c <= issued; ++c) {
+          const uint32_t ph = static_cast<uint32_t>(c >> 1) & 1u;
+          mbar_wait(bar(Q_FULL0 + (c & 1)), ph, 0x1f2, kWaitBudgetCycles / 16);
+          mbar_wait(bar(V_FULL0 + (c & 1)), ph, 0x1f3, kWaitBudgetCycles / 16);
+        }
+        mbar_wait(bar(K_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f1, kWaitBudgetCycles / 16);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------ MMA issuer -----------------------------
+    if (lane == 0 && rank == 0) {
+      const uint32_t tX = tmem + C::T_X, tD = tmem + C::T_D, tSH = tmem + C::T_SH;
+      constexpr uint32_t ID_P = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t ID_KV = idesc_bf16_f32(256, DK, 1, 1);
+      constexpr uint32_t ID_QS = idesc_bf16_f32(256, 128, 0, 0);
+      constexpr uint32_t ID_PV = idesc_bf16_f32(256, 128, 1, 0);
+      const uint64_t dQ0 = sdesc_sw128(sQ, 16, 1024);                  // K-major, 64 rows
+      const uint64_t dQ1 = sdesc_sw128(sQ + C::QH_BYTES, 16, 1024);
+      const uint64_t dKQ = sdesc_sw128(sKQ, 16, 1024);                 // K-major, 64 keys
+      const uint64_t dKV = sdesc_sw128(sKV, C::BOX, 1024);             // MN-major, d_k half
+      const uint64_t dV0 = sdesc_sw128(sV, C::BOX, 1024);              // MN-major
+      const uint64_t dV1 = sdesc_sw128(sV + C::V_BYTES, C::BOX, 1024);
+      const uint64_t dP = sdesc_sw128(sP, 16, 1024);                   // K-major, 64 rows
+      // k-step s of a K-major tile of 64-row boxes, in 16-byte units
+#define RET_PAIR_KMAJ(s) static_cast<uint32_t>((((s) >> 2) * C::HBOX + ((s) & 3) * 32) >> 4)
+      // Fully unrolled issue: S is the compile-time step index.  MN-major
+      // operands advance 2048 bytes (16 keys) per step.
+      uint64_t dQ = dQ0, dV = dV0;
+      auto issue_qk = [&](auto S) {
+        constexpr int k = decltype(S)::value;
+        mma_ss_pair_off<RET_PAIR_KMAJ(k), RET_PAIR_KMAJ(k)>(tX, dQ, dKQ, ID_P, k > 0 ? 1u : 0u);
+      };
+      auto issue_kv = [&](auto S) {
+        constexpr int k = decltype(S)::value;
+        mma_ss_pair_off<k * 128, k * 128>(tD, dV, dKV, ID_KV, k > 0 ? 1u : 0u);
+      };
+      auto issue_qs = [&](auto S) {
+        constexpr int k = decltype(S)::value;
+        mma_ts_pair_off<RET_PAIR_KMAJ(k)>(tX, tSH + k * 8, dQ, ID_QS, k > 0 ? 1u : 0u);
+      };
+      auto issue_pv = [&](auto S) {
+        constexpr int k = decltype(S)::value;
+        mma_ss_pair_off<k * 128, RET_PAIR_KMAJ(k)>(tX, dV, dP, ID_PV, 1u);
+      };
+#undef RET_PAIR_KMAJ
+      for (int i = 0; i < nch; ++i) {
+        const int s = i & 1;
+        const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+        const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
+        const uint32_t pq = static_cast<uint32_t>(i >> 1) & 1u;
+        dQ = s ? dQ1 : dQ0;
+        dV = s ? dV1 : dV0;
+        // 1. P̂ = Q′ K̂′ᵀ into X (needs Õ of the previous chunk read out)
+        if (!mbar_wait_cl(bar(K_FULL), pi, 0x201)) break;
+        if (!mbar_wait_cl(bar(Q_FULL0 + s), pq, 0x202)) break;
+        if (i > 0 && !mbar_wait_cl(bar(X_FREE), pp, 0x203)) break;
+        tc_fence_after();
+        static_for<DK / 16>(issue_qk);
+        mma_commit_pair(bar(P_FULL));
+        // 2. ΔSᵀ = Vᵀ K̂′ into D (needs the previous ΔS read out)
+        if (!mbar_wait_cl(bar(V_FULL0 + s), pq, 0x204)) break;
+        if (i > 0 && !mbar_wait_cl(bar(DS_FREE), pp, 0x205)) break;
+        tc_fence_after();
+        static_for<CH / 16>(issue_kv);
+        mma_commit_pair(bar(DS_FULL));
+        mma_commit_pair(bar(K_EMPTY));
+        // 3. Õᵀ = Ŝᵀ Q′ᵀ into X (needs P̂ read out and Ŝ of this chunk)
+        if (!mbar_wait_cl(bar(X_READ), pi, 0x206)) break;
+        if (!mbar_wait_cl(bar(SH_READY), pi, 0x207)) break;
+        tc_fence_after();
+        static_for<DK / 16>(issue_qs);
+        mma_commit_pair(bar(Q_EMPTY0 + s));
+        mma_commit_pair(bar(SH_FREE));
+        // 4. Õᵀ += Vᵀ P̂ᵀ (needs both P̂ halves in shared memory)
+        if (!mbar_wait_cl(bar(P_SMEM), pi, 0x208)) break;
+        tc_fence_after();
+        static_for<CH / 16>(issue_pv);
+        mma_commit_pair(bar(O_FULL));
+        mma_commit_pair(bar(V_EMPTY0 + s));
+      }
+      // All issued MMAs must finish before either CTA releases its TMEM.
+      mma_commit_pair(bar(MMA_DONE));
+      mbar_wait(bar(MMA_DONE), 0, 0x2ff);
+    }
+  } else {
+    // ------------------------------ drain warps ----------------------------
+    const int w = warp - 2;                 // 0..15
+    const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+    const int cs = w >> 2;                  // column slice
+    const int kr = w >> 2;                  // state k range [kr*SPT, kr*SPT+SPT)
+    const int vl = 32 * quarter + lane;     // TMEM lane: local v for Õ / ΔS / Ŝ
+    const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+    const size_t sbase = static_cast<size_t>(bh) * DK * d_v + v0 + vl;
+
+    float S[C::SPT];
+#pragma unroll
+    for (int u = 0; u < C::SPT; ++u)
+      S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
+
+    auto arrive_lead = [&](int b) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(b), 0));
+    };
+    // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
+    auto write_shat = [&]() {
+#pragma unroll
+      for (int c = 0; c < C::SPT / 16; ++c) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          pk[u] = pack_bf16x2(gb * S[c * 16 + 2 * u], gb * S[c * 16 + 2 * u + 1]);
+        tmem_st8(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 16) / 2, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      arrive_lead(SH_READY);
+    };
+    write_shat();
+
+    bool ok = true;
+    for (int i = 0; i < nch && ok; ++i) {
+      const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+      // ---- (a) P̂ drain: causal mask, bf16, into this CTA's query half ----
+      if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
+      tc_fence_after();
+      {
+        // Lane vl holds query row jl of this CTA's half for the keys of half
+        // mh (pair M = 128 layout), columns 16·cs … +15 of that half.
+        const int jl = vl & 63, mh = vl >> 6;
+        const int j = 64 * static_cast<int>(cluster_ctarank()) + jl;   // query row in the chunk
+#pragma unroll
+        for (int g = 0; g < 2; ++g) {   // two 8-column rounds keep the register peak low
+          uint32_t r[8];
+          tmem_ld8(tmem + C::T_X + lane_off + 16 * cs + 8 * g, r);
+          tmem_ld_wait();
+          if (g == 1) {
+            tc_fence_before();
+            arrive_lead(X_READ);
+          }
+          uint32_t pk[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int m = 64 * mh + 16 * cs + 8 * g + 2 * u;
+            const float a = (m <= j) ? __uint_as_float(r[2 * u]) : 0.f;
+            const float b = (m + 1 <= j) ? __uint_as_float(r[2 * u + 1]) : 0.f;
+            pk[u] = pack_bf16x2(a, b);
+          }
+          st_shared_v4(sP + mh * C::HBOX + sw128_offset(jl, 16 * cs + 8 * g), pk[0], pk[1], pk[2], pk[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      arrive_lead(P_SMEM);
+
+      // ---- (b) ΔS drain: S = fmaf(γ^b, S, ΔS) ----
+      if (!mbar_wait(bar(DS_FULL), pi, 0x302)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::SPT / 8; ++c) {   // 8 columns per load: S stays in registers
+        uint32_t d[8];
+        tmem_ld8(tmem + C::T_D + lane_off + kr * C::SPT + c * 8, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          S[8 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gb, S[8 * c + u], __uint_as_float(d[u]));
+      }
+      tc_fence_before();
+      arrive_lead(DS_FREE);
+
+      // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
+      if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
+      tc_fence_after();
+      write_shat();
+
+      // ---- (d) Õ drain: release X, then ω_j scale and store ----
+      if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const size_t base = (static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs) * d_v + v0 + vl;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r[16];
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16 * hf + 8, *reinterpret_cast<uint32_t(*)[8]>(&r[8]));
+          tmem_ld_wait();
+          if (hf == 1) {
+            tc_fence_before();
+            arrive_lead(X_FREE);
+          }
+          const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
+          if (!args.out) {
+          } else if (args.out_f32) {
+            float* o = reinterpret_cast<float*>(args.out) + gb0;
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]);
+          } else {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              o[static_cast<size_t>(c) * d_v] =
+                  __float2bfloat16_rn(omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]));
+          }
+        }
+      }
+    }
+    if (ok && args.state_out) {
+#pragma unroll
+      for (int u = 0; u < C::SPT; ++u)
+        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] = S[u];
+    }
+  }
+
+  // Neither CTA leaves (or frees its TMEM) while the other may still arrive
+  // on its barriers or the pair MMAs may still touch its memory.
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::T_COLS);
+  }
+}
+
+}  // namespace tcq
+}  // namespace ret

@@ -16,6 +16,7 @@
 #include "kernels_simt.cuh"
 #include "kernel_tc_chunk.cuh"
 #include "kernel_tc_parallel.cuh"
+#include "kernel_tc_pair.cuh"
 
 using namespace ret;
 
@@ -125,11 +126,12 @@ bool get_encode() {
 }
 
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box 64 × 128, 128-B swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
+              uint32_t box_rows = 128) {
   if (!get_encode()) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t es[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -158,6 +160,13 @@ bool tc_chunk_ok(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int
   if (!(d_k == 64 || d_k == 128 || d_k == 256)) return false;
   if (d_v % tcc::VT != 0 || chunk != tcc::CH || L % tcc::CH != 0) return false;
   return tc_gamma_ok(gamma, H, chunk);
+}
+
+// CTA pairs (cta_group::2) for the chunk kernels: the two d_v tiles of a
+// pair share one head, so d_v / 128 must be even.
+bool tc_pair_ok(int d_k, int d_v) {
+  return g_force_path != RET_PATH_TC_SINGLE && (d_k == 128 || d_k == 256) &&
+         (d_v / tcc::VT) % 2 == 0;
 }
 
 struct Plan {
@@ -310,6 +319,10 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   const uint64_t rows = static_cast<uint64_t>(BH) * L;
   if (!make_map(&mq, qr, rows, d_k) || !make_map(&mk, kr, rows, d_k) || !make_map(&mv, v, rows, d_v))
     return RET_ECUDA;
+  const bool pair = tc_pair_ok(d_k, d_v);
+  CUtensorMap mqh, mkh;   // 64-row boxes of Q′ / K̂′ for the pair kernel
+  if (pair && (!make_map(&mqh, qr, rows, d_k, 64) || !make_map(&mkh, kr, rows, d_k, 64)))
+    return RET_ECUDA;
   float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
   const int nch = L / tcc::CH;
   tcc::ChunkArgs a;
@@ -332,7 +345,33 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     kern<<<dim3(d_v / tcc::VT, rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
     return cudaGetLastError();
   };
+  // Pair kernel: clusters of two CTAs along the d_v tiles.
+  auto launch_pair = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args, int rows,
+                         const char* name) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d_v / tcc::VT, rows);
+    cfg.blockDim = dim3(tcc::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    Mark m(name, st);
+    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, args, cc);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  };
   auto run = [&](const tcc::ChunkArgs& args, int rows, const char* name) -> cudaError_t {
+    if (pair && d_k == 256)
+      return launch_pair(tcq::pair_tc_kernel<256>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name);
+    if (pair)
+      return launch_pair(tcq::pair_tc_kernel<128>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name);
     if (d_k == 256) return launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name);
     if (d_k == 128) return launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
     return launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
@@ -499,7 +538,8 @@ const char* ret_profile_kernel(int i) {
 }
 
 ret_status ret_force_path(int path) {
-  if (path != 0 && path != RET_PATH_SIMT && path != RET_PATH_TC) return RET_EINVAL;
+  if (path != 0 && path != RET_PATH_SIMT && path != RET_PATH_TC && path != RET_PATH_TC_SINGLE)
+    return RET_EINVAL;
   g_force_path = path;
   return RET_OK;
 }

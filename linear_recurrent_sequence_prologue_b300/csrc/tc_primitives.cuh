@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda.h>   // CUtensorMap (type only)
 #include "common.cuh"
 
@@ -227,6 +228,159 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
   const uint32_t chunk = (col >> 3) ^ (row & 7u);
   return row * 128u + (chunk << 4) + ((col & 7u) << 1);
+}
+
+// ------------------------- CTA pairs (cta_group::2) ------------------------
+// Two CTAs of a cluster whose ranks differ in bit 0 form a pair: one thread
+// of the even CTA issues MMAs that read operands from both CTAs' shared
+// memory (and tensor memory) and write each CTA's share of D into its own
+// TMEM.  Every tcgen05 instruction of a kernel uses the same cta_group.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Every thread of every CTA of the cluster arrives, then waits for all.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                   "memory");
+}
+// Arrive on an mbarrier given by its shared::cluster address (this CTA's or
+// a peer's) with the default release at CTA scope.  The hand-offs that use
+// it (TMEM reads finished by tcgen05.wait::ld, TMEM writes finished by
+// tcgen05.wait::st, shared-memory operands fenced to the async proxy) are
+// complete when it executes; a cluster-scope release would also wait for
+// every global store still in flight from this thread (the output tiles),
+// which costs thousands of cycles per hand-off.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (the phase may have been completed
+// by arrivals from the peer CTA); same budget and status rules as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, unsigned where,
+                                             long long budget = kWaitBudgetCycles) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (status_aborted()) return false;
+      if (clock64() - t0 > budget) {
+        report_timeout(where);
+        return false;
+      }
+    }
+  }
+}
+// 2-D tiled load into this CTA's shared memory whose completion is counted
+// on an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                                 uint32_t cl_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(cl_bar)
+      : "memory");
+}
+// TMEM allocation for a pair: one warp of each CTA executes it; both CTAs
+// receive the same column base.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Pair MMAs.  M = 256: each CTA supplies 128 rows of A and receives those
+// rows of D in TMEM lanes 0..127.  M = 128: each CTA supplies 64 rows of A;
+// its D rows sit in lanes 0..63 for the first N/2 columns and in lanes
+// 64..127 for the second N/2 columns, both at TMEM columns [0, N/2).  B is
+// split by N: the even CTA holds columns [0, N/2), the odd CTA [N/2, N),
+// each at the same shared-memory offset.
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same two forms with each descriptor given as a base plus an immediate
+// offset (16-byte units) added inside the asm, so that an unrolled issue
+// loop keeps one register pair per operand instead of one per step.
+template <uint32_t AOFF, uint32_t BOFF>
+__device__ __forceinline__ void mma_ss_pair_off(uint32_t d_tmem, uint64_t a_base, uint64_t b_base,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "add.u64 da, %1, %5;\n\tadd.u64 db, %2, %6;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_base), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(AOFF), "n"(BOFF)
+      : "memory");
+}
+template <uint32_t BOFF>
+__device__ __forceinline__ void mma_ts_pair_off(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_base,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "add.u64 db, %2, %5;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_base), "r"(idesc), "r"(accumulate), "n"(BOFF)
+      : "memory");
+}
+// Calls f(std::integral_constant<int, s>{}) for s = 0 … N−1.
+template <int S, int N, typename F>
+__device__ __forceinline__ void static_for_impl(F& f) {
+  if constexpr (S < N) {
+    f(std::integral_constant<int, S>{});
+    static_for_impl<S + 1, N>(f);
+  }
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F f) {
+  static_for_impl<0, N>(f);
+}
+
+// Arrive once on the mbarrier at offset `bar` of both CTAs of the pair when
+// the pair MMAs issued so far by this thread are done.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(static_cast<uint16_t>(3))
+      : "memory");
 }
 
 }  // namespace tc

@@ -210,6 +210,35 @@ def test_tc_scan_layout_is_bit_identical_to_carry(d_k, d_v, L, H):
     assert_close(gpu_np(s2), ref_s, torch.bfloat16, "scan state")
 
 
+@pytest.mark.parametrize("d_k,d_v,L,H", [(256, 256, 512, 2), (128, 512, 384, 1), (256, 512, 640, 2)])
+def test_tc_pair_kernel_matches_single_cta_kernel(d_k, d_v, L, H):
+    """The CTA-pair chunk kernel (cta_group::2, two d_v tiles per cluster)
+    against the one-CTA-per-tile kernel: the same products in the same
+    order, so the same bits, for outputs and state, on every layout."""
+    w, inp = _custom(2, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1, seed=d_k + 3 * L)
+    d = _cuda(inp)
+    res = {}
+    try:
+        for mode in (0, R.RET_PATH_TC_SINGLE):
+            R.force_path(mode)
+            for odt in (torch.bfloat16, torch.float32):
+                for layout in ("carry", "scan"):
+                    res[mode, odt, layout] = R.chunkwise(
+                        d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=11,
+                        state_in=d["state_in"], out_dtype=odt, layout=layout)
+                    assert R.sync_status() == R.RET_OK
+    finally:
+        R.force_path(0)
+    for key, (o, s) in res.items():
+        o1, s1 = res[R.RET_PATH_TC_SINGLE, key[1], key[2]]
+        assert torch.equal(s, s1), key
+        assert torch.equal(o, o1), key
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", 128, pos0=11)
+    o, s = res[0, torch.float32, "carry"]
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "pair out")
+    assert_close(gpu_np(s), ref_s, torch.bfloat16, "pair state")
+
+
 @pytest.mark.parametrize("d_k,d_v,L,H,state", [(64, 128, 256, 1, False), (128, 256, 384, 2, True),
                                                (256, 512, 512, 2, True)])
 def test_tc_parallel_form_vs_oracle(d_k, d_v, L, H, state):
