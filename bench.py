@@ -69,15 +69,17 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-def kernel_source_sha(files=("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh")):
+CHUNK_KERNEL_FILES = ("kernel_tc_pair.cuh", "kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh")
+
+
+def kernel_source_sha(files=CHUNK_KERNEL_FILES):
     h = hashlib.sha256()
     for f in files:
         h.update(open(os.path.join(ROOT, "linear_recurrent_sequence_prologue_b300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel, workload="msr7b",
-                     files=("kernel_tc_chunk.cuh", "tc_primitives.cuh", "common.cuh")):
+def profiled_traffic(kernel, workload="msr7b", files=CHUNK_KERNEL_FILES):
     """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(p):

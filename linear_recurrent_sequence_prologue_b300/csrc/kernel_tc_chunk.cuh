@@ -10,9 +10,10 @@
 // Ŝ = bf16(γ^b S):
 //   o_j = ω_j · (Q′Ŝ + P̂V)_j   with ω_j = γ^{j+1−b}
 // because ω_j·γ^b = γ^{j+1} and ω_j·ζ_m = γ^{j−m}.  So one fp32 accumulator
-// holds both output terms and the decay mask reduces to a per-row scale
-// applied at the store (γ^{b−1} ≥ 2^-60 keeps every factor in range; the host
-// routes other heads to the fp32 path).
+// holds both output terms and the decay mask reduces to a per-row scale,
+// which the front pass folds into row j of Q′ (it then reaches P̂ through
+// Q′K̂′ᵀ), so the accumulator is stored as it is (γ^{b−1} ≥ 2^-60 keeps every
+// factor in range; the host routes other heads to the fp32 path).
 //
 // Each CTA owns one (b·h, 128-wide d_v tile) and walks the chunks in order.
 // Transposed products keep d_v on the 128 TMEM lanes:
@@ -72,8 +73,7 @@ struct Cfg {
   static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + Q_BYTES;
   static constexpr uint32_t OFF_P = OFF_V + V_BYTES;
-  static constexpr uint32_t OFF_OMEGA = OFF_P + P_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_OMEGA + CH * 4;
+  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
   static constexpr uint32_t OFF_TPTR = OFF_BAR + NBAR_ * 8;
   static constexpr uint32_t USED = OFF_TPTR + 16;
   static constexpr uint32_t SMEM_BYTES = USED + 1024;   // slack for 1024-B alignment
@@ -95,6 +95,10 @@ struct ChunkArgs {
 
 // ---------------------------------------------------------------------------
 // Front pass: Q′ = R(nθ)q and K̂′ = d_k^{-1/2}·ζ_{t mod b}·R(nθ)k in bf16.
+// With fold_omega, Q′ row t also carries ω_{t mod b} = γ^{(t mod b)+1−b}:
+// o_j = ω_j (Q′Ŝ + P̂V)_j, and scaling row j of Q′ scales both terms (P̂
+// inherits it through Q′K̂′ᵀ), so the chunk kernels store their
+// accumulator as it is.
 // Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by all
 // B·H heads of that row, eight heads' loads in flight at a time; raw q and
 // k are read with the evict-first hint.
@@ -102,7 +106,7 @@ struct ChunkArgs {
 __global__ void __launch_bounds__(256) rotate_qk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ qo, __nv_bfloat16* __restrict__ ko, CallConsts cc, int BH,
-    int H, int L, int d, float pos0, int chunk) {
+    int H, int L, int d, float pos0, int chunk, int fold_omega) {
   constexpr int U = 8;   // heads in flight per thread (the pass is HBM-bound)
   const int vecs = d / 8;
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -132,13 +136,14 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
       const int bh = bh0 + uu;
       if (bh >= BH) break;
       const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
+      const float wq = fold_omega ? gpow(cc.lg2g[bh % H], static_cast<float>((t % chunk) + 1 - chunk)) : 1.f;
       const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
       const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
       uint32_t qr[4], kr[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
-        qr[u] = pack_bf16x2(a * c[u] - b * s[u], fmaf(a, s[u], b * c[u]));
+        qr[u] = pack_bf16x2(wq * (a * c[u] - b * s[u]), wq * fmaf(a, s[u], b * c[u]));
         const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
         const float cz = zk * c[u], sz = zk * s[u];
         kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
@@ -167,7 +172,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
-  float* omega = reinterpret_cast<float*>(smem + C::OFF_OMEGA);
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,7 +196,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_alloc(sb + C::OFF_TPTR, C::T_COLS);
     tmem_relinquish();
   }
-  if (threadIdx.x < CH) omega[threadIdx.x] = gpow(cc.lg2g[h], static_cast<float>(static_cast<int>(threadIdx.x) + 1 - CH));
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       write_shat();
 
-      // ---- (d) Õ drain: release X, then ω_j scale and store ----
+      // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
       tc_fence_after();
       {
@@ -402,13 +405,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float* o = reinterpret_cast<float*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]);
+              o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
           } else {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
               o[static_cast<size_t>(c) * d_v] =
-                  __float2bfloat16_rn(omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]));
+                  __float2bfloat16_rn(__uint_as_float(r[c]));
           }
         }
       }

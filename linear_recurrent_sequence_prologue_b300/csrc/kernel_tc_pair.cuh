@@ -74,8 +74,7 @@ struct Cfg {
   static constexpr uint32_t OFF_KV = OFF_KQ + KQ_BYTES;
   static constexpr uint32_t OFF_V = OFF_KV + KV_BYTES;     // two slots
   static constexpr uint32_t OFF_P = OFF_V + 2 * V_BYTES;
-  static constexpr uint32_t OFF_OMEGA = OFF_P + P_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_OMEGA + CH * 4;
+  static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
   static constexpr uint32_t OFF_TPTR = OFF_BAR + NBAR_ * 8;
   static constexpr uint32_t USED = OFF_TPTR + 16;
   static constexpr uint32_t SMEM_BYTES = USED + 1024;     // slack for 1024-B alignment
@@ -100,7 +99,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t sb = smem_u32(smem);
   const uint32_t sQ = sb + C::OFF_Q, sKQ = sb + C::OFF_KQ, sKV = sb + C::OFF_KV;
   const uint32_t sV = sb + C::OFF_V, sP = sb + C::OFF_P;
-  float* omega = reinterpret_cast<float*>(smem + C::OFF_OMEGA);
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
   // The even CTA's barriers in the cluster window (offsets are preserved).
   const uint32_t lead_bar0 = mapa_shared(bar(0), 0);
@@ -130,7 +128,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tmem_alloc_pair(sb + C::OFF_TPTR, C::T_COLS);
     tmem_relinquish_pair();
   }
-  if (threadIdx.x < CH) omega[threadIdx.x] = gpow(cc.lg2g[h], static_cast<float>(static_cast<int>(threadIdx.x) + 1 - CH));
   // Both CTAs' barriers exist before any copy or arrival can target them.
   tc_fence_before();
   cluster_sync_all();
@@ -342,7 +339,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       write_shat();
 
-      // ---- (d) Õ drain: release X, then ω_j scale and store ----
+      // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
       tc_fence_after();
       {
@@ -363,13 +360,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             float* o = reinterpret_cast<float*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] = omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]);
+              o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
           } else {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
               o[static_cast<size_t>(c) * d_v] =
-                  __float2bfloat16_rn(omega[32 * cs + 16 * hf + c] * __uint_as_float(r[c]));
+                  __float2bfloat16_rn(__uint_as_float(r[c]));
           }
         }
       }

@@ -313,7 +313,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     const size_t n = static_cast<size_t>(L) * (d_k / 8);
     Mark m("rotate_qk_bf16", st);
     tcc::rotate_qk_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        q, k, qr, kr, cc, BH, H, L, d_k, static_cast<float>(pos0), tcc::CH);
+        q, k, qr, kr, cc, BH, H, L, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1);
   }
   CUtensorMap mq, mk, mv;
   const uint64_t rows = static_cast<uint64_t>(BH) * L;
