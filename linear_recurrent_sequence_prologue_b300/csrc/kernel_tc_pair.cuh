@@ -21,11 +21,17 @@
 // own fp32 state tile, as in the single-CTA kernel, and the results are
 // the same numbers in the same order.
 //
+// Per chunk the products are issued ΔS, QK, QS, PV.  The chain that bounds
+// a chunk is QK → P̂ drain → QS → PV → Õ drain → next QK (P̂ and Õᵀ share
+// TMEM columns), and ΔS of the next chunk, which needs neither, runs on
+// the tensor cores while the drains store Õ.  K̂′ is staged as two pieces
+// with their own barriers (the key half with all d_k for QK, all keys with
+// a d_k half for ΔS), each reloaded as soon as its product is done.
+//
 // Synchronisation: TMA loads of both CTAs count their bytes on the even
 // CTA's FULL barriers; pair commits arrive on the barriers of both CTAs;
-// drain warps of both CTAs arrive on the even CTA's barriers with
-// cluster-scope release, and the issuing thread waits on them with
-// cluster-scope acquire.
+// drain warps of both CTAs arrive on the even CTA's barriers (CTA-scope
+// release after their TMEM / shared-memory hand-off has completed).
 #pragma once
 
 #include "common.cuh"
@@ -43,8 +49,10 @@ using tcc::NTHREADS;
 using tcc::VT;
 
 enum Bar : int {
-  Q_FULL0 = 0, Q_FULL1, V_FULL0, V_FULL1, K_FULL,   // TMA → MMA (even CTA's copy counts)
-  Q_EMPTY0, Q_EMPTY1, V_EMPTY0, V_EMPTY1, K_EMPTY,  // MMA → TMA (both CTAs)
+  // TMA → MMA (the even CTA's copy counts both CTAs' bytes)
+  Q_FULL0 = 0, Q_FULL1, V_FULL0, V_FULL1, KQ_FULL, KV_FULL,
+  // MMA → TMA (both CTAs)
+  Q_EMPTY0, Q_EMPTY1, V_EMPTY0, V_EMPTY1, KQ_EMPTY, KV_EMPTY,
   P_FULL,     // QK done                      (MMA → drains)
   X_READ,     // P̂ read out of X              (drains → MMA)
   P_SMEM,     // P̂ halves in shared memory    (drains → MMA)
@@ -136,31 +144,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   if (warp == 0) {
     // ------------------------------ TMA producer ---------------------------
-    // Per chunk: Q′ rows of this CTA's query half, V tile, then K̂′ (its
-    // key half with all d_k, and all keys with its d_k half).  Q′ and V
-    // slots were freed a chunk earlier, so they land well ahead; K̂′ waits
-    // for ΔS of the previous chunk.
+    // Per chunk, in the order the products need them: the V tile and all
+    // keys with this CTA's d_k half (ΔS, first), then Q′ rows of this
+    // CTA's query half and its key half with all d_k (QK).  Each buffer is
+    // refilled as soon as the last product reading it has finished.
     if (lane == 0) {
       int issued = -1;
       const int yh = 64 * static_cast<int>(rank);
       for (int i = 0; i < nch; ++i) {
         const int y = bh * L + i * CH;
         const int s = i & 1;
-        if (i > 1 && !mbar_wait(bar(Q_EMPTY0 + s), static_cast<uint32_t>((i >> 1) - 1) & 1u, 0x102)) break;
-        if (rank == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + s), 2 * C::QH_BYTES);
-        for (int b = 0; b < C::QBOX; ++b)
-          tma_load_2d_pair(sQ + s * C::QH_BYTES + b * C::HBOX, &tm_qh, 64 * b, y + yh, lead_bar(Q_FULL0 + s));
-        if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), static_cast<uint32_t>((i >> 1) - 1) & 1u, 0x103)) break;
+        const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
+        const uint32_t ps = static_cast<uint32_t>((i >> 1) - 1) & 1u;
+        if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), ps, 0x103)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(V_FULL0 + s), 2 * C::V_BYTES);
         for (int b = 0; b < 2; ++b)
           tma_load_2d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, y, lead_bar(V_FULL0 + s));
-        if (i > 0 && !mbar_wait(bar(K_EMPTY), static_cast<uint32_t>(i - 1) & 1u, 0x101)) break;
-        if (rank == 0) mbar_arrive_expect_tx(bar(K_FULL), 2 * (C::KQ_BYTES + C::KV_BYTES));
-        for (int b = 0; b < C::QBOX; ++b)
-          tma_load_2d_pair(sKQ + b * C::HBOX, &tm_kh, 64 * b, y + yh, lead_bar(K_FULL));
+        if (i > 0 && !mbar_wait(bar(KV_EMPTY), pp, 0x104)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(KV_FULL), 2 * C::KV_BYTES);
         for (int b = 0; b < C::QBOX / 2; ++b)
           tma_load_2d_pair(sKV + b * C::BOX, &tm_k, 64 * (static_cast<int>(rank) * (C::QBOX / 2) + b), y,
-                           lead_bar(K_FULL));
+                           lead_bar(KV_FULL));
+        if (i > 1 && !mbar_wait(bar(Q_EMPTY0 + s), ps, 0x102)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + s), 2 * C::QH_BYTES);
+        for (int b = 0; b < C::QBOX; ++b)
+          tma_load_2d_pair(sQ + s * C::QH_BYTES + b * C::HBOX, &tm_qh, 64 * b, y + yh, lead_bar(Q_FULL0 + s));
+        if (i > 0 && !mbar_wait(bar(KQ_EMPTY), pp, 0x101)) break;
+        if (rank == 0) mbar_arrive_expect_tx(bar(KQ_FULL), 2 * C::KQ_BYTES);
+        for (int b = 0; b < C::QBOX; ++b)
+          tma_load_2d_pair(sKQ + b * C::HBOX, &tm_kh, 64 * b, y + yh, lead_bar(KQ_FULL));
         issued = i;
       }
       // Never leave with copies still landing: the even CTA's FULL barriers
@@ -171,7 +183,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_wait(bar(Q_FULL0 + (c & 1)), ph, 0x1f2, kWaitBudgetCycles / 16);
           mbar_wait(bar(V_FULL0 + (c & 1)), ph, 0x1f3, kWaitBudgetCycles / 16);
         }
-        mbar_wait(bar(K_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f1, kWaitBudgetCycles / 16);
+        mbar_wait(bar(KQ_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f1, kWaitBudgetCycles / 16);
+        mbar_wait(bar(KV_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f4, kWaitBudgetCycles / 16);
       }
     }
   } else if (warp == 1) {
@@ -218,29 +231,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t pq = static_cast<uint32_t>(i >> 1) & 1u;
         dQ = s ? dQ1 : dQ0;
         dV = s ? dV1 : dV0;
-        // 1. P̂ = Q′ K̂′ᵀ into X (needs Õ of the previous chunk read out)
-        if (!mbar_wait_cl(bar(K_FULL), pi, 0x201)) break;
-        if (!mbar_wait_cl(bar(Q_FULL0 + s), pq, 0x202)) break;
-        if (i > 0 && !mbar_wait_cl(bar(X_FREE), pp, 0x203)) break;
-        tc_fence_after();
-        static_for<DK / 16>(issue_qk);
-        mma_commit_pair(bar(P_FULL));
-        // 2. ΔSᵀ = Vᵀ K̂′ into D (needs the previous ΔS read out)
-        if (!mbar_wait_cl(bar(V_FULL0 + s), pq, 0x204)) break;
-        if (i > 0 && !mbar_wait_cl(bar(DS_FREE), pp, 0x205)) break;
+        // 1. ΔSᵀ = Vᵀ K̂′ into D (needs the previous ΔS read out); issued
+        // right after PV of the previous chunk, it runs during that Õ drain
+        if (!mbar_wait_cl(bar(KV_FULL), pi, 0x201)) break;
+        if (!mbar_wait_cl(bar(V_FULL0 + s), pq, 0x202)) break;
+        if (i > 0 && !mbar_wait_cl(bar(DS_FREE), pp, 0x203)) break;
         tc_fence_after();
         static_for<CH / 16>(issue_kv);
         mma_commit_pair(bar(DS_FULL));
-        mma_commit_pair(bar(K_EMPTY));
+        mma_commit_pair(bar(KV_EMPTY));
+        // 2. P̂ = Q′ K̂′ᵀ into X (needs Õ of the previous chunk read out)
+        if (!mbar_wait_cl(bar(KQ_FULL), pi, 0x204)) break;
+        if (!mbar_wait_cl(bar(Q_FULL0 + s), pq, 0x205)) break;
+        if (i > 0 && !mbar_wait_cl(bar(X_FREE), pp, 0x206)) break;
+        tc_fence_after();
+        static_for<DK / 16>(issue_qk);
+        mma_commit_pair(bar(P_FULL));
+        mma_commit_pair(bar(KQ_EMPTY));
         // 3. Õᵀ = Ŝᵀ Q′ᵀ into X (needs P̂ read out and Ŝ of this chunk)
-        if (!mbar_wait_cl(bar(X_READ), pi, 0x206)) break;
-        if (!mbar_wait_cl(bar(SH_READY), pi, 0x207)) break;
+        if (!mbar_wait_cl(bar(X_READ), pi, 0x207)) break;
+        if (!mbar_wait_cl(bar(SH_READY), pi, 0x208)) break;
         tc_fence_after();
         static_for<DK / 16>(issue_qs);
         mma_commit_pair(bar(Q_EMPTY0 + s));
         mma_commit_pair(bar(SH_FREE));
         // 4. Õᵀ += Vᵀ P̂ᵀ (needs both P̂ halves in shared memory)
-        if (!mbar_wait_cl(bar(P_SMEM), pi, 0x208)) break;
+        if (!mbar_wait_cl(bar(P_SMEM), pi, 0x209)) break;
         tc_fence_after();
         static_for<CH / 16>(issue_pv);
         mma_commit_pair(bar(O_FULL));
