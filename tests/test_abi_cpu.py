@@ -114,6 +114,12 @@ def test_step_and_rotate_validation(lib):
     assert st == _lib.RET_EINVAL
     assert lib.ret_selftest_timeout(0, None) == _lib.RET_EINVAL
     assert lib.ret_force_path(5) == _lib.RET_EINVAL
+    # the one-CTA tensor-core variant is selectable; plans still report the tensor-core path
+    assert lib.ret_force_path(_lib.RET_PATH_TC_SINGLE) == _lib.RET_OK
+    try:
+        assert _plan(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128)[0] == _lib.RET_PATH_TC
+    finally:
+        assert lib.ret_force_path(0) == _lib.RET_OK
 
 
 def _plan(lib, in_dt, B, H, L, d_k, d_v, chunk, gn=0, gamma=None):
