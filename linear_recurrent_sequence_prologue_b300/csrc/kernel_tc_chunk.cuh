@@ -82,14 +82,23 @@ struct Cfg {
 };
 
 struct ChunkArgs {
-  const float* state_in;   // [BH][DK][d_v] or nullptr
+  const float* state_in;   // per grid row [DK][d_v], or nullptr
   float* state_out;        // or nullptr
-  void* out;               // [BH][L][d_v] bf16, or fp32 when out_f32; nullptr: no output
+  void* out;               // [BH][seq_len][d_v] bf16, or fp32 when out_f32; nullptr: no output
   int out_f32;
-  int H, L, d_v, nchunks;
+  int H, d_v;
+  int nchunks;             // chunks this CTA walks
+  // One sequence: seq_len tokens (any length), seq_chunks chunks of 128,
+  // seq_lp = 128·seq_chunks rows of it in the rotated Q′ / K̂′ workspace
+  // (rows past seq_len are zero).  The last chunk has seq_len − 128·(seq_chunks−1)
+  // tokens and carries with γ^that instead of γ^128.
+  int seq_len, seq_lp, seq_chunks;
+  void* tail_out;          // staging [sequences][128][d_v] (out's type) for a short
+                           // last chunk, or nullptr when seq_len is a multiple of 128
   // Chunk-parallel layout: the rows of grid.y are (sequence, chunk) pairs of
-  // one chunk each, head = (blockIdx.y / seq_div) % H.  raw_ds: state_out
-  // receives the chunk's ΔS itself instead of fmaf(γ^b, S, ΔS).
+  // one chunk each: sequence = blockIdx.y / seq_div, chunk = blockIdx.y % seq_div,
+  // head = sequence % H.  raw_ds: state_out receives the chunk's ΔS itself
+  // instead of fmaf(γ^b, S, ΔS).
   int seq_div, raw_ds;
 };
 
@@ -101,25 +110,39 @@ struct ChunkArgs {
 // accumulator as it is.
 // Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by all
 // B·H heads of that row, eight heads' loads in flight at a time; raw q and
-// k are read with the evict-first hint.
+// k are read with the evict-first hint.  q, k have L rows per head; Q′, K̂′
+// have Lp = 128·⌈L/128⌉ rows per head, the rows past L written as zeros, and
+// the last chunk's factors use its own length b_c (ζ = γ^{b_c−1−(t mod b)},
+// ω = γ^{(t mod b)+1−b_c}).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) rotate_qk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ qo, __nv_bfloat16* __restrict__ ko, CallConsts cc, int BH,
-    int H, int L, int d, float pos0, int chunk, int fold_omega) {
+    int H, int L, int Lp, int d, float pos0, int chunk, int fold_omega) {
   constexpr int U = 8;   // heads in flight per thread (the pass is HBM-bound)
   const int vecs = d / 8;
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<size_t>(L) * vecs) return;
+  if (idx >= static_cast<size_t>(Lp) * vecs) return;
   // Positions are walked last to first, so the first chunks the main kernel
   // reads are the last ones written and are still in L2.
   const int tt = static_cast<int>(idx / vecs), cidx = static_cast<int>(idx % vecs);
-  const int t = L - 1 - tt;
+  const int t = Lp - 1 - tt;
+  const size_t ostride = static_cast<size_t>(Lp) * d;   // output elements between heads
+  const size_t oofs = static_cast<size_t>(t) * d + 8 * cidx;
+  if (t >= L) {   // padding rows of the last chunk
+    for (int bh = 0; bh < BH; ++bh) {
+      *reinterpret_cast<uint4*>(qo + oofs + static_cast<size_t>(bh) * ostride) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(ko + oofs + static_cast<size_t>(bh) * ostride) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
   float c[4], s[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cidx + u], c[u], s[u]);
-  const float e = static_cast<float>(chunk - 1 - (t % chunk));
-  const size_t hstride = static_cast<size_t>(L) * d;   // elements between heads
+  const int bc = (t / chunk == Lp / chunk - 1) ? L - (Lp - chunk) : chunk;   // length of t's chunk
+  const float e = static_cast<float>(bc - 1 - (t % chunk));
+  const float ew = static_cast<float>((t % chunk) + 1 - bc);
+  const size_t hstride = static_cast<size_t>(L) * d;   // input elements between heads
   const size_t off0 = static_cast<size_t>(t) * d + 8 * cidx;
   for (int bh0 = 0; bh0 < BH; bh0 += U) {
     uint4 qv[U], kv[U];
@@ -136,7 +159,7 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
       const int bh = bh0 + uu;
       if (bh >= BH) break;
       const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
-      const float wq = fold_omega ? gpow(cc.lg2g[bh % H], static_cast<float>((t % chunk) + 1 - chunk)) : 1.f;
+      const float wq = fold_omega ? gpow(cc.lg2g[bh % H], ew) : 1.f;
       const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
       const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
       uint32_t qr[4], kr[4];
@@ -148,11 +171,26 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
         const float cz = zk * c[u], sz = zk * s[u];
         kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
       }
-      const size_t off = off0 + static_cast<size_t>(bh) * hstride;
+      const size_t off = oofs + static_cast<size_t>(bh) * ostride;
       *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
       *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
     }
   }
+}
+
+// ---------------------------------------------------------------------------
+// Rows 0 … T−1 of each sequence's staged last chunk ([BH][128][row_vecs]
+// 16-byte vectors) to rows row0 … row0+T−1 of out ([BH][L][row_vecs]).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tail_copy_kernel(const uint4* __restrict__ src,
+                                                        uint4* __restrict__ dst, int BH, int T,
+                                                        int L, int row0, int row_vecs) {
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t per = static_cast<size_t>(T) * row_vecs;
+  if (idx >= per * BH) return;
+  const size_t bh = idx / per, rem = idx % per;
+  const size_t r = rem / row_vecs, c = rem % row_vecs;
+  dst[(bh * L + row0 + r) * row_vecs + c] = src[(bh * CH + r) * row_vecs + c];
 }
 
 // ---------------------------------------------------------------------------
@@ -177,9 +215,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
   const int bh = blockIdx.y;
-  const int h = (bh / args.seq_div) % args.H;
-  const int L = args.L, d_v = args.d_v, nch = args.nchunks;
-  const float gb = cc.gb[h];
+  const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
+  const int h = seq % args.H;
+  const int d_v = args.d_v, nch = args.nchunks;
+  // γ^{b_c} of chunk c of the sequence (its last chunk may be shorter)
+  auto gch = [&](int c) -> float { return c == args.seq_chunks - 1 ? cc.gtail[h] : cc.gb[h]; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_q);
@@ -208,7 +248,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int issued = -1;   // last chunk whose loads were all issued
       for (int i = 0; i < nch; ++i) {
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
-        const int y = bh * L + i * CH;
+        const int y = seq * args.seq_lp + (c0 + i) * CH;   // row of Q′ / K̂′
+        const int yv = (c0 + i) * CH;                       // row of V within the sequence
         if (i > 0 && !mbar_wait(bar(K_EMPTY), pp, 0x101)) break;
         mbar_arrive_expect_tx(bar(K_FULL), C::Q_BYTES);
         for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL));
@@ -217,7 +258,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sQ + b * C::BOX, &tm_q, 64 * b, y, bar(Q_FULL));
         if (i > 0 && !mbar_wait(bar(V_EMPTY), pp, 0x103)) break;
         mbar_arrive_expect_tx(bar(V_FULL), C::V_BYTES);
-        for (int b = 0; b < 2; ++b) tma_load_2d(sV + b * C::BOX, &tm_v, v0 + 64 * b, y, bar(V_FULL));
+        for (int b = 0; b < 2; ++b) tma_load_3d(sV + b * C::BOX, &tm_v, v0 + 64 * b, yv, seq, bar(V_FULL));
         issued = i;
       }
       if (issued >= 0 && status_aborted()) {
@@ -305,13 +346,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
 
     // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
-    auto write_shat = [&]() {
+    auto write_shat = [&](float g) {
 #pragma unroll
       for (int c = 0; c < C::SPT / 16; ++c) {
         uint32_t pk[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          pk[u] = pack_bf16x2(gb * S[c * 16 + 2 * u], gb * S[c * 16 + 2 * u + 1]);
+          pk[u] = pack_bf16x2(g * S[c * 16 + 2 * u], g * S[c * 16 + 2 * u + 1]);
         tmem_st8(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 16) / 2, pk);
       }
       tmem_st_wait();
@@ -319,11 +360,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SH_READY));
     };
-    write_shat();
+    write_shat(gch(c0));
 
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
       const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+      const float gi = gch(c0 + i);
       // ---- (a) P̂ drain: causal mask, bf16, into the K-major swizzled tile ----
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
@@ -372,7 +414,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int u = 0; u < 16; ++u)
-          S[16 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gb, S[16 * c + u], __uint_as_float(d[u]));
+          S[16 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gi, S[16 * c + u], __uint_as_float(d[u]));
       }
       tc_fence_before();
       __syncwarp();
@@ -381,13 +423,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
       if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
       tc_fence_after();
-      write_shat();
+      write_shat(gch(c0 + i + 1));
 
       // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
       tc_fence_after();
       {
-        const size_t base = (static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs) * d_v + v0 + vl;
+        // A short last chunk goes whole to the staging tile [sequence][128][d_v]
+        // (a copy kernel then moves its valid rows), so no store needs a check.
+        const bool staged = args.tail_out && c0 + i == args.seq_chunks - 1;
+        void* const obuf = staged ? args.tail_out : args.out;
+        const size_t base = staged
+            ? (static_cast<size_t>(seq) * CH + 32 * cs) * d_v + v0 + vl
+            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(c0 + i) * CH + 32 * cs) * d_v + v0 + vl;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[16];
@@ -402,16 +450,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
           if (!args.out) {
           } else if (args.out_f32) {
-            float* o = reinterpret_cast<float*>(args.out) + gb0;
+            float* o = reinterpret_cast<float*>(obuf) + gb0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
+            for (int c = 0; c < 16; ++c) o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
           } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(obuf) + gb0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] =
-                  __float2bfloat16_rn(__uint_as_float(r[c]));
+            for (int c = 0; c < 16; ++c) o[static_cast<size_t>(c) * d_v] = __float2bfloat16_rn(__uint_as_float(r[c]));
           }
         }
       }

@@ -116,9 +116,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
   const int bh = blockIdx.y;
-  const int h = (bh / args.seq_div) % args.H;
-  const int L = args.L, d_v = args.d_v, nch = args.nchunks;
-  const float gb = cc.gb[h];
+  const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
+  const int h = seq % args.H;
+  const int d_v = args.d_v, nch = args.nchunks;
+  // γ^{b_c} of chunk c of the sequence (its last chunk may be shorter)
+  auto gch = [&](int c) -> float { return c == args.seq_chunks - 1 ? cc.gtail[h] : cc.gb[h]; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_qh);
@@ -152,14 +154,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int issued = -1;
       const int yh = 64 * static_cast<int>(rank);
       for (int i = 0; i < nch; ++i) {
-        const int y = bh * L + i * CH;
+        const int y = seq * args.seq_lp + (c0 + i) * CH;   // row of Q′ / K̂′
+        const int yv = (c0 + i) * CH;                       // row of V within the sequence
         const int s = i & 1;
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
         const uint32_t ps = static_cast<uint32_t>((i >> 1) - 1) & 1u;
         if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), ps, 0x103)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(V_FULL0 + s), 2 * C::V_BYTES);
         for (int b = 0; b < 2; ++b)
-          tma_load_2d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, y, lead_bar(V_FULL0 + s));
+          tma_load_3d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, yv, seq, lead_bar(V_FULL0 + s));
         if (i > 0 && !mbar_wait(bar(KV_EMPTY), pp, 0x104)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(KV_FULL), 2 * C::KV_BYTES);
         for (int b = 0; b < C::QBOX / 2; ++b)
@@ -286,24 +289,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive_cluster(mapa_shared(bar(b), 0));
     };
     // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
-    auto write_shat = [&]() {
+    auto write_shat = [&](float g) {
 #pragma unroll
       for (int c = 0; c < C::SPT / 16; ++c) {
         uint32_t pk[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          pk[u] = pack_bf16x2(gb * S[c * 16 + 2 * u], gb * S[c * 16 + 2 * u + 1]);
+          pk[u] = pack_bf16x2(g * S[c * 16 + 2 * u], g * S[c * 16 + 2 * u + 1]);
         tmem_st8(tmem + C::T_SH + lane_off + (kr * C::SPT + c * 16) / 2, pk);
       }
       tmem_st_wait();
       tc_fence_before();
       arrive_lead(SH_READY);
     };
-    write_shat();
+    write_shat(gch(c0));
 
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
       const uint32_t pi = static_cast<uint32_t>(i) & 1u;
+      const float gi = gch(c0 + i);
       // ---- (a) P̂ drain: causal mask, bf16, into this CTA's query half ----
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          S[8 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gb, S[8 * c + u], __uint_as_float(d[u]));
+          S[8 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gi, S[8 * c + u], __uint_as_float(d[u]));
       }
       tc_fence_before();
       arrive_lead(DS_FREE);
@@ -353,13 +357,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
       if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
       tc_fence_after();
-      write_shat();
+      write_shat(gch(c0 + i + 1));
 
       // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
       tc_fence_after();
       {
-        const size_t base = (static_cast<size_t>(bh) * L + static_cast<size_t>(i) * CH + 32 * cs) * d_v + v0 + vl;
+        // A short last chunk goes whole to the staging tile [sequence][128][d_v]
+        // (a copy kernel then moves its valid rows), so no store needs a check.
+        const bool staged = args.tail_out && c0 + i == args.seq_chunks - 1;
+        void* const obuf = staged ? args.tail_out : args.out;
+        const size_t base = staged
+            ? (static_cast<size_t>(seq) * CH + 32 * cs) * d_v + v0 + vl
+            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(c0 + i) * CH + 32 * cs) * d_v + v0 + vl;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[16];
@@ -373,16 +383,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
           if (!args.out) {
           } else if (args.out_f32) {
-            float* o = reinterpret_cast<float*>(args.out) + gb0;
+            float* o = reinterpret_cast<float*>(obuf) + gb0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
+            for (int c = 0; c < 16; ++c) o[static_cast<size_t>(c) * d_v] = __uint_as_float(r[c]);
           } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(args.out) + gb0;
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(obuf) + gb0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              o[static_cast<size_t>(c) * d_v] =
-                  __float2bfloat16_rn(__uint_as_float(r[c]));
+            for (int c = 0; c < 16; ++c) o[static_cast<size_t>(c) * d_v] = __float2bfloat16_rn(__uint_as_float(r[c]));
           }
         }
       }

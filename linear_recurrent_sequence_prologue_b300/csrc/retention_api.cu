@@ -139,6 +139,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [n][rows][cols] bf16 viewed in 3-D with boxes of 64 columns × box_rows rows
+// of one matrix: rows past `rows` read as zeros (never the next matrix's).
+bool make_map3(CUtensorMap* m, const void* base, uint64_t n, uint64_t rows, uint64_t cols,
+               uint32_t box_rows = 128) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[3] = {cols, rows, n};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // Path choice
 // ---------------------------------------------------------------------------
@@ -158,7 +173,7 @@ bool tc_chunk_ok(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int
   if (g_force_path == RET_PATH_SIMT) return false;
   if (in_dt != RET_BF16) return false;
   if (!(d_k == 64 || d_k == 128 || d_k == 256)) return false;
-  if (d_v % tcc::VT != 0 || chunk != tcc::CH || L % tcc::CH != 0) return false;
+  if (d_v % tcc::VT != 0 || chunk != tcc::CH || L < 1) return false;
   return tc_gamma_ok(gamma, H, chunk);
 }
 
@@ -174,6 +189,7 @@ struct Plan {
   size_t bytes = 0;
   // workspace offsets
   size_t off_q = 0, off_k = 0, off_states = 0, off_ofp32 = 0;
+  size_t off_tail = 0;   // staging of a short last chunk's outputs (tensor-core path)
 };
 
 // Grid rows of the tensor-core launches: B·H (carry layout) or B·H·L/128
@@ -189,9 +205,12 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
   if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk) &&
       (scan ? BH * nch : BH) <= kMaxGridRows) {
     p.path = RET_PATH_TC;
-    p.off_q = off; off += up256(BH * L * d_k * 2);
-    p.off_k = off; off += up256(BH * L * d_k * 2);
+    // rotated Q′ / K̂′, each sequence padded with zero rows to whole chunks
+    const size_t Lp = static_cast<size_t>(nch) * tcc::CH;
+    p.off_q = off; off += up256(BH * Lp * d_k * 2);
+    p.off_k = off; off += up256(BH * Lp * d_k * 2);
     if (scan) { p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4); }
+    if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * static_cast<size_t>(d_v) * 4); }
   } else {
     p.path = RET_PATH_SIMT;
     p.off_q = off; off += up256(BH * L * d_k * 4);
@@ -208,7 +227,7 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   size_t off = 0;
-  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && BH <= kMaxGridRows &&
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && L % tcc::CH == 0 && BH <= kMaxGridRows &&
       static_cast<size_t>(L / tcc::CH) <= kMaxGridRows &&
       (!want_state || BH * (L / tcc::CH) <= kMaxGridRows)) {
     // rotated Q′ / K̂′ in bf16; per-block ΔS states when state_out is wanted
@@ -309,31 +328,40 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   const int BH = B * H;
   __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
+  const int nch = (L + tcc::CH - 1) / tcc::CH;
+  const int Lp = nch * tcc::CH;   // rows per sequence in the rotated workspace
   {
-    const size_t n = static_cast<size_t>(L) * (d_k / 8);
+    const size_t n = static_cast<size_t>(Lp) * (d_k / 8);
     Mark m("rotate_qk_bf16", st);
     tcc::rotate_qk_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        q, k, qr, kr, cc, BH, H, L, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1);
+        q, k, qr, kr, cc, BH, H, L, Lp, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1);
   }
-  CUtensorMap mq, mk, mv;
-  const uint64_t rows = static_cast<uint64_t>(BH) * L;
-  if (!make_map(&mq, qr, rows, d_k) || !make_map(&mk, kr, rows, d_k) || !make_map(&mv, v, rows, d_v))
+  // Q′ / K̂′: the padded workspace, flat; V: [B·H][L][d_v] in 3-D for the
+  // chunk kernels (a short last chunk reads zeros past L), flat for the
+  // parallel form (L a multiple of 128 there).
+  CUtensorMap mq, mk, mv, mv2;
+  const uint64_t rows = static_cast<uint64_t>(BH) * Lp;
+  if (!make_map(&mq, qr, rows, d_k) || !make_map(&mk, kr, rows, d_k) ||
+      !make_map3(&mv, v, static_cast<uint64_t>(BH), static_cast<uint64_t>(L), d_v) ||
+      (parallel && !make_map(&mv2, v, static_cast<uint64_t>(BH) * L, d_v)))
     return RET_ECUDA;
   const bool pair = tc_pair_ok(d_k, d_v);
   CUtensorMap mqh, mkh;   // 64-row boxes of Q′ / K̂′ for the pair kernel
   if (pair && (!make_map(&mqh, qr, rows, d_k, 64) || !make_map(&mkh, kr, rows, d_k, 64)))
     return RET_ECUDA;
   float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
-  const int nch = L / tcc::CH;
   tcc::ChunkArgs a;
   a.state_in = s_in;
   a.state_out = s_out;
   a.out = ofp ? static_cast<void*>(ofp) : static_cast<void*>(out);
   a.out_f32 = (ofp || sizeof(Tout) == 4) ? 1 : 0;
   a.H = H;
-  a.L = L;
   a.d_v = d_v;
   a.nchunks = nch;
+  a.seq_len = L;
+  a.seq_lp = Lp;
+  a.seq_chunks = nch;
+  a.tail_out = (L % tcc::CH != 0 && a.out) ? wsp<void>(ws, p.off_tail) : nullptr;
   a.seq_div = 1;
   a.raw_ds = 0;
   auto launch = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args, int rows,
@@ -390,7 +418,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
                                             static_cast<int>(smem));
       if (e2 != cudaSuccess) return e2;
       Mark m("parallel_tc", st);
-      kern<<<dim3(d_v / tcp::VT, BH, nch), tcp::NTHREADS, smem, st>>>(mq, mk, mv, pa, cc);
+      kern<<<dim3(d_v / tcp::VT, BH, nch), tcp::NTHREADS, smem, st>>>(mq, mk, mv2, pa, cc);
       return cudaGetLastError();
     };
     if (d_k == 256) e = plaunch(tcp::parallel_tc_kernel<256>, tcp::Cfg<256>::SMEM_BYTES);
@@ -399,13 +427,13 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     if (e == cudaSuccess && s_out) {   // closed-form final state: ΔS per block, then the scan
       float* states = wsp<float>(ws, p.off_states);
       tcc::ChunkArgs d = a;
-      d.L = tcc::CH;
       d.nchunks = 1;
       d.seq_div = nch;
       d.raw_ds = 1;
       d.state_in = nullptr;
       d.state_out = states;
       d.out = nullptr;
+      d.tail_out = nullptr;
       e = run(d, BH * nch, "chunk_tc_dS");
       if (e == cudaSuccess) {
         const size_t n = static_cast<size_t>(BH) * d_k * d_v;
@@ -421,13 +449,13 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     // The [BH, L, d] tensors viewed as [BH·nch, 128, d]: one chunk per row.
     float* states = wsp<float>(ws, p.off_states);
     tcc::ChunkArgs d = a;
-    d.L = tcc::CH;
     d.nchunks = 1;
     d.seq_div = nch;
     d.raw_ds = 1;
     d.state_in = nullptr;
     d.state_out = states;   // ΔS of every chunk
     d.out = nullptr;
+    d.tail_out = nullptr;
     e = run(d, BH * nch, "chunk_tc_dS");
     if (e == cudaSuccess) {
       const size_t n = static_cast<size_t>(BH) * d_k * d_v;
@@ -438,7 +466,6 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     }
     if (e == cudaSuccess) {
       tcc::ChunkArgs o = a;
-      o.L = tcc::CH;
       o.nchunks = 1;
       o.seq_div = nch;
       o.state_in = states;    // state entering every chunk
@@ -447,6 +474,16 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     }
   }
   if (e != cudaSuccess) return RET_ECUDA;
+  if (a.tail_out && !parallel) {   // the short last chunk's valid rows, from the staging tile
+    const int T = L - (nch - 1) * tcc::CH;
+    const int row_vecs = d_v * (a.out_f32 ? 4 : 2) / 16;
+    const size_t n = static_cast<size_t>(BH) * T * row_vecs;
+    Mark m("tail_copy", st);
+    tcc::tail_copy_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint4*>(a.tail_out), static_cast<uint4*>(a.out), BH, T, L, (nch - 1) * tcc::CH,
+        row_vecs);
+    if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  }
   if (ofp) {
     const size_t r = static_cast<size_t>(BH) * L;
     Mark m("groupnorm", st);

@@ -146,6 +146,14 @@ def test_path_selection(lib):
                                  C.byref(path), C.byref(nb2)) == _lib.RET_OK
     assert path.value == _lib.RET_PATH_TC and nb2.value == nb   # rotated Q′ / K̂′ only
     # fp32 inputs, chunk 64, d_v 64 → fp32 kernels
+    # a length that is not a multiple of the chunk stays on the tensor cores, with
+    # the rotated Q′ / K̂′ padded to whole chunks; the parallel form needs whole blocks
+    p, nb = _plan(lib, _lib.RET_BF16, 2, 16, 8000, 256, 512, 128)
+    # (+ an fp32 staging tile of 128 rows per sequence for the short last chunk's outputs)
+    assert p == _lib.RET_PATH_TC and nb == 2 * 2 * 16 * 8064 * 256 * 2 + 2 * 16 * 128 * 512 * 4
+    assert lib.ret_parallel_plan(_lib.RET_BF16, None, 2, 16, 8000, 256, 512, _lib.RET_BF16, 0, 0,
+                                 C.byref(path), C.byref(nb2)) == _lib.RET_OK
+    assert path.value == _lib.RET_PATH_SIMT
     assert _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)[0] == _lib.RET_PATH_SIMT
     assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64)[0] == _lib.RET_PATH_SIMT
     # a head whose γ^127 underflows the rewritten form goes to the fp32 kernels

@@ -239,6 +239,54 @@ def test_tc_pair_kernel_matches_single_cta_kernel(d_k, d_v, L, H):
     assert_close(gpu_np(s), ref_s, torch.bfloat16, "pair state")
 
 
+@pytest.mark.parametrize("d_k,d_v,L,H", [
+    (256, 512, 300, 2),    # pair kernel, short last chunk of 44
+    (256, 256, 1000, 1),   # pair kernel, 8 chunks, last of 104
+    (256, 256, 77, 2),     # pair kernel, one short chunk
+    (128, 128, 200, 2),    # one-CTA kernel
+    (64, 128, 129, 2),     # one-CTA kernel, last chunk of 1 token
+])
+def test_tc_ragged_length_vs_oracle(d_k, d_v, L, H):
+    """L not a multiple of the chunk on the tensor-core path: the rotated
+    workspace is padded with zero rows, V is read per head (zeros past L),
+    the last chunk carries with γ^{L mod 128} and its outputs stop at L.
+    Against the oracle; carry and chunk-parallel layouts agree bit for bit,
+    and so do the pair and one-CTA kernels."""
+    w, inp = _custom(2, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1, seed=L + d_k)
+    path, _ = R.plan("chunkwise", torch.bfloat16, 2, H, L, d_k, d_v, 128, gamma=inp["gamma"])
+    assert path == R.RET_PATH_TC
+    d = _cuda(inp)
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", 128, pos0=21)
+    res = {}
+    try:
+        for mode in (0, R.RET_PATH_TC_SINGLE):
+            R.force_path(mode)
+            for odt in (torch.bfloat16, torch.float32):
+                for layout in ("carry", "scan"):
+                    res[mode, odt, layout] = R.chunkwise(
+                        d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=21,
+                        state_in=d["state_in"], out_dtype=odt, layout=layout)
+                    assert R.sync_status() == R.RET_OK
+    finally:
+        R.force_path(0)
+    for (mode, odt, layout), (o, s) in res.items():
+        o0, s0 = res[0, odt, "carry"]
+        assert torch.equal(s, s0), (mode, odt, layout)
+        assert torch.equal(o, o0), (mode, odt, layout)
+    o, s = res[0, torch.float32, "carry"]
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "ragged out")
+    assert_close(gpu_np(s), ref_s, torch.bfloat16, "ragged state")
+    # nothing is written past row L of any head: the output is a view at the
+    # start of a NaN-filled buffer whose tail (a chunk's worth of rows) must stay NaN
+    n = 2 * H * L * d_v
+    big = torch.full((n + 128 * d_v,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o2, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=21,
+                        state_in=d["state_in"], out=big[:n].view(2, H, L, d_v))
+    assert R.sync_status() == R.RET_OK
+    assert torch.equal(o2, res[0, torch.bfloat16, "carry"][0])
+    assert torch.isnan(big[n:].float()).all()
+
+
 @pytest.mark.parametrize("d_k,d_v,L,H,state", [(64, 128, 256, 1, False), (128, 256, 384, 2, True),
                                                (256, 512, 512, 2, True)])
 def test_tc_parallel_form_vs_oracle(d_k, d_v, L, H, state):

@@ -39,8 +39,9 @@ def _noalloc(lib, inp, w, pos0, out, state_out):
 
 @pytest.mark.parametrize("w", [
     Workload("tc", 1, 2, 512, 256, 256, "bf16", 128, 1.0, state_std=0.1),    # tensor-core path
+    Workload("tc_ragged", 1, 2, 300, 256, 256, "bf16", 128, 1.0, state_std=0.1),  # short last chunk
     Workload("fp32", 2, 3, 96, 32, 24, "f32", 32, 1.0, state_std=0.1),       # fp32 path
-], ids=["tensor_core", "fp32"])
+], ids=["tensor_core", "tensor_core_ragged", "fp32"])
 def test_noalloc_matches_chunkwise_on_two_calls(w):
     build.build()
     lib = R.load()
