@@ -343,13 +343,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (!mbar_wait(bar(DS_FULL), pi, 0x302)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < C::SPT / 8; ++c) {   // 8 columns per load: S stays in registers
-        uint32_t d[8];
-        tmem_ld8(tmem + C::T_D + lane_off + kr * C::SPT + c * 8, d);
+      for (int c = 0; c < C::SPT / 16; ++c) {   // 16 columns per wait
+        uint32_t d[16];
+        tmem_ld16(tmem + C::T_D + lane_off + kr * C::SPT + c * 16, d);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          S[8 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gi, S[8 * c + u], __uint_as_float(d[u]));
+        for (int u = 0; u < 16; ++u)
+          S[16 * c + u] = args.raw_ds ? __uint_as_float(d[u]) : fmaf(gi, S[16 * c + u], __uint_as_float(d[u]));
       }
       tc_fence_before();
       arrive_lead(DS_FREE);
