@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           } else {
             __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(obuf) + gb0;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) o[static_cast<size_t>(c) * d_v] = __float2bfloat16_rn(__uint_as_float(r[c]));
+            for (int c = 0; c < 16; ++c)   // streaming stores: the output is not read again here
+              __stcs(reinterpret_cast<unsigned short*>(o + static_cast<size_t>(c) * d_v),
+                     __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[c]))));
           }
         }
       }

@@ -274,19 +274,23 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_bar) : "memory");
 }
+// The arrivals it waits for come from both CTAs of a pair, each a CTA-scope
+// release issued after that thread's hand-off (TMEM access waited for, shared
+// memory fenced to the async proxy) was complete; a CTA-scope acquire
+// suffices, as for the local barriers.
 __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait with cluster-scope acquire (the phase may have been completed
-// by arrivals from the peer CTA); same budget and status rules as mbar_wait.
+// Bounded wait on a barrier that the peer CTA also arrives on; same budget
+// and status rules as mbar_wait.
 __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, unsigned where,
                                              long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait_cl(bar, parity)) return true;
