@@ -28,8 +28,12 @@
  *           pointers owned by the caller.  gamma[H] and theta[d_k/2] are HOST
  *           arrays, read during the call only.  The library allocates no
  *           device memory in any call.
- * Dtypes    RET_BF16 inputs run on the tensor cores (fp32 accumulate);
- *           RET_F32 inputs run on fp32 FFMA kernels.  out may be bf16 or fp32.
+ * Dtypes    RET_BF16 inputs run on the tensor cores (fp32 accumulate) when
+ *           d_k ∈ {64, 128, 256}, d_v is a multiple of 128, chunk = 128 and
+ *           every head has γ^127 ≥ 2^-60 (any L for the chunkwise entry
+ *           points, L a multiple of 128 for ret_parallel); other bf16 calls
+ *           and RET_F32 inputs run on fp32 FFMA kernels.  ret_*_plan reports
+ *           the path.  out may be bf16 or fp32.
  * Sizes     1 ≤ H ≤ 128; d_k even, 2 ≤ d_k ≤ 512; 1 ≤ d_v ≤ 1024;
  *           0 ≤ pos0 and pos0 + L ≤ 2^24 (positions are exact in fp32);
  *           every pointer 16-byte aligned; 0 < γ_h ≤ 1; θ finite.
