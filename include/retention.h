@@ -107,6 +107,19 @@ ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype 
                          void* out, ret_dtype out_dt, const ret_gn* gn,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ret_chunkwise with one start position per batch row: the tokens of row b
+ * sit at positions row_pos0[b] … row_pos0[b] + L − 1 (row_pos0: HOST array
+ * of B values, each ≥ 0 with row_pos0[b] + L ≤ 2^24).  B ≤ 256, else
+ * RET_EUNSUPPORTED; row_pos0 == NULL is RET_EINVAL.  Same layouts, workspace
+ * (ret_chunkwise_plan), paths and results as ret_chunkwise, which it equals
+ * bit for bit when every row_pos0[b] equals its pos0. */
+ret_status ret_chunkwise_rowpos(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                                const float* gamma, const float* theta,
+                                int B, int H, int L, int d_k, int d_v, const int64_t* row_pos0,
+                                int chunk, const float* state_in, float* state_out,
+                                void* out, ret_dtype out_dt, const ret_gn* gn,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Path and workspace bytes ret_chunkwise would use for these arguments.
  * gamma may be NULL (then the tensor-core path is assumed allowed). */
 ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,

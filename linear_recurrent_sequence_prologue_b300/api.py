@@ -121,6 +121,8 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
 
     layout="carry" runs ret_chunkwise (state carried across chunks);
     layout="scan" runs ret_chunkwise_scan (chunk-parallel then scan).
+    pos0 is one start position, or a sequence of B start positions (one per
+    batch row: ret_chunkwise_rowpos, carry layout).
     out / state_out / workspace may be given to avoid allocations.
     """
     lib = load()
@@ -139,10 +141,21 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
     _, nbytes = plan("chunkwise_scan" if layout == "scan" else "chunkwise", q.dtype, B, H, L, d_k,
                      d_v, chunk, odtype, bool(gn), gamma=garr)
     wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
-    fn = lib.ret_chunkwise_scan if layout == "scan" else lib.ret_chunkwise
-    st = fn(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, L, d_k, d_v, int(pos0),
-            int(chunk), st_in, _dev(state_out, "state_out"), _dev(out, "out"), odt, gns, wsp, wsn,
-            _stream(stream))
+    if np.ndim(pos0) == 1:   # one start position per batch row
+        if layout != "carry":
+            raise ValueError("per-row start positions use the carry layout")
+        rows = np.ascontiguousarray(np.asarray(pos0, dtype=np.int64))
+        if rows.shape != (B,):
+            raise ValueError(f"pos0 needs {B} start positions, got {rows.shape}")
+        fn = lib.ret_chunkwise_rowpos
+        st = fn(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, L, d_k, d_v,
+                rows.ctypes.data_as(C.POINTER(C.c_int64)), int(chunk), st_in,
+                _dev(state_out, "state_out"), _dev(out, "out"), odt, gns, wsp, wsn, _stream(stream))
+    else:
+        fn = lib.ret_chunkwise_scan if layout == "scan" else lib.ret_chunkwise
+        st = fn(_dev(q, "q"), _dev(k, "k"), _dev(v, "v"), idt, gp, tp, B, H, L, d_k, d_v, int(pos0),
+                int(chunk), st_in, _dev(state_out, "state_out"), _dev(out, "out"), odt, gns, wsp, wsn,
+                _stream(stream))
     check(fn.__name__, st)
     return out, state_out
 

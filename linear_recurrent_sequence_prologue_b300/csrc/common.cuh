@@ -13,6 +13,14 @@ constexpr int kMaxPairs = 256;   // d_k ≤ 512
 
 // Per-call constants passed by value to every kernel.  Filled on the host
 // from the host-side gamma/theta arrays.
+// Start position of every batch row when the rows do not share one pos0
+// (on = 0: every row starts at the call's pos0).  Positions are exact in fp32.
+constexpr int kMaxRowPos = 256;
+struct RowPos {
+  float p[kMaxRowPos];
+  int on;
+};
+
 struct CallConsts {
   float theta[kMaxPairs];    // θ_i
   float lg2g[kMaxHeads];     // log2(γ_h), rounded from double

@@ -118,7 +118,7 @@ struct ChunkArgs {
 __global__ void __launch_bounds__(256) rotate_qk_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ qo, __nv_bfloat16* __restrict__ ko, CallConsts cc, int BH,
-    int H, int L, int Lp, int d, float pos0, int chunk, int fold_omega) {
+    int H, int L, int Lp, int d, float pos0, int chunk, int fold_omega, RowPos rp) {
   constexpr int U = 8;   // heads in flight per thread (the pass is HBM-bound)
   const int vecs = d / 8;
   const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -136,45 +136,53 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
     }
     return;
   }
-  float c[4], s[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cidx + u], c[u], s[u]);
   const int bc = (t / chunk == Lp / chunk - 1) ? L - (Lp - chunk) : chunk;   // length of t's chunk
   const float e = static_cast<float>(bc - 1 - (t % chunk));
   const float ew = static_cast<float>((t % chunk) + 1 - bc);
   const size_t hstride = static_cast<size_t>(L) * d;   // input elements between heads
   const size_t off0 = static_cast<size_t>(t) * d + 8 * cidx;
-  for (int bh0 = 0; bh0 < BH; bh0 += U) {
-    uint4 qv[U], kv[U];
+  // Heads [bh_lo, bh_hi) whose rows start at position `start`.
+  auto rows = [&](float start, int bh_lo, int bh_hi) {
+    float c[4], s[4];
 #pragma unroll
-    for (int uu = 0; uu < U; ++uu) {
-      if (bh0 + uu < BH) {
-        const size_t off = off0 + static_cast<size_t>(bh0 + uu) * hstride;
-        qv[uu] = __ldcs(reinterpret_cast<const uint4*>(q + off));
-        kv[uu] = __ldcs(reinterpret_cast<const uint4*>(k + off));
+    for (int u = 0; u < 4; ++u) angle_cs(start + static_cast<float>(t), cc.theta[4 * cidx + u], c[u], s[u]);
+    for (int bh0 = bh_lo; bh0 < bh_hi; bh0 += U) {
+      uint4 qv[U], kv[U];
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) {
+        if (bh0 + uu < bh_hi) {
+          const size_t off = off0 + static_cast<size_t>(bh0 + uu) * hstride;
+          qv[uu] = __ldcs(reinterpret_cast<const uint4*>(q + off));
+          kv[uu] = __ldcs(reinterpret_cast<const uint4*>(k + off));
+        }
+      }
+#pragma unroll
+      for (int uu = 0; uu < U; ++uu) {
+        const int bh = bh0 + uu;
+        if (bh >= bh_hi) break;
+        const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
+        const float wq = fold_omega ? gpow(cc.lg2g[bh % H], ew) : 1.f;
+        const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
+        const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
+        uint32_t qr[4], kr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
+          qr[u] = pack_bf16x2(wq * (a * c[u] - b * s[u]), wq * fmaf(a, s[u], b * c[u]));
+          const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
+          const float cz = zk * c[u], sz = zk * s[u];
+          kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
+        }
+        const size_t off = oofs + static_cast<size_t>(bh) * ostride;
+        *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
+        *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
       }
     }
-#pragma unroll
-    for (int uu = 0; uu < U; ++uu) {
-      const int bh = bh0 + uu;
-      if (bh >= BH) break;
-      const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
-      const float wq = fold_omega ? gpow(cc.lg2g[bh % H], ew) : 1.f;
-      const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
-      const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
-      uint32_t qr[4], kr[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
-        qr[u] = pack_bf16x2(wq * (a * c[u] - b * s[u]), wq * fmaf(a, s[u], b * c[u]));
-        const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
-        const float cz = zk * c[u], sz = zk * s[u];
-        kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
-      }
-      const size_t off = oofs + static_cast<size_t>(bh) * ostride;
-      *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);
-      *reinterpret_cast<uint4*>(ko + off) = make_uint4(kr[0], kr[1], kr[2], kr[3]);
-    }
+  };
+  if (!rp.on) {
+    rows(pos0, 0, BH);   // one sincos per (position, pair) for all heads
+  } else {
+    for (int b = 0; b < BH / H; ++b) rows(rp.p[b], b * H, b * H + H);
   }
 }
 

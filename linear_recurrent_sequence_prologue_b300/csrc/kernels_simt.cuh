@@ -17,22 +17,28 @@ namespace simt {
 
 // ---------------------------------------------------------------------------
 // Θ prologue: y[bh, t, :] = scale · R((pos0 + t)θ) x[bh, t, :]   (§2 theta_shift)
-// Block (32, 8): x → pair index, y → row.  Angles depend on (t, i) only, so
-// each thread loops over all BH heads with one sincos.
+// with pos0 the row's own start when rp.on (row = bh / H).
+// Block (32, 8): x → pair index, y → row.  Angles depend on (position, i)
+// only, so each thread loops over the BH heads with one sincos per row start.
 // ---------------------------------------------------------------------------
 template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
                                                      Tout* __restrict__ y, CallConsts cc,
-                                                     int BH, int L, int d, float pos0,
-                                                     float scale) {
+                                                     int BH, int H, int L, int d, float pos0,
+                                                     float scale, RowPos rp) {
   const int i = blockIdx.x * 32 + threadIdx.x;   // pair
   const int t = blockIdx.y * 8 + threadIdx.y;    // row
   if (i >= d / 2 || t >= L) return;
-  float c, s;
-  angle_cs(pos0 + static_cast<float>(t), cc.theta[i], c, s);
-  c *= scale;
-  s *= scale;
+  float c = 0.f, s = 0.f;
+  int cur = -1;
   for (int bh = 0; bh < BH; ++bh) {
+    const int row = rp.on ? bh / H : 0;
+    if (row != cur) {
+      angle_cs((rp.on ? rp.p[row] : pos0) + static_cast<float>(t), cc.theta[i], c, s);
+      c *= scale;
+      s *= scale;
+      cur = row;
+    }
     const size_t off = (static_cast<size_t>(bh) * L + t) * d + 2 * i;
     const float a = to_f32(x[off]);
     const float b = to_f32(x[off + 1]);

@@ -53,6 +53,13 @@ struct Mark {
 
 constexpr int64_t kMaxPos = int64_t(1) << 24;
 
+// Calls whose rows all start at the call's pos0.
+RowPos no_rowpos() {
+  RowPos r;
+  std::memset(&r, 0, sizeof(r));
+  return r;
+}
+
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -262,7 +269,8 @@ template <typename Tin, typename Tout>
 ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const CallConsts& cc,
                             int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
                             const float* s_in, float* s_out, Tout* out, const ret_gn* gn,
-                            void* ws, const Plan& p, bool need_states, cudaStream_t st) {
+                            void* ws, const Plan& p, bool need_states, cudaStream_t st,
+                            const RowPos& rp) {
   const int BH = B * H;
   const int nch = (L + chunk - 1) / chunk;
   float* qp = wsp<float>(ws, p.off_q);
@@ -271,13 +279,13 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
     dim3 grid((d_k / 2 + 31) / 32, (L + 7) / 8);
     {
       Mark m("rotate_q_f32", st);
-      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(q, qp, cc, BH, L, d_k,
-                                                                    static_cast<float>(pos0), 1.f);
+      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(q, qp, cc, BH, H, L, d_k,
+                                                                    static_cast<float>(pos0), 1.f, rp);
     }
     {
       Mark m("rotate_k_f32", st);
-      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(k, kp, cc, BH, L, d_k,
-                                                                    static_cast<float>(pos0), cc.kscale);
+      simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(k, kp, cc, BH, H, L, d_k,
+                                                                    static_cast<float>(pos0), cc.kscale, rp);
     }
   }
   float* states = need_states ? wsp<float>(ws, p.off_states) : nullptr;
@@ -324,7 +332,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
                         const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
                         int64_t pos0, const float* s_in, float* s_out, Tout* out,
                         const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st,
-                        bool scan = false, bool parallel = false) {
+                        const RowPos& rp, bool scan = false, bool parallel = false) {
   const int BH = B * H;
   __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
@@ -334,7 +342,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     const size_t n = static_cast<size_t>(Lp) * (d_k / 8);
     Mark m("rotate_qk_bf16", st);
     tcc::rotate_qk_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        q, k, qr, kr, cc, BH, H, L, Lp, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1);
+        q, k, qr, kr, cc, BH, H, L, Lp, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1, rp);
   }
   // Q′ / K̂′: the padded workspace, flat; V: [B·H][L][d_v] in 3-D for the
   // chunk kernels (a short last chunk reads zeros past L), flat for the
@@ -498,16 +506,17 @@ ret_status dispatch_simt_out(const void* q, const void* k, const void* v, const 
                              int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
                              const float* s_in, float* s_out, void* out, ret_dtype out_dt,
                              const ret_gn* gn, void* ws, const Plan& p, bool need_states,
-                             cudaStream_t st) {
+                             cudaStream_t st, const RowPos& rp) {
   const Tin* qq = static_cast<const Tin*>(q);
   const Tin* kk = static_cast<const Tin*>(k);
   const Tin* vv = static_cast<const Tin*>(v);
   if (out_dt == RET_F32)
     return run_simt_chunked<Tin, float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, chunk, s_in,
-                                        s_out, static_cast<float*>(out), gn, ws, p, need_states, st);
+                                        s_out, static_cast<float*>(out), gn, ws, p, need_states, st,
+                                        rp);
   return run_simt_chunked<Tin, __nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, chunk,
                                                s_in, s_out, static_cast<__nv_bfloat16*>(out), gn,
-                                               ws, p, need_states, st);
+                                               ws, p, need_states, st, rp);
 }
 
 // Scratch of ret_chunkwise_noalloc: part of this module's device image, so
@@ -605,10 +614,19 @@ ret_status chunkwise_impl(const void* q, const void* k, const void* v, ret_dtype
                           int d_v, int64_t pos0, int chunk, const float* state_in,
                           float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream,
-                          bool scan) {
+                          bool scan, const int64_t* row_pos0 = nullptr) {
   ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
                               out_dt, gn);
   if (s != RET_OK) return s;
+  RowPos rp = no_rowpos();
+  if (row_pos0) {   // one start position per batch row
+    if (B > kMaxRowPos) return RET_EUNSUPPORTED;
+    for (int b = 0; b < B; ++b) {
+      if (row_pos0[b] < 0 || row_pos0[b] + L > kMaxPos) return RET_EINVAL;
+      rp.p[b] = static_cast<float>(row_pos0[b]);
+    }
+    rp.on = 1;
+  }
   if (chunk < 1) return RET_EINVAL;
   CallConsts cc;
   if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
@@ -621,17 +639,18 @@ ret_status chunkwise_impl(const void* q, const void* k, const void* v, ret_dtype
     const auto* vv = static_cast<const __nv_bfloat16*>(v);
     if (out_dt == RET_F32)
       return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
-                                 static_cast<float*>(out), gn, workspace, p, stream, scan);
+                                 static_cast<float*>(out), gn, workspace, p, stream, rp, scan);
     return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
                                        state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
-                                       p, stream, scan);
+                                       p, stream, rp, scan);
   }
   // The fp32 kernels always run in the chunk-parallel layout.
   if (in_dt == RET_F32)
     return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
-                                    state_out, out, out_dt, gn, workspace, p, true, stream);
+                                    state_out, out, out_dt, gn, workspace, p, true, stream, rp);
   return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
-                                          state_out, out, out_dt, gn, workspace, p, true, stream);
+                                          state_out, out, out_dt, gn, workspace, p, true, stream,
+                                          rp);
 }
 }  // namespace
 
@@ -644,6 +663,18 @@ ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype 
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, false);
+}
+
+ret_status ret_chunkwise_rowpos(const void* q, const void* k, const void* v, ret_dtype in_dt,
+                                const float* gamma, const float* theta, int B, int H, int L,
+                                int d_k, int d_v, const int64_t* row_pos0, int chunk,
+                                const float* state_in, float* state_out, void* out,
+                                ret_dtype out_dt, const ret_gn* gn, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  if (!row_pos0) return RET_EINVAL;
+  return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, 0, chunk, state_in,
+                        state_out, out, out_dt, gn, workspace, workspace_bytes, stream, false,
+                        row_pos0);
 }
 
 ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, ret_dtype in_dt,
@@ -721,19 +752,21 @@ ret_status ret_parallel(const void* q, const void* k, const void* v, ret_dtype i
     const auto* vv = static_cast<const __nv_bfloat16*>(v);
     if (out_dt == RET_F32)
       return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
-                                 static_cast<float*>(out), gn, workspace, p, stream, false, true);
+                                 static_cast<float*>(out), gn, workspace, p, stream, no_rowpos(),
+                                 false, true);
     return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
                                        state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
-                                       p, stream, false, true);
+                                       p, stream, no_rowpos(), false, true);
   }
   if ((s = make_consts(cc, gamma, theta, H, d_k, L, L)) != RET_OK) return s;
   // One chunk of length L: the fp32 chunk kernels evaluate the parallel form.
   if (in_dt == RET_F32)
     return dispatch_simt_out<float>(q, k, v, cc, B, H, L, d_k, d_v, pos0, L, state_in, state_out,
-                                    out, out_dt, gn, workspace, p, state_out != nullptr, stream);
+                                    out, out_dt, gn, workspace, p, state_out != nullptr, stream,
+                                    no_rowpos());
   return dispatch_simt_out<__nv_bfloat16>(q, k, v, cc, B, H, L, d_k, d_v, pos0, L, state_in,
                                           state_out, out, out_dt, gn, workspace, p,
-                                          state_out != nullptr, stream);
+                                          state_out != nullptr, stream, no_rowpos());
 }
 
 ret_status ret_step(const void* q, const void* k, const void* v, ret_dtype in_dt,
@@ -791,16 +824,16 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B,
   const float p0 = static_cast<float>(pos0);
   if (in_dt == RET_BF16 && out_dt == RET_BF16)
     simt::rotate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, L, d, p0, scale);
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
   else if (in_dt == RET_BF16)
     simt::rotate_kernel<__nv_bfloat16, float><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), cc, BH, L, d, p0, scale);
+        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
   else if (out_dt == RET_BF16)
     simt::rotate_kernel<float, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, L, d, p0, scale);
+        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
   else
     simt::rotate_kernel<float, float><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const float*>(x), static_cast<float*>(y), cc, BH, L, d, p0, scale);
+        static_cast<const float*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
   return last_launch();
 }
 

@@ -122,6 +122,25 @@ def test_step_and_rotate_validation(lib):
         assert lib.ret_force_path(0) == _lib.RET_OK
 
 
+def test_rowpos_validation(lib):
+    """ret_chunkwise_rowpos checks its per-row start positions before any launch."""
+    g = np.full(2, 0.99, np.float32)
+    t = np.ones(8, np.float32)
+    fp = lambda a: a.ctypes.data_as(C.POINTER(C.c_float))
+    P = C.c_void_p(0x1000)
+
+    def call(rows, B=2):
+        arr = None if rows is None else (C.c_int64 * len(rows))(*rows)
+        return lib.ret_chunkwise_rowpos(P, P, P, _lib.RET_F32, fp(g), fp(t), B, 2, 64, 16, 16, arr, 16,
+                                        None, None, P, _lib.RET_F32, None, None, 0, None)
+
+    assert call(None) == _lib.RET_EINVAL                      # no array
+    assert call([0, -1]) == _lib.RET_EINVAL                   # negative start
+    assert call([0, (1 << 24) - 10]) == _lib.RET_EINVAL       # positions past 2^24
+    assert call([0] * 300, B=300) == _lib.RET_EUNSUPPORTED    # more rows than the constant block holds
+    assert call([0, 5]) == _lib.RET_EWORKSPACE                # valid: stops at the missing workspace
+
+
 def _plan(lib, in_dt, B, H, L, d_k, d_v, chunk, gn=0, gamma=None):
     path, nb = C.c_int(0), C.c_size_t(0)
     gp = _fp(gamma) if gamma is not None else None

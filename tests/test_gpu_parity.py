@@ -287,6 +287,36 @@ def test_tc_ragged_length_vs_oracle(d_k, d_v, L, H):
     assert torch.isnan(big[n:].float()).all()
 
 
+@pytest.mark.parametrize("dtype,d_k,d_v,L,H", [
+    ("bf16", 256, 256, 300, 2),   # tensor cores (CTA pairs, short last chunk)
+    ("bf16", 128, 128, 256, 1),   # tensor cores (one CTA per tile)
+    ("f32", 32, 24, 96, 2),       # fp32 path
+])
+def test_rowpos_vs_oracle(dtype, d_k, d_v, L, H):
+    """ret_chunkwise_rowpos: each batch row at its own start position, against
+    the oracle run row by row; with one shared start it equals ret_chunkwise
+    bit for bit."""
+    B = 3
+    w, inp = _custom(B, H, L, d_k, d_v, dtype, 128 if dtype == "bf16" else 32, std=1.0,
+                     state_std=0.1, seed=L + H)
+    d = _cuda(inp)
+    rows = [0, 37, 5000]
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk, pos0=rows,
+                       state_in=d["state_in"], out_dtype=torch.float32)
+    assert R.sync_status() == R.RET_OK
+    for b, p0 in enumerate(rows):
+        one = {k: (v[b:b + 1] if torch.is_tensor(v) else v) for k, v in inp.items()}
+        ref_o, ref_s = _oracle_full(one, w, "chunkwise", w.chunk, pos0=p0)
+        assert_close(gpu_np(o[b:b + 1]), ref_o, w.torch_dtype, f"row {b} out")
+        assert_close(gpu_np(s[b:b + 1]), ref_s, w.torch_dtype, f"row {b} state")
+    o1, s1 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
+                         pos0=[41] * B, state_in=d["state_in"])
+    o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk, pos0=41,
+                         state_in=d["state_in"])
+    assert R.sync_status() == R.RET_OK
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
 @pytest.mark.parametrize("d_k,d_v,L,H,state", [(64, 128, 256, 1, False), (128, 256, 384, 2, True),
                                                (256, 512, 512, 2, True)])
 def test_tc_parallel_form_vs_oracle(d_k, d_v, L, H, state):
