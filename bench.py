@@ -43,7 +43,7 @@ def parse():
 
 
 # --------------------------------------------------------------------------
-# Algorithmic work (per call), stated in the design doc
+# Algorithmic work and bytes of one call, as the chunkwise form states them
 # --------------------------------------------------------------------------
 def chunk_flops(w):
     """2b·d_k + 2b·d_v + 4·d_k·d_v flop per token per head (QKᵀ, PV, Q·S, KᵀV)."""

@@ -23,7 +23,7 @@ Sources (web pages about RetNet; formulas partly garbled by extraction):
   is used for its scale invariance; complex-valued position encoding.
 
 Readings taken where the pages are silent or garbled (each is listed again in
-DESIGN.md):
+the design notes):
 
 R1  rotate_every_two acts on interleaved pairs (2i, 2i+1) and maps
     (a, b) → (−b, a); theta_shift(x) = x·cos + rotate_every_two(x)·sin with the
