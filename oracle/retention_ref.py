@@ -261,6 +261,59 @@ def retention(q, k, v, gamma, theta, pos0=0, state_in=None, form="chunkwise",
     return out, S
 
 
+def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
+                       d_state_out=None):
+    """Gradients of ``retention`` (no GroupNorm) with respect to q, k, v and
+    state_in, for the upstream gradients d_out (of out) and d_state_out (of
+    state_out, or None).  Returns (dq, dk, dv, d_state_in).
+
+    The chain rule applied to the parallel form with the state terms
+    ([P1] §4.1, R4), per head with A = D (the causal decay mask),
+    ξ_t = γ^{t+1} and w_m = γ^{L−1−m}:
+      out    = (Q′K′ᵀ ⊙ A) V + ξ ⊙ (Q′ S_in)
+      S_out  = γ^L S_in + Σ_m w_m k′_mᵀ v_m
+    give, with G = (dO Vᵀ) ⊙ A,
+      dV     = (Q′K′ᵀ ⊙ A)ᵀ dO + (w ⊙ K′) dS_out
+      dQ′    = G K′ + ξ ⊙ (dO S_inᵀ)
+      dK′    = Gᵀ Q′ + (w ⊙ V) dS_outᵀ
+      dS_in  = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
+    and through the prologue (R1-R3: q′ = R q, k′ = d_k^{-1/2} R k with R an
+    orthogonal rotation per position) dq = Rᵀ dQ′, dk = d_k^{-1/2} Rᵀ dK′,
+    Rᵀ being the rotation by −n·θ.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d_k = q.shape
+    d_v = v.shape[-1]
+    g = _heads(gamma, H)
+    qp, kp = prologue(q, k, theta, pos0)
+    dO = _f64(d_out)
+    dqp = np.zeros_like(qp)
+    dkp = np.zeros_like(kp)
+    dv = np.zeros_like(v)
+    dS_in = np.zeros((B, H, d_k, d_v))
+    for h in range(H):
+        A = decay_mask(g[h], L)
+        P = (qp[:, h] @ np.swapaxes(kp[:, h], -1, -2)) * A            # scores with decay
+        G = (dO[:, h] @ np.swapaxes(v[:, h], -1, -2)) * A
+        xi = np.power(g[h], np.arange(1, L + 1, dtype=np.float64))
+        w = np.power(g[h], np.arange(L - 1, -1, -1, dtype=np.float64))
+        dv[:, h] = np.swapaxes(P, -1, -2) @ dO[:, h]
+        dqp[:, h] = G @ kp[:, h]
+        dkp[:, h] = np.swapaxes(G, -1, -2) @ qp[:, h]
+        dS_in[:, h] = np.swapaxes(xi[None, :, None] * qp[:, h], -1, -2) @ dO[:, h]
+        if state_in is not None:
+            dqp[:, h] += xi[None, :, None] * (dO[:, h] @ np.swapaxes(_f64(state_in)[:, h], -1, -2))
+        if d_state_out is not None:
+            dSo = _f64(d_state_out)[:, h]
+            dv[:, h] += (w[None, :, None] * kp[:, h]) @ dSo
+            dkp[:, h] += (w[None, :, None] * v[:, h]) @ np.swapaxes(dSo, -1, -2)
+            dS_in[:, h] += np.power(g[h], float(L)) * dSo
+    sin, cos = rotation_tables(np.arange(L) + int(pos0), theta)
+    dq = theta_shift(dqp, -sin, cos)                                   # Rᵀ = rotation by −nθ
+    dk = theta_shift(dkp, -sin, cos) / math.sqrt(d_k)
+    return dq, dk, dv, dS_in
+
+
 def decode_step(q, k, v, gamma, theta, pos, state, gn=None):
     """One recurrent step at absolute position ``pos`` ([P1] §4.2, R5).
 

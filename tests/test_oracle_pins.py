@@ -326,3 +326,46 @@ def test_mutants_are_caught(name, monkeypatch):
     finally:
         R = saved
     assert caught, f"mutant {name} was not caught by any pin"
+
+
+# ------------------------------------------------------------- backward --
+@pytest.mark.parametrize("with_state,with_dso,pos0", [(False, False, 0), (True, False, 3), (True, True, 11)])
+def test_backward_matches_finite_differences(with_state, with_dso, pos0):
+    """retention_backward against central differences of the (pinned) forward
+    oracle, for the scalar <dO, out> + <dS_out, S_out>: every gradient term
+    (intra-chunk scores, the state_in term, the state_out path, the rotation
+    adjoint and the 1/√d_k scale) enters one of the four checks."""
+    rng = np.random.default_rng(7 + pos0)
+    B, H, L, d_k, d_v = 1, 2, 6, 4, 3
+    q, k = rng.standard_normal((B, H, L, d_k)), rng.standard_normal((B, H, L, d_k))
+    v = rng.standard_normal((B, H, L, d_v))
+    S0 = 0.3 * rng.standard_normal((B, H, d_k, d_v)) if with_state else None
+    g, th = np.array([0.9, 0.6]), np.array([0.4, 1.3])
+    dO = rng.standard_normal((B, H, L, d_v))
+    dSo = rng.standard_normal((B, H, d_k, d_v)) if with_dso else None
+
+    def f(q_, k_, v_, s_):
+        o, S = R.retention(q_, k_, v_, g, th, pos0, s_, "parallel")
+        return (o * dO).sum() + ((S * dSo).sum() if with_dso else 0.0)
+
+    grads = R.retention_backward(q, k, v, g, th, pos0, S0, dO, dSo)
+    args = [q, k, v, S0 if with_state else np.zeros((B, H, d_k, d_v))]
+    eps = 1e-6
+    for which in range(4 if with_state else 3):
+        x = args[which]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a = [t.copy() for t in args]
+            a[which][idx] += eps
+            fp = f(*(a[:3] + [a[3] if with_state else None]))
+            a[which][idx] -= 2 * eps
+            fm = f(*(a[:3] + [a[3] if with_state else None]))
+            num[idx] = (fp - fm) / (2 * eps)
+        assert np.max(np.abs(num - grads[which])) < 1e-6, which
+    if not with_state:   # d_state_in is still defined: the gradient at S_in = 0
+        num = np.zeros((B, H, d_k, d_v))
+        for idx in np.ndindex(num.shape):
+            e = np.zeros_like(num)
+            e[idx] = eps
+            num[idx] = (f(q, k, v, e) - f(q, k, v, -e)) / (2 * eps)
+        assert np.max(np.abs(num - grads[3])) < 1e-6
