@@ -38,6 +38,7 @@ def parse():
     ap.add_argument("--workload", default="msr7b")
     ap.add_argument("--decode-steps", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=12)
+    ap.add_argument("--backward-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -59,6 +60,16 @@ def chunk_bytes(w):
 def decode_bytes(w):
     """Read and write the fp32 state once, plus q, k, v in and o out (bf16)."""
     return 2 * w.B * w.H * w.d_k * w.d_v * 4 + w.B * w.H * (2 * w.d_k + 2 * w.d_v) * 2
+
+
+def backward_flops(w):
+    """Three chunkwise evaluations per gradient pass: (chunk_out share, chunk_dS share)."""
+    b, n = w.chunk, w.B * w.H * w.L
+    return 3 * n * (2 * b * (w.d_k + w.d_v) + 2 * w.d_k * w.d_v), 3 * n * 2 * w.d_k * w.d_v
+
+
+# fp32 FFMA peak: 148 SMs x 128 fp32 lanes x 2 flop per FFMA at the 2032 MHz maximum SM clock.
+FFMA_TFLOPS = 148 * 128 * 2 * 2032e6 / 1e12
 
 
 def measured_peaks():
@@ -399,6 +410,66 @@ def main():
               "gpu_launches": dsteps, "clocks": dsampler.summary()}
     del dinp, dstate
 
+    # ---------------- gradient pass (fp32 kernels) on the same workload ----------------
+    backward = None
+    if args.backward_steps > 0:
+        from linear_recurrent_sequence_prologue_b300.inputs import make_grad_inputs
+        gi = make_grad_inputs(w, seed=5, d_state_std=1.0)
+        d_o, dso = gi["d_out"].to(dev), gi["d_state_out"].to(dev)
+        grads = tuple(torch.empty_like(t) for t in (q, k, v))
+        dsi = torch.empty_like(dso)
+        _, bws_bytes = R.backward_plan(torch.bfloat16, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk)
+        bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
+        bargs = (vp(q), vp(k), vp(v), vp(d_o), _lib.RET_BF16, fptr(garr), fptr(tarr), w.B, w.H, w.L,
+                 w.d_k, w.d_v, 0, w.chunk, vp(s_in), vp(dso), vp(grads[0]), vp(grads[1]),
+                 vp(grads[2]), _lib.RET_BF16, vp(dsi), vp(bws), bws_bytes, C.c_void_p(stream.cuda_stream))
+
+        def bstep():
+            st = lib.ret_chunkwise_backward(*bargs)
+            if st != _lib.RET_OK:
+                raise RuntimeError(f"ret_chunkwise_backward returned {st}")
+
+        for _ in range(max(3, args.warmup)):
+            bstep()
+        torch.cuda.synchronize()
+        bs, be = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        bsampler = ClockSampler(local)
+        bhook = min(args.backward_steps, 2)
+        barrier()
+        with bsampler:
+            bs.record(stream)
+            lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+            for it in range(args.backward_steps):
+                bstep()
+                if it + 1 == bhook:
+                    nb_k = lib.ret_profile_end()
+            be.record(stream)
+            torch.cuda.synchronize()
+        bnames = [lib.ret_profile_kernel(i).decode() for i in range(nb_k)]
+        bper = {}
+        for i, nm in enumerate(bnames):
+            bper.setdefault(nm, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+        bms = max_over_ranks(bs.elapsed_time(be) / args.backward_steps, world, dev)
+        f_out, f_ds = backward_flops(w)
+        step_ms = {nm: sum(t) / bhook for nm, t in bper.items()}   # all launches of a name, per step
+        btop = max(step_ms, key=step_ms.get)
+        bflops = {"bwd_chunk_out": f_out, "bwd_chunk_dS": f_ds}.get(btop)
+        bach = bflops / (step_ms[btop] / 1e3) / 1e12 if bflops else None
+        backward = {
+            "metric": "gradient pass tokens/s", "value": replica_throughput(w.B * w.L, bms / 1e3, world),
+            "unit": "tokens/s", "ms_per_step": bms, "steps": args.backward_steps,
+            "dtype": "f32 (bf16 inputs and gradients)",
+            "config": {"workload": w.name, "chunk": w.chunk, "state_in": True, "d_state_out": True},
+            "roofline": {"bound": "alu", "kernel": btop, "achieved": bach, "peak": FFMA_TFLOPS,
+                         "unit": "TFLOP/s", "frac": bach / FFMA_TFLOPS if bach else None,
+                         "traffic": None,
+                         "peak_kind": "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2032 MHz",
+                         "algorithmic_flop_per_step": f_out + f_ds},
+            "kernels_ms_per_step": step_ms,
+            "gpu_launches": int(round(nb_k / bhook * args.backward_steps)),
+            "clocks": bsampler.summary()}
+        del bws, grads, dsi, d_o, dso, gi
+
     # ---------------- end to end through the API with host buffers ----------------
     # Every step copies its inputs host → device from pinned memory, runs
     # ret_chunkwise through the Python API and copies out and state_out back.
@@ -486,6 +557,7 @@ def main():
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": sampler.summary(),
             "decode": decode,
+            "backward": backward,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

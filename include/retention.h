@@ -177,6 +177,38 @@ ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, i
                                    int gn_enabled, int* path, size_t* workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * ret_chunkwise_backward — gradients of ret_chunkwise (without the GroupNorm
+ * epilogue) with respect to q, k, v and state_in, given the gradient d_out
+ * of out and d_state_out of state_out.  Per head, with the decay mask A,
+ * ξ_t = γ^{t+1}, w_m = γ^{L−1−m} and G = (dO Vᵀ) ⊙ A (the chain rule applied
+ * to the parallel form with state terms, «从RoPE到Retention…» §4.1):
+ *   dQ′ = G K′ + ξ ⊙ (dO S_inᵀ)          dV = (Q′K′ᵀ ⊙ A)ᵀ dO + (w ⊙ K′) dS_out
+ *   dK′ = Gᵀ Q′ + (w ⊙ V) dS_outᵀ         dS_in = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
+ *   dq = R(−nθ) dQ′,  dk = d_k^{-1/2} R(−nθ) dK′    (the Θ prologue's adjoint)
+ * Computed on the fp32 kernels as three chunkwise evaluations (one in
+ * order, two over the reversed sequence, which turns the sums over t ≥ m
+ * into causal ones); `chunk` is their chunk length (any ≥ 1).
+ * q, k, v, d_out: DEVICE, in_dt, layouts as above.  dq, dk [B, H, L, d_k]
+ * and dv [B, H, L, d_v]: DEVICE, grad_dt; they must not alias any input.
+ * state_in, d_state_out: DEVICE fp32 [B, H, d_k, d_v] or NULL (zero).
+ * d_state_in: DEVICE fp32 or NULL (not computed); it may alias state_in or
+ * d_state_out.  workspace: DEVICE, at least ret_chunkwise_backward_plan's
+ * bytes (never 0).  B·H·ceil(L/chunk) > 65535, L > 524280 or a γ_h below
+ * 2^-64 (the reversed evaluations start from dS_out/γ) is RET_EUNSUPPORTED.  Validation and errors as for the other entry points.
+ * ------------------------------------------------------------------------ */
+ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, const void* d_out,
+                                  ret_dtype in_dt, const float* gamma, const float* theta,
+                                  int B, int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                                  const float* state_in, const float* d_state_out,
+                                  void* dq, void* dk, void* dv, ret_dtype grad_dt,
+                                  float* d_state_in, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream);
+
+/* Path (always RET_PATH_SIMT) and workspace bytes of ret_chunkwise_backward. */
+ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, int B, int H, int L, int d_k, int d_v,
+                                       int chunk, int* path, size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
  * ret_parallel — parallel form O = (Q′K′ᵀ ⊙ D) V + γ^{t+1} q′_t S_in
  * («从RoPE到Retention…» §4.1; RetNet 保留网络 explainer, 并行表征).
  * O(L²) work.  state_out (optional) is the closed-form final state.

@@ -160,6 +160,53 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
     return out, state_out
 
 
+def backward_plan(in_dtype, B, H, L, d_k, d_v, chunk):
+    """(path, workspace bytes) of the gradient pass (path 2 = fp32 kernels)."""
+    lib = load()
+    path, nbytes = C.c_int(0), C.c_size_t(0)
+    check("ret_chunkwise_backward_plan",
+          lib.ret_chunkwise_backward_plan(_DT[in_dtype], B, H, L, d_k, d_v, int(chunk),
+                                          C.byref(path), C.byref(nbytes)))
+    return path.value, nbytes.value
+
+
+def chunkwise_backward(q, k, v, d_out, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
+                       d_state_out=None, return_d_state_in: bool = True, grad_dtype=None,
+                       grads=None, d_state_in=None, workspace=None, stream=None):
+    """Gradients of chunkwise retention (no GroupNorm) for upstream gradients
+    d_out [B, H, L, d_v] (dtype of q) and d_state_out [B, H, d_k, d_v] fp32
+    (None = 0).  Returns (dq, dk, dv, d_state_in or None).  grads may be a
+    (dq, dk, dv) tuple of preallocated outputs; d_state_in a preallocated
+    fp32 state (it may be state_in or d_state_out itself)."""
+    lib = load()
+    B, H, L, d_k, d_v = _check_seq(q, k, v)
+    idt = _dtype_code(q)
+    _dev(d_out, "d_out", q.dtype, (B, H, L, d_v))
+    gdtype = grad_dtype or q.dtype
+    if grads is None:
+        grads = (torch.empty((B, H, L, d_k), dtype=gdtype, device=q.device),
+                 torch.empty((B, H, L, d_k), dtype=gdtype, device=q.device),
+                 torch.empty((B, H, L, d_v), dtype=gdtype, device=q.device))
+    dq, dk, dv = grads
+    gdt = _dtype_code(dq)
+    for name, t, shp in (("dq", dq, (B, H, L, d_k)), ("dk", dk, (B, H, L, d_k)), ("dv", dv, (B, H, L, d_v))):
+        _dev(t, name, dq.dtype, shp)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
+    sshape = (B, H, d_k, d_v)
+    if d_state_in is None and return_d_state_in:
+        d_state_in = torch.empty(sshape, dtype=torch.float32, device=q.device)
+    _, nbytes = backward_plan(q.dtype, B, H, L, d_k, d_v, chunk)
+    wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
+    st = lib.ret_chunkwise_backward(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(d_out, "d_out"), idt, gp, tp, B, H, L, d_k,
+        d_v, int(pos0), int(chunk), _dev(state_in, "state_in", torch.float32, sshape),
+        _dev(d_state_out, "d_state_out", torch.float32, sshape), _dev(dq, "dq"), _dev(dk, "dk"),
+        _dev(dv, "dv"), gdt, _dev(d_state_in, "d_state_in", torch.float32, sshape), wsp, wsn, _stream(stream))
+    check("ret_chunkwise_backward", st)
+    return dq, dk, dv, d_state_in
+
+
 def parallel(q, k, v, gamma, theta, pos0: int = 0, state_in=None, return_state: bool = False,
              out=None, out_dtype=None, gn=None, workspace=None, stream=None):
     """Parallel-form retention.  Returns (out, state_out or None)."""

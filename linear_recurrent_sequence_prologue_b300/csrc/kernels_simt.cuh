@@ -18,6 +18,8 @@ namespace simt {
 // ---------------------------------------------------------------------------
 // Θ prologue: y[bh, t, :] = scale · R((pos0 + t)θ) x[bh, t, :]   (§2 theta_shift)
 // with pos0 the row's own start when rp.on (row = bh / H).
+// flip (for the gradients): bit 0 reads x at row L−1−t, bit 1 writes y at row
+// L−1−t; the angle always belongs to position pos0 + t.
 // Block (32, 8): x → pair index, y → row.  Angles depend on (position, i)
 // only, so each thread loops over the BH heads with one sincos per row start.
 // ---------------------------------------------------------------------------
@@ -25,7 +27,7 @@ template <typename Tin, typename Tout>
 __global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
                                                      Tout* __restrict__ y, CallConsts cc,
                                                      int BH, int H, int L, int d, float pos0,
-                                                     float scale, RowPos rp) {
+                                                     float scale, RowPos rp, int flip) {
   const int i = blockIdx.x * 32 + threadIdx.x;   // pair
   const int t = blockIdx.y * 8 + threadIdx.y;    // row
   if (i >= d / 2 || t >= L) return;
@@ -39,11 +41,12 @@ __global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
       s *= scale;
       cur = row;
     }
-    const size_t off = (static_cast<size_t>(bh) * L + t) * d + 2 * i;
-    const float a = to_f32(x[off]);
-    const float b = to_f32(x[off + 1]);
-    y[off] = from_f32<Tout>(a * c - b * s);
-    y[off + 1] = from_f32<Tout>(fmaf(a, s, b * c));
+    const size_t xo = (static_cast<size_t>(bh) * L + ((flip & 1) ? L - 1 - t : t)) * d + 2 * i;
+    const size_t yo = (static_cast<size_t>(bh) * L + ((flip & 2) ? L - 1 - t : t)) * d + 2 * i;
+    const float a = to_f32(x[xo]);
+    const float b = to_f32(x[xo + 1]);
+    y[yo] = from_f32<Tout>(a * c - b * s);
+    y[yo + 1] = from_f32<Tout>(fmaf(a, s, b * c));
   }
 }
 
@@ -405,6 +408,51 @@ __global__ void __launch_bounds__(256) decode_step_kernel(
   if (active) {
 #pragma unroll
     for (int u = 0; u < VEC; ++u) out[static_cast<size_t>(bh) * d_v + c0 + u] = from_f32<Tout>(o[u]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Helpers of the gradient pass (ret_chunkwise_backward).  The gradients are
+// three evaluations of the chunkwise form on reordered operands: reading the
+// sequence backwards turns the anti-causal sums Σ_{t≥m} of the gradient into
+// the causal sums Σ_{m≤t} of the forward form.
+// ---------------------------------------------------------------------------
+struct HeadScale {
+  float s[kMaxHeads];
+};
+
+// y[bh, t', c] = x[bh, t, c] converted to Tout, with t' = L−1−t when flip,
+// else t.  Grid-stride over the BH·L·d elements (rows contiguous).
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(256) flip_cvt_kernel(const Tin* __restrict__ x,
+                                                       Tout* __restrict__ y, int BH, int L,
+                                                       int d, int flip) {
+  const size_t n = static_cast<size_t>(BH) * L * d;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t row = e / d;
+    const int c = static_cast<int>(e - row * d);
+    const size_t bh = row / L;
+    const int t = static_cast<int>(row - bh * L);
+    const size_t dst = (bh * L + (flip ? L - 1 - t : t)) * d + c;
+    y[dst] = from_f32<Tout>(to_f32(x[e]));
+  }
+}
+
+// dst = hs.s[h] · src for BH states of rows × cols, transposed into
+// [BH][cols][rows] when transpose.  src == dst only without transpose.
+__global__ void __launch_bounds__(256) state_prep_kernel(const float* __restrict__ src,
+                                                         float* dst, int BH, int H, int rows,
+                                                         int cols, int transpose, HeadScale hs) {
+  const size_t per = static_cast<size_t>(rows) * cols;
+  const size_t n = per * BH;
+  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
+       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t bh = e / per;
+    const size_t rc = e - bh * per;
+    const size_t r = rc / cols, c = rc - r * cols;
+    const float val = src[e] * hs.s[bh % H];
+    dst[transpose ? bh * per + c * rows + r : e] = val;
   }
 }
 

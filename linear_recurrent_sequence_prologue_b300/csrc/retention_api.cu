@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -280,12 +281,12 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
     {
       Mark m("rotate_q_f32", st);
       simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(q, qp, cc, BH, H, L, d_k,
-                                                                    static_cast<float>(pos0), 1.f, rp);
+                                                                    static_cast<float>(pos0), 1.f, rp, 0);
     }
     {
       Mark m("rotate_k_f32", st);
       simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(k, kp, cc, BH, H, L, d_k,
-                                                                    static_cast<float>(pos0), cc.kscale, rp);
+                                                                    static_cast<float>(pos0), cc.kscale, rp, 0);
     }
   }
   float* states = need_states ? wsp<float>(ws, p.off_states) : nullptr;
@@ -519,6 +520,213 @@ ret_status dispatch_simt_out(const void* q, const void* k, const void* v, const 
                                                ws, p, need_states, st, rp);
 }
 
+// ---------------------------------------------------------------------------
+// Gradient pass (fp32 kernels)
+// ---------------------------------------------------------------------------
+// Workspace: rotated Q′ (reversed), K′ (in order and reversed), dO and V in
+// fp32 (in order — only for bf16 inputs, fp32 inputs are read in place — and
+// reversed), one fp32 output of the forward-form evaluations, the per-chunk
+// states of those evaluations, and one prepared d×d state.
+struct BwdPlan {
+  size_t off_qpf = 0, off_kp = 0, off_kpf = 0, off_do = 0, off_dof = 0, off_v = 0, off_vf = 0;
+  size_t off_fout = 0, off_states = 0, off_sprep = 0, bytes = 0;
+};
+
+BwdPlan plan_backward(ret_dtype in_dt, int B, int H, int L, int d_k, int d_v, int chunk) {
+  BwdPlan p;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nch = (static_cast<size_t>(L) + chunk - 1) / chunk;
+  const size_t rk = up256(BH * L * d_k * 4), rv = up256(BH * L * static_cast<size_t>(d_v) * 4);
+  size_t off = 0;
+  p.off_qpf = off; off += rk;
+  p.off_kp = off; off += rk;
+  p.off_kpf = off; off += rk;
+  if (in_dt == RET_BF16) {
+    p.off_do = off; off += rv;
+    p.off_v = off; off += rv;
+  }
+  p.off_dof = off; off += rv;
+  p.off_vf = off; off += rv;
+  p.off_fout = off; off += up256(BH * L * static_cast<size_t>(d_k > d_v ? d_k : d_v) * 4);
+  p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4);
+  p.off_sprep = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4);
+  p.bytes = off;
+  return p;
+}
+
+unsigned stride_grid(size_t n) {
+  const size_t b = (n + 255) / 256;
+  return static_cast<unsigned>(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
+}
+
+// One evaluation of the chunkwise form on fp32 operands that are already
+// rotated and scaled (no Θ step): out = o(qp, kp, v; s_in), s_out optional.
+// qp, kp: [BH, L, dk]; v, out: [BH, L, dv]; states: [BH, nch, dk, dv].
+ret_status run_simt_core(const float* qp, const float* kp, const float* v, const CallConsts& cc,
+                         int BH, int H, int L, int dk, int dv, int chunk, const float* s_in,
+                         float* s_out, float* out, float* states, cudaStream_t st) {
+  const int nch = (L + chunk - 1) / chunk;
+  const bool need = nch > 1 || s_out;
+  if (need) {
+    dim3 g1((dv + 63) / 64, (dk + 63) / 64, BH * nch);
+    {
+      Mark m("bwd_chunk_dS", st);
+      simt::chunk_dS_kernel<float><<<g1, dim3(16, 16), 0, st>>>(kp, v, states, cc, H, L, dk, dv,
+                                                                chunk, nch);
+    }
+    const size_t n = static_cast<size_t>(BH) * dk * dv;
+    Mark m("bwd_state_scan", st);
+    simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        states, s_in, s_out, cc, H, dk, dv, nch, BH);
+  }
+  dim3 g2((dv + 63) / 64, (chunk + 15) / 16, BH * nch);
+  const size_t smem = (16 * static_cast<size_t>(dk) + 16 * 64) * sizeof(float);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(simt::chunk_out_kernel<float, float>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return RET_ECUDA;
+  Mark m("bwd_chunk_out", st);
+  simt::chunk_out_kernel<float, float><<<g2, 256, smem, st>>>(qp, kp, v, need ? states : nullptr,
+                                                              s_in, out, nullptr, cc, H, L, dk,
+                                                              dv, chunk, nch);
+  return last_launch();
+}
+
+// Gradients of o and S_out with respect to q, k, v, S_in, per head with the
+// decay mask A, ξ_t = γ^{t+1}, w_m = γ^{L−1−m} and G = (dO Vᵀ) ⊙ A (the
+// chain rule on the parallel form of «从RoPE到Retention…» §4.1 with the state
+// terms):
+//   dQ′ = G K′ + ξ ⊙ (dO S_inᵀ)            dV = (Q′K′ᵀ ⊙ A)ᵀ dO + (w ⊙ K′) dS_out
+//   dK′ = Gᵀ Q′ + (w ⊙ V) dS_outᵀ           dS_in = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
+// Each is one evaluation F(a, b, c; S) of the chunkwise form (o_t =
+// Σ_{m≤t} γ^{t−m}(a_t·b_m) c_m + γ^{t+1} a_t S, S_out = γ^L S + Σ γ^{L−1−m}
+// b_mᵀ c_m): dQ′ = F(dO, V, K′; S_inᵀ); over the reversed sequence (↓),
+// dV↓ = F(K′↓, Q′↓, dO↓; dS_out/γ) with dS_in = γ · its S_out, and
+// dK′↓ = F(V↓, dO↓, Q′↓; dS_outᵀ/γ).  Then dq = R(−nθ) dQ′ and
+// dk = d_k^{-1/2} R(−nθ) dK′ (R is orthogonal).
+template <typename Tin, typename Tg>
+ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o,
+                        const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
+                        int64_t pos0, int chunk, const float* s_in, const float* dso, Tg* dq,
+                        Tg* dk, Tg* dv, float* dsi, void* ws, const BwdPlan& p,
+                        cudaStream_t st) {
+  const int BH = B * H;
+  float* qpf = wsp<float>(ws, p.off_qpf);
+  float* kp = wsp<float>(ws, p.off_kp);
+  float* kpf = wsp<float>(ws, p.off_kpf);
+  float* dof = wsp<float>(ws, p.off_dof);
+  float* vf = wsp<float>(ws, p.off_vf);
+  float* fout = wsp<float>(ws, p.off_fout);
+  float* states = wsp<float>(ws, p.off_states);
+  float* sprep = wsp<float>(ws, p.off_sprep);
+  const RowPos rp = no_rowpos();
+  const float p0 = static_cast<float>(pos0);
+  const dim3 rg((d_k / 2 + 31) / 32, (L + 7) / 8);
+  const size_t nk = static_cast<size_t>(BH) * L * d_k, nv = static_cast<size_t>(BH) * L * d_v;
+  const size_t ns = static_cast<size_t>(BH) * d_k * d_v;
+  {
+    Mark m("bwd_rotate", st);
+    simt::rotate_kernel<Tin, float><<<rg, dim3(32, 8), 0, st>>>(q, qpf, cc, BH, H, L, d_k, p0,
+                                                                1.f, rp, 2);
+  }
+  {
+    Mark m("bwd_rotate", st);
+    simt::rotate_kernel<Tin, float><<<rg, dim3(32, 8), 0, st>>>(k, kp, cc, BH, H, L, d_k, p0,
+                                                                cc.kscale, rp, 0);
+  }
+  {
+    Mark m("bwd_flip", st);
+    simt::flip_cvt_kernel<float, float><<<stride_grid(nk), 256, 0, st>>>(kp, kpf, BH, L, d_k, 1);
+  }
+  const float* do32;
+  const float* v32;
+  if constexpr (std::is_same<Tin, float>::value) {
+    do32 = d_o;
+    v32 = v;
+  } else {   // bf16 inputs: fp32 copies in order
+    float* a = wsp<float>(ws, p.off_do);
+    float* b = wsp<float>(ws, p.off_v);
+    {
+      Mark m("bwd_flip", st);
+      simt::flip_cvt_kernel<Tin, float><<<stride_grid(nv), 256, 0, st>>>(d_o, a, BH, L, d_v, 0);
+    }
+    {
+      Mark m("bwd_flip", st);
+      simt::flip_cvt_kernel<Tin, float><<<stride_grid(nv), 256, 0, st>>>(v, b, BH, L, d_v, 0);
+    }
+    do32 = a;
+    v32 = b;
+  }
+  {
+    Mark m("bwd_flip", st);
+    simt::flip_cvt_kernel<Tin, float><<<stride_grid(nv), 256, 0, st>>>(d_o, dof, BH, L, d_v, 1);
+  }
+  {
+    Mark m("bwd_flip", st);
+    simt::flip_cvt_kernel<Tin, float><<<stride_grid(nv), 256, 0, st>>>(v, vf, BH, L, d_v, 1);
+  }
+  simt::HeadScale one, ginv, gam;
+  for (int h = 0; h < kMaxHeads; ++h) {
+    one.s[h] = 1.f;
+    ginv.s[h] = h < H ? static_cast<float>(1.0 / static_cast<double>(cc.gamma[h])) : 1.f;
+    gam.s[h] = h < H ? cc.gamma[h] : 1.f;
+  }
+  CallConsts ca = cc;   // R(−nθ): the same angles with θ negated
+  for (int i = 0; i < kMaxPairs; ++i) ca.theta[i] = -cc.theta[i];
+  ret_status s;
+  // dQ′ = F(dO, V, K′; S_inᵀ), then dq = R(−nθ) dQ′
+  const float* x = nullptr;
+  if (s_in) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1, one);
+    x = sprep;
+  }
+  if ((s = run_simt_core(do32, v32, kp, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
+                         st)) != RET_OK)
+    return s;
+  {
+    Mark m("bwd_rotate", st);
+    simt::rotate_kernel<float, Tg><<<rg, dim3(32, 8), 0, st>>>(fout, dq, ca, BH, H, L, d_k, p0,
+                                                               1.f, rp, 0);
+  }
+  // dK′↓ = F(V↓, dO↓, Q′↓; dS_outᵀ/γ), then dk = d_k^{-1/2} R(−nθ) dK′
+  x = nullptr;
+  if (dso) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1, ginv);
+    x = sprep;
+  }
+  if ((s = run_simt_core(vf, dof, qpf, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
+                         st)) != RET_OK)
+    return s;
+  {
+    Mark m("bwd_rotate", st);
+    simt::rotate_kernel<float, Tg><<<rg, dim3(32, 8), 0, st>>>(fout, dk, ca, BH, H, L, d_k, p0,
+                                                               cc.kscale, rp, 1);
+  }
+  // dV↓ = F(K′↓, Q′↓, dO↓; dS_out/γ) and dS_in = γ · S_out of that evaluation.
+  // dS_out is read (into sprep) before dS_in is written, so the two may alias.
+  x = nullptr;
+  if (dso) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, ginv);
+    x = sprep;
+  }
+  if ((s = run_simt_core(kpf, qpf, dof, cc, BH, H, L, d_k, d_v, chunk, x, dsi, fout, states,
+                         st)) != RET_OK)
+    return s;
+  {
+    Mark m("bwd_flip", st);
+    simt::flip_cvt_kernel<float, Tg><<<stride_grid(nv), 256, 0, st>>>(fout, dv, BH, L, d_v, 1);
+  }
+  if (dsi) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, gam);
+  }
+  return last_launch();
+}
+
 // Scratch of ret_chunkwise_noalloc: part of this module's device image, so
 // using it allocates nothing at call time.  Its device address is looked up
 // once per device (with that device current) and cached.
@@ -718,6 +926,68 @@ ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_d
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, true);
 }
 
+ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, int B, int H, int L, int d_k, int d_v,
+                                       int chunk, int* path, size_t* workspace_bytes) {
+  if (!path || !workspace_bytes) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || chunk < 1)
+    return RET_EINVAL;
+  *path = RET_PATH_SIMT;
+  *workspace_bytes = plan_backward(in_dt, B, H, L, d_k, d_v, chunk).bytes;
+  return RET_OK;
+}
+
+ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, const void* d_out,
+                                  ret_dtype in_dt, const float* gamma, const float* theta, int B,
+                                  int H, int L, int d_k, int d_v, int64_t pos0, int chunk,
+                                  const float* state_in, const float* d_state_out, void* dq,
+                                  void* dk, void* dv, ret_dtype grad_dt, float* d_state_in,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, d_state_in, dq,
+                              grad_dt, nullptr);
+  if (s != RET_OK) return s;
+  if (!d_out || !dk || !dv || !al16(d_out) || !al16(dk) || !al16(dv)) return RET_EINVAL;
+  if (d_state_out && !al16(d_state_out)) return RET_EINVAL;
+  if (chunk < 1) return RET_EINVAL;
+  const int64_t nch = (static_cast<int64_t>(L) + chunk - 1) / chunk;
+  if (static_cast<int64_t>(B) * H * nch > 65535 || (L + 7) / 8 > 65535) return RET_EUNSUPPORTED;
+  CallConsts cc;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
+  for (int h = 0; h < H; ++h)   // the reversed evaluations start from dS_out/γ
+    if (gamma[h] < 0x1p-64f) return RET_EUNSUPPORTED;
+  const BwdPlan p = plan_backward(in_dt, B, H, L, d_k, d_v, chunk);
+  if (!workspace || workspace_bytes < p.bytes || !al16(workspace)) return RET_EWORKSPACE;
+  if (in_dt == RET_F32) {
+    const auto* a = static_cast<const float*>(q);
+    const auto* b = static_cast<const float*>(k);
+    const auto* c = static_cast<const float*>(v);
+    const auto* d = static_cast<const float*>(d_out);
+    if (grad_dt == RET_F32)
+      return run_backward<float, float>(a, b, c, d, cc, B, H, L, d_k, d_v, pos0, chunk, state_in,
+                                        d_state_out, static_cast<float*>(dq),
+                                        static_cast<float*>(dk), static_cast<float*>(dv),
+                                        d_state_in, workspace, p, stream);
+    return run_backward<float, __nv_bfloat16>(
+        a, b, c, d, cc, B, H, L, d_k, d_v, pos0, chunk, state_in, d_state_out,
+        static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+        static_cast<__nv_bfloat16*>(dv), d_state_in, workspace, p, stream);
+  }
+  const auto* a = static_cast<const __nv_bfloat16*>(q);
+  const auto* b = static_cast<const __nv_bfloat16*>(k);
+  const auto* c = static_cast<const __nv_bfloat16*>(v);
+  const auto* d = static_cast<const __nv_bfloat16*>(d_out);
+  if (grad_dt == RET_F32)
+    return run_backward<__nv_bfloat16, float>(a, b, c, d, cc, B, H, L, d_k, d_v, pos0, chunk,
+                                              state_in, d_state_out, static_cast<float*>(dq),
+                                              static_cast<float*>(dk), static_cast<float*>(dv),
+                                              d_state_in, workspace, p, stream);
+  return run_backward<__nv_bfloat16, __nv_bfloat16>(
+      a, b, c, d, cc, B, H, L, d_k, d_v, pos0, chunk, state_in, d_state_out,
+      static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), d_state_in, workspace, p, stream);
+}
+
 ret_status ret_parallel_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,
                              int d_v, ret_dtype out_dt, int gn_enabled, int state_out_wanted,
                              int* path, size_t* workspace_bytes) {
@@ -824,16 +1094,16 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B,
   const float p0 = static_cast<float>(pos0);
   if (in_dt == RET_BF16 && out_dt == RET_BF16)
     simt::rotate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos(), 0);
   else if (in_dt == RET_BF16)
     simt::rotate_kernel<__nv_bfloat16, float><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
+        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos(), 0);
   else if (out_dt == RET_BF16)
     simt::rotate_kernel<float, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
+        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), cc, BH, H, L, d, p0, scale, no_rowpos(), 0);
   else
     simt::rotate_kernel<float, float><<<grid, dim3(32, 8), 0, stream>>>(
-        static_cast<const float*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos());
+        static_cast<const float*>(x), static_cast<float*>(y), cc, BH, H, L, d, p0, scale, no_rowpos(), 0);
   return last_launch();
 }
 

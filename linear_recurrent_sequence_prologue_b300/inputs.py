@@ -104,6 +104,17 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     }
 
 
+def make_grad_inputs(w: Workload, seed: int = 1, d_out_std: float = 1.0,
+                     d_state_std: float = 0.0) -> dict:
+    """Upstream gradients for the gradient pass: d_out [B, H, L, d_v] in the
+    workload dtype and (when d_state_std > 0) d_state_out [B, H, d_k, d_v]
+    fp32, both N(0, std²) on the CPU."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    d_out = _randn(gen, (w.B, w.H, w.L, w.d_v), d_out_std).to(w.torch_dtype)
+    d_state = _randn(gen, (w.B, w.H, w.d_k, w.d_v), d_state_std) if d_state_std > 0 else None
+    return {"d_out": d_out, "d_state_out": d_state}
+
+
 def make_decode_inputs(w: Workload, seed: int = 0, steps: int | None = None,
                        device: str = "cpu") -> dict:
     """Initial state and per-step q, k, v for the decode workload.

@@ -180,3 +180,41 @@ def test_path_selection(lib):
     assert _plan(lib, _lib.RET_BF16, 1, 2, 256, 256, 128, 128, gamma=g)[0] == _lib.RET_PATH_SIMT
     g = np.array([0.9, 0.99], np.float32)
     assert _plan(lib, _lib.RET_BF16, 1, 2, 256, 256, 128, 128, gamma=g)[0] == _lib.RET_PATH_TC
+
+
+def test_backward_plan_and_validation(lib):
+    """ret_chunkwise_backward: workspace layout and synchronous argument checks."""
+    path, nb = C.c_int(0), C.c_size_t(0)
+    assert lib.ret_chunkwise_backward_plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128,
+                                           C.byref(path), C.byref(nb)) == _lib.RET_OK
+    BH, L = 32, 8192
+    rk, rv = BH * L * 256 * 4, BH * L * 512 * 4
+    # Q′↓, K′, K′↓ (fp32); dO, V in order (bf16 inputs only) and reversed; one
+    # evaluation output; per-chunk states; one prepared state
+    assert path.value == _lib.RET_PATH_SIMT
+    assert nb.value == 3 * rk + 4 * rv + rv + BH * 64 * 256 * 512 * 4 + BH * 256 * 512 * 4
+    nb32 = C.c_size_t(0)
+    assert lib.ret_chunkwise_backward_plan(_lib.RET_F32, 2, 16, 8192, 256, 512, 128,
+                                           C.byref(path), C.byref(nb32)) == _lib.RET_OK
+    assert nb32.value == nb.value - 2 * rv          # fp32 inputs are read in place
+    assert lib.ret_chunkwise_backward_plan(_lib.RET_F32, 1, 1, 8, 16, 16, 0,
+                                           C.byref(path), C.byref(nb32)) == _lib.RET_EINVAL
+
+    g = np.full(2, 0.9, np.float32)
+    t = np.ones(8, np.float32)
+    P, M = C.c_void_p(0x1000), C.c_void_p(0x1008)
+
+    def call(d_out=P, dk=P, gamma=g, B=1, H=2, L=64, chunk=16, ws=None, wsn=0):
+        return lib.ret_chunkwise_backward(P, P, P, d_out, _lib.RET_F32, _fp(gamma), _fp(t), B, H, L, 16,
+                                          16, 0, chunk, None, None, P, dk, P, _lib.RET_F32, None, ws,
+                                          wsn, None)
+
+    assert call(d_out=None) == _lib.RET_EINVAL                       # no upstream gradient
+    assert call(dk=M) == _lib.RET_EINVAL                             # misaligned output
+    assert call(chunk=0) == _lib.RET_EINVAL
+    assert call(gamma=np.array([0.9, 1.5], np.float32)) == _lib.RET_EINVAL
+    assert call(gamma=np.array([0.9, 2.0 ** -70], np.float32)) == _lib.RET_EUNSUPPORTED
+    gh = np.full(128, 0.9, np.float32)
+    assert call(gamma=gh, H=128, L=65536, chunk=64) == _lib.RET_EUNSUPPORTED   # grid rows
+    assert call() == _lib.RET_EWORKSPACE                             # valid: no workspace
+    assert call(ws=P, wsn=16) == _lib.RET_EWORKSPACE                 # too small

@@ -11,8 +11,8 @@ import torch
 
 import linear_recurrent_sequence_prologue_b300 as R
 from linear_recurrent_sequence_prologue_b300.inputs import (WORKLOADS, Workload, gamma_schedule,
-                                                            make_decode_inputs, make_inputs,
-                                                            theta_schedule, to_f64)
+                                                            make_decode_inputs, make_grad_inputs,
+                                                            make_inputs, theta_schedule, to_f64)
 from oracle import retention_ref as O
 
 from helpers import BF16_TOL, assert_close, gpu_np, head_slice, max_rel_inf, rel_fro
@@ -389,6 +389,91 @@ def test_msr7b_sampled_heads():
         ref_o, ref_s = O.retention(q, k, v, g, th, 0, si, "chunkwise", w.chunk)
         assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref_o, torch.bfloat16, f"7B out (b={b},h={h})")
         assert_close(gpu_np(s[b:b + 1, h:h + 1]), ref_s, torch.bfloat16, f"7B state (b={b},h={h})")
+
+
+# --------------------------------------------------------------- gradients --
+def _oracle_bwd(inp, gi, pos0):
+    return O.retention_backward(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                                np.asarray(inp["gamma"], np.float64),
+                                np.asarray(inp["theta"], np.float64), pos0,
+                                to_f64(inp["state_in"]), to_f64(gi["d_out"]),
+                                to_f64(gi["d_state_out"]))
+
+
+@pytest.mark.parametrize("dtype,gdtype,B,H,L,d_k,d_v,chunk,pos0,state,dso", [
+    (torch.float32, torch.float32, 2, 3, 300, 64, 96, 64, 7, True, True),      # 5 chunks, ragged
+    (torch.float32, torch.float32, 1, 2, 77, 32, 768, 100, 0, True, False),    # one chunk, wide d_v
+    (torch.bfloat16, torch.float32, 2, 2, 256, 128, 128, 128, 100, False, True),
+    (torch.bfloat16, torch.bfloat16, 1, 2, 200, 256, 256, 48, 3, True, True),
+])
+def test_backward_vs_oracle(dtype, gdtype, B, H, L, d_k, d_v, chunk, pos0, state, dso):
+    w, inp = _custom(B, H, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0)
+    gi = make_grad_inputs(w, seed=5, d_state_std=1.0 if dso else 0.0)
+    ref = _oracle_bwd(inp, gi, pos0)
+    d = _cuda(inp)
+    dso_c = gi["d_state_out"].cuda() if dso else None
+    got = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
+                               chunk=chunk, pos0=pos0, state_in=d["state_in"], d_state_out=dso_c,
+                               grad_dtype=gdtype)
+    assert R.sync_status() == R.RET_OK
+    for g, r, name in zip(got, ref, ("dq", "dk", "dv", "dS_in")):
+        assert_close(gpu_np(g), r, torch.float32 if name == "dS_in" else gdtype, name)
+
+
+def test_backward_zero_upstream_and_state_aliasing():
+    w, inp = _custom(1, 2, 130, 64, 64, torch.float32, 32, state_std=0.1)
+    d = _cuda(inp)
+    # zero upstream gradients give exactly zero gradients
+    z = torch.zeros((1, 2, 130, 64), device="cuda")
+    zs = torch.zeros((1, 2, 64, 64), device="cuda")
+    got = R.chunkwise_backward(d["q"], d["k"], d["v"], z, inp["gamma"], inp["theta"], chunk=32,
+                               state_in=d["state_in"], d_state_out=zs)
+    assert all(int(torch.count_nonzero(t)) == 0 for t in got)
+    # d_state_in written over d_state_out: the same values as into a separate buffer
+    gi = make_grad_inputs(w, seed=2, d_state_std=1.0)
+    dso = gi["d_state_out"].cuda()
+    a = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
+                             chunk=32, pos0=9, state_in=d["state_in"], d_state_out=dso)
+    buf = dso.clone()
+    b = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
+                             chunk=32, pos0=9, state_in=d["state_in"], d_state_out=buf, d_state_in=buf)
+    assert R.sync_status() == R.RET_OK
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_backward_msr7b_sampled_heads():
+    """The 7B shape (bf16 inputs, fp32 gradients): one head against the
+    oracle over the whole sequence; another on the prefix that fixes dq
+    (positions ≤ t and S_in) and the suffix that fixes dk, dv (positions ≥ m
+    and dS_out)."""
+    w = WORKLOADS["msr7b"]
+    inp = make_inputs(w, seed=0)
+    gi = make_grad_inputs(w, seed=5, d_state_std=1.0)
+    d = _cuda(inp)
+    dq, dk, dv, dsi = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"],
+                                           inp["theta"], chunk=w.chunk, state_in=d["state_in"],
+                                           d_state_out=gi["d_state_out"].cuda(),
+                                           grad_dtype=torch.float32)
+    assert R.sync_status() == R.RET_OK
+    b, h = 1, 15
+    q, k, v, si, g, th = head_slice(inp, b, h)
+    dO = to_f64(gi["d_out"][b:b + 1, h:h + 1])
+    dSo = to_f64(gi["d_state_out"][b:b + 1, h:h + 1])
+    ref = O.retention_backward(q, k, v, g, th, 0, si, dO, dSo)
+    for got, r, name in zip((dq, dk, dv, dsi), ref, ("dq", "dk", "dv", "dS_in")):
+        assert_close(gpu_np(got[b:b + 1, h:h + 1]), r, torch.float32, f"7B {name} (b={b},h={h})")
+    b, h, n = 0, 0, 384
+    q, k, v, si, g, th = head_slice(inp, b, h)
+    dO = to_f64(gi["d_out"][b:b + 1, h:h + 1])
+    dSo = to_f64(gi["d_state_out"][b:b + 1, h:h + 1])
+    rq = O.retention_backward(q[:, :, :n], k[:, :, :n], v[:, :, :n], g, th, 0, si, dO[:, :, :n])[0]
+    assert_close(gpu_np(dq[b:b + 1, h:h + 1, :n]), rq, torch.float32, "7B dq prefix")
+    m0 = w.L - n
+    _, rk, rv, _ = O.retention_backward(q[:, :, m0:], k[:, :, m0:], v[:, :, m0:], g, th, m0, None,
+                                        dO[:, :, m0:], dSo)
+    assert_close(gpu_np(dk[b:b + 1, h:h + 1, m0:]), rk, torch.float32, "7B dk suffix")
+    assert_close(gpu_np(dv[b:b + 1, h:h + 1, m0:]), rv, torch.float32, "7B dv suffix")
 
 
 def test_decode_1024_steps_vs_chunkwise_and_oracle():
