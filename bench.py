@@ -68,6 +68,21 @@ def backward_flops(w):
     return 3 * n * (2 * b * (w.d_k + w.d_v) + 2 * w.d_k * w.d_v), 3 * n * 2 * w.d_k * w.d_v
 
 
+def backward_tc_bytes(w, grad_bytes=2):
+    """Bytes the HBM-bound kernels of the tensor-core gradient pass move per
+    step: the operand layouts (bwd_prep: q, k, V read twice, dO three times;
+    ω/ζ-folded operands padded to whole chunks, the multiplied operand once
+    per 256-column piece of d_v) and the gradients (bwd_grad_out: fp32
+    piece outputs in, gradients out)."""
+    n = w.B * w.H
+    Lp = -(-w.L // 128) * 128
+    P = -(-w.d_v // 256)
+    rd = n * w.L * 2 * (3 * w.d_v + 2 * w.d_v + 2 * w.d_k + 2 * w.d_k)
+    wr = n * 2 * (4 * Lp * w.d_v + 2 * P * w.L * w.d_k + 2 * Lp * w.d_k + w.L * w.d_v)
+    go = n * w.L * (2 * (P * w.d_k * 4 + w.d_k * grad_bytes) + w.d_v * 4 + w.d_v * grad_bytes)
+    return {"bwd_prep": rd + wr, "bwd_grad_out": go}
+
+
 # fp32 FFMA peak: 148 SMs x 128 fp32 lanes x 2 flop per FFMA at the 2032 MHz maximum SM clock.
 FFMA_TFLOPS = 148 * 128 * 2 * 2032e6 / 1e12
 
@@ -418,7 +433,8 @@ def main():
         d_o, dso = gi["d_out"].to(dev), gi["d_state_out"].to(dev)
         grads = tuple(torch.empty_like(t) for t in (q, k, v))
         dsi = torch.empty_like(dso)
-        _, bws_bytes = R.backward_plan(torch.bfloat16, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk)
+        bpath, bws_bytes = R.backward_plan(torch.bfloat16, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk,
+                                           gamma=inp["gamma"])
         bws = torch.empty(bws_bytes, dtype=torch.uint8, device=dev)
         bargs = (vp(q), vp(k), vp(v), vp(d_o), _lib.RET_BF16, fptr(garr), fptr(tarr), w.B, w.H, w.L,
                  w.d_k, w.d_v, 0, w.chunk, vp(s_in), vp(dso), vp(grads[0]), vp(grads[1]),
@@ -453,18 +469,39 @@ def main():
         f_out, f_ds = backward_flops(w)
         step_ms = {nm: sum(t) / bhook for nm, t in bper.items()}   # all launches of a name, per step
         btop = max(step_ms, key=step_ms.get)
-        bflops = {"bwd_chunk_out": f_out, "bwd_chunk_dS": f_ds}.get(btop)
-        bach = bflops / (step_ms[btop] / 1e3) / 1e12 if bflops else None
+        bbytes = None
+        if bpath == _lib.RET_PATH_TC:
+            # the chunk kernels run all four products of the three evaluations;
+            # the operand and gradient passes are HBM-bound
+            bflops = {"bwd_chunk_tc": f_out + f_ds}.get(btop)
+            bbytes = backward_tc_bytes(w).get(btop)
+            if bflops:
+                bpeak, bbound, bkind = peak, "tensor", f"bf16_tflops burst ({peak_kind})"
+            else:
+                bpeak, bbound, bkind = peaks["hbm_gbs"], "hbm", f"hbm_gbs ({peak_kind})"
+            bdt = "bf16 (bf16 operands, fp32 accumulation; bf16 gradients)"
+        else:
+            bflops = {"bwd_chunk_out": f_out, "bwd_chunk_dS": f_ds}.get(btop)
+            bpeak, bbound = FFMA_TFLOPS, "alu"
+            bkind = "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2032 MHz"
+            bdt = "f32 (bf16 inputs and gradients)"
+        if bflops:
+            bach = bflops / (step_ms[btop] / 1e3) / 1e12
+        elif bbytes:
+            bach = bbytes / (step_ms[btop] / 1e3) / 1e9
+        else:
+            bach = None
         backward = {
             "metric": "gradient pass tokens/s", "value": replica_throughput(w.B * w.L, bms / 1e3, world),
             "unit": "tokens/s", "ms_per_step": bms, "steps": args.backward_steps,
-            "dtype": "f32 (bf16 inputs and gradients)",
+            "dtype": bdt, "path": "tensor cores" if bpath == _lib.RET_PATH_TC else "fp32 kernels",
             "config": {"workload": w.name, "chunk": w.chunk, "state_in": True, "d_state_out": True},
-            "roofline": {"bound": "alu", "kernel": btop, "achieved": bach, "peak": FFMA_TFLOPS,
-                         "unit": "TFLOP/s", "frac": bach / FFMA_TFLOPS if bach else None,
-                         "traffic": None,
-                         "peak_kind": "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2032 MHz",
-                         "algorithmic_flop_per_step": f_out + f_ds},
+            "roofline": {"bound": bbound, "kernel": btop, "achieved": bach, "peak": bpeak,
+                         "unit": "GB/s" if bbound == "hbm" else "TFLOP/s",
+                         "frac": bach / bpeak if bach else None,
+                         "traffic": None, "peak_kind": bkind,
+                         "algorithmic_flop_per_step": f_out + f_ds,
+                         "algorithmic_bytes_of_kernel_per_step": bbytes},
             "kernels_ms_per_step": step_ms,
             "gpu_launches": int(round(nb_k / bhook * args.backward_steps)),
             "clocks": bsampler.summary()}

@@ -185,9 +185,14 @@ ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, i
  *   dQ′ = G K′ + ξ ⊙ (dO S_inᵀ)          dV = (Q′K′ᵀ ⊙ A)ᵀ dO + (w ⊙ K′) dS_out
  *   dK′ = Gᵀ Q′ + (w ⊙ V) dS_outᵀ         dS_in = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
  *   dq = R(−nθ) dQ′,  dk = d_k^{-1/2} R(−nθ) dK′    (the Θ prologue's adjoint)
- * Computed on the fp32 kernels as three chunkwise evaluations (one in
- * order, two over the reversed sequence, which turns the sums over t ≥ m
- * into causal ones); `chunk` is their chunk length (any ≥ 1).
+ * Computed as three chunkwise evaluations (one in order, two over the
+ * reversed sequence, which turns the sums over t ≥ m into causal ones).
+ * Paths: bf16 inputs with chunk = 128, d_k ∈ {128, 256}, d_v a multiple of
+ * 128 and every γ^127 ≥ 2^-60 run the evaluations on the tensor-core chunk
+ * kernels (bf16 operands, fp32 accumulation; the two evaluations that
+ * contract over d_v run as sums of pieces of at most 256 columns);
+ * everything else runs on the fp32 kernels with `chunk` as the chunk length
+ * (any ≥ 1).
  * q, k, v, d_out: DEVICE, in_dt, layouts as above.  dq, dk [B, H, L, d_k]
  * and dv [B, H, L, d_v]: DEVICE, grad_dt; they must not alias any input.
  * state_in, d_state_out: DEVICE fp32 [B, H, d_k, d_v] or NULL (zero).
@@ -204,9 +209,11 @@ ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, c
                                   float* d_state_in, void* workspace, size_t workspace_bytes,
                                   cudaStream_t stream);
 
-/* Path (always RET_PATH_SIMT) and workspace bytes of ret_chunkwise_backward. */
-ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, int B, int H, int L, int d_k, int d_v,
-                                       int chunk, int* path, size_t* workspace_bytes);
+/* Path and workspace bytes of ret_chunkwise_backward.  gamma may be NULL
+ * (then the tensor-core path is assumed allowed). */
+ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                       int d_k, int d_v, int chunk, int* path,
+                                       size_t* workspace_bytes);
 
 /* ------------------------------------------------------------------------
  * ret_parallel — parallel form O = (Q′K′ᵀ ⊙ D) V + γ^{t+1} q′_t S_in

@@ -160,12 +160,15 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
     return out, state_out
 
 
-def backward_plan(in_dtype, B, H, L, d_k, d_v, chunk):
-    """(path, workspace bytes) of the gradient pass (path 2 = fp32 kernels)."""
+def backward_plan(in_dtype, B, H, L, d_k, d_v, chunk, gamma=None):
+    """(path, workspace bytes) of the gradient pass (1 = tcgen05, 2 = fp32 kernels)."""
     lib = load()
+    gp = None
+    if gamma is not None:
+        garr, gp = _host_f32(gamma, H, "gamma")
     path, nbytes = C.c_int(0), C.c_size_t(0)
     check("ret_chunkwise_backward_plan",
-          lib.ret_chunkwise_backward_plan(_DT[in_dtype], B, H, L, d_k, d_v, int(chunk),
+          lib.ret_chunkwise_backward_plan(_DT[in_dtype], gp, B, H, L, d_k, d_v, int(chunk),
                                           C.byref(path), C.byref(nbytes)))
     return path.value, nbytes.value
 
@@ -196,7 +199,7 @@ def chunkwise_backward(q, k, v, d_out, gamma, theta, chunk: int, pos0: int = 0, 
     sshape = (B, H, d_k, d_v)
     if d_state_in is None and return_d_state_in:
         d_state_in = torch.empty(sshape, dtype=torch.float32, device=q.device)
-    _, nbytes = backward_plan(q.dtype, B, H, L, d_k, d_v, chunk)
+    _, nbytes = backward_plan(q.dtype, B, H, L, d_k, d_v, chunk, gamma=garr)
     wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
     st = lib.ret_chunkwise_backward(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(d_out, "d_out"), idt, gp, tp, B, H, L, d_k,

@@ -439,20 +439,155 @@ __global__ void __launch_bounds__(256) flip_cvt_kernel(const Tin* __restrict__ x
   }
 }
 
-// dst = hs.s[h] · src for BH states of rows × cols, transposed into
-// [BH][cols][rows] when transpose.  src == dst only without transpose.
+// dst = hs.s[h] · M for BH states src [BH][rows][cols], where M = src or,
+// with transpose, srcᵀ ([cols][rows]).  M's rows are cut into pieces of
+// prows rows (the last may be shorter); piece p of all BH states comes
+// before piece p+1: dst = [piece][BH][rows of the piece][columns of M].
+// prows ≥ M's rows gives the plain [BH][M rows][M cols] layout.  src == dst
+// only without transpose and pieces.
 __global__ void __launch_bounds__(256) state_prep_kernel(const float* __restrict__ src,
                                                          float* dst, int BH, int H, int rows,
-                                                         int cols, int transpose, HeadScale hs) {
+                                                         int cols, int transpose, int prows,
+                                                         HeadScale hs) {
   const size_t per = static_cast<size_t>(rows) * cols;
   const size_t n = per * BH;
+  const int mrows = transpose ? cols : rows, mcols = transpose ? rows : cols;
   for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
        e += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const size_t bh = e / per;
-    const size_t rc = e - bh * per;
-    const size_t r = rc / cols, c = rc - r * cols;
-    const float val = src[e] * hs.s[bh % H];
-    dst[transpose ? bh * per + c * rows + r : e] = val;
+    const int rc = static_cast<int>(e - bh * per);
+    const int r = rc / cols, c = rc - r * cols;
+    const int mr = transpose ? c : r, mc = transpose ? r : c;
+    const int piece = mr / prows, rl = mr - piece * prows;
+    const int ph = min(prows, mrows - piece * prows);
+    const size_t di = static_cast<size_t>(piece) * prows * mcols * BH +
+                      (bh * ph + rl) * static_cast<size_t>(mcols) + mc;
+    dst[di] = src[e] * hs.s[bh % H];
+  }
+}
+
+// Operands of the tensor-core evaluations in the gradient pass, bf16:
+//   op[bh][t][:] = f(t) · scale · R?((pos0 + t_s)θ) src[bh][t_s][:]   (t < L)
+//   op[bh][t][:] = 0                                                  (L ≤ t < rows_out)
+// with t_s = L−1−t when flip, else t; the rotation only when rotate.  f(t) is
+// 1 (fold 0), ω = γ^{(t mod b)+1−b_c} (fold 1) or ζ = γ^{b_c−1−(t mod b)}
+// (fold 2), b_c the length of t's chunk of b rows (the last may be shorter):
+// the per-row factors of the chunk kernels' rewritten form, taken over the
+// sequence as it is read (reversed when flip).  The columns are stored in
+// pieces of pw (the last may be narrower), piece-major:
+// dst[piece][bh][t][columns of the piece]; ncopy copies of the whole
+// operand follow each other.  d and pw multiples of 8.
+// Thread ↔ (row t, 8 columns): the angles and the fold exponent are computed
+// once and used for all B·H heads, eight heads' loads in flight.
+__global__ void __launch_bounds__(256) prep_operand_kernel(
+    const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, CallConsts cc,
+    int BH, int H, int L, int rows_out, int d, int pw, int ncopy, int flip, int rotate,
+    float pos0, float scale, int fold, int chunk) {
+  constexpr int U = 8;
+  const int vecs = d / 8;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows_out * vecs) return;
+  const int t = idx / vecs, cv = idx - t * vecs;
+  const int piece = (8 * cv) / pw;
+  const int wp = min(pw, d - piece * pw);   // width of this piece
+  const size_t pbase = static_cast<size_t>(piece) * pw * rows_out * BH;
+  const size_t copy = static_cast<size_t>(rows_out) * d * BH;
+  const size_t ocol = 8 * cv - piece * pw;
+  auto optr = [&](int bh, int cp) {
+    return reinterpret_cast<uint4*>(dst + cp * copy + pbase +
+                                    (static_cast<size_t>(bh) * rows_out + t) * wp + ocol);
+  };
+  if (t >= L) {
+    for (int bh = 0; bh < BH; ++bh)
+      for (int cp = 0; cp < ncopy; ++cp) *optr(bh, cp) = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int ts = flip ? L - 1 - t : t;
+  float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (rotate) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(ts), cc.theta[4 * cv + u], c[u], sn[u]);
+  }
+  float ex = 0.f;
+  if (fold) {
+    const int nch = (L + chunk - 1) / chunk;
+    const int bc = (t / chunk == nch - 1) ? L - (nch - 1) * chunk : chunk;
+    const int j = t % chunk;
+    ex = fold == 1 ? static_cast<float>(j + 1 - bc) : static_cast<float>(bc - 1 - j);
+  }
+  const size_t hstride = static_cast<size_t>(L) * d;
+  const __nv_bfloat16* s0 = src + static_cast<size_t>(ts) * d + 8 * cv;
+  for (int bh0 = 0; bh0 < BH; bh0 += U) {
+    uint4 raw[U];
+#pragma unroll
+    for (int uu = 0; uu < U; ++uu)
+      if (bh0 + uu < BH) raw[uu] = __ldcs(reinterpret_cast<const uint4*>(s0 + (bh0 + uu) * hstride));
+#pragma unroll
+    for (int uu = 0; uu < U; ++uu) {
+      const int bh = bh0 + uu;
+      if (bh >= BH) break;
+      const float f = fold ? scale * gpow(cc.lg2g[bh % H], ex) : scale;
+      const uint32_t w[4] = {raw[uu].x, raw[uu].y, raw[uu].z, raw[uu].w};
+      uint32_t o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float a = bf16lo_to_f32(w[u]), b = bf16hi_to_f32(w[u]);
+        o[u] = pack_bf16x2(f * (a * c[u] - b * sn[u]), f * fmaf(a, sn[u], b * c[u]));
+      }
+      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int cp = 0; cp < ncopy; ++cp) *optr(bh, cp) = ov;
+    }
+  }
+}
+
+// Gradients from the fp32 outputs of the evaluations:
+//   y[bh][t][:] = scale · R?(−(pos0 + t)θ) Σ_{p<np} x[p][bh][t_s][:]
+// with t_s = L−1−t when flip; x pieces `pstride` elements apart; R(−φ) the
+// adjoint (inverse) of the prologue's rotation, only when rotate.
+// Thread ↔ (row t, 8 columns), looping over the B·H heads.  d a multiple of 8.
+template <typename Tg>
+__global__ void __launch_bounds__(256) grad_out_kernel(const float* __restrict__ x,
+                                                       size_t pstride, int np,
+                                                       Tg* __restrict__ y, CallConsts cc,
+                                                       int BH, int L, int d, int flip,
+                                                       int rotate, float pos0, float scale) {
+  const int vecs = d / 8;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= L * vecs) return;
+  const int t = idx / vecs, cv = idx - t * vecs;
+  const int ts = flip ? L - 1 - t : t;
+  float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
+  if (rotate) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
+  }
+  for (int bh = 0; bh < BH; ++bh) {
+    const float* xr = x + (static_cast<size_t>(bh) * L + ts) * d + 8 * cv;
+    float4 a0 = __ldcs(reinterpret_cast<const float4*>(xr));
+    float4 a1 = __ldcs(reinterpret_cast<const float4*>(xr) + 1);
+    for (int p = 1; p < np; ++p) {
+      const float4 b0 = __ldcs(reinterpret_cast<const float4*>(xr + p * pstride));
+      const float4 b1 = __ldcs(reinterpret_cast<const float4*>(xr + p * pstride) + 1);
+      a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+      a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+    }
+    const float e[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    float r[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float a = e[2 * u], b = e[2 * u + 1];
+      // R(−φ): (a cos φ + b sin φ, b cos φ − a sin φ)
+      r[2 * u] = scale * fmaf(a, c[u], b * sn[u]);
+      r[2 * u + 1] = scale * fmaf(b, c[u], -a * sn[u]);
+    }
+    Tg* yr = y + (static_cast<size_t>(bh) * L + t) * d + 8 * cv;
+    if constexpr (sizeof(Tg) == 2) {
+      *reinterpret_cast<uint4*>(yr) = make_uint4(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]),
+                                                 pack_bf16x2(r[4], r[5]), pack_bf16x2(r[6], r[7]));
+    } else {
+      reinterpret_cast<float4*>(yr)[0] = make_float4(r[0], r[1], r[2], r[3]);
+      reinterpret_cast<float4*>(yr)[1] = make_float4(r[4], r[5], r[6], r[7]);
+    }
   }
 }
 

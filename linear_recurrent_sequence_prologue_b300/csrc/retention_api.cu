@@ -1,6 +1,7 @@
 // libretention.so — C ABI (include/retention.h): argument validation, path
 // selection, workspace layout and kernel launches.  One translation unit so
 // the device status word and the kernels share a module.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -679,7 +680,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   const float* x = nullptr;
   if (s_in) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1, one);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1, d_v, one);
     x = sprep;
   }
   if ((s = run_simt_core(do32, v32, kp, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
@@ -694,7 +695,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   x = nullptr;
   if (dso) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1, ginv);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1, d_v, ginv);
     x = sprep;
   }
   if ((s = run_simt_core(vf, dof, qpf, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
@@ -710,7 +711,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   x = nullptr;
   if (dso) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, ginv);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, d_k, ginv);
     x = sprep;
   }
   if ((s = run_simt_core(kpf, qpf, dof, cc, BH, H, L, d_k, d_v, chunk, x, dsi, fout, states,
@@ -722,7 +723,239 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   }
   if (dsi) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, gam);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, d_k, gam);
+  }
+  return last_launch();
+}
+
+// ---------------------------------------------------------------------------
+// Gradient pass on the tensor cores (bf16 inputs): the same three
+// evaluations, each run by the chunk kernels on operands that
+// prep_operand_kernel lays out as the front pass lays out Q′ and K̂′ (ω and
+// ζ folded, rows padded to whole chunks).  The two evaluations whose scores
+// contract over d_v run as a sum of pieces of at most 256 columns (the
+// scores are linear in the contracted columns, and so is the cross term
+// once S_in is cut by the same rows).  When every piece is 256 wide, the
+// pieces run in one launch as extra grid rows (piece p of (b, h) is row
+// p·B·H + b·H + h), which keeps enough CTAs in flight when d_k = 256 gives
+// only two d_v tiles per row; the operand the scores multiply is then
+// stored once per piece.
+// ---------------------------------------------------------------------------
+constexpr int kBwdPiece = 256;
+
+int bwd_pieces(int d_v) { return (d_v + kBwdPiece - 1) / kBwdPiece; }
+
+bool tc_backward_ok(ret_dtype in_dt, const float* gamma, int H, int d_k, int d_v, int chunk,
+                    int B) {
+  if (g_force_path == RET_PATH_SIMT || in_dt != RET_BF16 || chunk != tcc::CH) return false;
+  if (!(d_k == 128 || d_k == 256) || d_v % tcc::VT != 0) return false;
+  if (static_cast<size_t>(B) * H * bwd_pieces(d_v) > kMaxGridRows) return false;
+  return tc_gamma_ok(gamma, H, chunk);
+}
+
+struct TcBwdPlan {
+  size_t off_a = 0, off_b = 0, off_c = 0, off_x = 0, off_sprep = 0, off_tail = 0, bytes = 0;
+  int pieces = 0;
+  bool as_rows = false;   // all pieces in one launch
+};
+
+TcBwdPlan plan_tc_backward(int B, int H, int L, int d_k, int d_v) {
+  TcBwdPlan p;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Lp = static_cast<size_t>((L + tcc::CH - 1) / tcc::CH) * tcc::CH;
+  const size_t W = d_k > d_v ? d_k : d_v;
+  p.pieces = bwd_pieces(d_v);
+  p.as_rows = d_v % kBwdPiece == 0;
+  const size_t pk = static_cast<size_t>(p.pieces) * d_k;
+  const size_t xw = std::max(pk, static_cast<size_t>(d_v));
+  const size_t cw = std::max(p.as_rows ? pk : static_cast<size_t>(d_k), static_cast<size_t>(d_v));
+  size_t off = 0;
+  p.off_a = off; off += up256(BH * Lp * W * 2);       // ω-folded left operand
+  p.off_b = off; off += up256(BH * Lp * W * 2);       // ζ-folded right operand
+  p.off_c = off; off += up256(BH * L * cw * 2);       // the operand the scores multiply
+  p.off_x = off; off += up256(BH * L * xw * 4);       // fp32 outputs (one per piece)
+  p.off_sprep = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4);
+  if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * xw * 4); }
+  p.bytes = off;
+  return p;
+}
+
+// out (fp32 [rows][L][dvF]) = the chunkwise form over `rows` sequences with
+// Q″ = a and K̂′ = b (bf16 [rows][Lp][dkF]), V = c (bf16 [rows][L][dvF]);
+// s_in / s_out per row [dkF][dvF].  Head of row r: r mod H.
+ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
+                       const __nv_bfloat16* c, int dvF, const float* s_in, float* s_out,
+                       float* out, void* tail, const CallConsts& cc, int rows, int H, int L,
+                       cudaStream_t st) {
+  const int nch = (L + tcc::CH - 1) / tcc::CH;
+  const int Lp = nch * tcc::CH;
+  const uint64_t qrows = static_cast<uint64_t>(rows) * Lp;
+  const bool pair = tc_pair_ok(dkF, dvF);
+  CUtensorMap mq, mk, mv, mqh, mkh;
+  if (!make_map(&mq, a, qrows, dkF) || !make_map(&mk, b, qrows, dkF) ||
+      !make_map3(&mv, c, static_cast<uint64_t>(rows), static_cast<uint64_t>(L), dvF))
+    return RET_ECUDA;
+  if (pair && (!make_map(&mqh, a, qrows, dkF, 64) || !make_map(&mkh, b, qrows, dkF, 64)))
+    return RET_ECUDA;
+  tcc::ChunkArgs g;
+  g.state_in = s_in;
+  g.state_out = s_out;
+  g.out = out;
+  g.out_f32 = 1;
+  g.H = H;
+  g.d_v = dvF;
+  g.nchunks = nch;
+  g.seq_len = L;
+  g.seq_lp = Lp;
+  g.seq_chunks = nch;
+  g.tail_out = (L % tcc::CH != 0) ? tail : nullptr;
+  g.seq_div = 1;
+  g.raw_ds = 0;
+  auto launch_pair = [&](auto kern, uint32_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(dvF / tcc::VT, rows);
+    cfg.blockDim = dim3(tcc::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    Mark m("bwd_chunk_tc", st);
+    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, g, cc);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  };
+  auto launch = [&](auto kern, uint32_t smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    Mark m("bwd_chunk_tc", st);
+    kern<<<dim3(dvF / tcc::VT, rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, g, cc);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if (pair && dkF == 256) e = launch_pair(tcq::pair_tc_kernel<256>, tcq::Cfg<256>::SMEM_BYTES);
+  else if (pair) e = launch_pair(tcq::pair_tc_kernel<128>, tcq::Cfg<128>::SMEM_BYTES);
+  else if (dkF == 256) e = launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES);
+  else e = launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES);
+  if (e != cudaSuccess) return RET_ECUDA;
+  if (g.tail_out) {
+    const int T = L - (nch - 1) * tcc::CH;
+    const int row_vecs = dvF * 4 / 16;
+    const size_t n = static_cast<size_t>(rows) * T * row_vecs;
+    Mark m("bwd_tail_copy", st);
+    tcc::tail_copy_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint4*>(g.tail_out), reinterpret_cast<uint4*>(out), rows, T, L,
+        (nch - 1) * tcc::CH, row_vecs);
+  }
+  return last_launch();
+}
+
+template <typename Tg>
+ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
+                           const __nv_bfloat16* v, const __nv_bfloat16* d_o, const CallConsts& cc,
+                           int B, int H, int L, int d_k, int d_v, int64_t pos0, const float* s_in,
+                           const float* dso, Tg* dq, Tg* dk, Tg* dv, float* dsi, void* ws,
+                           const TcBwdPlan& p, cudaStream_t st) {
+  const int BH = B * H;
+  const int nch = (L + tcc::CH - 1) / tcc::CH;
+  const int Lp = nch * tcc::CH;
+  auto* A = wsp<__nv_bfloat16>(ws, p.off_a);
+  auto* Bo = wsp<__nv_bfloat16>(ws, p.off_b);
+  auto* Cc = wsp<__nv_bfloat16>(ws, p.off_c);
+  float* X = wsp<float>(ws, p.off_x);
+  float* sprep = wsp<float>(ws, p.off_sprep);
+  void* tail = p.off_tail ? wsp<void>(ws, p.off_tail) : nullptr;
+  const float p0 = static_cast<float>(pos0);
+  const size_t nk = static_cast<size_t>(BH) * L * d_k;
+  const size_t ns = static_cast<size_t>(BH) * d_k * d_v;
+  // operand = f · scale · R?(nθ) src (flip: the reversed sequence), rows_out
+  // rows per head, columns in pieces of pw, ncopy copies
+  auto prep = [&](const __nv_bfloat16* src, __nv_bfloat16* dst, int rows_out, int d, int pw,
+                  int ncopy, int flip, int rotate, float scale, int fold) {
+    const int n = rows_out * (d / 8);
+    Mark m("bwd_prep", st);
+    simt::prep_operand_kernel<<<(n + 255) / 256, 256, 0, st>>>(src, dst, cc, BH, H, L, rows_out,
+                                                               d, pw, ncopy, flip, rotate, p0,
+                                                               scale, fold, tcc::CH);
+  };
+  // gradient = scale · R?(−nθ) Σ pieces of X (flip: X holds the reversed sequence)
+  auto grad_out = [&](Tg* y, int d, int np, int flip, int rotate, float scale) {
+    Mark m("bwd_grad_out", st);
+    simt::grad_out_kernel<Tg><<<(L * (d / 8) + 255) / 256, 256, 0, st>>>(
+        X, nk, np, y, cc, BH, L, d, flip, rotate, p0, scale);
+  };
+  simt::HeadScale one, ginv, gam;
+  for (int h = 0; h < kMaxHeads; ++h) {
+    one.s[h] = 1.f;
+    ginv.s[h] = h < H ? static_cast<float>(1.0 / static_cast<double>(cc.gamma[h])) : 1.f;
+    gam.s[h] = h < H ? cc.gamma[h] : 1.f;
+  }
+  const int ncopy = p.as_rows ? p.pieces : 1;
+  ret_status s;
+  // The evaluations that contract over d_v: A, Bo hold the piece-major
+  // operands, sprep the pieces of S_in; piece outputs land nk apart in X.
+  auto pieces = [&](const float* s_pieces) -> ret_status {
+    if (p.as_rows)
+      return run_tc_eval(A, Bo, kBwdPiece, Cc, d_k, s_pieces, nullptr, X, tail, cc,
+                         p.pieces * BH, H, L, st);
+    for (int pc = 0; pc < p.pieces; ++pc) {
+      const int c0 = pc * kBwdPiece;
+      const int w = std::min(kBwdPiece, d_v - c0);
+      const size_t ob = static_cast<size_t>(c0) * Lp * BH;   // piece base in A, Bo
+      const float* sp = s_pieces ? s_pieces + static_cast<size_t>(c0) * d_k * BH : nullptr;
+      ret_status r = run_tc_eval(A + ob, Bo + ob, w, Cc, d_k, sp, nullptr,
+                                 X + static_cast<size_t>(pc) * nk, tail, cc, BH, H, L, st);
+      if (r != RET_OK) return r;
+    }
+    return RET_OK;
+  };
+  // dQ′ = F(dO, V, K′; S_inᵀ), then dq = R(−nθ) dQ′
+  prep(d_o, A, Lp, d_v, kBwdPiece, 1, 0, 0, 1.f, 1);
+  prep(v, Bo, Lp, d_v, kBwdPiece, 1, 0, 0, 1.f, 2);
+  prep(k, Cc, L, d_k, d_k, ncopy, 0, 1, cc.kscale, 0);
+  if (s_in) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1,
+                                                             kBwdPiece, one);
+  }
+  if ((s = pieces(s_in ? sprep : nullptr)) != RET_OK) return s;
+  grad_out(dq, d_k, p.pieces, 0, 1, 1.f);
+  // dK′↓ = F(V↓, dO↓, Q′↓; dS_outᵀ/γ), then dk = d_k^{-1/2} R(−nθ) dK′
+  prep(v, A, Lp, d_v, kBwdPiece, 1, 1, 0, 1.f, 1);
+  prep(d_o, Bo, Lp, d_v, kBwdPiece, 1, 1, 0, 1.f, 2);
+  prep(q, Cc, L, d_k, d_k, ncopy, 1, 1, 1.f, 0);
+  if (dso) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1,
+                                                             kBwdPiece, ginv);
+  }
+  if ((s = pieces(dso ? sprep : nullptr)) != RET_OK) return s;
+  grad_out(dk, d_k, p.pieces, 1, 1, cc.kscale);
+  // dV↓ = F(K′↓, Q′↓, dO↓; dS_out/γ) and dS_in = γ · its S_out (dS_out is
+  // read into sprep before dS_in is written, so the two may alias)
+  prep(k, A, Lp, d_k, d_k, 1, 1, 1, cc.kscale, 1);
+  prep(q, Bo, Lp, d_k, d_k, 1, 1, 1, 1.f, 2);
+  prep(d_o, Cc, L, d_v, d_v, 1, 1, 0, 1.f, 0);
+  if (dso) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, d_k,
+                                                             ginv);
+  }
+  if ((s = run_tc_eval(A, Bo, d_k, Cc, d_v, dso ? sprep : nullptr, dsi, X, tail, cc, BH, H, L,
+                       st)) != RET_OK)
+    return s;
+  grad_out(dv, d_v, 1, 1, 0, 1.f);
+  if (dsi) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, d_k,
+                                                             gam);
   }
   return last_launch();
 }
@@ -926,15 +1159,21 @@ ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_d
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, true);
 }
 
-ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, int B, int H, int L, int d_k, int d_v,
-                                       int chunk, int* path, size_t* workspace_bytes) {
+ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                       int d_k, int d_v, int chunk, int* path,
+                                       size_t* workspace_bytes) {
   if (!path || !workspace_bytes) return RET_EINVAL;
   if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
   if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
       d_v < 1 || d_v > 1024 || chunk < 1)
     return RET_EINVAL;
-  *path = RET_PATH_SIMT;
-  *workspace_bytes = plan_backward(in_dt, B, H, L, d_k, d_v, chunk).bytes;
+  if (tc_backward_ok(in_dt, gamma, H, d_k, d_v, chunk, B)) {
+    *path = RET_PATH_TC;
+    *workspace_bytes = plan_tc_backward(B, H, L, d_k, d_v).bytes;
+  } else {
+    *path = RET_PATH_SIMT;
+    *workspace_bytes = plan_backward(in_dt, B, H, L, d_k, d_v, chunk).bytes;
+  }
   return RET_OK;
 }
 
@@ -956,6 +1195,23 @@ ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, c
   if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
   for (int h = 0; h < H; ++h)   // the reversed evaluations start from dS_out/γ
     if (gamma[h] < 0x1p-64f) return RET_EUNSUPPORTED;
+  if (tc_backward_ok(in_dt, gamma, H, d_k, d_v, chunk, B)) {
+    const TcBwdPlan tp = plan_tc_backward(B, H, L, d_k, d_v);
+    if (!workspace || workspace_bytes < tp.bytes || !al16(workspace)) return RET_EWORKSPACE;
+    const auto* a = static_cast<const __nv_bfloat16*>(q);
+    const auto* b = static_cast<const __nv_bfloat16*>(k);
+    const auto* c = static_cast<const __nv_bfloat16*>(v);
+    const auto* d = static_cast<const __nv_bfloat16*>(d_out);
+    if (grad_dt == RET_F32)
+      return run_tc_backward<float>(a, b, c, d, cc, B, H, L, d_k, d_v, pos0, state_in, d_state_out,
+                                    static_cast<float*>(dq), static_cast<float*>(dk),
+                                    static_cast<float*>(dv), d_state_in, workspace, tp, stream);
+    return run_tc_backward<__nv_bfloat16>(a, b, c, d, cc, B, H, L, d_k, d_v, pos0, state_in,
+                                          d_state_out, static_cast<__nv_bfloat16*>(dq),
+                                          static_cast<__nv_bfloat16*>(dk),
+                                          static_cast<__nv_bfloat16*>(dv), d_state_in, workspace,
+                                          tp, stream);
+  }
   const BwdPlan p = plan_backward(in_dt, B, H, L, d_k, d_v, chunk);
   if (!workspace || workspace_bytes < p.bytes || !al16(workspace)) return RET_EWORKSPACE;
   if (in_dt == RET_F32) {

@@ -185,20 +185,41 @@ def test_path_selection(lib):
 def test_backward_plan_and_validation(lib):
     """ret_chunkwise_backward: workspace layout and synchronous argument checks."""
     path, nb = C.c_int(0), C.c_size_t(0)
-    assert lib.ret_chunkwise_backward_plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128,
-                                           C.byref(path), C.byref(nb)) == _lib.RET_OK
+
+    def plan(in_dt, B, H, L, d_k, d_v, chunk, gamma=None):
+        st = lib.ret_chunkwise_backward_plan(in_dt, _fp(gamma) if gamma is not None else None, B, H, L,
+                                             d_k, d_v, chunk, C.byref(path), C.byref(nb))
+        assert st == _lib.RET_OK
+        return path.value, nb.value
+
     BH, L = 32, 8192
     rk, rv = BH * L * 256 * 4, BH * L * 512 * 4
-    # Q′↓, K′, K′↓ (fp32); dO, V in order (bf16 inputs only) and reversed; one
-    # evaluation output; per-chunk states; one prepared state
-    assert path.value == _lib.RET_PATH_SIMT
-    assert nb.value == 3 * rk + 4 * rv + rv + BH * 64 * 256 * 512 * 4 + BH * 256 * 512 * 4
-    nb32 = C.c_size_t(0)
-    assert lib.ret_chunkwise_backward_plan(_lib.RET_F32, 2, 16, 8192, 256, 512, 128,
-                                           C.byref(path), C.byref(nb32)) == _lib.RET_OK
-    assert nb32.value == nb.value - 2 * rv          # fp32 inputs are read in place
-    assert lib.ret_chunkwise_backward_plan(_lib.RET_F32, 1, 1, 8, 16, 16, 0,
-                                           C.byref(path), C.byref(nb32)) == _lib.RET_EINVAL
+    # tensor cores: ω- and ζ-folded bf16 operands at the wider of d_k, d_v, the
+    # operand the scores multiply, fp32 outputs (two 256-column pieces of d_k
+    # each, or d_v), one prepared state
+    p, n = plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128)
+    assert p == _lib.RET_PATH_TC
+    assert n == 3 * BH * L * 512 * 2 + BH * L * 512 * 4 + BH * 256 * 512 * 4
+    # a ragged length pads the folded operands to whole chunks and adds a staging tile
+    p, n = plan(_lib.RET_BF16, 2, 16, 8000, 256, 512, 128)
+    assert p == _lib.RET_PATH_TC
+    assert n == (2 * BH * 8064 * 512 * 2 + BH * 8000 * 512 * 2 + BH * 8000 * 512 * 4
+                 + BH * 256 * 512 * 4 + BH * 128 * 512 * 4)
+    # fp32 kernels: Q′↓, K′, K′↓ (fp32); dO, V in order (bf16 inputs only) and
+    # reversed; one evaluation output; per-chunk states; one prepared state
+    simt = 3 * rk + 4 * rv + rv + BH * 64 * 256 * 512 * 4 + BH * 256 * 512 * 4
+    assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 64)[0] == _lib.RET_PATH_SIMT      # chunk 64
+    assert plan(_lib.RET_BF16, 2, 16, 8192, 64, 512, 128)[0] == _lib.RET_PATH_SIMT      # d_k 64
+    g = np.array([0.5] + [0.99] * 15, np.float32)                                         # γ^127 underflows
+    assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128, gamma=g) == (_lib.RET_PATH_SIMT, simt)
+    assert lib.ret_force_path(_lib.RET_PATH_SIMT) == _lib.RET_OK
+    try:
+        assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_SIMT, simt)
+    finally:
+        assert lib.ret_force_path(0) == _lib.RET_OK
+    assert plan(_lib.RET_F32, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_SIMT, simt - 2 * rv)
+    assert lib.ret_chunkwise_backward_plan(_lib.RET_F32, None, 1, 1, 8, 16, 16, 0,
+                                           C.byref(path), C.byref(nb)) == _lib.RET_EINVAL
 
     g = np.full(2, 0.9, np.float32)
     t = np.ones(8, np.float32)

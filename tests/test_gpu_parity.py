@@ -45,6 +45,7 @@ def _oracle_full(inp, w, form="chunkwise", chunk=None, pos0=0, gn=None):
 
 
 def _custom(B, H, L, d_k, d_v, dtype, chunk, std=1.0, state_std=0.0, seed=0):
+    assert dtype in ("f32", "bf16"), dtype
     w = Workload("custom", B, H, L, d_k, d_v, dtype, chunk, std, state_std=state_std)
     return w, make_inputs(w, seed)
 
@@ -401,15 +402,22 @@ def _oracle_bwd(inp, gi, pos0):
 
 
 @pytest.mark.parametrize("dtype,gdtype,B,H,L,d_k,d_v,chunk,pos0,state,dso", [
-    (torch.float32, torch.float32, 2, 3, 300, 64, 96, 64, 7, True, True),      # 5 chunks, ragged
-    (torch.float32, torch.float32, 1, 2, 77, 32, 768, 100, 0, True, False),    # one chunk, wide d_v
-    (torch.bfloat16, torch.float32, 2, 2, 256, 128, 128, 128, 100, False, True),
-    (torch.bfloat16, torch.bfloat16, 1, 2, 200, 256, 256, 48, 3, True, True),
+    # fp32 kernels
+    ("f32", torch.float32, 2, 3, 300, 64, 96, 64, 7, True, True),       # 5 chunks, ragged
+    ("f32", torch.float32, 1, 2, 77, 32, 768, 100, 0, True, False),     # one chunk, wide d_v
+    ("f32", torch.bfloat16, 1, 1, 65, 2, 1, 16, 40, False, False),      # smallest widths
+    ("bf16", torch.bfloat16, 1, 2, 200, 256, 256, 48, 3, True, True),   # chunk 48
+    # tensor cores
+    ("bf16", torch.float32, 2, 2, 256, 128, 128, 128, 100, False, True),   # one-CTA kernels
+    ("bf16", torch.float32, 1, 2, 300, 256, 512, 128, 5, True, True),      # two d_v pieces, pairs, ragged
+    ("bf16", torch.bfloat16, 1, 3, 200, 128, 384, 128, 0, True, True),     # pieces of 256 and 128
 ])
 def test_backward_vs_oracle(dtype, gdtype, B, H, L, d_k, d_v, chunk, pos0, state, dso):
     w, inp = _custom(B, H, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0)
     gi = make_grad_inputs(w, seed=5, d_state_std=1.0 if dso else 0.0)
     ref = _oracle_bwd(inp, gi, pos0)
+    path, _ = R.backward_plan(w.torch_dtype, B, H, L, d_k, d_v, chunk, gamma=inp["gamma"])
+    assert path == (R.RET_PATH_TC if dtype == "bf16" and chunk == 128 else R.RET_PATH_SIMT)
     d = _cuda(inp)
     dso_c = gi["d_state_out"].cuda() if dso else None
     got = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
@@ -417,36 +425,61 @@ def test_backward_vs_oracle(dtype, gdtype, B, H, L, d_k, d_v, chunk, pos0, state
                                grad_dtype=gdtype)
     assert R.sync_status() == R.RET_OK
     for g, r, name in zip(got, ref, ("dq", "dk", "dv", "dS_in")):
-        assert_close(gpu_np(g), r, torch.float32 if name == "dS_in" else gdtype, name)
+        # fp32 kernels: fp32 tolerance unless the gradients are stored in bf16;
+        # tensor cores: bf16 operands, the bf16 tolerance
+        tol = torch.bfloat16 if (path == R.RET_PATH_TC or (gdtype == torch.bfloat16 and name != "dS_in")) \
+            else torch.float32
+        assert_close(gpu_np(g), r, tol, name)
 
 
-def test_backward_zero_upstream_and_state_aliasing():
-    w, inp = _custom(1, 2, 130, 64, 64, torch.float32, 32, state_std=0.1)
-    d = _cuda(inp)
+@pytest.mark.parametrize("dtype,d,chunk", [("f32", 64, 32), ("bf16", 128, 128)])
+def test_backward_zero_upstream_and_state_aliasing(dtype, d, chunk):
+    w, inp = _custom(1, 2, 130, d, d, dtype, chunk, state_std=0.1)
+    d_ = _cuda(inp)
     # zero upstream gradients give exactly zero gradients
-    z = torch.zeros((1, 2, 130, 64), device="cuda")
-    zs = torch.zeros((1, 2, 64, 64), device="cuda")
-    got = R.chunkwise_backward(d["q"], d["k"], d["v"], z, inp["gamma"], inp["theta"], chunk=32,
-                               state_in=d["state_in"], d_state_out=zs)
+    z = torch.zeros((1, 2, 130, d), device="cuda", dtype=w.torch_dtype)
+    zs = torch.zeros((1, 2, d, d), device="cuda")
+    got = R.chunkwise_backward(d_["q"], d_["k"], d_["v"], z, inp["gamma"], inp["theta"], chunk=chunk,
+                               state_in=d_["state_in"], d_state_out=zs)
     assert all(int(torch.count_nonzero(t)) == 0 for t in got)
     # d_state_in written over d_state_out: the same values as into a separate buffer
     gi = make_grad_inputs(w, seed=2, d_state_std=1.0)
     dso = gi["d_state_out"].cuda()
-    a = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
-                             chunk=32, pos0=9, state_in=d["state_in"], d_state_out=dso)
+    a = R.chunkwise_backward(d_["q"], d_["k"], d_["v"], gi["d_out"].cuda(), inp["gamma"],
+                             inp["theta"], chunk=chunk, pos0=9, state_in=d_["state_in"], d_state_out=dso)
     buf = dso.clone()
-    b = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
-                             chunk=32, pos0=9, state_in=d["state_in"], d_state_out=buf, d_state_in=buf)
+    b = R.chunkwise_backward(d_["q"], d_["k"], d_["v"], gi["d_out"].cuda(), inp["gamma"],
+                             inp["theta"], chunk=chunk, pos0=9, state_in=d_["state_in"], d_state_out=buf,
+                             d_state_in=buf)
     assert R.sync_status() == R.RET_OK
     for x, y in zip(a, b):
         assert torch.equal(x, y)
 
 
+def test_backward_tc_matches_fp32_kernels():
+    """The tensor-core gradient pass against the fp32 kernels on the same bf16 inputs."""
+    w, inp = _custom(2, 2, 384, 256, 256, "bf16", 128, state_std=0.1, seed=21)
+    gi = make_grad_inputs(w, seed=22, d_state_std=1.0)
+    d = _cuda(inp)
+    args = (d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"])
+    kw = dict(chunk=128, pos0=17, state_in=d["state_in"], d_state_out=gi["d_state_out"].cuda(),
+              grad_dtype=torch.float32)
+    tc = R.chunkwise_backward(*args, **kw)
+    R.force_path(R.RET_PATH_SIMT)
+    try:
+        ref = R.chunkwise_backward(*args, **kw)
+    finally:
+        R.force_path(0)
+    assert R.sync_status() == R.RET_OK
+    for x, y, name in zip(tc, ref, ("dq", "dk", "dv", "dS_in")):
+        assert_close(gpu_np(x), gpu_np(y), torch.bfloat16, name)
+
+
 def test_backward_msr7b_sampled_heads():
-    """The 7B shape (bf16 inputs, fp32 gradients): one head against the
-    oracle over the whole sequence; another on the prefix that fixes dq
-    (positions ≤ t and S_in) and the suffix that fixes dk, dv (positions ≥ m
-    and dS_out)."""
+    """The 7B shape (bf16 inputs, fp32 gradients, tensor-core path): one head
+    against the oracle over the whole sequence; another on the prefix that
+    fixes dq (positions ≤ t and S_in) and the suffix that fixes dk, dv
+    (positions ≥ m and dS_out)."""
     w = WORKLOADS["msr7b"]
     inp = make_inputs(w, seed=0)
     gi = make_grad_inputs(w, seed=5, d_state_std=1.0)
@@ -462,18 +495,18 @@ def test_backward_msr7b_sampled_heads():
     dSo = to_f64(gi["d_state_out"][b:b + 1, h:h + 1])
     ref = O.retention_backward(q, k, v, g, th, 0, si, dO, dSo)
     for got, r, name in zip((dq, dk, dv, dsi), ref, ("dq", "dk", "dv", "dS_in")):
-        assert_close(gpu_np(got[b:b + 1, h:h + 1]), r, torch.float32, f"7B {name} (b={b},h={h})")
+        assert_close(gpu_np(got[b:b + 1, h:h + 1]), r, torch.bfloat16, f"7B {name} (b={b},h={h})")
     b, h, n = 0, 0, 384
     q, k, v, si, g, th = head_slice(inp, b, h)
     dO = to_f64(gi["d_out"][b:b + 1, h:h + 1])
     dSo = to_f64(gi["d_state_out"][b:b + 1, h:h + 1])
     rq = O.retention_backward(q[:, :, :n], k[:, :, :n], v[:, :, :n], g, th, 0, si, dO[:, :, :n])[0]
-    assert_close(gpu_np(dq[b:b + 1, h:h + 1, :n]), rq, torch.float32, "7B dq prefix")
+    assert_close(gpu_np(dq[b:b + 1, h:h + 1, :n]), rq, torch.bfloat16, "7B dq prefix")
     m0 = w.L - n
     _, rk, rv, _ = O.retention_backward(q[:, :, m0:], k[:, :, m0:], v[:, :, m0:], g, th, m0, None,
                                         dO[:, :, m0:], dSo)
-    assert_close(gpu_np(dk[b:b + 1, h:h + 1, m0:]), rk, torch.float32, "7B dk suffix")
-    assert_close(gpu_np(dv[b:b + 1, h:h + 1, m0:]), rv, torch.float32, "7B dv suffix")
+    assert_close(gpu_np(dk[b:b + 1, h:h + 1, m0:]), rk, torch.bfloat16, "7B dk suffix")
+    assert_close(gpu_np(dv[b:b + 1, h:h + 1, m0:]), rv, torch.bfloat16, "7B dv suffix")
 
 
 def test_decode_1024_steps_vs_chunkwise_and_oracle():
