@@ -444,76 +444,113 @@ __global__ void __launch_bounds__(256) flip_cvt_kernel(const Tin* __restrict__ x
 // prows rows (the last may be shorter); piece p of all BH states comes
 // before piece p+1: dst = [piece][BH][rows of the piece][columns of M].
 // prows ≥ M's rows gives the plain [BH][M rows][M cols] layout.  src == dst
-// only without transpose and pieces.
-__global__ void __launch_bounds__(256) state_prep_kernel(const float* __restrict__ src,
-                                                         float* dst, int BH, int H, int rows,
-                                                         int cols, int transpose, int prows,
+// only without transpose and pieces (every element is read and written by
+// the same thread).  Block (32, 8) per 32×32 tile, grid (⌈cols/32⌉,
+// ⌈rows/32⌉, BH); the tile goes through shared memory so that both the
+// reads and the (transposed) writes are coalesced.
+__global__ void __launch_bounds__(256) state_prep_kernel(const float* src, float* dst, int BH,
+                                                         int H, int rows, int cols,
+                                                         int transpose, int prows,
                                                          HeadScale hs) {
-  const size_t per = static_cast<size_t>(rows) * cols;
-  const size_t n = per * BH;
+  __shared__ float tile[32][33];
+  const int bh = blockIdx.z;
+  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  const float sc = hs.s[bh % H];
+  const size_t sb = static_cast<size_t>(bh) * rows * cols;
   const int mrows = transpose ? cols : rows, mcols = transpose ? rows : cols;
-  for (size_t e = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
-       e += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t bh = e / per;
-    const int rc = static_cast<int>(e - bh * per);
-    const int r = rc / cols, c = rc - r * cols;
-    const int mr = transpose ? c : r, mc = transpose ? r : c;
+  auto dst_index = [&](int mr, int mc) {
     const int piece = mr / prows, rl = mr - piece * prows;
     const int ph = min(prows, mrows - piece * prows);
-    const size_t di = static_cast<size_t>(piece) * prows * mcols * BH +
-                      (bh * ph + rl) * static_cast<size_t>(mcols) + mc;
-    dst[di] = src[e] * hs.s[bh % H];
+    return static_cast<size_t>(piece) * prows * mcols * BH +
+           (static_cast<size_t>(bh) * ph + rl) * mcols + mc;
+  };
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty + 8 * i, c = c0 + tx;
+    if (r < rows && c < cols) tile[ty + 8 * i][tx] = src[sb + static_cast<size_t>(r) * cols + c] * sc;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (transpose) {   // M row = source column c0 + ty + 8i, M column = source row r0 + tx
+      const int mr = c0 + ty + 8 * i, mc = r0 + tx;
+      if (mr < cols && mc < rows) dst[dst_index(mr, mc)] = tile[tx][ty + 8 * i];
+    } else {
+      const int mr = r0 + ty + 8 * i, mc = c0 + tx;
+      if (mr < rows && mc < cols) dst[dst_index(mr, mc)] = tile[ty + 8 * i][tx];
+    }
   }
 }
 
-// Operands of the tensor-core evaluations in the gradient pass, bf16:
+// Operands of the tensor-core evaluations in the gradient pass, bf16, all
+// derived from one source tensor src [BH][L][d] in one pass:
 //   op[bh][t][:] = f(t) · scale · R?((pos0 + t_s)θ) src[bh][t_s][:]   (t < L)
 //   op[bh][t][:] = 0                                                  (L ≤ t < rows_out)
-// with t_s = L−1−t when flip, else t; the rotation only when rotate.  f(t) is
+// with t_s = L−1−t when the operand is reversed (flip), else t; the rotation
+// (the prologue's, at the source row's position) only when rotate.  f(t) is
 // 1 (fold 0), ω = γ^{(t mod b)+1−b_c} (fold 1) or ζ = γ^{b_c−1−(t mod b)}
 // (fold 2), b_c the length of t's chunk of b rows (the last may be shorter):
 // the per-row factors of the chunk kernels' rewritten form, taken over the
-// sequence as it is read (reversed when flip).  The columns are stored in
-// pieces of pw (the last may be narrower), piece-major:
-// dst[piece][bh][t][columns of the piece]; ncopy copies of the whole
-// operand follow each other.  d and pw multiples of 8.
-// Thread ↔ (row t, 8 columns): the angles and the fold exponent are computed
-// once and used for all B·H heads, eight heads' loads in flight.
+// sequence as it is read.  Each operand's columns are stored in pieces of
+// pw (the last may be narrower), piece-major: [piece][bh][t][columns of the
+// piece]; ncopy copies of the whole operand follow each other.  d and pw
+// multiples of 8.
+struct OpSpec {
+  __nv_bfloat16* dst;
+  int rows_out, pw, ncopy, flip, fold;
+  float scale;
+};
+template <int NS>
+struct OpSpecs {
+  OpSpec o[NS];
+};
+
+// Thread ↔ (source row t_s, 8 columns); threads with t_s ≥ L zero the
+// padding rows.  The angles are computed once per thread and used for all
+// B·H heads, whose loads are issued eight at a time.  NS operands.
+template <int NS>
 __global__ void __launch_bounds__(256) prep_operand_kernel(
-    const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, CallConsts cc,
-    int BH, int H, int L, int rows_out, int d, int pw, int ncopy, int flip, int rotate,
-    float pos0, float scale, int fold, int chunk) {
+    const __nv_bfloat16* __restrict__ src, OpSpecs<NS> sp, CallConsts cc, int BH, int H, int L,
+    int rows_max, int d, int rotate, float pos0, int chunk) {
   constexpr int U = 8;
   const int vecs = d / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= rows_out * vecs) return;
-  const int t = idx / vecs, cv = idx - t * vecs;
-  const int piece = (8 * cv) / pw;
-  const int wp = min(pw, d - piece * pw);   // width of this piece
-  const size_t pbase = static_cast<size_t>(piece) * pw * rows_out * BH;
-  const size_t copy = static_cast<size_t>(rows_out) * d * BH;
-  const size_t ocol = 8 * cv - piece * pw;
-  auto optr = [&](int bh, int cp) {
-    return reinterpret_cast<uint4*>(dst + cp * copy + pbase +
-                                    (static_cast<size_t>(bh) * rows_out + t) * wp + ocol);
+  if (idx >= rows_max * vecs) return;
+  const int ts = idx / vecs, cv = idx - ts * vecs;
+  const int nch = (L + chunk - 1) / chunk;
+  auto optr = [&](const OpSpec& o, int bh, int t, int cp) {
+    const int piece = (8 * cv) / o.pw;
+    const int wp = min(o.pw, d - piece * o.pw);
+    const size_t at = static_cast<size_t>(cp) * o.rows_out * d * BH +
+                      static_cast<size_t>(piece) * o.pw * o.rows_out * BH +
+                      (static_cast<size_t>(bh) * o.rows_out + t) * wp + (8 * cv - piece * o.pw);
+    return reinterpret_cast<uint4*>(o.dst + at);
   };
-  if (t >= L) {
-    for (int bh = 0; bh < BH; ++bh)
-      for (int cp = 0; cp < ncopy; ++cp) *optr(bh, cp) = make_uint4(0u, 0u, 0u, 0u);
+  if (ts >= L) {   // padding rows of the operands that have them
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+      const OpSpec& o = sp.o[i];
+      if (ts >= o.rows_out) continue;
+      for (int bh = 0; bh < BH; ++bh)
+        for (int cp = 0; cp < o.ncopy; ++cp) *optr(o, bh, ts, cp) = make_uint4(0u, 0u, 0u, 0u);
+    }
     return;
   }
-  const int ts = flip ? L - 1 - t : t;
   float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
   if (rotate) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(ts), cc.theta[4 * cv + u], c[u], sn[u]);
   }
-  float ex = 0.f;
-  if (fold) {
-    const int nch = (L + chunk - 1) / chunk;
+  int trow[NS];
+  float ex[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    const int t = sp.o[i].flip ? L - 1 - ts : ts;
     const int bc = (t / chunk == nch - 1) ? L - (nch - 1) * chunk : chunk;
     const int j = t % chunk;
-    ex = fold == 1 ? static_cast<float>(j + 1 - bc) : static_cast<float>(bc - 1 - j);
+    trow[i] = t;
+    ex[i] = sp.o[i].fold == 1 ? static_cast<float>(j + 1 - bc) : static_cast<float>(bc - 1 - j);
   }
   const size_t hstride = static_cast<size_t>(L) * d;
   const __nv_bfloat16* s0 = src + static_cast<size_t>(ts) * d + 8 * cv;
@@ -526,16 +563,23 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
     for (int uu = 0; uu < U; ++uu) {
       const int bh = bh0 + uu;
       if (bh >= BH) break;
-      const float f = fold ? scale * gpow(cc.lg2g[bh % H], ex) : scale;
       const uint32_t w[4] = {raw[uu].x, raw[uu].y, raw[uu].z, raw[uu].w};
-      uint32_t o[4];
+      float r[8];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const float a = bf16lo_to_f32(w[u]), b = bf16hi_to_f32(w[u]);
-        o[u] = pack_bf16x2(f * (a * c[u] - b * sn[u]), f * fmaf(a, sn[u], b * c[u]));
+        r[2 * u] = a * c[u] - b * sn[u];
+        r[2 * u + 1] = fmaf(a, sn[u], b * c[u]);
       }
-      const uint4 ov = make_uint4(o[0], o[1], o[2], o[3]);
-      for (int cp = 0; cp < ncopy; ++cp) *optr(bh, cp) = ov;
+      const float lg = cc.lg2g[bh % H];
+#pragma unroll
+      for (int i = 0; i < NS; ++i) {
+        const OpSpec& o = sp.o[i];
+        const float f = o.fold ? o.scale * gpow(lg, ex[i]) : o.scale;
+        const uint4 ov = make_uint4(pack_bf16x2(f * r[0], f * r[1]), pack_bf16x2(f * r[2], f * r[3]),
+                                    pack_bf16x2(f * r[4], f * r[5]), pack_bf16x2(f * r[6], f * r[7]));
+        for (int cp = 0; cp < o.ncopy; ++cp) *optr(o, bh, trow[i], cp) = ov;
+      }
     }
   }
 }

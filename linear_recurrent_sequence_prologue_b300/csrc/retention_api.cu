@@ -625,7 +625,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   const float p0 = static_cast<float>(pos0);
   const dim3 rg((d_k / 2 + 31) / 32, (L + 7) / 8);
   const size_t nk = static_cast<size_t>(BH) * L * d_k, nv = static_cast<size_t>(BH) * L * d_v;
-  const size_t ns = static_cast<size_t>(BH) * d_k * d_v;
+  const dim3 sgrid((d_v + 31) / 32, (d_k + 31) / 32, BH);   // state_prep_kernel tiles
   {
     Mark m("bwd_rotate", st);
     simt::rotate_kernel<Tin, float><<<rg, dim3(32, 8), 0, st>>>(q, qpf, cc, BH, H, L, d_k, p0,
@@ -680,7 +680,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   const float* x = nullptr;
   if (s_in) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1, d_v, one);
+    simt::state_prep_kernel<<<sgrid, dim3(32, 8), 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1, d_v, one);
     x = sprep;
   }
   if ((s = run_simt_core(do32, v32, kp, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
@@ -695,7 +695,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   x = nullptr;
   if (dso) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1, d_v, ginv);
+    simt::state_prep_kernel<<<sgrid, dim3(32, 8), 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1, d_v, ginv);
     x = sprep;
   }
   if ((s = run_simt_core(vf, dof, qpf, cc, BH, H, L, d_v, d_k, chunk, x, nullptr, fout, states,
@@ -711,7 +711,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   x = nullptr;
   if (dso) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, d_k, ginv);
+    simt::state_prep_kernel<<<sgrid, dim3(32, 8), 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, d_k, ginv);
     x = sprep;
   }
   if ((s = run_simt_core(kpf, qpf, dof, cc, BH, H, L, d_k, d_v, chunk, x, dsi, fout, states,
@@ -723,7 +723,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   }
   if (dsi) {
     Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, d_k, gam);
+    simt::state_prep_kernel<<<sgrid, dim3(32, 8), 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, d_k, gam);
   }
   return last_launch();
 }
@@ -754,7 +754,10 @@ bool tc_backward_ok(ret_dtype in_dt, const float* gamma, int H, int d_k, int d_v
 }
 
 struct TcBwdPlan {
-  size_t off_a = 0, off_b = 0, off_c = 0, off_x = 0, off_sprep = 0, off_tail = 0, bytes = 0;
+  // operands of the three evaluations: dQ′ (1), dK′↓ (3), dV↓ (2)
+  size_t off_a1 = 0, off_b1 = 0, off_c1 = 0, off_a3 = 0, off_b3 = 0, off_c3 = 0;
+  size_t off_a2 = 0, off_b2 = 0, off_c2 = 0;
+  size_t off_x = 0, off_sprep = 0, off_tail = 0, bytes = 0;
   int pieces = 0;
   bool as_rows = false;   // all pieces in one launch
 };
@@ -763,16 +766,22 @@ TcBwdPlan plan_tc_backward(int B, int H, int L, int d_k, int d_v) {
   TcBwdPlan p;
   const size_t BH = static_cast<size_t>(B) * H;
   const size_t Lp = static_cast<size_t>((L + tcc::CH - 1) / tcc::CH) * tcc::CH;
-  const size_t W = d_k > d_v ? d_k : d_v;
   p.pieces = bwd_pieces(d_v);
   p.as_rows = d_v % kBwdPiece == 0;
-  const size_t pk = static_cast<size_t>(p.pieces) * d_k;
-  const size_t xw = std::max(pk, static_cast<size_t>(d_v));
-  const size_t cw = std::max(p.as_rows ? pk : static_cast<size_t>(d_k), static_cast<size_t>(d_v));
+  const size_t ncopy = p.as_rows ? p.pieces : 1;
+  const size_t xw = std::max(static_cast<size_t>(p.pieces) * d_k, static_cast<size_t>(d_v));
+  const size_t av = up256(BH * Lp * d_v * 2), ak = up256(BH * Lp * d_k * 2);
+  const size_t ck = up256(ncopy * BH * L * d_k * 2), cv = up256(BH * L * static_cast<size_t>(d_v) * 2);
   size_t off = 0;
-  p.off_a = off; off += up256(BH * Lp * W * 2);       // ω-folded left operand
-  p.off_b = off; off += up256(BH * Lp * W * 2);       // ζ-folded right operand
-  p.off_c = off; off += up256(BH * L * cw * 2);       // the operand the scores multiply
+  p.off_a1 = off; off += av;   // ω·dO, 256-column pieces
+  p.off_b1 = off; off += av;   // ζ·V
+  p.off_c1 = off; off += ck;   // K′, once per piece
+  p.off_a3 = off; off += av;   // ω·V↓
+  p.off_b3 = off; off += av;   // ζ·dO↓
+  p.off_c3 = off; off += ck;   // Q′↓, once per piece
+  p.off_a2 = off; off += ak;   // ω·K′↓
+  p.off_b2 = off; off += ak;   // ζ·Q′↓
+  p.off_c2 = off; off += cv;   // dO↓
   p.off_x = off; off += up256(BH * L * xw * 4);       // fp32 outputs (one per piece)
   p.off_sprep = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4);
   if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * xw * 4); }
@@ -866,30 +875,43 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   const int BH = B * H;
   const int nch = (L + tcc::CH - 1) / tcc::CH;
   const int Lp = nch * tcc::CH;
-  auto* A = wsp<__nv_bfloat16>(ws, p.off_a);
-  auto* Bo = wsp<__nv_bfloat16>(ws, p.off_b);
-  auto* Cc = wsp<__nv_bfloat16>(ws, p.off_c);
+  auto op = [&](size_t off) { return wsp<__nv_bfloat16>(ws, off); };
   float* X = wsp<float>(ws, p.off_x);
   float* sprep = wsp<float>(ws, p.off_sprep);
   void* tail = p.off_tail ? wsp<void>(ws, p.off_tail) : nullptr;
   const float p0 = static_cast<float>(pos0);
   const size_t nk = static_cast<size_t>(BH) * L * d_k;
-  const size_t ns = static_cast<size_t>(BH) * d_k * d_v;
-  // operand = f · scale · R?(nθ) src (flip: the reversed sequence), rows_out
-  // rows per head, columns in pieces of pw, ncopy copies
-  auto prep = [&](const __nv_bfloat16* src, __nv_bfloat16* dst, int rows_out, int d, int pw,
-                  int ncopy, int flip, int rotate, float scale, int fold) {
-    const int n = rows_out * (d / 8);
+  const int ncopy = p.as_rows ? p.pieces : 1;
+  // All operands, one pass per source tensor.
+  auto prep = [&](const __nv_bfloat16* src, int d, int rotate, const auto& sp) {
+    const int n = Lp * (d / 8);
     Mark m("bwd_prep", st);
-    simt::prep_operand_kernel<<<(n + 255) / 256, 256, 0, st>>>(src, dst, cc, BH, H, L, rows_out,
-                                                               d, pw, ncopy, flip, rotate, p0,
-                                                               scale, fold, tcc::CH);
+    constexpr int NS = sizeof(sp.o) / sizeof(sp.o[0]);
+    simt::prep_operand_kernel<NS><<<(n + 255) / 256, 256, 0, st>>>(src, sp, cc, BH, H, L, Lp, d,
+                                                                   rotate, p0, tcc::CH);
   };
+  //                                   dst         rows pw         copies flip fold scale
+  prep(d_o, d_v, 0, simt::OpSpecs<3>{{{op(p.off_a1), Lp, kBwdPiece, 1, 0, 1, 1.f},
+                                      {op(p.off_b3), Lp, kBwdPiece, 1, 1, 2, 1.f},
+                                      {op(p.off_c2), L, d_v, 1, 1, 0, 1.f}}});
+  prep(v, d_v, 0, simt::OpSpecs<2>{{{op(p.off_b1), Lp, kBwdPiece, 1, 0, 2, 1.f},
+                                    {op(p.off_a3), Lp, kBwdPiece, 1, 1, 1, 1.f}}});
+  prep(k, d_k, 1, simt::OpSpecs<2>{{{op(p.off_c1), L, d_k, ncopy, 0, 0, cc.kscale},
+                                    {op(p.off_a2), Lp, d_k, 1, 1, 1, cc.kscale}}});
+  prep(q, d_k, 1, simt::OpSpecs<2>{{{op(p.off_c3), L, d_k, ncopy, 1, 0, 1.f},
+                                    {op(p.off_b2), Lp, d_k, 1, 1, 2, 1.f}}});
   // gradient = scale · R?(−nθ) Σ pieces of X (flip: X holds the reversed sequence)
   auto grad_out = [&](Tg* y, int d, int np, int flip, int rotate, float scale) {
     Mark m("bwd_grad_out", st);
     simt::grad_out_kernel<Tg><<<(L * (d / 8) + 255) / 256, 256, 0, st>>>(
         X, nk, np, y, cc, BH, L, d, flip, rotate, p0, scale);
+  };
+  // dst = scale_h · (S or Sᵀ), cut into pieces of prows rows
+  auto state_prep = [&](const float* src, float* dst, int transpose, int prows,
+                        const simt::HeadScale& hs) {
+    Mark m("bwd_state_prep", st);
+    simt::state_prep_kernel<<<dim3((d_v + 31) / 32, (d_k + 31) / 32, BH), dim3(32, 8), 0, st>>>(
+        src, dst, BH, H, d_k, d_v, transpose, prows, hs);
   };
   simt::HeadScale one, ginv, gam;
   for (int h = 0; h < kMaxHeads; ++h) {
@@ -897,66 +919,44 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
     ginv.s[h] = h < H ? static_cast<float>(1.0 / static_cast<double>(cc.gamma[h])) : 1.f;
     gam.s[h] = h < H ? cc.gamma[h] : 1.f;
   }
-  const int ncopy = p.as_rows ? p.pieces : 1;
   ret_status s;
-  // The evaluations that contract over d_v: A, Bo hold the piece-major
-  // operands, sprep the pieces of S_in; piece outputs land nk apart in X.
-  auto pieces = [&](const float* s_pieces) -> ret_status {
+  // The evaluations that contract over d_v: a, b piece-major, c the operand
+  // the scores multiply, s_pieces the pieces of S_in; piece outputs land nk
+  // apart in X.
+  auto pieces = [&](const __nv_bfloat16* a, const __nv_bfloat16* b, const __nv_bfloat16* c,
+                    const float* s_pieces) -> ret_status {
     if (p.as_rows)
-      return run_tc_eval(A, Bo, kBwdPiece, Cc, d_k, s_pieces, nullptr, X, tail, cc,
-                         p.pieces * BH, H, L, st);
+      return run_tc_eval(a, b, kBwdPiece, c, d_k, s_pieces, nullptr, X, tail, cc, p.pieces * BH,
+                         H, L, st);
     for (int pc = 0; pc < p.pieces; ++pc) {
       const int c0 = pc * kBwdPiece;
       const int w = std::min(kBwdPiece, d_v - c0);
-      const size_t ob = static_cast<size_t>(c0) * Lp * BH;   // piece base in A, Bo
+      const size_t ob = static_cast<size_t>(c0) * Lp * BH;   // piece base in a, b
       const float* sp = s_pieces ? s_pieces + static_cast<size_t>(c0) * d_k * BH : nullptr;
-      ret_status r = run_tc_eval(A + ob, Bo + ob, w, Cc, d_k, sp, nullptr,
+      ret_status r = run_tc_eval(a + ob, b + ob, w, c, d_k, sp, nullptr,
                                  X + static_cast<size_t>(pc) * nk, tail, cc, BH, H, L, st);
       if (r != RET_OK) return r;
     }
     return RET_OK;
   };
   // dQ′ = F(dO, V, K′; S_inᵀ), then dq = R(−nθ) dQ′
-  prep(d_o, A, Lp, d_v, kBwdPiece, 1, 0, 0, 1.f, 1);
-  prep(v, Bo, Lp, d_v, kBwdPiece, 1, 0, 0, 1.f, 2);
-  prep(k, Cc, L, d_k, d_k, ncopy, 0, 1, cc.kscale, 0);
-  if (s_in) {
-    Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(s_in, sprep, BH, H, d_k, d_v, 1,
-                                                             kBwdPiece, one);
-  }
-  if ((s = pieces(s_in ? sprep : nullptr)) != RET_OK) return s;
+  if (s_in) state_prep(s_in, sprep, 1, kBwdPiece, one);
+  if ((s = pieces(op(p.off_a1), op(p.off_b1), op(p.off_c1), s_in ? sprep : nullptr)) != RET_OK)
+    return s;
   grad_out(dq, d_k, p.pieces, 0, 1, 1.f);
   // dK′↓ = F(V↓, dO↓, Q′↓; dS_outᵀ/γ), then dk = d_k^{-1/2} R(−nθ) dK′
-  prep(v, A, Lp, d_v, kBwdPiece, 1, 1, 0, 1.f, 1);
-  prep(d_o, Bo, Lp, d_v, kBwdPiece, 1, 1, 0, 1.f, 2);
-  prep(q, Cc, L, d_k, d_k, ncopy, 1, 1, 1.f, 0);
-  if (dso) {
-    Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 1,
-                                                             kBwdPiece, ginv);
-  }
-  if ((s = pieces(dso ? sprep : nullptr)) != RET_OK) return s;
+  if (dso) state_prep(dso, sprep, 1, kBwdPiece, ginv);
+  if ((s = pieces(op(p.off_a3), op(p.off_b3), op(p.off_c3), dso ? sprep : nullptr)) != RET_OK)
+    return s;
   grad_out(dk, d_k, p.pieces, 1, 1, cc.kscale);
   // dV↓ = F(K′↓, Q′↓, dO↓; dS_out/γ) and dS_in = γ · its S_out (dS_out is
   // read into sprep before dS_in is written, so the two may alias)
-  prep(k, A, Lp, d_k, d_k, 1, 1, 1, cc.kscale, 1);
-  prep(q, Bo, Lp, d_k, d_k, 1, 1, 1, 1.f, 2);
-  prep(d_o, Cc, L, d_v, d_v, 1, 1, 0, 1.f, 0);
-  if (dso) {
-    Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dso, sprep, BH, H, d_k, d_v, 0, d_k,
-                                                             ginv);
-  }
-  if ((s = run_tc_eval(A, Bo, d_k, Cc, d_v, dso ? sprep : nullptr, dsi, X, tail, cc, BH, H, L,
-                       st)) != RET_OK)
+  if (dso) state_prep(dso, sprep, 0, d_k, ginv);
+  if ((s = run_tc_eval(op(p.off_a2), op(p.off_b2), d_k, op(p.off_c2), d_v, dso ? sprep : nullptr,
+                       dsi, X, tail, cc, BH, H, L, st)) != RET_OK)
     return s;
   grad_out(dv, d_v, 1, 1, 0, 1.f);
-  if (dsi) {
-    Mark m("bwd_state_prep", st);
-    simt::state_prep_kernel<<<stride_grid(ns), 256, 0, st>>>(dsi, dsi, BH, H, d_k, d_v, 0, d_k,
-                                                             gam);
-  }
+  if (dsi) state_prep(dsi, dsi, 0, d_k, gam);
   return last_launch();
 }
 

@@ -194,17 +194,18 @@ def test_backward_plan_and_validation(lib):
 
     BH, L = 32, 8192
     rk, rv = BH * L * 256 * 4, BH * L * 512 * 4
-    # tensor cores: ω- and ζ-folded bf16 operands at the wider of d_k, d_v, the
-    # operand the scores multiply, fp32 outputs (two 256-column pieces of d_k
-    # each, or d_v), one prepared state
-    p, n = plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128)
-    assert p == _lib.RET_PATH_TC
-    assert n == 3 * BH * L * 512 * 2 + BH * L * 512 * 4 + BH * 256 * 512 * 4
+    # tensor cores, the operands of the three evaluations in bf16: four ω/ζ-folded
+    # d_v-wide ones and two d_k-wide ones padded to whole chunks, K′ and Q′↓ once
+    # per 256-column piece of d_v (two), dO↓; then fp32 outputs (two pieces of d_k,
+    # or d_v) and one prepared state
+    def tc_bytes(Lx, Lpx, tail):
+        return (4 * BH * Lpx * 512 * 2 + 2 * 2 * BH * Lx * 256 * 2 + 2 * BH * Lpx * 256 * 2
+                + BH * Lx * 512 * 2 + BH * Lx * 512 * 4 + BH * 256 * 512 * 4
+                + (BH * 128 * 512 * 4 if tail else 0))
+
+    assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_TC, tc_bytes(8192, 8192, False))
     # a ragged length pads the folded operands to whole chunks and adds a staging tile
-    p, n = plan(_lib.RET_BF16, 2, 16, 8000, 256, 512, 128)
-    assert p == _lib.RET_PATH_TC
-    assert n == (2 * BH * 8064 * 512 * 2 + BH * 8000 * 512 * 2 + BH * 8000 * 512 * 4
-                 + BH * 256 * 512 * 4 + BH * 128 * 512 * 4)
+    assert plan(_lib.RET_BF16, 2, 16, 8000, 256, 512, 128) == (_lib.RET_PATH_TC, tc_bytes(8000, 8064, True))
     # fp32 kernels: Q′↓, K′, K′↓ (fp32); dO, V in order (bf16 inputs only) and
     # reversed; one evaluation output; per-chunk states; one prepared state
     simt = 3 * rk + 4 * rv + rv + BH * 64 * 256 * 512 * 4 + BH * 256 * 512 * 4
