@@ -43,6 +43,13 @@ R6  Masked entries (n < m) are exact zeros.
 R7  GroupNorm: one group per head over the d_v channels of one token,
     biased variance, eps given by the caller (1e-5 default), optional affine.
 R8  A ragged last chunk of length r uses carry γ^r and ζ_j = γ^{r-1-j}.
+R9  The row-normalised decay of [P1] §5 ("三重标准化": the √d division, the
+    decay weights normalised per row, a global scaling): row N of D is
+    divided by its sum over the absolute positions 0..N it covers,
+    r_N = Σ_{i=0}^{N} γ^i, the state term standing for the positions before
+    pos0 (so split calls agree); the global scaling has no stated value and is
+    1.  With GroupNorm after it, the whole normalisation cancels up to eps
+    (the scale invariance of [P5]).
 
 Conventions: q, k are [B, H, L, d_k]; v is [B, H, L, d_v]; gamma is [H];
 theta is [d_k/2]; states are [B, H, d_k, d_v]; absolute position of local
@@ -66,6 +73,9 @@ __all__ = [
     "chunkwise_core",
     "state_closed_form",
     "retention",
+    "retention_backward",
+    "decay_row_sums",
+    "normalised_retention",
     "decode_step",
     "group_norm",
     "brute_force",
@@ -259,6 +269,40 @@ def retention(q, k, v, gamma, theta, pos0=0, state_in=None, form="chunkwise",
     if gn is not None:
         out = group_norm(out, gn.get("eps", 1e-5), gn.get("weight"), gn.get("bias"))
     return out, S
+
+
+def decay_row_sums(gamma, pos0, L):
+    """r[h, t] = Σ_{i=0}^{N} γ_h^i with N = pos0 + t: the sum of row N of the
+    decay mask over every position it covers (R9), summed term by term."""
+    g = _f64(gamma).reshape(-1)
+    n_max = int(pos0) + int(L)
+    r = np.empty((g.shape[0], int(L)))
+    for h in range(g.shape[0]):
+        terms = np.power(g[h], np.arange(n_max, dtype=np.float64))   # γ^0 … γ^{N_max}
+        r[h] = np.cumsum(terms)[int(pos0):]
+    return r
+
+
+def normalised_retention(q, k, v, gamma, theta, pos0=0, state_in=None, gn=None):
+    """Retention with the row-normalised decay D̃ of [P1] §5 (R9), parallel
+    form: out = (Q′K′ᵀ ⊙ D̃)V + (ξ/r) ⊙ (Q′ S_in) with D̃_tm = D_tm / r_t and
+    ξ_t = γ^{t+1}, then the optional GroupNorm.  Returns out only (the state
+    is not affected by the normalisation)."""
+    qp, kp = prologue(q, k, theta, pos0)
+    v = _f64(v)
+    B, H, L, _ = qp.shape
+    g = _heads(gamma, H)
+    r = decay_row_sums(g, pos0, L)
+    out = np.zeros((B, H, L, v.shape[-1]))
+    for h in range(H):
+        Dn = decay_mask(g[h], L) / r[h][:, None]
+        out[:, h] = ((qp[:, h] @ np.swapaxes(kp[:, h], -1, -2)) * Dn) @ v[:, h]
+        if state_in is not None:
+            xi = np.power(g[h], np.arange(1, L + 1, dtype=np.float64)) / r[h]
+            out[:, h] += xi[None, :, None] * (qp[:, h] @ _f64(state_in)[:, h])
+    if gn is not None:
+        out = group_norm(out, gn.get("eps", 1e-5), gn.get("weight"), gn.get("bias"))
+    return out
 
 
 def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,

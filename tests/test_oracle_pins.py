@@ -242,12 +242,112 @@ def pin_groupnorm_matches_torch():
     assert np.allclose(y0.var(-1), 1, atol=1e-4)
 
 
+def _backward_fd_check(with_state, with_dso, pos0):
+    """retention_backward against central differences of the forward oracle,
+    for the scalar <dO, out> + <dS_out, S_out>: every gradient term
+    (intra-chunk scores, the state_in term, the state_out path, the rotation
+    adjoint and the 1/√d_k scale) enters one of the four checks."""
+    rng = np.random.default_rng(7 + pos0)
+    B, H, L, d_k, d_v = 1, 2, 6, 4, 3
+    q, k = rng.standard_normal((B, H, L, d_k)), rng.standard_normal((B, H, L, d_k))
+    v = rng.standard_normal((B, H, L, d_v))
+    S0 = 0.3 * rng.standard_normal((B, H, d_k, d_v)) if with_state else None
+    g, th = np.array([0.9, 0.6]), np.array([0.4, 1.3])
+    dO = rng.standard_normal((B, H, L, d_v))
+    dSo = rng.standard_normal((B, H, d_k, d_v)) if with_dso else None
+
+    def f(q_, k_, v_, s_):
+        o, S = R.retention(q_, k_, v_, g, th, pos0, s_, "parallel")
+        return (o * dO).sum() + ((S * dSo).sum() if with_dso else 0.0)
+
+    grads = R.retention_backward(q, k, v, g, th, pos0, S0, dO, dSo)
+    args = [q, k, v, S0 if with_state else np.zeros((B, H, d_k, d_v))]
+    eps = 1e-6
+    for which in range(4 if with_state else 3):
+        x = args[which]
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            a = [t.copy() for t in args]
+            a[which][idx] += eps
+            fp = f(*(a[:3] + [a[3] if with_state else None]))
+            a[which][idx] -= 2 * eps
+            fm = f(*(a[:3] + [a[3] if with_state else None]))
+            num[idx] = (fp - fm) / (2 * eps)
+        assert np.max(np.abs(num - grads[which])) < 1e-6, which
+    if not with_state:   # d_state_in is still defined: the gradient at S_in = 0
+        num = np.zeros((B, H, d_k, d_v))
+        for idx in np.ndindex(num.shape):
+            e = np.zeros_like(num)
+            e[idx] = eps
+            num[idx] = (f(q, k, v, e) - f(q, k, v, -e)) / (2 * eps)
+        assert np.max(np.abs(num - grads[3])) < 1e-6
+
+
+def pin_backward_finite_differences():
+    _backward_fd_check(True, True, 11)
+    _backward_fd_check(False, False, 0)
+
+
+# Row-normalised decay (R9)
+def pin_decay_row_sums_geometric_series():
+    """r_N = Σ_{i≤N} γ^i is the geometric series (1 − γ^{N+1}) / (1 − γ); N + 1 at γ = 1."""
+    g = np.array([0.9, 0.999, 1.0])
+    r = R.decay_row_sums(g, 5, 40)
+    N = np.arange(5, 45)
+    for h, gh in enumerate(g):
+        ref = N + 1.0 if gh == 1.0 else (1 - gh ** (N + 1)) / (1 - gh)
+        assert np.allclose(r[h], ref, rtol=1e-13, atol=0)
+
+
+def pin_normalised_gamma_one_is_a_running_mean():
+    """γ = 1, θ = 0: o_t = q_t · (Σ_{m≤t} k′_mᵀ v_m) / (t + 1), a cumulative mean."""
+    rng = np.random.default_rng(31)
+    q, k, v = rng.standard_normal((1, 1, 12, 4)), rng.standard_normal((1, 1, 12, 4)), rng.standard_normal((1, 1, 12, 3))
+    out = R.normalised_retention(q, k, v, np.array([1.0]), np.zeros(2))
+    kv = np.cumsum(np.einsum("td,te->tde", k[0, 0] / 2.0, v[0, 0]), axis=0)   # k′ = k/√4
+    ref = np.einsum("td,tde->te", q[0, 0], kv) / np.arange(1, 13)[:, None]
+    assert np.allclose(out[0, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_normalised_cancels_under_groupnorm():
+    """GroupNorm is invariant to a positive per-(token, head) scale ([P5]): with
+    eps = 0 the normalised and the plain outputs agree after it; without it
+    they differ by exactly r_t per row."""
+    rng = np.random.default_rng(32)
+    q, k = rng.standard_normal((2, 2, 20, 8)), rng.standard_normal((2, 2, 20, 8))
+    v, s = rng.standard_normal((2, 2, 20, 6)), 0.1 * rng.standard_normal((2, 2, 8, 6))
+    g, th = np.array([0.95, 0.7]), rng.uniform(0.01, 1, 4)
+    a = R.normalised_retention(q, k, v, g, th, 3, s, gn={"eps": 0.0})
+    b, _ = R.retention(q, k, v, g, th, 3, s, "parallel", gn={"eps": 0.0})
+    assert np.allclose(a, b, rtol=1e-10, atol=1e-10)
+    a = R.normalised_retention(q, k, v, g, th, 3, s)
+    b, _ = R.retention(q, k, v, g, th, 3, s, "parallel")
+    N = np.arange(3, 23)
+    r = (1 - g[:, None] ** (N + 1)) / (1 - g[:, None])          # geometric series
+    assert np.allclose(a * r[None, :, :, None], b, rtol=1e-12, atol=1e-12)
+
+
+def pin_normalised_split_calls():
+    """Positions are absolute: [0, L) in one call equals [0, L/2) then [L/2, L)
+    with the state passed through and pos0 = L/2."""
+    rng = np.random.default_rng(33)
+    q, k, v = rng.standard_normal((1, 2, 24, 4)), rng.standard_normal((1, 2, 24, 4)), rng.standard_normal((1, 2, 24, 5))
+    g, th = np.array([0.9, 0.99]), rng.uniform(0.01, 1, 2)
+    whole = R.normalised_retention(q, k, v, g, th)
+    first = R.normalised_retention(q[:, :, :12], k[:, :, :12], v[:, :, :12], g, th)
+    _, S = R.retention(q[:, :, :12], k[:, :, :12], v[:, :, :12], g, th, 0, None, "parallel")
+    second = R.normalised_retention(q[:, :, 12:], k[:, :, 12:], v[:, :, 12:], g, th, 12, S)
+    assert np.allclose(whole, np.concatenate([first, second], axis=2), rtol=1e-12, atol=1e-12)
+
+
 PINS = [
     pin_demo_parallel_equals_recurrent, pin_rotation_fixed_angles, pin_retention_hand_case,
     pin_forms_match_brute_force, pin_linear_attention_limit, pin_gamma_zero, pin_single_token,
     pin_theta_zero_is_identity, pin_rotation_preserves_pair_norms, pin_position_shift_invariance,
     pin_exact_causality, pin_chunk_limits, pin_split_call, pin_ragged_tail, pin_linearity,
-    pin_decode_steps_equal_recurrent, pin_groupnorm_matches_torch,
+    pin_decode_steps_equal_recurrent, pin_groupnorm_matches_torch, pin_backward_finite_differences,
+    pin_decay_row_sums_geometric_series, pin_normalised_gamma_one_is_a_running_mean,
+    pin_normalised_cancels_under_groupnorm, pin_normalised_split_calls,
 ]
 
 
@@ -286,6 +386,17 @@ MUTANTS = {
                     "((o - mu) ** 2).sum(axis=-1, keepdims=True) / (o.shape[-1] - 1)"),
     "gn_eps_outside": ("group_norm", "np.sqrt(var + float(eps))", "(np.sqrt(var) + float(eps))"),
     "decode_no_decay": ("decode_step", "S = g * state +", "S = state +"),
+    "bwd_no_state_in_term": ("retention_backward", "dqp[:, h] += xi[None, :, None] * (dO[:, h] @",
+                             "dqp[:, h] += 0.0 * xi[None, :, None] * (dO[:, h] @"),
+    "bwd_adjoint_not_inverse": ("retention_backward", "dq = theta_shift(dqp, -sin, cos)",
+                                "dq = theta_shift(dqp, sin, cos)"),
+    "bwd_dk_untransposed": ("retention_backward", "np.swapaxes(G, -1, -2) @ qp[:, h]", "G @ qp[:, h]"),
+    "bwd_dsin_power": ("retention_backward", "np.power(g[h], float(L)) * dSo", "np.power(g[h], float(L - 1)) * dSo"),
+    "bwd_dk_no_scale": ("retention_backward", "/ math.sqrt(d_k)", ""),
+    "rowsum_local_positions": ("decay_row_sums", "np.cumsum(terms)[int(pos0):]", "np.cumsum(terms)[:int(L)]"),
+    "rowsum_off_by_one": ("decay_row_sums", "np.arange(n_max,", "np.arange(1, n_max + 1,"),
+    "normalised_state_unscaled": ("normalised_retention", "np.arange(1, L + 1, dtype=np.float64)) / r[h]",
+                                  "np.arange(1, L + 1, dtype=np.float64))"),
 }
 
 
@@ -331,41 +442,4 @@ def test_mutants_are_caught(name, monkeypatch):
 # ------------------------------------------------------------- backward --
 @pytest.mark.parametrize("with_state,with_dso,pos0", [(False, False, 0), (True, False, 3), (True, True, 11)])
 def test_backward_matches_finite_differences(with_state, with_dso, pos0):
-    """retention_backward against central differences of the (pinned) forward
-    oracle, for the scalar <dO, out> + <dS_out, S_out>: every gradient term
-    (intra-chunk scores, the state_in term, the state_out path, the rotation
-    adjoint and the 1/√d_k scale) enters one of the four checks."""
-    rng = np.random.default_rng(7 + pos0)
-    B, H, L, d_k, d_v = 1, 2, 6, 4, 3
-    q, k = rng.standard_normal((B, H, L, d_k)), rng.standard_normal((B, H, L, d_k))
-    v = rng.standard_normal((B, H, L, d_v))
-    S0 = 0.3 * rng.standard_normal((B, H, d_k, d_v)) if with_state else None
-    g, th = np.array([0.9, 0.6]), np.array([0.4, 1.3])
-    dO = rng.standard_normal((B, H, L, d_v))
-    dSo = rng.standard_normal((B, H, d_k, d_v)) if with_dso else None
-
-    def f(q_, k_, v_, s_):
-        o, S = R.retention(q_, k_, v_, g, th, pos0, s_, "parallel")
-        return (o * dO).sum() + ((S * dSo).sum() if with_dso else 0.0)
-
-    grads = R.retention_backward(q, k, v, g, th, pos0, S0, dO, dSo)
-    args = [q, k, v, S0 if with_state else np.zeros((B, H, d_k, d_v))]
-    eps = 1e-6
-    for which in range(4 if with_state else 3):
-        x = args[which]
-        num = np.zeros_like(x)
-        for idx in np.ndindex(x.shape):
-            a = [t.copy() for t in args]
-            a[which][idx] += eps
-            fp = f(*(a[:3] + [a[3] if with_state else None]))
-            a[which][idx] -= 2 * eps
-            fm = f(*(a[:3] + [a[3] if with_state else None]))
-            num[idx] = (fp - fm) / (2 * eps)
-        assert np.max(np.abs(num - grads[which])) < 1e-6, which
-    if not with_state:   # d_state_in is still defined: the gradient at S_in = 0
-        num = np.zeros((B, H, d_k, d_v))
-        for idx in np.ndindex(num.shape):
-            e = np.zeros_like(num)
-            e[idx] = eps
-            num[idx] = (f(q, k, v, e) - f(q, k, v, -e)) / (2 * eps)
-        assert np.max(np.abs(num - grads[3])) < 1e-6
+    _backward_fd_check(with_state, with_dso, pos0)
