@@ -425,6 +425,31 @@ def main():
               "gpu_launches": dsteps, "clocks": dsampler.summary()}
     del dinp, dstate
 
+    # ---------------- row-normalised decay variant on the chunkwise output ----------------
+    nsteps = 20
+    garr_c = fptr(garr)
+    for _ in range(3):
+        lib.ret_decay_row_norm(vp(out), _lib.RET_BF16, garr_c, w.B, w.H, w.L, w.d_v, 0,
+                               C.c_void_p(stream.cuda_stream))
+    torch.cuda.synchronize()
+    ns_, ne_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ns_.record(stream)
+    for _ in range(nsteps):
+        st_ = lib.ret_decay_row_norm(vp(out), _lib.RET_BF16, garr_c, w.B, w.H, w.L, w.d_v, 0,
+                                     C.c_void_p(stream.cuda_stream))
+        if st_ != _lib.RET_OK:
+            raise RuntimeError(f"ret_decay_row_norm returned {st_}")
+    ne_.record(stream)
+    torch.cuda.synchronize()
+    nms = ns_.elapsed_time(ne_) / nsteps
+    nbytes = 2 * w.B * w.H * w.L * w.d_v * 2   # read and write the bf16 output
+    ngbs = nbytes / (nms / 1e3) / 1e9
+    row_norm = {"metric": "row-normalised decay pass GB/s", "value": ngbs, "unit": "GB/s",
+                "ms_per_launch": nms, "launches": nsteps,
+                "roofline": {"bound": "hbm", "achieved": ngbs, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": ngbs / peaks["hbm_gbs"], "traffic": None,
+                             "algorithmic_bytes_per_launch": nbytes}}
+
     # ---------------- gradient pass (fp32 kernels) on the same workload ----------------
     backward = None
     if args.backward_steps > 0:
@@ -595,6 +620,7 @@ def main():
             "clocks": sampler.summary(),
             "decode": decode,
             "backward": backward,
+            "decay_row_norm": row_norm,
             "e2e": e2e,
             "cpu_baseline": cpu,
         }

@@ -252,6 +252,23 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta,
                       int B, int H, int L, int d, int64_t pos0, float scale,
                       void* y, ret_dtype out_dt, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * ret_decay_row_norm — the row-normalised decay variant («从RoPE到Retention…»
+ * §5: the decay weights normalised per row), applied in place to `out` of a
+ * plain call (ret_chunkwise / ret_parallel without GroupNorm, or ret_step
+ * with L = 1 and pos0 = its pos).  Row N of the decay mask covers positions
+ * 0..N (the state term standing for the positions before pos0); divided by
+ * its sum r_N = Σ_{i=0}^{N} γ^i it divides output row N by r_N, so
+ *   out[b][h][t][:] /= r_{pos0+t},  r_N = (1 − γ_h^{N+1}) / (1 − γ_h).
+ * The pages' "global scaling" has no stated value and is 1.  A GroupNorm
+ * after the variant cancels it up to eps (GroupNorm is invariant to a
+ * positive per-token scale), so the variant is meant for outputs without
+ * GroupNorm.  out: DEVICE [B, H, L, d_v] in out_dt; gamma: HOST [H].
+ * 0 < γ_h ≤ 1, else RET_EINVAL.  The state is not affected.
+ * ------------------------------------------------------------------------ */
+ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, int B, int H,
+                              int L, int d_v, int64_t pos0, cudaStream_t stream);
+
 /* Synchronise `stream`, then return and clear the device status word:
  * RET_ETIMEOUT if a kernel's bounded wait expired since the last call,
  * RET_ECUDA on a CUDA error, else RET_OK. */

@@ -47,6 +47,7 @@ SIGNATURES = {
     "ret_step": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i64, _vp, _vp, _i,
                       C.POINTER(RetGN), _vp]),
     "ret_rotate": (_i, [_vp, _i, _fp, _i, _i, _i, _i, _i64, _f, _vp, _i, _vp]),
+    "ret_decay_row_norm": (_i, [_vp, _i, _fp, _i, _i, _i, _i, _i64, _vp]),
     "ret_sync_status": (_i, [_vp]),
     "ret_selftest_timeout": (_i, [_i, _vp]),
     "ret_force_path": (_i, [_i]),

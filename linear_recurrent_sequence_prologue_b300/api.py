@@ -268,6 +268,19 @@ def rotate(x, theta, pos0: int = 0, scale: float = 1.0, out_dtype=None, stream=N
     return y
 
 
+def decay_row_norm(out, gamma, pos0: int = 0, stream=None):
+    """Row-normalised decay variant, in place on out [B, H, L, d_v] (or [B, H, d_v]
+    of a decode step at position pos0): row t divided by Σ_{i≤pos0+t} γ^i."""
+    lib = load()
+    x = out if out.dim() == 4 else out.unsqueeze(2)
+    B, H, L, d_v = x.shape
+    garr, gp = _host_f32(gamma, H, "gamma")
+    st = lib.ret_decay_row_norm(_dev(out, "out"), _dtype_code(out), gp, B, H, L, d_v, int(pos0),
+                                _stream(stream))
+    check("ret_decay_row_norm", st)
+    return out
+
+
 def sync_status(stream=None) -> int:
     """Synchronise and return (and clear) the device status word as a ret_status code."""
     return load().ret_sync_status(_stream(stream))

@@ -412,6 +412,29 @@ __global__ void __launch_bounds__(256) decode_step_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Row-normalised decay («从RoPE到Retention…» §5, the decay weights normalised
+// per row): dividing row N of the decay mask by its sum over the positions
+// 0..N it covers, r_N = Σ_{i=0}^{N} γ^i, divides output row N by r_N, so
+// the variant is this in-place pass over an output of the plain form:
+//   out[bh][t][:] /= r_{pos0+t},  r_N = (1 − γ^{N+1}) / (1 − γ)  (N + 1 at γ = 1)
+// r is evaluated as expm1((N+1)·ln γ) / expm1(ln γ), with ln γ from the
+// host's double-precision log2 γ, which keeps full relative precision when
+// γ is close to 1.  One block of 128 threads per row.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(128) decay_row_norm_kernel(T* __restrict__ out, CallConsts cc,
+                                                             int H, int L, int d_v, float pos0) {
+  const size_t row = blockIdx.x;
+  const int t = static_cast<int>(row % L);
+  const int h = static_cast<int>((row / L) % H);
+  const float lg = cc.lg2g[h] * 0.69314718f;   // ln γ
+  const float n1 = pos0 + static_cast<float>(t) + 1.f;
+  const float r = lg == 0.f ? n1 : expm1f(n1 * lg) / expm1f(lg);
+  T* o = out + row * d_v;
+  for (int c = threadIdx.x; c < d_v; c += blockDim.x) o[c] = from_f32<T>(to_f32(o[c]) / r);
+}
+
+// ---------------------------------------------------------------------------
 // Helpers of the gradient pass (ret_chunkwise_backward).  The gradients are
 // three evaluations of the chunkwise form on reordered operands: reading the
 // sequence backwards turns the anti-causal sums Σ_{t≥m} of the gradient into

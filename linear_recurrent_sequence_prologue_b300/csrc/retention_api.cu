@@ -1363,6 +1363,30 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B,
   return last_launch();
 }
 
+ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, int B, int H,
+                              int L, int d_v, int64_t pos0, cudaStream_t stream) {
+  if (!out || !al16(out) || (out_dt != RET_F32 && out_dt != RET_BF16)) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  if (pos0 < 0 || pos0 + L > kMaxPos) return RET_EINVAL;
+  const int64_t rows = static_cast<int64_t>(B) * H * L;
+  if (rows >= (int64_t(1) << 31)) return RET_EINVAL;
+  if (!gamma) return RET_EINVAL;
+  CallConsts cc;
+  std::memset(&cc, 0, sizeof(cc));
+  for (int h = 0; h < H; ++h) {
+    if (!(gamma[h] > 0.f) || !(gamma[h] <= 1.f)) return RET_EINVAL;
+    cc.lg2g[h] = static_cast<float>(std::log2(static_cast<double>(gamma[h])));
+  }
+  Mark m("decay_row_norm", stream);
+  if (out_dt == RET_F32)
+    simt::decay_row_norm_kernel<float><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
+        static_cast<float*>(out), cc, H, L, d_v, static_cast<float>(pos0));
+  else
+    simt::decay_row_norm_kernel<__nv_bfloat16><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
+        static_cast<__nv_bfloat16*>(out), cc, H, L, d_v, static_cast<float>(pos0));
+  return last_launch();
+}
+
 ret_status ret_sync_status(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return RET_ECUDA;
   unsigned int h[4] = {0, 0, 0, 0};

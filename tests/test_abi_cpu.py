@@ -240,3 +240,20 @@ def test_backward_plan_and_validation(lib):
     assert call(gamma=gh, H=128, L=65536, chunk=64) == _lib.RET_EUNSUPPORTED   # grid rows
     assert call() == _lib.RET_EWORKSPACE                             # valid: no workspace
     assert call(ws=P, wsn=16) == _lib.RET_EWORKSPACE                 # too small
+
+
+def test_decay_row_norm_validation(lib):
+    """ret_decay_row_norm checks its arguments before any launch."""
+    g = np.array([0.9, 0.99], np.float32)
+    P = C.c_void_p(0x1000)
+
+    def call(out=P, gamma=g, H=2, L=8, pos0=0, dt=_lib.RET_F32):
+        return lib.ret_decay_row_norm(out, dt, _fp(gamma), 1, H, L, 16, pos0, None)
+
+    assert call(out=None) == _lib.RET_EINVAL
+    assert call(out=C.c_void_p(0x1004)) == _lib.RET_EINVAL                 # misaligned
+    assert call(gamma=np.array([0.9, 1.01], np.float32)) == _lib.RET_EINVAL
+    assert call(gamma=np.array([0.9, 0.0], np.float32)) == _lib.RET_EINVAL
+    assert call(pos0=-1) == _lib.RET_EINVAL
+    assert call(pos0=(1 << 24) - 4) == _lib.RET_EINVAL                     # positions past 2^24
+    assert call(dt=7) == _lib.RET_EINVAL

@@ -509,6 +509,39 @@ def test_backward_msr7b_sampled_heads():
     assert_close(gpu_np(dv[b:b + 1, h:h + 1, m0:]), rv, torch.bfloat16, "7B dv suffix")
 
 
+# ------------------------------------------------- row-normalised decay --
+@pytest.mark.parametrize("dtype,d_k,d_v,L,chunk,pos0,state", [
+    ("bf16", 256, 256, 300, 128, 0, True),     # tensor-core output, ragged
+    ("bf16", 128, 128, 256, 128, 7, False),
+    ("f32", 16, 24, 70, 16, 500, True),        # fp32 kernels
+])
+def test_decay_row_norm_vs_oracle(dtype, d_k, d_v, L, chunk, pos0, state):
+    w, inp = _custom(2, 3, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0, seed=L + pos0)
+    d = _cuda(inp)
+    o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=chunk, pos0=pos0,
+                       state_in=d["state_in"], return_state=False)
+    R.decay_row_norm(o, inp["gamma"], pos0=pos0)
+    assert R.sync_status() == R.RET_OK
+    ref = O.normalised_retention(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                                 np.asarray(inp["gamma"], np.float64),
+                                 np.asarray(inp["theta"], np.float64), pos0, to_f64(inp["state_in"]))
+    assert_close(gpu_np(o), ref, w.torch_dtype, "row-normalised")
+
+
+def test_decay_row_norm_decode_step():
+    """A decode step's output at position pos, normalised by r_pos."""
+    g = torch.Generator().manual_seed(41)
+    q, k = torch.randn(2, 4, 64, generator=g), torch.randn(2, 4, 64, generator=g)
+    v, S = torch.randn(2, 4, 128, generator=g), 0.1 * torch.randn(2, 4, 64, 128, generator=g)
+    gam, th = gamma_schedule(4), theta_schedule(64)
+    st = S.cuda()
+    out = R.step(q.cuda(), k.cuda(), v.cuda(), gam, th, 1234, st)
+    R.decay_row_norm(out, gam, pos0=1234)
+    ref = O.normalised_retention(to_f64(q)[:, :, None], to_f64(k)[:, :, None], to_f64(v)[:, :, None],
+                                 gam.astype(np.float64), th.astype(np.float64), 1234, to_f64(S))
+    assert_close(gpu_np(out)[:, :, None], ref, torch.float32, "decode row-normalised")
+
+
 def test_decode_1024_steps_vs_chunkwise_and_oracle():
     w = WORKLOADS["decode"]
     inp = make_decode_inputs(w, seed=0, device="cuda")
