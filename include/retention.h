@@ -126,6 +126,15 @@ ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H,
                               int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
                               int* path, size_t* workspace_bytes);
 
+/* Chunk length for a chunkwise call of this shape: 128 (the tensor-core
+ * tile) wherever the tensor-core path applies, otherwise b = round(√L), the
+ * square-root balance of the RetNet 保留网络 explainer (分块循环: n/b chunks
+ * of O(b²) work each, O(n·b) in total, with n/b sequential state steps),
+ * at least 1.  √8192 ≈ 91, so at the 7B shape the tile is the nearest
+ * power of two above the balance.  gamma: HOST [H] or NULL (then the
+ * tensor-core path is assumed allowed).  Returns 0 for invalid arguments. */
+int ret_chunk_size(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int d_v);
+
 /* ------------------------------------------------------------------------
  * ret_chunkwise_noalloc — ret_chunkwise for callers that may not allocate
  * device memory themselves, e.g. plugins whose host application owns the

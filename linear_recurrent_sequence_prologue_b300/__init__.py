@@ -4,13 +4,13 @@ The compute path is the CUDA library (csrc/, C ABI in include/retention.h);
 this package only marshals torch tensors into that ABI.
 """
 
-from .api import (backward_plan, chunkwise, chunkwise_backward, decay_row_norm, force_path, parallel,
-                  plan, rotate, selftest_timeout, status_string, step, sync_status)
+from .api import (backward_plan, chunk_size, chunkwise, chunkwise_backward, decay_row_norm, force_path,
+                  parallel, plan, rotate, selftest_timeout, status_string, step, sync_status)
 from ._lib import (RET_BF16, RET_EINVAL, RET_ETIMEOUT, RET_EUNSUPPORTED, RET_EWORKSPACE, RET_F32,
                    RET_OK, RET_PATH_SIMT, RET_PATH_TC, RET_PATH_TC_SINGLE, RetentionError, load)
 
 __all__ = [
-    "chunkwise", "chunkwise_backward", "backward_plan", "decay_row_norm", "parallel", "step", "rotate", "plan", "sync_status", "selftest_timeout",
+    "chunkwise", "chunk_size", "chunkwise_backward", "backward_plan", "decay_row_norm", "parallel", "step", "rotate", "plan", "sync_status", "selftest_timeout",
     "force_path", "status_string", "load", "RetentionError",
     "RET_OK", "RET_EINVAL", "RET_EUNSUPPORTED", "RET_ETIMEOUT", "RET_EWORKSPACE",
     "RET_F32", "RET_BF16", "RET_PATH_TC", "RET_PATH_SIMT", "RET_PATH_TC_SINGLE",

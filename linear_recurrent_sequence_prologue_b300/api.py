@@ -114,11 +114,24 @@ def plan(form: str, in_dtype, B, H, L, d_k, d_v, chunk=None, out_dtype=None, gn=
     return path.value, nbytes.value
 
 
-def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
+def chunk_size(in_dtype, H, L, d_k, d_v, gamma=None) -> int:
+    """The library's chunk length for this shape: 128 on the tensor-core path,
+    else round(√L)."""
+    gp = None
+    if gamma is not None:
+        garr, gp = _host_f32(gamma, H, "gamma")
+    b = load().ret_chunk_size(_DT[in_dtype], gp, H, L, d_k, d_v)
+    if b < 1:
+        raise ValueError("invalid shape for ret_chunk_size")
+    return b
+
+
+def chunkwise(q, k, v, gamma, theta, chunk: Optional[int] = None, pos0: int = 0, state_in=None,
               return_state: bool = True, out=None, out_dtype=None, gn=None, workspace=None,
               stream=None, layout: str = "carry", state_out=None):
     """Chunkwise retention.  Returns (out, state_out or None).
 
+    chunk=None takes ret_chunk_size's choice.
     layout="carry" runs ret_chunkwise (state carried across chunks);
     layout="scan" runs ret_chunkwise_scan (chunk-parallel then scan).
     pos0 is one start position, or a sequence of B start positions (one per
@@ -128,6 +141,8 @@ def chunkwise(q, k, v, gamma, theta, chunk: int, pos0: int = 0, state_in=None,
     lib = load()
     B, H, L, d_k, d_v = _check_seq(q, k, v)
     idt = _dtype_code(q)
+    if chunk is None:
+        chunk = chunk_size(q.dtype, H, L, d_k, d_v, gamma)
     odtype = out_dtype or q.dtype
     if out is None:
         out = torch.empty((B, H, L, d_v), dtype=odtype, device=q.device)

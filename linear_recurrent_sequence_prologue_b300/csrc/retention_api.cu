@@ -1031,6 +1031,19 @@ ret_status ret_force_path(int path) {
   return RET_OK;
 }
 
+int ret_chunk_size(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int d_v) {
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return 0;
+  if (H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 ||
+      d_v > 1024)
+    return 0;
+  if (gamma)
+    for (int h = 0; h < H; ++h)
+      if (!(gamma[h] > 0.f) || !(gamma[h] <= 1.f)) return 0;
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH)) return tcc::CH;
+  const long long b = std::llround(std::sqrt(static_cast<double>(L)));
+  return static_cast<int>(std::max(1LL, std::min<long long>(b, L)));
+}
+
 ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k,
                               int d_v, int chunk, ret_dtype out_dt, int gn_enabled, int* path,
                               size_t* workspace_bytes) {

@@ -257,3 +257,22 @@ def test_decay_row_norm_validation(lib):
     assert call(pos0=-1) == _lib.RET_EINVAL
     assert call(pos0=(1 << 24) - 4) == _lib.RET_EINVAL                     # positions past 2^24
     assert call(dt=7) == _lib.RET_EINVAL
+
+
+def test_chunk_size_policy(lib):
+    """128 where the tensor-core path applies, else round(√L) (at least 1)."""
+    def b(dt, L, d_k=256, d_v=512, H=16, gamma=None):
+        return lib.ret_chunk_size(dt, _fp(gamma) if gamma is not None else None, H, L, d_k, d_v)
+
+    assert b(_lib.RET_BF16, 8192) == 128                  # 7B shape: the tensor-core tile
+    assert b(_lib.RET_BF16, 8000) == 128                  # ragged lengths stay on the tile
+    assert b(_lib.RET_F32, 8192) == 91                    # √8192 = 90.5
+    assert b(_lib.RET_F32, 2048, 64, 64, 8) == 45         # √2048 = 45.3
+    assert b(_lib.RET_BF16, 4096, 512, 512) == 64         # d_k outside the tensor-core shapes
+    assert b(_lib.RET_BF16, 4096, 256, 96) == 64          # d_v not a multiple of 128
+    assert b(_lib.RET_F32, 1, 16, 16, 1) == 1
+    assert b(_lib.RET_F32, 2, 16, 16, 1) == 1
+    g = np.array([0.5] + [0.99] * 15, np.float32)         # γ^127 underflows the rewritten form
+    assert b(_lib.RET_BF16, 8192, gamma=g) == 91
+    assert b(_lib.RET_F32, 0) == 0 and b(7, 64) == 0      # invalid arguments
+    assert b(_lib.RET_F32, 64, gamma=np.array([1.5] * 16, np.float32)) == 0
