@@ -247,9 +247,30 @@ def cpu_baseline(w, inp, budget_s=12.0):
     dt = time.perf_counter() - t0
     per_head = dt / done
     value = (w.B * w.L) / (per_head * len(heads))
-    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {len(heads)} (b,h) heads of the {w.name} workload, float64 "
-                      f"chunkwise oracle, {dt:.1f} s; tokens/s scaled to all heads"}
+    out = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{done} of {len(heads)} (b,h) heads of the {w.name} workload, float64 "
+                     f"chunkwise oracle, {dt:.1f} s; tokens/s scaled to all heads"}
+    # the same oracle on one thread, on at most two heads (a few seconds)
+    try:
+        from threadpoolctl import threadpool_limits
+        with threadpool_limits(limits=1):
+            done1, t1 = 0, time.perf_counter()
+            for b, h in heads[:2]:
+                sl = lambda t: to_f64(t[b:b + 1, h:h + 1])
+                O.retention(sl(inp["q"]), sl(inp["k"]), sl(inp["v"]),
+                            np.asarray(inp["gamma"], np.float64)[h:h + 1],
+                            np.asarray(inp["theta"], np.float64), 0,
+                            None if inp["state_in"] is None else sl(inp["state_in"]), "chunkwise",
+                            w.chunk)
+                done1 += 1
+                if time.perf_counter() - t1 > budget_s / 3:
+                    break
+            dt1 = time.perf_counter() - t1
+        out["value_1_thread"] = (w.B * w.L) / (dt1 / done1 * len(heads))
+        out["sample_1_thread"] = f"{done1} head(s) on 1 thread, {dt1:.1f} s; scaled to all heads"
+    except ImportError:
+        pass
+    return out
 
 
 # --------------------------------------------------------------------------
