@@ -19,6 +19,9 @@ Sources (web pages about RetNet; formulas partly garbled by extraction):
   carry between chunks, b=1 → recurrent, b=n → parallel), "Python 演示"
   (parallel and recurrent agree to < 1e-8), "常见误区" (the factorisation
   γ^{n-j} = γ^n·γ^{-j} turns the pairwise sum into a state recurrence).
+* [P4] «RetNet：Transformer的革命性继任者？» (project page of a PyTorch
+  implementation): SimpleRetention with W_Q, W_K, W_V applied to the input X;
+  MultiScaleRetention as one SimpleRetention per head in parallel.
 * [P5] «Transformer后繼有模！MSRA提出全新大模型基礎架構» (b99b.cn): GroupNorm
   is used for its scale invariance; complex-valued position encoding.
 
@@ -43,6 +46,12 @@ R6  Masked entries (n < m) are exact zeros.
 R7  GroupNorm: one group per head over the d_v channels of one token,
     biased variance, eps given by the caller (1e-5 default), optional affine.
 R8  A ragged last chunk of length r uses carry γ^r and ζ_j = γ^{r-1-j}.
+R10 The MSR block around the core (the projections of [P4]'s SimpleRetention,
+    q = X·W_Q, k = X·W_K, v = X·W_V per head; heads in parallel, outputs
+    concatenated; per-head GroupNorm of [P1] §5).  The pages give no output
+    projection or gate; the block takes the published RetNet MSR
+    definition for them: Z = (swish(X·W_G) ⊙ concat_h GN(O_h))·W_O with
+    swish(x) = x·σ(x).
 R9  The row-normalised decay of [P1] §5 ("三重标准化": the √d division, the
     decay weights normalised per row, a global scaling): row N of D is
     divided by its sum over the absolute positions 0..N it covers,
@@ -76,6 +85,7 @@ __all__ = [
     "retention_backward",
     "decay_row_sums",
     "normalised_retention",
+    "msr_block",
     "decode_step",
     "group_norm",
     "brute_force",
@@ -303,6 +313,25 @@ def normalised_retention(q, k, v, gamma, theta, pos0=0, state_in=None, gn=None):
     if gn is not None:
         out = group_norm(out, gn.get("eps", 1e-5), gn.get("weight"), gn.get("bias"))
     return out
+
+
+def msr_block(x, w_q, w_k, w_v, w_g, w_o, gamma, theta, pos0=0, state_in=None,
+              gn_eps=1e-5, chunk=None):
+    """The MSR block around the core (R10): x [B, L, D]; w_q, w_k [D, H, d_k];
+    w_v, w_g [D, H, d_v]; w_o [H, d_v, D_out].  Per head q = x·W_Q, k = x·W_K,
+    v = x·W_V ([P4]), the chunkwise core with the prologue, GroupNorm per
+    head ([P1] §5), the swish gate and the output projection.  Returns
+    (z [B, L, D_out], state_out)."""
+    x = _f64(x)
+    q = np.einsum("bld,dhk->bhlk", x, _f64(w_q))
+    k = np.einsum("bld,dhk->bhlk", x, _f64(w_k))
+    v = np.einsum("bld,dhv->bhlv", x, _f64(w_v))
+    o, S = retention(q, k, v, gamma, theta, pos0, state_in, "chunkwise", chunk)
+    y = group_norm(o, gn_eps)
+    gpre = np.einsum("bld,dhv->bhlv", x, _f64(w_g))
+    gate = gpre / (1.0 + np.exp(-gpre))                               # swish(x) = x·σ(x)
+    z = np.einsum("bhlv,hvo->blo", gate * y, _f64(w_o))
+    return z, S
 
 
 def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,

@@ -340,6 +340,68 @@ def pin_normalised_split_calls():
     assert np.allclose(whole, np.concatenate([first, second], axis=2), rtol=1e-12, atol=1e-12)
 
 
+# MSR block around the core (R10)
+def _block_inputs(seed, B=2, L=10, D=12, H=3, d_k=4, d_v=5, D_out=7):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.standard_normal((B, L, D)), w_q=rng.standard_normal((D, H, d_k)),
+                w_k=rng.standard_normal((D, H, d_k)), w_v=rng.standard_normal((D, H, d_v)),
+                w_g=rng.standard_normal((D, H, d_v)), w_o=rng.standard_normal((H, d_v, D_out)),
+                gamma=np.array([0.9, 0.8, 0.99]), theta=rng.uniform(0.01, 1, d_k // 2))
+
+
+def pin_block_projections_feed_the_core():
+    """With one-hot projections (D = H·d_k = H·d_v, W_Q = W_K = W_V = the head's
+    slice of the identity), q, k, v are the head slices of x; with w_g large
+    the gate is the identity to 1e-12 and w_o the identity reassembles the
+    heads, so the block equals GroupNorm of the core on the sliced x."""
+    rng = np.random.default_rng(41)
+    B, L, H, d = 2, 9, 3, 4
+    x = rng.standard_normal((B, L, H * d))
+    eye = np.eye(H * d).reshape(H * d, H, d)
+    w_o = np.eye(H * d).reshape(H, d, H * d)
+    g, th = np.array([0.9, 0.7, 0.99]), rng.uniform(0.01, 1, d // 2)
+    # swish(c·1) with c = 60 is 60·σ(60) = 60 to 1e-24; GroupNorm removes the factor 60
+    ones = np.zeros((H * d, H, d))
+    z, _ = R.msr_block(np.concatenate([x, np.ones((B, L, 1))], -1),
+                       np.concatenate([eye, np.zeros((1, H, d))], 0),
+                       np.concatenate([eye, np.zeros((1, H, d))], 0),
+                       np.concatenate([eye, np.zeros((1, H, d))], 0),
+                       np.concatenate([ones, np.full((1, H, d), 60.0)], 0), w_o, g, th)
+    xs = x.reshape(B, L, H, d).transpose(0, 2, 1, 3)
+    o, _ = R.retention(xs, xs, xs, g, th)
+    ref = 60.0 * R.group_norm(o)
+    assert np.allclose(z, ref.transpose(0, 2, 1, 3).reshape(B, L, H * d), rtol=1e-12, atol=1e-10)
+
+
+def pin_block_gate_and_projection():
+    """swish(0) = 0 gives z = 0; z is linear in W_O; swish matches x·expit(x)."""
+    p = _block_inputs(42)
+    z0, _ = R.msr_block(**{**p, "w_g": np.zeros_like(p["w_g"])})
+    assert np.all(z0 == 0.0)
+    z1, _ = R.msr_block(**p)
+    z2, _ = R.msr_block(**{**p, "w_o": 2.5 * p["w_o"]})
+    assert np.allclose(z2, 2.5 * z1, rtol=1e-12, atol=1e-12)
+    # one head, one gate column: compare against scipy's logistic function
+    from scipy.special import expit
+    o, _ = R.retention(np.einsum("bld,dhk->bhlk", p["x"], p["w_q"]),
+                       np.einsum("bld,dhk->bhlk", p["x"], p["w_k"]),
+                       np.einsum("bld,dhv->bhlv", p["x"], p["w_v"]), p["gamma"], p["theta"])
+    y = R.group_norm(o)
+    gp = np.einsum("bld,dhv->bhlv", p["x"], p["w_g"])
+    ref = np.einsum("bhlv,hvo->blo", gp * expit(gp) * y, p["w_o"])
+    assert np.allclose(z1, ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_block_groupnorm_removes_value_scale():
+    """The core is linear in v, so scaling W_V by c > 0 scales every head's
+    output by c, which GroupNorm with eps = 0 removes; the state scales by c."""
+    p = _block_inputs(43)
+    z1, s1 = R.msr_block(**p, gn_eps=0.0)
+    z2, s2 = R.msr_block(**{**p, "w_v": 3.0 * p["w_v"]}, gn_eps=0.0)
+    assert np.allclose(z1, z2, rtol=1e-10, atol=1e-10)
+    assert np.allclose(s2, 3.0 * s1, rtol=1e-12, atol=1e-12)
+
+
 PINS = [
     pin_demo_parallel_equals_recurrent, pin_rotation_fixed_angles, pin_retention_hand_case,
     pin_forms_match_brute_force, pin_linear_attention_limit, pin_gamma_zero, pin_single_token,
@@ -348,6 +410,8 @@ PINS = [
     pin_decode_steps_equal_recurrent, pin_groupnorm_matches_torch, pin_backward_finite_differences,
     pin_decay_row_sums_geometric_series, pin_normalised_gamma_one_is_a_running_mean,
     pin_normalised_cancels_under_groupnorm, pin_normalised_split_calls,
+    pin_block_projections_feed_the_core, pin_block_gate_and_projection,
+    pin_block_groupnorm_removes_value_scale,
 ]
 
 
@@ -395,6 +459,12 @@ MUTANTS = {
     "bwd_dk_no_scale": ("retention_backward", "/ math.sqrt(d_k)", ""),
     "rowsum_local_positions": ("decay_row_sums", "np.cumsum(terms)[int(pos0):]", "np.cumsum(terms)[:int(L)]"),
     "rowsum_off_by_one": ("decay_row_sums", "np.arange(n_max,", "np.arange(1, n_max + 1,"),
+    "block_q_from_w_k": ("msr_block", 'q = np.einsum("bld,dhk->bhlk", x, _f64(w_q))',
+                         'q = np.einsum("bld,dhk->bhlk", x, _f64(w_k))'),
+    "block_sigmoid_gate": ("msr_block", "gate = gpre / (1.0 + np.exp(-gpre))", "gate = 1.0 / (1.0 + np.exp(-gpre))"),
+    "block_gate_after_projection": ("msr_block", 'z = np.einsum("bhlv,hvo->blo", gate * y, _f64(w_o))',
+                                    'z = np.einsum("bhlv,hvo->blo", y, _f64(w_o)) * gate.mean()'),
+    "block_no_groupnorm": ("msr_block", "y = group_norm(o, gn_eps)", "y = o"),
     "normalised_state_unscaled": ("normalised_retention", "np.arange(1, L + 1, dtype=np.float64)) / r[h]",
                                   "np.arange(1, L + 1, dtype=np.float64))"),
 }
