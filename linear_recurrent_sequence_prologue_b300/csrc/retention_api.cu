@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "retention.h"
 #include "common.cuh"
@@ -35,6 +36,15 @@ struct ProfileHook {
 } g_prof;
 
 // Brackets one kernel launch with the hook's events when it is armed.
+// NVTX range around an entry point, for timeline tools (header-only NVTX:
+// without an attached tool each push / pop is a no-op call).
+struct Range {
+  explicit Range(const char* name) { nvtxRangePushA(name); }
+  ~Range() { nvtxRangePop(); }
+  Range(const Range&) = delete;
+  Range& operator=(const Range&) = delete;
+};
+
 struct Mark {
   cudaStream_t st;
   bool on;
@@ -1115,6 +1125,7 @@ ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype 
                          int d_v, int64_t pos0, int chunk, const float* state_in,
                          float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_chunkwise");
   return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, false);
 }
@@ -1125,6 +1136,7 @@ ret_status ret_chunkwise_rowpos(const void* q, const void* k, const void* v, ret
                                 const float* state_in, float* state_out, void* out,
                                 ret_dtype out_dt, const ret_gn* gn, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_chunkwise_rowpos");
   if (!row_pos0) return RET_EINVAL;
   return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, 0, chunk, state_in,
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, false,
@@ -1136,6 +1148,7 @@ ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, re
                                  int d_k, int d_v, int64_t pos0, int chunk,
                                  const float* state_in, float* state_out, void* out,
                                  ret_dtype out_dt, const ret_gn* gn, cudaStream_t stream) {
+  Range nv("ret_chunkwise_noalloc");
   ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
                               out_dt, gn);
   if (s != RET_OK) return s;
@@ -1168,6 +1181,7 @@ ret_status ret_chunkwise_scan(const void* q, const void* k, const void* v, ret_d
                               int d_k, int d_v, int64_t pos0, int chunk, const float* state_in,
                               float* state_out, void* out, ret_dtype out_dt, const ret_gn* gn,
                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_chunkwise_scan");
   return chunkwise_impl(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
                         state_out, out, out_dt, gn, workspace, workspace_bytes, stream, true);
 }
@@ -1196,6 +1210,7 @@ ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, c
                                   const float* state_in, const float* d_state_out, void* dq,
                                   void* dk, void* dv, ret_dtype grad_dt, float* d_state_in,
                                   void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_chunkwise_backward");
   ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, d_state_in, dq,
                               grad_dt, nullptr);
   if (s != RET_OK) return s;
@@ -1277,6 +1292,7 @@ ret_status ret_parallel(const void* q, const void* k, const void* v, ret_dtype i
                         int d_v, int64_t pos0, const float* state_in, float* state_out,
                         void* out, ret_dtype out_dt, const ret_gn* gn, void* workspace,
                         size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_parallel");
   ret_status s = check_common(q, k, v, in_dt, B, H, L, d_k, d_v, pos0, state_in, state_out, out,
                               out_dt, gn);
   if (s != RET_OK) return s;
@@ -1312,6 +1328,7 @@ ret_status ret_step(const void* q, const void* k, const void* v, ret_dtype in_dt
                     const float* gamma, const float* theta, int B, int H, int d_k, int d_v,
                     int64_t pos, float* state, void* out, ret_dtype out_dt, const ret_gn* gn,
                     cudaStream_t stream) {
+  Range nv("ret_step");
   ret_status s = check_common(q, k, v, in_dt, B, H, 1, d_k, d_v, pos, state, state, out, out_dt, gn);
   if (s != RET_OK) return s;
   if (!state) return RET_EINVAL;
@@ -1347,6 +1364,7 @@ ret_status ret_step(const void* q, const void* k, const void* v, ret_dtype in_dt
 ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B, int H, int L,
                       int d, int64_t pos0, float scale, void* y, ret_dtype out_dt,
                       cudaStream_t stream) {
+  Range nv("ret_rotate");
   if (!x || !y || !theta || !al16(x) || !al16(y)) return RET_EINVAL;
   if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
   if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
@@ -1378,6 +1396,7 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B,
 
 ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, int B, int H,
                               int L, int d_v, int64_t pos0, cudaStream_t stream) {
+  Range nv("ret_decay_row_norm");
   if (!out || !al16(out) || (out_dt != RET_F32 && out_dt != RET_BF16)) return RET_EINVAL;
   if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
   if (pos0 < 0 || pos0 + L > kMaxPos) return RET_EINVAL;
