@@ -139,6 +139,49 @@ def replica_throughput(units_per_rank: float, seconds_max: float, world: int) ->
     return world * units_per_rank / seconds_max
 
 
+def sustained_window(step, stream, dev_index, work, unit, peak, seconds=1.0):
+    """The same step repeated for at least `seconds` right after the timed
+    region, with its own device time and clock record: how the step runs once
+    the GPU has settled under this load (the power cap of the part can lower
+    the SM clock within a second).  Work per step in `unit` × 1e12 (TFLOP/s)
+    or 1e9 (GB/s); compared with the sustained peak when one is given."""
+    import torch
+    sampler = ClockSampler(dev_index)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        sampler.mark()
+        s.record(stream)
+        n = soak(step, torch.cuda.synchronize, seconds)
+        e.record(stream)
+        torch.cuda.synchronize()
+        sampler.mark()
+    ms = s.elapsed_time(e) / n
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    ach = work / (ms / 1e3) / scale
+    out = {"ms_per_step": ms, "steps": n, "achieved": ach, "unit": unit,
+           "clocks": sampler.summary(),
+           "note": "the step repeated for >= 1 s after the timed region (synchronised every 16 "
+                   "steps), device time over all of them"}
+    if peak:
+        out["peak"] = peak
+        out["frac"] = ach / peak
+    return out
+
+
+def soak(step, sync, seconds=1.0, batch=16):
+    """Run `step` (untimed) for at least `seconds` of wall clock, synchronising
+    every `batch` calls so that host time tracks device time; the clock
+    sampler runs through it, so the record covers a second of this load."""
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < seconds:
+        for _ in range(batch):
+            step()
+        n += batch
+        sync()
+    return n
+
+
 # --------------------------------------------------------------------------
 # Clock sampling during the timed region (NVML reads only)
 # --------------------------------------------------------------------------
@@ -154,7 +197,8 @@ class ClockSampler:
                   "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, dev_index, period_s=0.002):
-        self.samples, self.reasons, self.err = [], set(), None
+        self.samples, self.reasons, self.err, self.marks = [], set(), None, []
+        self.nvml_error = None
         self.dev, self.period, self.max_mhz, self.source = dev_index, period_s, None, None
         self._stop = threading.Event()
         try:
@@ -167,10 +211,16 @@ class ClockSampler:
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.source = "nvml"
         except Exception as e:  # noqa: BLE001
-            self.err = f"{type(e).__name__}: {e}"
+            self.nvml_error = f"{type(e).__name__}: {e}"
             import shutil
             if shutil.which("nvidia-smi"):
-                self.source, self.err = "nvidia-smi", None
+                self.source = "nvidia-smi"
+            else:
+                self.err = self.nvml_error
+
+    def mark(self):
+        """Record the current sample count (start / end of the timed region)."""
+        self.marks.append(len(self.samples))
 
     def _sample_nvml(self):
         self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
@@ -216,8 +266,16 @@ class ClockSampler:
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                "samples": len(self.samples), "source": self.source}
+        if len(self.marks) >= 2:
+            inside = self.samples[self.marks[0]:self.marks[1] + 1]
+            out["samples_in_timed_region"] = len(inside)
+            if inside:
+                out["sm_mhz_timed_region"] = statistics.median(inside)
+            out["window"] = "samples from the sampler's start through the end of the timed region"
         if self.err:
             out["error"] = self.err
+        if self.nvml_error and self.source != "nvml":
+            out["nvml_unavailable"] = self.nvml_error
         return out
 
 
@@ -374,6 +432,7 @@ def main():
     barrier()
     torch.cuda.synchronize()
     with sampler:
+        sampler.mark()
         start.record(stream)
         lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
         for it in range(args.steps):
@@ -382,9 +441,12 @@ def main():
                 n_k = lib.ret_profile_end()
         end.record(stream)
         torch.cuda.synchronize()
+        sampler.mark()
     names = [lib.ret_profile_kernel(i).decode() for i in range(n_k)]
     barrier()
     ms = start.elapsed_time(end)
+    sustained = sustained_window(cstep, stream, local, chunk_flops(w), "TFLOP/s",
+                                 peaks.get("bf16_tflops_sustained"))
     per_kernel = {}
     for i, nm in enumerate(names):
         per_kernel.setdefault(nm, []).append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
@@ -398,6 +460,97 @@ def main():
     achieved = flops / (top_ms / 1e3) / 1e12
     peak = peaks["bf16_tflops"]
     traffic = profiled_traffic(top)
+
+    # ---------------- the Small and 1.3B-shape workloads ----------------
+    def bench_config(name, steps):
+        """Time ret_chunkwise on one more workload: tokens/s, per-kernel times and
+        a roofline (the HBM bound for Small, whose arithmetic intensity is below
+        the ridge; the bf16 peak for the 1.3B shape).  Inputs smaller than L2 are
+        replicated into enough copies that consecutive steps read different
+        ones and the copies together exceed twice the 126 MB L2."""
+        cw = WORKLOADS[name]
+        cin = make_inputs(cw, seed=0)
+        in_bytes = sum(cin[n].numel() * cin[n].element_size() for n in ("q", "k", "v"))
+        copies = max(1, -(-2 * 126 * 2 ** 20 // in_bytes))
+        sets = [tuple(cin[n].to(dev) for n in ("q", "k", "v")) for _ in range(copies)]
+        cs_in = cin["state_in"].to(dev) if cin["state_in"] is not None else None
+        couts = [torch.empty((cw.B, cw.H, cw.L, cw.d_v), dtype=torch.bfloat16, device=dev)
+                 for _ in range(copies)]
+        cs_out = torch.empty((cw.B, cw.H, cw.d_k, cw.d_v), dtype=torch.float32, device=dev)
+        cpath, cws_bytes = R.plan("chunkwise", torch.bfloat16, cw.B, cw.H, cw.L, cw.d_k, cw.d_v,
+                                  cw.chunk, gn=cw.groupnorm, gamma=cin["gamma"])
+        cws = torch.empty(max(cws_bytes, 1), dtype=torch.uint8, device=dev)
+        cg = np.ascontiguousarray(cin["gamma"], np.float32)
+        ct = np.ascontiguousarray(cin["theta"], np.float32)
+        gns = _lib.RetGN(1, cw.gn_eps, None, None) if cw.groupnorm else None
+        gnp = C.byref(gns) if gns is not None else None
+        cargs_ = [(vp(a), vp(b), vp(c_), _lib.RET_BF16, fptr(cg), fptr(ct), cw.B, cw.H, cw.L,
+                   cw.d_k, cw.d_v, 0, cw.chunk, vp(cs_in), vp(cs_out), vp(o_), _lib.RET_BF16, gnp,
+                   vp(cws), cws_bytes, C.c_void_p(stream.cuda_stream))
+                  for (a, b, c_), o_ in zip(sets, couts)]
+        it_ = [0]
+
+        def one():
+            st_ = lib.ret_chunkwise(*cargs_[it_[0] % copies])
+            it_[0] += 1
+            if st_ != _lib.RET_OK:
+                raise RuntimeError(f"ret_chunkwise ({name}) returned {st_}")
+
+        for _ in range(max(3, args.warmup)):
+            one()
+        torch.cuda.synchronize()
+        hook = min(steps, 8)
+        csampler = ClockSampler(local)
+        cs_, ce_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        with csampler:
+            csampler.mark()
+            cs_.record(stream)
+            lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+            for i_ in range(steps):
+                one()
+                if i_ + 1 == hook:
+                    nk_ = lib.ret_profile_end()
+            ce_.record(stream)
+            torch.cuda.synchronize()
+            csampler.mark()
+        cnames = [lib.ret_profile_kernel(i).decode() for i in range(nk_)]
+        cper = {}
+        for i_, nm in enumerate(cnames):
+            cper.setdefault(nm, []).append(evs[2 * i_].elapsed_time(evs[2 * i_ + 1]))
+        cms = max_over_ranks(cs_.elapsed_time(ce_) / steps, world, dev)
+        cstep_ms = {nm: sum(t) / hook for nm, t in cper.items()}
+        ctop = max(cstep_ms, key=cstep_ms.get)
+        cfl, cby = chunk_flops(cw), chunk_bytes(cw)
+        if name == "small":
+            bound, pk, unit_ = "hbm", peaks["hbm_gbs"], "GB/s"
+            ach = cby / (cms / 1e3) / 1e9
+            knote = "whole call: algorithmic bytes / call time"
+        else:
+            bound, pk, unit_ = "tensor", peak, "TFLOP/s"
+            ach = cfl / (cstep_ms[ctop] / 1e3) / 1e12
+            knote = f"kernel {ctop}: algorithmic flop / its launch time"
+        res = {"metric": "chunkwise retention tokens/s", "unit": "tokens/s",
+               "value": replica_throughput(cw.B * cw.L, cms / 1e3, world), "ms_per_step": cms,
+               "steps": steps, "path": "tensor cores" if cpath == _lib.RET_PATH_TC else "fp32 kernels",
+               "config": {"workload": cw.name, "B": cw.B, "H": cw.H, "L": cw.L, "d_k": cw.d_k,
+                          "d_v": cw.d_v, "chunk": cw.chunk, "groupnorm": cw.groupnorm,
+                          "state_in": cs_in is not None, "input_copies": copies},
+               "roofline": {"bound": bound, "achieved": ach, "peak": pk, "unit": unit_,
+                            "frac": ach / pk, "note": knote, "traffic": None,
+                            "peak_kind": peak_kind,
+                            "algorithmic_flop_per_call": cfl, "algorithmic_bytes_per_call": cby,
+                            "call_tflops": cfl / (cms / 1e3) / 1e12,
+                            "call_frac_of_bf16_peak": cfl / (cms / 1e3) / 1e12 / peak},
+               "kernels_ms_per_step": cstep_ms,
+               "gpu_launches": int(round(nk_ / hook * steps)), "clocks": csampler.summary()}
+        del sets, couts, cws
+        return res
+
+    extra = {}
+    for name, steps_ in (("small", 200), ("msr1p3b", 50)):
+        if name != w.name:
+            extra[name] = bench_config(name, steps_)
 
     # ---------------- decode workload ----------------
     dw = WORKLOADS["decode"]
@@ -426,12 +579,16 @@ def main():
     dsampler = ClockSampler(local)
     barrier()
     with dsampler:
+        dsampler.mark()
         ds.record(stream)
         for t in range(dsteps):
             dstep(t)
         de.record(stream)
         torch.cuda.synchronize()
+        dsampler.mark()
     dms = max_over_ranks(ds.elapsed_time(de) / dsteps, world, dev)
+    dsus = sustained_window(lambda: dstep(0), stream, local, decode_bytes(dw), "GB/s",
+                            peaks["hbm_gbs"])
     dgbs = decode_bytes(dw) / (dms / 1e3) / 1e9
     decode = {"metric": "decode state GB/s", "value": replica_throughput(dgbs, 1.0, world), "unit": "GB/s",
               "ms_per_step": dms, "steps": dsteps,
@@ -443,7 +600,7 @@ def main():
                            "traffic": profiled_traffic("decode_step", "decode",
                                                        ("kernels_simt.cuh", "common.cuh")),
                            "peak_kind": peak_kind},
-              "gpu_launches": dsteps, "clocks": dsampler.summary()}
+              "gpu_launches": dsteps, "clocks": dsampler.summary(), "sustained": dsus}
     del dinp, dstate
 
     # ---------------- row-normalised decay variant on the chunkwise output ----------------
@@ -635,11 +792,18 @@ def main():
                          "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
                          "algorithmic_flop_per_launch": flops,
                          "algorithmic_bytes_per_launch": chunk_bytes(w),
-                         "launch_ms": top_ms},
+                         "launch_ms": top_ms,
+                         "call_achieved": flops / (ms / args.steps / 1e3) / 1e12,
+                         "call_frac": flops / (ms / args.steps / 1e3) / 1e12 / peak,
+                         "call_note": "the whole ret_chunkwise call (every kernel it launches) "
+                                      "against the same peak"},
             "kernels_ms": {n: statistics.mean(t) for n, t in per_kernel.items()},
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": sampler.summary(),
+            "sustained": sustained,
             "decode": decode,
+            "small": extra.get("small"),
+            "msr1p3b": extra.get("msr1p3b"),
             "backward": backward,
             "decay_row_norm": row_norm,
             "e2e": e2e,

@@ -147,8 +147,11 @@ int ret_chunk_size(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, i
  * exits.  Arguments as ret_chunkwise (all data pointers still come from the
  * caller).  A problem whose plan needs more scratch than the array holds
  * (ret_chunkwise_plan's workspace_bytes) returns RET_EWORKSPACE with no
- * launch.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current), so make that first call
+ * launch.  Every call made outside stream capture looks the array's device
+ * address up afresh (cudaGetSymbolAddress, with the caller's device
+ * current), so a cudaDeviceReset or a re-created context is picked up; a
+ * call made while its stream is capturing reuses the address found by the
+ * last uncaptured call on that device, so make one call on each device
  * before any stream capture.  All calls share the one array and it keeps
  * whatever the previous call left; every kernel that reads it writes it
  * first, so nothing needs clearing, but calls that can overlap on the GPU

@@ -421,17 +421,78 @@ __global__ void __launch_bounds__(256) decode_step_kernel(
 // host's double-precision log2 γ, which keeps full relative precision when
 // γ is close to 1.  One block of 128 threads per row.
 // ---------------------------------------------------------------------------
-template <typename T>
-__global__ void __launch_bounds__(128) decay_row_norm_kernel(T* __restrict__ out, CallConsts cc,
-                                                             int H, int L, int d_v, float pos0) {
-  const size_t row = blockIdx.x;
+__device__ __forceinline__ float decay_row_sum(const CallConsts& cc, size_t row, int H, int L,
+                                               float pos0) {
   const int t = static_cast<int>(row % L);
   const int h = static_cast<int>((row / L) % H);
   const float lg = cc.lg2g[h] * 0.69314718f;   // ln γ
   const float n1 = pos0 + static_cast<float>(t) + 1.f;
-  const float r = lg == 0.f ? n1 : expm1f(n1 * lg) / expm1f(lg);
+  return lg == 0.f ? n1 : expm1f(n1 * lg) / expm1f(lg);
+}
+
+// Any d_v: one block of 128 threads per row, element by element.
+template <typename T>
+__global__ void __launch_bounds__(128) decay_row_norm_kernel(T* __restrict__ out, CallConsts cc,
+                                                             int H, int L, int d_v, float pos0) {
+  const size_t row = blockIdx.x;
+  const float inv = 1.f / decay_row_sum(cc, row, H, L, pos0);
   T* o = out + row * d_v;
-  for (int c = threadIdx.x; c < d_v; c += blockDim.x) o[c] = from_f32<T>(to_f32(o[c]) / r);
+  for (int c = threadIdx.x; c < d_v; c += blockDim.x) o[c] = from_f32<T>(to_f32(o[c]) * inv);
+}
+
+// Rows of a whole number of 16-byte vectors (vpr per row): each warp takes 32
+// consecutive rows, which are one contiguous run of 32·vpr vectors; lane i
+// computes 1/r of row i once, and the run is rewritten in place with 16-byte
+// accesses, eight vectors in flight per lane, each multiplied by the 1/r of
+// its row (a warp shuffle).  The row of vector e of the run is
+// ⌊(e + ½)/vpr⌋ evaluated with one fp32 multiply: e < 32·vpr ≤ 2^14, so the
+// product's rounding error (< 2^-9) stays far below the ½/vpr ≥ 2^-10
+// distance of the exact quotient to the next integer.  Grid-stride over
+// the groups of 32 rows.
+template <typename T>
+__device__ __forceinline__ uint4 scale_vec(uint4 x, float s);
+template <>
+__device__ __forceinline__ uint4 scale_vec<float>(uint4 x, float s) {
+  return make_uint4(__float_as_uint(__uint_as_float(x.x) * s), __float_as_uint(__uint_as_float(x.y) * s),
+                    __float_as_uint(__uint_as_float(x.z) * s), __float_as_uint(__uint_as_float(x.w) * s));
+}
+template <>
+__device__ __forceinline__ uint4 scale_vec<__nv_bfloat16>(uint4 x, float s) {
+  auto f = [s](uint32_t w) { return pack_bf16x2(bf16lo_to_f32(w) * s, bf16hi_to_f32(w) * s); };
+  return make_uint4(f(x.x), f(x.y), f(x.z), f(x.w));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) decay_row_norm_vec_kernel(uint4* __restrict__ out,
+                                                                 CallConsts cc, int H, int L,
+                                                                 int vpr, size_t rows, float pos0) {
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
+  for (size_t g = static_cast<size_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       g * 32 < rows; g += warps) {
+    const size_t r0 = g * 32;
+    const int nr = static_cast<int>(rows - r0 < 32 ? rows - r0 : 32);
+    const float inv = lane < nr ? 1.f / decay_row_sum(cc, r0 + lane, H, L, pos0) : 1.f;
+    const float rvpr = 1.f / static_cast<float>(vpr);
+    uint4* base = out + r0 * vpr;
+    const int n = nr * vpr;   // vectors of the run
+    for (int e0 = 0; e0 < n; e0 += 32 * U) {
+      uint4 x[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + 32 * u + lane;
+        if (e < n) x[u] = __ldcs(base + e);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int e = e0 + 32 * u + lane;
+        const int row = static_cast<int>((static_cast<float>(e < n ? e : 0) + 0.5f) * rvpr);
+        const float s = __shfl_sync(0xffffffffu, inv, row);
+        if (e < n) __stcs(base + e, scale_vec<T>(x[u], s));
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------

@@ -971,20 +971,28 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
 }
 
 // Scratch of ret_chunkwise_noalloc: part of this module's device image, so
-// using it allocates nothing at call time.  Its device address is looked up
-// once per device (with that device current) and cached.
+// using it allocates nothing at call time.  In host code the array's name is
+// only a stand-in; its device address comes from cudaGetSymbolAddress with
+// the caller's device current.  The lookup is repeated on every call made
+// outside stream capture, so a device reset or a re-created primary context
+// (which reloads the module and may move the array) never leaves a stale
+// address behind.  A call made while its stream is capturing reuses the
+// address that the last uncaptured call on that device found (the lookup may
+// have to load the module, which does not belong inside a capture).
 __device__ __align__(256) unsigned char g_noalloc_scratch[RET_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 
-ret_status noalloc_scratch(void** out) {
+ret_status noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return RET_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return RET_EUNSUPPORTED;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return RET_ECUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone || !g_noalloc_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return RET_ECUDA;
@@ -1156,7 +1164,7 @@ ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, re
   const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn));
   if (p.bytes > static_cast<size_t>(RET_NOALLOC_SCRATCH_BYTES)) return RET_EWORKSPACE;
   void* scratch = nullptr;
-  if ((s = noalloc_scratch(&scratch)) != RET_OK) return s;
+  if ((s = noalloc_scratch(stream, &scratch)) != RET_OK) return s;
   return ret_chunkwise(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,
                        state_out, out, out_dt, gn, scratch, RET_NOALLOC_SCRATCH_BYTES, stream);
 }
@@ -1410,6 +1418,19 @@ ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, i
     cc.lg2g[h] = static_cast<float>(std::log2(static_cast<double>(gamma[h])));
   }
   Mark m("decay_row_norm", stream);
+  const int esz = out_dt == RET_F32 ? 4 : 2;
+  if ((static_cast<size_t>(d_v) * esz) % 16 == 0) {   // whole 16-byte vectors per row
+    const int vpr = d_v * esz / 16;
+    const size_t groups = (static_cast<size_t>(rows) + 31) / 32;
+    const unsigned grid = static_cast<unsigned>(std::min<size_t>((groups + 7) / 8, 148 * 8));
+    if (out_dt == RET_F32)
+      simt::decay_row_norm_vec_kernel<float><<<grid, 256, 0, stream>>>(
+          static_cast<uint4*>(out), cc, H, L, vpr, static_cast<size_t>(rows), static_cast<float>(pos0));
+    else
+      simt::decay_row_norm_vec_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+          static_cast<uint4*>(out), cc, H, L, vpr, static_cast<size_t>(rows), static_cast<float>(pos0));
+    return last_launch();
+  }
   if (out_dt == RET_F32)
     simt::decay_row_norm_kernel<float><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
         static_cast<float*>(out), cc, H, L, d_v, static_cast<float>(pos0));

@@ -118,10 +118,12 @@ def test_groupnorm_fp32_with_affine():
 def test_small_workload_all_heads():
     w = WORKLOADS["small"]
     inp = make_inputs(w, seed=0)
-    ref_o, _ = _oracle_full(inp, w, "chunkwise", w.chunk)
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", w.chunk)
     d = _cuda(inp)
     o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk)
+    assert R.sync_status() == R.RET_OK
     assert_close(gpu_np(o), ref_o, torch.bfloat16, "small out")
+    assert_close(gpu_np(s), ref_s, torch.bfloat16, "small state")
 
 
 @pytest.mark.parametrize("d_k,d_v,L,H", [(64, 128, 128, 1), (128, 128, 384, 2), (256, 256, 512, 2),
@@ -151,8 +153,8 @@ def test_tc_matches_fp32_kernels():
                                state_in=d["state_in"], out_dtype=torch.float32)
     finally:
         R.force_path(0)
-    assert rel_fro(gpu_np(o_tc), gpu_np(o_f)) < BF16_TOL
-    assert rel_fro(gpu_np(s_tc), gpu_np(s_f)) < BF16_TOL
+    assert_close(gpu_np(o_tc), gpu_np(o_f), torch.bfloat16, "tensor cores vs fp32 kernels, out")
+    assert_close(gpu_np(s_tc), gpu_np(s_f), torch.bfloat16, "tensor cores vs fp32 kernels, state")
 
 
 @pytest.mark.parametrize("path", [0, 2])
@@ -359,20 +361,24 @@ def test_tc_parallel_groupnorm_and_causality():
 
 
 # -------------------------------------------------------- full workloads --
-def test_msr1p3b_groupnorm_sampled_heads():
+def test_msr1p3b_groupnorm_all_heads():
+    """The 1.3B-shape workload (GroupNorm on) against the oracle on all 64 (b, h)."""
     w = WORKLOADS["msr1p3b"]
     inp = make_inputs(w, seed=0)
     d = _cuda(inp)
     o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
                        gn={"eps": w.gn_eps}, return_state=False)
     assert R.sync_status() == R.RET_OK
-    for b, h in ((0, 0), (3, 5), (7, 7)):
-        q, k, v, s, g, th = head_slice(inp, b, h)
-        ref, _ = O.retention(q, k, v, g, th, 0, s, "chunkwise", w.chunk, {"eps": w.gn_eps})
-        assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref, torch.bfloat16, f"1.3B (b={b},h={h})")
+    og = gpu_np(o)
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v, s, g, th = head_slice(inp, b, h)
+            ref, _ = O.retention(q, k, v, g, th, 0, s, "chunkwise", w.chunk, {"eps": w.gn_eps})
+            assert_close(og[b:b + 1, h:h + 1], ref, torch.bfloat16, f"1.3B (b={b},h={h})")
 
 
-def test_msr7b_sampled_heads():
+def test_msr7b_all_heads():
+    """The 7B-shape workload against the oracle on all 32 (b, h), out and state."""
     w = WORKLOADS["msr7b"]
     inp = make_inputs(w, seed=0)
     d = _cuda(inp)
@@ -385,11 +391,13 @@ def test_msr7b_sampled_heads():
     assert R.sync_status() == R.RET_OK
     assert torch.equal(s, s2) and torch.equal(o, o2)
     del o2, s2
-    for b, h in ((0, 0), (1, 15)):
-        q, k, v, si, g, th = head_slice(inp, b, h)
-        ref_o, ref_s = O.retention(q, k, v, g, th, 0, si, "chunkwise", w.chunk)
-        assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref_o, torch.bfloat16, f"7B out (b={b},h={h})")
-        assert_close(gpu_np(s[b:b + 1, h:h + 1]), ref_s, torch.bfloat16, f"7B state (b={b},h={h})")
+    og, sg = gpu_np(o), gpu_np(s)
+    for b in range(w.B):
+        for h in range(w.H):
+            q, k, v, si, g, th = head_slice(inp, b, h)
+            ref_o, ref_s = O.retention(q, k, v, g, th, 0, si, "chunkwise", w.chunk)
+            assert_close(og[b:b + 1, h:h + 1], ref_o, torch.bfloat16, f"7B out (b={b},h={h})")
+            assert_close(sg[b:b + 1, h:h + 1], ref_s, torch.bfloat16, f"7B state (b={b},h={h})")
 
 
 # --------------------------------------------------------------- gradients --
@@ -514,6 +522,7 @@ def test_backward_msr7b_sampled_heads():
     ("bf16", 256, 256, 300, 128, 0, True),     # tensor-core output, ragged
     ("bf16", 128, 128, 256, 128, 7, False),
     ("f32", 16, 24, 70, 16, 500, True),        # fp32 kernels
+    ("bf16", 32, 36, 100, 32, 3, True),        # rows of 72 bytes: the element-wise pass
 ])
 def test_decay_row_norm_vs_oracle(dtype, d_k, d_v, L, chunk, pos0, state):
     w, inp = _custom(2, 3, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0, seed=L + pos0)
@@ -556,10 +565,13 @@ def test_decode_1024_steps_vs_chunkwise_and_oracle():
     v = inp["v"].permute(1, 2, 0, 3).contiguous()
     oc, sc = R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=128, state_in=S0)
     od = outs.permute(1, 2, 0, 3)
-    assert rel_fro(gpu_np(od), gpu_np(oc)) <= BF16_TOL
-    assert rel_fro(gpu_np(st), gpu_np(sc)) <= BF16_TOL
-    # two sampled heads against the float64 recurrent form
-    for b, h in ((0, 0), (77, 9)):
+    assert_close(gpu_np(od), gpu_np(oc), torch.bfloat16, "decode vs chunkwise, out")
+    assert_close(gpu_np(st), gpu_np(sc), torch.bfloat16, "decode vs chunkwise, state")
+    # 17 heads against the float64 recurrent form: the even heads of batch row
+    # 0, the odd heads of row 127 (so the first and the last (b, h)) and one
+    # in between
+    heads = [(0, h) for h in range(w.H)[::2]] + [(127, h) for h in range(w.H)[1::2]] + [(77, 9)]
+    for b, h in heads:
         ref_o, ref_s = O.retention(to_f64(q[b:b + 1, h:h + 1]), to_f64(k[b:b + 1, h:h + 1]),
                                    to_f64(v[b:b + 1, h:h + 1]), inp["gamma"][h:h + 1].astype(np.float64),
                                    inp["theta"].astype(np.float64), 0, to_f64(S0[b:b + 1, h:h + 1]),
