@@ -461,6 +461,48 @@ def main():
     peak = peaks["bf16_tflops"]
     traffic = profiled_traffic(top)
 
+    # ---------------- the same call in the compact-workspace mode ----------------
+    # For comparison: ret_chunkwise given only ret_chunkwise_plan_compact's
+    # workspace runs the Θ prologue inside the chunk launch (producer CTAs
+    # and an L2-resident ring) instead of the front pass.
+    def compact_line(steps=20):
+        _, cb = R.plan("chunkwise_compact", torch.bfloat16, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk,
+                       gamma=inp["gamma"])
+        if cb >= ws_bytes:
+            return None
+        cws_ = torch.empty(max(cb, 1), dtype=torch.uint8, device=dev)
+        fargs = list(cargs)
+        fargs[18], fargs[19] = vp(cws_), cb
+
+        def fstep():
+            st_ = lib.ret_chunkwise(*fargs)
+            if st_ != _lib.RET_OK:
+                raise RuntimeError(f"ret_chunkwise (compact workspace) returned {st_}")
+
+        for _ in range(3):
+            fstep()
+        torch.cuda.synchronize()
+        fs_, fe_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fs_.record(stream)
+        lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+        for i_ in range(steps):
+            fstep()
+            if i_ + 1 == 8:
+                nf = lib.ret_profile_end()
+        fe_.record(stream)
+        torch.cuda.synchronize()
+        fper = {}
+        for i_ in range(nf):
+            fper.setdefault(lib.ret_profile_kernel(i_).decode(), []).append(
+                evs[2 * i_].elapsed_time(evs[2 * i_ + 1]))
+        del cws_
+        return {"ms_per_step": fs_.elapsed_time(fe_) / steps, "steps": steps, "workspace_bytes": cb,
+                "kernels_ms": {n: statistics.mean(t) for n, t in fper.items()},
+                "note": "ret_chunkwise with ret_chunkwise_plan_compact's workspace: the rotation "
+                        "inside the chunk launch (producer CTAs, L2 ring), for comparison"}
+
+    compact = compact_line()
+
     # ---------------- the Small and 1.3B-shape workloads ----------------
     def bench_config(name, steps):
         """Time ret_chunkwise on one more workload: tokens/s, per-kernel times and
@@ -801,6 +843,8 @@ def main():
             "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": sampler.summary(),
             "sustained": sustained,
+            "compact_workspace_mode": compact,
+            "workspace_bytes": ws_bytes,
             "decode": decode,
             "small": extra.get("small"),
             "msr1p3b": extra.get("msr1p3b"),

@@ -98,7 +98,8 @@ typedef enum {
  * with ΔS_i accumulated from zero; ret_chunkwise_scan uses the same order,
  * so the two layouts return bit-identical state_out.
  * workspace: DEVICE scratch of at least ret_chunkwise_plan(...)->bytes
- * (NULL allowed when that is 0).  The required size depends on the path.
+ * (NULL allowed when that is 0), or of at least ret_chunkwise_plan_compact's
+ * bytes for the compact mode.  The required size depends on the path.
  * ------------------------------------------------------------------------ */
 ret_status ret_chunkwise(const void* q, const void* k, const void* v, ret_dtype in_dt,
                          const float* gamma, const float* theta,
@@ -126,6 +127,26 @@ ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H,
                               int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
                               int* path, size_t* workspace_bytes);
 
+/* The smallest workspace ret_chunkwise (and ret_chunkwise_rowpos) accepts
+ * for these arguments.  On the tensor-core path with CTA pairs (d_k 128 or
+ * 256, an even number of 128-wide d_v tiles) this is the compact mode: the
+ * Θ prologue runs inside the chunk launch — producer CTAs on the SMs that
+ * the consumer pairs leave free rotate q and k into a ring of 4 chunk slots
+ * per head, which stays in L2 — instead of as a front pass that writes the
+ * rotated Q′ and K̂′ of the whole sequence.  Workspace: the ring (4 chunks
+ * of Q′ and K̂′ for at most 128/(d_v/128) heads), an angle table
+ * [L][d_k/2] (cos, sin) and the same staging buffers as the plan's (25 MB at
+ * the 7B shape against 268 MB).  ret_chunkwise takes this mode by itself
+ * whenever its workspace is smaller than ret_chunkwise_plan's bytes but at
+ * least these; the results are bit-identical to the front-pass mode's, and
+ * it runs about 2.3× slower at the 7B shape (the producers' share of the SMs
+ * cannot move and rotate q, k as fast as a front pass on all SMs).  Where
+ * the ring is not smaller (sequences of a few chunks) and on every other
+ * path it returns the same bytes as ret_chunkwise_plan. */
+ret_status ret_chunkwise_plan_compact(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                      int d_k, int d_v, int chunk, ret_dtype out_dt,
+                                      int gn_enabled, int* path, size_t* workspace_bytes);
+
 /* Chunk length for a chunkwise call of this shape: 128 (the tensor-core
  * tile) wherever the tensor-core path applies, otherwise b = round(√L), the
  * square-root balance of the RetNet 保留网络 explainer (分块循环: n/b chunks
@@ -145,8 +166,9 @@ int ret_chunk_size(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, i
  * RET_NOALLOC_SCRATCH_BYTES that lives in the library's own device image.
  * Every GPU that loads the library holds that array until the process
  * exits.  Arguments as ret_chunkwise (all data pointers still come from the
- * caller).  A problem whose plan needs more scratch than the array holds
- * (ret_chunkwise_plan's workspace_bytes) returns RET_EWORKSPACE with no
+ * caller).  It runs the front-pass mode when ret_chunkwise_plan's bytes fit
+ * in the array, else the compact mode when ret_chunkwise_plan_compact's
+ * bytes do; a problem that fits neither returns RET_EWORKSPACE with no
  * launch.  Every call made outside stream capture looks the array's device
  * address up afresh (cudaGetSymbolAddress, with the caller's device
  * current), so a cudaDeviceReset or a re-created context is picked up; a

@@ -43,6 +43,8 @@ SIGNATURES = {
     "ret_chunkwise_backward_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
     "ret_chunk_size": (_i, [_i, _fp, _i, _i, _i, _i]),
     "ret_chunkwise_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
+    "ret_chunkwise_plan_compact": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i),
+                                        C.POINTER(_sz)]),
     "ret_chunkwise_scan_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
     "ret_parallel_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
     "ret_step": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i64, _vp, _vp, _i,

@@ -102,6 +102,9 @@ def plan(form: str, in_dtype, B, H, L, d_k, d_v, chunk=None, out_dtype=None, gn=
     if form == "chunkwise":
         st = lib.ret_chunkwise_plan(idt, gp, B, H, L, d_k, d_v, chunk, odt, int(bool(gn)),
                                     C.byref(path), C.byref(nbytes))
+    elif form == "chunkwise_compact":
+        st = lib.ret_chunkwise_plan_compact(idt, gp, B, H, L, d_k, d_v, chunk, odt, int(bool(gn)),
+                                            C.byref(path), C.byref(nbytes))
     elif form == "chunkwise_scan":
         st = lib.ret_chunkwise_scan_plan(idt, gp, B, H, L, d_k, d_v, chunk, odt, int(bool(gn)),
                                          C.byref(path), C.byref(nbytes))
@@ -128,7 +131,7 @@ def chunk_size(in_dtype, H, L, d_k, d_v, gamma=None) -> int:
 
 def chunkwise(q, k, v, gamma, theta, chunk: Optional[int] = None, pos0: int = 0, state_in=None,
               return_state: bool = True, out=None, out_dtype=None, gn=None, workspace=None,
-              stream=None, layout: str = "carry", state_out=None):
+              stream=None, layout: str = "carry", state_out=None, compact: bool = False):
     """Chunkwise retention.  Returns (out, state_out or None).
 
     chunk=None takes ret_chunk_size's choice.
@@ -136,6 +139,8 @@ def chunkwise(q, k, v, gamma, theta, chunk: Optional[int] = None, pos0: int = 0,
     layout="scan" runs ret_chunkwise_scan (chunk-parallel then scan).
     pos0 is one start position, or a sequence of B start positions (one per
     batch row: ret_chunkwise_rowpos, carry layout).
+    compact=True allocates only ret_chunkwise_plan_compact's workspace (the
+    Θ prologue inside the chunk launch where that mode applies).
     out / state_out / workspace may be given to avoid allocations.
     """
     lib = load()
@@ -153,8 +158,8 @@ def chunkwise(q, k, v, gamma, theta, chunk: Optional[int] = None, pos0: int = 0,
     if state_out is None and return_state:
         state_out = torch.empty((B, H, d_k, d_v), dtype=torch.float32, device=q.device)
     gns, keep = _gn_struct(gn, H, d_v, q.device)
-    _, nbytes = plan("chunkwise_scan" if layout == "scan" else "chunkwise", q.dtype, B, H, L, d_k,
-                     d_v, chunk, odtype, bool(gn), gamma=garr)
+    form = "chunkwise_scan" if layout == "scan" else ("chunkwise_compact" if compact else "chunkwise")
+    _, nbytes = plan(form, q.dtype, B, H, L, d_k, d_v, chunk, odtype, bool(gn), gamma=garr)
     wsp, wsn, ws = _workspace(nbytes, q.device, workspace)
     if np.ndim(pos0) == 1:   # one start position per batch row
         if layout != "carry":

@@ -81,26 +81,88 @@ struct Cfg {
   static constexpr uint32_t T_COLS = (128 + DK + DK / 2) <= 256 ? 256 : 512;
 };
 
+// Every field has a default (zero / null), so a ChunkArgs built field by
+// field never carries garbage into a mode it does not set up.
 struct ChunkArgs {
-  const float* state_in;   // per grid row [DK][d_v], or nullptr
-  float* state_out;        // or nullptr
-  void* out;               // [BH][seq_len][d_v] bf16, or fp32 when out_f32; nullptr: no output
-  int out_f32;
-  int H, d_v;
-  int nchunks;             // chunks this CTA walks
+  const float* state_in = nullptr;   // per grid row [DK][d_v], or nullptr
+  float* state_out = nullptr;        // or nullptr
+  void* out = nullptr;               // [BH][seq_len][d_v] bf16, or fp32 when out_f32; nullptr: no output
+  int out_f32 = 0;
+  int H = 0, d_v = 0;
+  int nchunks = 0;                   // chunks this CTA walks
   // One sequence: seq_len tokens (any length), seq_chunks chunks of 128,
   // seq_lp = 128·seq_chunks rows of it in the rotated Q′ / K̂′ workspace
   // (rows past seq_len are zero).  The last chunk has seq_len − 128·(seq_chunks−1)
   // tokens and carries with γ^that instead of γ^128.
-  int seq_len, seq_lp, seq_chunks;
-  void* tail_out;          // staging [sequences][128][d_v] (out's type) for a short
-                           // last chunk, or nullptr when seq_len is a multiple of 128
+  int seq_len = 0, seq_lp = 0, seq_chunks = 0;
+  void* tail_out = nullptr;          // staging [sequences][128][d_v] (out's type) for a short
+                                     // last chunk, or nullptr when seq_len is a multiple of 128
   // Chunk-parallel layout: the rows of grid.y are (sequence, chunk) pairs of
   // one chunk each: sequence = blockIdx.y / seq_div, chunk = blockIdx.y % seq_div,
   // head = sequence % H.  raw_ds: state_out receives the chunk's ΔS itself
   // instead of fmaf(γ^b, S, ΔS).
-  int seq_div, raw_ds;
+  int seq_div = 1, raw_ds = 0;
+  // Ring mode of the pair kernel (ring > 0, carried layout only): grid rows
+  // [0, ring_prod_rows) are producer CTAs that rotate raw q, k (read through
+  // their own tensor maps) into `ring` chunk slots per head — ring_q / ring_k
+  // [ring_heads][ring][128][d_k] bf16 — and the rows after them are the
+  // consumer pairs of heads ring_bh0 + (row − ring_prod_rows).  ring_flags
+  // holds ready[ring] (producer CTAs done with a slot's chunk, cumulative) and
+  // consumed[ring] (consumer pairs done loading it, cumulative); ring_cs is
+  // the (cos, sin) table [seq_len][d_k/2]; ring_nbuf the producers' shared-
+  // memory buffers.
+  int ring = 0, ring_prod_rows = 0, ring_heads = 0, ring_bh0 = 0, ring_npairs = 0, ring_nbuf = 0;
+  uint32_t* ring_flags = nullptr;
+  __nv_bfloat16* ring_q = nullptr;
+  __nv_bfloat16* ring_k = nullptr;
+  const float2* ring_cs = nullptr;
 };
+
+// ---------------------------------------------------------------------------
+// One 32-bit word (an interleaved pair x_{2i}, x_{2i+1} in bf16) rotated by
+// the angle with cosine c and sine s and scaled by w, rounded to bf16:
+//   Q″ pair: w·(a·c − b·s), w·(a·s + b·c)     (w = ω for Q″, 1 for Q′)
+//   K̂′ pair: a·(zc) − b·(zs), a·(zs) + b·(zc) (z = d_k^{-1/2}·ζ, zc = z·c, zs = z·s)
+// Every operation is rounded explicitly (no contraction left to the
+// compiler), so the front pass and the ring producers of the chunk kernel
+// produce the same bits from the same inputs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t rot_q_word(uint32_t w, float c, float s, float wq) {
+  const float a = bf16lo_to_f32(w), b = bf16hi_to_f32(w);
+  const float x = __fmaf_rn(a, c, __fmul_rn(-b, s));
+  const float y = __fmaf_rn(a, s, __fmul_rn(b, c));
+  return pack_bf16x2(__fmul_rn(wq, x), __fmul_rn(wq, y));
+}
+__device__ __forceinline__ uint32_t rot_k_word(uint32_t w, float zc, float zs) {
+  const float a = bf16lo_to_f32(w), b = bf16hi_to_f32(w);
+  return pack_bf16x2(__fmaf_rn(a, zc, __fmul_rn(-b, zs)), __fmaf_rn(a, zs, __fmul_rn(b, zc)));
+}
+// Per-row factors of the folded form for local position t of a sequence of
+// L tokens (chunks of 128, the last one of length bc): ζ·d_k^{-1/2} for K̂′
+// and ω for Q″ (1 when the ω fold is off).
+__device__ __forceinline__ void row_factors(const CallConsts& cc, int h, int t, int L, int Lp, int chunk,
+                                            int fold_omega, float& zk, float& wq) {
+  const int bc = (t / chunk == Lp / chunk - 1) ? L - (Lp - chunk) : chunk;   // length of t's chunk
+  const float e = static_cast<float>(bc - 1 - (t % chunk));
+  const float ew = static_cast<float>((t % chunk) + 1 - bc);
+  zk = __fmul_rn(cc.kscale, gpow(cc.lg2g[h], e));
+  wq = fold_omega ? gpow(cc.lg2g[h], ew) : 1.f;
+}
+
+// ---------------------------------------------------------------------------
+// (cos, sin) of the rotation angle (pos0 + t)·θ_i for t < L, i < d/2:
+// cs[t][i], the table the ring producers read (one accurate sincos per
+// (position, pair) for the whole call).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) angle_table_kernel(float2* __restrict__ cs, CallConsts cc,
+                                                          int L, int half, float pos0) {
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<size_t>(L) * half) return;
+  const int t = static_cast<int>(idx / half), i = static_cast<int>(idx % half);
+  float c, s;
+  angle_cs(pos0 + static_cast<float>(t), cc.theta[i], c, s);
+  cs[idx] = make_float2(c, s);
+}
 
 // ---------------------------------------------------------------------------
 // Front pass: Q′ = R(nθ)q and K̂′ = d_k^{-1/2}·ζ_{t mod b}·R(nθ)k in bf16.
@@ -136,9 +198,6 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
     }
     return;
   }
-  const int bc = (t / chunk == Lp / chunk - 1) ? L - (Lp - chunk) : chunk;   // length of t's chunk
-  const float e = static_cast<float>(bc - 1 - (t % chunk));
-  const float ew = static_cast<float>((t % chunk) + 1 - bc);
   const size_t hstride = static_cast<size_t>(L) * d;   // input elements between heads
   const size_t off0 = static_cast<size_t>(t) * d + 8 * cidx;
   // Heads [bh_lo, bh_hi) whose rows start at position `start`.
@@ -160,18 +219,15 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
       for (int uu = 0; uu < U; ++uu) {
         const int bh = bh0 + uu;
         if (bh >= bh_hi) break;
-        const float zk = cc.kscale * gpow(cc.lg2g[bh % H], e);
-        const float wq = fold_omega ? gpow(cc.lg2g[bh % H], ew) : 1.f;
+        float zk, wq;
+        row_factors(cc, bh % H, t, L, Lp, chunk, fold_omega, zk, wq);
         const uint32_t qw[4] = {qv[uu].x, qv[uu].y, qv[uu].z, qv[uu].w};
         const uint32_t kw[4] = {kv[uu].x, kv[uu].y, kv[uu].z, kv[uu].w};
         uint32_t qr[4], kr[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float a = bf16lo_to_f32(qw[u]), b = bf16hi_to_f32(qw[u]);
-          qr[u] = pack_bf16x2(wq * (a * c[u] - b * s[u]), wq * fmaf(a, s[u], b * c[u]));
-          const float ka = bf16lo_to_f32(kw[u]), kb = bf16hi_to_f32(kw[u]);
-          const float cz = zk * c[u], sz = zk * s[u];
-          kr[u] = pack_bf16x2(ka * cz - kb * sz, fmaf(ka, sz, kb * cz));
+          qr[u] = rot_q_word(qw[u], c[u], s[u], wq);
+          kr[u] = rot_k_word(kw[u], __fmul_rn(zk, c[u]), __fmul_rn(zk, s[u]));
         }
         const size_t off = oofs + static_cast<size_t>(bh) * ostride;
         *reinterpret_cast<uint4*>(qo + off) = make_uint4(qr[0], qr[1], qr[2], qr[3]);

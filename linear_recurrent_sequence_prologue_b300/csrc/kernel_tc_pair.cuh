@@ -47,6 +47,9 @@ using tcc::CH;
 using tcc::NCW;
 using tcc::NTHREADS;
 using tcc::VT;
+using tcc::rot_k_word;
+using tcc::rot_q_word;
+using tcc::row_factors;
 
 enum Bar : int {
   // TMA → MMA (the even CTA's copy counts both CTAs' bytes)
@@ -90,6 +93,140 @@ struct Cfg {
   static constexpr uint32_t T_COLS = 512;
 };
 
+// ---------------------------------------------------------------------------
+// Ring producer (ring mode, grid rows [0, ring_prod_rows); both CTAs of such
+// a cluster are producers).  The P producer CTAs share the rows of every
+// chunk: producer p rotates rows r ≡ p (mod P) of chunk c for all the
+// launch's heads, chunk after chunk.  Per row, warp 16 loads the raw q and k
+// rows of all heads (two 3-D TMA boxes of d_k × 1 × heads, streamed with an
+// evict-first hint) and the row of the angle table into one of ring_nbuf
+// shared-memory buffers; warps 0..15 rotate it (warp w takes heads w, w+16,
+// …; each lane 8 consecutive columns) with the front pass's arithmetic
+// (rot_q_word / rot_k_word / row_factors) into slot c mod R of the ring
+// (angles from the call's table, or, when every batch row has its own start
+// position, from angle_cs per head).
+// Before its first row of chunk c a rotation warp waits until every
+// consumer pair has loaded chunk c − R out of that slot; after its last row
+// of chunk c the CTA publishes the slot (release) once all rotation warps
+// are done.  Rows past the sequence's end are written as zeros.  After a
+// failed wait a warp stops working but still reaches every named barrier.
+// ---------------------------------------------------------------------------
+template <int DK>
+__device__ __forceinline__ void ring_producer(const CUtensorMap* tm_rq, const CUtensorMap* tm_rk,
+                                              const ChunkArgs& a, const CallConsts& cc,
+                                              const RowPos& rp, uint32_t sb) {
+  constexpr int VECS = DK / 8;     // 16-byte vectors per row
+  constexpr int HPW = 32 / VECS;   // heads per warp and round
+  constexpr int NROT = 16;         // rotation warps
+  const int G = a.ring_heads, R = a.ring, NB = a.ring_nbuf;
+  const int P = a.ring_prod_rows * static_cast<int>(gridDim.x);
+  const int p = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+  const int rows_p = (CH - p + P - 1) / P;   // rows r = p, p + P, … of every chunk
+  const int L = a.seq_len, Lp = a.seq_lp;
+  const int total = a.seq_chunks * rows_p;
+  const uint32_t box = static_cast<uint32_t>(G) * DK * 2;
+  const uint32_t stride = (2 * box + DK * 4 + 1023u) & ~1023u;
+  auto buf = [&](int b) { return sb + static_cast<uint32_t>(b) * stride; };
+  const uint32_t bars = sb + static_cast<uint32_t>(NB) * stride;
+  auto full = [&](int b) { return bars + 8u * static_cast<uint32_t>(b); };
+  auto empty = [&](int b) { return bars + 8u * static_cast<uint32_t>(NB + b); };
+  uint32_t* ready = a.ring_flags;
+  uint32_t* consumed = a.ring_flags + R;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < NB; ++b) {
+      mbar_init(full(b), 1);
+      mbar_init(empty(b), NROT);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp == NROT) {
+    // ---- loader ----
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      int issued = -1;
+      for (int n = 0; n < total; ++n) {
+        const int b = n % NB;
+        if (n >= NB && !mbar_wait(empty(b), static_cast<uint32_t>(n / NB - 1) & 1u, 0x501)) break;
+        const int t = (n / rows_p) * CH + p + (n % rows_p) * P;
+        if (t < L) {
+          mbar_arrive_expect_tx(full(b), 2 * box + DK * 4);
+          tma_load_3d_hint(buf(b), tm_rq, 0, t, a.ring_bh0, full(b), pol);
+          tma_load_3d_hint(buf(b) + box, tm_rk, 0, t, a.ring_bh0, full(b), pol);
+          bulk_load_1d(buf(b) + 2 * box, a.ring_cs + static_cast<size_t>(t) * (DK / 2), DK * 4, full(b));
+        } else {
+          mbar_arrive(full(b));   // a padding row: nothing to load
+        }
+        issued = n;
+      }
+      // Never leave with copies still landing in this CTA's shared memory.
+      if (status_aborted())
+        for (int n = issued - NB + 1 > 0 ? issued - NB + 1 : 0; n <= issued; ++n)
+          mbar_wait(full(n % NB), static_cast<uint32_t>(n / NB) & 1u, 0x5f0, kWaitBudgetCycles / 16);
+    }
+  } else if (warp < NROT) {
+    // ---- rotation ----
+    const int cidx = lane % VECS, hsub = lane / VECS;
+    bool alive = true;
+    for (int n = 0; n < total; ++n) {
+      const int b = n % NB;
+      const int c = n / rows_p, ri = n % rows_p;
+      const int r = p + ri * P, t = c * CH + r, slot = c % R;
+      if (alive && ri == 0) {   // this CTA's first row of chunk c: is the slot free?
+        int ok = 1;
+        if (lane == 0)
+          ok = wait_flag_ge(consumed + slot, static_cast<uint32_t>(a.ring_npairs) * static_cast<uint32_t>(c / R),
+                            0x502) ? 1 : 0;
+        alive = __shfl_sync(0xffffffffu, ok, 0) != 0;
+      }
+      if (alive) alive = mbar_wait(full(b), static_cast<uint32_t>(n / NB) & 1u, 0x503);
+      if (alive) {
+        const uint32_t base = buf(b);
+        float cv[4] = {0.f, 0.f, 0.f, 0.f}, sv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (t < L && !rp.on) {   // the call's table (rows with their own start: below)
+          const uint4 c01 = ld_shared_v4(base + 2 * box + cidx * 32);
+          const uint4 c23 = ld_shared_v4(base + 2 * box + cidx * 32 + 16);
+          cv[0] = __uint_as_float(c01.x); sv[0] = __uint_as_float(c01.y);
+          cv[1] = __uint_as_float(c01.z); sv[1] = __uint_as_float(c01.w);
+          cv[2] = __uint_as_float(c23.x); sv[2] = __uint_as_float(c23.y);
+          cv[3] = __uint_as_float(c23.z); sv[3] = __uint_as_float(c23.w);
+        }
+        for (int hl = warp * HPW + hsub; hl < G; hl += NROT * HPW) {
+          const size_t dst = ((static_cast<size_t>(hl) * R + slot) * CH + r) * DK + 8 * cidx;
+          uint4 qo = make_uint4(0u, 0u, 0u, 0u), ko = make_uint4(0u, 0u, 0u, 0u);
+          if (t < L) {
+            if (rp.on) {   // one start position per batch row: angles of this head's row
+              const float pos = rp.p[(a.ring_bh0 + hl) / a.H] + static_cast<float>(t);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) angle_cs(pos, cc.theta[4 * cidx + u], cv[u], sv[u]);
+            }
+            float zk, wq;
+            row_factors(cc, (a.ring_bh0 + hl) % a.H, t, L, Lp, CH, 1, zk, wq);
+            const uint4 qv = ld_shared_v4(base + static_cast<uint32_t>(hl) * DK * 2 + cidx * 16);
+            const uint4 kv = ld_shared_v4(base + box + static_cast<uint32_t>(hl) * DK * 2 + cidx * 16);
+            qo = make_uint4(rot_q_word(qv.x, cv[0], sv[0], wq), rot_q_word(qv.y, cv[1], sv[1], wq),
+                            rot_q_word(qv.z, cv[2], sv[2], wq), rot_q_word(qv.w, cv[3], sv[3], wq));
+            ko = make_uint4(rot_k_word(kv.x, __fmul_rn(zk, cv[0]), __fmul_rn(zk, sv[0])),
+                            rot_k_word(kv.y, __fmul_rn(zk, cv[1]), __fmul_rn(zk, sv[1])),
+                            rot_k_word(kv.z, __fmul_rn(zk, cv[2]), __fmul_rn(zk, sv[2])),
+                            rot_k_word(kv.w, __fmul_rn(zk, cv[3]), __fmul_rn(zk, sv[3])));
+          }
+          *reinterpret_cast<uint4*>(a.ring_q + dst) = qo;
+          *reinterpret_cast<uint4*>(a.ring_k + dst) = ko;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty(b));
+      }
+      if (ri == rows_p - 1) {   // this CTA's last row of chunk c: publish the slot
+        fence_proxy_async_global();
+        named_bar_sync(1, NROT * 32);
+        if (threadIdx.x == 0 && !status_aborted()) red_release_gpu_add(ready + slot, 1);
+      }
+    }
+  }
+}
+
 // grid = (d_v / 128, rows), cluster = (2, 1, 1); block = 576 threads.
 // Warp 0: TMA producer (both CTAs).  Warp 1: pair MMA issuer (even CTA).
 // Warps 2..17: drain warps, as in the single-CTA kernel.
@@ -99,12 +236,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tm_kh,   // K̂′, 64-row boxes
                    const __grid_constant__ CUtensorMap tm_k,    // K̂′, 128-row boxes
                    const __grid_constant__ CUtensorMap tm_v,    // V, 128-row boxes
-                   ChunkArgs args, CallConsts cc) {
+                   const __grid_constant__ CUtensorMap tm_rq,   // ring mode: raw q, boxes d_k × 1 × heads
+                   const __grid_constant__ CUtensorMap tm_rk,   // ring mode: raw k
+                   ChunkArgs args, CallConsts cc, RowPos rp) {
   using C = Cfg<DK>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
+  if (args.ring && static_cast<int>(blockIdx.y) < args.ring_prod_rows) {
+    ring_producer<DK>(&tm_rq, &tm_rk, args, cc, rp, sb);
+    return;
+  }
   const uint32_t sQ = sb + C::OFF_Q, sKQ = sb + C::OFF_KQ, sKV = sb + C::OFF_KV;
   const uint32_t sV = sb + C::OFF_V, sP = sb + C::OFF_P;
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8u * static_cast<uint32_t>(i); };
@@ -115,8 +258,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int bh = blockIdx.y;
+  const int bh = args.ring ? args.ring_bh0 + static_cast<int>(blockIdx.y) - args.ring_prod_rows
+                           : static_cast<int>(blockIdx.y);
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
+  // Row of chunk c of this sequence in the rotated Q′ / K̂′ source: the
+  // padded workspace, or slot c mod R of the ring.
+  auto qrow = [&](int c) -> int {
+    return args.ring ? ((seq - args.ring_bh0) * args.ring + c % args.ring) * CH : seq * args.seq_lp + c * CH;
+  };
   const int h = seq % args.H;
   const int d_v = args.d_v, nch = args.nchunks;
   // γ^{b_c} of chunk c of the sequence (its last chunk may be shorter)
@@ -151,43 +300,57 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // CTA's query half and its key half with all d_k (QK).  Each buffer is
     // refilled as soon as the last product reading it has finished.
     if (lane == 0) {
-      int issued = -1;
+      // last chunk whose loads were issued, per buffer (for the abort path)
+      int iv = -1, ikv = -1, iq = -1, ikq = -1;
       const int yh = 64 * static_cast<int>(rank);
       for (int i = 0; i < nch; ++i) {
-        const int y = seq * args.seq_lp + (c0 + i) * CH;   // row of Q′ / K̂′
-        const int yv = (c0 + i) * CH;                       // row of V within the sequence
+        const int y = qrow(c0 + i);       // row of Q′ / K̂′
+        const int yv = (c0 + i) * CH;     // row of V within the sequence
         const int s = i & 1;
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
         const uint32_t ps = static_cast<uint32_t>((i >> 1) - 1) & 1u;
+        if (args.ring) {   // the producers have published this chunk's slot
+          const int c = c0 + i;
+          if (!wait_flag_ge(args.ring_flags + c % args.ring,
+                            static_cast<uint32_t>(args.ring_prod_rows * static_cast<int>(gridDim.x)) *
+                                static_cast<uint32_t>(c / args.ring + 1),
+                            0x105))
+            break;
+          fence_proxy_async_global();
+        }
         if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), ps, 0x103)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(V_FULL0 + s), 2 * C::V_BYTES);
         for (int b = 0; b < 2; ++b)
           tma_load_3d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, yv, seq, lead_bar(V_FULL0 + s));
+        iv = i;
         if (i > 0 && !mbar_wait(bar(KV_EMPTY), pp, 0x104)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(KV_FULL), 2 * C::KV_BYTES);
         for (int b = 0; b < C::QBOX / 2; ++b)
           tma_load_2d_pair(sKV + b * C::BOX, &tm_k, 64 * (static_cast<int>(rank) * (C::QBOX / 2) + b), y,
                            lead_bar(KV_FULL));
+        ikv = i;
         if (i > 1 && !mbar_wait(bar(Q_EMPTY0 + s), ps, 0x102)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(Q_FULL0 + s), 2 * C::QH_BYTES);
         for (int b = 0; b < C::QBOX; ++b)
           tma_load_2d_pair(sQ + s * C::QH_BYTES + b * C::HBOX, &tm_qh, 64 * b, y + yh, lead_bar(Q_FULL0 + s));
+        iq = i;
         if (i > 0 && !mbar_wait(bar(KQ_EMPTY), pp, 0x101)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(KQ_FULL), 2 * C::KQ_BYTES);
         for (int b = 0; b < C::QBOX; ++b)
           tma_load_2d_pair(sKQ + b * C::HBOX, &tm_kh, 64 * b, y + yh, lead_bar(KQ_FULL));
-        issued = i;
+        ikq = i;
       }
       // Never leave with copies still landing: the even CTA's FULL barriers
-      // count both CTAs' bytes, so it waits (bounded) for the last phases.
-      if (rank == 0 && issued >= 0 && status_aborted()) {
-        for (int c = issued > 0 ? issued - 1 : 0; c <= issued; ++c) {
-          const uint32_t ph = static_cast<uint32_t>(c >> 1) & 1u;
-          mbar_wait(bar(Q_FULL0 + (c & 1)), ph, 0x1f2, kWaitBudgetCycles / 16);
-          mbar_wait(bar(V_FULL0 + (c & 1)), ph, 0x1f3, kWaitBudgetCycles / 16);
-        }
-        mbar_wait(bar(KQ_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f1, kWaitBudgetCycles / 16);
-        mbar_wait(bar(KV_FULL), static_cast<uint32_t>(issued) & 1u, 0x1f4, kWaitBudgetCycles / 16);
+      // count both CTAs' bytes, so it waits (bounded) for the last phase of
+      // every buffer that was loaded (and of the other slot of the doubled ones).
+      if (rank == 0 && status_aborted()) {
+        constexpr long long kB = kWaitBudgetCycles / 16;
+        for (int c = iv > 0 ? iv - 1 : 0; c <= iv; ++c)
+          mbar_wait(bar(V_FULL0 + (c & 1)), static_cast<uint32_t>(c >> 1) & 1u, 0x1f3, kB);
+        for (int c = iq > 0 ? iq - 1 : 0; c <= iq; ++c)
+          mbar_wait(bar(Q_FULL0 + (c & 1)), static_cast<uint32_t>(c >> 1) & 1u, 0x1f2, kB);
+        if (ikv >= 0) mbar_wait(bar(KV_FULL), static_cast<uint32_t>(ikv) & 1u, 0x1f4, kB);
+        if (ikq >= 0) mbar_wait(bar(KQ_FULL), static_cast<uint32_t>(ikq) & 1u, 0x1f1, kB);
       }
     }
   } else if (warp == 1) {
@@ -248,6 +411,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait_cl(bar(Q_FULL0 + s), pq, 0x205)) break;
         if (i > 0 && !mbar_wait_cl(bar(X_FREE), pp, 0x206)) break;
         tc_fence_after();
+        if (args.ring)   // this pair has loaded chunk c0 + i out of its ring slot
+          red_release_gpu_add(args.ring_flags + args.ring + (c0 + i) % args.ring, 1);
         static_for<DK / 16>(issue_qk);
         mma_commit_pair(bar(P_FULL));
         mma_commit_pair(bar(KQ_EMPTY));

@@ -209,25 +209,58 @@ struct Plan {
   // workspace offsets
   size_t off_q = 0, off_k = 0, off_states = 0, off_ofp32 = 0;
   size_t off_tail = 0;   // staging of a short last chunk's outputs (tensor-core path)
+  // Ring mode (carried layout on CTA pairs): off_q / off_k hold the ring of
+  // `ring` chunk slots for ring_heads heads; off_flags its counters; off_cs
+  // the angle table [L][d_k/2] (cos, sin).
+  int ring = 0, ring_heads = 0;
+  size_t off_flags = 0, off_cs = 0;
 };
+
+// Compact-workspace mode of the carried layout on CTA pairs: the Θ prologue
+// runs inside the chunk launch (producer CTAs on the SMs the consumer pairs
+// leave over, writing an L2-resident ring of chunk slots) instead of as a
+// front pass over the whole sequence.  Chunk slots per head in the ring, and
+// the most consumer CTAs one ring launch plans for (148 SMs, about a seventh
+// of them left to the producers; the launch re-checks co-residency with the
+// occupancy query).
+constexpr int kRing = 4;
+constexpr int kRingConsumers = 128;
+constexpr int kRingMaxProducers = 40;
+
+bool ring_mode_ok(int d_k, int d_v) { return tc_pair_ok(d_k, d_v); }
 
 // Grid rows of the tensor-core launches: B·H (carry layout) or B·H·L/128
 // (one chunk per row) must fit gridDim.y.
 constexpr size_t kMaxGridRows = 65535;
 
+// compact: the compact-workspace mode where it applies (carried layout on
+// CTA pairs), else the same plan as without it.
 Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, int d_k, int d_v,
-                    int chunk, bool gn, bool scan = false) {
+                    int chunk, bool gn, bool scan = false, bool compact = false) {
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   const int nch = (L + chunk - 1) / chunk;
   size_t off = 0;
   if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk) &&
-      (scan ? BH * nch : BH) <= kMaxGridRows) {
+      ((compact && !scan && ring_mode_ok(d_k, d_v)) || (scan ? BH * nch : BH) <= kMaxGridRows)) {
     p.path = RET_PATH_TC;
-    // rotated Q′ / K̂′, each sequence padded with zero rows to whole chunks
-    const size_t Lp = static_cast<size_t>(nch) * tcc::CH;
-    p.off_q = off; off += up256(BH * Lp * d_k * 2);
-    p.off_k = off; off += up256(BH * Lp * d_k * 2);
+    if (compact && !scan && ring_mode_ok(d_k, d_v)) {
+      // producer ring: kRing chunk slots of Q″ and K̂′ per head of one launch,
+      // the launch's counters and the call's angle table
+      const int ntiles = d_v / tcc::VT;
+      p.ring = kRing;
+      p.ring_heads = static_cast<int>(std::min<size_t>(BH, std::max(1, kRingConsumers / ntiles)));
+      const size_t slots = static_cast<size_t>(p.ring_heads) * kRing * tcc::CH * d_k * 2;
+      p.off_flags = off; off += 256;
+      p.off_q = off; off += up256(slots);
+      p.off_k = off; off += up256(slots);
+      p.off_cs = off; off += up256(static_cast<size_t>(L) * (d_k / 2) * 8);
+    } else {
+      // rotated Q′ / K̂′, each sequence padded with zero rows to whole chunks
+      const size_t Lp = static_cast<size_t>(nch) * tcc::CH;
+      p.off_q = off; off += up256(BH * Lp * d_k * 2);
+      p.off_k = off; off += up256(BH * Lp * d_k * 2);
+    }
     if (scan) { p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4); }
     if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * static_cast<size_t>(d_v) * 4); }
   } else {
@@ -332,6 +365,174 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
   return last_launch();
 }
 
+// ---------------------------------------------------------------------------
+// Ring mode: the Θ prologue fused into the CTA-pair launch
+// ---------------------------------------------------------------------------
+// Largest number of clusters of two pair-kernel CTAs that can be resident at
+// once on the current device (0 if the query fails), cached per device.
+constexpr int kMaxDev = 64;
+
+template <int DK>
+int pair_max_clusters() {
+  static std::mutex mu;
+  static int cache[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  const uint32_t smem = tcq::Cfg<DK>::SMEM_BYTES;
+  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 128);
+  cfg.blockDim = dim3(tcc::NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tcq::pair_tc_kernel<DK>, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cache[dev] = n;
+  return n;
+}
+
+// [n][rows][cols] bf16 read in boxes of one row of `cols` × `box_n` matrices
+// (no swizzle): the raw q / k rows of the ring producers.
+bool make_map_rows(CUtensorMap* m, const void* base, uint64_t n, uint64_t rows, uint64_t cols,
+                   uint32_t box_n) {
+  if (!get_encode()) return false;
+  cuuint64_t dims[3] = {cols, rows, n};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(cols), 1, box_n};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Carried layout on CTA pairs with the Θ prologue inside the launch.  The
+// heads run in groups sized so that every CTA of a launch is resident at
+// once: per group, producer CTAs (the SMs the consumer pairs leave over, at
+// most kRingMaxProducers) rotate raw q, k into the ring and the consumer
+// pairs read it from there (kernel_tc_pair.cuh, ring_producer).  The ring's
+// counters are cleared before each group's launch.  Q″ and K̂′ are the front
+// pass's values bit for bit, so results equal the front-pass path's.
+template <int DK, typename Tout>
+ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __nv_bfloat16* v,
+                       const CallConsts& cc, int B, int H, int L, int d_v, int64_t pos0,
+                       const float* s_in, float* s_out, Tout* out, const ret_gn* gn, void* ws,
+                       const Plan& p, cudaStream_t st, const RowPos& rp) {
+  using CfgP = tcq::Cfg<DK>;
+  const int BH = B * H;
+  const int nch = (L + tcc::CH - 1) / tcc::CH;
+  const int Lp = nch * tcc::CH;
+  const int ntiles = d_v / tcc::VT;
+  const int ncl = pair_max_clusters<DK>();
+  const int per_row = 2 * ncl / ntiles;          // grid rows that fit at once
+  const int G = std::min(p.ring_heads, per_row - 1);
+  if (G < 1) return RET_EUNSUPPORTED;
+  uint32_t* flags = wsp<uint32_t>(ws, p.off_flags);
+  auto* rq = wsp<__nv_bfloat16>(ws, p.off_q);
+  auto* rk = wsp<__nv_bfloat16>(ws, p.off_k);
+  auto* cs = wsp<float2>(ws, p.off_cs);
+  if (!rp.on) {
+    const size_t n = static_cast<size_t>(L) * (DK / 2);
+    Mark m("angle_table", st);
+    tcc::angle_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        cs, cc, L, DK / 2, static_cast<float>(pos0));
+    if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  }
+  const uint64_t ring_rows = static_cast<uint64_t>(p.ring_heads) * kRing * tcc::CH;
+  CUtensorMap mqh, mkh, mk, mv, mrq, mrk;
+  if (!make_map(&mqh, rq, ring_rows, DK, 64) || !make_map(&mkh, rk, ring_rows, DK, 64) ||
+      !make_map(&mk, rk, ring_rows, DK) ||
+      !make_map3(&mv, v, static_cast<uint64_t>(BH), static_cast<uint64_t>(L), d_v))
+    return RET_ECUDA;
+  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
+  tcc::ChunkArgs a;
+  a.state_in = s_in;
+  a.state_out = s_out;
+  a.out = ofp ? static_cast<void*>(ofp) : static_cast<void*>(out);
+  a.out_f32 = (ofp || sizeof(Tout) == 4) ? 1 : 0;
+  a.H = H;
+  a.d_v = d_v;
+  a.nchunks = nch;
+  a.seq_len = L;
+  a.seq_lp = Lp;
+  a.seq_chunks = nch;
+  a.tail_out = (L % tcc::CH != 0) ? wsp<void>(ws, p.off_tail) : nullptr;
+  a.seq_div = 1;
+  a.raw_ds = 0;
+  a.ring = kRing;
+  a.ring_flags = flags;
+  a.ring_q = rq;
+  a.ring_k = rk;
+  a.ring_cs = cs;
+  const uint32_t smem = CfgP::SMEM_BYTES;
+  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return RET_ECUDA;
+  for (int bh0 = 0; bh0 < BH; bh0 += G) {
+    const int Gl = std::min(G, BH - bh0);
+    const int prod_rows = std::min(per_row - Gl, std::max(1, kRingMaxProducers / ntiles));
+    const uint32_t stride = (2u * Gl * DK * 2 + DK * 4 + 1023u) & ~1023u;
+    const int nbuf = static_cast<int>(std::min<uint32_t>(4, (CfgP::USED - 256) / stride));
+    if (nbuf < 2) return RET_EUNSUPPORTED;
+    if (!make_map_rows(&mrq, q, static_cast<uint64_t>(BH), static_cast<uint64_t>(L), DK, Gl) ||
+        !make_map_rows(&mrk, k, static_cast<uint64_t>(BH), static_cast<uint64_t>(L), DK, Gl))
+      return RET_ECUDA;
+    a.ring_prod_rows = prod_rows;
+    a.ring_heads = Gl;
+    a.ring_bh0 = bh0;
+    a.ring_npairs = Gl * ntiles / 2;
+    a.ring_nbuf = nbuf;
+    if (cudaMemsetAsync(flags, 0, 2 * kRing * sizeof(uint32_t), st) != cudaSuccess) return RET_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ntiles, prod_rows + Gl);
+    cfg.blockDim = dim3(tcc::NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    Mark m("chunk_tc_ring", st);
+    if (cudaLaunchKernelEx(&cfg, tcq::pair_tc_kernel<DK>, mqh, mkh, mk, mv, mrq, mrk, a, cc, rp) !=
+        cudaSuccess)
+      return RET_ECUDA;
+  }
+  if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  if (a.tail_out) {   // the short last chunk's valid rows, from the staging tile
+    const int T = L - (nch - 1) * tcc::CH;
+    const int row_vecs = d_v * (a.out_f32 ? 4 : 2) / 16;
+    const size_t n = static_cast<size_t>(BH) * T * row_vecs;
+    Mark m("tail_copy", st);
+    tcc::tail_copy_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        static_cast<const uint4*>(a.tail_out), static_cast<uint4*>(a.out), BH, T, L, (nch - 1) * tcc::CH,
+        row_vecs);
+    if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  }
+  if (ofp) {
+    const size_t r = static_cast<size_t>(BH) * L;
+    Mark m("groupnorm", st);
+    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
+        ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+  }
+  return last_launch();
+}
+
 // scan = false: one CTA walks all chunks of its (b, h), carrying the state.
 // scan = true: chunk-parallel layout — every chunk's ΔS from zero (one CTA
 // per chunk), the fp32 scan over chunks, then every chunk's outputs from its
@@ -345,6 +546,9 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
                         int64_t pos0, const float* s_in, float* s_out, Tout* out,
                         const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st,
                         const RowPos& rp, bool scan = false, bool parallel = false) {
+  if (p.ring && !scan && !parallel)
+    return d_k == 256 ? run_tc_ring<256, Tout>(q, k, v, cc, B, H, L, d_v, pos0, s_in, s_out, out, gn, ws, p, st, rp)
+                      : run_tc_ring<128, Tout>(q, k, v, cc, B, H, L, d_v, pos0, s_in, s_out, out, gn, ws, p, st, rp);
   const int BH = B * H;
   __nv_bfloat16* qr = wsp<__nv_bfloat16>(ws, p.off_q);
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
@@ -412,7 +616,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     cfg.attrs = at;
     cfg.numAttrs = 1;
     Mark m(name, st);
-    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, args, cc);
+    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, mk, mk, args, cc, rp);
     return e != cudaSuccess ? e : cudaGetLastError();
   };
   auto run = [&](const tcc::ChunkArgs& args, int rows, const char* name) -> cudaError_t {
@@ -847,7 +1051,7 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
     cfg.attrs = at;
     cfg.numAttrs = 1;
     Mark m("bwd_chunk_tc", st);
-    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, g, cc);
+    e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, mk, mk, g, cc, no_rowpos());
     return e != cudaSuccess ? e : cudaGetLastError();
   };
   auto launch = [&](auto kern, uint32_t smem) -> cudaError_t {
@@ -1077,6 +1281,23 @@ ret_status ret_chunkwise_plan(ret_dtype in_dt, const float* gamma, int B, int H,
   return RET_OK;
 }
 
+ret_status ret_chunkwise_plan_compact(ret_dtype in_dt, const float* gamma, int B, int H, int L,
+                                      int d_k, int d_v, int chunk, ret_dtype out_dt, int gn_enabled,
+                                      int* path, size_t* workspace_bytes) {
+  if (!path || !workspace_bytes) return RET_EINVAL;
+  if (in_dt != RET_F32 && in_dt != RET_BF16) return RET_EINVAL;
+  if (out_dt != RET_F32 && out_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1 || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || chunk < 1)
+    return RET_EINVAL;
+  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_enabled != 0);
+  const Plan pc = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_enabled != 0, false, true);
+  const Plan& best = pc.bytes < p.bytes ? pc : p;   // the compact mode only where it is smaller
+  *path = best.path;
+  *workspace_bytes = best.bytes;
+  return RET_OK;
+}
+
 }  // extern "C"
 
 namespace {
@@ -1102,7 +1323,12 @@ ret_status chunkwise_impl(const void* q, const void* k, const void* v, ret_dtype
   if (chunk < 1) return RET_EINVAL;
   CallConsts cc;
   if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
-  const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), scan);
+  Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), scan);
+  if (p.bytes > 0 && workspace && al16(workspace) && workspace_bytes < p.bytes && !scan) {
+    // too short for the front pass: the compact-workspace mode, where it applies
+    const Plan pc = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), false, true);
+    if (pc.ring && workspace_bytes >= pc.bytes) p = pc;
+  }
   if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes || !al16(workspace)))
     return RET_EWORKSPACE;
   if (p.path == RET_PATH_TC) {
@@ -1162,7 +1388,10 @@ ret_status ret_chunkwise_noalloc(const void* q, const void* k, const void* v, re
   if (s != RET_OK) return s;
   if (chunk < 1) return RET_EINVAL;
   const Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn));
-  if (p.bytes > static_cast<size_t>(RET_NOALLOC_SCRATCH_BYTES)) return RET_EWORKSPACE;
+  const Plan pc = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), false, true);
+  if (p.bytes > static_cast<size_t>(RET_NOALLOC_SCRATCH_BYTES) &&
+      pc.bytes > static_cast<size_t>(RET_NOALLOC_SCRATCH_BYTES))
+    return RET_EWORKSPACE;
   void* scratch = nullptr;
   if ((s = noalloc_scratch(stream, &scratch)) != RET_OK) return s;
   return ret_chunkwise(q, k, v, in_dt, gamma, theta, B, H, L, d_k, d_v, pos0, chunk, state_in,

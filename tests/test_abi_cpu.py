@@ -149,27 +149,57 @@ def _plan(lib, in_dt, B, H, L, d_k, d_v, chunk, gn=0, gamma=None):
     return path.value, nb.value
 
 
+def _ring_bytes(heads, L, d_k):
+    """Workspace of the carried layout on CTA pairs: the ring's counters (256 B),
+    4 chunk slots of Q″ and of K̂′ per head of one launch (bf16), the
+    (cos, sin) table [L][d_k/2]."""
+    return 256 + 2 * heads * 4 * 128 * d_k * 2 + L * (d_k // 2) * 8
+
+
+def _plan_compact(lib, in_dt, B, H, L, d_k, d_v, chunk, gn=0):
+    path, nb = C.c_int(0), C.c_size_t(0)
+    st = lib.ret_chunkwise_plan_compact(in_dt, None, B, H, L, d_k, d_v, chunk, in_dt, gn, C.byref(path),
+                                        C.byref(nb))
+    assert st == _lib.RET_OK
+    return path.value, nb.value
+
+
 def test_path_selection(lib):
     # 7B shape: tensor-core path, workspace = rotated Q′ and K̂′ in bf16
-    p, nb = _plan(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128)
-    assert p == _lib.RET_PATH_TC
-    assert nb == 2 * 2 * 16 * 8192 * 256 * 2
-    # the chunk-parallel layout adds one fp32 d_k×d_v state per (b, h, chunk)
+    front = 2 * 2 * 16 * 8192 * 256 * 2
+    assert _plan(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_TC, front)
+    # the compact mode: 32 heads (128 consumer CTAs) per launch in the ring
+    assert _plan_compact(lib, _lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == \
+        (_lib.RET_PATH_TC, _ring_bytes(32, 8192, 256))
+    nb = front
+    # the chunk-parallel layout (front pass) adds one fp32 d_k×d_v state per (b, h, chunk)
     path, nb2 = C.c_int(0), C.c_size_t(0)
     assert lib.ret_chunkwise_scan_plan(_lib.RET_BF16, None, 2, 16, 8192, 256, 512, 128,
                                        _lib.RET_BF16, 0, C.byref(path), C.byref(nb2)) == _lib.RET_OK
     assert path.value == _lib.RET_PATH_TC
-    assert nb2.value == nb + 2 * 16 * 64 * 256 * 512 * 4
+    assert nb2.value == front + 2 * 16 * 64 * 256 * 512 * 4
     # the parallel form of the same shape runs on the tensor cores as well
     assert lib.ret_parallel_plan(_lib.RET_BF16, None, 2, 16, 8192, 256, 512, _lib.RET_BF16, 0, 0,
                                  C.byref(path), C.byref(nb2)) == _lib.RET_OK
-    assert path.value == _lib.RET_PATH_TC and nb2.value == nb   # rotated Q′ / K̂′ only
-    # fp32 inputs, chunk 64, d_v 64 → fp32 kernels
+    assert path.value == _lib.RET_PATH_TC and nb2.value == front   # rotated Q′ / K̂′ only
+    # the ring holds at most 128 consumer CTAs' heads: 64 at d_v = 256, fewer when B·H is smaller
+    assert _plan_compact(lib, _lib.RET_BF16, 8, 16, 2048, 256, 256, 128)[1] == _ring_bytes(64, 2048, 256)
+    assert _plan_compact(lib, _lib.RET_BF16, 1, 3, 1300, 128, 256, 128)[1] == \
+        _ring_bytes(3, 1300, 128) + 3 * 128 * 256 * 4
+    # sequences of no more chunks than the ring holds: the front pass is smaller
+    assert _plan_compact(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128) == \
+        _plan(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128)
+    # no compact mode off the CTA-pair shapes: the same bytes as the plan
+    assert _plan_compact(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128) == \
+        _plan(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128)
+    assert _plan_compact(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16) == _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)
     # a length that is not a multiple of the chunk stays on the tensor cores, with
     # the rotated Q′ / K̂′ padded to whole chunks; the parallel form needs whole blocks
     p, nb = _plan(lib, _lib.RET_BF16, 2, 16, 8000, 256, 512, 128)
     # (+ an fp32 staging tile of 128 rows per sequence for the short last chunk's outputs)
     assert p == _lib.RET_PATH_TC and nb == 2 * 2 * 16 * 8064 * 256 * 2 + 2 * 16 * 128 * 512 * 4
+    assert _plan_compact(lib, _lib.RET_BF16, 2, 16, 8000, 256, 512, 128)[1] == \
+        _ring_bytes(32, 8000, 256) + 2 * 16 * 128 * 512 * 4
     assert lib.ret_parallel_plan(_lib.RET_BF16, None, 2, 16, 8000, 256, 512, _lib.RET_BF16, 0, 0,
                                  C.byref(path), C.byref(nb2)) == _lib.RET_OK
     assert path.value == _lib.RET_PATH_SIMT

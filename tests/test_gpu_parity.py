@@ -242,6 +242,52 @@ def test_tc_pair_kernel_matches_single_cta_kernel(d_k, d_v, L, H):
     assert_close(gpu_np(s), ref_s, torch.bfloat16, "pair state")
 
 
+@pytest.mark.parametrize("B,H,L,d_k,d_v,rowpos", [
+    (2, 2, 1024, 256, 512, False),   # 8 chunks: every ring slot used twice
+    (1, 3, 1300, 256, 256, False),   # 11 chunks, the last of 20 tokens
+    (2, 40, 260, 256, 512, False),   # 80 heads: three launches of 32, 32 and 16 heads
+    (3, 2, 700, 128, 256, True),     # d_k 128, one start position per batch row
+    (1, 2, 900, 256, 256, False),    # 8 chunks, the last of 4 tokens
+])
+def test_compact_workspace_matches_front_pass(B, H, L, d_k, d_v, rowpos):
+    """The compact-workspace mode of the carried layout on CTA pairs (the Θ
+    prologue fused into the launch: producer CTAs rotating q, k into an
+    L2-resident ring of chunk slots) against the same kernels fed by the
+    front pass over the whole sequence, and against the chunk-parallel
+    layout: the same Q″ and K̂′ bits reach the same products, so out and
+    state agree bit for bit."""
+    w, inp = _custom(B, H, L, d_k, d_v, "bf16", 128, std=1.0, state_std=0.1, seed=L + H)
+    d = _cuda(inp)
+    pos = [0, 37, 5000][:B] if rowpos else 13
+    full = R.plan("chunkwise", torch.bfloat16, B, H, L, d_k, d_v, 128)[1]
+    small = R.plan("chunkwise_compact", torch.bfloat16, B, H, L, d_k, d_v, 128)[1]
+    assert small < full
+    res = {}
+    for compact in (True, False):
+        for odt in (torch.bfloat16, torch.float32):
+            res[compact, odt] = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"],
+                                            chunk=128, pos0=pos, state_in=d["state_in"], out_dtype=odt,
+                                            compact=compact)
+            assert R.sync_status() == R.RET_OK
+    for odt in (torch.bfloat16, torch.float32):
+        o, s = res[True, odt]
+        o1, s1 = res[False, odt]
+        assert torch.equal(s, s1), odt
+        assert torch.equal(o, o1), odt
+        if not rowpos:
+            o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128,
+                                 pos0=pos, state_in=d["state_in"], out_dtype=odt, layout="scan")
+            assert torch.equal(s, s2) and torch.equal(o, o2), odt
+    o, s = res[True, torch.float32]
+    for b in range(B):
+        for h in (0, H - 1):
+            one = {k: (v[b:b + 1, h:h + 1] if torch.is_tensor(v) else v) for k, v in inp.items()}
+            one["gamma"] = inp["gamma"][h:h + 1]
+            ref_o, ref_s = _oracle_full(one, w, "chunkwise", 128, pos0=pos[b] if rowpos else pos)
+            assert_close(gpu_np(o[b:b + 1, h:h + 1]), ref_o, torch.bfloat16, f"ring out (b={b},h={h})")
+            assert_close(gpu_np(s[b:b + 1, h:h + 1]), ref_s, torch.bfloat16, f"ring state (b={b},h={h})")
+
+
 @pytest.mark.parametrize("d_k,d_v,L,H", [
     (256, 512, 300, 2),    # pair kernel, short last chunk of 44
     (256, 256, 1000, 1),   # pair kernel, 8 chunks, last of 104

@@ -106,11 +106,42 @@ def test_noalloc_sequence_of_shapes_after_nan_fill():
         _check_against_chunkwise(lib, w, 10 + i, 7, gn)
 
 
-def test_noalloc_rejects_problems_beyond_the_array():
+def test_noalloc_runs_the_7b_shape_in_the_compact_mode():
+    """The 7B-shape problem needs 268 MB of workspace for the front pass but
+    only 25 MB in the compact mode, so it runs from the 32 MiB array; the
+    compact mode feeds the same Q″ and K̂′ bits to the same kernels, so the
+    result equals ret_chunkwise's (front pass, caller workspace) bit for bit,
+    on two calls in a row."""
     lib = R.load()
-    w = Workload("big", 2, 16, 8192, 256, 512, "bf16", 128, 1.0)   # needs 268 MB of scratch
-    q = torch.empty((1,), dtype=torch.bfloat16, device="cuda")
-    inp = {"q": q, "k": q, "v": q, "state_in": None,
+    w = Workload("msr7b", 2, 16, 8192, 256, 512, "bf16", 128, 1.28, state_std=0.1)
+    assert R.plan("chunkwise", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk)[1] > \
+        _lib.RET_NOALLOC_SCRATCH_BYTES
+    assert R.plan("chunkwise_compact", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk)[1] <= \
+        _lib.RET_NOALLOC_SCRATCH_BYTES
+    for seed in (3, 4):
+        inp = make_inputs(w, seed=seed)
+        d = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in inp.items()}
+        ref_o, ref_s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk,
+                                   state_in=d["state_in"])
+        out = torch.full_like(ref_o, float("nan"))
+        s_out = torch.full_like(ref_s, float("nan"))
+        assert _noalloc(lib, d, w, 0, out, s_out) == _lib.RET_OK
+        assert R.sync_status() == R.RET_OK
+        assert torch.equal(out, ref_o) and torch.equal(s_out, ref_s)
+
+
+def test_noalloc_rejects_problems_beyond_the_array():
+    """A problem whose plan needs more scratch than the array holds is
+    refused before any launch.  The buffers are real and full-sized, so even a
+    launch by mistake would stay in bounds."""
+    lib = R.load()
+    w = Workload("big", 2, 16, 8192, 256, 512, "f32", 128, 1.0)   # fp32 path: over 1.5 GB of scratch
+    need = R.plan("chunkwise", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk)[1]
+    assert need > _lib.RET_NOALLOC_SCRATCH_BYTES
+    q = torch.empty((w.B, w.H, w.L, w.d_k), dtype=torch.float32, device="cuda")
+    v = torch.empty((w.B, w.H, w.L, w.d_v), dtype=torch.float32, device="cuda")
+    inp = {"q": q, "k": q, "v": v, "state_in": None,
            "gamma": np.full(w.H, 0.99, np.float32), "theta": np.ones(w.d_k // 2, np.float32)}
-    out = torch.empty((1,), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(v)
     assert _noalloc(lib, inp, w, 0, out, None) == _lib.RET_EWORKSPACE
+    assert R.sync_status() == R.RET_OK
