@@ -230,7 +230,10 @@ __device__ __forceinline__ void ring_producer(const CUtensorMap* tm_rq, const CU
 // grid = (d_v / 128, rows), cluster = (2, 1, 1); block = 576 threads.
 // Warp 0: TMA producer (both CTAs).  Warp 1: pair MMA issuer (even CTA).
 // Warps 2..17: drain warps, as in the single-CTA kernel.
-template <int DK>
+// RING: the compact-workspace instantiation (producer CTAs in the first
+// grid rows, Q′ / K̂′ read from the ring); without it none of that code is
+// compiled in, so the front-pass path keeps its own register allocation.
+template <int DK, bool RING>
 __global__ void __launch_bounds__(NTHREADS, 1)
     pair_tc_kernel(const __grid_constant__ CUtensorMap tm_qh,   // Q′, 64-row boxes
                    const __grid_constant__ CUtensorMap tm_kh,   // K̂′, 64-row boxes
@@ -244,9 +247,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  if (args.ring && static_cast<int>(blockIdx.y) < args.ring_prod_rows) {
-    ring_producer<DK>(&tm_rq, &tm_rk, args, cc, rp, sb);
-    return;
+  if constexpr (RING) {
+    if (static_cast<int>(blockIdx.y) < args.ring_prod_rows) {
+      ring_producer<DK>(&tm_rq, &tm_rk, args, cc, rp, sb);
+      return;
+    }
   }
   const uint32_t sQ = sb + C::OFF_Q, sKQ = sb + C::OFF_KQ, sKV = sb + C::OFF_KV;
   const uint32_t sV = sb + C::OFF_V, sP = sb + C::OFF_P;
@@ -258,13 +263,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int bh = args.ring ? args.ring_bh0 + static_cast<int>(blockIdx.y) - args.ring_prod_rows
-                           : static_cast<int>(blockIdx.y);
+  const int bh = RING ? args.ring_bh0 + static_cast<int>(blockIdx.y) - args.ring_prod_rows
+                     : static_cast<int>(blockIdx.y);
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
   // Row of chunk c of this sequence in the rotated Q′ / K̂′ source: the
   // padded workspace, or slot c mod R of the ring.
   auto qrow = [&](int c) -> int {
-    return args.ring ? ((seq - args.ring_bh0) * args.ring + c % args.ring) * CH : seq * args.seq_lp + c * CH;
+    if constexpr (RING) return ((seq - args.ring_bh0) * args.ring + c % args.ring) * CH;
+    return seq * args.seq_lp + c * CH;
   };
   const int h = seq % args.H;
   const int d_v = args.d_v, nch = args.nchunks;
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = i & 1;
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
         const uint32_t ps = static_cast<uint32_t>((i >> 1) - 1) & 1u;
-        if (args.ring) {   // the producers have published this chunk's slot
+        if constexpr (RING) {   // the producers have published this chunk's slot
           const int c = c0 + i;
           if (!wait_flag_ge(args.ring_flags + c % args.ring,
                             static_cast<uint32_t>(args.ring_prod_rows * static_cast<int>(gridDim.x)) *
@@ -411,7 +417,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait_cl(bar(Q_FULL0 + s), pq, 0x205)) break;
         if (i > 0 && !mbar_wait_cl(bar(X_FREE), pp, 0x206)) break;
         tc_fence_after();
-        if (args.ring)   // this pair has loaded chunk c0 + i out of its ring slot
+        if constexpr (RING)   // this pair has loaded chunk c0 + i out of its ring slot
           red_release_gpu_add(args.ring_flags + args.ring + (c0 + i) % args.ring, 1);
         static_for<DK / 16>(issue_qk);
         mma_commit_pair(bar(P_FULL));

@@ -381,7 +381,7 @@ int pair_max_clusters() {
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] > 0) return cache[dev];
   const uint32_t smem = tcq::Cfg<DK>::SMEM_BYTES;
-  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
@@ -396,7 +396,7 @@ int pair_max_clusters() {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tcq::pair_tc_kernel<DK>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tcq::pair_tc_kernel<DK, true>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
@@ -478,7 +478,7 @@ ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __n
   a.ring_k = rk;
   a.ring_cs = cs;
   const uint32_t smem = CfgP::SMEM_BYTES;
-  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(tcq::pair_tc_kernel<DK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return RET_ECUDA;
   for (int bh0 = 0; bh0 < BH; bh0 += G) {
@@ -509,7 +509,7 @@ ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __n
     cfg.attrs = at;
     cfg.numAttrs = 1;
     Mark m("chunk_tc_ring", st);
-    if (cudaLaunchKernelEx(&cfg, tcq::pair_tc_kernel<DK>, mqh, mkh, mk, mv, mrq, mrk, a, cc, rp) !=
+    if (cudaLaunchKernelEx(&cfg, tcq::pair_tc_kernel<DK, true>, mqh, mkh, mk, mv, mrq, mrk, a, cc, rp) !=
         cudaSuccess)
       return RET_ECUDA;
   }
@@ -621,9 +621,9 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   };
   auto run = [&](const tcc::ChunkArgs& args, int rows, const char* name) -> cudaError_t {
     if (pair && d_k == 256)
-      return launch_pair(tcq::pair_tc_kernel<256>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name);
+      return launch_pair(tcq::pair_tc_kernel<256, false>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name);
     if (pair)
-      return launch_pair(tcq::pair_tc_kernel<128>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name);
+      return launch_pair(tcq::pair_tc_kernel<128, false>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name);
     if (d_k == 256) return launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name);
     if (d_k == 128) return launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
     return launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
@@ -1063,8 +1063,8 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
     return cudaGetLastError();
   };
   cudaError_t e;
-  if (pair && dkF == 256) e = launch_pair(tcq::pair_tc_kernel<256>, tcq::Cfg<256>::SMEM_BYTES);
-  else if (pair) e = launch_pair(tcq::pair_tc_kernel<128>, tcq::Cfg<128>::SMEM_BYTES);
+  if (pair && dkF == 256) e = launch_pair(tcq::pair_tc_kernel<256, false>, tcq::Cfg<256>::SMEM_BYTES);
+  else if (pair) e = launch_pair(tcq::pair_tc_kernel<128, false>, tcq::Cfg<128>::SMEM_BYTES);
   else if (dkF == 256) e = launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES);
   else e = launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES);
   if (e != cudaSuccess) return RET_ECUDA;
