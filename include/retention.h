@@ -83,8 +83,11 @@ typedef struct {
 typedef enum {
   RET_PATH_TC = 1,     /* tcgen05 tensor-core kernels (bf16 inputs)       */
   RET_PATH_SIMT = 2,   /* fp32 FFMA kernels                               */
-  RET_PATH_TC_SINGLE = 3  /* ret_force_path only: the tensor-core path with
+  RET_PATH_TC_SINGLE = 3, /* ret_force_path only: the tensor-core path with
                              one CTA per d_v tile instead of CTA pairs    */
+  RET_PATH_TC_CARRY = 4   /* ret_force_path only: ret_chunkwise keeps the
+                             carried layout where it would take the
+                             chunk-parallel one for a small grid          */
 } ret_path;
 
 /* ------------------------------------------------------------------------

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(HERE, "libretention.so")
 
 RET_OK, RET_EINVAL, RET_EUNSUPPORTED, RET_ECUDA, RET_ETIMEOUT, RET_EWORKSPACE = range(6)
 RET_F32, RET_BF16 = 0, 1
-RET_PATH_TC, RET_PATH_SIMT, RET_PATH_TC_SINGLE = 1, 2, 3
+RET_PATH_TC, RET_PATH_SIMT, RET_PATH_TC_SINGLE, RET_PATH_TC_CARRY = 1, 2, 3, 4
 RET_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 STATUS_NAMES = {

@@ -170,8 +170,10 @@ __global__ void __launch_bounds__(256) angle_table_kernel(float2* __restrict__ c
 // o_j = ω_j (Q′Ŝ + P̂V)_j, and scaling row j of Q′ scales both terms (P̂
 // inherits it through Q′K̂′ᵀ), so the chunk kernels store their
 // accumulator as it is.
-// Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by all
-// B·H heads of that row, eight heads' loads in flight at a time; raw q and
+// Thread ↔ (row t, 4 consecutive pairs); one sincos per pair shared by the
+// heads of that row in the block's slice of heads (grid.y slices, one slice
+// unless the rows alone give too few blocks), eight heads' loads in flight
+// at a time; raw q and
 // k are read with the evict-first hint.  q, k have L rows per head; Q′, K̂′
 // have Lp = 128·⌈L/128⌉ rows per head, the rows past L written as zeros, and
 // the last chunk's factors use its own length b_c (ζ = γ^{b_c−1−(t mod b)},
@@ -191,8 +193,11 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
   const int t = Lp - 1 - tt;
   const size_t ostride = static_cast<size_t>(Lp) * d;   // output elements between heads
   const size_t oofs = static_cast<size_t>(t) * d + 8 * cidx;
+  // grid.y splits the heads into slices (short sequences: enough blocks)
+  const int hpy = (BH + static_cast<int>(gridDim.y) - 1) / static_cast<int>(gridDim.y);
+  const int y0 = static_cast<int>(blockIdx.y) * hpy, y1 = min(BH, y0 + hpy);
   if (t >= L) {   // padding rows of the last chunk
-    for (int bh = 0; bh < BH; ++bh) {
+    for (int bh = y0; bh < y1; ++bh) {
       *reinterpret_cast<uint4*>(qo + oofs + static_cast<size_t>(bh) * ostride) = make_uint4(0u, 0u, 0u, 0u);
       *reinterpret_cast<uint4*>(ko + oofs + static_cast<size_t>(bh) * ostride) = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -236,9 +241,9 @@ __global__ void __launch_bounds__(256) rotate_qk_kernel(
     }
   };
   if (!rp.on) {
-    rows(pos0, 0, BH);   // one sincos per (position, pair) for all heads
+    rows(pos0, y0, y1);   // one sincos per (position, pair) for the slice's heads
   } else {
-    for (int b = 0; b < BH / H; ++b) rows(rp.p[b], b * H, b * H + H);
+    for (int b = y0 / H; b * H < y1; ++b) rows(rp.p[b], max(b * H, y0), min(b * H + H, y1));
   }
 }
 
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(const uint4* __restrict_
 }
 
 // ---------------------------------------------------------------------------
-// Main kernel.  grid = (d_v / 128, B·H); block = 576 threads; 1 CTA per SM.
+// Main kernel.  grid = (⌈d_v / 128⌉, B·H); block = 576 threads; 1 CTA per SM.
 // Warp 0: TMA producer.  Warp 1: MMA issuer.  Warps 2..17: drain warps; the
 // drain warp with hardware warp id w reads TMEM lanes 32·(w % 4) … +31
 // (v for Õᵀ/ΔSᵀ/Ŝᵀ, j for P̂) and handles column slice (w − 2) / 4.
@@ -403,11 +408,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int vl = 32 * quarter + lane;     // local v (TMEM lane) for Õ / ΔS / Ŝ
     const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
     const size_t sbase = static_cast<size_t>(bh) * DK * d_v + v0 + vl;
+    // A tile narrower than 128 (d_v = 64): lanes past d_v only carry zeros
+    // (V's missing columns read as zeros) and touch no memory.
+    const bool vlive = v0 + vl < d_v;
 
     float S[C::SPT];
 #pragma unroll
     for (int u = 0; u < C::SPT; ++u)
-      S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
+      S[u] = (args.state_in && vlive) ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
 
     // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
     auto write_shat = [&](float g) {
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (lane == 0) mbar_arrive(bar(X_FREE));
           }
           const size_t gb0 = base + static_cast<size_t>(16 * hf) * d_v;
-          if (!args.out) {
+          if (!args.out || !vlive) {
           } else if (args.out_f32) {
             float* o = reinterpret_cast<float*>(obuf) + gb0;
 #pragma unroll
@@ -525,7 +533,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-    if (ok && args.state_out) {
+    if (ok && args.state_out && vlive) {
 #pragma unroll
       for (int u = 0; u < C::SPT; ++u)
         args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] = S[u];

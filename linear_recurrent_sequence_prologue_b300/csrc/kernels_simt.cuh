@@ -139,11 +139,23 @@ __global__ void __launch_bounds__(256) state_scan_kernel(float* __restrict__ ws,
   const int h = static_cast<int>(bh % H);
   float S = state_in ? state_in[idx] : 0.f;
   float* p = ws + bh * nchunks * per + e;
-  for (int i = 0; i < nchunks; ++i) {
-    const float d = p[static_cast<size_t>(i) * per];
-    p[static_cast<size_t>(i) * per] = S;
-    const float g = (i == nchunks - 1) ? cc.gtail[h] : cc.gb[h];
-    S = fmaf(g, S, d);
+  // Sixteen chunks' ΔS are loaded before any of them is combined, so the
+  // loads overlap instead of waiting one after another.
+  constexpr int PF = 16;
+  for (int i0 = 0; i0 < nchunks; i0 += PF) {
+    float d[PF];
+#pragma unroll
+    for (int u = 0; u < PF; ++u)
+      if (i0 + u < nchunks) d[u] = p[static_cast<size_t>(i0 + u) * per];
+#pragma unroll
+    for (int u = 0; u < PF; ++u) {
+      const int i = i0 + u;
+      if (i < nchunks) {
+        p[static_cast<size_t>(i) * per] = S;
+        const float g = (i == nchunks - 1) ? cc.gtail[h] : cc.gb[h];
+        S = fmaf(g, S, d[u]);
+      }
+    }
   }
   if (state_out) state_out[idx] = S;
 }

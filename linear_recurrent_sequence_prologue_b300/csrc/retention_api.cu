@@ -187,21 +187,33 @@ bool tc_gamma_ok(const float* gamma, int H, int chunk) {
   return true;
 }
 
+// The tensor-core chunk kernels: tiles of 128 d_v columns (d_v a multiple
+// of 128, or one tile of which the first 64 columns are live) and chunks of
+// 128 tokens.  A requested chunk of 64 runs on the same 128-token tiles: the
+// chunkwise form's value does not depend on the chunk length (b = 1 gives the
+// recurrent form, b = L the parallel one), so only the rounding differs.
 bool tc_chunk_ok(ret_dtype in_dt, const float* gamma, int H, int L, int d_k, int d_v,
                  int chunk) {
   if (g_force_path == RET_PATH_SIMT) return false;
   if (in_dt != RET_BF16) return false;
   if (!(d_k == 64 || d_k == 128 || d_k == 256)) return false;
-  if (d_v % tcc::VT != 0 || chunk != tcc::CH || L < 1) return false;
-  return tc_gamma_ok(gamma, H, chunk);
+  if ((d_v % tcc::VT != 0 && d_v != 64) || (chunk != tcc::CH && chunk != tcc::CH / 2) || L < 1)
+    return false;
+  return tc_gamma_ok(gamma, H, tcc::CH);
 }
 
+int tc_tiles(int d_v) { return (d_v + tcc::VT - 1) / tcc::VT; }
+
 // CTA pairs (cta_group::2) for the chunk kernels: the two d_v tiles of a
-// pair share one head, so d_v / 128 must be even.
+// pair share one head, so d_v must hold an even number of whole tiles.
 bool tc_pair_ok(int d_k, int d_v) {
-  return g_force_path != RET_PATH_TC_SINGLE && (d_k == 128 || d_k == 256) &&
+  return g_force_path != RET_PATH_TC_SINGLE && (d_k == 128 || d_k == 256) && d_v % tcc::VT == 0 &&
          (d_v / tcc::VT) % 2 == 0;
 }
+
+// Grid rows of the tensor-core launches: B·H (carry layout) or B·H·L/128
+// (one chunk per row) must fit gridDim.y.
+constexpr size_t kMaxGridRows = 65535;
 
 struct Plan {
   int path = 0;
@@ -214,7 +226,19 @@ struct Plan {
   // the angle table [L][d_k/2] (cos, sin).
   int ring = 0, ring_heads = 0;
   size_t off_flags = 0, off_cs = 0;
+  // ret_chunkwise on the tensor cores in the chunk-parallel layout (a grid
+  // of B·H·tiles CTAs too small to keep the SMs busy for the carried one).
+  bool scan = false;
 };
+
+// The carried layout runs B·H·tiles CTAs that each walk every chunk; below
+// half the SMs (and with several chunks) the chunk-parallel layout, whose
+// launches have one CTA per chunk, finishes sooner.  Both give the same bits.
+constexpr size_t kCarryMinCtas = 74;
+bool prefer_scan(size_t BH, int d_v, int nch) {
+  return g_force_path == 0 && BH * tc_tiles(d_v) < kCarryMinCtas && nch >= 4 &&
+         BH * nch <= kMaxGridRows;
+}
 
 // Compact-workspace mode of the carried layout on CTA pairs: the Θ prologue
 // runs inside the chunk launch (producer CTAs on the SMs the consumer pairs
@@ -229,9 +253,6 @@ constexpr int kRingMaxProducers = 40;
 
 bool ring_mode_ok(int d_k, int d_v) { return tc_pair_ok(d_k, d_v); }
 
-// Grid rows of the tensor-core launches: B·H (carry layout) or B·H·L/128
-// (one chunk per row) must fit gridDim.y.
-constexpr size_t kMaxGridRows = 65535;
 
 // compact: the compact-workspace mode where it applies (carried layout on
 // CTA pairs), else the same plan as without it.
@@ -239,15 +260,15 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
                     int chunk, bool gn, bool scan = false, bool compact = false) {
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
-  const int nch = (L + chunk - 1) / chunk;
+  const bool tc = tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk);
+  const int nch = (L + (tc ? tcc::CH : chunk) - 1) / (tc ? tcc::CH : chunk);
   size_t off = 0;
-  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk) &&
-      ((compact && !scan && ring_mode_ok(d_k, d_v)) || (scan ? BH * nch : BH) <= kMaxGridRows)) {
+  if (tc && ((compact && !scan && ring_mode_ok(d_k, d_v)) || (scan ? BH * nch : BH) <= kMaxGridRows)) {
     p.path = RET_PATH_TC;
     if (compact && !scan && ring_mode_ok(d_k, d_v)) {
       // producer ring: kRing chunk slots of Q″ and K̂′ per head of one launch,
       // the launch's counters and the call's angle table
-      const int ntiles = d_v / tcc::VT;
+      const int ntiles = tc_tiles(d_v);
       p.ring = kRing;
       p.ring_heads = static_cast<int>(std::min<size_t>(BH, std::max(1, kRingConsumers / ntiles)));
       const size_t slots = static_cast<size_t>(p.ring_heads) * kRing * tcc::CH * d_k * 2;
@@ -261,7 +282,8 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
       p.off_q = off; off += up256(BH * Lp * d_k * 2);
       p.off_k = off; off += up256(BH * Lp * d_k * 2);
     }
-    if (scan) { p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4); }
+    if (!scan && !p.ring && prefer_scan(BH, d_v, nch)) p.scan = true;
+    if (scan || p.scan) { p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4); }
     if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * static_cast<size_t>(d_v) * 4); }
   } else {
     p.path = RET_PATH_SIMT;
@@ -279,7 +301,8 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
   Plan p;
   const size_t BH = static_cast<size_t>(B) * H;
   size_t off = 0;
-  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && L % tcc::CH == 0 && BH <= kMaxGridRows &&
+  if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && d_v % tcc::VT == 0 && L % tcc::CH == 0 &&
+      BH <= kMaxGridRows &&
       static_cast<size_t>(L / tcc::CH) <= kMaxGridRows &&
       (!want_state || BH * (L / tcc::CH) <= kMaxGridRows)) {
     // rotated Q′ / K̂′ in bf16; per-block ΔS states when state_out is wanted
@@ -557,7 +580,10 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   {
     const size_t n = static_cast<size_t>(Lp) * (d_k / 8);
     Mark m("rotate_qk_bf16", st);
-    tcc::rotate_qk_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+    const unsigned bx = static_cast<unsigned>((n + 255) / 256);
+    const unsigned by = static_cast<unsigned>(std::max<size_t>(
+        1, std::min<size_t>((static_cast<size_t>(BH) + 7) / 8, (2 * 148 + bx - 1) / bx)));
+    tcc::rotate_qk_kernel<<<dim3(bx, by), 256, 0, st>>>(
         q, k, qr, kr, cc, BH, H, L, Lp, d_k, static_cast<float>(pos0), tcc::CH, parallel ? 0 : 1, rp);
   }
   // Q′ / K̂′: the padded workspace, flat; V: [B·H][L][d_v] in 3-D for the
@@ -594,7 +620,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     Mark m(name, st);
-    kern<<<dim3(d_v / tcc::VT, rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
+    kern<<<dim3(tc_tiles(d_v), rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
     return cudaGetLastError();
   };
   // Pair kernel: clusters of two CTAs along the d_v tiles.
@@ -1059,7 +1085,7 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     Mark m("bwd_chunk_tc", st);
-    kern<<<dim3(dvF / tcc::VT, rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, g, cc);
+    kern<<<dim3(tc_tiles(dvF), rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, g, cc);
     return cudaGetLastError();
   };
   cudaError_t e;
@@ -1247,7 +1273,8 @@ const char* ret_profile_kernel(int i) {
 }
 
 ret_status ret_force_path(int path) {
-  if (path != 0 && path != RET_PATH_SIMT && path != RET_PATH_TC && path != RET_PATH_TC_SINGLE)
+  if (path != 0 && path != RET_PATH_SIMT && path != RET_PATH_TC && path != RET_PATH_TC_SINGLE &&
+      path != RET_PATH_TC_CARRY)
     return RET_EINVAL;
   g_force_path = path;
   return RET_OK;
@@ -1321,26 +1348,30 @@ ret_status chunkwise_impl(const void* q, const void* k, const void* v, ret_dtype
     rp.on = 1;
   }
   if (chunk < 1) return RET_EINVAL;
-  CallConsts cc;
-  if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
+  if (!gamma || !theta) return RET_EINVAL;
   Plan p = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), scan);
   if (p.bytes > 0 && workspace && al16(workspace) && workspace_bytes < p.bytes && !scan) {
     // too short for the front pass: the compact-workspace mode, where it applies
     const Plan pc = plan_chunkwise(in_dt, gamma, B, H, L, d_k, d_v, chunk, gn_on(gn), false, true);
     if (pc.ring && workspace_bytes >= pc.bytes) p = pc;
   }
+  // γ^b of the chunks: the 128-token tile on the tensor-core path
+  CallConsts cc;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, p.path == RET_PATH_TC ? tcc::CH : chunk, L)) != RET_OK)
+    return s;
   if (p.bytes > 0 && (!workspace || workspace_bytes < p.bytes || !al16(workspace)))
     return RET_EWORKSPACE;
   if (p.path == RET_PATH_TC) {
     const auto* qq = static_cast<const __nv_bfloat16*>(q);
     const auto* kk = static_cast<const __nv_bfloat16*>(k);
     const auto* vv = static_cast<const __nv_bfloat16*>(v);
+    const bool sc = scan || p.scan;
     if (out_dt == RET_F32)
       return run_tc_chunk<float>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in, state_out,
-                                 static_cast<float*>(out), gn, workspace, p, stream, rp, scan);
+                                 static_cast<float*>(out), gn, workspace, p, stream, rp, sc);
     return run_tc_chunk<__nv_bfloat16>(qq, kk, vv, cc, B, H, L, d_k, d_v, pos0, state_in,
                                        state_out, static_cast<__nv_bfloat16*>(out), gn, workspace,
-                                       p, stream, rp, scan);
+                                       p, stream, rp, sc);
   }
   // The fp32 kernels always run in the chunk-parallel layout.
   if (in_dt == RET_F32)

@@ -187,8 +187,21 @@ def test_path_selection(lib):
     assert _plan_compact(lib, _lib.RET_BF16, 1, 3, 1300, 128, 256, 128)[1] == \
         _ring_bytes(3, 1300, 128) + 3 * 128 * 256 * 4
     # sequences of no more chunks than the ring holds: the front pass is smaller
-    assert _plan_compact(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128) == \
-        _plan(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128)
+    assert _plan_compact(lib, _lib.RET_BF16, 2, 16, 512, 256, 512, 128) == \
+        _plan(lib, _lib.RET_BF16, 2, 16, 512, 256, 512, 128) == (_lib.RET_PATH_TC, 2 * 2 * 16 * 512 * 256 * 2)
+    # a grid too small for the carried layout (B·H·tiles < 74 CTAs, 4 chunks or
+    # more): the chunk-parallel layout, whose workspace adds the per-chunk states
+    assert _plan(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128) == \
+        (_lib.RET_PATH_TC, 2 * 2 * 2 * 512 * 256 * 2 + 2 * 2 * 4 * 256 * 512 * 4)
+    # the Small MSR workload (d_v = 64, one 128-wide tile of which 64 columns
+    # are live; chunk 64 runs on the 128-token tile): tensor cores, chunk-parallel
+    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64) == \
+        (_lib.RET_PATH_TC, 2 * 32 * 2048 * 64 * 2 + 32 * 16 * 64 * 64 * 4)
+    assert lib.ret_force_path(_lib.RET_PATH_TC_CARRY) == _lib.RET_OK
+    try:   # the carried layout kept: the rotated Q′ / K̂′ only
+        assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64) == (_lib.RET_PATH_TC, 2 * 32 * 2048 * 64 * 2)
+    finally:
+        assert lib.ret_force_path(0) == _lib.RET_OK
     # no compact mode off the CTA-pair shapes: the same bytes as the plan
     assert _plan_compact(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128) == \
         _plan(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128)
@@ -204,7 +217,8 @@ def test_path_selection(lib):
                                  C.byref(path), C.byref(nb2)) == _lib.RET_OK
     assert path.value == _lib.RET_PATH_SIMT
     assert _plan(lib, _lib.RET_F32, 1, 2, 64, 16, 16, 16)[0] == _lib.RET_PATH_SIMT
-    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64)[0] == _lib.RET_PATH_SIMT
+    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 32)[0] == _lib.RET_PATH_SIMT   # chunk 32
+    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 96, 64)[0] == _lib.RET_PATH_SIMT   # d_v 96
     # a head whose γ^127 underflows the rewritten form goes to the fp32 kernels
     g = np.array([0.5, 0.99], np.float32)
     assert _plan(lib, _lib.RET_BF16, 1, 2, 256, 256, 128, 128, gamma=g)[0] == _lib.RET_PATH_SIMT

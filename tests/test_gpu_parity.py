@@ -201,8 +201,12 @@ def test_tc_scan_layout_is_bit_identical_to_carry(d_k, d_v, L, H):
     assert path == R.RET_PATH_TC
     d = _cuda(inp)
     for odt in (torch.bfloat16, torch.float32):
-        o1, s1 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=9,
-                             state_in=d["state_in"], out_dtype=odt)
+        R.force_path(R.RET_PATH_TC_CARRY)   # keep the carried layout for a grid this small
+        try:
+            o1, s1 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=9,
+                                 state_in=d["state_in"], out_dtype=odt)
+        finally:
+            R.force_path(0)
         o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=128, pos0=9,
                              state_in=d["state_in"], out_dtype=odt, layout="scan")
         assert R.sync_status() == R.RET_OK
@@ -211,6 +215,52 @@ def test_tc_scan_layout_is_bit_identical_to_carry(d_k, d_v, L, H):
     ref_o, ref_s = _oracle_full(inp, w, "chunkwise", 128, pos0=9)
     assert_close(gpu_np(o2), ref_o, torch.bfloat16, "scan out")
     assert_close(gpu_np(s2), ref_s, torch.bfloat16, "scan state")
+
+
+@pytest.mark.parametrize("d_k,L,H,chunk,pos0", [(64, 640, 3, 64, 0), (128, 300, 2, 128, 9), (256, 129, 1, 64, 40)])
+def test_tc_narrow_value_tile(d_k, L, H, chunk, pos0):
+    """d_v = 64 on the tensor cores (the Small MSR shape): one 128-wide tile of
+    which the first 64 columns are live; a requested chunk of 64 runs on the
+    128-token tile.  Carried and chunk-parallel layouts give the same bits;
+    against the oracle at the requested chunk."""
+    w, inp = _custom(2, H, L, d_k, 64, "bf16", chunk, std=0.125, state_std=0.1, seed=L + d_k)
+    path, _ = R.plan("chunkwise", torch.bfloat16, 2, H, L, d_k, 64, chunk, gamma=inp["gamma"])
+    assert path == R.RET_PATH_TC
+    d = _cuda(inp)
+    res = {}
+    for layout in ("carry", "scan"):
+        R.force_path(R.RET_PATH_TC_CARRY if layout == "carry" else 0)
+        try:
+            for odt in (torch.bfloat16, torch.float32):
+                res[layout, odt] = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"],
+                                               chunk=chunk, pos0=pos0, state_in=d["state_in"],
+                                               out_dtype=odt, layout=layout)
+                assert R.sync_status() == R.RET_OK
+        finally:
+            R.force_path(0)
+    for odt in (torch.bfloat16, torch.float32):
+        assert torch.equal(res["carry", odt][0], res["scan", odt][0])
+        assert torch.equal(res["carry", odt][1], res["scan", odt][1])
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", chunk, pos0=pos0)
+    o, s = res["carry", torch.float32]
+    assert_close(gpu_np(o), ref_o, torch.bfloat16, "d_v 64 out")
+    assert_close(gpu_np(s), ref_s, torch.bfloat16, "d_v 64 state")
+    # the idle columns write nothing: out and state_out are views at the start
+    # of NaN-filled buffers whose tails must stay NaN, and the values match
+    n, m = 2 * H * L * 64, 2 * H * d_k * 64
+    ob = torch.full((n + 128 * 128,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    sb = torch.full((m + 128 * 128,), float("nan"), dtype=torch.float32, device="cuda")
+    for layout in ("carry", "scan"):
+        R.force_path(R.RET_PATH_TC_CARRY if layout == "carry" else 0)
+        try:
+            o2, s2 = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=chunk, pos0=pos0,
+                                 state_in=d["state_in"], out=ob[:n].view(2, H, L, 64),
+                                 state_out=sb[:m].view(2, H, d_k, 64), layout=layout)
+            assert R.sync_status() == R.RET_OK
+        finally:
+            R.force_path(0)
+        assert torch.equal(o2, res["carry", torch.bfloat16][0]) and torch.equal(s2, res["carry", torch.bfloat16][1])
+        assert torch.isnan(ob[n:].float()).all() and torch.isnan(sb[m:]).all()
 
 
 @pytest.mark.parametrize("d_k,d_v,L,H", [(256, 256, 512, 2), (128, 512, 384, 1), (256, 512, 640, 2)])

@@ -86,12 +86,13 @@ def _poison(lib, w):
 def test_noalloc_sequence_of_shapes_after_nan_fill():
     """Calls of different shapes and kernel paths share one array: each must
     depend only on what it wrote itself.  The array is first filled with NaN
-    by two large problems (tensor-core and fp32 path, GroupNorm staging on),
-    then three different problems run back to back."""
+    by three large problems (tensor cores in both layouts and the fp32 path,
+    GroupNorm staging on), then four different problems run back to back."""
     lib = R.load()
-    big_tc = Workload("nan_tc", 1, 2, 8000, 256, 256, "bf16", 128, 1.0, groupnorm=True)
+    big_tc = Workload("nan_tc", 2, 20, 384, 256, 256, "bf16", 128, 1.0, groupnorm=True)     # carried layout
+    big_scan = Workload("nan_scan", 1, 2, 1024, 256, 256, "bf16", 128, 1.0, groupnorm=True)  # chunk-parallel
     big_f32 = Workload("nan_f32", 1, 4, 4096, 64, 64, "f32", 64, 1.0, groupnorm=True)
-    for w in (big_tc, big_f32):
+    for w in (big_tc, big_scan, big_f32):
         need = R.plan("chunkwise", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk,
                       out_dtype=torch.float32, gn=True)[1]
         assert need <= _lib.RET_NOALLOC_SCRATCH_BYTES
