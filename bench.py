@@ -594,6 +594,74 @@ def main():
         if name != w.name:
             extra[name] = bench_config(name, steps_)
 
+    # ---------------- the MSR block around the core (projections, gate) ----------------
+    def block_line(steps=10):
+        """ret_msr_block at the 7B shape (hidden 4096, H16, d_k 256, d_v 512) with
+        seeded random bf16 weights: tokens/s, TFLOP/s of the whole block and the
+        roofline of its dominant kernel."""
+        D, Dout = w.H * w.d_k, w.H * w.d_k
+        HK, HV = w.H * w.d_k, w.H * w.d_v
+        gen = torch.Generator(device=dev).manual_seed(11)
+        rn = lambda shape, std: (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+        xb = rn((w.B, w.L, D), 1.0)
+        wq, wk = rn((D, w.H, w.d_k), D ** -0.5), rn((D, w.H, w.d_k), D ** -0.5)
+        wv, wg = rn((D, w.H, w.d_v), D ** -0.5), rn((D, w.H, w.d_v), D ** -0.5)
+        wo = rn((w.H, w.d_v, Dout), HV ** -0.5)
+        zb = torch.empty((w.B, w.L, Dout), dtype=torch.bfloat16, device=dev)
+        sb_ = torch.empty((w.B, w.H, w.d_k, w.d_v), dtype=torch.float32, device=dev)
+        nbytes = R.msr_block_plan(w.B, w.L, D, w.H, w.d_k, w.d_v, Dout, gamma=inp["gamma"])
+        bws_ = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        bargs_ = (vp(xb), vp(wq), vp(wk), vp(wv), vp(wg), vp(wo), fptr(garr), fptr(tarr), w.B, w.L, D, w.H,
+                  w.d_k, w.d_v, Dout, 0, vp(s_in), vp(sb_), vp(zb), _lib.RET_BF16, 1e-5, vp(bws_), nbytes,
+                  C.c_void_p(stream.cuda_stream))
+
+        def one():
+            st_ = lib.ret_msr_block(*bargs_)
+            if st_ != _lib.RET_OK:
+                raise RuntimeError(f"ret_msr_block returned {st_}")
+
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize()
+        bsamp = ClockSampler(local)
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with bsamp:
+            bsamp.mark()
+            s0.record(stream)
+            lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+            for i_ in range(steps):
+                one()
+                if i_ == 1:
+                    nk_ = lib.ret_profile_end()
+            e0.record(stream)
+            torch.cuda.synchronize()
+            bsamp.mark()
+        bper = {}
+        for i_ in range(nk_):
+            bper.setdefault(lib.ret_profile_kernel(i_).decode(), []).append(evs[2 * i_].elapsed_time(evs[2 * i_ + 1]))
+        step_ms = {nm: sum(t) / 2 for nm, t in bper.items()}
+        bms_ = max_over_ranks(s0.elapsed_time(e0) / steps, world, dev)
+        M = w.B * w.L
+        gemm_fl = {"proj_q_rot": 2 * M * D * HK, "proj_k_rot": 2 * M * D * HK, "proj_v": 2 * M * D * HV,
+                   "proj_gate": 2 * M * D * HV, "proj_out": 2 * M * HV * Dout}
+        total = sum(gemm_fl.values()) + chunk_flops(w)
+        gtop = max(gemm_fl, key=lambda n: step_ms.get(n, 0.0))
+        gach = gemm_fl[gtop] / (step_ms[gtop] / 1e3) / 1e12
+        del bws_, xb, wq, wk, wv, wg, wo, zb
+        return {"metric": "MSR block tokens/s", "value": replica_throughput(M, bms_ / 1e3, world),
+                "unit": "tokens/s", "ms_per_step": bms_, "steps": steps,
+                "config": {"workload": "msr7b block", "B": w.B, "L": w.L, "hidden": D, "H": w.H, "d_k": w.d_k,
+                           "d_v": w.d_v, "D_out": Dout, "weights": "seeded random bf16, N(0, 1/fan_in)"},
+                "tflops": total / (bms_ / 1e3) / 1e12, "frac_of_bf16_peak": total / (bms_ / 1e3) / 1e12 / peak,
+                "algorithmic_flop_per_step": total,
+                "roofline": {"bound": "tensor", "kernel": gtop, "achieved": gach, "peak": peak,
+                             "unit": "TFLOP/s", "frac": gach / peak, "traffic": None,
+                             "algorithmic_flop_per_launch": gemm_fl[gtop]},
+                "kernels_ms_per_step": step_ms,
+                "gpu_launches": int(round(nk_ / 2 * steps)), "clocks": bsamp.summary()}
+
+    block = block_line()
+
     # ---------------- decode workload ----------------
     dw = WORKLOADS["decode"]
     dsteps = max(args.decode_steps, 1)
@@ -846,6 +914,7 @@ def main():
             "compact_workspace_mode": compact,
             "workspace_bytes": ws_bytes,
             "decode": decode,
+            "msr_block": block,
             "small": extra.get("small"),
             "msr1p3b": extra.get("msr1p3b"),
             "backward": backward,

@@ -306,6 +306,49 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta,
 ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, int B, int H,
                               int L, int d_v, int64_t pos0, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------
+ * ret_matmul — C = A·W on the tensor cores (the projection GEMM of
+ * ret_msr_block, exposed on its own).  A: DEVICE [M][K] bf16, W: DEVICE [K][N]
+ * bf16, both row-major; C: DEVICE [M][N] in c_dt (bf16 rounded to nearest, or
+ * fp32); fp32 accumulation.  N a multiple of 256 and K of 64, else
+ * RET_EUNSUPPORTED; any M ≥ 1.  Tiles of 256 × 256 on CTA pairs
+ * (tcgen05.mma.cta_group::2), operands staged by TMA.
+ * ------------------------------------------------------------------------ */
+ret_status ret_matmul(const void* a, const void* w, void* c, ret_dtype c_dt, int M, int N, int K,
+                      cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * ret_msr_block — the multi-scale retention block around the core:
+ *   q = x·W_Q, k = x·W_K, v = x·W_V per head (the SimpleRetention of
+ *   «RetNet：Transformer的革命性继任者？»: one projection per head, the heads
+ *   side by side), o = the chunkwise retention of q, k, v (with the Θ
+ *   prologue, state_in / state_out as ret_chunkwise), per-head GroupNorm of
+ *   o («从RoPE到Retention…» §5), then the gate and output projection of the
+ *   published MSR definition, which the pages do not spell out:
+ *   z = (swish(x·W_G) ⊙ concat_h GN(o_h))·W_O, swish(u) = u·σ(u).
+ * x: DEVICE [B][L][D] bf16.  w_q, w_k: [D][H·d_k]; w_v, w_g: [D][H·d_v];
+ * w_o: [H·d_v][D_out]; all DEVICE bf16 row-major (column h·d + c belongs to
+ * head h).  z: DEVICE [B][L][D_out] in z_dt.  gamma, theta: HOST as for
+ * ret_chunkwise.  GroupNorm: eps = gn_eps > 0, no affine terms.
+ * The q and k projections' epilogues write the chunk kernels' rotated,
+ * decay-folded operands directly (no separate Θ pass); v goes to the head
+ * layout; the chunkwise core runs on the tensor cores (its shape rules:
+ * bf16, d_k ∈ {64, 128, 256}, d_v = 64 or a multiple of 128, every
+ * γ^127 ≥ 2^-60), and D a multiple of 64, H·d_k, H·d_v and D_out multiples
+ * of 256; anything else is RET_EUNSUPPORTED.  workspace: DEVICE, at least
+ * ret_msr_block_plan's bytes (the projected operands, the fp32 core output,
+ * the gate and the gated, normalised rows: 1.6 GB at B2 L8192 D4096 H16
+ * d_k256 d_v512).
+ * ------------------------------------------------------------------------ */
+ret_status ret_msr_block(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                         const void* w_g, const void* w_o, const float* gamma, const float* theta,
+                         int B, int L, int D, int H, int d_k, int d_v, int D_out, int64_t pos0,
+                         const float* state_in, float* state_out, void* z, ret_dtype z_dt,
+                         float gn_eps, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+ret_status ret_msr_block_plan(const float* gamma, int B, int L, int D, int H, int d_k, int d_v,
+                              int D_out, size_t* workspace_bytes);
+
 /* Synchronise `stream`, then return and clear the device status word:
  * RET_ETIMEOUT if a kernel's bounded wait expired since the last call,
  * RET_ECUDA on a CUDA error, else RET_OK. */

@@ -47,6 +47,10 @@ SIGNATURES = {
                                         C.POINTER(_sz)]),
     "ret_chunkwise_scan_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
     "ret_parallel_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
+    "ret_matmul": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "ret_msr_block": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _fp, _fp, _i, _i, _i, _i, _i, _i, _i, _i64,
+                           _vp, _vp, _vp, _i, _f, _vp, _sz, _vp]),
+    "ret_msr_block_plan": (_i, [_fp, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_sz)]),
     "ret_step": (_i, [_vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i64, _vp, _vp, _i,
                       C.POINTER(RetGN), _vp]),
     "ret_rotate": (_i, [_vp, _i, _fp, _i, _i, _i, _i, _i64, _f, _vp, _i, _vp]),

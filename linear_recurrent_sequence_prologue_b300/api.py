@@ -301,6 +301,65 @@ def decay_row_norm(out, gamma, pos0: int = 0, stream=None):
     return out
 
 
+def matmul(a, w, out_dtype=None, stream=None):
+    """C = A·W on the tensor cores: a [M, K], w [K, N] bf16 (N % 256 == 0, K % 64 == 0)."""
+    lib = load()
+    if a.dim() != 2 or w.dim() != 2 or a.shape[1] != w.shape[0]:
+        raise ValueError("a: [M, K], w: [K, N]")
+    M, K = a.shape
+    N = w.shape[1]
+    c = torch.empty((M, N), dtype=out_dtype or torch.bfloat16, device=a.device)
+    st = lib.ret_matmul(_dev(a, "a", torch.bfloat16), _dev(w, "w", torch.bfloat16), _dev(c, "c"),
+                        _dtype_code(c), M, N, K, _stream(stream))
+    check("ret_matmul", st)
+    return c
+
+
+def msr_block_plan(B, L, D, H, d_k, d_v, D_out, gamma=None) -> int:
+    """Workspace bytes of ret_msr_block."""
+    lib = load()
+    gp = None
+    if gamma is not None:
+        garr, gp = _host_f32(gamma, H, "gamma")
+    nbytes = C.c_size_t(0)
+    check("ret_msr_block_plan", lib.ret_msr_block_plan(gp, B, L, D, H, d_k, d_v, D_out, C.byref(nbytes)))
+    return nbytes.value
+
+
+def msr_block(x, w_q, w_k, w_v, w_g, w_o, gamma, theta, pos0: int = 0, state_in=None,
+              return_state: bool = True, gn_eps: float = 1e-5, out=None, out_dtype=None,
+              workspace=None, stream=None):
+    """The MSR block: z = (swish(x·W_G) ⊙ GN(retention(x·W_Q, x·W_K, x·W_V)))·W_O.
+
+    x [B, L, D] bf16; w_q, w_k [D, H, d_k]; w_v, w_g [D, H, d_v]; w_o [H, d_v, D_out]
+    (bf16, contiguous).  Returns (z [B, L, D_out], state_out or None)."""
+    lib = load()
+    if x.dim() != 3 or w_q.dim() != 3 or w_v.dim() != 3 or w_o.dim() != 3:
+        raise ValueError("x [B, L, D]; w_q, w_k [D, H, d_k]; w_v, w_g [D, H, d_v]; w_o [H, d_v, D_out]")
+    B, L, D = x.shape
+    _, H, d_k = w_q.shape
+    d_v, D_out = w_v.shape[2], w_o.shape[2]
+    for name, t, shp in (("w_k", w_k, (D, H, d_k)), ("w_v", w_v, (D, H, d_v)), ("w_g", w_g, (D, H, d_v)),
+                         ("w_o", w_o, (H, d_v, D_out))):
+        _dev(t, name, torch.bfloat16, shp)
+    if out is None:
+        out = torch.empty((B, L, D_out), dtype=out_dtype or torch.bfloat16, device=x.device)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
+    sshape = (B, H, d_k, d_v)
+    state_out = torch.empty(sshape, dtype=torch.float32, device=x.device) if return_state else None
+    nbytes = msr_block_plan(B, L, D, H, d_k, d_v, D_out, gamma=garr)
+    wsp, wsn, ws = _workspace(nbytes, x.device, workspace)
+    st = lib.ret_msr_block(_dev(x, "x", torch.bfloat16), _dev(w_q, "w_q"), _dev(w_k, "w_k"),
+                           _dev(w_v, "w_v"), _dev(w_g, "w_g"), _dev(w_o, "w_o"), gp, tp, B, L, D, H,
+                           d_k, d_v, D_out, int(pos0),
+                           _dev(state_in, "state_in", torch.float32, sshape),
+                           _dev(state_out, "state_out"), _dev(out, "out"), _dtype_code(out),
+                           float(gn_eps), wsp, wsn, _stream(stream))
+    check("ret_msr_block", st)
+    return out, state_out
+
+
 def sync_status(stream=None) -> int:
     """Synchronise and return (and clear) the device status word as a ret_status code."""
     return load().ret_sync_status(_stream(stream))

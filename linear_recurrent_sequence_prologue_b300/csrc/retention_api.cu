@@ -20,6 +20,7 @@
 #include "kernel_tc_chunk.cuh"
 #include "kernel_tc_parallel.cuh"
 #include "kernel_tc_pair.cuh"
+#include "kernel_tc_gemm.cuh"
 
 using namespace ret;
 
@@ -568,7 +569,8 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
                         const CallConsts& cc, int B, int H, int L, int d_k, int d_v,
                         int64_t pos0, const float* s_in, float* s_out, Tout* out,
                         const ret_gn* gn, void* ws, const Plan& p, cudaStream_t st,
-                        const RowPos& rp, bool scan = false, bool parallel = false) {
+                        const RowPos& rp, bool scan = false, bool parallel = false,
+                        bool prerot = false) {
   if (p.ring && !scan && !parallel)
     return d_k == 256 ? run_tc_ring<256, Tout>(q, k, v, cc, B, H, L, d_v, pos0, s_in, s_out, out, gn, ws, p, st, rp)
                       : run_tc_ring<128, Tout>(q, k, v, cc, B, H, L, d_v, pos0, s_in, s_out, out, gn, ws, p, st, rp);
@@ -577,7 +579,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   __nv_bfloat16* kr = wsp<__nv_bfloat16>(ws, p.off_k);
   const int nch = (L + tcc::CH - 1) / tcc::CH;
   const int Lp = nch * tcc::CH;   // rows per sequence in the rotated workspace
-  {
+  if (!prerot) {   // (prerot: the workspace already holds Q″ and K̂′)
     const size_t n = static_cast<size_t>(Lp) * (d_k / 8);
     Mark m("rotate_qk_bf16", st);
     const unsigned bx = static_cast<unsigned>((n + 255) / 256);
@@ -1200,6 +1202,65 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   return last_launch();
 }
 
+// ---------------------------------------------------------------------------
+// MSR block: projections (tcgen05 GEMMs with fused epilogues), the chunkwise
+// core on the projected operands, GroupNorm with the swish gate, the output
+// projection.
+// ---------------------------------------------------------------------------
+struct BlockPlan {
+  Plan core;            // the chunkwise core (front-pass layout; Q″ / K̂′ come from the GEMMs)
+  size_t off_cs = 0, off_v = 0, off_o = 0, off_g = 0, off_a = 0, bytes = 0;
+  bool ok = false;
+};
+
+BlockPlan plan_block(const float* gamma, int B, int L, int D, int H, int d_k, int d_v, int D_out) {
+  BlockPlan bp;
+  bp.core = plan_chunkwise(RET_BF16, gamma, B, H, L, d_k, d_v, tcc::CH, false);
+  bp.ok = bp.core.path == RET_PATH_TC && !bp.core.ring && D % tcg::BK == 0 && (H * d_k) % tcg::BN == 0 &&
+          (H * d_v) % tcg::BN == 0 && (H * d_v) % tcg::BK == 0 && D_out % tcg::BN == 0 && d_v % 8 == 0;
+  const size_t M = static_cast<size_t>(B) * L, HV = static_cast<size_t>(H) * d_v;
+  size_t off = bp.core.bytes;
+  bp.off_cs = off; off += up256(static_cast<size_t>(L) * (d_k / 2) * 8);
+  bp.off_v = off; off += up256(M * HV * 2);
+  bp.off_o = off; off += up256(M * HV * 4);
+  bp.off_g = off; off += up256(M * HV * 2);
+  bp.off_a = off; off += up256(M * HV * 2);
+  bp.bytes = off;
+  return bp;
+}
+
+// C = A·W on the pair GEMM kernel; A [M][K] bf16, W [K][N] bf16.
+template <int MODE>
+cudaError_t launch_gemm(const void* A, int M, int K, const void* W, int N, tcg::GemmArgs g,
+                        const CallConsts& cc, cudaStream_t st, const char* name) {
+  CUtensorMap ma, mw;
+  if (!make_map(&ma, A, static_cast<uint64_t>(M), static_cast<uint64_t>(K)) ||
+      !make_map(&mw, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 64))
+    return cudaErrorInvalidValue;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  cudaError_t e = cudaFuncSetAttribute(tcg::proj_gemm_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(tcg::SMEM_BYTES));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * ((M + 2 * tcg::BM - 1) / (2 * tcg::BM)), N / tcg::BN);
+  cfg.blockDim = dim3(tcg::NTHREADS);
+  cfg.dynamicSmemBytes = tcg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  Mark m(name, st);
+  e = cudaLaunchKernelEx(&cfg, tcg::proj_gemm_kernel<MODE>, ma, mw, g, cc);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // Scratch of ret_chunkwise_noalloc: part of this module's device image, so
 // using it allocates nothing at call time.  In host code the array's name is
 // only a stand-in; its device address comes from cudaGetSymbolAddress with
@@ -1697,6 +1758,113 @@ ret_status ret_decay_row_norm(void* out, ret_dtype out_dt, const float* gamma, i
   else
     simt::decay_row_norm_kernel<__nv_bfloat16><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
         static_cast<__nv_bfloat16*>(out), cc, H, L, d_v, static_cast<float>(pos0));
+  return last_launch();
+}
+
+ret_status ret_matmul(const void* a, const void* w, void* c, ret_dtype c_dt, int M, int N, int K,
+                      cudaStream_t stream) {
+  Range nv("ret_matmul");
+  if (!a || !w || !c || !al16(a) || !al16(w) || !al16(c)) return RET_EINVAL;
+  if (c_dt != RET_F32 && c_dt != RET_BF16) return RET_EINVAL;
+  if (M < 1 || N < 1 || K < 1) return RET_EINVAL;
+  if (N % tcg::BN != 0 || K % tcg::BK != 0) return RET_EUNSUPPORTED;
+  CallConsts cc;
+  std::memset(&cc, 0, sizeof(cc));
+  tcg::GemmArgs g;
+  g.out = c;
+  g.out_f32 = c_dt == RET_F32 ? 1 : 0;
+  return launch_gemm<tcg::PLAIN>(a, M, K, w, N, g, cc, stream, "matmul") == cudaSuccess ? RET_OK : RET_ECUDA;
+}
+
+ret_status ret_msr_block_plan(const float* gamma, int B, int L, int D, int H, int d_k, int d_v,
+                              int D_out, size_t* workspace_bytes) {
+  if (!workspace_bytes) return RET_EINVAL;
+  if (B < 1 || L < 1 || D < 1 || H < 1 || H > kMaxHeads || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || D_out < 1)
+    return RET_EINVAL;
+  const BlockPlan bp = plan_block(gamma, B, L, D, H, d_k, d_v, D_out);
+  if (!bp.ok) return RET_EUNSUPPORTED;
+  *workspace_bytes = bp.bytes;
+  return RET_OK;
+}
+
+ret_status ret_msr_block(const void* x, const void* w_q, const void* w_k, const void* w_v,
+                         const void* w_g, const void* w_o, const float* gamma, const float* theta,
+                         int B, int L, int D, int H, int d_k, int d_v, int D_out, int64_t pos0,
+                         const float* state_in, float* state_out, void* z, ret_dtype z_dt,
+                         float gn_eps, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_msr_block");
+  if (!x || !w_q || !w_k || !w_v || !w_g || !w_o || !z) return RET_EINVAL;
+  for (const void* ptr : {x, w_q, w_k, w_v, w_g, w_o, static_cast<const void*>(z)})
+    if (!al16(ptr)) return RET_EINVAL;
+  if ((state_in && !al16(state_in)) || (state_out && !al16(state_out))) return RET_EINVAL;
+  if (z_dt != RET_F32 && z_dt != RET_BF16) return RET_EINVAL;
+  if (B < 1 || L < 1 || D < 1 || H < 1 || H > kMaxHeads || d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) ||
+      d_v < 1 || d_v > 1024 || D_out < 1)
+    return RET_EINVAL;
+  if (pos0 < 0 || pos0 + L > kMaxPos || static_cast<int64_t>(B) * H * L >= (int64_t(1) << 31)) return RET_EINVAL;
+  if (!(gn_eps > 0.f) || !std::isfinite(gn_eps)) return RET_EINVAL;
+  CallConsts cc;
+  ret_status s;
+  if ((s = make_consts(cc, gamma, theta, H, d_k, tcc::CH, L)) != RET_OK) return s;
+  const BlockPlan bp = plan_block(gamma, B, L, D, H, d_k, d_v, D_out);
+  if (!bp.ok) return RET_EUNSUPPORTED;
+  if (!workspace || workspace_bytes < bp.bytes || !al16(workspace)) return RET_EWORKSPACE;
+  const int M = B * L, HK = H * d_k, HV = H * d_v;
+  const int Lp = ((L + tcc::CH - 1) / tcc::CH) * tcc::CH;
+  auto* qr = wsp<__nv_bfloat16>(workspace, bp.core.off_q);
+  auto* kr = wsp<__nv_bfloat16>(workspace, bp.core.off_k);
+  auto* cs = wsp<float2>(workspace, bp.off_cs);
+  auto* vh = wsp<__nv_bfloat16>(workspace, bp.off_v);
+  auto* of = wsp<float>(workspace, bp.off_o);
+  auto* gt = wsp<__nv_bfloat16>(workspace, bp.off_g);
+  auto* ao = wsp<__nv_bfloat16>(workspace, bp.off_a);
+  {
+    const size_t n = static_cast<size_t>(L) * (d_k / 2);
+    Mark m("angle_table", stream);
+    tcc::angle_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        cs, cc, L, d_k / 2, static_cast<float>(pos0));
+    if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  }
+  tcg::GemmArgs g;
+  g.L = L;
+  g.Lp = Lp;
+  g.H = H;
+  g.dh = d_k;
+  g.pos0 = static_cast<float>(pos0);
+  g.cs = cs;
+  g.out = qr;   // q = x·W_Q → Q″ (rotated, ω folded)
+  if (launch_gemm<tcg::ROT_Q>(x, M, D, w_q, HK, g, cc, stream, "proj_q_rot") != cudaSuccess) return RET_ECUDA;
+  g.out = kr;   // k = x·W_K → K̂′ (rotated, d_k^{-1/2}·ζ folded)
+  if (launch_gemm<tcg::ROT_K>(x, M, D, w_k, HK, g, cc, stream, "proj_k_rot") != cudaSuccess) return RET_ECUDA;
+  if (Lp > L) {   // the zero rows that pad every sequence to whole chunks
+    const size_t pitch = static_cast<size_t>(Lp) * d_k * 2, width = static_cast<size_t>(Lp - L) * d_k * 2;
+    const size_t start = static_cast<size_t>(L) * d_k;
+    if (cudaMemset2DAsync(qr + start, pitch, 0, width, static_cast<size_t>(B) * H, stream) != cudaSuccess ||
+        cudaMemset2DAsync(kr + start, pitch, 0, width, static_cast<size_t>(B) * H, stream) != cudaSuccess)
+      return RET_ECUDA;
+  }
+  g.out = vh;   // v = x·W_V, per head
+  g.dh = d_v;
+  if (launch_gemm<tcg::HEADS>(x, M, D, w_v, HV, g, cc, stream, "proj_v") != cudaSuccess) return RET_ECUDA;
+  // the chunkwise core on the projected operands, fp32 output for GroupNorm
+  if ((s = run_tc_chunk<float>(nullptr, nullptr, vh, cc, B, H, L, d_k, d_v, pos0, state_in, state_out, of,
+                               nullptr, workspace, bp.core, stream, no_rowpos(), bp.core.scan, false,
+                               true)) != RET_OK)
+    return s;
+  tcg::GemmArgs gp;
+  gp.out = gt;   // the gate's pre-activation x·W_G
+  if (launch_gemm<tcg::PLAIN>(x, M, D, w_g, HV, gp, cc, stream, "proj_gate") != cudaSuccess) return RET_ECUDA;
+  {
+    const size_t rows = static_cast<size_t>(B) * H * L;
+    Mark m("gn_gate", stream);
+    tcg::gn_gate_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(of, gt, ao, H, L, d_v, rows,
+                                                                                    gn_eps);
+    if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
+  }
+  gp.out = z;   // z = (swish(x·W_G) ⊙ GN(O))·W_O
+  gp.out_f32 = z_dt == RET_F32 ? 1 : 0;
+  if (launch_gemm<tcg::PLAIN>(ao, M, HV, w_o, D_out, gp, cc, stream, "proj_out") != cudaSuccess) return RET_ECUDA;
   return last_launch();
 }
 

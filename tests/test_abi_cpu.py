@@ -320,3 +320,36 @@ def test_chunk_size_policy(lib):
     assert b(_lib.RET_BF16, 8192, gamma=g) == 91
     assert b(_lib.RET_F32, 0) == 0 and b(7, 64) == 0      # invalid arguments
     assert b(_lib.RET_F32, 64, gamma=np.array([1.5] * 16, np.float32)) == 0
+
+
+def test_msr_block_and_matmul_validation(lib):
+    """ret_msr_block / ret_matmul: workspace layout and synchronous checks."""
+    nb = C.c_size_t(0)
+    g = np.full(16, 0.99, np.float32)
+    assert lib.ret_msr_block_plan(_fp(g), 2, 8192, 4096, 16, 256, 512, 4096, C.byref(nb)) == _lib.RET_OK
+    M, HV = 2 * 8192, 16 * 512
+    core = 2 * 2 * 16 * 8192 * 256 * 2                  # Q″ and K̂′ from the projection epilogues
+    assert nb.value == core + 8192 * 128 * 8 + M * HV * (2 + 4 + 2 + 2)   # table, v, fp32 o, gate, gated rows
+    # shapes outside the tensor-core core or the GEMM tiling
+    for args in ((2, 8192, 4000, 16, 256, 512, 4096),      # D not a multiple of 64
+                 (2, 8192, 4096, 16, 256, 512, 4000),      # D_out not a multiple of 256
+                 (2, 8192, 4096, 16, 512, 512, 4096),      # d_k outside the tensor-core shapes
+                 (2, 8192, 4096, 3, 64, 64, 4096)):        # H·d_k not a multiple of 256
+        h = args[3]
+        assert lib.ret_msr_block_plan(_fp(np.full(h, 0.99, np.float32)), *args, C.byref(nb)) == \
+            _lib.RET_EUNSUPPORTED
+    assert lib.ret_msr_block_plan(_fp(g), 2, 8192, 4096, 16, 256, 512, 4096, None) == _lib.RET_EINVAL
+    P = C.c_void_p(0x1000)
+    t = np.ones(128, np.float32)
+    call = lambda **kw: lib.ret_msr_block(*[kw.get(n, P) for n in ("x", "wq", "wk", "wv", "wg", "wo")],
+                                          _fp(g), _fp(t), 2, 8192, 4096, 16, 256, 512, 4096, 0, None, None,
+                                          kw.get("z", P), _lib.RET_BF16, kw.get("eps", 1e-5), None, 0, None)
+    assert call(x=None) == _lib.RET_EINVAL
+    assert call(wo=C.c_void_p(0x1008)) == _lib.RET_EINVAL          # misaligned
+    assert call(eps=0.0) == _lib.RET_EINVAL
+    assert call() == _lib.RET_EWORKSPACE                           # valid: no workspace
+    # the GEMM alone
+    assert lib.ret_matmul(None, P, P, _lib.RET_F32, 300, 512, 192, None) == _lib.RET_EINVAL
+    assert lib.ret_matmul(P, P, P, _lib.RET_F32, 300, 500, 192, None) == _lib.RET_EUNSUPPORTED
+    assert lib.ret_matmul(P, P, P, _lib.RET_F32, 300, 512, 100, None) == _lib.RET_EUNSUPPORTED
+    assert lib.ret_matmul(P, P, P, 7, 300, 512, 192, None) == _lib.RET_EINVAL
