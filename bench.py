@@ -40,7 +40,51 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--backward-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b"],
+                    help="run one case (two warm-up calls, then one call) for an ncu capture and exit")
     return ap.parse_args()
+
+
+def run_profile_case(case):
+    """One call of one case, after two warm-up calls, for ncu (no timing, no
+    JSON line).  chunk7b: ret_chunkwise on the 7B-shape workload; chunk_medium:
+    the same shape at L = 2048 (134 MB of inputs, above the 126 MB L2);
+    gemm: ret_matmul 8192 x 8192 x 4096; rownorm7b: ret_decay_row_norm on a
+    7B-shape bf16 output; block7b: ret_msr_block at the 7B shape."""
+    import torch
+    import linear_recurrent_sequence_prologue_b300 as R
+    from linear_recurrent_sequence_prologue_b300 import build
+    from linear_recurrent_sequence_prologue_b300.inputs import WORKLOADS, make_inputs
+    build.build()
+    R.load()
+    dev = torch.device("cuda", 0)
+    gen = torch.Generator(device=dev).manual_seed(3)
+    rn = lambda shape, std: (torch.randn(*shape, generator=gen, device=dev) * std).to(torch.bfloat16)
+    w = WORKLOADS["msr7b"]
+    if case == "chunk_medium":
+        w = w.with_(L=2048)
+    inp = make_inputs(w, seed=0)
+    if case in ("chunk7b", "chunk_medium"):
+        q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+        s_in = inp["state_in"].to(dev)
+        fn = lambda: R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=w.chunk, state_in=s_in)
+    elif case == "gemm":
+        a, wt = rn((8192, 4096), 1.0), rn((4096, 8192), 4096 ** -0.5)
+        fn = lambda: R.matmul(a, wt)
+    elif case == "rownorm7b":
+        o = rn((w.B, w.H, w.L, w.d_v), 1.0)
+        fn = lambda: R.decay_row_norm(o, inp["gamma"])
+    else:
+        D = w.H * w.d_k
+        x = rn((w.B, w.L, D), 1.0)
+        ws = [rn((D, w.H, w.d_k), D ** -0.5), rn((D, w.H, w.d_k), D ** -0.5), rn((D, w.H, w.d_v), D ** -0.5),
+              rn((D, w.H, w.d_v), D ** -0.5), rn((w.H, w.d_v, D), (w.H * w.d_v) ** -0.5)]
+        fn = lambda: R.msr_block(x, *ws, inp["gamma"], inp["theta"])
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    assert R.sync_status() == R.RET_OK
+    return 0
 
 
 # --------------------------------------------------------------------------
@@ -360,6 +404,8 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.profile:
+        return run_profile_case(args.profile)
     if args.impl == "reference":
         return run_reference(args)
 
