@@ -541,6 +541,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const size_t base = staged
             ? (static_cast<size_t>(seq) * CH + 32 * cs) * d_v + v0 + vl
             : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(c0 + i) * CH + 32 * cs) * d_v + v0 + vl;
+        if (args.out && !args.out_f32) {
+          // bf16 output: the first 16 rows packed to bf16 pairs, the last 16
+          // loaded, X released, and only then the 32 stores, so that no store
+          // sits on the chain Õ drain → QK of the next chunk.
+          uint32_t pk[8], r[16];
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 8, *reinterpret_cast<uint32_t(*)[8]>(&r[8]));
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) pk[u] = pack_bf16x2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 16, *reinterpret_cast<uint32_t(*)[8]>(&r[0]));
+          tmem_ld8(tmem + C::T_X + lane_off + 32 * cs + 24, *reinterpret_cast<uint32_t(*)[8]>(&r[8]));
+          tmem_ld_wait();
+          tc_fence_before();
+          arrive_lead(X_FREE);
+          unsigned short* o = reinterpret_cast<unsigned short*>(static_cast<__nv_bfloat16*>(obuf) + base);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {   // streaming stores: the output is not read again here
+            __stcs(o + static_cast<size_t>(2 * u) * d_v, static_cast<unsigned short>(pk[u] & 0xffffu));
+            __stcs(o + static_cast<size_t>(2 * u + 1) * d_v, static_cast<unsigned short>(pk[u] >> 16));
+          }
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            __stcs(o + static_cast<size_t>(16 + c) * d_v,
+                   __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(r[c]))));
+        } else
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[16];
