@@ -83,6 +83,8 @@ __all__ = [
     "state_closed_form",
     "retention",
     "retention_backward",
+    "retention_param_grads",
+    "groupnorm_backward",
     "decay_row_sums",
     "normalised_retention",
     "msr_block",
@@ -256,6 +258,31 @@ def group_norm(o, eps=1e-5, weight=None, bias=None):
     return y
 
 
+def groupnorm_backward(o, d_y, eps=1e-5, weight=None):
+    """Gradients of ``group_norm`` (R7) for the upstream gradient d_y of its
+    output.  Returns (d_o, d_weight, d_bias); d_weight and d_bias have the
+    affine's shape [H, d_v] and sum over batch and tokens (weight None means
+    ones).  Per row, over its N = d_v channels, with μ the mean, var the
+    biased variance, σ = √(var + eps), x̂ = (o − μ)/σ and g = d_y ⊙ weight,
+    differentiating y = x̂·weight + bias through μ and var (both depend on
+    every channel of the row):
+      d_o      = (g − mean(g) − x̂·mean(g ⊙ x̂)) / σ
+      d_weight = Σ_rows d_y ⊙ x̂,   d_bias = Σ_rows d_y
+    """
+    o, d_y = _f64(o), _f64(d_y)
+    H, d_v = o.shape[1], o.shape[-1]
+    w = np.ones((H, d_v)) if weight is None else _f64(weight)
+    mu = o.mean(axis=-1, keepdims=True)
+    var = ((o - mu) ** 2).mean(axis=-1, keepdims=True)
+    sigma = np.sqrt(var + float(eps))
+    xhat = (o - mu) / sigma
+    gw = d_y * w[None, :, None, :]
+    d_o = (gw - gw.mean(axis=-1, keepdims=True) - xhat * (gw * xhat).mean(axis=-1, keepdims=True)) / sigma
+    d_weight = (d_y * xhat).sum(axis=(0, 2))
+    d_bias = d_y.sum(axis=(0, 2))
+    return d_o, d_weight, d_bias
+
+
 # --------------------------------------------------------------------------
 # Full operation and the decode step
 # --------------------------------------------------------------------------
@@ -334,13 +361,9 @@ def msr_block(x, w_q, w_k, w_v, w_g, w_o, gamma, theta, pos0=0, state_in=None,
     return z, S
 
 
-def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
-                       d_state_out=None):
-    """Gradients of ``retention`` (no GroupNorm) with respect to q, k, v and
-    state_in, for the upstream gradients d_out (of out) and d_state_out (of
-    state_out, or None).  Returns (dq, dk, dv, d_state_in).
-
-    The chain rule applied to the parallel form with the state terms
+def _rotated_grads(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
+                   d_state_out=None):
+    """The chain rule applied to the parallel form with the state terms
     ([P1] §4.1, R4), per head with A = D (the causal decay mask),
     ξ_t = γ^{t+1} and w_m = γ^{L−1−m}:
       out    = (Q′K′ᵀ ⊙ A) V + ξ ⊙ (Q′ S_in)
@@ -350,10 +373,8 @@ def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
       dQ′    = G K′ + ξ ⊙ (dO S_inᵀ)
       dK′    = Gᵀ Q′ + (w ⊙ V) dS_outᵀ
       dS_in  = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
-    and through the prologue (R1-R3: q′ = R q, k′ = d_k^{-1/2} R k with R an
-    orthogonal rotation per position) dq = Rᵀ dQ′, dk = d_k^{-1/2} Rᵀ dK′,
-    Rᵀ being the rotation by −n·θ.
-    """
+    Returns (q′, k′, dQ′, dK′, dV, dS_in): the gradients with respect to the
+    rotated operands, before the prologue's adjoint."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, L, d_k = q.shape
     d_v = v.shape[-1]
@@ -381,10 +402,80 @@ def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
             dv[:, h] += (w[None, :, None] * kp[:, h]) @ dSo
             dkp[:, h] += (w[None, :, None] * v[:, h]) @ np.swapaxes(dSo, -1, -2)
             dS_in[:, h] += np.power(g[h], float(L)) * dSo
+    return qp, kp, dqp, dkp, dv, dS_in
+
+
+def retention_backward(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
+                       d_state_out=None):
+    """Gradients of ``retention`` (no GroupNorm) with respect to q, k, v and
+    state_in, for the upstream gradients d_out (of out) and d_state_out (of
+    state_out, or None).  Returns (dq, dk, dv, d_state_in).
+
+    dQ′, dK′, dV and dS_in come from the chain rule through the parallel
+    form (``_rotated_grads``); then through the prologue (R1-R3: q′ = R q,
+    k′ = d_k^{-1/2} R k with R an orthogonal rotation per position)
+    dq = Rᵀ dQ′, dk = d_k^{-1/2} Rᵀ dK′, Rᵀ being the rotation by −n·θ.
+    """
+    _, _, dqp, dkp, dv, dS_in = _rotated_grads(q, k, v, gamma, theta, pos0, state_in, d_out,
+                                               d_state_out)
+    L, d_k = dqp.shape[-2], dqp.shape[-1]
     sin, cos = rotation_tables(np.arange(L) + int(pos0), theta)
     dq = theta_shift(dqp, -sin, cos)                                   # Rᵀ = rotation by −nθ
     dk = theta_shift(dkp, -sin, cos) / math.sqrt(d_k)
     return dq, dk, dv, dS_in
+
+
+def retention_param_grads(q, k, v, gamma, theta, pos0=0, state_in=None, d_out=None,
+                          d_state_out=None):
+    """Gradients of ``retention`` (no GroupNorm) with respect to the decay
+    rates γ [H] and the rotation frequencies θ [d_k/2], for the same
+    upstream gradients as ``retention_backward``.  Returns (d_gamma, d_theta).
+
+    [P1] §2 makes θ a learnable parameter; γ is set per head at
+    initialisation ([P1] §3) and is differentiated too, for callers that
+    learn it.  The gradients sum over the batch (and d_theta over the heads).
+
+    d_gamma: every γ-dependent factor of the parallel form with the state
+    terms (R4) is differentiated and contracted with what it multiplies:
+      ∂D_nm/∂γ = (n−m)·γ^{n−m−1}   below the diagonal (0 on and above it)
+      ∂ξ_t/∂γ  = (t+1)·γ^t          the state_in term of token t
+      ∂w_m/∂γ  = (L−1−m)·γ^{L−2−m}  key m's share of state_out
+      ∂γ^L/∂γ  = L·γ^{L−1}           state_in's share of state_out
+    d_theta: through the prologue.  Pair i of q′_t is pair i of q_t rotated
+    by the angle (pos0+t)·θ_i, so ∂q′_t/∂θ_i is (pos0+t)·rotate_every_two(q′_t)
+    on that pair and zero elsewhere; the same holds for k′_t (the 1/√d_k
+    scale rides along).  Both are contracted with dQ′, dK′.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, L, d_k = q.shape
+    g = _heads(gamma, H)
+    qp, kp, dqp, dkp, _, _ = _rotated_grads(q, k, v, gamma, theta, pos0, state_in, d_out,
+                                            d_state_out)
+    dO = _f64(d_out)
+    diff = (np.arange(L)[:, None] - np.arange(L)[None, :]).astype(np.float64)
+    t = np.arange(L, dtype=np.float64)
+    d_gamma = np.zeros(H)
+    for h in range(H):
+        gh = g[h]
+        dD = np.where(diff > 0, diff * np.power(gh, np.maximum(diff - 1.0, 0.0)), 0.0)
+        scores = qp[:, h] @ np.swapaxes(kp[:, h], -1, -2)              # q′_n · k′_m
+        dov = dO[:, h] @ np.swapaxes(v[:, h], -1, -2)                  # dO_n · v_m
+        d_gamma[h] = np.sum(scores * dov * dD[None])
+        if state_in is not None:
+            S0 = _f64(state_in)[:, h]
+            dxi = (t + 1.0) * np.power(gh, t)
+            d_gamma[h] += np.sum(dxi[None, :, None] * (qp[:, h] @ S0) * dO[:, h])
+        if d_state_out is not None:
+            dSo = _f64(d_state_out)[:, h]
+            e = L - 1.0 - t                                            # exponent of w_m
+            dw = np.where(e > 0, e * np.power(gh, np.maximum(e - 1.0, 0.0)), 0.0)
+            d_gamma[h] += np.einsum("m,bmk,bmv,bkv->", dw, kp[:, h], v[:, h], dSo)
+            if state_in is not None:
+                d_gamma[h] += L * np.power(gh, L - 1.0) * np.sum(dSo * _f64(state_in)[:, h])
+    pos = t + int(pos0)
+    per_elem = pos[None, None, :, None] * (dqp * rotate_every_two(qp) + dkp * rotate_every_two(kp))
+    d_theta = per_elem[..., 0::2].sum(axis=(0, 1, 2)) + per_elem[..., 1::2].sum(axis=(0, 1, 2))
+    return d_gamma, d_theta
 
 
 def decode_step(q, k, v, gamma, theta, pos, state, gn=None):

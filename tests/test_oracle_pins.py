@@ -288,6 +288,100 @@ def pin_backward_finite_differences():
     _backward_fd_check(False, False, 0)
 
 
+def _param_grads_fd_check(with_states, pos0):
+    """retention_param_grads against central differences in γ and θ of the
+    scalar <dO, out> + <dS_out, S_out>, the forward taken in the chunkwise
+    form with a ragged last chunk (B = 2: the gradients sum over the batch)."""
+    rng = np.random.default_rng(19 + pos0)
+    B, H, L, d_k, d_v = 2, 2, 7, 4, 3
+    q, k = rng.standard_normal((B, H, L, d_k)), rng.standard_normal((B, H, L, d_k))
+    v = rng.standard_normal((B, H, L, d_v))
+    S0 = 0.3 * rng.standard_normal((B, H, d_k, d_v)) if with_states else None
+    dO = rng.standard_normal((B, H, L, d_v))
+    dSo = rng.standard_normal((B, H, d_k, d_v)) if with_states else None
+    g, th = np.array([0.9, 0.6]), np.array([0.4, 1.3])
+
+    def f(g_, th_):
+        o, S = R.retention(q, k, v, g_, th_, pos0, S0, "chunkwise", 3)
+        return (o * dO).sum() + ((S * dSo).sum() if with_states else 0.0)
+
+    dg, dth = R.retention_param_grads(q, k, v, g, th, pos0, S0, dO, dSo)
+    eps = 1e-6
+    for i in range(2):
+        e = eps * np.eye(2)[i]
+        num_g = (f(g + e, th) - f(g - e, th)) / (2 * eps)
+        num_t = (f(g, th + e) - f(g, th - e)) / (2 * eps)
+        assert abs(num_g - dg[i]) < 1e-6 * max(1.0, abs(num_g)), ("gamma", i)
+        assert abs(num_t - dth[i]) < 1e-6 * max(1.0, abs(num_t)), ("theta", i)
+
+
+def pin_param_grads_finite_differences():
+    _param_grads_fd_check(True, 5)
+    _param_grads_fd_check(False, 0)
+
+
+def pin_theta_grad_position_shift_invariance():
+    """Without state terms the output depends on θ only through (n − m)·θ,
+    so the θ gradient is the same at every start position."""
+    rng = np.random.default_rng(23)
+    B, H, L, d_k, d_v = 1, 2, 9, 6, 2
+    q, k = rng.standard_normal((B, H, L, d_k)), rng.standard_normal((B, H, L, d_k))
+    v, dO = rng.standard_normal((B, H, L, d_v)), rng.standard_normal((B, H, L, d_v))
+    g, th = np.array([0.8, 0.97]), np.array([0.3, 0.05, 1.1])
+    _, a = R.retention_param_grads(q, k, v, g, th, 0, None, dO, None)
+    _, b = R.retention_param_grads(q, k, v, g, th, 1000, None, dO, None)
+    assert np.max(np.abs(a - b)) < 1e-9 * np.max(np.abs(a))
+    assert np.max(np.abs(a)) > 1e-3
+
+
+def pin_gamma_grad_single_token():
+    """One token: out = (q′·k′)v + γ·q′S_in, S_out = γS_in + k′ᵀv.  So with
+    no state the γ gradient is exactly 0, and with state_in and dS_out it
+    is Σ dO·(q′S_in) + <dS_out, S_in>."""
+    rng = np.random.default_rng(29)
+    q, k = rng.standard_normal((2, 1, 1, 4)), rng.standard_normal((2, 1, 1, 4))
+    v, dO = rng.standard_normal((2, 1, 1, 3)), rng.standard_normal((2, 1, 1, 3))
+    S0, dSo = rng.standard_normal((2, 1, 4, 3)), rng.standard_normal((2, 1, 4, 3))
+    g, th = np.array([0.7]), np.array([0.5, 2.0])
+    dg0, _ = R.retention_param_grads(q, k, v, g, th, 3, None, dO, None)
+    assert dg0[0] == 0.0
+    dg, _ = R.retention_param_grads(q, k, v, g, th, 3, S0, dO, dSo)
+    qp, _ = R.prologue(q, k, th, 3)
+    ref = np.sum(dO[:, 0, 0] * np.einsum("bk,bkv->bv", qp[:, 0, 0], S0[:, 0])) + np.sum(dSo * S0)
+    assert abs(dg[0] - ref) < 1e-12 * max(1.0, abs(ref))
+
+
+def pin_groupnorm_backward():
+    """groupnorm_backward against central differences of <d_y, group_norm(o)>
+    in o, weight and bias, and against torch autograd of
+    torch.nn.functional.group_norm (float64, one group per head)."""
+    rng = np.random.default_rng(31)
+    B, H, L, d_v = 2, 2, 3, 5
+    o = rng.standard_normal((B, H, L, d_v)) * 2 + 0.5
+    w, b = rng.standard_normal((H, d_v)), rng.standard_normal((H, d_v))
+    dy = rng.standard_normal((B, H, L, d_v))
+    d_o, d_w, d_b = R.groupnorm_backward(o, dy, 1e-3, w)
+    f = lambda o_, w_, b_: np.sum(dy * R.group_norm(o_, 1e-3, w_, b_))
+    eps = 1e-6
+    for x, ref, which in ((o, d_o, 0), (w, d_w, 1), (b, d_b, 2)):
+        for idx in np.ndindex(x.shape):
+            a = [o.copy(), w.copy(), b.copy()]
+            a[which][idx] += eps
+            fp = f(*a)
+            a[which][idx] -= 2 * eps
+            num = (fp - f(*a)) / (2 * eps)
+            assert abs(num - ref[idx]) < 1e-6 * max(1.0, abs(num)), (which, idx)
+    x = torch.from_numpy(o).permute(0, 2, 1, 3).reshape(B * L, H * d_v).requires_grad_(True)
+    tw = torch.from_numpy(w.reshape(-1)).requires_grad_(True)
+    tb = torch.from_numpy(b.reshape(-1)).requires_grad_(True)
+    y = torch.nn.functional.group_norm(x, H, tw, tb, eps=1e-3)
+    y.backward(torch.from_numpy(dy).permute(0, 2, 1, 3).reshape(B * L, H * d_v))
+    t_do = x.grad.reshape(B, L, H, d_v).permute(0, 2, 1, 3).numpy()
+    assert _rel(d_o, t_do) < 1e-12
+    assert _rel(d_w, tw.grad.reshape(H, d_v).numpy()) < 1e-12
+    assert _rel(d_b, tb.grad.reshape(H, d_v).numpy()) < 1e-12
+
+
 # Row-normalised decay (R9)
 def pin_decay_row_sums_geometric_series():
     """r_N = Σ_{i≤N} γ^i is the geometric series (1 − γ^{N+1}) / (1 − γ); N + 1 at γ = 1."""
@@ -408,6 +502,8 @@ PINS = [
     pin_theta_zero_is_identity, pin_rotation_preserves_pair_norms, pin_position_shift_invariance,
     pin_exact_causality, pin_chunk_limits, pin_split_call, pin_ragged_tail, pin_linearity,
     pin_decode_steps_equal_recurrent, pin_groupnorm_matches_torch, pin_backward_finite_differences,
+    pin_param_grads_finite_differences, pin_theta_grad_position_shift_invariance,
+    pin_gamma_grad_single_token, pin_groupnorm_backward,
     pin_decay_row_sums_geometric_series, pin_normalised_gamma_one_is_a_running_mean,
     pin_normalised_cancels_under_groupnorm, pin_normalised_split_calls,
     pin_block_projections_feed_the_core, pin_block_gate_and_projection,
@@ -450,13 +546,23 @@ MUTANTS = {
                     "((o - mu) ** 2).sum(axis=-1, keepdims=True) / (o.shape[-1] - 1)"),
     "gn_eps_outside": ("group_norm", "np.sqrt(var + float(eps))", "(np.sqrt(var) + float(eps))"),
     "decode_no_decay": ("decode_step", "S = g * state +", "S = state +"),
-    "bwd_no_state_in_term": ("retention_backward", "dqp[:, h] += xi[None, :, None] * (dO[:, h] @",
+    "bwd_no_state_in_term": ("_rotated_grads", "dqp[:, h] += xi[None, :, None] * (dO[:, h] @",
                              "dqp[:, h] += 0.0 * xi[None, :, None] * (dO[:, h] @"),
     "bwd_adjoint_not_inverse": ("retention_backward", "dq = theta_shift(dqp, -sin, cos)",
                                 "dq = theta_shift(dqp, sin, cos)"),
-    "bwd_dk_untransposed": ("retention_backward", "np.swapaxes(G, -1, -2) @ qp[:, h]", "G @ qp[:, h]"),
-    "bwd_dsin_power": ("retention_backward", "np.power(g[h], float(L)) * dSo", "np.power(g[h], float(L - 1)) * dSo"),
+    "bwd_dk_untransposed": ("_rotated_grads", "np.swapaxes(G, -1, -2) @ qp[:, h]", "G @ qp[:, h]"),
+    "bwd_dsin_power": ("_rotated_grads", "np.power(g[h], float(L)) * dSo", "np.power(g[h], float(L - 1)) * dSo"),
     "bwd_dk_no_scale": ("retention_backward", "/ math.sqrt(d_k)", ""),
+    "pg_mask_derivative_power": ("retention_param_grads", "np.maximum(diff - 1.0, 0.0)", "np.maximum(diff, 0.0)"),
+    "pg_xi_derivative": ("retention_param_grads", "dxi = (t + 1.0) * np.power(gh, t)", "dxi = t * np.power(gh, t)"),
+    "pg_w_derivative": ("retention_param_grads", "e = L - 1.0 - t", "e = L - t"),
+    "pg_sin_into_sout": ("retention_param_grads", "L * np.power(gh, L - 1.0)", "(L - 1.0) * np.power(gh, L - 1.0)"),
+    "pg_theta_local_positions": ("retention_param_grads", "pos = t + int(pos0)", "pos = t"),
+    "pg_theta_no_k_term": ("retention_param_grads", " + dkp * rotate_every_two(kp)", ""),
+    "gnb_no_xhat_term": ("groupnorm_backward", " - xhat * (gw * xhat).mean(axis=-1, keepdims=True)", ""),
+    "gnb_weight_not_applied": ("groupnorm_backward", "gw = d_y * w[None, :, None, :]", "gw = d_y"),
+    "gnb_dweight_no_xhat": ("groupnorm_backward", "d_weight = (d_y * xhat).sum(axis=(0, 2))",
+                            "d_weight = d_y.sum(axis=(0, 2))"),
     "rowsum_local_positions": ("decay_row_sums", "np.cumsum(terms)[int(pos0):]", "np.cumsum(terms)[:int(L)]"),
     "rowsum_off_by_one": ("decay_row_sums", "np.arange(n_max,", "np.arange(1, n_max + 1,"),
     "block_q_from_w_k": ("msr_block", 'q = np.einsum("bld,dhk->bhlk", x, _f64(w_q))',
