@@ -444,6 +444,21 @@ def main():
         if world > 1:
             dist.barrier()
 
+    def time_launches(fn, n, warm=3):
+        """Average device time of one fn() call (CUDA events on the launching
+        stream, synchronised on both sides, after warm-up calls)."""
+        for _ in range(warm):
+            if fn() != _lib.RET_OK:
+                raise RuntimeError("warm-up call failed")
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
     # The timed loop calls the C ABI directly with arguments marshalled once,
     # so host-side Python work cannot leave gaps between launches.
     import ctypes as C
@@ -864,7 +879,56 @@ def main():
             "kernels_ms_per_step": step_ms,
             "gpu_launches": int(round(nb_k / bhook * args.backward_steps)),
             "clocks": bsampler.summary()}
+
+        # γ and θ gradients from this forward (out, s_out) and backward (grads, dsi):
+        # two HBM-bound row passes over 8 token-major tensors plus the states
+        if lib.ret_chunkwise(*(cargs[:14] + (vp(s_out),) + cargs[15:])) != _lib.RET_OK:   # fills s_out
+            raise RuntimeError("ret_chunkwise with state_out failed")
+        pws_n = C.c_size_t(0)
+        lib.ret_chunkwise_param_grads_plan(w.B, w.H, w.L, w.d_k, w.d_v, C.byref(pws_n))
+        pws = torch.empty(max(pws_n.value, 1), dtype=torch.uint8, device=dev)
+        dgam = torch.empty(w.H, dtype=torch.float32, device=dev)
+        dthe = torch.empty(w.d_k // 2, dtype=torch.float32, device=dev)
+        pargs = (vp(q), vp(k), vp(v), vp(d_o), _lib.RET_BF16, vp(out), _lib.RET_BF16, vp(grads[0]),
+                 vp(grads[1]), vp(grads[2]), _lib.RET_BF16, fptr(garr), w.B, w.H, w.L, w.d_k, w.d_v, 0,
+                 vp(s_in), vp(dsi), vp(s_out), vp(dso), vp(dgam), vp(dthe), vp(pws), pws_n.value,
+                 C.c_void_p(stream.cuda_stream))
+        pms = time_launches(lambda: lib.ret_chunkwise_param_grads(*pargs), 10)
+        tok = w.B * w.H * w.L
+        pbytes = tok * (4 * w.d_v + 4 * w.d_k) * 2 + 4 * w.B * w.H * w.d_k * w.d_v * 4
+        pgbs = pbytes / (pms / 1e3) / 1e9
+        backward["param_grads"] = {
+            "metric": "gamma/theta gradient pass GB/s", "value": pgbs, "unit": "GB/s", "ms_per_call": pms,
+            "launches_per_call": 3, "algorithmic_bytes_per_call": pbytes,
+            "roofline": {"bound": "hbm", "achieved": pgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": pgbs / peaks["hbm_gbs"], "traffic": None}}
+        del pws, dgam, dthe
         del bws, grads, dsi, d_o, dso, gi
+
+        # GroupNorm backward at the 1.3B shape (bf16 rows of 512 channels, with weight)
+        gw_ = WORKLOADS["msr1p3b"]
+        gg = torch.Generator(device=dev).manual_seed(12)
+        gx = torch.randn((gw_.B, gw_.H, gw_.L, gw_.d_v), generator=gg, device=dev).to(torch.bfloat16)
+        gdy = torch.randn((gw_.B, gw_.H, gw_.L, gw_.d_v), generator=gg, device=dev).to(torch.bfloat16)
+        gwt = torch.randn((gw_.H, gw_.d_v), generator=gg, device=dev)
+        gdx = torch.empty_like(gx)
+        gdw, gdb = torch.empty_like(gwt), torch.empty_like(gwt)
+        gws_n = C.c_size_t(0)
+        lib.ret_groupnorm_backward_plan(gw_.B, gw_.H, gw_.L, gw_.d_v, C.byref(gws_n))
+        gws = torch.empty(gws_n.value, dtype=torch.uint8, device=dev)
+        gargs = (vp(gx), vp(gdy), _lib.RET_BF16, vp(gwt), C.c_float(1e-5), gw_.B, gw_.H, gw_.L, gw_.d_v,
+                 vp(gdx), _lib.RET_BF16, vp(gdw), vp(gdb), vp(gws), gws_n.value, C.c_void_p(stream.cuda_stream))
+        gms = time_launches(lambda: lib.ret_groupnorm_backward(*gargs), 20)
+        gbytes = 3 * gx.numel() * 2 + gws_n.value
+        ggbs = gbytes / (gms / 1e3) / 1e9
+        backward["groupnorm_backward"] = {
+            "metric": "GroupNorm backward GB/s", "value": ggbs, "unit": "GB/s", "ms_per_call": gms,
+            "config": {"workload": gw_.name, "B": gw_.B, "H": gw_.H, "L": gw_.L, "d_v": gw_.d_v,
+                       "dtype": "bf16 x, dy, dx; fp32 weight and parameter gradients"},
+            "launches_per_call": 2, "algorithmic_bytes_per_call": gbytes,
+            "roofline": {"bound": "hbm", "achieved": ggbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ggbs / peaks["hbm_gbs"], "traffic": None}}
+        del gx, gdy, gwt, gdx, gdw, gdb, gws
 
     # ---------------- end to end through the API with host buffers ----------------
     # Every step copies its inputs host → device from pinned memory, runs

@@ -253,6 +253,78 @@ ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, const float* gamma, int 
                                        size_t* workspace_bytes);
 
 /* ------------------------------------------------------------------------
+ * ret_chunkwise_param_grads — gradients of ret_chunkwise (without the
+ * GroupNorm epilogue) with respect to the decay rates γ [H] and the rotation
+ * frequencies θ [d_k/2] («从RoPE到Retention…» §2 makes θ learnable; §3 sets
+ * γ per head).  Differentiating the decay factors γ^{n−m}, γ^{t+1}
+ * (state_in) and γ^{L−1−m}, γ^L (state_out) of the parallel form (§3, §4.1)
+ * and the rotation angles (pos0 + t)·θ_i of the Θ prologue (§2) gives, with
+ * t the local token index and J(a, b) = (−b, a) on each pair:
+ *   dγ_h = γ_h⁻¹ Σ_b [ Σ_t t·(dO_t·o_t − v_t·dv_t) + <S_in, dS_in>
+ *                       + (L − 1)·<dS_out, S_out> ]
+ *   dθ_i = Σ_{b,h,t} (pos0 + t)·( dq_t·J q_t + dk_t·J k_t )   on pair i
+ * so the call consumes the forward call's out and state_out and the
+ * backward call's dq, dk, dv and d_state_in for the same inputs, upstream
+ * gradients and pos0; it reads each of them once (HBM-bound row passes).
+ * q, k, v, d_out: DEVICE, in_dt, [B, H, L, d_k|d_v].  out: DEVICE, out_dt,
+ * [B, H, L, d_v] (the forward output before any GroupNorm).  dq, dk, dv:
+ * DEVICE, grad_dt.  state_in / d_state_in and state_out / d_state_out:
+ * DEVICE fp32 [B, H, d_k, d_v] or NULL (zero); d_state_in is required when
+ * state_in is given and state_out when d_state_out is given (dγ only).
+ * gamma: HOST [H], each in (0, 1] (read during the call; dγ only).
+ * d_gamma [H], d_theta [d_k/2]: DEVICE fp32 outputs, overwritten; either may
+ * be NULL (not computed; then its inputs may be NULL too), not both.
+ * workspace: DEVICE, at least ret_chunkwise_param_grads_plan's bytes.
+ * Deterministic: fixed-order sums (fp32 per 64-token segment, double across
+ * segments).  Validation and errors as for the other entry points.
+ * ------------------------------------------------------------------------ */
+ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v,
+                                     const void* d_out, ret_dtype in_dt, const void* out,
+                                     ret_dtype out_dt, const void* dq, const void* dk,
+                                     const void* dv, ret_dtype grad_dt, const float* gamma,
+                                     int B, int H, int L, int d_k, int d_v, int64_t pos0,
+                                     const float* state_in, const float* d_state_in,
+                                     const float* state_out, const float* d_state_out,
+                                     float* d_gamma, float* d_theta, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of ret_chunkwise_param_grads. */
+ret_status ret_chunkwise_param_grads_plan(int B, int H, int L, int d_k, int d_v,
+                                          size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
+ * ret_groupnorm — the per-head GroupNorm epilogue as a call of its own
+ * («从RoPE到Retention…» §5): each (b, h, t) row of x [B, H, L, d_v] is
+ * normalised over its d_v channels (biased variance, gn->eps), then scaled
+ * and shifted by gn->weight / gn->bias [H, d_v] (DEVICE fp32, each may be
+ * NULL).  gn->enabled is ignored.  x: DEVICE, x_dt; y: DEVICE, y_dt; y may
+ * be x when the types agree.  With ret_groupnorm_backward it gives the
+ * training path: forward ret_chunkwise without GroupNorm, then this call.
+ * ------------------------------------------------------------------------ */
+ret_status ret_groupnorm(const void* x, ret_dtype x_dt, void* y, ret_dtype y_dt, int B, int H,
+                         int L, int d_v, const ret_gn* gn, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------
+ * ret_groupnorm_backward — gradients of ret_groupnorm for the upstream
+ * gradient d_y: with x̂ = (x − μ)·rstd and g = d_y ⊙ weight per row,
+ *   d_x = rstd·(g − mean(g) − x̂·mean(g ⊙ x̂)),
+ *   d_weight = Σ_{b,t} d_y ⊙ x̂,   d_bias = Σ_{b,t} d_y   ([H, d_v]).
+ * x (the GroupNorm input), d_y: DEVICE, x_dt, [B, H, L, d_v], 16-byte
+ * aligned.  weight: DEVICE fp32 [H, d_v] or NULL (ones).  d_x: DEVICE,
+ * grad_dt, must not alias x or d_y.  d_weight, d_bias: DEVICE fp32 [H, d_v]
+ * or NULL (not computed); when either is wanted the workspace must hold
+ * ret_groupnorm_backward_plan's bytes (else it may be NULL).  Sums are in a
+ * fixed order (deterministic).
+ * ------------------------------------------------------------------------ */
+ret_status ret_groupnorm_backward(const void* x, const void* d_y, ret_dtype x_dt,
+                                  const float* weight, float eps, int B, int H, int L, int d_v,
+                                  void* d_x, ret_dtype grad_dt, float* d_weight, float* d_bias,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes of ret_groupnorm_backward (for d_weight / d_bias). */
+ret_status ret_groupnorm_backward_plan(int B, int H, int L, int d_v, size_t* workspace_bytes);
+
+/* ------------------------------------------------------------------------
  * ret_parallel — parallel form O = (Q′K′ᵀ ⊙ D) V + γ^{t+1} q′_t S_in
  * («从RoPE到Retention…» §4.1; RetNet 保留网络 explainer, 并行表征).
  * O(L²) work.  state_out (optional) is the closed-form final state.

@@ -230,6 +230,81 @@ def chunkwise_backward(q, k, v, d_out, gamma, theta, chunk: int, pos0: int = 0, 
     return dq, dk, dv, d_state_in
 
 
+def param_grads(q, k, v, d_out, out, dq, dk, dv, gamma, pos0: int = 0, state_in=None,
+                d_state_in=None, state_out=None, d_state_out=None, want_gamma: bool = True,
+                want_theta: bool = True, workspace=None, stream=None):
+    """Gradients with respect to γ [H] and θ [d_k/2] (fp32 device tensors;
+    None where not wanted), from the forward call's out / state_out and the
+    backward call's dq, dk, dv / d_state_in for the same inputs."""
+    lib = load()
+    B, H, L, d_k, d_v = _check_seq(q, k, v)
+    idt = _dtype_code(q)
+    _dev(d_out, "d_out", q.dtype, (B, H, L, d_v))
+    _dev(out, "out", None, (B, H, L, d_v))
+    gdt = _dtype_code(dq)
+    for name, t, shp in (("dq", dq, (B, H, L, d_k)), ("dk", dk, (B, H, L, d_k)), ("dv", dv, (B, H, L, d_v))):
+        _dev(t, name, dq.dtype, shp)
+    garr, gp = _host_f32(gamma, H, "gamma")
+    sshape = (B, H, d_k, d_v)
+    d_gamma = torch.empty(H, dtype=torch.float32, device=q.device) if want_gamma else None
+    d_theta = torch.empty(d_k // 2, dtype=torch.float32, device=q.device) if want_theta else None
+    nb = C.c_size_t(0)
+    check("ret_chunkwise_param_grads_plan", lib.ret_chunkwise_param_grads_plan(B, H, L, d_k, d_v, C.byref(nb)))
+    wsp, wsn, ws = _workspace(nb.value, q.device, workspace)
+    st = lib.ret_chunkwise_param_grads(
+        _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(d_out, "d_out"), idt, _dev(out, "out"),
+        _dtype_code(out), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"), gdt, gp, B, H, L, d_k, d_v,
+        int(pos0), _dev(state_in, "state_in", torch.float32, sshape),
+        _dev(d_state_in, "d_state_in", torch.float32, sshape),
+        _dev(state_out, "state_out", torch.float32, sshape),
+        _dev(d_state_out, "d_state_out", torch.float32, sshape), _dev(d_gamma, "d_gamma"),
+        _dev(d_theta, "d_theta"), wsp, wsn, _stream(stream))
+    check("ret_chunkwise_param_grads", st)
+    return d_gamma, d_theta
+
+
+def groupnorm(x, eps: float = 1e-5, weight=None, bias=None, out=None, out_dtype=None, stream=None):
+    """Per-head GroupNorm of x [B, H, L, d_v] over d_v (out may be x)."""
+    lib = load()
+    if x.dim() != 4:
+        raise ValueError("x: [B, H, L, d_v]")
+    B, H, L, d_v = x.shape
+    if out is None:
+        out = torch.empty(x.shape, dtype=out_dtype or x.dtype, device=x.device)
+    _dev(out, "out", None, x.shape)
+    gns, keep = _gn_struct({"eps": eps, "weight": weight, "bias": bias}, H, d_v, x.device)
+    st = lib.ret_groupnorm(_dev(x, "x"), _dtype_code(x), _dev(out, "out"), _dtype_code(out), B, H, L, d_v,
+                           gns, _stream(stream))
+    check("ret_groupnorm", st)
+    return out
+
+
+def groupnorm_backward(x, d_y, eps: float = 1e-5, weight=None, grad_dtype=None, want_params: bool = True,
+                       workspace=None, stream=None):
+    """Gradients of ``groupnorm``: (d_x, d_weight, d_bias); the last two are
+    fp32 [H, d_v] (None unless want_params)."""
+    lib = load()
+    if x.dim() != 4:
+        raise ValueError("x: [B, H, L, d_v]")
+    B, H, L, d_v = x.shape
+    _dev(d_y, "d_y", x.dtype, x.shape)
+    if weight is not None:
+        _dev(weight, "weight", torch.float32)
+        if weight.numel() != H * d_v:
+            raise ValueError("weight must have H*d_v values")
+    d_x = torch.empty(x.shape, dtype=grad_dtype or x.dtype, device=x.device)
+    d_w = torch.empty((H, d_v), dtype=torch.float32, device=x.device) if want_params else None
+    d_b = torch.empty((H, d_v), dtype=torch.float32, device=x.device) if want_params else None
+    nb = C.c_size_t(0)
+    check("ret_groupnorm_backward_plan", lib.ret_groupnorm_backward_plan(B, H, L, d_v, C.byref(nb)))
+    wsp, wsn, ws = _workspace(nb.value if want_params else 0, x.device, workspace)
+    st = lib.ret_groupnorm_backward(_dev(x, "x"), _dev(d_y, "d_y"), _dtype_code(x), _dev(weight, "weight"),
+                                    float(eps), B, H, L, d_v, _dev(d_x, "d_x"), _dtype_code(d_x),
+                                    _dev(d_w, "d_weight"), _dev(d_b, "d_bias"), wsp, wsn, _stream(stream))
+    check("ret_groupnorm_backward", st)
+    return d_x, d_w, d_b
+
+
 def parallel(q, k, v, gamma, theta, pos0: int = 0, state_in=None, return_state: bool = False,
              out=None, out_dtype=None, gn=None, workspace=None, stream=None):
     """Parallel-form retention.  Returns (out, state_out or None)."""

@@ -254,12 +254,13 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// GroupNorm over d_v for each (b, h, t) row: one warp per row, fp32 input.
-// («从RoPE到Retention…» §5; one group per head, biased variance.)
+// GroupNorm over d_v for each (b, h, t) row: one warp per row.
+// («从RoPE到Retention…» §5; one group per head, biased variance.)  y may be
+// x itself (same type): every value is read by the lane that writes it, and
+// the reductions between the passes order all reads before any write.
 // ---------------------------------------------------------------------------
-template <typename Tout>
-__global__ void __launch_bounds__(256) groupnorm_kernel(const float* __restrict__ x,
-                                                        Tout* __restrict__ y,
+template <typename Tx, typename Tout>
+__global__ void __launch_bounds__(256) groupnorm_kernel(const Tx* x, Tout* y,
                                                         const float* __restrict__ w,
                                                         const float* __restrict__ b, int H,
                                                         int L, int d_v, size_t rows, float eps) {
@@ -267,15 +268,15 @@ __global__ void __launch_bounds__(256) groupnorm_kernel(const float* __restrict_
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int h = static_cast<int>((row / L) % H);
-  const float* xr = x + row * d_v;
+  const Tx* xr = x + row * d_v;
   float s = 0.f;
-  for (int c = lane; c < d_v; c += 32) s += xr[c];
+  for (int c = lane; c < d_v; c += 32) s += to_f32(xr[c]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float mu = s / static_cast<float>(d_v);
   float q = 0.f;
   for (int c = lane; c < d_v; c += 32) {
-    const float dlt = xr[c] - mu;
+    const float dlt = to_f32(xr[c]) - mu;
     q = fmaf(dlt, dlt, q);
   }
 #pragma unroll
@@ -283,7 +284,7 @@ __global__ void __launch_bounds__(256) groupnorm_kernel(const float* __restrict_
   const float rstd = rsqrtf(q / static_cast<float>(d_v) + eps);
   Tout* yr = y + row * d_v;
   for (int c = lane; c < d_v; c += 32) {
-    float val = (xr[c] - mu) * rstd;
+    float val = (to_f32(xr[c]) - mu) * rstd;
     if (w) val *= w[h * d_v + c];
     if (b) val += b[h * d_v + c];
     yr[c] = from_f32<Tout>(val);

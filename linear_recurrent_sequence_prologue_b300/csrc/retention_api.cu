@@ -21,6 +21,7 @@
 #include "kernel_tc_parallel.cuh"
 #include "kernel_tc_pair.cuh"
 #include "kernel_tc_gemm.cuh"
+#include "kernels_grad.cuh"
 
 using namespace ret;
 
@@ -383,7 +384,7 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
   if (ofp) {
     const size_t rows = static_cast<size_t>(BH) * L;
     Mark m("groupnorm", st);
-    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
         ofp, out, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
   }
   return last_launch();
@@ -551,7 +552,7 @@ ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __n
   if (ofp) {
     const size_t r = static_cast<size_t>(BH) * L;
     Mark m("groupnorm", st);
-    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
+    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
         ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
   }
   return last_launch();
@@ -739,7 +740,7 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   if (ofp) {
     const size_t r = static_cast<size_t>(BH) * L;
     Mark m("groupnorm", st);
-    simt::groupnorm_kernel<Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
+    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
         ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
   }
   return last_launch();
@@ -1865,6 +1866,237 @@ ret_status ret_msr_block(const void* x, const void* w_q, const void* w_k, const 
   gp.out = z;   // z = (swish(x·W_G) ⊙ GN(O))·W_O
   gp.out_f32 = z_dt == RET_F32 ? 1 : 0;
   if (launch_gemm<tcg::PLAIN>(ao, M, HV, w_o, D_out, gp, cc, stream, "proj_out") != cudaSuccess) return RET_ECUDA;
+  return last_launch();
+}
+
+}  // extern "C"
+
+namespace {
+// ---------------------------------------------------------------------------
+// Parameter gradients and GroupNorm backward: workspace layouts and launches
+// ---------------------------------------------------------------------------
+struct ParamPlan {
+  int nseg;
+  size_t off_g, off_s, off_t, bytes;
+};
+
+ParamPlan plan_param_grads(int B, int H, int L, int d_k) {
+  ParamPlan p{};
+  p.nseg = (L + grad::kRowsPerBlock - 1) / grad::kRowsPerBlock;
+  const size_t nblk = static_cast<size_t>(B) * H * p.nseg;
+  size_t off = 0;
+  p.off_g = off; off += up256(nblk * sizeof(double));
+  p.off_s = off; off += up256(static_cast<size_t>(B) * H * grad::kStateSlices * sizeof(double));
+  p.off_t = off; off += up256(nblk * static_cast<size_t>(d_k / 2) * sizeof(float));
+  p.bytes = off;
+  return p;
+}
+
+template <typename Tin, typename Tout, typename Tg>
+void launch_param_rows(const grad::ParamArgs& a, unsigned grid, bool vec, cudaStream_t st) {
+  if (vec) grad::param_rows_kernel<Tin, Tout, Tg, true><<<grid, 256, 0, st>>>(a);
+  else grad::param_rows_kernel<Tin, Tout, Tg, false><<<grid, 256, 0, st>>>(a);
+}
+
+template <typename Tin, typename Tout>
+void launch_param_rows_g(const grad::ParamArgs& a, unsigned grid, bool vec, ret_dtype g_dt,
+                         cudaStream_t st) {
+  if (g_dt == RET_F32) launch_param_rows<Tin, Tout, float>(a, grid, vec, st);
+  else launch_param_rows<Tin, Tout, __nv_bfloat16>(a, grid, vec, st);
+}
+
+template <typename Tx, typename Tg, int NV>
+void launch_gn_backward_nv(const void* x, const void* dy, const float* w, void* dx, float* wpart,
+                           int H, int L, int d_v, int nseg, float eps, unsigned grid, bool vec,
+                           cudaStream_t st) {
+  const size_t smem = wpart ? static_cast<size_t>(8) * d_v * sizeof(float) : 0;
+  if (vec)
+    grad::gn_backward_kernel<Tx, Tg, true, NV><<<grid, 128, smem, st>>>(
+        static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w, static_cast<Tg*>(dx), wpart, H,
+        L, d_v, nseg, eps);
+  else
+    grad::gn_backward_kernel<Tx, Tg, false, NV><<<grid, 128, smem, st>>>(
+        static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w, static_cast<Tg*>(dx), wpart, H,
+        L, d_v, nseg, eps);
+}
+
+// NV = channels per lane: the smallest of 8, 16, 32 with d_v ≤ 32·NV.
+template <typename Tx, typename Tg>
+void launch_gn_backward(const void* x, const void* dy, const float* w, void* dx, float* wpart,
+                        int H, int L, int d_v, int nseg, float eps, unsigned grid, bool vec,
+                        cudaStream_t st) {
+  if (d_v <= 256)
+    launch_gn_backward_nv<Tx, Tg, 8>(x, dy, w, dx, wpart, H, L, d_v, nseg, eps, grid, vec, st);
+  else if (d_v <= 512)
+    launch_gn_backward_nv<Tx, Tg, 16>(x, dy, w, dx, wpart, H, L, d_v, nseg, eps, grid, vec, st);
+  else
+    launch_gn_backward_nv<Tx, Tg, 32>(x, dy, w, dx, wpart, H, L, d_v, nseg, eps, grid, vec, st);
+}
+
+size_t gn_backward_bytes(int B, int H, int L, int d_v) {
+  const size_t nseg = (static_cast<size_t>(L) + grad::kRowsPerBlock - 1) / grad::kRowsPerBlock;
+  return up256(static_cast<size_t>(B) * H * nseg * 2 * d_v * sizeof(float));
+}
+
+bool ok_dt(ret_dtype d) { return d == RET_F32 || d == RET_BF16; }
+}  // namespace
+
+extern "C" {
+
+ret_status ret_groupnorm(const void* x, ret_dtype x_dt, void* y, ret_dtype y_dt, int B, int H,
+                         int L, int d_v, const ret_gn* gn, cudaStream_t stream) {
+  Range nv("ret_groupnorm");
+  if (!x || !y || !gn || !ok_dt(x_dt) || !ok_dt(y_dt)) return RET_EINVAL;
+  if (B < 1 || H < 1 || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  const int64_t rows = static_cast<int64_t>(B) * H * L;
+  if (rows >= (int64_t(1) << 31)) return RET_EINVAL;
+  if (!(gn->eps > 0.f) || !std::isfinite(gn->eps)) return RET_EINVAL;
+  if (x == y && x_dt != y_dt) return RET_EINVAL;   // in place only with one type
+  Mark m("groupnorm", stream);
+  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
+  const size_t r = static_cast<size_t>(rows);
+  if (x_dt == RET_F32 && y_dt == RET_F32)
+    simt::groupnorm_kernel<float, float><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(x), static_cast<float*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+  else if (x_dt == RET_F32)
+    simt::groupnorm_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+  else if (y_dt == RET_F32)
+    simt::groupnorm_kernel<__nv_bfloat16, float><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+  else
+    simt::groupnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), gn->weight, gn->bias, H, L, d_v, r,
+        gn->eps);
+  return last_launch();
+}
+
+ret_status ret_groupnorm_backward_plan(int B, int H, int L, int d_v, size_t* workspace_bytes) {
+  if (!workspace_bytes || B < 1 || H < 1 || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  *workspace_bytes = gn_backward_bytes(B, H, L, d_v);
+  return RET_OK;
+}
+
+ret_status ret_groupnorm_backward(const void* x, const void* d_y, ret_dtype x_dt,
+                                  const float* weight, float eps, int B, int H, int L, int d_v,
+                                  void* d_x, ret_dtype grad_dt, float* d_weight, float* d_bias,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_groupnorm_backward");
+  if (!x || !d_y || !d_x || !ok_dt(x_dt) || !ok_dt(grad_dt)) return RET_EINVAL;
+  if (!al16(x) || !al16(d_y) || !al16(d_x) || (weight && !al16(weight))) return RET_EINVAL;
+  if (B < 1 || H < 1 || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  if (static_cast<int64_t>(B) * H * L >= (int64_t(1) << 31)) return RET_EINVAL;
+  if (!(eps > 0.f) || !std::isfinite(eps)) return RET_EINVAL;
+  if (d_x == x || d_x == d_y) return RET_EINVAL;
+  const int nseg = (L + grad::kRowsPerBlock - 1) / grad::kRowsPerBlock;
+  const int64_t nblk = static_cast<int64_t>(B) * H * nseg;
+  float* wpart = nullptr;
+  if (d_weight || d_bias) {
+    if (!workspace || !al16(workspace) || workspace_bytes < gn_backward_bytes(B, H, L, d_v))
+      return RET_EWORKSPACE;
+    wpart = static_cast<float*>(workspace);
+  }
+  const bool vec = d_v % 8 == 0;
+  const unsigned grid = static_cast<unsigned>(nblk);
+  {
+    Mark m("gn_backward", stream);
+    if (x_dt == RET_F32) {
+      if (grad_dt == RET_F32)
+        launch_gn_backward<float, float>(x, d_y, weight, d_x, wpart, H, L, d_v, nseg, eps, grid, vec, stream);
+      else
+        launch_gn_backward<float, __nv_bfloat16>(x, d_y, weight, d_x, wpart, H, L, d_v, nseg, eps, grid, vec, stream);
+    } else {
+      if (grad_dt == RET_F32)
+        launch_gn_backward<__nv_bfloat16, float>(x, d_y, weight, d_x, wpart, H, L, d_v, nseg, eps, grid, vec, stream);
+      else
+        launch_gn_backward<__nv_bfloat16, __nv_bfloat16>(x, d_y, weight, d_x, wpart, H, L, d_v, nseg, eps, grid,
+                                                         vec, stream);
+    }
+  }
+  ret_status s = last_launch();
+  if (s != RET_OK || !wpart) return s;
+  Mark m("gn_param_finish", stream);
+  grad::gn_param_finish_kernel<<<dim3((d_v + 31) / 32, H), 256, 0, stream>>>(wpart, d_weight, d_bias, B, H,
+                                                                             d_v, nseg);
+  return last_launch();
+}
+
+ret_status ret_chunkwise_param_grads_plan(int B, int H, int L, int d_k, int d_v,
+                                          size_t* workspace_bytes) {
+  if (!workspace_bytes || B < 1 || H < 1 || H > kMaxHeads || L < 1) return RET_EINVAL;
+  if (d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  *workspace_bytes = plan_param_grads(B, H, L, d_k).bytes;
+  return RET_OK;
+}
+
+ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v,
+                                     const void* d_out, ret_dtype in_dt, const void* out,
+                                     ret_dtype out_dt, const void* dq, const void* dk,
+                                     const void* dv, ret_dtype grad_dt, const float* gamma,
+                                     int B, int H, int L, int d_k, int d_v, int64_t pos0,
+                                     const float* state_in, const float* d_state_in,
+                                     const float* state_out, const float* d_state_out,
+                                     float* d_gamma, float* d_theta, void* workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  Range nv("ret_chunkwise_param_grads");
+  if (!ok_dt(in_dt) || !ok_dt(out_dt) || !ok_dt(grad_dt)) return RET_EINVAL;
+  if (!d_gamma && !d_theta) return RET_EINVAL;
+  if (B < 1 || H < 1 || H > kMaxHeads || L < 1) return RET_EINVAL;
+  if (d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 || d_v > 1024) return RET_EINVAL;
+  if (pos0 < 0 || pos0 + L > kMaxPos) return RET_EINVAL;
+  if (static_cast<int64_t>(B) * H * L >= (int64_t(1) << 31)) return RET_EINVAL;
+  const void* need_t[4] = {q, k, dq, dk};
+  const void* need_g[4] = {v, d_out, out, dv};
+  if (d_theta)
+    for (const void* p : need_t)
+      if (!p || !al16(p)) return RET_EINVAL;
+  if (d_gamma) {
+    for (const void* p : need_g)
+      if (!p || !al16(p)) return RET_EINVAL;
+    if (!gamma) return RET_EINVAL;
+    for (int h = 0; h < H; ++h)
+      if (!(gamma[h] > 0.f) || !(gamma[h] <= 1.f)) return RET_EINVAL;
+    // the state terms need both factors of each inner product
+    if ((state_in && !d_state_in) || (d_state_out && !state_out)) return RET_EINVAL;
+  }
+  const ParamPlan p = plan_param_grads(B, H, L, d_k);
+  if (!workspace || !al16(workspace) || workspace_bytes < p.bytes) return RET_EWORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  grad::ParamArgs a{};
+  a.q = q; a.k = k; a.v = v; a.d_out = d_out; a.out = out; a.dq = dq; a.dk = dk; a.dv = dv;
+  a.H = H; a.L = L; a.d_k = d_k; a.d_v = d_v; a.nseg = p.nseg;
+  a.pos0 = static_cast<float>(pos0);
+  a.gpart = d_gamma ? reinterpret_cast<double*>(ws + p.off_g) : nullptr;
+  a.tpart = d_theta ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
+  const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(B) * H * p.nseg);
+  const bool vec = d_k % 8 == 0 && d_v % 8 == 0;
+  {
+    Mark m("param_rows", stream);
+    if (in_dt == RET_F32) {
+      if (out_dt == RET_F32) launch_param_rows_g<float, float>(a, grid, vec, grad_dt, stream);
+      else launch_param_rows_g<float, __nv_bfloat16>(a, grid, vec, grad_dt, stream);
+    } else {
+      if (out_dt == RET_F32) launch_param_rows_g<__nv_bfloat16, float>(a, grid, vec, grad_dt, stream);
+      else launch_param_rows_g<__nv_bfloat16, __nv_bfloat16>(a, grid, vec, grad_dt, stream);
+    }
+  }
+  ret_status s = last_launch();
+  if (s != RET_OK) return s;
+  const bool have_state = d_gamma && (state_in || d_state_out);
+  double* spart = reinterpret_cast<double*>(ws + p.off_s);
+  if (have_state) {
+    Mark m("param_state", stream);
+    grad::state_dot_kernel<<<static_cast<unsigned>(B * H * grad::kStateSlices), 256, 0, stream>>>(
+        state_in, d_state_in, state_out, d_state_out, d_k * d_v, static_cast<float>(L - 1), spart);
+    if ((s = last_launch()) != RET_OK) return s;
+  }
+  grad::FinishArgs f{};
+  f.gpart = a.gpart; f.spart = spart; f.tpart = a.tpart;
+  f.d_gamma = d_gamma; f.d_theta = d_theta;
+  f.B = B; f.H = H; f.nseg = p.nseg; f.P = d_k / 2; f.have_state = have_state ? 1 : 0;
+  for (int h = 0; h < H; ++h) f.inv_gamma[h] = d_gamma ? 1.0 / static_cast<double>(gamma[h]) : 0.0;
+  Mark m("param_finish", stream);
+  grad::param_finish_kernel<<<static_cast<unsigned>(H + d_k / 2), 256, 0, stream>>>(f);
   return last_launch();
 }
 

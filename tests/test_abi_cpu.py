@@ -353,3 +353,57 @@ def test_msr_block_and_matmul_validation(lib):
     assert lib.ret_matmul(P, P, P, _lib.RET_F32, 300, 500, 192, None) == _lib.RET_EUNSUPPORTED
     assert lib.ret_matmul(P, P, P, _lib.RET_F32, 300, 512, 100, None) == _lib.RET_EUNSUPPORTED
     assert lib.ret_matmul(P, P, P, 7, 300, 512, 192, None) == _lib.RET_EINVAL
+
+
+def test_param_grads_and_groupnorm_validation(lib):
+    """ret_chunkwise_param_grads, ret_groupnorm and ret_groupnorm_backward
+    check their arguments (and workspace) before any launch; the plans give
+    the documented sizes."""
+    P, P2, P3 = C.c_void_p(0x1000), C.c_void_p(0x2000), C.c_void_p(0x3000)
+    g = np.array([0.9, 0.99], np.float32)
+    nb = C.c_size_t(0)
+    assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 64, 32, C.byref(nb)) == _lib.RET_OK
+    # 2 segments of 64 tokens × 4 heads: doubles, 16 state slices per head, 32 pairs of floats
+    assert nb.value == 256 + 512 + 1024
+    assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 63, 32, C.byref(nb)) == _lib.RET_EINVAL
+
+    def call(d_gamma=P, d_theta=P, gamma=g, d_k=64, pos0=0, s_in=None, ds_in=None, s_out=None,
+             ds_out=None, ws=P, wsn=1 << 20, dq=P, in_dt=_lib.RET_BF16):
+        return lib.ret_chunkwise_param_grads(P, P, P, P, in_dt, P, _lib.RET_BF16, dq, P, P, _lib.RET_F32,
+                                             _fp(gamma), 2, 2, 100, d_k, 32, pos0, s_in, ds_in, s_out,
+                                             ds_out, d_gamma, d_theta, ws, wsn, None)
+
+    assert call(d_gamma=None, d_theta=None) == _lib.RET_EINVAL
+    assert call(d_k=63) == _lib.RET_EINVAL
+    assert call(gamma=np.array([0.9, 0.0], np.float32)) == _lib.RET_EINVAL
+    assert call(s_in=P) == _lib.RET_EINVAL                      # state_in without d_state_in
+    assert call(ds_out=P) == _lib.RET_EINVAL                    # d_state_out without state_out
+    assert call(pos0=(1 << 24) - 50) == _lib.RET_EINVAL
+    assert call(dq=None) == _lib.RET_EINVAL
+    assert call(dq=C.c_void_p(0x1008)) == _lib.RET_EINVAL       # misaligned
+    assert call(in_dt=5) == _lib.RET_EINVAL
+    assert call(ws=None) == _lib.RET_EWORKSPACE
+    assert call(wsn=100) == _lib.RET_EWORKSPACE
+
+    gn = _lib.RetGN(1, 1e-5, None, None)
+    assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_BF16, 1, 2, 8, 0, C.byref(gn), None) == _lib.RET_EINVAL
+    assert lib.ret_groupnorm(P, _lib.RET_F32, P, _lib.RET_BF16, 1, 2, 8, 16, C.byref(gn), None) == \
+        _lib.RET_EINVAL                                          # in place needs one type
+    assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_F32, 1, 2, 8, 16, None, None) == _lib.RET_EINVAL
+    bad = _lib.RetGN(1, 0.0, None, None)
+    assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_F32, 1, 2, 8, 16, C.byref(bad), None) == \
+        _lib.RET_EINVAL
+
+    assert lib.ret_groupnorm_backward_plan(2, 2, 100, 48, C.byref(nb)) == _lib.RET_OK
+    assert nb.value == 2 * 2 * 2 * 2 * 48 * 4                  # [blocks][2][d_v] floats
+
+    def gcall(x=P, dx=P3, eps=1e-5, d_v=48, dw=None, ws=None, wsn=0):
+        return lib.ret_groupnorm_backward(x, P2, _lib.RET_F32, None, eps, 2, 2, 100, d_v, dx, _lib.RET_F32,
+                                          dw, None, ws, wsn, None)
+
+    assert gcall(dx=P) == _lib.RET_EINVAL                       # d_x aliases x
+    assert gcall(eps=0.0) == _lib.RET_EINVAL
+    assert gcall(d_v=1025) == _lib.RET_EINVAL
+    assert gcall(x=C.c_void_p(0x1004)) == _lib.RET_EINVAL
+    assert gcall(dw=P) == _lib.RET_EWORKSPACE                   # parameter sums need the workspace
+    assert gcall(dw=P, ws=P, wsn=100) == _lib.RET_EWORKSPACE
