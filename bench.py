@@ -882,26 +882,42 @@ def main():
 
         # γ and θ gradients from this forward (out, s_out) and backward (grads, dsi):
         # two HBM-bound row passes over 8 token-major tensors plus the states
-        if lib.ret_chunkwise(*(cargs[:14] + (vp(s_out),) + cargs[15:])) != _lib.RET_OK:   # fills s_out
-            raise RuntimeError("ret_chunkwise with state_out failed")
         pws_n = C.c_size_t(0)
         lib.ret_chunkwise_param_grads_plan(w.B, w.H, w.L, w.d_k, w.d_v, C.byref(pws_n))
         pws = torch.empty(max(pws_n.value, 1), dtype=torch.uint8, device=dev)
         dgam = torch.empty(w.H, dtype=torch.float32, device=dev)
         dthe = torch.empty(w.d_k // 2, dtype=torch.float32, device=dev)
         pargs = (vp(q), vp(k), vp(v), vp(d_o), _lib.RET_BF16, vp(out), _lib.RET_BF16, vp(grads[0]),
-                 vp(grads[1]), vp(grads[2]), _lib.RET_BF16, fptr(garr), w.B, w.H, w.L, w.d_k, w.d_v, 0,
-                 vp(s_in), vp(dsi), vp(s_out), vp(dso), vp(dgam), vp(dthe), vp(pws), pws_n.value,
+                 vp(grads[1]), vp(grads[2]), _lib.RET_BF16, fptr(garr), fptr(tarr), w.B, w.H, w.L, w.d_k,
+                 w.d_v, 0, vp(s_in), vp(dso), vp(dgam), vp(dthe), vp(pws), pws_n.value,
                  C.c_void_p(stream.cuda_stream))
+        lib.ret_profile_begin(C.cast(ev_handles, C.c_void_p), len(evs))
+        if lib.ret_chunkwise_param_grads(*pargs) != _lib.RET_OK:
+            raise RuntimeError("ret_chunkwise_param_grads failed")
+        np_k = lib.ret_profile_end()
+        torch.cuda.synchronize()
+        pker = {}
+        for i in range(np_k):
+            nm = lib.ret_profile_kernel(i).decode()
+            pker[nm] = pker.get(nm, 0.0) + evs[2 * i].elapsed_time(evs[2 * i + 1])
         pms = time_launches(lambda: lib.ret_chunkwise_param_grads(*pargs), 10)
         tok = w.B * w.H * w.L
-        pbytes = tok * (4 * w.d_v + 4 * w.d_k) * 2 + 4 * w.B * w.H * w.d_k * w.d_v * 4
-        pgbs = pbytes / (pms / 1e3) / 1e9
+        # the walks: two rank-128 updates of every (b, h) state per chunk (fp32 FFMA)
+        pflops = 2 * 2 * tok * w.d_k * w.d_v
+        walk_ms = pker.get("param_walk_fwd", 0.0) + pker.get("param_walk_bwd", 0.0)
+        wtf = pflops / (walk_ms / 1e3) / 1e12 if walk_ms else None
+        rbytes = tok * (4 * w.d_v + 4 * w.d_k) * 2
+        rgbs = rbytes / (pker["param_rows"] / 1e3) / 1e9 if pker.get("param_rows") else None
         backward["param_grads"] = {
-            "metric": "gamma/theta gradient pass GB/s", "value": pgbs, "unit": "GB/s", "ms_per_call": pms,
-            "launches_per_call": 3, "algorithmic_bytes_per_call": pbytes,
-            "roofline": {"bound": "hbm", "achieved": pgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": pgbs / peaks["hbm_gbs"], "traffic": None}}
+            "metric": "gamma/theta gradient call ms", "value": pms, "unit": "ms", "ms_per_call": pms,
+            "launches_per_call": np_k, "kernels_ms": pker,
+            "roofline": {"bound": "alu", "kernel": "param_walk_fwd + param_walk_bwd",
+                         "achieved": wtf, "peak": FFMA_TFLOPS, "unit": "TFLOP/s",
+                         "frac": wtf / FFMA_TFLOPS if wtf else None, "traffic": None,
+                         "peak_kind": "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2032 MHz",
+                         "algorithmic_flop_per_call": pflops},
+            "row_pass": {"algorithmic_bytes": rbytes, "achieved_gbs": rgbs,
+                         "frac_of_hbm": rgbs / peaks["hbm_gbs"] if rgbs else None}}
         del pws, dgam, dthe
         del bws, grads, dsi, d_o, dso, gi
 

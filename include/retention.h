@@ -256,37 +256,43 @@ ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, const float* gamma, int 
  * ret_chunkwise_param_grads — gradients of ret_chunkwise (without the
  * GroupNorm epilogue) with respect to the decay rates γ [H] and the rotation
  * frequencies θ [d_k/2] («从RoPE到Retention…» §2 makes θ learnable; §3 sets
- * γ per head).  Differentiating the decay factors γ^{n−m}, γ^{t+1}
- * (state_in) and γ^{L−1−m}, γ^L (state_out) of the parallel form (§3, §4.1)
- * and the rotation angles (pos0 + t)·θ_i of the Θ prologue (§2) gives, with
- * t the local token index and J(a, b) = (−b, a) on each pair:
- *   dγ_h = γ_h⁻¹ Σ_b [ Σ_t t·(dO_t·o_t − v_t·dv_t) + <S_in, dS_in>
- *                       + (L − 1)·<dS_out, S_out> ]
- *   dθ_i = Σ_{b,h,t} (pos0 + t)·( dq_t·J q_t + dk_t·J k_t )   on pair i
- * so the call consumes the forward call's out and state_out and the
- * backward call's dq, dk, dv and d_state_in for the same inputs, upstream
- * gradients and pos0; it reads each of them once (HBM-bound row passes).
+ * γ per head), for the upstream gradients d_out and d_state_out.  Both are
+ * sums over (query, key) pairs of the terms of <dO, out> + <dS_out, S_out>
+ * weighted by the derivative of their decay γ^{n−m} (n − m)·γ^{n−m−1} or of
+ * their rotation angle (m − n)·θ (§3, §4.1, §2), plus the state terms.  The
+ * call evaluates them split at 128-token chunk boundaries, so that no weight
+ * exceeds the chunk length except the genuine absolute-position weights of
+ * the state terms (κ = 63.5, j the index inside a chunk, S_c / dS_c the state
+ * after chunk c and its gradient, r the last chunk's length, J(a, b) =
+ * (−b, a) on each rotation pair, Z_c = Σ_v S_c[2i+1]dS_c[2i] − S_c[2i]dS_c[2i+1]):
+ *   γ·dγ = Σ_t (j−κ)(dO_t·o_t − v_t·dv_t) + (1+κ)<S_in, dS_in>
+ *          + (r−1−κ)<S_out, dS_out> + 128·Σ_{interior c} <S_c, dS_c>
+ *   dθ_i = Σ_t (j−κ)(dq_t·J q_t + dk_t·J k_t)_i + (pos0+κ)Z_{−1}
+ *          − (pos0+L−r+κ)Z_{C−1} + 128·Σ_{interior c} Z_c
+ * The row sums read the forward call's out and the backward call's dq, dk,
+ * dv for the same inputs, upstream gradients and pos0; the states are
+ * recomputed in fp32 from q, k, v, d_out (two sequential walks over the
+ * chunks, 64 × 64 state tiles per block).
  * q, k, v, d_out: DEVICE, in_dt, [B, H, L, d_k|d_v].  out: DEVICE, out_dt,
- * [B, H, L, d_v] (the forward output before any GroupNorm).  dq, dk, dv:
- * DEVICE, grad_dt.  state_in / d_state_in and state_out / d_state_out:
- * DEVICE fp32 [B, H, d_k, d_v] or NULL (zero); d_state_in is required when
- * state_in is given and state_out when d_state_out is given (dγ only).
- * gamma: HOST [H], each in (0, 1] (read during the call; dγ only).
- * d_gamma [H], d_theta [d_k/2]: DEVICE fp32 outputs, overwritten; either may
- * be NULL (not computed; then its inputs may be NULL too), not both.
- * workspace: DEVICE, at least ret_chunkwise_param_grads_plan's bytes.
- * Deterministic: fixed-order sums (fp32 per 64-token segment, double across
- * segments).  Validation and errors as for the other entry points.
+ * [B, H, L, d_v] (the forward output before any GroupNorm; dγ only).  dq,
+ * dk (dθ only), dv (dγ only): DEVICE, grad_dt.  state_in, d_state_out:
+ * DEVICE fp32 [B, H, d_k, d_v] or NULL (zero).  gamma [H] in (0, 1], theta
+ * [d_k/2]: HOST, read during the call.  d_gamma [H], d_theta [d_k/2]: DEVICE
+ * fp32 outputs, overwritten; either may be NULL (not computed), not both.
+ * workspace: DEVICE, at least ret_chunkwise_param_grads_plan's bytes
+ * (B·H·⌈L/128⌉·d_k·d_v·4 bytes for the states, plus small terms).
+ * Deterministic: fixed-order sums.  Validation and errors as for the other
+ * entry points.
  * ------------------------------------------------------------------------ */
 ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v,
                                      const void* d_out, ret_dtype in_dt, const void* out,
                                      ret_dtype out_dt, const void* dq, const void* dk,
                                      const void* dv, ret_dtype grad_dt, const float* gamma,
-                                     int B, int H, int L, int d_k, int d_v, int64_t pos0,
-                                     const float* state_in, const float* d_state_in,
-                                     const float* state_out, const float* d_state_out,
-                                     float* d_gamma, float* d_theta, void* workspace,
-                                     size_t workspace_bytes, cudaStream_t stream);
+                                     const float* theta, int B, int H, int L, int d_k, int d_v,
+                                     int64_t pos0, const float* state_in,
+                                     const float* d_state_out, float* d_gamma, float* d_theta,
+                                     void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
 
 /* Workspace bytes of ret_chunkwise_param_grads. */
 ret_status ret_chunkwise_param_grads_plan(int B, int H, int L, int d_k, int d_v,

@@ -41,8 +41,8 @@ SIGNATURES = {
     "ret_chunkwise_backward": (_i, [_vp, _vp, _vp, _vp, _i, _fp, _fp, _i, _i, _i, _i, _i, _i64, _i,
                                     _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _sz, _vp]),
     "ret_chunkwise_backward_plan": (_i, [_i, _fp, _i, _i, _i, _i, _i, _i, C.POINTER(_i), C.POINTER(_sz)]),
-    "ret_chunkwise_param_grads": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _i, _fp, _i, _i,
-                                       _i, _i, _i, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "ret_chunkwise_param_grads": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _vp, _vp, _vp, _i, _fp, _fp, _i,
+                                       _i, _i, _i, _i, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ret_chunkwise_param_grads_plan": (_i, [_i, _i, _i, _i, _i, C.POINTER(_sz)]),
     "ret_groupnorm": (_i, [_vp, _i, _vp, _i, _i, _i, _i, _i, C.POINTER(RetGN), _vp]),
     "ret_groupnorm_backward": (_i, [_vp, _vp, _i, _vp, _f, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _sz,

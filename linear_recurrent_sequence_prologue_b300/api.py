@@ -230,12 +230,12 @@ def chunkwise_backward(q, k, v, d_out, gamma, theta, chunk: int, pos0: int = 0, 
     return dq, dk, dv, d_state_in
 
 
-def param_grads(q, k, v, d_out, out, dq, dk, dv, gamma, pos0: int = 0, state_in=None,
-                d_state_in=None, state_out=None, d_state_out=None, want_gamma: bool = True,
-                want_theta: bool = True, workspace=None, stream=None):
+def param_grads(q, k, v, d_out, out, dq, dk, dv, gamma, theta, pos0: int = 0, state_in=None,
+                d_state_out=None, want_gamma: bool = True, want_theta: bool = True, workspace=None,
+                stream=None):
     """Gradients with respect to γ [H] and θ [d_k/2] (fp32 device tensors;
-    None where not wanted), from the forward call's out / state_out and the
-    backward call's dq, dk, dv / d_state_in for the same inputs."""
+    None where not wanted), from the forward call's out and the backward
+    call's dq, dk, dv for the same inputs and upstream gradients."""
     lib = load()
     B, H, L, d_k, d_v = _check_seq(q, k, v)
     idt = _dtype_code(q)
@@ -245,6 +245,7 @@ def param_grads(q, k, v, d_out, out, dq, dk, dv, gamma, pos0: int = 0, state_in=
     for name, t, shp in (("dq", dq, (B, H, L, d_k)), ("dk", dk, (B, H, L, d_k)), ("dv", dv, (B, H, L, d_v))):
         _dev(t, name, dq.dtype, shp)
     garr, gp = _host_f32(gamma, H, "gamma")
+    tarr, tp = _host_f32(theta, d_k // 2, "theta")
     sshape = (B, H, d_k, d_v)
     d_gamma = torch.empty(H, dtype=torch.float32, device=q.device) if want_gamma else None
     d_theta = torch.empty(d_k // 2, dtype=torch.float32, device=q.device) if want_theta else None
@@ -253,10 +254,8 @@ def param_grads(q, k, v, d_out, out, dq, dk, dv, gamma, pos0: int = 0, state_in=
     wsp, wsn, ws = _workspace(nb.value, q.device, workspace)
     st = lib.ret_chunkwise_param_grads(
         _dev(q, "q"), _dev(k, "k"), _dev(v, "v"), _dev(d_out, "d_out"), idt, _dev(out, "out"),
-        _dtype_code(out), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"), gdt, gp, B, H, L, d_k, d_v,
+        _dtype_code(out), _dev(dq, "dq"), _dev(dk, "dk"), _dev(dv, "dv"), gdt, gp, tp, B, H, L, d_k, d_v,
         int(pos0), _dev(state_in, "state_in", torch.float32, sshape),
-        _dev(d_state_in, "d_state_in", torch.float32, sshape),
-        _dev(state_out, "state_out", torch.float32, sshape),
         _dev(d_state_out, "d_state_out", torch.float32, sshape), _dev(d_gamma, "d_gamma"),
         _dev(d_theta, "d_theta"), wsp, wsn, _stream(stream))
     check("ret_chunkwise_param_grads", st)

@@ -1,21 +1,30 @@
 // Parameter gradients of the retention core (γ per head, θ per rotation
 // pair) and the GroupNorm backward.  All HBM-bound row passes.
 //
-// dγ_h.  Differentiating the decay factors of the parallel form with its
-// state terms («从RoPE到Retention…» §3 and §4.1; ∂γ^e/∂γ = e·γ^{e−1})
-// gives γ⁻¹·Σ (n − m)·A_nm over every (query n, key m) pair, A_nm being the
-// pair's share of <dO, out> + <dS_out, S_out>.  The row sums of A are
-// dO_n·o_n (the state_in term counted as a key at m = −1, the state_out read
-// as a query at n = L − 1) and its column sums are v_m·dv_m, so per (b, h)
-//   γ·dγ = Σ_t t·(dO_t·o_t − v_t·dv_t) + <S_in, dS_in> + (L − 1)·<dS_out, S_out>
-// with t the local token index (the decay depends on index differences only).
-//
-// dθ_i.  Pair i of q′_t is pair i of q_t rotated by (pos0 + t)·θ_i («从RoPE到
-// Retention…» §2, where θ is learnable), so ∂q′/∂θ_i = (pos0 + t)·J q′ on that
-// pair, J(a, b) = (−b, a).  With dq = Rᵀ dQ′ and J commuting with the
-// rotation, dQ′·J q′ = dq·J q, and likewise for k (the 1/√d_k scale cancels
-// between dk and k′):
-//   dθ_i = Σ_{b,h,t} (pos0 + t)·(dq₂ᵢ₊₁ q₂ᵢ − dq₂ᵢ q₂ᵢ₊₁ + dk₂ᵢ₊₁ k₂ᵢ − dk₂ᵢ k₂ᵢ₊₁)
+// dγ_h, dθ_i.  Both are sums over (query n, key m) pairs of the decay- or
+// angle-weighted terms of <dO, out> + <dS_out, S_out> («从RoPE到Retention…»
+// §2-§4: ∂γ^{n−m}/∂γ = (n−m)·γ^{n−m−1}; θ is learnable, and pair i of
+// q′_t, k′_t is rotated by (pos0 + t)·θ_i, so the angle of a pair's score
+// moves with (m − n)).  Written with positions over the whole sequence
+// (Σ_t t·(dO_t·o_t − v_t·dv_t) for γ) the weights grow with L while the
+// result only grows with the decay window, and the two big sums cancel: the
+// rounding of bf16 operands would be amplified by L / window.  So the sums
+// are split at chunk boundaries (chunks of b = 128 tokens, c = 0..C−1, the
+// last of r tokens; S_c the state after chunk c, dS_c its gradient, S_{−1} =
+// S_in, dS_{C−1} = dS_out; j the index inside a chunk, κ = (b−1)/2).  Reverse
+// mode through the chunk recurrence (o_j = Σ_{i≤j} γ^{j−i}(q′_j·k′_i)v_i +
+// γ^{j+1}q′_j S_{c−1}, S_c = γ^{b_c}S_{c−1} + Σ_i γ^{b_c−1−i}k′_iᵀv_i) gives
+//   γ·dγ = Σ_t (j−κ)·(dO_t·o_t − v_t·dv_t) + (1+κ)<S_{−1}, dS_{−1}>
+//          + (r−1−κ)<S_{C−1}, dS_{C−1}> + b·Σ_{c=0}^{C−2} <S_c, dS_c>
+//   dθ_i = Σ_t (j−κ)·(dq_t·J q_t + dk_t·J k_t)_i + (pos0+κ)·Z_{−1,i}
+//          − (pos0+(C−1)b+κ)·Z_{C−1,i} + b·Σ_{c=0}^{C−2} Z_{c,i}
+// with J(a, b) = (−b, a) on each pair (dQ′·J q′ = dq·J q since J commutes
+// with the rotation) and Z_{c,i} = Σ_v (S_c[2i+1,v]·dS_c[2i,v] −
+// S_c[2i,v]·dS_c[2i+1,v]).  Every weight is now at most b or is the genuine
+// absolute-position weight of the state terms.  The row sums use the
+// caller's out, dv, dq, dk; the states are recomputed here in fp32 from q,
+// k, v, d_out (a forward walk stores S_c, a backward walk carries dS_c and
+// forms the boundary products), so they carry no bf16 rounding.
 //
 // GroupNorm backward (one group per (b, h, t) row over d_v channels, biased
 // variance, «从RoPE到Retention…» §5): with x̂ = (x − μ)·rstd and g = dy ⊙ w,
@@ -31,6 +40,8 @@ namespace ret {
 namespace grad {
 
 constexpr int kRowsPerBlock = 64;
+constexpr int kGradChunk = 128;                         // b of the boundary split
+constexpr float kKappa = 0.5f * (kGradChunk - 1);      // κ, exact in fp32
 
 // 8 consecutive row elements as fp32: one 16-byte load for bf16, two for fp32.
 template <typename T> __device__ __forceinline__ void load8(const T* p, float (&x)[8]);
@@ -69,16 +80,15 @@ __device__ __forceinline__ float warp_sum(float s) {
 // ---------------------------------------------------------------------------
 // Row pass of the parameter gradients.  Block = (b, h, segment of
 // kRowsPerBlock tokens), 8 warps, warp w takes tokens w, w + 8, …  Writes
-// gpart[block] (the segment's Σ t·(dO·o − v·dv), double) and tpart[i][block]
-// (the segment's share of dθ_i; pair-major, so the finishing sums read it
-// contiguously).  VEC: d_k and d_v are multiples of 8 (rows
+// gpart[block] (the segment's Σ (j−κ)·(dO·o − v·dv), double) and
+// tpart[i][block] (the segment's Σ (j−κ)·(dq·J q + dk·J k)_i; pair-major, so
+// the finishing sums read it contiguously), j = t mod kGradChunk.  VEC: d_k and d_v are multiples of 8 (rows
 // read as 16-byte vectors); otherwise element by element.
 // ---------------------------------------------------------------------------
 struct ParamArgs {
   const void* q; const void* k; const void* v; const void* d_out;
   const void* out; const void* dq; const void* dk; const void* dv;
   int H, L, d_k, d_v, nseg;
-  float pos0;          // exact: pos0 + L ≤ 2^24
   double* gpart;       // [B·H·nseg] or null (no dγ)
   float* tpart;        // [d_k/2][B·H·nseg] or null (no dθ)
 };
@@ -116,10 +126,10 @@ __global__ void __launch_bounds__(256) param_rows_kernel(ParamArgs a) {
         for (int c = lane; c < a.d_v; c += 32)
           s = fmaf(to_f32(dO[c]), to_f32(o[c]), fmaf(-to_f32(v[c]), to_f32(dv[c]), s));
       }
-      gacc = fmaf(static_cast<float>(t), s, gacc);
+      gacc = fmaf(static_cast<float>(t % kGradChunk) - kKappa, s, gacc);
     }
     if (a.tpart) {
-      const float pos = a.pos0 + static_cast<float>(t);
+      const float pos = static_cast<float>(t % kGradChunk) - kKappa;
       const Tin* q = static_cast<const Tin*>(a.q) + row * a.d_k;
       const Tin* k = static_cast<const Tin*>(a.k) + row * a.d_k;
       const Tg* dq = static_cast<const Tg*>(a.dq) + row * a.d_k;
@@ -189,42 +199,236 @@ __global__ void __launch_bounds__(256) param_rows_kernel(ParamArgs a) {
     }
 }
 
-// <S_in, dS_in> + (L − 1)·<dS_out, S_out> per (b, h), in NS slices:
-// spart[bh·NS + slice] (double).  Either product may be absent (null).
-constexpr int kStateSlices = 16;
+// ---------------------------------------------------------------------------
+// State walks.  Block = (b, h, 64 × 64 tile of the d_k × d_v state), 256
+// threads; thread (ty, tx) = (tid / 16, tid % 16) owns rows 4ty … 4ty+3 and
+// columns 4tx … 4tx+3 of the tile (rows 4ty, 4ty+1 and 4ty+2, 4ty+3 are two
+// rotation pairs).  A chunk's rank-b_c update Σ_i w_i a_iᵀ b_i is staged 32
+// rows at a time in shared memory (a: the rotated, weighted k′ or q′ columns
+// of the tile; b: the v or dO columns).  The angle table cs[t][i] holds
+// (cos, sin) of (pos0 + t)·θ_i.  States are stored per (b, h, chunk, tile)
+// in thread order, 16 floats per thread.
+// ---------------------------------------------------------------------------
+constexpr int kTile = 64;
+constexpr int kStage = 32;
 
-__global__ void __launch_bounds__(256) state_dot_kernel(const float* s_in, const float* ds_in,
-                                                        const float* s_out, const float* ds_out,
-                                                        int n, float lm1, double* spart) {
-  __shared__ double red[8];
-  const size_t bh = blockIdx.x / kStateSlices;
-  const int slice = blockIdx.x % kStateSlices;
-  const int per = (n + kStateSlices - 1) / kStateSlices;
-  const int i0 = slice * per, i1 = min(n, i0 + per);
-  float s = 0.f;
-  const size_t base = bh * static_cast<size_t>(n);
-  for (int i = i0 + threadIdx.x; i < i1; i += 256) {
-    if (s_in) s = fmaf(s_in[base + i], ds_in[base + i], s);
-    if (ds_out) s = fmaf(lm1 * ds_out[base + i], s_out[base + i], s);
+struct WalkArgs {
+  const void* a;        // k (forward walk) or q (backward walk) [BH][L][d_k]
+  const void* b;        // v or d_out [BH][L][d_v]
+  const float* s0;      // forward: S_in; backward: dS_out [BH][d_k][d_v], or null
+  const float* s_in;    // backward: S_in (the state before chunk 0), or null
+  float* states;        // [BH][C][tiles][4096]: S_c written (forward), read (backward)
+  const float2* cs;     // [L][d_k/2]
+  double* gpart;        // backward: [BH·tiles] weighted Σ <S_c, dS_c>
+  float* zpart;         // backward: [BH·tiles][32] weighted Σ Z_c per pair of the tile
+  int H, L, d_k, d_v, C, ntk, ntv;
+  float ascale;         // forward: d_k^{-1/2}; backward: 1
+  float pos0;
+  CallConsts cc;
+};
+
+// Stage rows t0 … t0+kStage−1 of chunk c (local indices j0 …) into As, Bs.
+// Forward: weight γ^{b_c−1−j}; backward: γ^{j+1}.
+template <typename Tin, bool FWD>
+__device__ __forceinline__ void stage_rows(const WalkArgs& w, size_t bh, int h, int c, int bc, int j0,
+                                           int k0, int v0, float (*As)[kTile + 4],
+                                           float (*Bs)[kTile + 4]) {
+  const Tin* A = static_cast<const Tin*>(w.a);
+  const Tin* Bm = static_cast<const Tin*>(w.b);
+  const int tid = threadIdx.x;
+  const float lg = w.cc.lg2g[h];
+  // a: kStage rows × 32 pairs; thread → (row tid / 8, pairs 4·(tid % 8) … +3)
+  {
+    const int r = tid >> 3, jl = j0 + r;
+    const int t = c * kGradChunk + jl;
+    const bool live = jl < bc;
+    const float wgt = live ? w.ascale * exp2f((FWD ? static_cast<float>(bc - 1 - jl)
+                                                   : static_cast<float>(jl + 1)) * lg) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int pl = 4 * (tid & 7) + u;        // pair within the tile
+      const int col = k0 + 2 * pl;
+      float x0 = 0.f, x1 = 0.f;
+      if (live && col < w.d_k) {
+        const size_t off = (bh * w.L + t) * static_cast<size_t>(w.d_k) + col;
+        const float2 e = w.cs[static_cast<size_t>(t) * (w.d_k / 2) + col / 2];
+        const float a0 = to_f32(A[off]), a1 = to_f32(A[off + 1]);
+        x0 = wgt * fmaf(a0, e.x, -a1 * e.y);   // rotate by the angle: (a0 c − a1 s, a1 c + a0 s)
+        x1 = wgt * fmaf(a1, e.x, a0 * e.y);
+      }
+      As[r][2 * pl] = x0;
+      As[r][2 * pl + 1] = x1;
+    }
   }
-  s = warp_sum(s);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = static_cast<double>(s);
+  // b: kStage rows × 64 columns; thread → (row tid / 8, columns 8·(tid % 8) … +7)
+  {
+    const int r = tid >> 3, jl = j0 + r;
+    const int t = c * kGradChunk + jl;
+    const bool live = jl < bc;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int col = v0 + 8 * (tid & 7) + u;
+      Bs[r][8 * (tid & 7) + u] =
+          live && col < w.d_v ? to_f32(Bm[(bh * w.L + t) * static_cast<size_t>(w.d_v) + col]) : 0.f;
+    }
+  }
+}
+
+// acc (4 × 4 of the tile) += Σ over the chunk's rows of As[i][rows]ᵀ Bs[i][cols].
+template <typename Tin, bool FWD>
+__device__ __forceinline__ void chunk_update(const WalkArgs& w, size_t bh, int h, int c, int k0, int v0,
+                                             float (&acc)[4][4], float (*As)[kTile + 4],
+                                             float (*Bs)[kTile + 4]) {
+  const int bc = min(kGradChunk, w.L - c * kGradChunk);
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  for (int j0 = 0; j0 < bc; j0 += kStage) {
+    __syncthreads();
+    stage_rows<Tin, FWD>(w, bh, h, c, bc, j0, k0, v0, As, Bs);
+    __syncthreads();
+#pragma unroll 8
+    for (int i = 0; i < kStage; ++i) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[i][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[i][4 * tx]);
+      const float ar[4] = {a.x, a.y, a.z, a.w}, br[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[r][q] = fmaf(ar[r], br[q], acc[r][q]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_tile(const float* src, size_t bh, int d_k, int d_v, int k0, int v0,
+                                          float (&x)[4][4]) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = k0 + 4 * ty + r, col = v0 + 4 * tx + q;
+      x[r][q] = src && row < d_k && col < d_v ? src[(bh * d_k + row) * static_cast<size_t>(d_v) + col] : 0.f;
+    }
+}
+
+// Forward walk: S_{−1} = S_in; S_c = γ^{b_c}·S_{c−1} + Σ_i γ^{b_c−1−i} k′_iᵀ v_i,
+// stored for c = 0 … C−1.
+template <typename Tin>
+__global__ void __launch_bounds__(256) state_walk_fwd_kernel(WalkArgs w) {
+  __shared__ __align__(16) float As[kStage][kTile + 4];
+  __shared__ __align__(16) float Bs[kStage][kTile + 4];
+  const int ntiles = w.ntk * w.ntv;
+  const size_t bh = blockIdx.x / ntiles;
+  const int tile = blockIdx.x % ntiles;
+  const int h = static_cast<int>(bh % w.H);
+  const int k0 = (tile / w.ntv) * kTile, v0 = (tile % w.ntv) * kTile;
+  float S[4][4];
+  load_tile(w.s0, bh, w.d_k, w.d_v, k0, v0, S);
+  for (int c = 0; c < w.C; ++c) {
+    const int bc = min(kGradChunk, w.L - c * kGradChunk);
+    const float g = exp2f(static_cast<float>(bc) * w.cc.lg2g[h]);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) S[r][q] *= g;
+    chunk_update<Tin, true>(w, bh, h, c, k0, v0, S, As, Bs);
+    float4* dst = reinterpret_cast<float4*>(w.states + ((bh * w.C + c) * ntiles + tile) * 4096) + threadIdx.x * 4;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) dst[r] = make_float4(S[r][0], S[r][1], S[r][2], S[r][3]);
+  }
+}
+
+// Backward walk: dS_{C−1} = dS_out; dS_{c−1} = γ^{b_c}·dS_c + Σ_j γ^{j+1} q′_jᵀ dO_j.
+// At every boundary c = C−1 … −1 it adds the weighted <S_c, dS_c> and Z_c of
+// its tile (weights of the boundary split above).
+template <typename Tin>
+__global__ void __launch_bounds__(256) state_walk_bwd_kernel(WalkArgs w) {
+  __shared__ __align__(16) float As[kStage][kTile + 4];
+  __shared__ __align__(16) float Bs[kStage][kTile + 4];
+  __shared__ float zred[16][2][16];
+  __shared__ double gred[256];
+  const int ntiles = w.ntk * w.ntv;
+  const size_t bh = blockIdx.x / ntiles;
+  const int tile = blockIdx.x % ntiles;
+  const int h = static_cast<int>(bh % w.H);
+  const int k0 = (tile / w.ntv) * kTile, v0 = (tile % w.ntv) * kTile;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int r_last = w.L - (w.C - 1) * kGradChunk;
+  float dS[4][4];
+  load_tile(w.s0, bh, w.d_k, w.d_v, k0, v0, dS);
+  double gacc = 0.0, zacc0 = 0.0, zacc1 = 0.0;
+  // boundary products of dS (already dS_c) with S_c
+  auto boundary = [&](int c) {
+    float Sx[4][4];
+    if (c >= 0) {
+      const float4* src = reinterpret_cast<const float4*>(w.states + ((bh * w.C + c) * ntiles + tile) * 4096) +
+                          threadIdx.x * 4;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 x = src[r];
+        Sx[r][0] = x.x; Sx[r][1] = x.y; Sx[r][2] = x.z; Sx[r][3] = x.w;
+      }
+    } else {
+      load_tile(w.s_in, bh, w.d_k, w.d_v, k0, v0, Sx);
+    }
+    float ip = 0.f, z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) ip = fmaf(Sx[r][q], dS[r][q], ip);
+      z0 += Sx[1][q] * dS[0][q] - Sx[0][q] * dS[1][q];
+      z1 += Sx[3][q] * dS[2][q] - Sx[2][q] * dS[3][q];
+    }
+    float wg, wt;
+    if (c == w.C - 1) {          // checked first: with one chunk, boundary 0 is the last
+      wg = static_cast<float>(r_last - 1) - kKappa;
+      wt = -(w.pos0 + static_cast<float>((w.C - 1) * kGradChunk) + kKappa);
+    } else if (c < 0) {
+      wg = 1.f + kKappa;
+      wt = w.pos0 + kKappa;
+    } else {
+      wg = wt = static_cast<float>(kGradChunk);
+    }
+    gacc += static_cast<double>(wg) * ip;
+    zacc0 += static_cast<double>(wt) * z0;
+    zacc1 += static_cast<double>(wt) * z1;
+  };
+  boundary(w.C - 1);
+  for (int c = w.C - 1; c >= 0; --c) {
+    const int bc = min(kGradChunk, w.L - c * kGradChunk);
+    const float g = exp2f(static_cast<float>(bc) * w.cc.lg2g[h]);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dS[r][q] *= g;
+    chunk_update<Tin, false>(w, bh, h, c, k0, v0, dS, As, Bs);   // now dS_{c−1}
+    boundary(c - 1);
+  }
+  // block sums: Σ over threads of gacc; per pair of the tile Σ over tx
+  gred[threadIdx.x] = gacc;
+  zred[ty][0][tx] = static_cast<float>(zacc0);
+  zred[ty][1][tx] = static_cast<float>(zacc1);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double t = 0.0;
-    for (int w = 0; w < 8; ++w) t += red[w];
-    spart[blockIdx.x] = t;
+  for (int s = 128; s > 0; s >>= 1) {
+    if (static_cast<int>(threadIdx.x) < s) gred[threadIdx.x] += gred[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) w.gpart[blockIdx.x] = gred[0];
+  if (threadIdx.x < 32) {   // pair p of the tile = 2·ty + u
+    const int p = threadIdx.x, yy = p >> 1, u = p & 1;
+    float z = 0.f;
+    for (int x = 0; x < 16; ++x) z += zred[yy][u][x];
+    w.zpart[static_cast<size_t>(blockIdx.x) * 32 + p] = z;
   }
 }
 
 // Finishing sums, in double and in a fixed order (strided per thread, then a
-// fixed tree).  Blocks [0, H): dγ_h over the B·nseg row partials and
-// B·kStateSlices state partials of head h, times 1/γ_h.  Blocks [H, H + P):
-// dθ_i over the B·H·nseg row partials of pair i.
+// fixed tree).  Blocks [0, H): dγ_h = γ_h⁻¹ · (the B·nseg row partials +
+// the B·tiles boundary partials of head h).  Blocks [H, H + P): dθ_i = the
+// B·H·nseg row partials of pair i + the B·H·ntv boundary partials of its tile.
 struct FinishArgs {
-  const double* gpart; const double* spart; const float* tpart;
+  const double* gpart; const double* gwalk; const float* tpart; const float* zpart;
   float* d_gamma; float* d_theta;
-  int B, H, nseg, P, have_state;
+  int B, H, nseg, P, ntk, ntv;
   double inv_gamma[kMaxHeads];
 };
 
@@ -240,6 +444,7 @@ __device__ __forceinline__ double block_sum_256(double s, double* red) {
 
 __global__ void __launch_bounds__(256) param_finish_kernel(FinishArgs a) {
   __shared__ double red[256];
+  const int ntiles = a.ntk * a.ntv;
   if (static_cast<int>(blockIdx.x) < a.H) {
     if (!a.d_gamma) return;
     const int h = blockIdx.x;
@@ -248,11 +453,10 @@ __global__ void __launch_bounds__(256) param_finish_kernel(FinishArgs a) {
       const int b = i / a.nseg, seg = i % a.nseg;
       s += a.gpart[(static_cast<size_t>(b) * a.H + h) * a.nseg + seg];
     }
-    if (a.have_state)
-      for (int i = threadIdx.x; i < a.B * kStateSlices; i += 256) {
-        const int b = i / kStateSlices, sl = i % kStateSlices;
-        s += a.spart[(static_cast<size_t>(b) * a.H + h) * kStateSlices + sl];
-      }
+    for (int i = threadIdx.x; i < a.B * ntiles; i += 256) {
+      const int b = i / ntiles, tl = i % ntiles;
+      s += a.gwalk[(static_cast<size_t>(b) * a.H + h) * ntiles + tl];
+    }
     s = block_sum_256(s, red);
     if (threadIdx.x == 0) a.d_gamma[h] = static_cast<float>(s * a.inv_gamma[h]);
     return;
@@ -263,6 +467,13 @@ __global__ void __launch_bounds__(256) param_finish_kernel(FinishArgs a) {
   const float* src = a.tpart + static_cast<size_t>(i) * nblk;
   double s = 0.0;
   for (size_t blk = threadIdx.x; blk < nblk; blk += 256) s += src[blk];
+  const int tk = i / 32, pl = i % 32;
+  const size_t nwalk = static_cast<size_t>(a.B) * a.H * a.ntv;
+  for (size_t m = threadIdx.x; m < nwalk; m += 256) {
+    const size_t bh = m / a.ntv;
+    const int tv = static_cast<int>(m % a.ntv);
+    s += a.zpart[((bh * ntiles) + static_cast<size_t>(tk) * a.ntv + tv) * 32 + pl];
+  }
   s = block_sum_256(s, red);
   if (threadIdx.x == 0) a.d_theta[i] = static_cast<float>(s);
 }

@@ -1876,18 +1876,25 @@ namespace {
 // Parameter gradients and GroupNorm backward: workspace layouts and launches
 // ---------------------------------------------------------------------------
 struct ParamPlan {
-  int nseg;
-  size_t off_g, off_s, off_t, bytes;
+  int nseg, C, ntk, ntv;
+  size_t off_g, off_t, off_cs, off_states, off_gw, off_z, bytes;
 };
 
-ParamPlan plan_param_grads(int B, int H, int L, int d_k) {
+ParamPlan plan_param_grads(int B, int H, int L, int d_k, int d_v) {
   ParamPlan p{};
   p.nseg = (L + grad::kRowsPerBlock - 1) / grad::kRowsPerBlock;
-  const size_t nblk = static_cast<size_t>(B) * H * p.nseg;
+  p.C = (L + grad::kGradChunk - 1) / grad::kGradChunk;
+  p.ntk = (d_k + grad::kTile - 1) / grad::kTile;
+  p.ntv = (d_v + grad::kTile - 1) / grad::kTile;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nblk = BH * p.nseg, nwalk = BH * p.ntk * p.ntv;
   size_t off = 0;
   p.off_g = off; off += up256(nblk * sizeof(double));
-  p.off_s = off; off += up256(static_cast<size_t>(B) * H * grad::kStateSlices * sizeof(double));
   p.off_t = off; off += up256(nblk * static_cast<size_t>(d_k / 2) * sizeof(float));
+  p.off_cs = off; off += up256(static_cast<size_t>(L) * (d_k / 2) * sizeof(float2));
+  p.off_states = off; off += up256(nwalk * p.C * 4096 * sizeof(float));
+  p.off_gw = off; off += up256(nwalk * sizeof(double));
+  p.off_z = off; off += up256(nwalk * 32 * sizeof(float));
   p.bytes = off;
   return p;
 }
@@ -2025,7 +2032,7 @@ ret_status ret_chunkwise_param_grads_plan(int B, int H, int L, int d_k, int d_v,
                                           size_t* workspace_bytes) {
   if (!workspace_bytes || B < 1 || H < 1 || H > kMaxHeads || L < 1) return RET_EINVAL;
   if (d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 || d_v > 1024) return RET_EINVAL;
-  *workspace_bytes = plan_param_grads(B, H, L, d_k).bytes;
+  *workspace_bytes = plan_param_grads(B, H, L, d_k, d_v).bytes;
   return RET_OK;
 }
 
@@ -2033,11 +2040,11 @@ ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v
                                      const void* d_out, ret_dtype in_dt, const void* out,
                                      ret_dtype out_dt, const void* dq, const void* dk,
                                      const void* dv, ret_dtype grad_dt, const float* gamma,
-                                     int B, int H, int L, int d_k, int d_v, int64_t pos0,
-                                     const float* state_in, const float* d_state_in,
-                                     const float* state_out, const float* d_state_out,
-                                     float* d_gamma, float* d_theta, void* workspace,
-                                     size_t workspace_bytes, cudaStream_t stream) {
+                                     const float* theta, int B, int H, int L, int d_k, int d_v,
+                                     int64_t pos0, const float* state_in,
+                                     const float* d_state_out, float* d_gamma, float* d_theta,
+                                     void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
   Range nv("ret_chunkwise_param_grads");
   if (!ok_dt(in_dt) || !ok_dt(out_dt) || !ok_dt(grad_dt)) return RET_EINVAL;
   if (!d_gamma && !d_theta) return RET_EINVAL;
@@ -2045,27 +2052,30 @@ ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v
   if (d_k < 2 || d_k > 2 * kMaxPairs || (d_k & 1) || d_v < 1 || d_v > 1024) return RET_EINVAL;
   if (pos0 < 0 || pos0 + L > kMaxPos) return RET_EINVAL;
   if (static_cast<int64_t>(B) * H * L >= (int64_t(1) << 31)) return RET_EINVAL;
-  const void* need_t[4] = {q, k, dq, dk};
-  const void* need_g[4] = {v, d_out, out, dv};
+  for (const void* ptr : {q, k, v, d_out})
+    if (!ptr || !al16(ptr)) return RET_EINVAL;
   if (d_theta)
-    for (const void* p : need_t)
-      if (!p || !al16(p)) return RET_EINVAL;
-  if (d_gamma) {
-    for (const void* p : need_g)
-      if (!p || !al16(p)) return RET_EINVAL;
-    if (!gamma) return RET_EINVAL;
-    for (int h = 0; h < H; ++h)
-      if (!(gamma[h] > 0.f) || !(gamma[h] <= 1.f)) return RET_EINVAL;
-    // the state terms need both factors of each inner product
-    if ((state_in && !d_state_in) || (d_state_out && !state_out)) return RET_EINVAL;
-  }
-  const ParamPlan p = plan_param_grads(B, H, L, d_k);
+    for (const void* ptr : {dq, dk})
+      if (!ptr || !al16(ptr)) return RET_EINVAL;
+  if (d_gamma)
+    for (const void* ptr : {out, dv})
+      if (!ptr || !al16(ptr)) return RET_EINVAL;
+  if (!gamma || !theta) return RET_EINVAL;
+  CallConsts cc;
+  ret_status s = make_consts(cc, gamma, theta, H, d_k, grad::kGradChunk, L);
+  if (s != RET_OK) return s;
+  for (int h = 0; h < H; ++h)
+    if (!(gamma[h] > 0.f)) return RET_EINVAL;   // dγ divides by γ; the walks take log2 γ
+  const ParamPlan p = plan_param_grads(B, H, L, d_k, d_v);
+  const int64_t nwalk = static_cast<int64_t>(B) * H * p.ntk * p.ntv;
+  if (static_cast<int64_t>(B) * H * p.nseg >= (int64_t(1) << 31) || nwalk >= (int64_t(1) << 31))
+    return RET_EUNSUPPORTED;
   if (!workspace || !al16(workspace) || workspace_bytes < p.bytes) return RET_EWORKSPACE;
   char* ws = static_cast<char*>(workspace);
+  // (1) row sums with the in-chunk weights
   grad::ParamArgs a{};
   a.q = q; a.k = k; a.v = v; a.d_out = d_out; a.out = out; a.dq = dq; a.dk = dk; a.dv = dv;
   a.H = H; a.L = L; a.d_k = d_k; a.d_v = d_v; a.nseg = p.nseg;
-  a.pos0 = static_cast<float>(pos0);
   a.gpart = d_gamma ? reinterpret_cast<double*>(ws + p.off_g) : nullptr;
   a.tpart = d_theta ? reinterpret_cast<float*>(ws + p.off_t) : nullptr;
   const unsigned grid = static_cast<unsigned>(static_cast<int64_t>(B) * H * p.nseg);
@@ -2080,21 +2090,47 @@ ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v
       else launch_param_rows_g<__nv_bfloat16, __nv_bfloat16>(a, grid, vec, grad_dt, stream);
     }
   }
-  ret_status s = last_launch();
-  if (s != RET_OK) return s;
-  const bool have_state = d_gamma && (state_in || d_state_out);
-  double* spart = reinterpret_cast<double*>(ws + p.off_s);
-  if (have_state) {
-    Mark m("param_state", stream);
-    grad::state_dot_kernel<<<static_cast<unsigned>(B * H * grad::kStateSlices), 256, 0, stream>>>(
-        state_in, d_state_in, state_out, d_state_out, d_k * d_v, static_cast<float>(L - 1), spart);
-    if ((s = last_launch()) != RET_OK) return s;
+  if ((s = last_launch()) != RET_OK) return s;
+  // (2) the state walks in fp32 and their boundary products
+  float2* cs = reinterpret_cast<float2*>(ws + p.off_cs);
+  {
+    Mark m("param_angles", stream);
+    const size_t n = static_cast<size_t>(L) * (d_k / 2);
+    tcc::angle_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+        cs, cc, L, d_k / 2, static_cast<float>(pos0));
   }
+  grad::WalkArgs w{};
+  w.states = reinterpret_cast<float*>(ws + p.off_states);
+  w.cs = cs;
+  w.gpart = reinterpret_cast<double*>(ws + p.off_gw);
+  w.zpart = reinterpret_cast<float*>(ws + p.off_z);
+  w.H = H; w.L = L; w.d_k = d_k; w.d_v = d_v; w.C = p.C; w.ntk = p.ntk; w.ntv = p.ntv;
+  w.pos0 = static_cast<float>(pos0);
+  w.cc = cc;
+  {
+    grad::WalkArgs f = w;
+    f.a = k; f.b = v; f.s0 = state_in; f.s_in = nullptr;
+    f.ascale = cc.kscale;
+    Mark m("param_walk_fwd", stream);
+    if (in_dt == RET_F32) grad::state_walk_fwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(f);
+    else grad::state_walk_fwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(f);
+  }
+  if ((s = last_launch()) != RET_OK) return s;
+  {
+    grad::WalkArgs bw = w;
+    bw.a = q; bw.b = d_out; bw.s0 = d_state_out; bw.s_in = state_in;
+    bw.ascale = 1.f;
+    Mark m("param_walk_bwd", stream);
+    if (in_dt == RET_F32) grad::state_walk_bwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
+    else grad::state_walk_bwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
+  }
+  if ((s = last_launch()) != RET_OK) return s;
+  // (3) fixed-order finishing sums
   grad::FinishArgs f{};
-  f.gpart = a.gpart; f.spart = spart; f.tpart = a.tpart;
+  f.gpart = a.gpart; f.gwalk = w.gpart; f.tpart = a.tpart; f.zpart = w.zpart;
   f.d_gamma = d_gamma; f.d_theta = d_theta;
-  f.B = B; f.H = H; f.nseg = p.nseg; f.P = d_k / 2; f.have_state = have_state ? 1 : 0;
-  for (int h = 0; h < H; ++h) f.inv_gamma[h] = d_gamma ? 1.0 / static_cast<double>(gamma[h]) : 0.0;
+  f.B = B; f.H = H; f.nseg = p.nseg; f.P = d_k / 2; f.ntk = p.ntk; f.ntv = p.ntv;
+  for (int h = 0; h < H; ++h) f.inv_gamma[h] = 1.0 / static_cast<double>(gamma[h]);
   Mark m("param_finish", stream);
   grad::param_finish_kernel<<<static_cast<unsigned>(H + d_k / 2), 256, 0, stream>>>(f);
   return last_launch();

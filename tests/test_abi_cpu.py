@@ -363,23 +363,27 @@ def test_param_grads_and_groupnorm_validation(lib):
     g = np.array([0.9, 0.99], np.float32)
     nb = C.c_size_t(0)
     assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 64, 32, C.byref(nb)) == _lib.RET_OK
-    # 2 segments of 64 tokens × 4 heads: doubles, 16 state slices per head, 32 pairs of floats
-    assert nb.value == 256 + 512 + 1024
+    # 8 row segments (2 per head) and 4 walk tiles: doubles, 32 pair sums per
+    # segment, the angle table (100 × 32 float2), one chunk of 64 × 64 fp32
+    # states per tile, the walk partials
+    assert nb.value == 256 + 1024 + 25600 + 4 * 16384 + 256 + 512
     assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 63, 32, C.byref(nb)) == _lib.RET_EINVAL
+    th = np.full(32, 0.1, np.float32)
 
-    def call(d_gamma=P, d_theta=P, gamma=g, d_k=64, pos0=0, s_in=None, ds_in=None, s_out=None,
-             ds_out=None, ws=P, wsn=1 << 20, dq=P, in_dt=_lib.RET_BF16):
-        return lib.ret_chunkwise_param_grads(P, P, P, P, in_dt, P, _lib.RET_BF16, dq, P, P, _lib.RET_F32,
-                                             _fp(gamma), 2, 2, 100, d_k, 32, pos0, s_in, ds_in, s_out,
-                                             ds_out, d_gamma, d_theta, ws, wsn, None)
+    def call(d_gamma=P, d_theta=P, gamma=g, d_k=64, pos0=0, ws=P, wsn=1 << 20, dq=P, in_dt=_lib.RET_BF16,
+             theta=th, out=P):
+        return lib.ret_chunkwise_param_grads(P, P, P, P, in_dt, out, _lib.RET_BF16, dq, P, P, _lib.RET_F32,
+                                             _fp(gamma), _fp(theta), 2, 2, 100, d_k, 32, pos0, None, None,
+                                             d_gamma, d_theta, ws, wsn, None)
 
     assert call(d_gamma=None, d_theta=None) == _lib.RET_EINVAL
     assert call(d_k=63) == _lib.RET_EINVAL
     assert call(gamma=np.array([0.9, 0.0], np.float32)) == _lib.RET_EINVAL
-    assert call(s_in=P) == _lib.RET_EINVAL                      # state_in without d_state_in
-    assert call(ds_out=P) == _lib.RET_EINVAL                    # d_state_out without state_out
+    assert call(theta=np.full(32, np.nan, np.float32)) == _lib.RET_EINVAL
     assert call(pos0=(1 << 24) - 50) == _lib.RET_EINVAL
-    assert call(dq=None) == _lib.RET_EINVAL
+    assert call(dq=None) == _lib.RET_EINVAL                      # dθ needs dq
+    assert call(dq=None, d_theta=None, ws=None) == _lib.RET_EWORKSPACE   # …dγ alone does not
+    assert call(out=None, d_gamma=None, ws=None) == _lib.RET_EWORKSPACE  # …and dθ needs no out
     assert call(dq=C.c_void_p(0x1008)) == _lib.RET_EINVAL       # misaligned
     assert call(in_dt=5) == _lib.RET_EINVAL
     assert call(ws=None) == _lib.RET_EWORKSPACE
