@@ -1,5 +1,5 @@
 // Parameter gradients of the retention core (γ per head, θ per rotation
-// pair) and the GroupNorm backward.  All HBM-bound row passes.
+// pair), and the GroupNorm forward (row-staged) and backward.
 //
 // dγ_h, dθ_i.  Both are sums over (query n, key m) pairs of the decay- or
 // angle-weighted terms of <dO, out> + <dS_out, S_out> («从RoPE到Retention…»
@@ -494,6 +494,7 @@ __global__ void __launch_bounds__(128) gn_backward_kernel(const Tx* __restrict__
                                                           float* __restrict__ wpart, int H, int L,
                                                           int d_v, int nseg, float eps) {
   extern __shared__ float wsum[];   // [4 warps][2][d_v] when wpart is set
+  constexpr int R = NV >= 32 ? 1 : 2;   // rows in flight per warp
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int seg = blockIdx.x % nseg;
   const size_t bh = blockIdx.x / nseg;
@@ -504,80 +505,106 @@ __global__ void __launch_bounds__(128) gn_backward_kernel(const Tx* __restrict__
     const int c = VEC ? 8 * (lane + 32 * (e >> 3)) + (e & 7) : lane + 32 * e;
     return c < d_v ? c : -1;
   };
-  float aw[NV], ab[NV];
+  float aw[NV], ab[NV], wv[NV];
 #pragma unroll
-  for (int e = 0; e < NV; ++e) aw[e] = ab[e] = 0.f;
+  for (int e = 0; e < NV; ++e) {
+    aw[e] = ab[e] = 0.f;
+    const int c = chan(e);
+    wv[e] = c < 0 ? 0.f : (w ? __ldg(w + static_cast<size_t>(h) * d_v + c) : 1.f);
+  }
 
-  for (int t = t0 + warp; t < t1; t += 4) {
-    const size_t row = bh * L + t;
-    const Tx* xr = x + row * d_v;
-    const Tx* gr = dy + row * d_v;
-    float xv[NV], gv[NV];
+  for (int t = t0 + warp; t < t1; t += 4 * R) {
+    float xv[R][NV], gv[R][NV];
+    bool live[R];
 #pragma unroll
-    for (int j = 0; j < NV / 8; ++j) {
-      if (VEC) {
-        const int c = 8 * (lane + 32 * j);
-        float a8[8], b8[8];
-        if (c < d_v) {
-          load8(xr + c, a8);
-          load8(gr + c, b8);
+    for (int r = 0; r < R; ++r) {   // all loads of the R rows first
+      const int tr = t + 4 * r;
+      live[r] = tr < t1;
+      const size_t row = bh * L + (live[r] ? tr : t);
+      const Tx* xr = x + row * d_v;
+      const Tx* gr = dy + row * d_v;
+#pragma unroll
+      for (int j = 0; j < NV / 8; ++j) {
+        if (VEC) {
+          const int c = 8 * (lane + 32 * j);
+          float a8[8], b8[8];
+          if (c < d_v) {
+            load8(xr + c, a8);
+            load8(gr + c, b8);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a8[e] = b8[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { xv[r][8 * j + e] = a8[e]; gv[r][8 * j + e] = b8[e]; }
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) a8[e] = b8[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { xv[8 * j + e] = a8[e]; gv[8 * j + e] = b8[e]; }
-      } else {
-#pragma unroll
-        for (int e = 8 * j; e < 8 * j + 8; ++e) {
-          const int c = lane + 32 * e;
-          xv[e] = c < d_v ? to_f32(xr[c]) : 0.f;
-          gv[e] = c < d_v ? to_f32(gr[c]) : 0.f;
+          for (int e = 8 * j; e < 8 * j + 8; ++e) {
+            const int c = lane + 32 * e;
+            xv[r][e] = c < d_v ? to_f32(xr[c]) : 0.f;
+            gv[r][e] = c < d_v ? to_f32(gr[c]) : 0.f;
+          }
         }
       }
     }
-    float s = 0.f;
+    float mu[R], rstd[R], mg[R], mgx[R];
 #pragma unroll
-    for (int e = 0; e < NV; ++e) s += xv[e];
-    const float mu = warp_sum(s) * inv_n;
-    float q = 0.f;
+    for (int r = 0; r < R; ++r) {
+      float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < NV; ++e) {
-      const float d = chan(e) >= 0 ? xv[e] - mu : 0.f;
-      q = fmaf(d, d, q);
+      for (int e = 0; e < NV; ++e) s += xv[r][e];
+      mu[r] = warp_sum(s) * inv_n;
     }
-    const float rstd = rsqrtf(warp_sum(q) * inv_n + eps);
-    float sg = 0.f, sgx = 0.f;
 #pragma unroll
-    for (int e = 0; e < NV; ++e) {
-      const int c = chan(e);
-      const float xh = (xv[e] - mu) * rstd;
-      const float gw = c >= 0 ? gv[e] * (w ? __ldg(w + static_cast<size_t>(h) * d_v + c) : 1.f) : 0.f;
-      aw[e] = fmaf(gv[e], c >= 0 ? xh : 0.f, aw[e]);
-      ab[e] += gv[e];
-      xv[e] = xh;
-      gv[e] = gw;
-      sg += gw;
-      sgx = fmaf(gw, xh, sgx);
+    for (int r = 0; r < R; ++r) {
+      float q = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const float d = chan(e) >= 0 ? xv[r][e] - mu[r] : 0.f;
+        q = fmaf(d, d, q);
+      }
+      rstd[r] = rsqrtf(warp_sum(q) * inv_n + eps);
     }
-    const float mg = warp_sum(sg) * inv_n, mgx = warp_sum(sgx) * inv_n;
-    Tg* dr = dx + row * d_v;
 #pragma unroll
-    for (int j = 0; j < NV / 8; ++j) {
-      if (VEC) {
-        const int c = 8 * (lane + 32 * j);
-        if (c < d_v) {
-          float o8[8];
+    for (int r = 0; r < R; ++r) {
+      float sg = 0.f, sgx = 0.f;
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            o8[e] = rstd * (gv[8 * j + e] - mg - xv[8 * j + e] * mgx);
-          store8(dr + c, o8);
+      for (int e = 0; e < NV; ++e) {
+        const float xh = chan(e) >= 0 ? (xv[r][e] - mu[r]) * rstd[r] : 0.f;
+        const float gw = gv[r][e] * wv[e];
+        if (live[r]) {
+          aw[e] = fmaf(gv[r][e], xh, aw[e]);
+          ab[e] += gv[r][e];
         }
-      } else {
+        xv[r][e] = xh;
+        gv[r][e] = gw;
+        sg += gw;
+        sgx = fmaf(gw, xh, sgx);
+      }
+      mg[r] = warp_sum(sg) * inv_n;
+      mgx[r] = warp_sum(sgx) * inv_n;
+    }
 #pragma unroll
-        for (int e = 8 * j; e < 8 * j + 8; ++e) {
-          const int c = lane + 32 * e;
-          if (c < d_v) dr[c] = from_f32<Tg>(rstd * (gv[e] - mg - xv[e] * mgx));
+    for (int r = 0; r < R; ++r) {
+      if (!live[r]) continue;
+      Tg* dr = dx + (bh * L + t + 4 * r) * d_v;
+#pragma unroll
+      for (int j = 0; j < NV / 8; ++j) {
+        if (VEC) {
+          const int c = 8 * (lane + 32 * j);
+          if (c < d_v) {
+            float o8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o8[e] = rstd[r] * (gv[r][8 * j + e] - mg[r] - xv[r][8 * j + e] * mgx[r]);
+            store8(dr + c, o8);
+          }
+        } else {
+#pragma unroll
+          for (int e = 8 * j; e < 8 * j + 8; ++e) {
+            const int c = lane + 32 * e;
+            if (c < d_v) dr[c] = from_f32<Tg>(rstd[r] * (gv[r][e] - mg[r] - xv[r][e] * mgx[r]));
+          }
         }
       }
     }
@@ -605,6 +632,259 @@ __global__ void __launch_bounds__(128) gn_backward_kernel(const Tx* __restrict__
   }
 }
 
+// The same computation for 16-byte rows (d_v a multiple of 8), with the rows
+// staged through shared memory by per-lane asynchronous copies: each lane
+// copies the 16-byte pieces of x and dy it owns (channels 8·(lane + 32j) …
+// +7) for the next R rows while it works on the current R rows from the
+// other stage, so loads stay in flight during the reductions.  A lane only
+// ever reads the pieces it copied itself, so its own wait_group is the only
+// synchronisation.  Shared memory: [4 warps][2 stages][R][x, dy][d_v] plus,
+// after the loop, the [4 warps][2][d_v] parameter sums in the same space.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <typename Tx>
+__device__ __forceinline__ void lds8(const Tx* p, float (&x)[8]);
+template <> __device__ __forceinline__ void lds8<float>(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <> __device__ __forceinline__ void lds8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { x[2 * i] = bf16lo_to_f32(w[i]); x[2 * i + 1] = bf16hi_to_f32(w[i]); }
+}
+
+template <typename Tx, typename Tg, int NV>
+__global__ void __launch_bounds__(128) gn_backward_async_kernel(const Tx* __restrict__ x,
+                                                                const Tx* __restrict__ dy,
+                                                                const float* __restrict__ w,
+                                                                Tg* __restrict__ dx,
+                                                                float* __restrict__ wpart, int H,
+                                                                int L, int d_v, int nseg, float eps) {
+  extern __shared__ __align__(16) unsigned char gsm[];
+  constexpr int R = 2;                       // rows per stage and warp
+  constexpr int PER = 16 / sizeof(Tx);       // elements per 16-byte piece (8 or 4)
+  constexpr int NP = NV / 8;                 // 8-channel groups per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seg = blockIdx.x % nseg;
+  const size_t bh = blockIdx.x / nseg;
+  const int h = static_cast<int>(bh % H);
+  const int t0 = seg * kRowsPerBlock, t1 = min(L, t0 + kRowsPerBlock);
+  const float inv_n = 1.f / static_cast<float>(d_v);
+  Tx* stage = reinterpret_cast<Tx*>(gsm) + static_cast<size_t>(warp) * 2 * R * 2 * d_v;
+  auto buf = [&](int st, int r, int arr) { return stage + ((st * R + r) * 2 + arr) * static_cast<size_t>(d_v); };
+  // issue the copies of the R rows starting at token tt into stage st
+  auto issue = [&](int tt, int st) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int tr = tt + 4 * r;
+      if (tr >= t1) continue;
+      const size_t row = (bh * L + tr) * static_cast<size_t>(d_v);
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        if (c >= d_v) continue;
+#pragma unroll
+        for (int u = 0; u < 8; u += PER) {
+          cp_async16(buf(st, r, 0) + c + u, x + row + c + u);
+          cp_async16(buf(st, r, 1) + c + u, dy + row + c + u);
+        }
+      }
+    }
+    cp_async_commit();
+  };
+  float aw[NV], ab[NV], wv[NV];
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    aw[e] = ab[e] = 0.f;
+    const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
+    wv[e] = c >= d_v ? 0.f : (w ? __ldg(w + static_cast<size_t>(h) * d_v + c) : 1.f);
+  }
+  int st = 0;
+  issue(t0 + warp, 0);
+  for (int t = t0 + warp; t < t1; t += 4 * R, st ^= 1) {
+    issue(t + 4 * R, st ^ 1);   // the next rows (an empty group past the end)
+    cp_async_wait1();           // this lane's copies of the current rows have landed
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int tr = t + 4 * r;
+      if (tr >= t1) break;      // uniform across the warp
+      float xv[NV], gv[NV];
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        float a8[8], b8[8];
+        if (c < d_v) {
+          lds8(buf(st, r, 0) + c, a8);
+          lds8(buf(st, r, 1) + c, b8);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a8[e] = b8[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { xv[8 * j + e] = a8[e]; gv[8 * j + e] = b8[e]; }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) s += xv[e];
+      const float mu = warp_sum(s) * inv_n;
+      float q = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
+        const float d = c < d_v ? xv[e] - mu : 0.f;
+        q = fmaf(d, d, q);
+      }
+      const float rstd = rsqrtf(warp_sum(q) * inv_n + eps);
+      float sg = 0.f, sgx = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
+        const float xh = c < d_v ? (xv[e] - mu) * rstd : 0.f;
+        const float gw = gv[e] * wv[e];
+        aw[e] = fmaf(gv[e], xh, aw[e]);
+        ab[e] += gv[e];
+        xv[e] = xh;
+        gv[e] = gw;
+        sg += gw;
+        sgx = fmaf(gw, xh, sgx);
+      }
+      const float mg = warp_sum(sg) * inv_n, mgx = warp_sum(sgx) * inv_n;
+      Tg* dr = dx + (bh * L + tr) * static_cast<size_t>(d_v);
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        if (c < d_v) {
+          float o8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o8[e] = rstd * (gv[8 * j + e] - mg - xv[8 * j + e] * mgx);
+          store8(dr + c, o8);
+        }
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (!wpart) return;
+  __syncthreads();   // every warp is done with the stages: reuse them for the sums
+  float* wsum = reinterpret_cast<float*>(gsm);
+#pragma unroll
+  for (int e = 0; e < NV; ++e) {
+    const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
+    if (c < d_v) {
+      wsum[(warp * 2) * d_v + c] = aw[e];
+      wsum[(warp * 2 + 1) * d_v + c] = ab[e];
+    }
+  }
+  __syncthreads();
+  float* dst = wpart + static_cast<size_t>(blockIdx.x) * 2 * d_v;
+  for (int c = threadIdx.x; c < d_v; c += 128) {
+    float sw = 0.f, sb = 0.f;
+#pragma unroll
+    for (int w4 = 0; w4 < 4; ++w4) {
+      sw += wsum[(w4 * 2) * d_v + c];
+      sb += wsum[(w4 * 2 + 1) * d_v + c];
+    }
+    dst[c] = sw;
+    dst[d_v + c] = sb;
+  }
+}
+
+// GroupNorm forward over 16-byte rows (d_v a multiple of 8), rows staged
+// through shared memory the same way: one group per (b, h, t) row over its d_v
+// channels, biased variance, optional affine («从RoPE到Retention…» §5).  y may
+// be x (same type): a lane writes only the channels it copied itself, after
+// copying them.  Block = 4 warps × R rows per stage; grid over rows.
+template <typename Tx, typename Ty, int NV>
+__global__ void __launch_bounds__(128) gn_forward_async_kernel(const Tx* x, Ty* y,
+                                                               const float* __restrict__ w,
+                                                               const float* __restrict__ b, int H,
+                                                               int L, int d_v, size_t rows,
+                                                               int rows_per_block, float eps) {
+  extern __shared__ __align__(16) unsigned char gsm[];
+  constexpr int R = 2;
+  constexpr int PER = 16 / sizeof(Tx);
+  constexpr int NP = NV / 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t r0 = static_cast<size_t>(blockIdx.x) * rows_per_block;
+  const size_t r1 = min(rows, r0 + rows_per_block);
+  const float inv_n = 1.f / static_cast<float>(d_v);
+  Tx* stage = reinterpret_cast<Tx*>(gsm) + static_cast<size_t>(warp) * 2 * R * d_v;
+  auto issue = [&](size_t rr, int st) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const size_t row = rr + 4 * r;
+      if (row >= r1) continue;
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        if (c >= d_v) continue;
+#pragma unroll
+        for (int u = 0; u < 8; u += PER)
+          cp_async16(stage + (st * R + r) * static_cast<size_t>(d_v) + c + u, x + row * d_v + c + u);
+      }
+    }
+    cp_async_commit();
+  };
+  int st = 0;
+  issue(r0 + warp, 0);
+  for (size_t row0 = r0 + warp; row0 < r1; row0 += 4 * R, st ^= 1) {
+    issue(row0 + 4 * R, st ^ 1);
+    cp_async_wait1();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const size_t row = row0 + 4 * r;
+      if (row >= r1) break;
+      const int h = static_cast<int>((row / L) % H);
+      float xv[NV];
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        float a8[8];
+        if (c < d_v) lds8(stage + (st * R + r) * static_cast<size_t>(d_v) + c, a8);
+        else
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a8[e] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) xv[8 * j + e] = a8[e];
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) s += xv[e];
+      const float mu = warp_sum(s) * inv_n;
+      float q = 0.f;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
+        const float d = c < d_v ? xv[e] - mu : 0.f;
+        q = fmaf(d, d, q);
+      }
+      const float rstd = rsqrtf(warp_sum(q) * inv_n + eps);
+#pragma unroll
+      for (int j = 0; j < NP; ++j) {
+        const int c = 8 * (lane + 32 * j);
+        if (c >= d_v) continue;
+        float o8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float val = (xv[8 * j + e] - mu) * rstd;
+          if (w) val *= __ldg(w + static_cast<size_t>(h) * d_v + c + e);
+          if (b) val += __ldg(b + static_cast<size_t>(h) * d_v + c + e);
+          o8[e] = val;
+        }
+        store8(y + row * d_v + c, o8);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // d_weight[h][c], d_bias[h][c] = Σ over b and segments of wpart, in double.
 // grid = (⌈d_v/32⌉, H), block = 32 channels × 8 row groups; group r takes the
 // partials r, r + 8, … and the 8 group sums are added in order.
@@ -616,13 +896,25 @@ __global__ void __launch_bounds__(256) gn_param_finish_kernel(const float* __res
   const int c = blockIdx.x * 32 + cx;
   const int h = blockIdx.y;
   double sw = 0.0, sb = 0.0;
-  if (c < d_v)
-    for (int i = r; i < B * nseg; i += 8) {
-      const int b = i / nseg, seg = i % nseg;
-      const float* p = wpart + ((static_cast<size_t>(b) * H + h) * nseg + seg) * 2 * d_v;
-      sw += p[c];
-      sb += p[d_v + c];
+  if (c < d_v) {
+    const int n = B * nseg;
+    for (int i0 = r; i0 < n; i0 += 64) {   // eight partials of this group in flight
+      float fw[8], fb[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + 8 * u;
+        fw[u] = fb[u] = 0.f;
+        if (i < n) {
+          const int b = i / nseg, seg = i % nseg;
+          const float* p = wpart + ((static_cast<size_t>(b) * H + h) * nseg + seg) * 2 * d_v;
+          fw[u] = p[c];
+          fb[u] = p[d_v + c];
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) { sw += fw[u]; sb += fb[u]; }
     }
+  }
   red[0][r][cx] = sw;
   red[1][r][cx] = sb;
   __syncthreads();

@@ -221,7 +221,7 @@ struct Plan {
   int path = 0;
   size_t bytes = 0;
   // workspace offsets
-  size_t off_q = 0, off_k = 0, off_states = 0, off_ofp32 = 0;
+  size_t off_q = 0, off_k = 0, off_states = 0;
   size_t off_tail = 0;   // staging of a short last chunk's outputs (tensor-core path)
   // Ring mode (carried layout on CTA pairs): off_q / off_k hold the ring of
   // `ring` chunk slots for ring_heads heads; off_flags its counters; off_cs
@@ -293,7 +293,6 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
     p.off_k = off; off += up256(BH * L * d_k * 4);
     p.off_states = off; off += up256(BH * nch * static_cast<size_t>(d_k) * d_v * 4);
   }
-  if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
   p.bytes = off;
   return p;
 }
@@ -315,7 +314,6 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
       p.off_states = off;
       off += up256(BH * (L / tcc::CH) * static_cast<size_t>(d_k) * d_v * 4);
     }
-    if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
     p.bytes = off;
     return p;
   }
@@ -323,9 +321,37 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
   p.off_q = off; off += up256(BH * L * d_k * 4);
   p.off_k = off; off += up256(BH * L * d_k * 4);
   if (want_state) { p.off_states = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4); }
-  if (gn) { p.off_ofp32 = off; off += up256(BH * L * static_cast<size_t>(d_v) * 4); }
   p.bytes = off;
   return p;
+}
+
+// GroupNorm over the rows of x into y (y may be x when Tx = Ty): the staged
+// 16-byte-row kernel when d_v is a multiple of 8, else one warp per row.
+template <typename Tx, typename Ty, int NV>
+void launch_gn_forward_nv(const Tx* x, Ty* y, const ret_gn* gn, int H, int L, int d_v, size_t rows,
+                          cudaStream_t st) {
+  constexpr int kRowsPerBlock = 64;
+  const size_t smem = static_cast<size_t>(4 * 2 * 2) * d_v * sizeof(Tx);
+  auto kern = grad::gn_forward_async_kernel<Tx, Ty, NV>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  kern<<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 128, smem, st>>>(
+      x, y, gn->weight, gn->bias, H, L, d_v, rows, kRowsPerBlock, gn->eps);
+}
+
+template <typename Tx, typename Ty>
+void launch_groupnorm(const Tx* x, Ty* y, const ret_gn* gn, int H, int L, int d_v, size_t rows,
+                      cudaStream_t st) {
+  Mark m("groupnorm", st);
+  if (d_v % 8 != 0) {
+    simt::groupnorm_kernel<Tx, Ty><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+        x, y, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
+  } else if (d_v <= 256) {
+    launch_gn_forward_nv<Tx, Ty, 8>(x, y, gn, H, L, d_v, rows, st);
+  } else if (d_v <= 512) {
+    launch_gn_forward_nv<Tx, Ty, 16>(x, y, gn, H, L, d_v, rows, st);
+  } else {
+    launch_gn_forward_nv<Tx, Ty, 32>(x, y, gn, H, L, d_v, rows, st);
+  }
 }
 
 template <typename T> T* wsp(void* ws, size_t off) {
@@ -371,22 +397,17 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
     simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
         states, s_in, s_out, cc, H, d_k, d_v, nch, BH);
   }
-  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
   {
     dim3 g2((d_v + 63) / 64, (chunk + 15) / 16, BH * nch);
     const size_t smem = (16 * static_cast<size_t>(d_k) + 16 * 64) * sizeof(float);
     // ws_states == nullptr means "use state_in for the single chunk" (parallel form)
     const float* wst = (nch > 1 || states) ? states : nullptr;
     Mark m("chunk_out_f32", st);
-    simt::chunk_out_kernel<Tin, Tout><<<g2, 256, smem, st>>>(qp, kp, v, wst, s_in, out, ofp, cc,
+    simt::chunk_out_kernel<Tin, Tout><<<g2, 256, smem, st>>>(qp, kp, v, wst, s_in, out, nullptr, cc,
                                                              H, L, d_k, d_v, chunk, nch);
   }
-  if (ofp) {
-    const size_t rows = static_cast<size_t>(BH) * L;
-    Mark m("groupnorm", st);
-    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-        ofp, out, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
-  }
+  if (gn_on(gn))   // in place over out
+    launch_groupnorm<Tout, Tout>(out, out, gn, H, L, d_v, static_cast<size_t>(BH) * L, st);
   return last_launch();
 }
 
@@ -482,12 +503,11 @@ ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __n
       !make_map(&mk, rk, ring_rows, DK) ||
       !make_map3(&mv, v, static_cast<uint64_t>(BH), static_cast<uint64_t>(L), d_v))
     return RET_ECUDA;
-  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
   tcc::ChunkArgs a;
   a.state_in = s_in;
   a.state_out = s_out;
-  a.out = ofp ? static_cast<void*>(ofp) : static_cast<void*>(out);
-  a.out_f32 = (ofp || sizeof(Tout) == 4) ? 1 : 0;
+  a.out = static_cast<void*>(out);
+  a.out_f32 = sizeof(Tout) == 4 ? 1 : 0;
   a.H = H;
   a.d_v = d_v;
   a.nchunks = nch;
@@ -549,12 +569,8 @@ ret_status run_tc_ring(const __nv_bfloat16* q, const __nv_bfloat16* k, const __n
         row_vecs);
     if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
   }
-  if (ofp) {
-    const size_t r = static_cast<size_t>(BH) * L;
-    Mark m("groupnorm", st);
-    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
-        ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
-  }
+  if (gn_on(gn))   // in place over out
+    launch_groupnorm<Tout, Tout>(out, out, gn, H, L, d_v, static_cast<size_t>(BH) * L, st);
   return last_launch();
 }
 
@@ -602,12 +618,11 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   CUtensorMap mqh, mkh;   // 64-row boxes of Q′ / K̂′ for the pair kernel
   if (pair && (!make_map(&mqh, qr, rows, d_k, 64) || !make_map(&mkh, kr, rows, d_k, 64)))
     return RET_ECUDA;
-  float* ofp = gn_on(gn) ? wsp<float>(ws, p.off_ofp32) : nullptr;
   tcc::ChunkArgs a;
   a.state_in = s_in;
   a.state_out = s_out;
-  a.out = ofp ? static_cast<void*>(ofp) : static_cast<void*>(out);
-  a.out_f32 = (ofp || sizeof(Tout) == 4) ? 1 : 0;
+  a.out = static_cast<void*>(out);
+  a.out_f32 = sizeof(Tout) == 4 ? 1 : 0;
   a.H = H;
   a.d_v = d_v;
   a.nchunks = nch;
@@ -737,12 +752,8 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
         row_vecs);
     if (cudaGetLastError() != cudaSuccess) return RET_ECUDA;
   }
-  if (ofp) {
-    const size_t r = static_cast<size_t>(BH) * L;
-    Mark m("groupnorm", st);
-    simt::groupnorm_kernel<float, Tout><<<static_cast<unsigned>((r + 7) / 8), 256, 0, st>>>(
-        ofp, out, gn->weight, gn->bias, H, L, d_v, r, gn->eps);
-  }
+  if (gn_on(gn))   // in place over out
+    launch_groupnorm<Tout, Tout>(out, out, gn, H, L, d_v, static_cast<size_t>(BH) * L, st);
   return last_launch();
 }
 
@@ -1917,7 +1928,13 @@ void launch_gn_backward_nv(const void* x, const void* dy, const float* w, void* 
                            int H, int L, int d_v, int nseg, float eps, unsigned grid, bool vec,
                            cudaStream_t st) {
   const size_t smem = wpart ? static_cast<size_t>(8) * d_v * sizeof(float) : 0;
-  if (vec)
+  if (vec) {   // rows staged through shared memory: [4 warps][2 stages][2 rows][x, dy][d_v]
+    const size_t ssm = std::max(static_cast<size_t>(4 * 2 * 2 * 2) * d_v * sizeof(Tx), smem);
+    auto kern = grad::gn_backward_async_kernel<Tx, Tg, NV>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
+    kern<<<grid, 128, ssm, st>>>(static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w,
+                                 static_cast<Tg*>(dx), wpart, H, L, d_v, nseg, eps);
+  } else if (vec)
     grad::gn_backward_kernel<Tx, Tg, true, NV><<<grid, 128, smem, st>>>(
         static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w, static_cast<Tg*>(dx), wpart, H,
         L, d_v, nseg, eps);
@@ -1953,28 +1970,22 @@ extern "C" {
 ret_status ret_groupnorm(const void* x, ret_dtype x_dt, void* y, ret_dtype y_dt, int B, int H,
                          int L, int d_v, const ret_gn* gn, cudaStream_t stream) {
   Range nv("ret_groupnorm");
-  if (!x || !y || !gn || !ok_dt(x_dt) || !ok_dt(y_dt)) return RET_EINVAL;
+  if (!x || !y || !gn || !ok_dt(x_dt) || !ok_dt(y_dt) || !al16(x) || !al16(y)) return RET_EINVAL;
   if (B < 1 || H < 1 || L < 1 || d_v < 1 || d_v > 1024) return RET_EINVAL;
   const int64_t rows = static_cast<int64_t>(B) * H * L;
   if (rows >= (int64_t(1) << 31)) return RET_EINVAL;
   if (!(gn->eps > 0.f) || !std::isfinite(gn->eps)) return RET_EINVAL;
   if (x == y && x_dt != y_dt) return RET_EINVAL;   // in place only with one type
-  Mark m("groupnorm", stream);
-  const unsigned grid = static_cast<unsigned>((rows + 7) / 8);
   const size_t r = static_cast<size_t>(rows);
   if (x_dt == RET_F32 && y_dt == RET_F32)
-    simt::groupnorm_kernel<float, float><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(x), static_cast<float*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+    launch_groupnorm(static_cast<const float*>(x), static_cast<float*>(y), gn, H, L, d_v, r, stream);
   else if (x_dt == RET_F32)
-    simt::groupnorm_kernel<float, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+    launch_groupnorm(static_cast<const float*>(x), static_cast<__nv_bfloat16*>(y), gn, H, L, d_v, r, stream);
   else if (y_dt == RET_F32)
-    simt::groupnorm_kernel<__nv_bfloat16, float><<<grid, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), gn->weight, gn->bias, H, L, d_v, r, gn->eps);
+    launch_groupnorm(static_cast<const __nv_bfloat16*>(x), static_cast<float*>(y), gn, H, L, d_v, r, stream);
   else
-    simt::groupnorm_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), gn->weight, gn->bias, H, L, d_v, r,
-        gn->eps);
+    launch_groupnorm(static_cast<const __nv_bfloat16*>(x), static_cast<__nv_bfloat16*>(y), gn, H, L, d_v, r,
+                     stream);
   return last_launch();
 }
 

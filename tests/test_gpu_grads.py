@@ -200,7 +200,7 @@ def test_training_chain_with_groupnorm():
     d_o, d_w, _ = R.groupnorm_backward(o, dz.cuda(), 1e-5, gw.cuda())
     dq, dk, dv, ds_in = R.chunkwise_backward(q, k, v, d_o, inp["gamma"], inp["theta"], chunk=32, pos0=4,
                                              state_in=s_in)
-    dg, dt = R.param_grads(q, k, v, d_o, o, dq, dk, dv, inp["gamma"], pos0=4, state_in=s_in, d_state_in=ds_in)
+    dg, dt = R.param_grads(q, k, v, d_o, o, dq, dk, dv, inp["gamma"], inp["theta"], pos0=4, state_in=s_in)
     assert R.sync_status() == R.RET_OK
     args = [to_f64(inp[n]) for n in ("q", "k", "v")]
     gam, th = np.asarray(inp["gamma"], np.float64), np.asarray(inp["theta"], np.float64)
