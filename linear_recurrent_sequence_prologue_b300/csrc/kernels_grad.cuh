@@ -71,6 +71,29 @@ template <> __device__ __forceinline__ void store8<__nv_bfloat16>(__nv_bfloat16*
                                             pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
 }
 
+// Per-thread asynchronous 16-byte copies global → shared (waited for with
+// cp.async.wait_group by the copying thread).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+template <typename Tx>
+__device__ __forceinline__ void lds8(const Tx* p, float (&x)[8]);
+template <> __device__ __forceinline__ void lds8<float>(const float* p, float (&x)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+template <> __device__ __forceinline__ void lds8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { x[2 * i] = bf16lo_to_f32(w[i]); x[2 * i + 1] = bf16hi_to_f32(w[i]); }
+}
+
 __device__ __forceinline__ float warp_sum(float s) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
@@ -421,6 +444,234 @@ __global__ void __launch_bounds__(256) state_walk_bwd_kernel(WalkArgs w) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// Faster walks for d_k and d_v multiples of 64.  A prep pass writes the walks'
+// left operands once, in fp32: kf[bh][t] = d_k^{-1/2}·γ^{b_c−1−j}·R k_t and
+// qb[bh][t] = γ^{j+1}·R q_t.  A walk block (64 threads, one 64 × 64 state
+// tile, thread (ty, tx) = (tid / 8, tid % 8) owning rows 8ty … 8ty+7 and
+// columns 8tx … 8tx+7) streams the rows of its chunks in stages of 32 through
+// a double-buffered shared-memory ring filled by asynchronous copies, so the
+// next stage loads while the current one is multiplied.  States are stored
+// per (b, h, chunk, tile) as [16 float4 slots][64 threads].
+// ---------------------------------------------------------------------------
+template <typename Tin>
+__global__ void __launch_bounds__(256) walk_prep_kernel(const Tin* __restrict__ q, const Tin* __restrict__ k,
+                                                        float* __restrict__ qb, float* __restrict__ kf,
+                                                        const float2* __restrict__ cs, CallConsts cc,
+                                                        int H, int L, int d_k, size_t rows) {
+  const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;   // (row, 4 pairs)
+  const int groups = d_k / 8;
+  if (idx >= rows * groups) return;
+  const size_t row = idx / groups;
+  const int g = static_cast<int>(idx % groups);
+  const int t = static_cast<int>(row % L);
+  const int h = static_cast<int>((row / L) % H);
+  const int c = t / kGradChunk, j = t % kGradChunk;
+  const int bc = min(kGradChunk, L - c * kGradChunk);
+  const float wk = cc.kscale * exp2f(static_cast<float>(bc - 1 - j) * cc.lg2g[h]);
+  const float wq = exp2f(static_cast<float>(j + 1) * cc.lg2g[h]);
+  float xq[8], xk[8];
+  load8(q + row * d_k + 8 * g, xq);
+  load8(k + row * d_k + 8 * g, xk);
+  float oq[8], ok[8];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float2 e = cs[static_cast<size_t>(t) * (d_k / 2) + 4 * g + u];
+    oq[2 * u] = wq * fmaf(xq[2 * u], e.x, -xq[2 * u + 1] * e.y);
+    oq[2 * u + 1] = wq * fmaf(xq[2 * u + 1], e.x, xq[2 * u] * e.y);
+    ok[2 * u] = wk * fmaf(xk[2 * u], e.x, -xk[2 * u + 1] * e.y);
+    ok[2 * u + 1] = wk * fmaf(xk[2 * u + 1], e.x, xk[2 * u] * e.y);
+  }
+  store8(qb + row * d_k + 8 * g, oq);
+  store8(kf + row * d_k + 8 * g, ok);
+}
+
+template <typename Tin>
+struct Walk2Smem {
+  static constexpr int A_BYTES = kStage * kTile * 4;
+  static constexpr int B_BYTES = kStage * kTile * static_cast<int>(sizeof(Tin));
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int BYTES = 2 * STAGE;
+};
+
+// Stage s of a walk: rows [t0, t0 + n) of the sequence (n ≤ 32, all in one chunk).
+struct StageRows { int c, t0, n; };
+
+__device__ __forceinline__ StageRows walk_stage(int s, int L, int C, bool fwd) {
+  StageRows r;
+  if (fwd) {
+    r.t0 = kStage * s;
+    r.c = r.t0 / kGradChunk;
+  } else {   // chunks from the last down, rows ascending inside each
+    const int rl = L - (C - 1) * kGradChunk;
+    const int nl = (rl + kStage - 1) / kStage;
+    if (s < nl) {
+      r.c = C - 1;
+      r.t0 = (C - 1) * kGradChunk + kStage * s;
+    } else {
+      const int s2 = s - nl;
+      r.c = C - 2 - s2 / (kGradChunk / kStage);
+      r.t0 = r.c * kGradChunk + kStage * (s2 % (kGradChunk / kStage));
+    }
+  }
+  r.n = min(kStage, min(L, (r.c + 1) * kGradChunk) - r.t0);
+  return r;
+}
+
+template <typename Tin, bool FWD>
+__global__ void __launch_bounds__(64) state_walk2_kernel(WalkArgs w, const float* __restrict__ aop) {
+  extern __shared__ __align__(16) unsigned char wsm[];
+  using SM = Walk2Smem<Tin>;
+  constexpr int PER = 16 / sizeof(Tin);
+  const int ntiles = w.ntk * w.ntv;
+  const size_t bh = blockIdx.x / ntiles;
+  const int tile = blockIdx.x % ntiles;
+  const int h = static_cast<int>(bh % w.H);
+  const int k0 = (tile / w.ntv) * kTile, v0 = (tile % w.ntv) * kTile;
+  const int tid = threadIdx.x, ty = tid >> 3, tx = tid & 7;
+  const Tin* Bm = static_cast<const Tin*>(w.b);
+  const int rl = w.L - (w.C - 1) * kGradChunk;
+  const int nstages = (w.C - 1) * (kGradChunk / kStage) + (rl + kStage - 1) / kStage;
+
+  auto issue = [&](int s) {
+    if (s < nstages) {
+      const StageRows sr = walk_stage(s, w.L, w.C, FWD);
+      float* As = reinterpret_cast<float*>(wsm + (s & 1) * SM::STAGE);
+      Tin* Bs = reinterpret_cast<Tin*>(wsm + (s & 1) * SM::STAGE + SM::A_BYTES);
+      for (int e = tid; e < sr.n * (kTile / 4); e += 64) {     // A: 16 pieces per row
+        const int r = e / (kTile / 4), pc = e % (kTile / 4);
+        cp_async16(As + r * kTile + 4 * pc, aop + (bh * w.L + sr.t0 + r) * static_cast<size_t>(w.d_k) + k0 + 4 * pc);
+      }
+      constexpr int BP = kTile / PER;                          // B pieces per row
+      for (int e = tid; e < sr.n * BP; e += 64) {
+        const int r = e / BP, pc = e % BP;
+        cp_async16(Bs + r * kTile + PER * pc, Bm + (bh * w.L + sr.t0 + r) * static_cast<size_t>(w.d_v) + v0 + PER * pc);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[8][8];
+  {   // S_in (forward) or dS_out (backward)
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        acc[r][q] = w.s0 ? w.s0[(bh * w.d_k + k0 + 8 * ty + r) * static_cast<size_t>(w.d_v) + v0 + 8 * tx + q] : 0.f;
+  }
+  double gacc = 0.0, zacc[4] = {0.0, 0.0, 0.0, 0.0};
+  auto state_slot = [&](int c) {
+    return reinterpret_cast<float4*>(w.states + ((bh * w.C + c) * ntiles + tile) * 4096);
+  };
+  // backward: weighted boundary products of acc (= dS_c) with S_c
+  auto boundary = [&](int c) {
+    float ip = 0.f, z[4] = {0.f, 0.f, 0.f, 0.f};
+    const float4* src = c >= 0 ? state_slot(c) : nullptr;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      float sx[8];
+      if (c >= 0) {
+        const float4 a = src[(2 * r) * 64 + tid], b = src[(2 * r + 1) * 64 + tid];
+        sx[0] = a.x; sx[1] = a.y; sx[2] = a.z; sx[3] = a.w; sx[4] = b.x; sx[5] = b.y; sx[6] = b.z; sx[7] = b.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          sx[q] = w.s_in ? w.s_in[(bh * w.d_k + k0 + 8 * ty + r) * static_cast<size_t>(w.d_v) + v0 + 8 * tx + q] : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) ip = fmaf(sx[q], acc[r][q], ip);
+      if (r & 1) {   // pair (r − 1, r): Σ S[r]·dS[r−1] − S[r−1]·dS[r]; S[r−1] kept from the last row
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[r >> 1] += sx[q] * acc[r - 1][q];
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) z[r >> 1] -= sx[q] * acc[r + 1][q];
+      }
+    }
+    float wg, wt;
+    if (c == w.C - 1) {
+      wg = static_cast<float>(rl - 1) - kKappa;
+      wt = -(w.pos0 + static_cast<float>((w.C - 1) * kGradChunk) + kKappa);
+    } else if (c < 0) {
+      wg = 1.f + kKappa;
+      wt = w.pos0 + kKappa;
+    } else {
+      wg = wt = static_cast<float>(kGradChunk);
+    }
+    gacc += static_cast<double>(wg) * ip;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) zacc[p] += static_cast<double>(wt) * z[p];
+  };
+  if (!FWD) boundary(w.C - 1);
+
+  issue(0);
+  for (int s = 0; s < nstages; ++s) {
+    const StageRows sr = walk_stage(s, w.L, w.C, FWD);
+    const int bc = min(kGradChunk, w.L - sr.c * kGradChunk);
+    if (sr.t0 == sr.c * kGradChunk) {   // first stage of a chunk: decay the carried state
+      const float g = exp2f(static_cast<float>(bc) * w.cc.lg2g[h]);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[r][q] *= g;
+    }
+    issue(s + 1);
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncthreads();
+    const float* As = reinterpret_cast<const float*>(wsm + (s & 1) * SM::STAGE);
+    const Tin* Bs = reinterpret_cast<const Tin*>(wsm + (s & 1) * SM::STAGE + SM::A_BYTES);
+    auto step = [&](int i) {
+      const float4 a0 = *reinterpret_cast<const float4*>(As + i * kTile + 8 * ty);
+      const float4 a1 = *reinterpret_cast<const float4*>(As + i * kTile + 8 * ty + 4);
+      float bv[8];
+      lds8(Bs + i * kTile + 8 * tx, bv);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+    };
+    if (sr.n == kStage) {   // full stage: unrolled, so the next rows' loads issue early
+#pragma unroll 8
+      for (int i = 0; i < kStage; ++i) step(i);
+    } else {
+      for (int i = 0; i < sr.n; ++i) step(i);
+    }
+    __syncthreads();   // the buffer of stage s is refilled by issue(s + 2)
+    if (sr.t0 + sr.n == sr.c * kGradChunk + bc) {   // last stage of the chunk
+      if (FWD) {
+        float4* dst = state_slot(sr.c);
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          dst[(2 * r) * 64 + tid] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+          dst[(2 * r + 1) * 64 + tid] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+        }
+      } else {
+        boundary(sr.c - 1);
+      }
+    }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (FWD) return;
+  __shared__ double gred[64];
+  __shared__ float zred[8][4][8];
+  gred[tid] = gacc;
+#pragma unroll
+  for (int p = 0; p < 4; ++p) zred[ty][p][tx] = static_cast<float>(zacc[p]);
+  __syncthreads();
+  if (tid == 0) {
+    double t = 0.0;
+    for (int i = 0; i < 64; ++i) t += gred[i];
+    w.gpart[blockIdx.x] = t;
+  }
+  if (tid < 32) {   // tile pair 4·ty + p = rows 8ty + 2p, 8ty + 2p + 1
+    const int yy = tid >> 2, p = tid & 3;
+    float z = 0.f;
+    for (int x = 0; x < 8; ++x) z += zred[yy][p][x];
+    w.zpart[static_cast<size_t>(blockIdx.x) * 32 + tid] = z;
+  }
+}
+
 // Finishing sums, in double and in a fixed order (strided per thread, then a
 // fixed tree).  Blocks [0, H): dγ_h = γ_h⁻¹ · (the B·nseg row partials +
 // the B·tiles boundary partials of head h).  Blocks [H, H + P): dθ_i = the
@@ -640,27 +891,6 @@ __global__ void __launch_bounds__(128) gn_backward_kernel(const Tx* __restrict__
 // ever reads the pieces it copied itself, so its own wait_group is the only
 // synchronisation.  Shared memory: [4 warps][2 stages][R][x, dy][d_v] plus,
 // after the loop, the [4 warps][2][d_v] parameter sums in the same space.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
-               "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-
-template <typename Tx>
-__device__ __forceinline__ void lds8(const Tx* p, float (&x)[8]);
-template <> __device__ __forceinline__ void lds8<float>(const float* p, float (&x)[8]) {
-  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-template <> __device__ __forceinline__ void lds8<__nv_bfloat16>(const __nv_bfloat16* p, float (&x)[8]) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) { x[2 * i] = bf16lo_to_f32(w[i]); x[2 * i + 1] = bf16hi_to_f32(w[i]); }
-}
-
 template <typename Tx, typename Tg, int NV>
 __global__ void __launch_bounds__(128) gn_backward_async_kernel(const Tx* __restrict__ x,
                                                                 const Tx* __restrict__ dy,

@@ -1888,7 +1888,8 @@ namespace {
 // ---------------------------------------------------------------------------
 struct ParamPlan {
   int nseg, C, ntk, ntv;
-  size_t off_g, off_t, off_cs, off_states, off_gw, off_z, bytes;
+  bool fast;   // d_k, d_v multiples of 64: prepped fp32 operands, 64-thread walks
+  size_t off_g, off_t, off_cs, off_states, off_gw, off_z, off_qb, off_kf, bytes;
 };
 
 ParamPlan plan_param_grads(int B, int H, int L, int d_k, int d_v) {
@@ -1906,6 +1907,12 @@ ParamPlan plan_param_grads(int B, int H, int L, int d_k, int d_v) {
   p.off_states = off; off += up256(nwalk * p.C * 4096 * sizeof(float));
   p.off_gw = off; off += up256(nwalk * sizeof(double));
   p.off_z = off; off += up256(nwalk * 32 * sizeof(float));
+  p.fast = d_k % grad::kTile == 0 && d_v % grad::kTile == 0;
+  if (p.fast) {
+    const size_t nop = BH * static_cast<size_t>(L) * d_k * sizeof(float);
+    p.off_qb = off; off += up256(nop);
+    p.off_kf = off; off += up256(nop);
+  }
   p.bytes = off;
   return p;
 }
@@ -2118,24 +2125,56 @@ ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v
   w.H = H; w.L = L; w.d_k = d_k; w.d_v = d_v; w.C = p.C; w.ntk = p.ntk; w.ntv = p.ntv;
   w.pos0 = static_cast<float>(pos0);
   w.cc = cc;
-  {
-    grad::WalkArgs f = w;
-    f.a = k; f.b = v; f.s0 = state_in; f.s_in = nullptr;
-    f.ascale = cc.kscale;
-    Mark m("param_walk_fwd", stream);
-    if (in_dt == RET_F32) grad::state_walk_fwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(f);
-    else grad::state_walk_fwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(f);
+  grad::WalkArgs fw = w;
+  fw.a = k; fw.b = v; fw.s0 = state_in; fw.s_in = nullptr;
+  fw.ascale = cc.kscale;
+  grad::WalkArgs bw = w;
+  bw.a = q; bw.b = d_out; bw.s0 = d_state_out; bw.s_in = state_in;
+  bw.ascale = 1.f;
+  if (p.fast) {
+    float* qb = reinterpret_cast<float*>(ws + p.off_qb);
+    float* kf = reinterpret_cast<float*>(ws + p.off_kf);
+    const size_t rows = static_cast<size_t>(B) * H * L;
+    const size_t n = rows * (d_k / 8);
+    {
+      Mark m("param_prep", stream);
+      if (in_dt == RET_F32)
+        grad::walk_prep_kernel<float><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+            static_cast<const float*>(q), static_cast<const float*>(k), qb, kf, cs, cc, H, L, d_k, rows);
+      else
+        grad::walk_prep_kernel<__nv_bfloat16><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qb, kf, cs, cc, H, L,
+            d_k, rows);
+    }
+    auto walk = [&](auto kern, const grad::WalkArgs& wa, const float* aop, int smem, const char* name) {
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      Mark m(name, stream);
+      kern<<<static_cast<unsigned>(nwalk), 64, smem, stream>>>(wa, aop);
+    };
+    if (in_dt == RET_F32) {
+      walk(grad::state_walk2_kernel<float, true>, fw, kf, grad::Walk2Smem<float>::BYTES, "param_walk_fwd");
+      walk(grad::state_walk2_kernel<float, false>, bw, qb, grad::Walk2Smem<float>::BYTES, "param_walk_bwd");
+    } else {
+      walk(grad::state_walk2_kernel<__nv_bfloat16, true>, fw, kf, grad::Walk2Smem<__nv_bfloat16>::BYTES,
+           "param_walk_fwd");
+      walk(grad::state_walk2_kernel<__nv_bfloat16, false>, bw, qb, grad::Walk2Smem<__nv_bfloat16>::BYTES,
+           "param_walk_bwd");
+    }
+    if ((s = last_launch()) != RET_OK) return s;
+  } else {
+    {
+      Mark m("param_walk_fwd", stream);
+      if (in_dt == RET_F32) grad::state_walk_fwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(fw);
+      else grad::state_walk_fwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(fw);
+    }
+    if ((s = last_launch()) != RET_OK) return s;
+    {
+      Mark m("param_walk_bwd", stream);
+      if (in_dt == RET_F32) grad::state_walk_bwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
+      else grad::state_walk_bwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
+    }
+    if ((s = last_launch()) != RET_OK) return s;
   }
-  if ((s = last_launch()) != RET_OK) return s;
-  {
-    grad::WalkArgs bw = w;
-    bw.a = q; bw.b = d_out; bw.s0 = d_state_out; bw.s_in = state_in;
-    bw.ascale = 1.f;
-    Mark m("param_walk_bwd", stream);
-    if (in_dt == RET_F32) grad::state_walk_bwd_kernel<float><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
-    else grad::state_walk_bwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(nwalk), 256, 0, stream>>>(bw);
-  }
-  if ((s = last_launch()) != RET_OK) return s;
   // (3) fixed-order finishing sums
   grad::FinishArgs f{};
   f.gpart = a.gpart; f.gwalk = w.gpart; f.tpart = a.tpart; f.zpart = w.zpart;
