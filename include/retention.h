@@ -235,8 +235,8 @@ ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, i
  * state_in, d_state_out: DEVICE fp32 [B, H, d_k, d_v] or NULL (zero).
  * d_state_in: DEVICE fp32 or NULL (not computed); it may alias state_in or
  * d_state_out.  workspace: DEVICE, at least ret_chunkwise_backward_plan's
- * bytes (never 0).  B·H·ceil(L/chunk) > 65535, L > 524280 or a γ_h below
- * 2^-64 (the reversed evaluations start from dS_out/γ) is RET_EUNSUPPORTED.  Validation and errors as for the other entry points.
+ * bytes (never 0).  B·H > 65535 or a γ_h below 2^-64 (the reversed
+ * evaluations start from dS_out/γ) is RET_EUNSUPPORTED.  Validation and errors as for the other entry points.
  * ------------------------------------------------------------------------ */
 ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, const void* d_out,
                                   ret_dtype in_dt, const float* gamma, const float* theta,

@@ -102,6 +102,10 @@ struct ChunkArgs {
   // head = sequence % H.  raw_ds: state_out receives the chunk's ΔS itself
   // instead of fmaf(γ^b, S, ΔS).
   int seq_div = 1, raw_ds = 0;
+  // Grids with more rows than gridDim.y allows fold them over grid.z: row =
+  // blockIdx.y + gridDim.y·blockIdx.z, and the CTAs past grid_rows exit at
+  // once.  0: one row per blockIdx.y (gridDim.z = 1).
+  int grid_rows = 0;
   // Ring mode of the pair kernel (ring > 0, carried layout only): grid rows
   // [0, ring_prod_rows) are producer CTAs that rotate raw q, k (read through
   // their own tensor maps) into `ring` chunk slots per head — ring_q / ring_k
@@ -283,7 +287,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int bh = blockIdx.y;
+  const int bh = static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z);
+  if (args.grid_rows && bh >= args.grid_rows) return;   // past the rows of a folded grid
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
   const int h = seq % args.H;
   const int d_v = args.d_v, nch = args.nchunks;

@@ -263,8 +263,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int bh = RING ? args.ring_bh0 + static_cast<int>(blockIdx.y) - args.ring_prod_rows
-                     : static_cast<int>(blockIdx.y);
+  const int grow = static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z);
+  if (!RING && args.grid_rows && grow >= args.grid_rows) return;   // both CTAs of the pair
+  const int bh = RING ? args.ring_bh0 + grow - args.ring_prod_rows : grow;
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
   // Row of chunk c of this sequence in the rotated Q′ / K̂′ source: the
   // padded workspace, or slot c mod R of the ring.

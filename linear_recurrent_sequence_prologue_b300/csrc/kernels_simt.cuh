@@ -29,7 +29,8 @@ __global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
                                                      int BH, int H, int L, int d, float pos0,
                                                      float scale, RowPos rp, int flip) {
   const int i = blockIdx.x * 32 + threadIdx.x;   // pair
-  const int t = blockIdx.y * 8 + threadIdx.y;    // row
+  // row (groups of 8 rows folded over grid.y and grid.z)
+  const int t = static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z) * 8 + threadIdx.y;
   if (i >= d / 2 || t >= L) return;
   float c = 0.f, s = 0.f;
   int cur = -1;
@@ -53,7 +54,9 @@ __global__ void __launch_bounds__(256) rotate_kernel(const Tin* __restrict__ x,
 // ---------------------------------------------------------------------------
 // ΔS_i[k][v] = Σ_j (γ^{r−1−j} k′_j[k]) v_j[v], accumulated in j order from 0.
 // Block 16×16 threads, 64 k × 64 v tile, 4×4 outputs per thread.
-// grid = (ceil(d_v/64), ceil(d_k/64), BH·nchunks); kp = rotated K′ (fp32).
+// grid = (ceil(d_v/64)·F, ceil(d_k/64), ⌈BH·nchunks / F⌉): the (b, h, chunk)
+// rows are folded over grid.z and F slices of grid.x (row = blockIdx.z +
+// gridDim.z·(blockIdx.x / ceil(d_v/64))); kp = rotated K′ (fp32).
 // out: ws[bh][chunk][k][v].
 // ---------------------------------------------------------------------------
 template <typename Tin>
@@ -61,13 +64,16 @@ __global__ void __launch_bounds__(256) chunk_dS_kernel(const float* __restrict__
                                                        const Tin* __restrict__ v,
                                                        float* __restrict__ ws, CallConsts cc,
                                                        int H, int L, int d_k, int d_v, int chunk,
-                                                       int nchunks) {
+                                                       int nchunks, int rows) {
   __shared__ float sk[16][64];
   __shared__ float sv[16][64];
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int tid = ty * 16 + tx;
-  const int v0 = blockIdx.x * 64, k0 = blockIdx.y * 64;
-  const int bh = blockIdx.z / nchunks, ci = blockIdx.z % nchunks;
+  const int ntx = (d_v + 63) / 64;
+  const int row = static_cast<int>(blockIdx.z + gridDim.z * (blockIdx.x / ntx));
+  if (row >= rows) return;
+  const int v0 = static_cast<int>(blockIdx.x % ntx) * 64, k0 = blockIdx.y * 64;
+  const int bh = row / nchunks, ci = row % nchunks;
   const int h = bh % H;
   const int start = ci * chunk;
   const int r = min(chunk, L - start);
@@ -172,13 +178,16 @@ __global__ void __launch_bounds__(256) chunk_out_kernel(
     const float* __restrict__ qp, const float* __restrict__ kp, const Tin* __restrict__ v,
     const float* __restrict__ ws_states, const float* __restrict__ state_in,
     Tout* __restrict__ out, float* __restrict__ out_f32, CallConsts cc, int H, int L, int d_k,
-    int d_v, int chunk, int nchunks) {
+    int d_v, int chunk, int nchunks, int rows) {
   extern __shared__ float smem[];
   float* sq = smem;                 // [16][d_k]
   float* sp = smem + 16 * d_k;      // [16][64] scores
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  const int v0 = blockIdx.x * 64;
-  const int bh = blockIdx.z / nchunks, ci = blockIdx.z % nchunks;
+  const int ntx = (d_v + 63) / 64;   // rows folded as in chunk_dS_kernel
+  const int row = static_cast<int>(blockIdx.z + gridDim.z * (blockIdx.x / ntx));
+  if (row >= rows) return;
+  const int v0 = static_cast<int>(blockIdx.x % ntx) * 64;
+  const int bh = row / nchunks, ci = row % nchunks;
   const int h = bh % H;
   const int start = ci * chunk;
   const int r = min(chunk, L - start);

@@ -217,6 +217,33 @@ bool tc_pair_ok(int d_k, int d_v) {
 // (one chunk per row) must fit gridDim.y.
 constexpr size_t kMaxGridRows = 65535;
 
+// Grids whose row count may exceed gridDim.y / gridDim.z (65535).  fold_z:
+// the SIMT chunk kernels, rows over grid.z and F slices of grid.x.
+// fold_rows: the tensor-core chunk kernels, rows over grid.y and grid.z
+// (ChunkArgs::grid_rows set when folded).
+dim3 fold_z(unsigned x, unsigned y, size_t rows) {
+  const size_t gz = std::min<size_t>(rows, kMaxGridRows);
+  const size_t f = (rows + gz - 1) / gz;
+  return dim3(static_cast<unsigned>(x * f), y, static_cast<unsigned>(gz));
+}
+
+// rotate_kernel: groups of 8 rows over grid.y and grid.z (it drops rows ≥ L).
+dim3 fold_y(unsigned x, size_t rows) {
+  const size_t gz = (rows + kMaxGridRows - 1) / kMaxGridRows;
+  return dim3(x, static_cast<unsigned>((rows + gz - 1) / gz), static_cast<unsigned>(gz));
+}
+
+dim3 fold_rows(unsigned x, size_t rows, int* grid_rows) {
+  if (rows <= kMaxGridRows) {
+    *grid_rows = 0;
+    return dim3(x, static_cast<unsigned>(rows));
+  }
+  const size_t gz = (rows + kMaxGridRows - 1) / kMaxGridRows;
+  const size_t gy = (rows + gz - 1) / gz;
+  *grid_rows = static_cast<int>(rows);
+  return dim3(x, static_cast<unsigned>(gy), static_cast<unsigned>(gz));
+}
+
 struct Plan {
   int path = 0;
   size_t bytes = 0;
@@ -238,8 +265,7 @@ struct Plan {
 // launches have one CTA per chunk, finishes sooner.  Both give the same bits.
 constexpr size_t kCarryMinCtas = 74;
 bool prefer_scan(size_t BH, int d_v, int nch) {
-  return g_force_path == 0 && BH * tc_tiles(d_v) < kCarryMinCtas && nch >= 4 &&
-         BH * nch <= kMaxGridRows;
+  return g_force_path == 0 && BH * tc_tiles(d_v) < kCarryMinCtas && nch >= 4;
 }
 
 // Compact-workspace mode of the carried layout on CTA pairs: the Θ prologue
@@ -265,7 +291,7 @@ Plan plan_chunkwise(ret_dtype in_dt, const float* gamma, int B, int H, int L, in
   const bool tc = tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, chunk);
   const int nch = (L + (tc ? tcc::CH : chunk) - 1) / (tc ? tcc::CH : chunk);
   size_t off = 0;
-  if (tc && ((compact && !scan && ring_mode_ok(d_k, d_v)) || (scan ? BH * nch : BH) <= kMaxGridRows)) {
+  if (tc) {
     p.path = RET_PATH_TC;
     if (compact && !scan && ring_mode_ok(d_k, d_v)) {
       // producer ring: kRing chunk slots of Q″ and K̂′ per head of one launch,
@@ -303,9 +329,7 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
   const size_t BH = static_cast<size_t>(B) * H;
   size_t off = 0;
   if (tc_chunk_ok(in_dt, gamma, H, L, d_k, d_v, tcc::CH) && d_v % tcc::VT == 0 && L % tcc::CH == 0 &&
-      BH <= kMaxGridRows &&
-      static_cast<size_t>(L / tcc::CH) <= kMaxGridRows &&
-      (!want_state || BH * (L / tcc::CH) <= kMaxGridRows)) {
+      BH <= kMaxGridRows && static_cast<size_t>(L / tcc::CH) <= kMaxGridRows) {   // parallel_tc grid (·, BH, blocks)
     // rotated Q′ / K̂′ in bf16; per-block ΔS states when state_out is wanted
     p.path = RET_PATH_TC;
     p.off_q = off; off += up256(BH * L * d_k * 2);
@@ -372,7 +396,7 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
   float* qp = wsp<float>(ws, p.off_q);
   float* kp = wsp<float>(ws, p.off_k);
   {
-    dim3 grid((d_k / 2 + 31) / 32, (L + 7) / 8);
+    const dim3 grid = fold_y((d_k / 2 + 31) / 32, (static_cast<size_t>(L) + 7) / 8);
     {
       Mark m("rotate_q_f32", st);
       simt::rotate_kernel<Tin, float><<<grid, dim3(32, 8), 0, st>>>(q, qp, cc, BH, H, L, d_k,
@@ -386,11 +410,11 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
   }
   float* states = need_states ? wsp<float>(ws, p.off_states) : nullptr;
   if (states) {
-    dim3 g1((d_v + 63) / 64, (d_k + 63) / 64, BH * nch);
+    const dim3 g1 = fold_z((d_v + 63) / 64, (d_k + 63) / 64, static_cast<size_t>(BH) * nch);
     {
       Mark m("chunk_dS_f32", st);
       simt::chunk_dS_kernel<Tin><<<g1, dim3(16, 16), 0, st>>>(kp, v, states, cc, H, L, d_k, d_v,
-                                                              chunk, nch);
+                                                              chunk, nch, BH * nch);
     }
     const size_t n = static_cast<size_t>(BH) * d_k * d_v;
     Mark m("state_scan", st);
@@ -398,13 +422,13 @@ ret_status run_simt_chunked(const Tin* q, const Tin* k, const Tin* v, const Call
         states, s_in, s_out, cc, H, d_k, d_v, nch, BH);
   }
   {
-    dim3 g2((d_v + 63) / 64, (chunk + 15) / 16, BH * nch);
+    const dim3 g2 = fold_z((d_v + 63) / 64, (chunk + 15) / 16, static_cast<size_t>(BH) * nch);
     const size_t smem = (16 * static_cast<size_t>(d_k) + 16 * 64) * sizeof(float);
     // ws_states == nullptr means "use state_in for the single chunk" (parallel form)
     const float* wst = (nch > 1 || states) ? states : nullptr;
     Mark m("chunk_out_f32", st);
     simt::chunk_out_kernel<Tin, Tout><<<g2, 256, smem, st>>>(qp, kp, v, wst, s_in, out, nullptr, cc,
-                                                             H, L, d_k, d_v, chunk, nch);
+                                                             H, L, d_k, d_v, chunk, nch, BH * nch);
   }
   if (gn_on(gn))   // in place over out
     launch_groupnorm<Tout, Tout>(out, out, gn, H, L, d_v, static_cast<size_t>(BH) * L, st);
@@ -632,23 +656,26 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
   a.tail_out = (L % tcc::CH != 0 && a.out) ? wsp<void>(ws, p.off_tail) : nullptr;
   a.seq_div = 1;
   a.raw_ds = 0;
-  auto launch = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args, int rows,
+  auto launch = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args0, int rows,
                     const char* name) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    tcc::ChunkArgs args = args0;
+    const dim3 grid = fold_rows(tc_tiles(d_v), static_cast<size_t>(rows), &args.grid_rows);
     Mark m(name, st);
-    kern<<<dim3(tc_tiles(d_v), rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
+    kern<<<grid, tcc::NTHREADS, smem, st>>>(mq, mk, mv, args, cc);
     return cudaGetLastError();
   };
   // Pair kernel: clusters of two CTAs along the d_v tiles.
-  auto launch_pair = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args, int rows,
+  auto launch_pair = [&](auto kern, uint32_t smem, const tcc::ChunkArgs& args0, int rows,
                          const char* name) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    tcc::ChunkArgs args = args0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(d_v / tcc::VT, rows);
+    cfg.gridDim = fold_rows(d_v / tcc::VT, static_cast<size_t>(rows), &args.grid_rows);
     cfg.blockDim = dim3(tcc::NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -823,18 +850,18 @@ ret_status run_simt_core(const float* qp, const float* kp, const float* v, const
   const int nch = (L + chunk - 1) / chunk;
   const bool need = nch > 1 || s_out;
   if (need) {
-    dim3 g1((dv + 63) / 64, (dk + 63) / 64, BH * nch);
+    const dim3 g1 = fold_z((dv + 63) / 64, (dk + 63) / 64, static_cast<size_t>(BH) * nch);
     {
       Mark m("bwd_chunk_dS", st);
       simt::chunk_dS_kernel<float><<<g1, dim3(16, 16), 0, st>>>(kp, v, states, cc, H, L, dk, dv,
-                                                                chunk, nch);
+                                                                chunk, nch, BH * nch);
     }
     const size_t n = static_cast<size_t>(BH) * dk * dv;
     Mark m("bwd_state_scan", st);
     simt::state_scan_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
         states, s_in, s_out, cc, H, dk, dv, nch, BH);
   }
-  dim3 g2((dv + 63) / 64, (chunk + 15) / 16, BH * nch);
+  const dim3 g2 = fold_z((dv + 63) / 64, (chunk + 15) / 16, static_cast<size_t>(BH) * nch);
   const size_t smem = (16 * static_cast<size_t>(dk) + 16 * 64) * sizeof(float);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(simt::chunk_out_kernel<float, float>,
@@ -844,7 +871,7 @@ ret_status run_simt_core(const float* qp, const float* kp, const float* v, const
   Mark m("bwd_chunk_out", st);
   simt::chunk_out_kernel<float, float><<<g2, 256, smem, st>>>(qp, kp, v, need ? states : nullptr,
                                                               s_in, out, nullptr, cc, H, L, dk,
-                                                              dv, chunk, nch);
+                                                              dv, chunk, nch, BH * nch);
   return last_launch();
 }
 
@@ -877,7 +904,7 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
   float* sprep = wsp<float>(ws, p.off_sprep);
   const RowPos rp = no_rowpos();
   const float p0 = static_cast<float>(pos0);
-  const dim3 rg((d_k / 2 + 31) / 32, (L + 7) / 8);
+  const dim3 rg = fold_y((d_k / 2 + 31) / 32, (static_cast<size_t>(L) + 7) / 8);
   const size_t nk = static_cast<size_t>(BH) * L * d_k, nv = static_cast<size_t>(BH) * L * d_v;
   const dim3 sgrid((d_v + 31) / 32, (d_k + 31) / 32, BH);   // state_prep_kernel tiles
   {
@@ -1003,7 +1030,6 @@ bool tc_backward_ok(ret_dtype in_dt, const float* gamma, int H, int d_k, int d_v
                     int B) {
   if (g_force_path == RET_PATH_SIMT || in_dt != RET_BF16 || chunk != tcc::CH) return false;
   if (!(d_k == 128 || d_k == 256) || d_v % tcc::VT != 0) return false;
-  if (static_cast<size_t>(B) * H * bwd_pieces(d_v) > kMaxGridRows) return false;
   return tc_gamma_ok(gamma, H, chunk);
 }
 
@@ -1079,7 +1105,7 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(dvF / tcc::VT, rows);
+    cfg.gridDim = fold_rows(dvF / tcc::VT, static_cast<size_t>(rows), &g.grid_rows);
     cfg.blockDim = dim3(tcc::NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1098,8 +1124,9 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    const dim3 grid = fold_rows(tc_tiles(dvF), static_cast<size_t>(rows), &g.grid_rows);
     Mark m("bwd_chunk_tc", st);
-    kern<<<dim3(tc_tiles(dvF), rows), tcc::NTHREADS, smem, st>>>(mq, mk, mv, g, cc);
+    kern<<<grid, tcc::NTHREADS, smem, st>>>(mq, mk, mv, g, cc);
     return cudaGetLastError();
   };
   cudaError_t e;
@@ -1559,7 +1586,7 @@ ret_status ret_chunkwise_backward(const void* q, const void* k, const void* v, c
   if (d_state_out && !al16(d_state_out)) return RET_EINVAL;
   if (chunk < 1) return RET_EINVAL;
   const int64_t nch = (static_cast<int64_t>(L) + chunk - 1) / chunk;
-  if (static_cast<int64_t>(B) * H * nch > 65535 || (L + 7) / 8 > 65535) return RET_EUNSUPPORTED;
+  if (static_cast<int64_t>(B) * H > 65535) return RET_EUNSUPPORTED;   // state tiles: one grid.z row per head
   CallConsts cc;
   if ((s = make_consts(cc, gamma, theta, H, d_k, chunk, L)) != RET_OK) return s;
   for (int h = 0; h < H; ++h)   // the reversed evaluations start from dS_out/γ
@@ -1718,7 +1745,7 @@ ret_status ret_rotate(const void* x, ret_dtype in_dt, const float* theta, int B,
     cc.theta[i] = theta[i];
   }
   const int BH = B * H;
-  dim3 grid((d / 2 + 31) / 32, (L + 7) / 8);
+  const dim3 grid = fold_y((d / 2 + 31) / 32, (static_cast<size_t>(L) + 7) / 8);
   const float p0 = static_cast<float>(pos0);
   if (in_dt == RET_BF16 && out_dt == RET_BF16)
     simt::rotate_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, dim3(32, 8), 0, stream>>>(

@@ -281,7 +281,10 @@ def test_backward_plan_and_validation(lib):
     assert call(gamma=np.array([0.9, 1.5], np.float32)) == _lib.RET_EINVAL
     assert call(gamma=np.array([0.9, 2.0 ** -70], np.float32)) == _lib.RET_EUNSUPPORTED
     gh = np.full(128, 0.9, np.float32)
-    assert call(gamma=gh, H=128, L=65536, chunk=64) == _lib.RET_EUNSUPPORTED   # grid rows
+    # 128 heads × 1024 chunks of 64: more (b, h, chunk) rows than one grid
+    # dimension holds, folded over two, so only the workspace is missing
+    assert call(gamma=gh, H=128, L=65536, chunk=64) == _lib.RET_EWORKSPACE
+    assert call(gamma=gh, B=512, H=128, L=1) == _lib.RET_EUNSUPPORTED        # B·H > 65535
     assert call() == _lib.RET_EWORKSPACE                             # valid: no workspace
     assert call(ws=P, wsn=16) == _lib.RET_EWORKSPACE                 # too small
 

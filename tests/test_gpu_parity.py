@@ -15,7 +15,7 @@ from linear_recurrent_sequence_prologue_b300.inputs import (WORKLOADS, Workload,
                                                             make_inputs, theta_schedule, to_f64)
 from oracle import retention_ref as O
 
-from helpers import BF16_TOL, assert_close, gpu_np, head_slice, max_rel_inf, rel_fro
+from helpers import BF16_TOL, FP32_TOL, assert_close, gpu_np, head_slice, max_rel_inf, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -701,3 +701,49 @@ def test_bounded_wait_timeout_reports_and_recovers():
     o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=16)
     ref_o, _ = _oracle_full(inp, w, "chunkwise", 16)
     assert_close(gpu_np(o), ref_o, torch.float32, "after timeout")
+
+
+# ----------------------------------------------------- grids past 65535 rows --
+def test_folded_grids_match_unfolded_launches():
+    """Launches with more rows than one grid dimension holds fold them over
+    two: the fp32 chunk kernels (B·H·⌈L/chunk⌉ > 65535, forward and
+    gradient pass), the Θ rotation (more than 65535 groups of 8 rows) and
+    the tensor-core chunk-parallel layout (B·H·⌈L/128⌉ > 65535 CTA rows).
+    Each against the same problem in launches that fit one dimension: the
+    chunkwise result does not depend on the chunk length (fp32: to rounding),
+    and the chunk-parallel layout equals the carried one bit for bit."""
+    g = torch.Generator().manual_seed(41)
+    # fp32 path: 2 heads × 40000 chunks of 1 token
+    q, k, v = (torch.randn(1, 2, 40000, 8, generator=g) for _ in range(3))
+    s0 = torch.randn(1, 2, 8, 8, generator=g) * 0.1
+    gam, th = np.array([0.9, 0.99], np.float32), theta_schedule(8)
+    qc, kc, vc, sc = q.cuda(), k.cuda(), v.cuda(), s0.cuda()
+    o1, s1 = R.chunkwise(qc, kc, vc, gam, th, chunk=1, pos0=5, state_in=sc)
+    o2, s2 = R.chunkwise(qc, kc, vc, gam, th, chunk=64, pos0=5, state_in=sc)
+    d_o = torch.randn(1, 2, 40000, 8, generator=g).cuda()
+    b1 = R.chunkwise_backward(qc, kc, vc, d_o, gam, th, chunk=1, pos0=5, state_in=sc)
+    b2 = R.chunkwise_backward(qc, kc, vc, d_o, gam, th, chunk=64, pos0=5, state_in=sc)
+    assert R.sync_status() == R.RET_OK
+    assert max_rel_inf(gpu_np(o1), gpu_np(o2)) < FP32_TOL and max_rel_inf(gpu_np(s1), gpu_np(s2)) < FP32_TOL
+    for x, y in zip(b1, b2):
+        assert max_rel_inf(gpu_np(x), gpu_np(y)) < FP32_TOL
+    # rotation: 600000 rows (75000 groups of 8)
+    x = torch.randn(1, 1, 600000, 8, generator=g).cuda()
+    y = R.rotate(x, th, pos0=3)
+    assert R.sync_status() == R.RET_OK
+    tail = x[0, 0, -4:].double().cpu().numpy()
+    sin, cos = O.rotation_tables(np.arange(600000 - 4, 600000) + 3, th.astype(np.float64))
+    assert np.max(np.abs(gpu_np(y[0, 0, -4:]) - O.theta_shift(tail, sin, cos))) < 1e-4
+    # tensor cores, chunk-parallel layout: 64 heads × 1100 chunks = 70400 rows
+    w = Workload("fold", 1, 64, 1100 * 128, 64, 64, "bf16", 128, 1.0 / 8, state_std=0.1)
+    inp = make_inputs(w, seed=3)
+    d = _cuda(inp)
+    args = (d["q"], d["k"], d["v"], inp["gamma"], inp["theta"])
+    R.force_path(R.RET_PATH_TC_CARRY)   # 64 one-tile heads would otherwise pick the chunk-parallel layout
+    try:
+        oc, sc_ = R.chunkwise(*args, chunk=128, state_in=d["state_in"])
+    finally:
+        R.force_path(0)
+    os_, ss = R.chunkwise(*args, chunk=128, state_in=d["state_in"], layout="scan")
+    assert R.sync_status() == R.RET_OK
+    assert torch.equal(oc, os_) and torch.equal(sc_, ss)
