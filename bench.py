@@ -40,7 +40,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=12)
     ap.add_argument("--backward-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b"],
+    ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b", "gn1p3b", "gnbwd1p3b",
+                             "pgrad_medium"],
                     help="run one case (two warm-up calls, then one call) for an ncu capture and exit")
     return ap.parse_args()
 
@@ -50,7 +51,10 @@ def run_profile_case(case):
     JSON line).  chunk7b: ret_chunkwise on the 7B-shape workload; chunk_medium:
     the same shape at L = 2048 (134 MB of inputs, above the 126 MB L2);
     gemm: ret_matmul 8192 x 8192 x 4096; rownorm7b: ret_decay_row_norm on a
-    7B-shape bf16 output; block7b: ret_msr_block at the 7B shape."""
+    7B-shape bf16 output; block7b: ret_msr_block at the 7B shape; gn1p3b:
+    ret_chunkwise with GroupNorm at the 1.3B shape; gnbwd1p3b:
+    ret_groupnorm_backward at the 1.3B shape; pgrad_medium:
+    ret_chunkwise_param_grads on B1 H4 L4096 d_k256 d_v512."""
     import torch
     import linear_recurrent_sequence_prologue_b300 as R
     from linear_recurrent_sequence_prologue_b300 import build
@@ -74,6 +78,29 @@ def run_profile_case(case):
     elif case == "rownorm7b":
         o = rn((w.B, w.H, w.L, w.d_v), 1.0)
         fn = lambda: R.decay_row_norm(o, inp["gamma"])
+    elif case == "gn1p3b":
+        w3 = WORKLOADS["msr1p3b"]
+        i3 = make_inputs(w3, seed=0)
+        q, k, v = (i3[n].to(dev) for n in ("q", "k", "v"))
+        fn = lambda: R.chunkwise(q, k, v, i3["gamma"], i3["theta"], chunk=w3.chunk, gn={"eps": 1e-5},
+                                 return_state=False)
+    elif case == "gnbwd1p3b":
+        w3 = WORKLOADS["msr1p3b"]
+        x, dy = rn((w3.B, w3.H, w3.L, w3.d_v), 1.0), rn((w3.B, w3.H, w3.L, w3.d_v), 1.0)
+        gw = torch.randn((w3.H, w3.d_v), generator=gen, device=dev)
+        fn = lambda: R.groupnorm_backward(x, dy, 1e-5, gw)
+    elif case == "pgrad_medium":
+        from linear_recurrent_sequence_prologue_b300.inputs import make_grad_inputs
+        wm = w.with_(B=1, H=4, L=4096)
+        im = make_inputs(wm, seed=0)
+        gi = make_grad_inputs(wm, seed=5, d_state_std=1.0)
+        q, k, v, s_in = (im[n].to(dev) for n in ("q", "k", "v", "state_in"))
+        d_o, dso = gi["d_out"].to(dev), gi["d_state_out"].to(dev)
+        out, _ = R.chunkwise(q, k, v, im["gamma"], im["theta"], chunk=128, state_in=s_in)
+        grads = R.chunkwise_backward(q, k, v, d_o, im["gamma"], im["theta"], chunk=128, state_in=s_in,
+                                     d_state_out=dso)
+        fn = lambda: R.param_grads(q, k, v, d_o, out, *grads[:3], im["gamma"], im["theta"], state_in=s_in,
+                                   d_state_out=dso)
     else:
         D = w.H * w.d_k
         x = rn((w.B, w.L, D), 1.0)
