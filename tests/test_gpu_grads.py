@@ -63,6 +63,7 @@ def _run_grads(w, pos0, chunk, out_dtype, grad_dtype, states, seed):
     ("f32", 2, 2, 129, 16, 16, 64, 0, False, torch.float32),    # no state terms
     ("bf16", 1, 2, 384, 256, 256, 128, 5, True, torch.float32),     # tensor-core pair kernels
     ("bf16", 2, 2, 300, 128, 256, 128, 0, False, torch.bfloat16),   # bf16 out, ragged, one-CTA kernel
+    ("bf16", 1, 2, 200, 48, 96, 32, 4, True, torch.float32),        # fp32 kernels, partial walk tiles
 ])
 def test_param_grads_vs_oracle(dtype, B, H, L, d_k, d_v, chunk, pos0, states, out_dtype):
     w = Workload("custom", B, H, L, d_k, d_v, dtype, chunk, 1.0, state_std=0.1 if states else 0.0)

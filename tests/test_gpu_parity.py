@@ -114,6 +114,34 @@ def test_groupnorm_fp32_with_affine():
     assert_close(gpu_np(o), ref_o, torch.float32, "gn")
 
 
+@pytest.mark.parametrize("B,H,L,d_k,d_v,dtype,chunk,layout,out_f32,affine,pos0", [
+    (1, 2, 300, 256, 256, "bf16", 128, "carry", False, True, 3),    # CTA pairs, short last chunk
+    (2, 2, 300, 128, 128, "bf16", 128, "carry", True, False, 0),    # one-CTA kernel, fp32 out
+    (1, 2, 1024, 256, 256, "bf16", 128, "scan", False, True, 5),    # chunk-parallel layout
+    (3, 2, 200, 64, 64, "bf16", 64, "carry", False, True, [0, 37, 900]),   # per-row positions
+    (1, 2, 130, 32, 20, "f32", 32, "carry", True, True, 0),         # fp32 path, 20-wide rows
+])
+def test_groupnorm_in_place_on_every_path(B, H, L, d_k, d_v, dtype, chunk, layout, out_f32, affine, pos0):
+    """GroupNorm runs in place over the output after everything that writes
+    it (the short-last-chunk copy included) on every path and layout."""
+    w, inp = _custom(B, H, L, d_k, d_v, dtype, chunk, std=1.0, state_std=0.1, seed=L + d_v)
+    g = torch.Generator().manual_seed(L)
+    gw, gb = (torch.randn(H, d_v, generator=g) if affine else None for _ in range(2))
+    d = _cuda(inp)
+    gn = {"eps": 1e-5, "weight": gw.cuda() if affine else None, "bias": gb.cuda() if affine else None}
+    o, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=chunk, pos0=pos0,
+                       state_in=d["state_in"], gn=gn, layout=layout,
+                       out_dtype=torch.float32 if out_f32 else None)
+    assert R.sync_status() == R.RET_OK
+    gref = {"eps": 1e-5, "weight": gw.numpy() if affine else None, "bias": gb.numpy() if affine else None}
+    rows = pos0 if isinstance(pos0, list) else [pos0] * B
+    tol = torch.float32 if dtype == "f32" else torch.bfloat16
+    for b, p0 in enumerate(rows):
+        one = {k: (v[b:b + 1] if torch.is_tensor(v) else v) for k, v in inp.items()}
+        ref_o, _ = _oracle_full(one, w, "chunkwise", chunk, pos0=p0, gn=gref)
+        assert_close(gpu_np(o[b:b + 1]), ref_o, tol, f"row {b}")
+
+
 # ------------------------------------------------------- bf16, small shapes --
 def test_small_workload_all_heads():
     w = WORKLOADS["small"]
