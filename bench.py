@@ -1031,9 +1031,61 @@ def main():
     ems = max_over_ranks(es.elapsed_time(ee) / args.e2e_steps, world, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hs,) if hs is not None else ()))
     d2h = hout.numel() * hout.element_size() + hsout.numel() * hsout.element_size()
+    # The host link alone: the same bytes as plain pinned copies, each direction
+    # timed by itself on its copy stream (4 repetitions after one warm-up).
+    def link_ms(fn, st):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(4):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 4
+
+    def copy_in():
+        with torch.cuda.stream(s_in_):
+            for name, host in (("q", hq), ("k", hk), ("v", hv), ("s", hs)):
+                if host is not None:
+                    bufs[0][name].copy_(host, non_blocking=True)
+
+    def copy_out():
+        with torch.cuda.stream(s_out_):
+            hout.copy_(bufs[0]["o"], non_blocking=True)
+            hsout.copy_(bufs[0]["so"], non_blocking=True)
+
+    def both():   # the two directions at once, as the pipelined steps run them
+        copy_in()
+        copy_out()
+
+    def link_both_ms():
+        both()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b_in, b_out = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s_in_)
+        s_out_.wait_event(a)
+        for _ in range(4):
+            both()
+        b_in.record(s_in_)
+        b_out.record(s_out_)
+        torch.cuda.synchronize()
+        return max(a.elapsed_time(b_in), a.elapsed_time(b_out)) / 4
+
+    h2d_ms, d2h_ms = link_ms(copy_in, s_in_), link_ms(copy_out, s_out_)
+    both_ms = link_both_ms()
     e2e = {"value": replica_throughput(tok_per_step, ems / 1e3, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": args.e2e_steps,
-           "pipelined": "copy-in, compute and copy-out of consecutive steps overlap (two buffer sets)"}
+           "pipelined": "copy-in, compute and copy-out of consecutive steps overlap (two buffer sets)",
+           "link": {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9,
+                    "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9,
+                    "both_directions_ms": both_ms,
+                    "bound_ms": max(h2d_ms, d2h_ms, both_ms),
+                    "frac": max(h2d_ms, d2h_ms, both_ms) / ems,
+                    "note": "plain pinned copies of the same bytes: each direction alone, and both at "
+                            "once on their two copy streams; with the steps pipelined the copies of "
+                            "consecutive steps overlap, so the slowest of these bounds a step"}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
