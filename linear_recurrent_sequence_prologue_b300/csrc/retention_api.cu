@@ -260,12 +260,20 @@ struct Plan {
   bool scan = false;
 };
 
-// The carried layout runs B·H·tiles CTAs that each walk every chunk; below
-// half the SMs (and with several chunks) the chunk-parallel layout, whose
-// launches have one CTA per chunk, finishes sooner.  Both give the same bits.
+// The carried layout runs B·H·tiles CTAs that each walk every chunk, one
+// chunk time per chunk; the chunk-parallel layout runs two passes of one-chunk
+// CTAs (each CTA's life, set-up and pipeline fill included, about three chunk
+// times) plus the scan and two more launches (about eight chunk times).  So
+// with fewer CTAs than half the SMs, the chunk-parallel layout is chosen when
+// 6·⌈B·H·tiles·chunks / 148⌉ + 8 < chunks (measured on eight shapes from 4 to
+// 32 carried CTAs and 8 to 128 chunks: it picks the faster layout on all of
+// them, within 6% where the two are close).  Both give the same bits.
 constexpr size_t kCarryMinCtas = 74;
 bool prefer_scan(size_t BH, int d_v, int nch) {
-  return g_force_path == 0 && BH * tc_tiles(d_v) < kCarryMinCtas && nch >= 4;
+  const size_t ctas = BH * tc_tiles(d_v);
+  if (g_force_path != 0 || ctas >= kCarryMinCtas) return false;
+  const size_t waves = (ctas * nch + 147) / 148;
+  return 6 * waves + 8 < static_cast<size_t>(nch);
 }
 
 // Compact-workspace mode of the carried layout on CTA pairs: the Θ prologue

@@ -189,19 +189,20 @@ def test_path_selection(lib):
     # sequences of no more chunks than the ring holds: the front pass is smaller
     assert _plan_compact(lib, _lib.RET_BF16, 2, 16, 512, 256, 512, 128) == \
         _plan(lib, _lib.RET_BF16, 2, 16, 512, 256, 512, 128) == (_lib.RET_PATH_TC, 2 * 2 * 16 * 512 * 256 * 2)
-    # a grid too small for the carried layout (B·H·tiles < 74 CTAs, 4 chunks or
-    # more): the chunk-parallel layout, whose workspace adds the per-chunk states
-    assert _plan(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128) == \
-        (_lib.RET_PATH_TC, 2 * 2 * 2 * 512 * 256 * 2 + 2 * 2 * 4 * 256 * 512 * 4)
-    # the Small MSR workload (d_v = 64, one 128-wide tile of which 64 columns
-    # are live; chunk 64 runs on the 128-token tile): tensor cores, chunk-parallel
-    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64) == \
-        (_lib.RET_PATH_TC, 2 * 32 * 2048 * 64 * 2 + 32 * 16 * 64 * 64 * 4)
+    # few CTAs walking many chunks (4 carried CTAs, 32 chunks: 6·1 + 8 < 32): the
+    # chunk-parallel layout, whose workspace adds the per-chunk states
+    assert _plan(lib, _lib.RET_BF16, 1, 2, 4096, 256, 512, 128) == \
+        (_lib.RET_PATH_TC, 2 * 2 * 4096 * 256 * 2 + 2 * 32 * 256 * 512 * 4)
     assert lib.ret_force_path(_lib.RET_PATH_TC_CARRY) == _lib.RET_OK
     try:   # the carried layout kept: the rotated Q′ / K̂′ only
-        assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64) == (_lib.RET_PATH_TC, 2 * 32 * 2048 * 64 * 2)
+        assert _plan(lib, _lib.RET_BF16, 1, 2, 4096, 256, 512, 128) == (_lib.RET_PATH_TC, 2 * 2 * 4096 * 256 * 2)
     finally:
         assert lib.ret_force_path(0) == _lib.RET_OK
+    # …but not for few chunks (4 CTAs, 4 chunks) or many one-chunk CTAs: the Small
+    # MSR workload (d_v = 64, one 128-wide tile of which 64 columns are live;
+    # chunk 64 runs on the 128-token tile: 32 CTAs × 16 chunks, 6·4 + 8 ≥ 16)
+    assert _plan(lib, _lib.RET_BF16, 2, 2, 512, 256, 512, 128) == (_lib.RET_PATH_TC, 2 * 2 * 2 * 512 * 256 * 2)
+    assert _plan(lib, _lib.RET_BF16, 4, 8, 2048, 64, 64, 64) == (_lib.RET_PATH_TC, 2 * 32 * 2048 * 64 * 2)
     # no compact mode off the CTA-pair shapes: the same bytes as the plan
     assert _plan_compact(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128) == \
         _plan(lib, _lib.RET_BF16, 2, 2, 512, 64, 128, 128)

@@ -775,3 +775,34 @@ def test_folded_grids_match_unfolded_launches():
     os_, ss = R.chunkwise(*args, chunk=128, state_in=d["state_in"], layout="scan")
     assert R.sync_status() == R.RET_OK
     assert torch.equal(oc, os_) and torch.equal(sc_, ss)
+
+
+# ------------------------------------------------------------------ limits --
+@pytest.mark.parametrize("case", ["widest_fp32", "most_heads_tc", "last_positions_tc", "no_decay_tc"])
+def test_limits_vs_oracle(case):
+    """The boundary's largest legal values: d_k = 512 and d_v = 1024 (fp32
+    kernels), 128 heads (tensor cores), a sequence ending at position 2^24
+    (the rotation at its largest angles, tensor cores), and γ = 1 (no decay:
+    the state is a plain sum) next to the smallest tensor-core γ."""
+    if case == "widest_fp32":
+        w, inp = _custom(1, 1, 70, 512, 1024, "f32", 32, state_std=0.1, seed=5)
+        pos0 = 11
+    elif case == "most_heads_tc":
+        w, inp = _custom(1, 128, 256, 64, 64, "bf16", 128, std=0.125, state_std=0.1, seed=6)
+        pos0 = 0
+    elif case == "last_positions_tc":
+        w, inp = _custom(1, 2, 300, 128, 128, "bf16", 128, state_std=0.1, seed=7)
+        pos0 = (1 << 24) - 300
+    else:
+        w, inp = _custom(1, 2, 384, 128, 128, "bf16", 128, std=0.5, state_std=0.1, seed=8)
+        inp["gamma"] = np.array([1.0, 0.75], np.float32)   # 0.75^127 ≈ 1.4e-16 ≥ 2^-60
+        pos0 = 2
+    d = _cuda(inp)
+    path = R.plan("chunkwise", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk, gamma=inp["gamma"])[0]
+    assert path == (R.RET_PATH_SIMT if w.dtype == "f32" else R.RET_PATH_TC)
+    o, s = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=w.chunk, pos0=pos0,
+                       state_in=d["state_in"], out_dtype=torch.float32)
+    assert R.sync_status() == R.RET_OK
+    ref_o, ref_s = _oracle_full(inp, w, "chunkwise", w.chunk, pos0=pos0)
+    assert_close(gpu_np(o), ref_o, w.torch_dtype, f"{case} out")
+    assert_close(gpu_np(s), ref_s, w.torch_dtype, f"{case} state")

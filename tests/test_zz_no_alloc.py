@@ -90,7 +90,7 @@ def test_noalloc_sequence_of_shapes_after_nan_fill():
     GroupNorm staging on), then four different problems run back to back."""
     lib = R.load()
     big_tc = Workload("nan_tc", 2, 20, 384, 256, 256, "bf16", 128, 1.0, groupnorm=True)     # carried layout
-    big_scan = Workload("nan_scan", 1, 2, 1024, 256, 256, "bf16", 128, 1.0, groupnorm=True)  # chunk-parallel
+    big_scan = Workload("nan_scan", 1, 2, 4096, 256, 256, "bf16", 128, 1.0, groupnorm=True)  # chunk-parallel
     big_f32 = Workload("nan_f32", 1, 4, 4096, 64, 64, "f32", 64, 1.0, groupnorm=True)
     for w in (big_tc, big_scan, big_f32):
         need = R.plan("chunkwise", w.torch_dtype, w.B, w.H, w.L, w.d_k, w.d_v, w.chunk,
