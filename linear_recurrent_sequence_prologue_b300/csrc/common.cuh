@@ -75,17 +75,19 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // ---------------------------------------------------------------------------
 // Rotation angle of the Θ prologue: (cos, sin) of n·θ.
 // n < 2^24 is exact in fp32; the product n·θ is split exactly into
-// hi + lo (hi = fl(n·θ), lo = fma(n, θ, −hi)); CUDA's sincosf handles hi and
-// the first-order term corrects for lo (|lo| ≤ ulp(hi)/2, so the dropped
-// second-order term is below 2^-48·|hi|²).
+// hi + lo (hi = fl(n·θ), lo = fma(n, θ, −hi), |lo| ≤ ulp(hi)/2 ≤ 1 for
+// |hi| ≤ 2^24), and sin/cos of the sum follow from the angle-addition
+// formulas with CUDA's sincosf of each part.  (A first-order correction for
+// lo alone drops lo²/2, which reaches 0.5 near 2^24 rad.)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void angle_cs(float n, float theta, float& c, float& s) {
   const float hi = n * theta;
   const float lo = fmaf(n, theta, -hi);
-  float sh, ch;
+  float sh, ch, sl, cl;
   sincosf(hi, &sh, &ch);
-  s = fmaf(lo, ch, sh);
-  c = fmaf(-lo, sh, ch);
+  sincosf(lo, &sl, &cl);
+  s = fmaf(sh, cl, ch * sl);
+  c = fmaf(ch, cl, -(sh * sl));
 }
 
 // γ^e for a (possibly negative) integer e, from log2 γ: exp2(e·log2 γ).

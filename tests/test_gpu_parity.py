@@ -778,7 +778,8 @@ def test_folded_grids_match_unfolded_launches():
 
 
 # ------------------------------------------------------------------ limits --
-@pytest.mark.parametrize("case", ["widest_fp32", "most_heads_tc", "last_positions_tc", "no_decay_tc"])
+@pytest.mark.parametrize("case", ["widest_fp32", "most_heads_tc", "last_positions_tc", "last_positions_fp32",
+                                  "no_decay_tc"])
 def test_limits_vs_oracle(case):
     """The boundary's largest legal values: d_k = 512 and d_v = 1024 (fp32
     kernels), 128 heads (tensor cores), a sequence ending at position 2^24
@@ -793,6 +794,9 @@ def test_limits_vs_oracle(case):
     elif case == "last_positions_tc":
         w, inp = _custom(1, 2, 300, 128, 128, "bf16", 128, state_std=0.1, seed=7)
         pos0 = (1 << 24) - 300
+    elif case == "last_positions_fp32":
+        w, inp = _custom(1, 2, 200, 64, 32, "f32", 64, state_std=0.1, seed=9)
+        pos0 = (1 << 24) - 200
     else:
         w, inp = _custom(1, 2, 384, 128, 128, "bf16", 128, std=0.5, state_std=0.1, seed=8)
         inp["gamma"] = np.array([1.0, 0.75], np.float32)   # 0.75^127 ≈ 1.4e-16 ≥ 2^-60
