@@ -810,3 +810,59 @@ def test_limits_vs_oracle(case):
     ref_o, ref_s = _oracle_full(inp, w, "chunkwise", w.chunk, pos0=pos0)
     assert_close(gpu_np(o), ref_o, w.torch_dtype, f"{case} out")
     assert_close(gpu_np(s), ref_s, w.torch_dtype, f"{case} state")
+
+
+def test_largest_positions_on_the_other_paths():
+    """Sequences that end at position 2^24 (the largest rotation angles)
+    through the decode step, the gradient pass on both paths, the parameter
+    gradients and the MSR block, each against the oracle."""
+    top = 1 << 24
+    # decode: one token at position 2^24 − 1, fp32 inputs
+    w, inp = _custom(2, 2, 1, 32, 24, "f32", 1, state_std=0.1, seed=31)
+    d = _cuda(inp)
+    st = d["state_in"].clone()
+    o = R.step(d["q"][:, :, 0].contiguous(), d["k"][:, :, 0].contiguous(), d["v"][:, :, 0].contiguous(),
+               inp["gamma"], inp["theta"], top - 1, st)
+    ref_o, ref_s = O.decode_step(to_f64(inp["q"][:, :, 0]), to_f64(inp["k"][:, :, 0]), to_f64(inp["v"][:, :, 0]),
+                                 inp["gamma"].astype(np.float64), inp["theta"].astype(np.float64), top - 1,
+                                 to_f64(inp["state_in"]))
+    assert R.sync_status() == R.RET_OK
+    assert_close(gpu_np(o), ref_o, torch.float32, "decode out")
+    assert_close(gpu_np(st), ref_s, torch.float32, "decode state")
+    # gradient pass and parameter gradients: fp32 kernels and tensor cores
+    for dtype, L, d_k, d_v, chunk in (("f32", 70, 16, 16, 16), ("bf16", 256, 128, 128, 128)):
+        w, inp = _custom(1, 2, L, d_k, d_v, dtype, chunk, state_std=0.1, seed=L)
+        gi = make_grad_inputs(w, seed=L + 1, d_state_std=1.0)
+        d = _cuda(inp)
+        p0 = top - L
+        d_o, dso = gi["d_out"].cuda(), gi["d_state_out"].cuda()
+        got = R.chunkwise_backward(d["q"], d["k"], d["v"], d_o, inp["gamma"], inp["theta"], chunk=chunk,
+                                   pos0=p0, state_in=d["state_in"], d_state_out=dso, grad_dtype=torch.float32)
+        out, _ = R.chunkwise(d["q"], d["k"], d["v"], inp["gamma"], inp["theta"], chunk=chunk, pos0=p0,
+                             state_in=d["state_in"], out_dtype=torch.float32)
+        dg, dt = R.param_grads(d["q"], d["k"], d["v"], d_o, out, *got[:3], inp["gamma"], inp["theta"], pos0=p0,
+                               state_in=d["state_in"], d_state_out=dso)
+        assert R.sync_status() == R.RET_OK
+        ref = _oracle_bwd(inp, gi, p0)
+        tol = torch.float32 if dtype == "f32" else torch.bfloat16
+        for g, r, name in zip(got, ref, ("dq", "dk", "dv", "dS_in")):
+            assert_close(gpu_np(g), r, tol, f"{dtype} {name}")
+        rg, rt = O.retention_param_grads(to_f64(inp["q"]), to_f64(inp["k"]), to_f64(inp["v"]),
+                                         np.asarray(inp["gamma"], np.float64), np.asarray(inp["theta"], np.float64),
+                                         p0, to_f64(inp["state_in"]), to_f64(gi["d_out"]),
+                                         to_f64(gi["d_state_out"]))
+        lim = 1e-4 if dtype == "f32" else BF16_TOL
+        assert max_rel_inf(gpu_np(dg), rg) <= lim and max_rel_inf(gpu_np(dt), rt) <= lim, dtype
+    # the MSR block (rotation in the projection epilogues)
+    g = torch.Generator().manual_seed(5)
+    B, L, D, H, d_k, d_v = 1, 300, 256, 2, 128, 256
+    x = (torch.randn(B, L, D, generator=g)).to(torch.bfloat16)
+    ws = [(torch.randn(*s, generator=g) * sc).to(torch.bfloat16) for s, sc in
+          (((D, H, d_k), D ** -0.5), ((D, H, d_k), D ** -0.5), ((D, H, d_v), D ** -0.5), ((D, H, d_v), D ** -0.5),
+           ((H, d_v, D), (H * d_v) ** -0.5))]
+    gam, th = gamma_schedule(H), theta_schedule(d_k)
+    z, _ = R.msr_block(x.cuda(), *[t.cuda() for t in ws], gam, th, pos0=top - L, out_dtype=torch.float32)
+    assert R.sync_status() == R.RET_OK
+    ref_z, _ = O.msr_block(to_f64(x), *[to_f64(t) for t in ws], gam.astype(np.float64), th.astype(np.float64),
+                           top - L, None, 1e-5, 128)
+    assert_close(gpu_np(z), ref_z, torch.bfloat16, "block z")
