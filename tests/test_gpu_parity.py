@@ -372,6 +372,8 @@ def test_compact_workspace_matches_front_pass(B, H, L, d_k, d_v, rowpos):
     (256, 256, 77, 2),     # pair kernel, one short chunk
     (128, 128, 200, 2),    # one-CTA kernel
     (64, 128, 129, 2),     # one-CTA kernel, last chunk of 1 token
+    (256, 256, 1, 2),      # pair kernel, a single token
+    (128, 128, 1, 3),      # one-CTA kernel, a single token
 ])
 def test_tc_ragged_length_vs_oracle(d_k, d_v, L, H):
     """L not a multiple of the chunk on the tensor-core path: the rotated
@@ -543,6 +545,7 @@ def _oracle_bwd(inp, gi, pos0):
     ("bf16", torch.float32, 2, 2, 256, 128, 128, 128, 100, False, True),   # one-CTA kernels
     ("bf16", torch.float32, 1, 2, 300, 256, 512, 128, 5, True, True),      # two d_v pieces, pairs, ragged
     ("bf16", torch.bfloat16, 1, 3, 200, 128, 384, 128, 0, True, True),     # pieces of 256 and 128
+    ("bf16", torch.float32, 2, 2, 1, 256, 256, 128, 9, True, True),        # a single token
 ])
 def test_backward_vs_oracle(dtype, gdtype, B, H, L, d_k, d_v, chunk, pos0, state, dso):
     w, inp = _custom(B, H, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0)
