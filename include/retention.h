@@ -222,14 +222,14 @@ ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, i
  *   dQ′ = G K′ + ξ ⊙ (dO S_inᵀ)          dV = (Q′K′ᵀ ⊙ A)ᵀ dO + (w ⊙ K′) dS_out
  *   dK′ = Gᵀ Q′ + (w ⊙ V) dS_outᵀ         dS_in = (ξ ⊙ Q′)ᵀ dO + γ^L dS_out
  *   dq = R(−nθ) dQ′,  dk = d_k^{-1/2} R(−nθ) dK′    (the Θ prologue's adjoint)
- * Computed as three chunkwise evaluations (one in order, two over the
- * reversed sequence, which turns the sums over t ≥ m into causal ones).
- * Paths: bf16 inputs with chunk = 128, d_k ∈ {128, 256}, d_v a multiple of
- * 128 and every γ^127 ≥ 2^-60 run the evaluations on the tensor-core chunk
- * kernels (bf16 operands, fp32 accumulation; the two evaluations that
- * contract over d_v run as sums of pieces of at most 256 columns);
- * everything else runs on the fp32 kernels with `chunk` as the chunk length
- * (any ≥ 1).
+ * Computed as three chunkwise evaluations: dQ′ in order, dK′ and dV as
+ * anti-causal ones (sums over t ≥ m).  Paths: bf16 inputs with chunk = 128,
+ * d_k ∈ {128, 256}, d_v a multiple of 128 and every γ^255 ≥ 2^-100 run
+ * the evaluations on the tensor-core chunk kernels (bf16 operands, fp32
+ * accumulation; the anti-causal ones walk the chunks from the last; the two
+ * evaluations that contract over d_v run as sums of pieces of at most 256
+ * columns); everything else runs on the fp32 kernels over the reversed
+ * sequence, with `chunk` as the chunk length (any ≥ 1).
  * q, k, v, d_out: DEVICE, in_dt, layouts as above.  dq, dk [B, H, L, d_k]
  * and dv [B, H, L, d_v]: DEVICE, grad_dt; they must not alias any input.
  * state_in, d_state_out: DEVICE fp32 [B, H, d_k, d_v] or NULL (zero).

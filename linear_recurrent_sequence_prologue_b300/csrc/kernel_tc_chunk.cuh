@@ -106,6 +106,10 @@ struct ChunkArgs {
   // blockIdx.y + gridDim.y·blockIdx.z, and the CTAs past grid_rows exit at
   // once.  0: one row per blockIdx.y (gridDim.z = 1).
   int grid_rows = 0;
+  // V's sequence index is the row's sequence mod v_seqs (0: the sequence
+  // itself), so that grid rows that differ only in a piece of the
+  // contracted columns read one copy of V.
+  int v_seqs = 0;
   // Ring mode of the pair kernel (ring > 0, carried layout only): grid rows
   // [0, ring_prod_rows) are producer CTAs that rotate raw q, k (read through
   // their own tensor maps) into `ring` chunk slots per head — ring_q / ring_k
@@ -271,13 +275,18 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(const uint4* __restrict_
 // Warp 0: TMA producer.  Warp 1: MMA issuer.  Warps 2..17: drain warps; the
 // drain warp with hardware warp id w reads TMEM lanes 32·(w % 4) … +31
 // (v for Õᵀ/ΔSᵀ/Ŝᵀ, j for P̂) and handles column slice (w − 2) / 4.
+// BWD: the gradient pass's instantiations (carried layout), where V's
+// sequence index is taken mod args.v_seqs; BWD = 2 is the anti-causal form:
+// chunks walked from the last to the first, key m kept for query j when
+// m ≥ j.  The forward instantiation (BWD = 0) compiles none of it.
 // ---------------------------------------------------------------------------
-template <int DK>
+template <int DK, int BWD = 0>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, ChunkArgs args, CallConsts cc) {
   using C = Cfg<DK>;
+  constexpr bool REV = BWD == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -294,6 +303,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int d_v = args.d_v, nch = args.nchunks;
   // γ^{b_c} of chunk c of the sequence (its last chunk may be shorter)
   auto gch = [&](int c) -> float { return c == args.seq_chunks - 1 ? cc.gtail[h] : cc.gb[h]; };
+  // chunk of the sequence handled at step i
+  auto cix = [&](int i) -> int { return REV ? nch - 1 - i : c0 + i; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_q);
@@ -320,10 +331,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // Buffers free up in the order K̂′ (after ΔS), Q′ (after QS), V (after PV).
     if (lane == 0) {
       int issued = -1;   // last chunk whose loads were all issued
+      const int vseq = BWD && args.v_seqs ? seq % args.v_seqs : seq;   // V's row in its tensor map
       for (int i = 0; i < nch; ++i) {
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
-        const int y = seq * args.seq_lp + (c0 + i) * CH;   // row of Q′ / K̂′
-        const int yv = (c0 + i) * CH;                       // row of V within the sequence
+        const int y = seq * args.seq_lp + cix(i) * CH;   // row of Q′ / K̂′
+        const int yv = cix(i) * CH;                       // row of V within the sequence
         if (i > 0 && !mbar_wait(bar(K_EMPTY), pp, 0x101)) break;
         mbar_arrive_expect_tx(bar(K_FULL), C::Q_BYTES);
         for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sK + b * C::BOX, &tm_k, 64 * b, y, bar(K_FULL));
@@ -332,7 +344,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int b = 0; b < C::QBOX; ++b) tma_load_2d(sQ + b * C::BOX, &tm_q, 64 * b, y, bar(Q_FULL));
         if (i > 0 && !mbar_wait(bar(V_EMPTY), pp, 0x103)) break;
         mbar_arrive_expect_tx(bar(V_FULL), C::V_BYTES);
-        for (int b = 0; b < 2; ++b) tma_load_3d(sV + b * C::BOX, &tm_v, v0 + 64 * b, yv, seq, bar(V_FULL));
+        for (int b = 0; b < 2; ++b) tma_load_3d(sV + b * C::BOX, &tm_v, v0 + 64 * b, yv, vseq, bar(V_FULL));
         issued = i;
       }
       if (issued >= 0 && status_aborted()) {
@@ -437,12 +449,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(SH_READY));
     };
-    write_shat(gch(c0));
+    write_shat(gch(cix(0)));
 
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
       const uint32_t pi = static_cast<uint32_t>(i) & 1u;
-      const float gi = gch(c0 + i);
+      const float gi = gch(cix(i));
       // ---- (a) P̂ drain: causal mask, bf16, into the K-major swizzled tile ----
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
@@ -468,8 +480,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const int m = 32 * cs + 16 * hf + 8 * g + 2 * u;
-              const float a = (m <= j) ? __uint_as_float(r[8 * g + 2 * u]) : 0.f;
-              const float b = (m + 1 <= j) ? __uint_as_float(r[8 * g + 2 * u + 1]) : 0.f;
+              const bool ka = REV ? m >= j : m <= j, kb = REV ? m + 1 >= j : m + 1 <= j;
+              const float a = ka ? __uint_as_float(r[8 * g + 2 * u]) : 0.f;
+              const float b = kb ? __uint_as_float(r[8 * g + 2 * u + 1]) : 0.f;
               pk[u] = pack_bf16x2(a, b);
             }
             const int m0 = 32 * cs + 16 * hf + 8 * g;
@@ -500,7 +513,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
       if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
       tc_fence_after();
-      write_shat(gch(c0 + i + 1));
+      write_shat(gch(cix(i + 1)));
 
       // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
@@ -508,11 +521,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       {
         // A short last chunk goes whole to the staging tile [sequence][128][d_v]
         // (a copy kernel then moves its valid rows), so no store needs a check.
-        const bool staged = args.tail_out && c0 + i == args.seq_chunks - 1;
+        const bool staged = args.tail_out && cix(i) == args.seq_chunks - 1;
         void* const obuf = staged ? args.tail_out : args.out;
         const size_t base = staged
             ? (static_cast<size_t>(seq) * CH + 32 * cs) * d_v + v0 + vl
-            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(c0 + i) * CH + 32 * cs) * d_v + v0 + vl;
+            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(cix(i)) * CH + 32 * cs) * d_v + v0 + vl;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t r[16];

@@ -233,7 +233,11 @@ __device__ __forceinline__ void ring_producer(const CUtensorMap* tm_rq, const CU
 // RING: the compact-workspace instantiation (producer CTAs in the first
 // grid rows, Q′ / K̂′ read from the ring); without it none of that code is
 // compiled in, so the front-pass path keeps its own register allocation.
-template <int DK, bool RING>
+// BWD: the gradient pass's instantiations (carried layout, one sequence per
+// row), where V's sequence index is taken mod args.v_seqs; BWD = 2 is the
+// anti-causal form: chunks walked from the last to the first, key m kept for
+// query j when m ≥ j.  The forward instantiation (BWD = 0) compiles none of it.
+template <int DK, bool RING, int BWD = 0>
 __global__ void __launch_bounds__(NTHREADS, 1)
     pair_tc_kernel(const __grid_constant__ CUtensorMap tm_qh,   // Q′, 64-row boxes
                    const __grid_constant__ CUtensorMap tm_kh,   // K̂′, 64-row boxes
@@ -243,6 +247,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tm_rk,   // ring mode: raw k
                    ChunkArgs args, CallConsts cc, RowPos rp) {
   using C = Cfg<DK>;
+  static_assert(!(RING && BWD), "the ring mode is a forward mode");
+  constexpr bool REV = BWD == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -277,6 +283,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int d_v = args.d_v, nch = args.nchunks;
   // γ^{b_c} of chunk c of the sequence (its last chunk may be shorter)
   auto gch = [&](int c) -> float { return c == args.seq_chunks - 1 ? cc.gtail[h] : cc.gb[h]; };
+  // chunk of the sequence handled at step i
+  auto cix = [&](int i) -> int { return REV ? nch - 1 - i : c0 + i; };
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tm_qh);
@@ -310,9 +318,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // last chunk whose loads were issued, per buffer (for the abort path)
       int iv = -1, ikv = -1, iq = -1, ikq = -1;
       const int yh = 64 * static_cast<int>(rank);
+      const int vseq = BWD && args.v_seqs ? seq % args.v_seqs : seq;   // V's row in its tensor map
       for (int i = 0; i < nch; ++i) {
-        const int y = qrow(c0 + i);       // row of Q′ / K̂′
-        const int yv = (c0 + i) * CH;     // row of V within the sequence
+        const int y = qrow(cix(i));       // row of Q′ / K̂′
+        const int yv = cix(i) * CH;       // row of V within the sequence
         const int s = i & 1;
         const uint32_t pp = static_cast<uint32_t>(i - 1) & 1u;
         const uint32_t ps = static_cast<uint32_t>((i >> 1) - 1) & 1u;
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (i > 1 && !mbar_wait(bar(V_EMPTY0 + s), ps, 0x103)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(V_FULL0 + s), 2 * C::V_BYTES);
         for (int b = 0; b < 2; ++b)
-          tma_load_3d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, yv, seq, lead_bar(V_FULL0 + s));
+          tma_load_3d_pair(sV + s * C::V_BYTES + b * C::BOX, &tm_v, v0 + 64 * b, yv, vseq, lead_bar(V_FULL0 + s));
         iv = i;
         if (i > 0 && !mbar_wait(bar(KV_EMPTY), pp, 0x104)) break;
         if (rank == 0) mbar_arrive_expect_tx(bar(KV_FULL), 2 * C::KV_BYTES);
@@ -474,12 +483,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       arrive_lead(SH_READY);
     };
-    write_shat(gch(c0));
+    write_shat(gch(cix(0)));
 
     bool ok = true;
     for (int i = 0; i < nch && ok; ++i) {
       const uint32_t pi = static_cast<uint32_t>(i) & 1u;
-      const float gi = gch(c0 + i);
+      const float gi = gch(cix(i));
       // ---- (a) P̂ drain: causal mask, bf16, into this CTA's query half ----
       if (!mbar_wait(bar(P_FULL), pi, 0x301)) { ok = false; break; }
       tc_fence_after();
@@ -501,8 +510,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int m = 64 * mh + 16 * cs + 8 * g + 2 * u;
-            const float a = (m <= j) ? __uint_as_float(r[2 * u]) : 0.f;
-            const float b = (m + 1 <= j) ? __uint_as_float(r[2 * u + 1]) : 0.f;
+            const bool ka = REV ? m >= j : m <= j, kb = REV ? m + 1 >= j : m + 1 <= j;
+            const float a = ka ? __uint_as_float(r[2 * u]) : 0.f;
+            const float b = kb ? __uint_as_float(r[2 * u + 1]) : 0.f;
             pk[u] = pack_bf16x2(a, b);
           }
           st_shared_v4(sP + mh * C::HBOX + sw128_offset(jl, 16 * cs + 8 * g), pk[0], pk[1], pk[2], pk[3]);
@@ -529,7 +539,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // ---- (c) Ŝ for the next chunk, once QS of this chunk has read Ŝ ----
       if (!mbar_wait(bar(SH_FREE), pi, 0x303)) { ok = false; break; }
       tc_fence_after();
-      write_shat(gch(c0 + i + 1));
+      write_shat(gch(cix(i + 1)));
 
       // ---- (d) Õ drain: release X, then store (ω_j rides on Q′) ----
       if (!mbar_wait(bar(O_FULL), pi, 0x304)) { ok = false; break; }
@@ -537,11 +547,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       {
         // A short last chunk goes whole to the staging tile [sequence][128][d_v]
         // (a copy kernel then moves its valid rows), so no store needs a check.
-        const bool staged = args.tail_out && c0 + i == args.seq_chunks - 1;
+        const bool staged = args.tail_out && cix(i) == args.seq_chunks - 1;
         void* const obuf = staged ? args.tail_out : args.out;
         const size_t base = staged
             ? (static_cast<size_t>(seq) * CH + 32 * cs) * d_v + v0 + vl
-            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(c0 + i) * CH + 32 * cs) * d_v + v0 + vl;
+            : (static_cast<size_t>(seq) * args.seq_len + static_cast<size_t>(cix(i)) * CH + 32 * cs) * d_v + v0 + vl;
         if (args.out && !args.out_f32) {
           // bf16 output: the first 16 rows packed to bf16 pairs, the last 16
           // loaded, X released, and only then the 32 stores, so that no store

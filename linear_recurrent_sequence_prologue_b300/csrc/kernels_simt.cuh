@@ -591,20 +591,17 @@ __global__ void __launch_bounds__(256) state_prep_kernel(const float* src, float
 
 // Operands of the tensor-core evaluations in the gradient pass, bf16, all
 // derived from one source tensor src [BH][L][d] in one pass:
-//   op[bh][t][:] = f(t) · scale · R?((pos0 + t_s)θ) src[bh][t_s][:]   (t < L)
-//   op[bh][t][:] = 0                                                  (L ≤ t < rows_out)
-// with t_s = L−1−t when the operand is reversed (flip), else t; the rotation
-// (the prologue's, at the source row's position) only when rotate.  f(t) is
-// 1 (fold 0), ω = γ^{(t mod b)+1−b_c} (fold 1) or ζ = γ^{b_c−1−(t mod b)}
-// (fold 2), b_c the length of t's chunk of b rows (the last may be shorter):
-// the per-row factors of the chunk kernels' rewritten form, taken over the
-// sequence as it is read.  Each operand's columns are stored in pieces of
+//   op[bh][t][:] = f(t) · scale · R?((pos0 + t)θ) src[bh][t][:]   (t < L)
+//   op[bh][t][:] = 0                                              (L ≤ t < rows_out)
+// with the rotation (the prologue's) only when rotate.  f(t) is 1 (fold 0),
+// ω = γ^{j−(b−1)} (fold 1) or ζ = γ^{b−1−j} (fold 2), j = t mod b, b the
+// chunk length: every chunk, the last included, is folded as a whole one
+// (rows past L are zero).  Each operand's columns are stored in pieces of
 // pw (the last may be narrower), piece-major: [piece][bh][t][columns of the
-// piece]; ncopy copies of the whole operand follow each other.  d and pw
-// multiples of 8.
+// piece].  d and pw multiples of 8.
 struct OpSpec {
   __nv_bfloat16* dst;
-  int rows_out, pw, ncopy, flip, fold;
+  int rows_out, pw, fold;
   float scale;
 };
 template <int NS>
@@ -612,9 +609,9 @@ struct OpSpecs {
   OpSpec o[NS];
 };
 
-// Thread ↔ (source row t_s, 8 columns); threads with t_s ≥ L zero the
-// padding rows.  The angles are computed once per thread and used for all
-// B·H heads, whose loads are issued eight at a time.  NS operands.
+// Thread ↔ (row t, 8 columns); threads with t ≥ L zero the padding rows.
+// The angles are computed once per thread and used for all B·H heads, whose
+// loads are issued eight at a time.  NS operands.
 template <int NS>
 __global__ void __launch_bounds__(256) prep_operand_kernel(
     const __nv_bfloat16* __restrict__ src, OpSpecs<NS> sp, CallConsts cc, int BH, int H, int L,
@@ -623,43 +620,31 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
   const int vecs = d / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows_max * vecs) return;
-  const int ts = idx / vecs, cv = idx - ts * vecs;
-  const int nch = (L + chunk - 1) / chunk;
-  auto optr = [&](const OpSpec& o, int bh, int t, int cp) {
+  const int t = idx / vecs, cv = idx - t * vecs;
+  auto optr = [&](const OpSpec& o, int bh) {
     const int piece = (8 * cv) / o.pw;
     const int wp = min(o.pw, d - piece * o.pw);
-    const size_t at = static_cast<size_t>(cp) * o.rows_out * d * BH +
-                      static_cast<size_t>(piece) * o.pw * o.rows_out * BH +
+    const size_t at = static_cast<size_t>(piece) * o.pw * o.rows_out * BH +
                       (static_cast<size_t>(bh) * o.rows_out + t) * wp + (8 * cv - piece * o.pw);
     return reinterpret_cast<uint4*>(o.dst + at);
   };
-  if (ts >= L) {   // padding rows of the operands that have them
+  if (t >= L) {   // padding rows of the operands that have them
 #pragma unroll
     for (int i = 0; i < NS; ++i) {
       const OpSpec& o = sp.o[i];
-      if (ts >= o.rows_out) continue;
-      for (int bh = 0; bh < BH; ++bh)
-        for (int cp = 0; cp < o.ncopy; ++cp) *optr(o, bh, ts, cp) = make_uint4(0u, 0u, 0u, 0u);
+      if (t >= o.rows_out) continue;
+      for (int bh = 0; bh < BH; ++bh) *optr(o, bh) = make_uint4(0u, 0u, 0u, 0u);
     }
     return;
   }
   float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
   if (rotate) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(ts), cc.theta[4 * cv + u], c[u], sn[u]);
+    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
   }
-  int trow[NS];
-  float ex[NS];
-#pragma unroll
-  for (int i = 0; i < NS; ++i) {
-    const int t = sp.o[i].flip ? L - 1 - ts : ts;
-    const int bc = (t / chunk == nch - 1) ? L - (nch - 1) * chunk : chunk;
-    const int j = t % chunk;
-    trow[i] = t;
-    ex[i] = sp.o[i].fold == 1 ? static_cast<float>(j + 1 - bc) : static_cast<float>(bc - 1 - j);
-  }
+  const int j = t % chunk;
   const size_t hstride = static_cast<size_t>(L) * d;
-  const __nv_bfloat16* s0 = src + static_cast<size_t>(ts) * d + 8 * cv;
+  const __nv_bfloat16* s0 = src + static_cast<size_t>(t) * d + 8 * cv;
   for (int bh0 = 0; bh0 < BH; bh0 += U) {
     uint4 raw[U];
 #pragma unroll
@@ -681,38 +666,35 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
 #pragma unroll
       for (int i = 0; i < NS; ++i) {
         const OpSpec& o = sp.o[i];
-        const float f = o.fold ? o.scale * gpow(lg, ex[i]) : o.scale;
-        const uint4 ov = make_uint4(pack_bf16x2(f * r[0], f * r[1]), pack_bf16x2(f * r[2], f * r[3]),
-                                    pack_bf16x2(f * r[4], f * r[5]), pack_bf16x2(f * r[6], f * r[7]));
-        for (int cp = 0; cp < o.ncopy; ++cp) *optr(o, bh, trow[i], cp) = ov;
+        const float ex = o.fold == 1 ? static_cast<float>(j + 1 - chunk) : static_cast<float>(chunk - 1 - j);
+        const float f = o.fold ? o.scale * gpow(lg, ex) : o.scale;
+        *optr(o, bh) = make_uint4(pack_bf16x2(f * r[0], f * r[1]), pack_bf16x2(f * r[2], f * r[3]),
+                                  pack_bf16x2(f * r[4], f * r[5]), pack_bf16x2(f * r[6], f * r[7]));
       }
     }
   }
 }
 
 // Gradients from the fp32 outputs of the evaluations:
-//   y[bh][t][:] = scale · R?(−(pos0 + t)θ) Σ_{p<np} x[p][bh][t_s][:]
-// with t_s = L−1−t when flip; x pieces `pstride` elements apart; R(−φ) the
-// adjoint (inverse) of the prologue's rotation, only when rotate.
-// Thread ↔ (row t, 8 columns), looping over the B·H heads.  d a multiple of 8.
+//   y[bh][t][:] = scale · R(−(pos0 + t)θ) Σ_{p<np} x[p][bh][t][:]
+// with x pieces `pstride` elements apart and R(−φ) the adjoint (inverse) of
+// the prologue's rotation.  Thread ↔ (row t, 8 columns), looping over the
+// B·H heads.  d a multiple of 8.
 template <typename Tg>
 __global__ void __launch_bounds__(256) grad_out_kernel(const float* __restrict__ x,
                                                        size_t pstride, int np,
                                                        Tg* __restrict__ y, CallConsts cc,
-                                                       int BH, int L, int d, int flip,
-                                                       int rotate, float pos0, float scale) {
+                                                       int BH, int L, int d, float pos0,
+                                                       float scale) {
   const int vecs = d / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= L * vecs) return;
   const int t = idx / vecs, cv = idx - t * vecs;
-  const int ts = flip ? L - 1 - t : t;
-  float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
-  if (rotate) {
+  float c[4], sn[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
-  }
+  for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
   for (int bh = 0; bh < BH; ++bh) {
-    const float* xr = x + (static_cast<size_t>(bh) * L + ts) * d + 8 * cv;
+    const float* xr = x + (static_cast<size_t>(bh) * L + t) * d + 8 * cv;
     float4 a0 = __ldcs(reinterpret_cast<const float4*>(xr));
     float4 a1 = __ldcs(reinterpret_cast<const float4*>(xr) + 1);
     for (int p = 1; p < np; ++p) {

@@ -1019,16 +1019,31 @@ ret_status run_backward(const Tin* q, const Tin* k, const Tin* v, const Tin* d_o
 
 // ---------------------------------------------------------------------------
 // Gradient pass on the tensor cores (bf16 inputs): the same three
-// evaluations, each run by the chunk kernels on operands that
-// prep_operand_kernel lays out as the front pass lays out Q′ and K̂′ (ω and
-// ζ folded, rows padded to whole chunks).  The two evaluations whose scores
-// contract over d_v run as a sum of pieces of at most 256 columns (the
-// scores are linear in the contracted columns, and so is the cross term
-// once S_in is cut by the same rows).  When every piece is 256 wide, the
-// pieces run in one launch as extra grid rows (piece p of (b, h) is row
-// p·B·H + b·H + h), which keeps enough CTAs in flight when d_k = 256 gives
-// only two d_v tiles per row; the operand the scores multiply is then
-// stored once per piece.
+// evaluations, run by the chunk kernels on operands that prep_operand_kernel
+// lays out as the front pass lays out Q″ and K̂′, with one difference: every
+// chunk, the last included, is folded as a whole chunk of 128 rows (ω_j =
+// γ^{j−127}, ζ_j = γ^{127−j}, j the row within the chunk; rows past L are
+// zero).  The sequence is then evaluated as if it had Lp rows, and:
+//  * the forward evaluation (dQ′) gives the same outputs when the last chunk
+//    carries with γ^128 too (only its final state, which is not used, is
+//    scaled);
+//  * the anti-causal evaluations (dK′, dV) run on the chunk kernels' reverse
+//    mode (last chunk first, keys m ≥ j) with the query operand folded by ζ
+//    and the key operand by ω: their scores are γ^{m−j} a_j·b_m, and the
+//    kernel's state is γ^{−127} times the state of the anti-causal recursion
+//    R ← γ^128 R + Σ_m γ^m b_m c_mᵀ started at row Lp.  So the dK′ evaluation
+//    reads the dQ′ evaluation's two folded operands with their roles
+//    exchanged (ζ·V as queries, ω·dO as keys), the dV evaluation reads K̂′ and
+//    Q″ as queries and keys and dO itself as values, and both start from
+//    γ^{−127}·γ^{r−128}·dS_out/γ (r the last chunk's length: dS_out/γ is the
+//    state at row L, γ^{r−128} moves it to row Lp) and dS_in = γ^128 · the
+//    final state.  The evaluations whose scores contract over d_v run as a
+//    sum of pieces of at most 256 columns (the scores are linear in the
+//    contracted columns, and so is the cross term once the state is cut by
+//    the same rows).  When every piece is 256 wide, the pieces run in one
+//    launch as extra grid rows (piece p of (b, h) is row p·B·H + b·H + h),
+//    which keeps enough CTAs in flight when d_k = 256 gives only two d_v
+//    tiles per row; those rows read one copy of the value operand.
 // ---------------------------------------------------------------------------
 constexpr int kBwdPiece = 256;
 
@@ -1038,13 +1053,19 @@ bool tc_backward_ok(ret_dtype in_dt, const float* gamma, int H, int d_k, int d_v
                     int B) {
   if (g_force_path == RET_PATH_SIMT || in_dt != RET_BF16 || chunk != tcc::CH) return false;
   if (!(d_k == 128 || d_k == 256) || d_v % tcc::VT != 0) return false;
-  return tc_gamma_ok(gamma, H, chunk);
+  if (!tc_gamma_ok(gamma, H, chunk)) return false;
+  // the reverse evaluations' states carry factors up to γ^{−255}: keep them
+  // within 2^100
+  for (int h = 0; gamma && h < H; ++h)
+    if (-(2 * chunk - 1) * std::log2(static_cast<double>(gamma[h])) > 100.0) return false;
+  return true;
 }
 
 struct TcBwdPlan {
-  // operands of the three evaluations: dQ′ (1), dK′↓ (3), dV↓ (2)
-  size_t off_a1 = 0, off_b1 = 0, off_c1 = 0, off_a3 = 0, off_b3 = 0, off_c3 = 0;
-  size_t off_a2 = 0, off_b2 = 0, off_c2 = 0;
+  // operands: ω·dO and ζ·V (dQ′ and, roles exchanged, dK′; 256-column
+  // pieces), K′ (dQ′'s values), Q′ (dK′'s values), K̂′ and Q″ (dV's queries
+  // and keys)
+  size_t off_dof = 0, off_vf = 0, off_kr = 0, off_qr = 0, off_kf = 0, off_qf = 0;
   size_t off_x = 0, off_sprep = 0, off_tail = 0, bytes = 0;
   int pieces = 0;
   bool as_rows = false;   // all pieces in one launch
@@ -1056,41 +1077,39 @@ TcBwdPlan plan_tc_backward(int B, int H, int L, int d_k, int d_v) {
   const size_t Lp = static_cast<size_t>((L + tcc::CH - 1) / tcc::CH) * tcc::CH;
   p.pieces = bwd_pieces(d_v);
   p.as_rows = d_v % kBwdPiece == 0;
-  const size_t ncopy = p.as_rows ? p.pieces : 1;
   const size_t xw = std::max(static_cast<size_t>(p.pieces) * d_k, static_cast<size_t>(d_v));
   const size_t av = up256(BH * Lp * d_v * 2), ak = up256(BH * Lp * d_k * 2);
-  const size_t ck = up256(ncopy * BH * L * d_k * 2), cv = up256(BH * L * static_cast<size_t>(d_v) * 2);
+  const size_t ck = up256(BH * L * d_k * 2);
   size_t off = 0;
-  p.off_a1 = off; off += av;   // ω·dO, 256-column pieces
-  p.off_b1 = off; off += av;   // ζ·V
-  p.off_c1 = off; off += ck;   // K′, once per piece
-  p.off_a3 = off; off += av;   // ω·V↓
-  p.off_b3 = off; off += av;   // ζ·dO↓
-  p.off_c3 = off; off += ck;   // Q′↓, once per piece
-  p.off_a2 = off; off += ak;   // ω·K′↓
-  p.off_b2 = off; off += ak;   // ζ·Q′↓
-  p.off_c2 = off; off += cv;   // dO↓
-  p.off_x = off; off += up256(BH * L * xw * 4);       // fp32 outputs (one per piece)
+  p.off_dof = off; off += av;
+  p.off_vf = off; off += av;
+  p.off_kr = off; off += ck;
+  p.off_qr = off; off += ck;
+  p.off_kf = off; off += ak;
+  p.off_qf = off; off += ak;
+  p.off_x = off; off += up256(BH * L * static_cast<size_t>(p.pieces) * d_k * 4);   // fp32, per piece
   p.off_sprep = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4);
   if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * xw * 4); }
   p.bytes = off;
   return p;
 }
 
-// out (fp32 [rows][L][dvF]) = the chunkwise form over `rows` sequences with
-// Q″ = a and K̂′ = b (bf16 [rows][Lp][dkF]), V = c (bf16 [rows][L][dvF]);
-// s_in / s_out per row [dkF][dvF].  Head of row r: r mod H.
+// out ([rows][L][dvF], fp32 or bf16) = the chunkwise form over `rows`
+// sequences with Q″ = a and K̂′ = b (bf16 [rows][Lp][dkF]), V = c (bf16
+// [rows mod v_seqs][L][dvF], v_seqs 0: [rows]); s_in / s_out per row
+// [dkF][dvF].  Head of row r: r mod H.  rev: the reverse mode (anti-causal).
 ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
-                       const __nv_bfloat16* c, int dvF, const float* s_in, float* s_out,
-                       float* out, void* tail, const CallConsts& cc, int rows, int H, int L,
-                       cudaStream_t st) {
+                       const __nv_bfloat16* c, int dvF, int v_seqs, const float* s_in,
+                       float* s_out, void* out, int out_f32, void* tail, const CallConsts& cc,
+                       int rows, int H, int L, bool rev, cudaStream_t st) {
   const int nch = (L + tcc::CH - 1) / tcc::CH;
   const int Lp = nch * tcc::CH;
   const uint64_t qrows = static_cast<uint64_t>(rows) * Lp;
   const bool pair = tc_pair_ok(dkF, dvF);
+  const uint64_t vrows = static_cast<uint64_t>(v_seqs ? v_seqs : rows);
   CUtensorMap mq, mk, mv, mqh, mkh;
   if (!make_map(&mq, a, qrows, dkF) || !make_map(&mk, b, qrows, dkF) ||
-      !make_map3(&mv, c, static_cast<uint64_t>(rows), static_cast<uint64_t>(L), dvF))
+      !make_map3(&mv, c, vrows, static_cast<uint64_t>(L), dvF))
     return RET_ECUDA;
   if (pair && (!make_map(&mqh, a, qrows, dkF, 64) || !make_map(&mkh, b, qrows, dkF, 64)))
     return RET_ECUDA;
@@ -1098,7 +1117,7 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
   g.state_in = s_in;
   g.state_out = s_out;
   g.out = out;
-  g.out_f32 = 1;
+  g.out_f32 = out_f32;
   g.H = H;
   g.d_v = dvF;
   g.nchunks = nch;
@@ -1108,6 +1127,7 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
   g.tail_out = (L % tcc::CH != 0) ? tail : nullptr;
   g.seq_div = 1;
   g.raw_ds = 0;
+  g.v_seqs = v_seqs;
   auto launch_pair = [&](auto kern, uint32_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1138,18 +1158,26 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
     return cudaGetLastError();
   };
   cudaError_t e;
-  if (pair && dkF == 256) e = launch_pair(tcq::pair_tc_kernel<256, false>, tcq::Cfg<256>::SMEM_BYTES);
-  else if (pair) e = launch_pair(tcq::pair_tc_kernel<128, false>, tcq::Cfg<128>::SMEM_BYTES);
-  else if (dkF == 256) e = launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES);
-  else e = launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES);
+  if (pair && dkF == 256)
+    e = rev ? launch_pair(tcq::pair_tc_kernel<256, false, 2>, tcq::Cfg<256>::SMEM_BYTES)
+            : launch_pair(tcq::pair_tc_kernel<256, false, 1>, tcq::Cfg<256>::SMEM_BYTES);
+  else if (pair)
+    e = rev ? launch_pair(tcq::pair_tc_kernel<128, false, 2>, tcq::Cfg<128>::SMEM_BYTES)
+            : launch_pair(tcq::pair_tc_kernel<128, false, 1>, tcq::Cfg<128>::SMEM_BYTES);
+  else if (dkF == 256)
+    e = rev ? launch(tcc::chunk_tc_kernel<256, 2>, tcc::Cfg<256>::SMEM_BYTES)
+            : launch(tcc::chunk_tc_kernel<256, 1>, tcc::Cfg<256>::SMEM_BYTES);
+  else
+    e = rev ? launch(tcc::chunk_tc_kernel<128, 2>, tcc::Cfg<128>::SMEM_BYTES)
+            : launch(tcc::chunk_tc_kernel<128, 1>, tcc::Cfg<128>::SMEM_BYTES);
   if (e != cudaSuccess) return RET_ECUDA;
   if (g.tail_out) {
     const int T = L - (nch - 1) * tcc::CH;
-    const int row_vecs = dvF * 4 / 16;
+    const int row_vecs = dvF * (out_f32 ? 4 : 2) / 16;
     const size_t n = static_cast<size_t>(rows) * T * row_vecs;
     Mark m("bwd_tail_copy", st);
     tcc::tail_copy_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
-        static_cast<const uint4*>(g.tail_out), reinterpret_cast<uint4*>(out), rows, T, L,
+        static_cast<const uint4*>(g.tail_out), static_cast<uint4*>(out), rows, T, L,
         (nch - 1) * tcc::CH, row_vecs);
   }
   return last_launch();
@@ -1157,20 +1185,22 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
 
 template <typename Tg>
 ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
-                           const __nv_bfloat16* v, const __nv_bfloat16* d_o, const CallConsts& cc,
+                           const __nv_bfloat16* v, const __nv_bfloat16* d_o, const CallConsts& cc0,
                            int B, int H, int L, int d_k, int d_v, int64_t pos0, const float* s_in,
                            const float* dso, Tg* dq, Tg* dk, Tg* dv, float* dsi, void* ws,
                            const TcBwdPlan& p, cudaStream_t st) {
   const int BH = B * H;
   const int nch = (L + tcc::CH - 1) / tcc::CH;
   const int Lp = nch * tcc::CH;
+  const int r = L - (nch - 1) * tcc::CH;   // rows of the last chunk
+  CallConsts cc = cc0;                     // every chunk carries as a whole one
+  for (int h = 0; h < H; ++h) cc.gtail[h] = cc.gb[h];
   auto op = [&](size_t off) { return wsp<__nv_bfloat16>(ws, off); };
   float* X = wsp<float>(ws, p.off_x);
   float* sprep = wsp<float>(ws, p.off_sprep);
   void* tail = p.off_tail ? wsp<void>(ws, p.off_tail) : nullptr;
   const float p0 = static_cast<float>(pos0);
   const size_t nk = static_cast<size_t>(BH) * L * d_k;
-  const int ncopy = p.as_rows ? p.pieces : 1;
   // All operands, one pass per source tensor.
   auto prep = [&](const __nv_bfloat16* src, int d, int rotate, const auto& sp) {
     const int n = Lp * (d / 8);
@@ -1179,21 +1209,18 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
     simt::prep_operand_kernel<NS><<<(n + 255) / 256, 256, 0, st>>>(src, sp, cc, BH, H, L, Lp, d,
                                                                    rotate, p0, tcc::CH);
   };
-  //                                   dst         rows pw         copies flip fold scale
-  prep(d_o, d_v, 0, simt::OpSpecs<3>{{{op(p.off_a1), Lp, kBwdPiece, 1, 0, 1, 1.f},
-                                      {op(p.off_b3), Lp, kBwdPiece, 1, 1, 2, 1.f},
-                                      {op(p.off_c2), L, d_v, 1, 1, 0, 1.f}}});
-  prep(v, d_v, 0, simt::OpSpecs<2>{{{op(p.off_b1), Lp, kBwdPiece, 1, 0, 2, 1.f},
-                                    {op(p.off_a3), Lp, kBwdPiece, 1, 1, 1, 1.f}}});
-  prep(k, d_k, 1, simt::OpSpecs<2>{{{op(p.off_c1), L, d_k, ncopy, 0, 0, cc.kscale},
-                                    {op(p.off_a2), Lp, d_k, 1, 1, 1, cc.kscale}}});
-  prep(q, d_k, 1, simt::OpSpecs<2>{{{op(p.off_c3), L, d_k, ncopy, 1, 0, 1.f},
-                                    {op(p.off_b2), Lp, d_k, 1, 1, 2, 1.f}}});
-  // gradient = scale · R?(−nθ) Σ pieces of X (flip: X holds the reversed sequence)
-  auto grad_out = [&](Tg* y, int d, int np, int flip, int rotate, float scale) {
+  //                                   dst            rows pw         fold scale
+  prep(d_o, d_v, 0, simt::OpSpecs<1>{{{op(p.off_dof), Lp, kBwdPiece, 1, 1.f}}});
+  prep(v, d_v, 0, simt::OpSpecs<1>{{{op(p.off_vf), Lp, kBwdPiece, 2, 1.f}}});
+  prep(k, d_k, 1, simt::OpSpecs<2>{{{op(p.off_kr), L, d_k, 0, cc.kscale},
+                                    {op(p.off_kf), Lp, d_k, 2, cc.kscale}}});
+  prep(q, d_k, 1, simt::OpSpecs<2>{{{op(p.off_qr), L, d_k, 0, 1.f},
+                                    {op(p.off_qf), Lp, d_k, 1, 1.f}}});
+  // gradient = scale · R(−nθ) Σ pieces of X
+  auto grad_out = [&](Tg* y, float scale) {
     Mark m("bwd_grad_out", st);
-    simt::grad_out_kernel<Tg><<<(L * (d / 8) + 255) / 256, 256, 0, st>>>(
-        X, nk, np, y, cc, BH, L, d, flip, rotate, p0, scale);
+    simt::grad_out_kernel<Tg><<<(L * (d_k / 8) + 255) / 256, 256, 0, st>>>(
+        X, nk, p.pieces, y, cc, BH, L, d_k, p0, scale);
   };
   // dst = scale_h · (S or Sᵀ), cut into pieces of prows rows
   auto state_prep = [&](const float* src, float* dst, int transpose, int prows,
@@ -1202,50 +1229,53 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
     simt::state_prep_kernel<<<dim3((d_v + 31) / 32, (d_k + 31) / 32, BH), dim3(32, 8), 0, st>>>(
         src, dst, BH, H, d_k, d_v, transpose, prows, hs);
   };
-  simt::HeadScale one, ginv, gam;
+  simt::HeadScale one, start, fin;
   for (int h = 0; h < kMaxHeads; ++h) {
+    const double g = h < H ? static_cast<double>(cc.gamma[h]) : 1.0;
     one.s[h] = 1.f;
-    ginv.s[h] = h < H ? static_cast<float>(1.0 / static_cast<double>(cc.gamma[h])) : 1.f;
-    gam.s[h] = h < H ? cc.gamma[h] : 1.f;
+    start.s[h] = static_cast<float>(std::pow(g, r - 2 * tcc::CH));   // γ^{−127}·γ^{r−128}/γ
+    fin.s[h] = h < H ? cc.gb[h] : 1.f;                                // γ^128
   }
   ret_status s;
-  // The evaluations that contract over d_v: a, b piece-major, c the operand
-  // the scores multiply, s_pieces the pieces of S_in; piece outputs land nk
-  // apart in X.
+  // The evaluations that contract over d_v: a, b piece-major, c the values,
+  // s_pieces the pieces of the starting state; piece outputs land nk apart
+  // in X.
   auto pieces = [&](const __nv_bfloat16* a, const __nv_bfloat16* b, const __nv_bfloat16* c,
-                    const float* s_pieces) -> ret_status {
+                    const float* s_pieces, bool rev) -> ret_status {
     if (p.as_rows)
-      return run_tc_eval(a, b, kBwdPiece, c, d_k, s_pieces, nullptr, X, tail, cc, p.pieces * BH,
-                         H, L, st);
+      return run_tc_eval(a, b, kBwdPiece, c, d_k, BH, s_pieces, nullptr, X, 1, tail, cc,
+                         p.pieces * BH, H, L, rev, st);
     for (int pc = 0; pc < p.pieces; ++pc) {
       const int c0 = pc * kBwdPiece;
       const int w = std::min(kBwdPiece, d_v - c0);
       const size_t ob = static_cast<size_t>(c0) * Lp * BH;   // piece base in a, b
       const float* sp = s_pieces ? s_pieces + static_cast<size_t>(c0) * d_k * BH : nullptr;
-      ret_status r = run_tc_eval(a + ob, b + ob, w, c, d_k, sp, nullptr,
-                                 X + static_cast<size_t>(pc) * nk, tail, cc, BH, H, L, st);
-      if (r != RET_OK) return r;
+      ret_status rs = run_tc_eval(a + ob, b + ob, w, c, d_k, 0, sp, nullptr,
+                                  X + static_cast<size_t>(pc) * nk, 1, tail, cc, BH, H, L, rev, st);
+      if (rs != RET_OK) return rs;
     }
     return RET_OK;
   };
-  // dQ′ = F(dO, V, K′; S_inᵀ), then dq = R(−nθ) dQ′
+  // dQ′ = F(ω·dO, ζ·V, K′; S_inᵀ), then dq = R(−nθ) dQ′
   if (s_in) state_prep(s_in, sprep, 1, kBwdPiece, one);
-  if ((s = pieces(op(p.off_a1), op(p.off_b1), op(p.off_c1), s_in ? sprep : nullptr)) != RET_OK)
+  if ((s = pieces(op(p.off_dof), op(p.off_vf), op(p.off_kr), s_in ? sprep : nullptr, false)) !=
+      RET_OK)
     return s;
-  grad_out(dq, d_k, p.pieces, 0, 1, 1.f);
-  // dK′↓ = F(V↓, dO↓, Q′↓; dS_outᵀ/γ), then dk = d_k^{-1/2} R(−nθ) dK′
-  if (dso) state_prep(dso, sprep, 1, kBwdPiece, ginv);
-  if ((s = pieces(op(p.off_a3), op(p.off_b3), op(p.off_c3), dso ? sprep : nullptr)) != RET_OK)
+  grad_out(dq, 1.f);
+  // dK′ = reverse F(ζ·V, ω·dO, Q′; start·dS_outᵀ), then dk = d_k^{-1/2} R(−nθ) dK′
+  if (dso) state_prep(dso, sprep, 1, kBwdPiece, start);
+  if ((s = pieces(op(p.off_vf), op(p.off_dof), op(p.off_qr), dso ? sprep : nullptr, true)) !=
+      RET_OK)
     return s;
-  grad_out(dk, d_k, p.pieces, 1, 1, cc.kscale);
-  // dV↓ = F(K′↓, Q′↓, dO↓; dS_out/γ) and dS_in = γ · its S_out (dS_out is
-  // read into sprep before dS_in is written, so the two may alias)
-  if (dso) state_prep(dso, sprep, 0, d_k, ginv);
-  if ((s = run_tc_eval(op(p.off_a2), op(p.off_b2), d_k, op(p.off_c2), d_v, dso ? sprep : nullptr,
-                       dsi, X, tail, cc, BH, H, L, st)) != RET_OK)
+  grad_out(dk, cc.kscale);
+  // dV = reverse F(K̂′, Q″, dO; start·dS_out), written in place, and dS_in =
+  // γ^128 · its final state (dS_out is read into sprep before dS_in is
+  // written, so the two may alias)
+  if (dso) state_prep(dso, sprep, 0, d_k, start);
+  if ((s = run_tc_eval(op(p.off_kf), op(p.off_qf), d_k, d_o, d_v, 0, dso ? sprep : nullptr, dsi,
+                       dv, sizeof(Tg) == 4, tail, cc, BH, H, L, true, st)) != RET_OK)
     return s;
-  grad_out(dv, d_v, 1, 1, 0, 1.f);
-  if (dsi) state_prep(dsi, dsi, 0, d_k, gam);
+  if (dsi) state_prep(dsi, dsi, 0, d_k, fin);
   return last_launch();
 }
 

@@ -239,13 +239,14 @@ def test_backward_plan_and_validation(lib):
 
     BH, L = 32, 8192
     rk, rv = BH * L * 256 * 4, BH * L * 512 * 4
-    # tensor cores, the operands of the three evaluations in bf16: four ω/ζ-folded
-    # d_v-wide ones and two d_k-wide ones padded to whole chunks, K′ and Q′↓ once
-    # per 256-column piece of d_v (two), dO↓; then fp32 outputs (two pieces of d_k,
-    # or d_v) and one prepared state
+    # tensor cores, the operands of the three evaluations in bf16: ω·dO and ζ·V
+    # (d_v wide, shared by the dQ′ and dK′ evaluations), K̂′ and Q″ (d_k wide),
+    # all padded to whole chunks; K′ and Q′ (the values of dQ′ and dK′, once);
+    # then fp32 outputs (two pieces of d_k), one prepared state and, for a
+    # ragged length, a staging tile
     def tc_bytes(Lx, Lpx, tail):
-        return (4 * BH * Lpx * 512 * 2 + 2 * 2 * BH * Lx * 256 * 2 + 2 * BH * Lpx * 256 * 2
-                + BH * Lx * 512 * 2 + BH * Lx * 512 * 4 + BH * 256 * 512 * 4
+        return (2 * BH * Lpx * 512 * 2 + 2 * BH * Lpx * 256 * 2 + 2 * BH * Lx * 256 * 2
+                + BH * Lx * 512 * 4 + BH * 256 * 512 * 4
                 + (BH * 128 * 512 * 4 if tail else 0))
 
     assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_TC, tc_bytes(8192, 8192, False))
@@ -256,6 +257,8 @@ def test_backward_plan_and_validation(lib):
     simt = 3 * rk + 4 * rv + rv + BH * 64 * 256 * 512 * 4 + BH * 256 * 512 * 4
     assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 64)[0] == _lib.RET_PATH_SIMT      # chunk 64
     assert plan(_lib.RET_BF16, 2, 16, 8192, 64, 512, 128)[0] == _lib.RET_PATH_SIMT      # d_k 64
+    g = np.array([0.74] + [0.99] * 15, np.float32)   # the reverse evaluations' γ^-255 > 2^100
+    assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128, gamma=g)[0] == _lib.RET_PATH_SIMT
     g = np.array([0.5] + [0.99] * 15, np.float32)                                         # γ^127 underflows
     assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128, gamma=g) == (_lib.RET_PATH_SIMT, simt)
     assert lib.ret_force_path(_lib.RET_PATH_SIMT) == _lib.RET_OK

@@ -32,14 +32,14 @@ def test_gradient_pass_work():
     assert f_out + f_ds == 3 * bench.chunk_flops(w)      # three evaluations of the form
     b = bench.backward_tc_bytes(w)
     n, L = 32, 8192
-    # operand pass: q, k, v, dO read once; ω/ζ-folded d_v-wide operands (4),
-    # K′ and Q′↓ once per 256-column piece (2 pieces each), d_k-wide folded
-    # operands (2), dO↓ — all bf16
+    # operand pass: q, k, v, dO read once; ω·dO and ζ·V (d_v wide), K̂′ and Q″
+    # (d_k wide, folded), K′ and Q′ (d_k wide) written once each, all bf16
     reads = n * L * 2 * (2 * 256 + 2 * 512)
-    writes = n * 2 * (4 * L * 512 + 2 * 2 * L * 256 + 2 * L * 256 + L * 512)
+    writes = n * 2 * (2 * L * 512 + 2 * L * 256 + 2 * L * 256)
     assert b["bwd_prep"] == reads + writes
-    # gradient outputs: two fp32 pieces of d_k in, bf16 dq and dk out; fp32 dV↓ in, bf16 dv out
-    assert b["bwd_grad_out"] == n * L * (2 * (2 * 256 * 4 + 256 * 2) + 512 * 4 + 512 * 2)
+    # gradient outputs: two fp32 pieces of d_k in, bf16 dq and dk out (dv is
+    # written by the chunk kernel)
+    assert b["bwd_grad_out"] == n * L * 2 * (2 * 256 * 4 + 256 * 2)
 
 
 def test_ffma_peak_from_unit_counts():
