@@ -143,14 +143,14 @@ def backward_tc_bytes(w, grad_bytes=2):
     """Bytes the HBM-bound kernels of the tensor-core gradient pass move per
     step: the operand layouts (bwd_prep: q, k, v, dO read once; ω·dO, ζ·V,
     K̂′ and Q″ padded to whole chunks, K′ and Q′ unpadded) and the gradients
-    dq, dk (bwd_grad_out: fp32 piece outputs in, gradients out; dv is written
-    by the chunk kernel itself)."""
+    dq, dk (bwd_grad_out: the piece outputs, in the gradients' type, in;
+    gradients out; dv is written by the chunk kernel itself)."""
     n = w.B * w.H
     Lp = -(-w.L // 128) * 128
     P = -(-w.d_v // 256)
     rd = n * w.L * 2 * (2 * w.d_v + 2 * w.d_k)
     wr = n * 2 * (2 * Lp * w.d_v + 2 * w.L * w.d_k + 2 * Lp * w.d_k)
-    go = n * w.L * 2 * (P * w.d_k * 4 + w.d_k * grad_bytes)
+    go = n * w.L * 2 * (P * w.d_k * grad_bytes + w.d_k * grad_bytes)
     return {"bwd_prep": rd + wr, "bwd_grad_out": go}
 
 

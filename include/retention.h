@@ -228,7 +228,8 @@ ret_status ret_chunkwise_scan_plan(ret_dtype in_dt, const float* gamma, int B, i
  * the evaluations on the tensor-core chunk kernels (bf16 operands, fp32
  * accumulation; the anti-causal ones walk the chunks from the last; the two
  * evaluations that contract over d_v run as sums of pieces of at most 256
- * columns); everything else runs on the fp32 kernels over the reversed
+ * columns, the pieces held in grad_dt and summed in fp32); everything else
+ * runs on the fp32 kernels over the reversed
  * sequence, with `chunk` as the chunk length (any ≥ 1).
  * q, k, v, d_out: DEVICE, in_dt, layouts as above.  dq, dk [B, H, L, d_k]
  * and dv [B, H, L, d_v]: DEVICE, grad_dt; they must not alias any input.

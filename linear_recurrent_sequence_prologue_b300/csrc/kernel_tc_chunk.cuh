@@ -110,6 +110,9 @@ struct ChunkArgs {
   // itself), so that grid rows that differ only in a piece of the
   // contracted columns read one copy of V.
   int v_seqs = 0;
+  // Gradient-pass instantiations only: the state is read as γ^s_in_exp ·
+  // state_in and written as γ^s_out_exp · S (0: unscaled).
+  int s_in_exp = 0, s_out_exp = 0;
   // Ring mode of the pair kernel (ring > 0, carried layout only): grid rows
   // [0, ring_prod_rows) are producer CTAs that rotate raw q, k (read through
   // their own tensor maps) into `ring` chunk slots per head — ring_q / ring_k
@@ -433,6 +436,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int u = 0; u < C::SPT; ++u)
       S[u] = (args.state_in && vlive) ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
+    if constexpr (BWD != 0) {
+      if (args.s_in_exp) {
+        const float f = gpow(cc.lg2g[h], static_cast<float>(args.s_in_exp));
+#pragma unroll
+        for (int u = 0; u < C::SPT; ++u) S[u] *= f;
+      }
+    }
 
     // Ŝᵀ = bf16(γ^b S) for this thread's v lane and k range.
     auto write_shat = [&](float g) {
@@ -554,7 +564,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && args.state_out && vlive) {
 #pragma unroll
       for (int u = 0; u < C::SPT; ++u)
-        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] = S[u];
+        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] =
+            BWD != 0 && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
     }
   }
 

@@ -464,6 +464,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int u = 0; u < C::SPT; ++u)
       S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
+    if constexpr (BWD != 0) {
+      if (args.s_in_exp) {
+        const float f = gpow(cc.lg2g[h], static_cast<float>(args.s_in_exp));
+#pragma unroll
+        for (int u = 0; u < C::SPT; ++u) S[u] *= f;
+      }
+    }
 
     auto arrive_lead = [&](int b) {
       __syncwarp();
@@ -607,7 +614,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && args.state_out) {
 #pragma unroll
       for (int u = 0; u < C::SPT; ++u)
-        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] = S[u];
+        args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] =
+            BWD != 0 && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
     }
   }
 

@@ -675,13 +675,33 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
   }
 }
 
-// Gradients from the fp32 outputs of the evaluations:
+// Gradients from the piece outputs of the evaluations (Tx: fp32, or bf16
+// when the gradients are bf16):
 //   y[bh][t][:] = scale · R(−(pos0 + t)θ) Σ_{p<np} x[p][bh][t][:]
-// with x pieces `pstride` elements apart and R(−φ) the adjoint (inverse) of
-// the prologue's rotation.  Thread ↔ (row t, 8 columns), looping over the
-// B·H heads.  d a multiple of 8.
-template <typename Tg>
-__global__ void __launch_bounds__(256) grad_out_kernel(const float* __restrict__ x,
+// with x pieces `pstride` elements apart (summed in fp32) and R(−φ) the
+// adjoint (inverse) of the prologue's rotation.  Thread ↔ (row t, 8
+// columns), looping over the heads of its group (blockIdx.y).  d a multiple
+// of 8.
+template <typename Tx>
+__device__ __forceinline__ void load8f(const Tx* p, float (&e)[8]) {
+  if constexpr (sizeof(Tx) == 2) {
+    const uint4 u = __ldcs(reinterpret_cast<const uint4*>(p));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e[2 * i] = bf16lo_to_f32(w[i]);
+      e[2 * i + 1] = bf16hi_to_f32(w[i]);
+    }
+  } else {
+    const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+    const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+    e[0] = a.x; e[1] = a.y; e[2] = a.z; e[3] = a.w;
+    e[4] = b.x; e[5] = b.y; e[6] = b.z; e[7] = b.w;
+  }
+}
+
+template <typename Tx, typename Tg>
+__global__ void __launch_bounds__(256) grad_out_kernel(const Tx* __restrict__ x,
                                                        size_t pstride, int np,
                                                        Tg* __restrict__ y, CallConsts cc,
                                                        int BH, int L, int d, float pos0,
@@ -693,17 +713,19 @@ __global__ void __launch_bounds__(256) grad_out_kernel(const float* __restrict__
   float c[4], sn[4];
 #pragma unroll
   for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
-  for (int bh = 0; bh < BH; ++bh) {
-    const float* xr = x + (static_cast<size_t>(bh) * L + t) * d + 8 * cv;
-    float4 a0 = __ldcs(reinterpret_cast<const float4*>(xr));
-    float4 a1 = __ldcs(reinterpret_cast<const float4*>(xr) + 1);
+  // blockIdx.y: a group of heads (more threads in flight than one loop over all)
+  const int hpg = (BH + gridDim.y - 1) / gridDim.y;
+  const int bh_end = min(BH, (static_cast<int>(blockIdx.y) + 1) * hpg);
+  for (int bh = blockIdx.y * hpg; bh < bh_end; ++bh) {
+    const Tx* xr = x + (static_cast<size_t>(bh) * L + t) * d + 8 * cv;
+    float e[8];
+    load8f(xr, e);
     for (int p = 1; p < np; ++p) {
-      const float4 b0 = __ldcs(reinterpret_cast<const float4*>(xr + p * pstride));
-      const float4 b1 = __ldcs(reinterpret_cast<const float4*>(xr + p * pstride) + 1);
-      a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
-      a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+      float f[8];
+      load8f(xr + p * pstride, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) e[i] += f[i];
     }
-    const float e[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
     float r[8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {

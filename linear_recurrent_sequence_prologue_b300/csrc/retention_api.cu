@@ -1097,11 +1097,14 @@ TcBwdPlan plan_tc_backward(int B, int H, int L, int d_k, int d_v) {
 // out ([rows][L][dvF], fp32 or bf16) = the chunkwise form over `rows`
 // sequences with Q″ = a and K̂′ = b (bf16 [rows][Lp][dkF]), V = c (bf16
 // [rows mod v_seqs][L][dvF], v_seqs 0: [rows]); s_in / s_out per row
-// [dkF][dvF].  Head of row r: r mod H.  rev: the reverse mode (anti-causal).
+// [dkF][dvF], the starting state read as γ^s_in_exp · s_in and the final
+// one written as γ^s_out_exp · S.  Head of row r: r mod H.  rev: the
+// reverse mode (anti-causal).
 ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
                        const __nv_bfloat16* c, int dvF, int v_seqs, const float* s_in,
-                       float* s_out, void* out, int out_f32, void* tail, const CallConsts& cc,
-                       int rows, int H, int L, bool rev, cudaStream_t st) {
+                       int s_in_exp, float* s_out, int s_out_exp, void* out, int out_f32,
+                       void* tail, const CallConsts& cc, int rows, int H, int L, bool rev,
+                       cudaStream_t st) {
   const int nch = (L + tcc::CH - 1) / tcc::CH;
   const int Lp = nch * tcc::CH;
   const uint64_t qrows = static_cast<uint64_t>(rows) * Lp;
@@ -1128,6 +1131,8 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
   g.seq_div = 1;
   g.raw_ds = 0;
   g.v_seqs = v_seqs;
+  g.s_in_exp = s_in_exp;
+  g.s_out_exp = s_out_exp;
   auto launch_pair = [&](auto kern, uint32_t smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -1196,7 +1201,9 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   CallConsts cc = cc0;                     // every chunk carries as a whole one
   for (int h = 0; h < H; ++h) cc.gtail[h] = cc.gb[h];
   auto op = [&](size_t off) { return wsp<__nv_bfloat16>(ws, off); };
-  float* X = wsp<float>(ws, p.off_x);
+  // dQ′, dK′ pieces in the gradients' type (the workspace is sized for fp32)
+  Tg* X = wsp<Tg>(ws, p.off_x);
+  constexpr int x_f32 = sizeof(Tg) == 4;
   float* sprep = wsp<float>(ws, p.off_sprep);
   void* tail = p.off_tail ? wsp<void>(ws, p.off_tail) : nullptr;
   const float p0 = static_cast<float>(pos0);
@@ -1219,7 +1226,8 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   // gradient = scale · R(−nθ) Σ pieces of X
   auto grad_out = [&](Tg* y, float scale) {
     Mark m("bwd_grad_out", st);
-    simt::grad_out_kernel<Tg><<<(L * (d_k / 8) + 255) / 256, 256, 0, st>>>(
+    const unsigned groups = static_cast<unsigned>(std::min(BH, 4));
+    simt::grad_out_kernel<Tg, Tg><<<dim3((L * (d_k / 8) + 255) / 256, groups), 256, 0, st>>>(
         X, nk, p.pieces, y, cc, BH, L, d_k, p0, scale);
   };
   // dst = scale_h · (S or Sᵀ), cut into pieces of prows rows
@@ -1229,12 +1237,12 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
     simt::state_prep_kernel<<<dim3((d_v + 31) / 32, (d_k + 31) / 32, BH), dim3(32, 8), 0, st>>>(
         src, dst, BH, H, d_k, d_v, transpose, prows, hs);
   };
-  simt::HeadScale one, start, fin;
+  const int start_exp = r - 2 * tcc::CH;   // γ^{−127}·γ^{r−128}/γ
+  simt::HeadScale one, start;
   for (int h = 0; h < kMaxHeads; ++h) {
     const double g = h < H ? static_cast<double>(cc.gamma[h]) : 1.0;
     one.s[h] = 1.f;
-    start.s[h] = static_cast<float>(std::pow(g, r - 2 * tcc::CH));   // γ^{−127}·γ^{r−128}/γ
-    fin.s[h] = h < H ? cc.gb[h] : 1.f;                                // γ^128
+    start.s[h] = static_cast<float>(std::pow(g, start_exp));
   }
   ret_status s;
   // The evaluations that contract over d_v: a, b piece-major, c the values,
@@ -1243,15 +1251,15 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   auto pieces = [&](const __nv_bfloat16* a, const __nv_bfloat16* b, const __nv_bfloat16* c,
                     const float* s_pieces, bool rev) -> ret_status {
     if (p.as_rows)
-      return run_tc_eval(a, b, kBwdPiece, c, d_k, BH, s_pieces, nullptr, X, 1, tail, cc,
+      return run_tc_eval(a, b, kBwdPiece, c, d_k, BH, s_pieces, 0, nullptr, 0, X, x_f32, tail, cc,
                          p.pieces * BH, H, L, rev, st);
     for (int pc = 0; pc < p.pieces; ++pc) {
       const int c0 = pc * kBwdPiece;
       const int w = std::min(kBwdPiece, d_v - c0);
       const size_t ob = static_cast<size_t>(c0) * Lp * BH;   // piece base in a, b
       const float* sp = s_pieces ? s_pieces + static_cast<size_t>(c0) * d_k * BH : nullptr;
-      ret_status rs = run_tc_eval(a + ob, b + ob, w, c, d_k, 0, sp, nullptr,
-                                  X + static_cast<size_t>(pc) * nk, 1, tail, cc, BH, H, L, rev, st);
+      ret_status rs = run_tc_eval(a + ob, b + ob, w, c, d_k, 0, sp, 0, nullptr, 0,
+                                  X + static_cast<size_t>(pc) * nk, x_f32, tail, cc, BH, H, L, rev, st);
       if (rs != RET_OK) return rs;
     }
     return RET_OK;
@@ -1268,14 +1276,12 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
       RET_OK)
     return s;
   grad_out(dk, cc.kscale);
-  // dV = reverse F(K̂′, Q″, dO; start·dS_out), written in place, and dS_in =
-  // γ^128 · its final state (dS_out is read into sprep before dS_in is
-  // written, so the two may alias)
-  if (dso) state_prep(dso, sprep, 0, d_k, start);
-  if ((s = run_tc_eval(op(p.off_kf), op(p.off_qf), d_k, d_o, d_v, 0, dso ? sprep : nullptr, dsi,
-                       dv, sizeof(Tg) == 4, tail, cc, BH, H, L, true, st)) != RET_OK)
+  // dV = reverse F(K̂′, Q″, dO; γ^start_exp·dS_out), written in place, and
+  // dS_in = γ^128 · its final state (each drain thread reads its elements of
+  // dS_out before it writes the same elements of dS_in, so the two may alias)
+  if ((s = run_tc_eval(op(p.off_kf), op(p.off_qf), d_k, d_o, d_v, 0, dso, start_exp, dsi, tcc::CH,
+                       dv, x_f32, tail, cc, BH, H, L, true, st)) != RET_OK)
     return s;
-  if (dsi) state_prep(dsi, dsi, 0, d_k, fin);
   return last_launch();
 }
 

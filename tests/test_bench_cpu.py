@@ -37,9 +37,9 @@ def test_gradient_pass_work():
     reads = n * L * 2 * (2 * 256 + 2 * 512)
     writes = n * 2 * (2 * L * 512 + 2 * L * 256 + 2 * L * 256)
     assert b["bwd_prep"] == reads + writes
-    # gradient outputs: two fp32 pieces of d_k in, bf16 dq and dk out (dv is
+    # gradient outputs: two bf16 pieces of d_k in, bf16 dq and dk out (dv is
     # written by the chunk kernel)
-    assert b["bwd_grad_out"] == n * L * 2 * (2 * 256 * 4 + 256 * 2)
+    assert b["bwd_grad_out"] == n * L * 2 * (2 * 256 * 2 + 256 * 2)
 
 
 def test_ffma_peak_from_unit_counts():
