@@ -81,6 +81,9 @@ struct Cfg {
   static constexpr uint32_t T_COLS = (128 + DK + DK / 2) <= 256 ? 256 : 512;
 };
 
+// Compile-time modes of the chunk kernels (template argument MODE, bits).
+constexpr int kModeBwd = 1, kModeRev = 2, kModeFold = 4;
+
 // Every field has a default (zero / null), so a ChunkArgs built field by
 // field never carries garbage into a mode it does not set up.
 struct ChunkArgs {
@@ -104,7 +107,8 @@ struct ChunkArgs {
   int seq_div = 1, raw_ds = 0;
   // Grids with more rows than gridDim.y allows fold them over grid.z: row =
   // blockIdx.y + gridDim.y·blockIdx.z, and the CTAs past grid_rows exit at
-  // once.  0: one row per blockIdx.y (gridDim.z = 1).
+  // once.  0: one row per blockIdx.y (gridDim.z = 1).  Only the
+  // instantiations with kModeFold read it (the others take row = blockIdx.y).
   int grid_rows = 0;
   // V's sequence index is the row's sequence mod v_seqs (0: the sequence
   // itself), so that grid rows that differ only in a piece of the
@@ -278,18 +282,21 @@ __global__ void __launch_bounds__(256) tail_copy_kernel(const uint4* __restrict_
 // Warp 0: TMA producer.  Warp 1: MMA issuer.  Warps 2..17: drain warps; the
 // drain warp with hardware warp id w reads TMEM lanes 32·(w % 4) … +31
 // (v for Õᵀ/ΔSᵀ/Ŝᵀ, j for P̂) and handles column slice (w − 2) / 4.
-// BWD: the gradient pass's instantiations (carried layout), where V's
-// sequence index is taken mod args.v_seqs; BWD = 2 is the anti-causal form:
-// chunks walked from the last to the first, key m kept for query j when
-// m ≥ j.  The forward instantiation (BWD = 0) compiles none of it.
+// MODE: bits kModeBwd (the gradient pass's instantiations, carried layout:
+// V's sequence index taken mod args.v_seqs, the state scaled on entry and
+// exit), kModeRev (the anti-causal form: chunks walked from the last to the
+// first, key m kept for query j when m ≥ j) and kModeFold (grid rows folded
+// over grid.z).  The plain forward instantiation (MODE = 0) compiles none
+// of it, so its rows are blockIdx.y itself.
 // ---------------------------------------------------------------------------
-template <int DK, int BWD = 0>
+template <int DK, int MODE = 0>
 __global__ void __launch_bounds__(NTHREADS, 1)
     chunk_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, ChunkArgs args, CallConsts cc) {
   using C = Cfg<DK>;
-  constexpr bool REV = BWD == 2;
+  constexpr bool BWD = (MODE & kModeBwd) != 0, REV = (MODE & kModeRev) != 0,
+                 FOLD = (MODE & kModeFold) != 0;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -299,8 +306,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int bh = static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z);
-  if (args.grid_rows && bh >= args.grid_rows) return;   // past the rows of a folded grid
+  const int bh = FOLD ? static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z) : static_cast<int>(blockIdx.y);
+  if (FOLD && args.grid_rows && bh >= args.grid_rows) return;   // past the rows of a folded grid
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
   const int h = seq % args.H;
   const int d_v = args.d_v, nch = args.nchunks;
@@ -436,7 +443,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int u = 0; u < C::SPT; ++u)
       S[u] = (args.state_in && vlive) ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
-    if constexpr (BWD != 0) {
+    if constexpr (BWD) {
       if (args.s_in_exp) {
         const float f = gpow(cc.lg2g[h], static_cast<float>(args.s_in_exp));
 #pragma unroll
@@ -565,7 +572,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int u = 0; u < C::SPT; ++u)
         args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] =
-            BWD != 0 && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
+            BWD && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
     }
   }
 

@@ -233,11 +233,9 @@ __device__ __forceinline__ void ring_producer(const CUtensorMap* tm_rq, const CU
 // RING: the compact-workspace instantiation (producer CTAs in the first
 // grid rows, Q′ / K̂′ read from the ring); without it none of that code is
 // compiled in, so the front-pass path keeps its own register allocation.
-// BWD: the gradient pass's instantiations (carried layout, one sequence per
-// row), where V's sequence index is taken mod args.v_seqs; BWD = 2 is the
-// anti-causal form: chunks walked from the last to the first, key m kept for
-// query j when m ≥ j.  The forward instantiation (BWD = 0) compiles none of it.
-template <int DK, bool RING, int BWD = 0>
+// MODE: the one-CTA kernel's mode bits (kModeBwd, kModeRev, kModeFold); the
+// plain forward instantiation (MODE = 0) compiles none of them.
+template <int DK, bool RING, int MODE = 0>
 __global__ void __launch_bounds__(NTHREADS, 1)
     pair_tc_kernel(const __grid_constant__ CUtensorMap tm_qh,   // Q′, 64-row boxes
                    const __grid_constant__ CUtensorMap tm_kh,   // K̂′, 64-row boxes
@@ -247,8 +245,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                    const __grid_constant__ CUtensorMap tm_rk,   // ring mode: raw k
                    ChunkArgs args, CallConsts cc, RowPos rp) {
   using C = Cfg<DK>;
-  static_assert(!(RING && BWD), "the ring mode is a forward mode");
-  constexpr bool REV = BWD == 2;
+  constexpr bool BWD = (MODE & tcc::kModeBwd) != 0, REV = (MODE & tcc::kModeRev) != 0,
+                 FOLD = (MODE & tcc::kModeFold) != 0;
+  static_assert(!(RING && MODE), "the ring mode is a plain forward mode");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -269,8 +268,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t rank = cluster_ctarank();   // 0: issues the pair MMAs
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int v0 = blockIdx.x * VT;
-  const int grow = static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z);
-  if (!RING && args.grid_rows && grow >= args.grid_rows) return;   // both CTAs of the pair
+  const int grow = FOLD ? static_cast<int>(blockIdx.y + gridDim.y * blockIdx.z) : static_cast<int>(blockIdx.y);
+  if (FOLD && args.grid_rows && grow >= args.grid_rows) return;   // both CTAs of the pair
   const int bh = RING ? args.ring_bh0 + grow - args.ring_prod_rows : grow;
   const int seq = bh / args.seq_div, c0 = bh % args.seq_div;   // sequence; its first chunk here
   // Row of chunk c of this sequence in the rotated Q′ / K̂′ source: the
@@ -464,7 +463,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
     for (int u = 0; u < C::SPT; ++u)
       S[u] = args.state_in ? args.state_in[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] : 0.f;
-    if constexpr (BWD != 0) {
+    if constexpr (BWD) {
       if (args.s_in_exp) {
         const float f = gpow(cc.lg2g[h], static_cast<float>(args.s_in_exp));
 #pragma unroll
@@ -615,7 +614,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
       for (int u = 0; u < C::SPT; ++u)
         args.state_out[sbase + static_cast<size_t>(kr * C::SPT + u) * d_v] =
-            BWD != 0 && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
+            BWD && args.s_out_exp ? S[u] * gpow(cc.lg2g[h], static_cast<float>(args.s_out_exp)) : S[u];
     }
   }
 

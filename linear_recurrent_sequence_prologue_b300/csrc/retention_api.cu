@@ -698,14 +698,24 @@ ret_status run_tc_chunk(const __nv_bfloat16* q, const __nv_bfloat16* k, const __
     e = cudaLaunchKernelEx(&cfg, kern, mqh, mkh, mk, mv, mk, mk, args, cc, rp);
     return e != cudaSuccess ? e : cudaGetLastError();
   };
+  // Grids of more than 65535 rows take the instantiations that fold them.
   auto run = [&](const tcc::ChunkArgs& args, int rows, const char* name) -> cudaError_t {
+    constexpr int F = tcc::kModeFold;
+    const bool fold = static_cast<size_t>(rows) > kMaxGridRows;
     if (pair && d_k == 256)
-      return launch_pair(tcq::pair_tc_kernel<256, false>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name);
+      return fold ? launch_pair(tcq::pair_tc_kernel<256, false, F>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name)
+                  : launch_pair(tcq::pair_tc_kernel<256, false>, tcq::Cfg<256>::SMEM_BYTES, args, rows, name);
     if (pair)
-      return launch_pair(tcq::pair_tc_kernel<128, false>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name);
-    if (d_k == 256) return launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name);
-    if (d_k == 128) return launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
-    return launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
+      return fold ? launch_pair(tcq::pair_tc_kernel<128, false, F>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name)
+                  : launch_pair(tcq::pair_tc_kernel<128, false>, tcq::Cfg<128>::SMEM_BYTES, args, rows, name);
+    if (d_k == 256)
+      return fold ? launch(tcc::chunk_tc_kernel<256, F>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name)
+                  : launch(tcc::chunk_tc_kernel<256>, tcc::Cfg<256>::SMEM_BYTES, args, rows, name);
+    if (d_k == 128)
+      return fold ? launch(tcc::chunk_tc_kernel<128, F>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name)
+                  : launch(tcc::chunk_tc_kernel<128>, tcc::Cfg<128>::SMEM_BYTES, args, rows, name);
+    return fold ? launch(tcc::chunk_tc_kernel<64, F>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name)
+                : launch(tcc::chunk_tc_kernel<64>, tcc::Cfg<64>::SMEM_BYTES, args, rows, name);
   };
   cudaError_t e = cudaSuccess;
   if (parallel) {
@@ -1163,18 +1173,21 @@ ret_status run_tc_eval(const __nv_bfloat16* a, const __nv_bfloat16* b, int dkF,
     return cudaGetLastError();
   };
   cudaError_t e;
+  // the gradient pass's instantiations (they also fold grids of more than
+  // 65535 rows)
+  constexpr int FW = tcc::kModeBwd | tcc::kModeFold, RV = FW | tcc::kModeRev;
   if (pair && dkF == 256)
-    e = rev ? launch_pair(tcq::pair_tc_kernel<256, false, 2>, tcq::Cfg<256>::SMEM_BYTES)
-            : launch_pair(tcq::pair_tc_kernel<256, false, 1>, tcq::Cfg<256>::SMEM_BYTES);
+    e = rev ? launch_pair(tcq::pair_tc_kernel<256, false, RV>, tcq::Cfg<256>::SMEM_BYTES)
+            : launch_pair(tcq::pair_tc_kernel<256, false, FW>, tcq::Cfg<256>::SMEM_BYTES);
   else if (pair)
-    e = rev ? launch_pair(tcq::pair_tc_kernel<128, false, 2>, tcq::Cfg<128>::SMEM_BYTES)
-            : launch_pair(tcq::pair_tc_kernel<128, false, 1>, tcq::Cfg<128>::SMEM_BYTES);
+    e = rev ? launch_pair(tcq::pair_tc_kernel<128, false, RV>, tcq::Cfg<128>::SMEM_BYTES)
+            : launch_pair(tcq::pair_tc_kernel<128, false, FW>, tcq::Cfg<128>::SMEM_BYTES);
   else if (dkF == 256)
-    e = rev ? launch(tcc::chunk_tc_kernel<256, 2>, tcc::Cfg<256>::SMEM_BYTES)
-            : launch(tcc::chunk_tc_kernel<256, 1>, tcc::Cfg<256>::SMEM_BYTES);
+    e = rev ? launch(tcc::chunk_tc_kernel<256, RV>, tcc::Cfg<256>::SMEM_BYTES)
+            : launch(tcc::chunk_tc_kernel<256, FW>, tcc::Cfg<256>::SMEM_BYTES);
   else
-    e = rev ? launch(tcc::chunk_tc_kernel<128, 2>, tcc::Cfg<128>::SMEM_BYTES)
-            : launch(tcc::chunk_tc_kernel<128, 1>, tcc::Cfg<128>::SMEM_BYTES);
+    e = rev ? launch(tcc::chunk_tc_kernel<128, RV>, tcc::Cfg<128>::SMEM_BYTES)
+            : launch(tcc::chunk_tc_kernel<128, FW>, tcc::Cfg<128>::SMEM_BYTES);
   if (e != cudaSuccess) return RET_ECUDA;
   if (g.tail_out) {
     const int T = L - (nch - 1) * tcc::CH;

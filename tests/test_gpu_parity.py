@@ -591,6 +591,28 @@ def test_backward_zero_upstream_and_state_aliasing(dtype, d, chunk):
         assert torch.equal(x, y)
 
 
+@pytest.mark.parametrize("L", [130, 256])
+def test_backward_tc_smallest_gamma(L):
+    """The tensor-core gradient pass at the γ bound of its path (γ^255 just
+    above 2^-100): the anti-causal evaluations start from γ^{r−256}·dS_out,
+    about 2^96 · dS_out for the ragged length, and must still match the
+    oracle."""
+    w, inp = _custom(1, 2, L, 128, 128, "bf16", 128, state_std=0.1, seed=31)
+    inp["gamma"] = np.array([0.77, 0.999], np.float32)
+    gi = make_grad_inputs(w, seed=32, d_state_std=1.0)
+    path, _ = R.backward_plan(w.torch_dtype, 1, 2, L, 128, 128, 128, gamma=inp["gamma"])
+    assert path == R.RET_PATH_TC
+    ref = _oracle_bwd(inp, gi, 3)
+    d = _cuda(inp)
+    got = R.chunkwise_backward(d["q"], d["k"], d["v"], gi["d_out"].cuda(), inp["gamma"], inp["theta"],
+                               chunk=128, pos0=3, state_in=d["state_in"],
+                               d_state_out=gi["d_state_out"].cuda(), grad_dtype=torch.float32)
+    assert R.sync_status() == R.RET_OK
+    for g, r, name in zip(got, ref, ("dq", "dk", "dv", "dS_in")):
+        assert np.isfinite(gpu_np(g)).all(), name
+        assert_close(gpu_np(g), r, torch.bfloat16, name)
+
+
 def test_backward_tc_matches_fp32_kernels():
     """The tensor-core gradient pass against the fp32 kernels on the same bf16 inputs."""
     w, inp = _custom(2, 2, 384, 256, 256, "bf16", 128, state_std=0.1, seed=21)
