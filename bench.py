@@ -154,6 +154,20 @@ def backward_tc_bytes(w, grad_bytes=2):
     return {"bwd_prep": rd + wr, "bwd_grad_out": go}
 
 
+def param_walk_bytes(w):
+    """Bytes the two tensor-core state walks of ret_chunkwise_param_grads move
+    per call (bf16 inputs): forward, v and kf (bf16 hi + lo, rows padded to
+    whole chunks) in, S_in in, the per-chunk fp32 states out; backward, dO
+    and qb in, the states, S_in and dS_out in."""
+    n = w.B * w.H
+    Lp = -(-w.L // 128) * 128
+    C = Lp // 128
+    rows = n * w.L * w.d_v * 2
+    ops = n * Lp * w.d_k * 4
+    state = n * w.d_k * w.d_v * 4
+    return (rows + ops + state + C * state) + (rows + ops + C * state + 2 * state)
+
+
 # fp32 FFMA peak: 148 SMs x 128 fp32 lanes x 2 flop per FFMA at the 2032 MHz maximum SM clock.
 FFMA_TFLOPS = 148 * 128 * 2 * 2032e6 / 1e12
 
@@ -929,20 +943,21 @@ def main():
             pker[nm] = pker.get(nm, 0.0) + evs[2 * i].elapsed_time(evs[2 * i + 1])
         pms = time_launches(lambda: lib.ret_chunkwise_param_grads(*pargs), 10)
         tok = w.B * w.H * w.L
-        # the walks: two rank-128 updates of every (b, h) state per chunk (fp32 FFMA)
-        pflops = 2 * 2 * tok * w.d_k * w.d_v
         walk_ms = pker.get("param_walk_fwd", 0.0) + pker.get("param_walk_bwd", 0.0)
-        wtf = pflops / (walk_ms / 1e3) / 1e12 if walk_ms else None
+        wbytes = param_walk_bytes(w)
+        wgbs = wbytes / (walk_ms / 1e3) / 1e9 if walk_ms else None
         rbytes = tok * (4 * w.d_v + 4 * w.d_k) * 2
         rgbs = rbytes / (pker["param_rows"] / 1e3) / 1e9 if pker.get("param_rows") else None
         backward["param_grads"] = {
             "metric": "gamma/theta gradient call ms", "value": pms, "unit": "ms", "ms_per_call": pms,
             "launches_per_call": np_k, "kernels_ms": pker,
-            "roofline": {"bound": "alu", "kernel": "param_walk_fwd + param_walk_bwd",
-                         "achieved": wtf, "peak": FFMA_TFLOPS, "unit": "TFLOP/s",
-                         "frac": wtf / FFMA_TFLOPS if wtf else None, "traffic": None,
-                         "peak_kind": "derived: 148 SMs x 128 fp32 lanes x 2 flop x 2032 MHz",
-                         "algorithmic_flop_per_call": pflops},
+            # the tensor-core walks stream their operands and the per-chunk states
+            "roofline": {"bound": "hbm", "kernel": "param_walk_fwd + param_walk_bwd",
+                         "achieved": wgbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": wgbs / peaks["hbm_gbs"] if wgbs else None, "traffic": None,
+                         "peak_kind": f"hbm_gbs ({peak_kind})",
+                         "algorithmic_bytes_per_call": wbytes,
+                         "walk_flop_per_call": 2 * 2 * 2 * tok * w.d_k * w.d_v},
             "row_pass": {"algorithmic_bytes": rbytes, "achieved_gbs": rgbs,
                          "frac_of_hbm": rgbs / peaks["hbm_gbs"] if rgbs else None}}
         del pws, dgam, dthe

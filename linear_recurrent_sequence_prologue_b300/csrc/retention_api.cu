@@ -22,6 +22,7 @@
 #include "kernel_tc_pair.cuh"
 #include "kernel_tc_gemm.cuh"
 #include "kernels_grad.cuh"
+#include "kernel_tc_walk.cuh"
 
 using namespace ret;
 
@@ -1971,8 +1972,9 @@ namespace {
 // Parameter gradients and GroupNorm backward: workspace layouts and launches
 // ---------------------------------------------------------------------------
 struct ParamPlan {
-  int nseg, C, ntk, ntv;
-  bool fast;   // d_k, d_v multiples of 64: prepped fp32 operands, 64-thread walks
+  int nseg, C, ntk, ntv, Lp;
+  bool fast;     // d_k, d_v multiples of 64: prepped fp32 operands, 64-thread walks
+  bool tc_ok;    // d_k, d_v multiples of 128: the tensor-core walks (bf16 inputs)
   size_t off_g, off_t, off_cs, off_states, off_gw, off_z, off_qb, off_kf, bytes;
 };
 
@@ -1992,8 +1994,11 @@ ParamPlan plan_param_grads(int B, int H, int L, int d_k, int d_v) {
   p.off_gw = off; off += up256(nwalk * sizeof(double));
   p.off_z = off; off += up256(nwalk * 32 * sizeof(float));
   p.fast = d_k % grad::kTile == 0 && d_v % grad::kTile == 0;
+  p.tc_ok = d_k % tcw::KT == 0 && d_v % tcw::VT == 0;
+  p.Lp = p.C * tcw::CH;
   if (p.fast) {
-    const size_t nop = BH * static_cast<size_t>(L) * d_k * sizeof(float);
+    // fp32 qb / kf [BH][L][d_k], or their bf16 hi / lo parts [BH][Lp][d_k]
+    const size_t nop = BH * static_cast<size_t>(p.tc_ok ? p.Lp : L) * d_k * sizeof(float);
     p.off_qb = off; off += up256(nop);
     p.off_kf = off; off += up256(nop);
   }
@@ -2215,7 +2220,51 @@ ret_status ret_chunkwise_param_grads(const void* q, const void* k, const void* v
   grad::WalkArgs bw = w;
   bw.a = q; bw.b = d_out; bw.s0 = d_state_out; bw.s_in = state_in;
   bw.ascale = 1.f;
-  if (p.fast) {
+  const int64_t BH64 = static_cast<int64_t>(B) * H;
+  if (p.tc_ok && in_dt == RET_BF16 && g_force_path != RET_PATH_SIMT && BH64 <= 65535) {
+    // tensor-core walks on hi + lo bf16 operands
+    const size_t half = static_cast<size_t>(BH64) * p.Lp * d_k;
+    auto* qh = reinterpret_cast<__nv_bfloat16*>(ws + p.off_qb);
+    auto* kh = reinterpret_cast<__nv_bfloat16*>(ws + p.off_kf);
+    __nv_bfloat16* ql = qh + half;
+    __nv_bfloat16* kl = kh + half;
+    const size_t rows = static_cast<size_t>(BH64) * p.Lp;
+    const size_t n = rows * (d_k / 8);
+    {
+      Mark m("param_prep", stream);
+      tcw::walk_prep_tc_kernel<__nv_bfloat16><<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
+          static_cast<const __nv_bfloat16*>(q), static_cast<const __nv_bfloat16*>(k), qh, ql, kh, kl, cs, cc, H,
+          L, p.Lp, d_k, rows);
+    }
+    CUtensorMap mv, mdo, mkh, mkl, mqh, mql;
+    if (!make_map3(&mv, v, static_cast<uint64_t>(BH64), static_cast<uint64_t>(L), d_v) ||
+        !make_map3(&mdo, d_out, static_cast<uint64_t>(BH64), static_cast<uint64_t>(L), d_v) ||
+        !make_map(&mkh, kh, rows, d_k) || !make_map(&mkl, kl, rows, d_k) ||
+        !make_map(&mqh, qh, rows, d_k) || !make_map(&mql, ql, rows, d_k))
+      return RET_ECUDA;
+    tcw::WalkTcArgs t{};
+    t.states = w.states;
+    t.gpart = w.gpart;
+    t.zpart = w.zpart;
+    t.H = H; t.L = L; t.Lp = p.Lp; t.d_k = d_k; t.d_v = d_v; t.C = p.C;
+    t.pos0 = static_cast<float>(pos0);
+    tcw::WalkTcArgs tf = t, tb = t;
+    tf.s0 = state_in;
+    tb.s0 = d_state_out;
+    tb.s_in = state_in;
+    const dim3 grid(static_cast<unsigned>(d_v / tcw::VT), static_cast<unsigned>(d_k / tcw::KT),
+                    static_cast<unsigned>(BH64));
+    auto walk = [&](auto kern, const CUtensorMap& mb, const CUtensorMap& mh, const CUtensorMap& ml,
+                    const tcw::WalkTcArgs& wa, const char* name) {
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(tcw::SMEM_BYTES));
+      Mark m(name, stream);
+      kern<<<grid, tcw::NTHREADS, tcw::SMEM_BYTES, stream>>>(mb, mh, ml, wa, cc);
+    };
+    walk(tcw::walk_tc_kernel<true>, mv, mkh, mkl, tf, "param_walk_fwd");
+    walk(tcw::walk_tc_kernel<false>, mdo, mqh, mql, tb, "param_walk_bwd");
+    if ((s = last_launch()) != RET_OK) return s;
+  } else if (p.fast) {
     float* qb = reinterpret_cast<float*>(ws + p.off_qb);
     float* kf = reinterpret_cast<float*>(ws + p.off_kf);
     const size_t rows = static_cast<size_t>(B) * H * L;

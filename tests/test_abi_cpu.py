@@ -374,6 +374,10 @@ def test_param_grads_and_groupnorm_validation(lib):
     # segment, the angle table (100 × 32 float2), one chunk of 64 × 64 fp32
     # states per tile, the walk partials
     assert nb.value == 256 + 1024 + 25600 + 4 * 16384 + 256 + 512
+    # d_k = d_v = 128: the same parts for 16 walk tiles, plus the walks' operands
+    # qb and kf as fp32, or as bf16 hi + lo rows padded to whole chunks of 128
+    assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 128, 128, C.byref(nb)) == _lib.RET_OK
+    assert nb.value == 256 + 2048 + 51200 + 16 * 16384 + 256 + 2048 + 2 * (4 * 128 * 128 * 4)
     assert lib.ret_chunkwise_param_grads_plan(2, 2, 100, 63, 32, C.byref(nb)) == _lib.RET_EINVAL
     th = np.full(32, 0.1, np.float32)
 

@@ -45,3 +45,14 @@ def test_gradient_pass_work():
 def test_ffma_peak_from_unit_counts():
     # 148 SMs × 128 fp32 lanes × 2 flop per FFMA × 2.032 GHz, in TFLOP/s
     assert abs(bench.FFMA_TFLOPS - 148 * 128 * 2 * 2.032e-3) < 1e-9
+
+
+def test_param_walk_bytes():
+    # 7B shape: per walk the value rows (v or dO, bf16), the hi + lo operand
+    # rows (4 bytes per element), 64 per-chunk fp32 states of 256 × 512 per
+    # (b, h), and the state terms (S_in forward; S_in and dS_out backward)
+    w = WORKLOADS["msr7b"]
+    n, L, st = 32, 8192, 256 * 512 * 4
+    rows, ops = n * L * 512 * 2, n * L * 256 * 4
+    assert bench.param_walk_bytes(w) == (rows + ops + n * st + 64 * n * st) + (rows + ops + 64 * n * st + 2 * n * st)
+

@@ -97,6 +97,39 @@ def test_param_grads_only_one_output_and_determinism():
     assert torch.equal(g1, g3) and torch.equal(t1, t3)
 
 
+@pytest.mark.parametrize("L,states", [(300, True), (256, False), (1, True)])
+def test_param_grads_tensor_core_walks_match_fp32_walks(L, states):
+    """The tensor-core state walks (bf16 hi + lo operands, fp32 accumulation)
+    against the fp32 walks on the same forward and gradient-pass outputs:
+    ragged and whole chunks, one token, with and without state terms; two
+    calls give the same bits."""
+    w = Workload("custom", 2, 2, L, 256, 256, "bf16", 128, 1.0, state_std=0.1 if states else 0.0)
+    inp = make_inputs(w, seed=7 + L)
+    gi = make_grad_inputs(w, seed=8 + L, d_state_std=1.0 if states else 0.0)
+    q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
+    s_in = inp["state_in"].cuda() if states else None
+    d_out = gi["d_out"].cuda()
+    d_so = gi["d_state_out"].cuda() if states else None
+    out, _ = R.chunkwise(q, k, v, inp["gamma"], inp["theta"], chunk=128, pos0=11, state_in=s_in,
+                         out_dtype=torch.float32)
+    dq, dk, dv, _ = R.chunkwise_backward(q, k, v, d_out, inp["gamma"], inp["theta"], chunk=128, pos0=11,
+                                         state_in=s_in, d_state_out=d_so, grad_dtype=torch.float32)
+    args = (q, k, v, d_out, out, dq, dk, dv, inp["gamma"], inp["theta"])
+    kw = dict(pos0=11, state_in=s_in, d_state_out=d_so)
+    g1, t1 = R.param_grads(*args, **kw)
+    g2, t2 = R.param_grads(*args, **kw)
+    R.force_path(R.RET_PATH_SIMT)
+    try:
+        gf, tf = R.param_grads(*args, **kw)
+    finally:
+        R.force_path(0)
+    assert R.sync_status() == R.RET_OK
+    assert torch.equal(g1, g2) and torch.equal(t1, t2)
+    # 16 significant bits per walk operand against fp32: far inside the bf16 bound
+    assert max_rel_inf(gpu_np(g1), gpu_np(gf)) <= 1e-3, (gpu_np(g1), gpu_np(gf))
+    assert max_rel_inf(gpu_np(t1), gpu_np(tf)) <= 1e-3
+
+
 @pytest.mark.parametrize("head", [0, 15])
 def test_param_grads_7b_shape_full_length(head):
     """The 7B shape's batch (2 sequences of 8192 tokens, d_k 256, d_v 512,
