@@ -38,7 +38,7 @@ def parse():
     ap.add_argument("--workload", default="msr7b")
     ap.add_argument("--decode-steps", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=12)
-    ap.add_argument("--backward-steps", type=int, default=5)
+    ap.add_argument("--backward-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b", "gn1p3b", "gnbwd1p3b",
                              "pgrad_medium"],
