@@ -303,8 +303,8 @@ ret_status ret_chunkwise_param_grads_plan(int B, int H, int L, int d_k, int d_v,
  * ret_groupnorm — the per-head GroupNorm epilogue as a call of its own
  * («从RoPE到Retention…» §5): each (b, h, t) row of x [B, H, L, d_v] is
  * normalised over its d_v channels (biased variance, gn->eps), then scaled
- * and shifted by gn->weight / gn->bias [H, d_v] (DEVICE fp32, each may be
- * NULL).  gn->enabled is ignored.  x: DEVICE, x_dt; y: DEVICE, y_dt; both
+ * and shifted by gn->weight / gn->bias [H, d_v] (DEVICE fp32, 16-byte
+ * aligned, each may be NULL).  gn->enabled is ignored.  x: DEVICE, x_dt; y: DEVICE, y_dt; both
  * 16-byte aligned; y may be x when the types agree.  With ret_groupnorm_backward it gives the
  * training path: forward ret_chunkwise without GroupNorm, then this call.
  * ------------------------------------------------------------------------ */

@@ -1026,93 +1026,108 @@ __global__ void __launch_bounds__(128) gn_backward_async_kernel(const Tx* __rest
   }
 }
 
-// GroupNorm forward over 16-byte rows (d_v a multiple of 8), rows staged
-// through shared memory the same way: one group per (b, h, t) row over its d_v
-// channels, biased variance, optional affine («从RoPE到Retention…» §5).  y may
-// be x (same type): a lane writes only the channels it copied itself, after
-// copying them.  Block = 4 warps × R rows per stage; grid over rows.
-template <typename Tx, typename Ty, int NV>
-__global__ void __launch_bounds__(128) gn_forward_async_kernel(const Tx* x, Ty* y,
-                                                               const float* __restrict__ w,
-                                                               const float* __restrict__ b, int H,
-                                                               int L, int d_v, size_t rows,
-                                                               int rows_per_block, float eps) {
-  extern __shared__ __align__(16) unsigned char gsm[];
-  constexpr int R = 2;
-  constexpr int PER = 16 / sizeof(Tx);
-  constexpr int NP = NV / 8;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t r0 = static_cast<size_t>(blockIdx.x) * rows_per_block;
-  const size_t r1 = min(rows, r0 + rows_per_block);
-  const float inv_n = 1.f / static_cast<float>(d_v);
-  Tx* stage = reinterpret_cast<Tx*>(gsm) + static_cast<size_t>(warp) * 2 * R * d_v;
-  auto issue = [&](size_t rr, int st) {
+// GroupNorm forward over 16-byte rows (d_v a multiple of 8): one group per
+// (b, h, t) row over its d_v channels, biased variance (mean first, then the
+// centred sum of squares), optional affine («从RoPE到Retention…» §5).  The
+// rows are held in registers as raw 16-byte vectors (converted to fp32 at
+// each use, so that a warp keeps 8 KB of loads in flight in 32 registers a
+// lane): a warp takes RW rows at a time with all their loads issued before
+// any arithmetic, grid-stride over the row groups.  y may be x (same type):
+// a lane writes only the channels it read itself.  w, b 16-byte aligned
+// (checked by the callers).
+template <typename Tx>
+__device__ __forceinline__ void unpack8(const uint4* v, float (&o)[8]) {
+  if constexpr (sizeof(Tx) == 2) {
+    const uint32_t wd[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const size_t row = rr + 4 * r;
-      if (row >= r1) continue;
-#pragma unroll
-      for (int j = 0; j < NP; ++j) {
-        const int c = 8 * (lane + 32 * j);
-        if (c >= d_v) continue;
-#pragma unroll
-        for (int u = 0; u < 8; u += PER)
-          cp_async16(stage + (st * R + r) * static_cast<size_t>(d_v) + c + u, x + row * d_v + c + u);
-      }
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = bf16lo_to_f32(wd[i]);
+      o[2 * i + 1] = bf16hi_to_f32(wd[i]);
     }
-    cp_async_commit();
-  };
-  int st = 0;
-  issue(r0 + warp, 0);
-  for (size_t row0 = r0 + warp; row0 < r1; row0 += 4 * R, st ^= 1) {
-    issue(row0 + 4 * R, st ^ 1);
-    cp_async_wait1();
+  } else {
+    o[0] = __uint_as_float(v[0].x); o[1] = __uint_as_float(v[0].y);
+    o[2] = __uint_as_float(v[0].z); o[3] = __uint_as_float(v[0].w);
+    o[4] = __uint_as_float(v[1].x); o[5] = __uint_as_float(v[1].y);
+    o[6] = __uint_as_float(v[1].z); o[7] = __uint_as_float(v[1].w);
+  }
+}
+
+template <typename Tx, typename Ty, int NV>
+__global__ void __launch_bounds__(256, 3) gn_forward_reg_kernel(const Tx* x, Ty* y,
+                                                                const float* __restrict__ w,
+                                                                const float* __restrict__ b, int H,
+                                                                int L, int d_v, size_t rows, float eps) {
+  constexpr int NP = NV / 8;                          // 8-channel pieces per lane
+  constexpr int U4 = 8 * static_cast<int>(sizeof(Tx)) / 16;   // 16-byte vectors per piece
+  constexpr int RW = (8 / (NP * U4)) > 0 ? 8 / (NP * U4) : 1;
+  const int lane = threadIdx.x & 31;
+  const size_t wg = (static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const size_t nw = (static_cast<size_t>(gridDim.x) * blockDim.x) >> 5;
+  const float inv_n = 1.f / static_cast<float>(d_v);
+  for (size_t r0 = wg * RW; r0 < rows; r0 += nw * RW) {
+    uint4 raw[RW][NP][U4];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const size_t row = row0 + 4 * r;
-      if (row >= r1) break;
-      const int h = static_cast<int>((row / L) % H);
-      float xv[NV];
+    for (int r = 0; r < RW; ++r)
 #pragma unroll
       for (int j = 0; j < NP; ++j) {
         const int c = 8 * (lane + 32 * j);
-        float a8[8];
-        if (c < d_v) lds8(stage + (st * R + r) * static_cast<size_t>(d_v) + c, a8);
-        else
 #pragma unroll
-          for (int e = 0; e < 8; ++e) a8[e] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) xv[8 * j + e] = a8[e];
+        for (int u = 0; u < U4; ++u)
+          raw[r][j][u] = (r0 + r < rows && c < d_v)
+                             ? *reinterpret_cast<const uint4*>(x + (r0 + r) * d_v + c + u * (16 / sizeof(Tx)))
+                             : make_uint4(0u, 0u, 0u, 0u);
       }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const size_t row = r0 + r;
+      if (row >= rows) break;
+      const int h = static_cast<int>((row / L) % H);
       float s = 0.f;
 #pragma unroll
-      for (int e = 0; e < NV; ++e) s += xv[e];
+      for (int j = 0; j < NP; ++j) {
+        float f[8];
+        unpack8<Tx>(raw[r][j], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += f[e];
+      }
       const float mu = warp_sum(s) * inv_n;
       float q = 0.f;
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        const int c = 8 * (lane + 32 * (e >> 3)) + (e & 7);
-        const float d = c < d_v ? xv[e] - mu : 0.f;
-        q = fmaf(d, d, q);
+      for (int j = 0; j < NP; ++j) {
+        float f[8];
+        unpack8<Tx>(raw[r][j], f);
+        const bool live = 8 * (lane + 32 * j) < d_v;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = live ? f[e] - mu : 0.f;
+          q = fmaf(d, d, q);
+        }
       }
       const float rstd = rsqrtf(warp_sum(q) * inv_n + eps);
 #pragma unroll
       for (int j = 0; j < NP; ++j) {
         const int c = 8 * (lane + 32 * j);
         if (c >= d_v) continue;
-        float o8[8];
+        float f[8], o8[8];
+        unpack8<Tx>(raw[r][j], f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float val = (xv[8 * j + e] - mu) * rstd;
-          if (w) val *= __ldg(w + static_cast<size_t>(h) * d_v + c + e);
-          if (b) val += __ldg(b + static_cast<size_t>(h) * d_v + c + e);
-          o8[e] = val;
+        for (int e = 0; e < 8; ++e) o8[e] = (f[e] - mu) * rstd;
+        if (w) {
+          const float4 u0 = __ldg(reinterpret_cast<const float4*>(w + static_cast<size_t>(h) * d_v + c));
+          const float4 u1 = __ldg(reinterpret_cast<const float4*>(w + static_cast<size_t>(h) * d_v + c) + 1);
+          o8[0] *= u0.x; o8[1] *= u0.y; o8[2] *= u0.z; o8[3] *= u0.w;
+          o8[4] *= u1.x; o8[5] *= u1.y; o8[6] *= u1.z; o8[7] *= u1.w;
+        }
+        if (b) {
+          const float4 u0 = __ldg(reinterpret_cast<const float4*>(b + static_cast<size_t>(h) * d_v + c));
+          const float4 u1 = __ldg(reinterpret_cast<const float4*>(b + static_cast<size_t>(h) * d_v + c) + 1);
+          o8[0] += u0.x; o8[1] += u0.y; o8[2] += u0.z; o8[3] += u0.w;
+          o8[4] += u1.x; o8[5] += u1.y; o8[6] += u1.z; o8[7] += u1.w;
         }
         store8(y + row * d_v + c, o8);
       }
     }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // d_weight[h][c], d_bias[h][c] = Σ over b and segments of wpart, in double.

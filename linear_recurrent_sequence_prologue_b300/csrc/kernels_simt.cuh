@@ -593,7 +593,8 @@ __global__ void __launch_bounds__(256) state_prep_kernel(const float* src, float
 // derived from one source tensor src [BH][L][d] in one pass:
 //   op[bh][t][:] = f(t) · scale · R?((pos0 + t)θ) src[bh][t][:]   (t < L)
 //   op[bh][t][:] = 0                                              (L ≤ t < rows_out)
-// with the rotation (the prologue's) only when rotate.  f(t) is 1 (fold 0),
+// with the rotation (the prologue's, (cos, sin) of (pos0 + t)·θ_i read from
+// the call's table cs [L][d_k/2]) only when rotate.  f(t) is 1 (fold 0),
 // ω = γ^{j−(b−1)} (fold 1) or ζ = γ^{b−1−j} (fold 2), j = t mod b, b the
 // chunk length: every chunk, the last included, is folded as a whole one
 // (rows past L are zero).  Each operand's columns are stored in pieces of
@@ -610,12 +611,12 @@ struct OpSpecs {
 };
 
 // Thread ↔ (row t, 8 columns); threads with t ≥ L zero the padding rows.
-// The angles are computed once per thread and used for all B·H heads, whose
+// The angles are read once per thread and used for all B·H heads, whose
 // loads are issued eight at a time.  NS operands.
 template <int NS>
 __global__ void __launch_bounds__(256) prep_operand_kernel(
-    const __nv_bfloat16* __restrict__ src, OpSpecs<NS> sp, CallConsts cc, int BH, int H, int L,
-    int rows_max, int d, int rotate, float pos0, int chunk) {
+    const __nv_bfloat16* __restrict__ src, OpSpecs<NS> sp, CallConsts cc, const float2* __restrict__ cs,
+    int BH, int H, int L, int rows_max, int d, int rotate, int chunk) {
   constexpr int U = 8;
   const int vecs = d / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
@@ -640,7 +641,11 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
   float c[4] = {1.f, 1.f, 1.f, 1.f}, sn[4] = {0.f, 0.f, 0.f, 0.f};
   if (rotate) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
+    for (int u = 0; u < 4; ++u) {
+      const float2 e = cs[static_cast<size_t>(t) * (d / 2) + 4 * cv + u];
+      c[u] = e.x;
+      sn[u] = e.y;
+    }
   }
   const int j = t % chunk;
   const size_t hstride = static_cast<size_t>(L) * d;
@@ -679,7 +684,8 @@ __global__ void __launch_bounds__(256) prep_operand_kernel(
 // when the gradients are bf16):
 //   y[bh][t][:] = scale · R(−(pos0 + t)θ) Σ_{p<np} x[p][bh][t][:]
 // with x pieces `pstride` elements apart (summed in fp32) and R(−φ) the
-// adjoint (inverse) of the prologue's rotation.  Thread ↔ (row t, 8
+// adjoint (inverse) of the prologue's rotation ((cos, sin) from the call's
+// table cs [L][d/2]).  Thread ↔ (row t, 8
 // columns), looping over the heads of its group (blockIdx.y).  d a multiple
 // of 8.
 template <typename Tx>
@@ -703,16 +709,20 @@ __device__ __forceinline__ void load8f(const Tx* p, float (&e)[8]) {
 template <typename Tx, typename Tg>
 __global__ void __launch_bounds__(256) grad_out_kernel(const Tx* __restrict__ x,
                                                        size_t pstride, int np,
-                                                       Tg* __restrict__ y, CallConsts cc,
-                                                       int BH, int L, int d, float pos0,
-                                                       float scale) {
+                                                       Tg* __restrict__ y,
+                                                       const float2* __restrict__ cs,
+                                                       int BH, int L, int d, float scale) {
   const int vecs = d / 8;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= L * vecs) return;
   const int t = idx / vecs, cv = idx - t * vecs;
   float c[4], sn[4];
 #pragma unroll
-  for (int u = 0; u < 4; ++u) angle_cs(pos0 + static_cast<float>(t), cc.theta[4 * cv + u], c[u], sn[u]);
+  for (int u = 0; u < 4; ++u) {
+    const float2 e = cs[static_cast<size_t>(t) * (d / 2) + 4 * cv + u];
+    c[u] = e.x;
+    sn[u] = e.y;
+  }
   // blockIdx.y: a group of heads (more threads in flight than one loop over all)
   const int hpg = (BH + gridDim.y - 1) / gridDim.y;
   const int bh_end = min(BH, (static_cast<int>(blockIdx.y) + 1) * hpg);

@@ -358,17 +358,16 @@ Plan plan_parallel(ret_dtype in_dt, const float* gamma, int B, int H, int L, int
   return p;
 }
 
-// GroupNorm over the rows of x into y (y may be x when Tx = Ty): the staged
-// 16-byte-row kernel when d_v is a multiple of 8, else one warp per row.
+// GroupNorm over the rows of x into y (y may be x when Tx = Ty): rows in
+// registers when d_v is a multiple of 8 (eight 256-thread blocks per SM's
+// worth of warps at most, grid-stride over the row groups), else one warp
+// per row.
 template <typename Tx, typename Ty, int NV>
-void launch_gn_forward_nv(const Tx* x, Ty* y, const ret_gn* gn, int H, int L, int d_v, size_t rows,
-                          cudaStream_t st) {
-  constexpr int kRowsPerBlock = 64;
-  const size_t smem = static_cast<size_t>(4 * 2 * 2) * d_v * sizeof(Tx);
-  auto kern = grad::gn_forward_async_kernel<Tx, Ty, NV>;
-  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  kern<<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock), 128, smem, st>>>(
-      x, y, gn->weight, gn->bias, H, L, d_v, rows, kRowsPerBlock, gn->eps);
+void launch_gn_forward_reg(const Tx* x, Ty* y, const ret_gn* gn, int H, int L, int d_v, size_t rows,
+                           cudaStream_t st) {
+  const size_t blocks = std::min<size_t>((rows + 7) / 8, static_cast<size_t>(148) * 8);
+  grad::gn_forward_reg_kernel<Tx, Ty, NV><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+      x, y, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
 }
 
 template <typename Tx, typename Ty>
@@ -379,11 +378,11 @@ void launch_groupnorm(const Tx* x, Ty* y, const ret_gn* gn, int H, int L, int d_
     simt::groupnorm_kernel<Tx, Ty><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
         x, y, gn->weight, gn->bias, H, L, d_v, rows, gn->eps);
   } else if (d_v <= 256) {
-    launch_gn_forward_nv<Tx, Ty, 8>(x, y, gn, H, L, d_v, rows, st);
+    launch_gn_forward_reg<Tx, Ty, 8>(x, y, gn, H, L, d_v, rows, st);
   } else if (d_v <= 512) {
-    launch_gn_forward_nv<Tx, Ty, 16>(x, y, gn, H, L, d_v, rows, st);
+    launch_gn_forward_reg<Tx, Ty, 16>(x, y, gn, H, L, d_v, rows, st);
   } else {
-    launch_gn_forward_nv<Tx, Ty, 32>(x, y, gn, H, L, d_v, rows, st);
+    launch_gn_forward_reg<Tx, Ty, 32>(x, y, gn, H, L, d_v, rows, st);
   }
 }
 
@@ -1077,7 +1076,7 @@ struct TcBwdPlan {
   // pieces), K′ (dQ′'s values), Q′ (dK′'s values), K̂′ and Q″ (dV's queries
   // and keys)
   size_t off_dof = 0, off_vf = 0, off_kr = 0, off_qr = 0, off_kf = 0, off_qf = 0;
-  size_t off_x = 0, off_sprep = 0, off_tail = 0, bytes = 0;
+  size_t off_x = 0, off_sprep = 0, off_cs = 0, off_tail = 0, bytes = 0;
   int pieces = 0;
   bool as_rows = false;   // all pieces in one launch
 };
@@ -1100,6 +1099,7 @@ TcBwdPlan plan_tc_backward(int B, int H, int L, int d_k, int d_v) {
   p.off_qf = off; off += ak;
   p.off_x = off; off += up256(BH * L * static_cast<size_t>(p.pieces) * d_k * 4);   // fp32, per piece
   p.off_sprep = off; off += up256(BH * static_cast<size_t>(d_k) * d_v * 4);
+  p.off_cs = off; off += up256(static_cast<size_t>(L) * (d_k / 2) * sizeof(float2));   // angle table
   if (L % tcc::CH != 0) { p.off_tail = off; off += up256(BH * tcc::CH * xw * 4); }
   p.bytes = off;
   return p;
@@ -1220,15 +1220,23 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
   constexpr int x_f32 = sizeof(Tg) == 4;
   float* sprep = wsp<float>(ws, p.off_sprep);
   void* tail = p.off_tail ? wsp<void>(ws, p.off_tail) : nullptr;
-  const float p0 = static_cast<float>(pos0);
   const size_t nk = static_cast<size_t>(BH) * L * d_k;
+  // (cos, sin) of (pos0 + t)·θ_i once for the call: the operand pass and the
+  // gradient outputs read it
+  float2* cs = wsp<float2>(ws, p.off_cs);
+  {
+    Mark m("bwd_angles", st);
+    const size_t n = static_cast<size_t>(L) * (d_k / 2);
+    tcc::angle_table_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(
+        cs, cc, L, d_k / 2, static_cast<float>(pos0));
+  }
   // All operands, one pass per source tensor.
   auto prep = [&](const __nv_bfloat16* src, int d, int rotate, const auto& sp) {
     const int n = Lp * (d / 8);
     Mark m("bwd_prep", st);
     constexpr int NS = sizeof(sp.o) / sizeof(sp.o[0]);
-    simt::prep_operand_kernel<NS><<<(n + 255) / 256, 256, 0, st>>>(src, sp, cc, BH, H, L, Lp, d,
-                                                                   rotate, p0, tcc::CH);
+    simt::prep_operand_kernel<NS><<<(n + 255) / 256, 256, 0, st>>>(src, sp, cc, cs, BH, H, L, Lp, d,
+                                                                   rotate, tcc::CH);
   };
   //                                   dst            rows pw         fold scale
   prep(d_o, d_v, 0, simt::OpSpecs<1>{{{op(p.off_dof), Lp, kBwdPiece, 1, 1.f}}});
@@ -1242,7 +1250,7 @@ ret_status run_tc_backward(const __nv_bfloat16* q, const __nv_bfloat16* k,
     Mark m("bwd_grad_out", st);
     const unsigned groups = static_cast<unsigned>(std::min(BH, 4));
     simt::grad_out_kernel<Tg, Tg><<<dim3((L * (d_k / 8) + 255) / 256, groups), 256, 0, st>>>(
-        X, nk, p.pieces, y, cc, BH, L, d_k, p0, scale);
+        X, nk, p.pieces, y, cs, BH, L, d_k, scale);
   };
   // dst = scale_h · (S or Sᵀ), cut into pieces of prows rows
   auto state_prep = [&](const float* src, float* dst, int transpose, int prows,
@@ -2072,6 +2080,7 @@ ret_status ret_groupnorm(const void* x, ret_dtype x_dt, void* y, ret_dtype y_dt,
   if (rows >= (int64_t(1) << 31)) return RET_EINVAL;
   if (!(gn->eps > 0.f) || !std::isfinite(gn->eps)) return RET_EINVAL;
   if (x == y && x_dt != y_dt) return RET_EINVAL;   // in place only with one type
+  if ((gn->weight && !al16(gn->weight)) || (gn->bias && !al16(gn->bias))) return RET_EINVAL;
   const size_t r = static_cast<size_t>(rows);
   if (x_dt == RET_F32 && y_dt == RET_F32)
     launch_groupnorm(static_cast<const float*>(x), static_cast<float*>(y), gn, H, L, d_v, r, stream);

@@ -242,11 +242,12 @@ def test_backward_plan_and_validation(lib):
     # tensor cores, the operands of the three evaluations in bf16: ω·dO and ζ·V
     # (d_v wide, shared by the dQ′ and dK′ evaluations), K̂′ and Q″ (d_k wide),
     # all padded to whole chunks; K′ and Q′ (the values of dQ′ and dK′, once);
-    # then fp32 outputs (two pieces of d_k), one prepared state and, for a
-    # ragged length, a staging tile
+    # then fp32 outputs (two pieces of d_k), one prepared state, the (cos, sin)
+    # table of the rotation and, for a ragged length, a staging tile
     def tc_bytes(Lx, Lpx, tail):
+        up = lambda n: -(-n // 256) * 256
         return (2 * BH * Lpx * 512 * 2 + 2 * BH * Lpx * 256 * 2 + 2 * BH * Lx * 256 * 2
-                + BH * Lx * 512 * 4 + BH * 256 * 512 * 4
+                + BH * Lx * 512 * 4 + BH * 256 * 512 * 4 + up(Lx * 128 * 8)
                 + (BH * 128 * 512 * 4 if tail else 0))
 
     assert plan(_lib.RET_BF16, 2, 16, 8192, 256, 512, 128) == (_lib.RET_PATH_TC, tc_bytes(8192, 8192, False))
