@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--backward-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b", "gn1p3b", "gnbwd1p3b",
-                             "pgrad_medium"],
+                             "pgrad_medium", "bwd7b"],
                     help="run one case (two warm-up calls, then one call) for an ncu capture and exit")
     return ap.parse_args()
 
@@ -54,7 +54,8 @@ def run_profile_case(case):
     7B-shape bf16 output; block7b: ret_msr_block at the 7B shape; gn1p3b:
     ret_chunkwise with GroupNorm at the 1.3B shape; gnbwd1p3b:
     ret_groupnorm_backward at the 1.3B shape; pgrad_medium:
-    ret_chunkwise_param_grads on B1 H4 L4096 d_k256 d_v512."""
+    ret_chunkwise_param_grads on B1 H4 L4096 d_k256 d_v512; bwd7b:
+    ret_chunkwise_backward on the 7B-shape workload (state_in and dS_out)."""
     import torch
     import linear_recurrent_sequence_prologue_b300 as R
     from linear_recurrent_sequence_prologue_b300 import build
@@ -101,6 +102,14 @@ def run_profile_case(case):
                                      d_state_out=dso)
         fn = lambda: R.param_grads(q, k, v, d_o, out, *grads[:3], im["gamma"], im["theta"], state_in=s_in,
                                    d_state_out=dso)
+    elif case == "bwd7b":
+        from linear_recurrent_sequence_prologue_b300.inputs import make_grad_inputs
+        im = make_inputs(w, seed=0)
+        gi = make_grad_inputs(w, seed=5, d_state_std=1.0)
+        q, k, v, s_in = (im[n].to(dev) for n in ("q", "k", "v", "state_in"))
+        d_o, dso = gi["d_out"].to(dev), gi["d_state_out"].to(dev)
+        fn = lambda: R.chunkwise_backward(q, k, v, d_o, im["gamma"], im["theta"], chunk=128, state_in=s_in,
+                                          d_state_out=dso)
     else:
         D = w.H * w.d_k
         x = rn((w.B, w.L, D), 1.0)
