@@ -403,6 +403,9 @@ def test_param_grads_and_groupnorm_validation(lib):
 
     gn = _lib.RetGN(1, 1e-5, None, None)
     assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_BF16, 1, 2, 8, 0, C.byref(gn), None) == _lib.RET_EINVAL
+    gmis = _lib.RetGN(1, 1e-5, C.c_void_p(0x1004), None)       # weights read as 16-byte vectors
+    assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_BF16, 1, 2, 8, 16, C.byref(gmis), None) == \
+        _lib.RET_EINVAL
     assert lib.ret_groupnorm(P, _lib.RET_F32, P, _lib.RET_BF16, 1, 2, 8, 16, C.byref(gn), None) == \
         _lib.RET_EINVAL                                          # in place needs one type
     assert lib.ret_groupnorm(P, _lib.RET_F32, P2, _lib.RET_F32, 1, 2, 8, 16, None, None) == _lib.RET_EINVAL

@@ -173,6 +173,9 @@ def _gn_inputs(B, H, L, d_v, dtype, seed, affine):
     (2, 3, 50, 48, torch.float32, True),
     (1, 2, 300, 512, torch.bfloat16, False),
     (1, 2, 33, 20, torch.float32, True),
+    (1, 3, 47, 1024, torch.bfloat16, True),     # 32 channels a lane, one row per warp at a time
+    (3, 1, 23, 256, torch.bfloat16, True),      # rows not a multiple of the rows a warp takes
+    (1, 2, 41, 512, torch.float32, True),       # fp32 rows: two 16-byte vectors per 8 channels
 ])
 def test_groupnorm_call_vs_oracle(B, H, L, d_v, dtype, affine):
     x, _, w, b = _gn_inputs(B, H, L, d_v, dtype, 5 + d_v, affine)
