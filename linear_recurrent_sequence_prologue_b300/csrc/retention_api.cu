@@ -2038,14 +2038,11 @@ void launch_gn_backward_nv(const void* x, const void* dy, const float* w, void* 
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(ssm));
     kern<<<grid, 128, ssm, st>>>(static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w,
                                  static_cast<Tg*>(dx), wpart, H, L, d_v, nseg, eps);
-  } else if (vec)
-    grad::gn_backward_kernel<Tx, Tg, true, NV><<<grid, 128, smem, st>>>(
-        static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w, static_cast<Tg*>(dx), wpart, H,
-        L, d_v, nseg, eps);
-  else
+  } else {   // rows that are not whole 16-byte vectors
     grad::gn_backward_kernel<Tx, Tg, false, NV><<<grid, 128, smem, st>>>(
         static_cast<const Tx*>(x), static_cast<const Tx*>(dy), w, static_cast<Tg*>(dx), wpart, H,
         L, d_v, nseg, eps);
+  }
 }
 
 // NV = channels per lane: the smallest of 8, 16, 32 with d_v ≤ 32·NV.
