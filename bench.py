@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--backward-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", choices=["chunk7b", "chunk_medium", "gemm", "rownorm7b", "block7b", "gn1p3b", "gnbwd1p3b",
-                             "pgrad_medium", "bwd7b"],
+                             "pgrad_medium", "bwd7b", "decode"],
                     help="run one case (two warm-up calls, then one call) for an ncu capture and exit")
     return ap.parse_args()
 
@@ -55,7 +55,8 @@ def run_profile_case(case):
     ret_chunkwise with GroupNorm at the 1.3B shape; gnbwd1p3b:
     ret_groupnorm_backward at the 1.3B shape; pgrad_medium:
     ret_chunkwise_param_grads on B1 H4 L4096 d_k256 d_v512; bwd7b:
-    ret_chunkwise_backward on the 7B-shape workload (state_in and dS_out)."""
+    ret_chunkwise_backward on the 7B-shape workload (state_in and dS_out);
+    decode: ret_step on the decode workload (batch 128, fp32 state 1.07 GB)."""
     import torch
     import linear_recurrent_sequence_prologue_b300 as R
     from linear_recurrent_sequence_prologue_b300 import build
@@ -102,6 +103,12 @@ def run_profile_case(case):
                                      d_state_out=dso)
         fn = lambda: R.param_grads(q, k, v, d_o, out, *grads[:3], im["gamma"], im["theta"], state_in=s_in,
                                    d_state_out=dso)
+    elif case == "decode":
+        from linear_recurrent_sequence_prologue_b300.inputs import make_decode_inputs
+        dw = WORKLOADS["decode"]
+        dinp = make_decode_inputs(dw, seed=0, steps=1, device="cuda:0")
+        fn = lambda: R.step(dinp["q"][0], dinp["k"][0], dinp["v"][0], dinp["gamma"], dinp["theta"], 0,
+                            dinp["state"])
     elif case == "bwd7b":
         from linear_recurrent_sequence_prologue_b300.inputs import make_grad_inputs
         im = make_inputs(w, seed=0)
