@@ -272,8 +272,11 @@ ret_status ret_chunkwise_backward_plan(ret_dtype in_dt, const float* gamma, int 
  *          − (pos0+L−r+κ)Z_{C−1} + 128·Σ_{interior c} Z_c
  * The row sums read the forward call's out and the backward call's dq, dk,
  * dv for the same inputs, upstream gradients and pos0; the states are
- * recomputed in fp32 from q, k, v, d_out (two sequential walks over the
- * chunks, 64 × 64 state tiles per block).
+ * recomputed from q, k, v, d_out by two sequential walks over the chunks
+ * with fp32 states: on the tensor cores for bf16 inputs with d_k and d_v
+ * multiples of 128 (the rotated, decay-weighted q and k rows as bf16 hi +
+ * lo parts, 16 significant bits), else in fp32 FMA (64 × 64 state tiles).
+ * ret_force_path(RET_PATH_SIMT) selects the fp32 walks.
  * q, k, v, d_out: DEVICE, in_dt, [B, H, L, d_k|d_v].  out: DEVICE, out_dt,
  * [B, H, L, d_v] (the forward output before any GroupNorm; dγ only).  dq,
  * dk (dθ only), dv (dγ only): DEVICE, grad_dt.  state_in, d_state_out:
