@@ -546,6 +546,8 @@ def _oracle_bwd(inp, gi, pos0):
     ("bf16", torch.float32, 1, 2, 300, 256, 512, 128, 5, True, True),      # two d_v pieces, pairs, ragged
     ("bf16", torch.bfloat16, 1, 3, 200, 128, 384, 128, 0, True, True),     # pieces of 256 and 128
     ("bf16", torch.float32, 2, 2, 1, 256, 256, 128, 9, True, True),        # a single token
+    ("bf16", torch.float32, 1, 2, 260, 128, 256, 128, 2, True, True),      # dV on d_k = 128 CTA pairs
+    ("bf16", torch.bfloat16, 1, 2, 140, 256, 384, 128, 6, True, True),     # a 128-wide piece on d_k = 128 pairs
 ])
 def test_backward_vs_oracle(dtype, gdtype, B, H, L, d_k, d_v, chunk, pos0, state, dso):
     w, inp = _custom(B, H, L, d_k, d_v, dtype, chunk, state_std=0.1 if state else 0.0)
